@@ -1,0 +1,204 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) GatedDeltaNet mixer library.
+ *
+ * The mixer (haskell-infer-demo README, "Highlights": "GatedDeltaNet layers
+ * (causal conv1d, gated delta rule, gated RMSNorm)"; "Architecture":
+ * kernels/gdn_conv.cu, kernels/fla_gdn.cu, kernels/gdn_norm.cu) is, per token
+ * t of a sequence and per v-head h (q/k head kh = h / (HV/HK)):
+ *
+ *   x^_t   = SiLU( sum_{j=0..3} w[c][j] * x_{t-3+j}[c] )        width-4 causal conv
+ *   q, k   = q_scale * q / |q|, k / |k|   (|x| = sqrt(sum x^2 + l2_eps))
+ *   g_t    = -exp(A_log[h]) * softplus(u_t + dt_bias[h]),  a_t = exp(g_t)
+ *   b_t    = sigmoid(b_logit_t)
+ *   S_t    = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   o_t = S_t q_t
+ *   y_t    = o_t / sqrt(mean(o_t^2) + norm_eps) * norm_w * SiLU(z_t)
+ *
+ * The pages name these steps without printing their formulas; the forms above
+ * are the standard statements, and the readings taken where the pages are
+ * silent (L2 eps placement, q_scale = 1, norm weight used as w and not 1+w,
+ * GQA grouping by consecutive v-heads) are listed in the design notes.
+ *
+ * Interface properties (hyperflare core-design, prepared short-convolution
+ * interface list: packed prefill and single-token decode, caller-owned state,
+ * explicit request-to-slot mapping, fixed capacities, inactive lanes write no
+ * state, capture-safe with no host read of sequence lengths; negative slot
+ * mappings suppress writes; "Main KV / GDN recurrence: BF16 / FP32";
+ * steady-state serving performs no CUDA allocations):
+ *
+ *  - Every pointer argument is a DEVICE pointer unless its comment says HOST.
+ *    The caller owns all buffers, the workspace and the stream.  The library
+ *    allocates no device memory in any call, never synchronises the stream
+ *    (except gdn_device_error) and never reads device data on the host, so
+ *    every call may be captured into a CUDA graph.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - Packed tokens: cu_seqlens is int32 [n_seqs + 1], cu_seqlens[0] = 0,
+ *    non-decreasing, cu_seqlens[n_seqs] = T.  Sequences may be empty.
+ *  - state_idx (nullable, int32 [n_seqs]) maps sequence n to a state slot;
+ *    NULL means slot n.  A negative entry marks a padding lane: no state or
+ *    conv history of it is read or written, and its outputs are zero.
+ *  - Recurrent state: fp32 [slots][HV][dk][dv]; element (i, j) of head h holds
+ *    S[j][i] (S is dv x dk; the buffer stores S transposed, so the dk index is
+ *    the slow one).  Conv history: act dtype [slots][CH][3], oldest tap first.
+ *  - Channels of the raw projection x: [q (HK*dk) | k (HK*dk) | v (HV*dv)],
+ *    head-major, CH = 2*HK*dk + HV*dv.  Row strides (ld_*) are in ELEMENTS and
+ *    must be multiples of 8 elements (16 bytes for bf16); base pointers must
+ *    be 16-byte aligned.
+ *  - Outputs never alias inputs, except state_out == state_in (in place).
+ *
+ * Errors: every entry point validates its arguments on the host BEFORE any
+ * launch and returns GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED /
+ * GDN_ERR_WORKSPACE without touching the GPU.  A failed launch returns
+ * GDN_ERR_CUDA.  Faults the kernels detect on the device (cu_seqlens that are
+ * not monotone or exceed T, a state slot index >= n_slots, a bounded wait that
+ * ran out) never trap: the kernel records a code in a device error word, skips
+ * the affected work and returns; gdn_device_error() reads and clears it.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null required pointer, bad size, bad stride or alignment */
+    GDN_ERR_UNSUPPORTED = 2, /* valid but not built: head dims, chunk, GQA ratio */
+    GDN_ERR_WORKSPACE = 3,   /* workspace missing or smaller than gdn_workspace_size() */
+    GDN_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    GDN_ERR_DEVICE = 5       /* a kernel reported a device-side fault (gdn_device_error) */
+} gdn_status;
+
+typedef enum gdn_dtype { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
+
+/* Device error codes reported through gdn_device_error(). */
+#define GDN_DEVERR_NONE 0u
+#define GDN_DEVERR_CU_SEQLENS 1u   /* cu_seqlens not monotone or beyond T */
+#define GDN_DEVERR_SLOT 2u         /* state_idx entry >= n_slots */
+#define GDN_DEVERR_TIMEOUT 4u      /* a bounded device wait gave up */
+
+/* Flags for gdn_chunk_prefill / gdn_recurrent_decode. */
+#define GDN_FLAG_L2NORM_QK 1u      /* normalise q and k in the kernel (and apply q_scale) */
+
+typedef struct gdn_config {
+    int32_t hk, hv;      /* q/k heads, v heads; hv % hk == 0, hv/hk in {1,2,4} */
+    int32_t dk, dv;      /* head dims; dk == dv in {32, 64, 128} */
+    int32_t chunk;       /* prefill chunk length: 16 or 64 */
+    gdn_dtype act;       /* dtype of x, z, u, b_logit, conv weights and conv history */
+    int32_t n_slots;     /* number of state / conv-history slots (capacity) */
+    float q_scale;       /* multiplies q after its L2 norm (1.0 = plain rule) */
+    float l2_eps;        /* 1e-6 */
+    float norm_eps;      /* 1e-6 */
+} gdn_config;
+
+/* Arguments of the fused mixer entry points (one struct so that the C ABI
+ * stays stable as layouts grow). */
+typedef struct gdn_mixer_io {
+    const void *x;            /* [T][ld_x] act: raw projected q|k|v channels */
+    int64_t ld_x;
+    const void *z;            /* [T][ld_z] act: gate input of the norm, HV*dv channels */
+    int64_t ld_z;
+    const void *u;            /* [T][ld_ub] act: decay projection, HV channels */
+    const void *b_logit;      /* [T][ld_ub] act: beta projection, HV channels */
+    int64_t ld_ub;
+    const void *conv_w;       /* [CH][4] act: conv taps, w[c][3] multiplies the current token */
+    const float *A_log;       /* [HV] */
+    const float *dt_bias;     /* [HV] */
+    const float *norm_w;      /* [dv] */
+    const int32_t *cu_seqlens;/* [n_seqs+1]; ignored (may be NULL) by gdn_mixer_decode */
+    int32_t n_seqs;
+    int64_t T;                /* packed tokens (decode: T == n_seqs) */
+    const int32_t *state_idx; /* [n_seqs] or NULL */
+    const float *state_in;    /* [n_slots][HV][dk][dv] or NULL = zero initial state */
+    float *state_out;         /* [n_slots][HV][dk][dv] or NULL = not written; may == state_in */
+    void *conv_state;         /* [n_slots][CH][3] act, in/out, or NULL = zero history, not written */
+    void *y;                  /* [T][HV*dv] y_dtype */
+    gdn_dtype y_dtype;
+} gdn_mixer_io;
+
+/* Bytes of workspace any entry point needs for up to max_tokens packed tokens
+ * and max_seqs sequences under cfg (0 when cfg is invalid).  HOST only. */
+size_t gdn_workspace_size(const gdn_config *cfg, int64_t max_tokens, int32_t max_seqs);
+
+/* a1 gate prep: g = -exp(A_log[h]) * softplus(u + dt_bias[h]), beta =
+ * sigmoid(b_logit), per token and v-head.  u, b_logit: [T][ld_ub] act;
+ * g, beta: [T][HV] fp32. */
+gdn_status gdn_gate_prep(const gdn_config *cfg, const void *u, const void *b_logit, int64_t ld_ub,
+                         int64_t T, const float *A_log, const float *dt_bias, float *g,
+                         float *beta, void *stream);
+
+/* a2/a3 causal conv1d prefill + SiLU over a packed batch (haskell-infer-demo
+ * README, "Architecture", kernels/gdn_conv.cu; hyperflare core-design, the
+ * short-convolution paragraph).  x: [T][ld_x] act; w: [CH][4] act;
+ * conv_state: [n_slots][CH][3] act in/out (NULL = zero history, not
+ * written): the history of sequence n is read at its first token and replaced
+ * by its last three raw inputs.  out: [T][CH] out_dtype, SiLU applied, no L2. */
+gdn_status gdn_conv1d_prefill(const gdn_config *cfg, const void *x, int64_t ld_x,
+                              const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
+                              const void *w, void *conv_state, const int32_t *state_idx,
+                              void *out, gdn_dtype out_dtype, void *stream);
+
+/* a8 conv part: one token for each of n sequences; x: [n][ld_x] act.  Shifts
+ * each history in place (requires conv_state).  out: [n][CH] out_dtype. */
+gdn_status gdn_conv1d_step(const gdn_config *cfg, const void *x, int64_t ld_x, int32_t n,
+                           const void *w, void *conv_state, const int32_t *state_idx, void *out,
+                           gdn_dtype out_dtype, void *stream);
+
+/* a4/a5/a7 chunked gated delta rule over a packed batch (haskell-infer-demo
+ * README, kernels/fla_gdn.cu "chunked prefill"; hyperflare core-design, GDN
+ * numerics paragraph: chunks restart at each sequence's first token in the
+ * call, FP32 state).  q, k: [T][ld_qk] in_dtype, head kh at column kh*dk;
+ * v: [T][ld_v] in_dtype, head h at column h*dv; g, beta: [T][HV] fp32.
+ * state_in may be NULL (zero state); state_out may be NULL or == state_in.
+ * o: [T][HV*dv] o_dtype.  flags: GDN_FLAG_L2NORM_QK. */
+gdn_status gdn_chunk_prefill(const gdn_config *cfg, const void *q, const void *k, int64_t ld_qk,
+                             const void *v, int64_t ld_v, gdn_dtype in_dtype, const float *g,
+                             const float *beta, const int32_t *cu_seqlens, int32_t n_seqs,
+                             int64_t T, const float *state_in, float *state_out,
+                             const int32_t *state_idx, void *o, gdn_dtype o_dtype, uint32_t flags,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* a8 one-token recurrent update for n sequences, state in place (haskell-
+ * infer-demo README, kernels/fla_gdn.cu "recurrent decode").  q, k: [n][ld_qk];
+ * v: [n][ld_v] in_dtype; g, beta: [n][HV] fp32; state: [n_slots][HV][dk][dv]
+ * read once and written once; o: [n][HV*dv] o_dtype. */
+gdn_status gdn_recurrent_decode(const gdn_config *cfg, const void *q, const void *k, int64_t ld_qk,
+                                const void *v, int64_t ld_v, gdn_dtype in_dtype, const float *g,
+                                const float *beta, int32_t n, float *state,
+                                const int32_t *state_idx, void *o, gdn_dtype o_dtype,
+                                uint32_t flags, void *stream);
+
+/* a6 gated RMSNorm per token and v-head (haskell-infer-demo README,
+ * kernels/gdn_norm.cu "model-specific gated norm"): y = o * rsqrt(mean(o^2) +
+ * norm_eps) * w * SiLU(z).  o: [T][HV*dv] o_dtype; z: [T][ld_z] act;
+ * w: [dv] fp32; y: [T][HV*dv] y_dtype. */
+gdn_status gdn_gated_rmsnorm(const gdn_config *cfg, const void *o, gdn_dtype o_dtype,
+                             const void *z, int64_t ld_z, const float *w, int64_t T, void *y,
+                             gdn_dtype y_dtype, void *stream);
+
+/* Fused prefill, a1..a7: raw projections in, y, final state and new conv
+ * history out.  Needs gdn_workspace_size(cfg, T, n_seqs) bytes of workspace. */
+gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/* Fused decode, a8: one token per sequence (io->T == io->n_seqs), conv history
+ * and state updated in place (io->state_out must equal io->state_in and be
+ * non-NULL; io->conv_state must be non-NULL).  Needs no workspace. */
+gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device into *code (HOST pointer; GDN_DEVERR_* bits).  Returns
+ * GDN_ERR_DEVICE when a code was set, GDN_OK otherwise. */
+gdn_status gdn_device_error(void *stream, uint32_t *code);
+
+/* Static description of a status code (HOST). */
+const char *gdn_status_string(gdn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

@@ -1,0 +1,172 @@
+"""fp64 CPU oracle for the GatedDeltaNet mixer (ctypes binding of gdn_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  It shares
+no code with the CUDA library; the only thing both sides share is the seeded
+input generator, which holds none of the method's arithmetic.
+
+The C file computes, in double precision and in the order the definition
+states: the width-4 causal conv1d with history and SiLU, the per-head L2 norm
+of q and k, the gates, the gated delta rule token by token (plus a separate
+chunked restatement used only to check chunk algebra), and the gated RMSNorm.
+Citations to the pages are in the C file's header.
+
+Arrays are numpy float64 (bf16 or fp32 inputs are widened exactly).  Layouts
+are the library's: state ``[slots, HV, dk, dv]`` holding S transposed, conv
+history ``[slots, CH, 3]`` oldest first, activations ``[T, ...]`` packed.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libgdn_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile gdn_oracle.c with gcc into oracle/_build/libgdn_oracle.so."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        os.makedirs(_BUILD, exist_ok=True)
+        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC,
+                               "-lm", "-lpthread"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            D = ctypes.c_double
+            lib.oracle_conv1d_silu.argtypes = [I, P, P, I, P, P, P, P]
+            lib.oracle_gates.argtypes = [I, I, P, P, P, P, P, P]
+            lib.oracle_l2norm_qk.argtypes = [I, I, I, I, D, D, P]
+            lib.oracle_delta_rule.argtypes = [I, P, P, I, I, I, I, P, P, P, P, P, I, I]
+            lib.oracle_gated_rmsnorm.argtypes = [I, I, I, P, P, P, D, P]
+            lib.oracle_mixer.argtypes = [I, P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, D, D, D,
+                                         P, P, P, P, I, I]
+            lib.oracle_mixer.restype = I
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor (CPU): widen exactly
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _i32(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def conv1d_silu(x, cu_seqlens, w, conv_state=None, slot_idx=None):
+    """Causal conv1d (width 4) + SiLU.  Returns (out [T, CH], new conv_state or None)."""
+    lib = _load()
+    x = _f64(x); w = _f64(w); cu = _i32(cu_seqlens); si = _i32(slot_idx)
+    cs = None if conv_state is None else _f64(conv_state).copy()
+    T, CH = x.shape
+    out = np.zeros((T, CH))
+    lib.oracle_conv1d_silu(CH, _p(x), _p(cu), len(cu) - 1, _p(w), _p(cs), _p(si), _p(out))
+    return out, cs
+
+
+def gates(u, b_logit, A_log, dt_bias):
+    """Returns (g, beta), both [T, HV]."""
+    lib = _load()
+    u = _f64(u); b = _f64(b_logit); A = _f64(A_log); dt = _f64(dt_bias)
+    T, HV = u.shape
+    g = np.zeros((T, HV)); beta = np.zeros((T, HV))
+    lib.oracle_gates(T, HV, _p(u), _p(b), _p(A), _p(dt), _p(g), _p(beta))
+    return g, beta
+
+
+def l2norm_qk(xa, HK, dk, eps=1e-6, q_scale=1.0):
+    """L2-normalise the q and k heads of [T, CH] activations (returns a copy)."""
+    lib = _load()
+    xa = _f64(xa).copy()
+    T, CH = xa.shape
+    lib.oracle_l2norm_qk(T, CH, HK, dk, eps, q_scale, _p(xa))
+    return xa
+
+
+def delta_rule(xa, g, beta, cu_seqlens, HK, HV, dk, dv, state=None, slot_idx=None, chunk=0,
+               n_threads=None):
+    """Gated delta rule over packed, already normalised activations.
+
+    Returns (o [T, HV*dv], final state or None).  chunk=0 is the token-by-token
+    definition; chunk>0 the chunked restatement (for checking chunk algebra)."""
+    lib = _load()
+    xa = _f64(xa); g = _f64(g); beta = _f64(beta); cu = _i32(cu_seqlens); si = _i32(slot_idx)
+    st = None if state is None else _f64(state).copy()
+    T = xa.shape[0]
+    o = np.zeros((T, HV * dv))
+    lib.oracle_delta_rule(len(cu) - 1, _p(cu), _p(si), HK, HV, dk, dv, _p(xa), _p(g), _p(beta),
+                          _p(st), _p(o), int(chunk), int(n_threads or default_threads()))
+    return o, st
+
+
+def gated_rmsnorm(o, z, w, HV, dv, eps=1e-6):
+    lib = _load()
+    o = _f64(o); z = _f64(z); w = _f64(w)
+    T = o.shape[0]
+    y = np.zeros((T, HV * dv))
+    lib.oracle_gated_rmsnorm(T, HV, dv, _p(o), _p(z), _p(w), eps, _p(y))
+    return y
+
+
+def mixer(x, conv_w, u, b_logit, A_log, dt_bias, z, norm_w, cu_seqlens, HK, HV, dk, dv,
+          state=None, conv_state=None, slot_idx=None, q_scale=1.0, l2_eps=1e-6, norm_eps=1e-6,
+          dumps=False, chunk=0, n_threads=None):
+    """The whole mixer over a packed batch.
+
+    Returns a dict with y [T, HV*dv], state (final, or None), conv_state (new,
+    or None) and, with dumps=True, xa (post-SiLU, q/k normalised) and o."""
+    lib = _load()
+    x = _f64(x); T, CH = x.shape
+    assert CH == 2 * HK * dk + HV * dv
+    cw = _f64(conv_w); u = _f64(u); b = _f64(b_logit); A = _f64(A_log); dt = _f64(dt_bias)
+    z = _f64(z); nw = _f64(norm_w); cu = _i32(cu_seqlens); si = _i32(slot_idx)
+    st = None if state is None else _f64(state).copy()
+    cs = None if conv_state is None else _f64(conv_state).copy()
+    y = np.zeros((T, HV * dv))
+    xa = np.zeros((T, CH)) if dumps else None
+    o = np.zeros((T, HV * dv)) if dumps else None
+    rc = lib.oracle_mixer(len(cu) - 1, _p(cu), _p(si), HK, HV, dk, dv, _p(x), _p(cw), _p(cs),
+                          _p(u), _p(b), _p(A), _p(dt), _p(z), _p(nw), q_scale, l2_eps, norm_eps,
+                          _p(st), _p(y), _p(xa), _p(o), int(chunk),
+                          int(n_threads or default_threads()))
+    if rc != 0:
+        raise MemoryError("oracle_mixer: allocation failed")
+    out = {"y": y, "state": st, "conv_state": cs}
+    if dumps:
+        out["xa"] = xa
+        out["o"] = o
+    return out

@@ -1,0 +1,354 @@
+"""Pins of the fp64 oracle to facts the mathematics fixes (CPU only).
+
+Each test checks the oracle against something other than itself: a closed
+form, a hand-worked example, brute force with dense matrices, a library
+routine that computes a special case, or an invariant (linearity, chunked ==
+sequential, split invariance).  Together they are chosen so that a dropped
+term, a wrong sign, a wrong index or a transposed operand in the oracle fails
+at least one of them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _pack(q, k, v):
+    """[T, HK*dk], [T, HK*dk], [T, HV*dv] -> xa [T, CH]."""
+    return np.concatenate([q, k, v], axis=1)
+
+
+def _run(q, k, v, g, beta, S0T=None, HK=1, HV=1, cu=None, chunk=0, slot_idx=None):
+    T = q.shape[0]
+    dk = q.shape[1] // HK
+    dv = v.shape[1] // HV
+    cu = np.array([0, T] if cu is None else cu, np.int32)
+    return oracle.delta_rule(_pack(q, k, v), g, beta, cu, HK, HV, dk, dv, state=S0T,
+                             slot_idx=slot_idx, chunk=chunk, n_threads=2)
+
+
+def _rand_unit(rng, T, d):
+    x = rng.standard_normal((T, d))
+    return x / np.linalg.norm(x, axis=1, keepdims=True)
+
+
+# ----------------------------------------------------------- hand example
+
+def test_hand_worked_example_d2():
+    G = json.load(open(os.path.join(GOLDEN, "hand_rule_d2.json")))
+    q = np.array(G["q"]); k = np.array(G["k"]); v = np.array(G["v"])
+    g = np.log(np.array(G["a"]))[:, None]
+    b = np.array(G["b"])[:, None]
+    S0 = np.array(G["S0"])
+    o, st = _run(q, k, v, g, b, S0T=S0.T[None, None].copy())
+    np.testing.assert_allclose(o, np.array(G["o"]), atol=1e-14)
+    np.testing.assert_allclose(st[0, 0].T, np.array(G["S_final"]), atol=1e-14)
+
+
+# ------------------------------------------------------------ special cases
+
+def test_beta0_a1_leaves_state_unchanged():
+    rng = np.random.default_rng(1)
+    T, d = 7, 8
+    q, k, v = rng.standard_normal((T, d)), _rand_unit(rng, T, d), rng.standard_normal((T, d))
+    S0T = rng.standard_normal((1, 1, d, d))
+    o, st = _run(q, k, v, np.zeros((T, 1)), np.zeros((T, 1)), S0T=S0T)
+    np.testing.assert_array_equal(st, S0T)
+    np.testing.assert_allclose(o, q @ S0T[0, 0], rtol=1e-13, atol=1e-13)  # o = S0 q
+
+
+def test_a0_resets_state():
+    rng = np.random.default_rng(2)
+    T, d = 5, 6
+    q, k, v = rng.standard_normal((T, d)), _rand_unit(rng, T, d), rng.standard_normal((T, d))
+    b = rng.uniform(0.1, 0.9, (T, 1))
+    S0T = rng.standard_normal((1, 1, d, d))
+    o, st = _run(q, k, v, np.full((T, 1), -np.inf), b, S0T=S0T)
+    S_last = b[-1, 0] * np.outer(v[-1], k[-1])          # S = b v k^T
+    np.testing.assert_allclose(st[0, 0].T, S_last, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(o[-1], S_last @ q[-1], rtol=1e-13, atol=1e-14)
+
+
+def test_beta1_unit_key_maps_key_to_value():
+    rng = np.random.default_rng(3)
+    T, d = 6, 16
+    q, k, v = rng.standard_normal((T, d)), _rand_unit(rng, T, d), rng.standard_normal((T, d))
+    g = -rng.uniform(0, 2, (T, 1))
+    for t in range(1, T + 1):
+        S0T = rng.standard_normal((1, 1, d, d))
+        _, st = _run(q[:t], k[:t], v[:t], g[:t], np.ones((t, 1)), S0T=S0T)
+        np.testing.assert_allclose(st[0, 0].T @ k[t - 1], v[t - 1], rtol=1e-12, atol=1e-12)
+
+
+def test_orthonormal_keys_build_associative_memory():
+    rng = np.random.default_rng(4)
+    d = 8
+    K = np.eye(d)
+    V = rng.standard_normal((d, d))
+    Q = np.eye(d)[::-1].copy()
+    _, st = _run(Q, K, V, np.zeros((d, 1)), np.ones((d, 1)), S0T=np.zeros((1, 1, d, d)))
+    S = st[0, 0].T
+    np.testing.assert_allclose(S, V.T @ K, atol=1e-14)          # S = sum_i v_i k_i^T
+    for i in range(d):
+        np.testing.assert_allclose(S @ np.eye(d)[i], V[i], atol=1e-14)
+
+
+def test_linear_in_values_and_initial_state():
+    rng = np.random.default_rng(5)
+    T, d = 9, 8
+    q, k = rng.standard_normal((T, d)), _rand_unit(rng, T, d)
+    g, b = -rng.uniform(0, 1, (T, 1)), rng.uniform(0, 1, (T, 1))
+    V1, V2 = rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    S1, S2 = rng.standard_normal((1, 1, d, d)), rng.standard_normal((1, 1, d, d))
+    o1, s1 = _run(q, k, V1, g, b, S0T=S1)
+    o2, s2 = _run(q, k, V2, g, b, S0T=S2)
+    o3, s3 = _run(q, k, 2.0 * V1 - 3.0 * V2, g, b, S0T=2.0 * S1 - 3.0 * S2)
+    np.testing.assert_allclose(o3, 2 * o1 - 3 * o2, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(s3, 2 * s1 - 3 * s2, rtol=1e-11, atol=1e-12)
+
+
+# --------------------------------------------------------------- brute force
+
+@pytest.mark.parametrize("T,d", [(1, 1), (2, 3), (3, 4), (4, 4), (4, 2)])
+def test_brute_force_product_form(T, d):
+    """S_T = S0 prod_i a_i (I - b_i k_i k_i^T) + sum_i b_i v_i k_i^T prod_{j>i} a_j (I - b_j k_j k_j^T)."""
+    rng = np.random.default_rng(10 + T * 7 + d)
+    q, k, v = rng.standard_normal((T, d)), rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    g, b = -rng.uniform(0, 2, (T, 1)), rng.uniform(0, 1, (T, 1))
+    S0 = rng.standard_normal((d, d))
+    o, st = _run(q, k, v, g, b, S0T=S0.T[None, None].copy())
+    F = [np.exp(g[i, 0]) * (np.eye(d) - b[i, 0] * np.outer(k[i], k[i])) for i in range(T)]
+    for t in range(1, T + 1):
+        S = S0.copy()
+        for i in range(t):
+            S = S @ F[i]
+        for i in range(t):
+            term = b[i, 0] * np.outer(v[i], k[i])
+            for j in range(i + 1, t):
+                term = term @ F[j]
+            S = S + term
+        np.testing.assert_allclose(o[t - 1], S @ q[t - 1], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(st[0, 0].T, S, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------ chunked == sequential
+
+@pytest.mark.parametrize("chunk", [1, 2, 16, 64])
+def test_chunked_equals_sequential(chunk):
+    rng = np.random.default_rng(20 + chunk)
+    HK, HV, d = 2, 4, 16
+    lens = [0, 1, 37, 130, 64]
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q = rng.standard_normal((T, HK * d))
+    k = np.concatenate([_rand_unit(rng, T, d) for _ in range(HK)], 1)
+    v = rng.standard_normal((T, HV * d))
+    g, b = -rng.uniform(0, 1.5, (T, HV)), rng.uniform(0, 1, (T, HV))
+    S0 = rng.standard_normal((len(lens), HV, d, d)) * 0.1
+    o_s, s_s = _run(q, k, v, g, b, S0T=S0, HK=HK, HV=HV, cu=cu, chunk=0)
+    o_c, s_c = _run(q, k, v, g, b, S0T=S0, HK=HK, HV=HV, cu=cu, chunk=chunk)
+    scale = np.abs(o_s).max()
+    assert np.abs(o_c - o_s).max() <= 1e-12 * scale
+    assert np.abs(s_c - s_s).max() <= 1e-12 * np.abs(s_s).max()
+
+
+def test_gqa_head_grouping_consecutive():
+    """v-head h reads q/k head h // (HV/HK)."""
+    rng = np.random.default_rng(30)
+    HK, HV, d, T = 2, 4, 4, 5
+    q = rng.standard_normal((T, HK * d)); k = rng.standard_normal((T, HK * d))
+    v = rng.standard_normal((T, HV * d))
+    g, b = -rng.uniform(0, 1, (T, HV)), rng.uniform(0, 1, (T, HV))
+    o, _ = _run(q, k, v, g, b, HK=HK, HV=HV)
+    for h in range(HV):
+        kh = h // (HV // HK)
+        oh, _ = _run(q[:, kh * d:(kh + 1) * d], k[:, kh * d:(kh + 1) * d], v[:, h * d:(h + 1) * d],
+                     g[:, h:h + 1], b[:, h:h + 1])
+        np.testing.assert_array_equal(o[:, h * d:(h + 1) * d], oh)
+
+
+# ------------------------------------------------------------------- conv
+
+def test_conv_impulse_response_and_library():
+    rng = np.random.default_rng(40)
+    CH, T = 5, 9
+    w = rng.standard_normal((CH, 4))
+    x = np.zeros((T, CH)); x[0] = 1.0
+    out, _ = oracle.conv1d_silu(x, [0, T], w)
+    silu = lambda t: t / (1 + np.exp(-t))
+    for t in range(4):
+        np.testing.assert_allclose(out[t], silu(w[:, 3 - t]), rtol=1e-15)
+    np.testing.assert_allclose(out[4:], silu(np.zeros((T - 4, CH))))
+    # random input, zero history == torch conv1d (cross-correlation) with left padding 3
+    x = rng.standard_normal((T, CH))
+    out, _ = oracle.conv1d_silu(x, [0, T], w)
+    ref = torch.nn.functional.conv1d(torch.tensor(x.T[None]), torch.tensor(w[:, None, :]),
+                                     padding=3, groups=CH)[0, :, :T].T
+    np.testing.assert_allclose(out, torch.nn.functional.silu(ref).numpy(), rtol=1e-13, atol=1e-15)
+
+
+def test_conv_history_and_split_invariance():
+    rng = np.random.default_rng(41)
+    CH = 6
+    w = rng.standard_normal((CH, 4))
+    hist = rng.standard_normal((1, CH, 3))
+    x = rng.standard_normal((11, CH))
+    full, h_full = oracle.conv1d_silu(x, [0, 11], w, conv_state=hist)
+    # history behaves as the three tokens before the sequence
+    ext = np.concatenate([hist[0].T, x])
+    ref, _ = oracle.conv1d_silu(ext, [0, 14], w)
+    np.testing.assert_allclose(full, ref[3:], rtol=1e-14)
+    np.testing.assert_array_equal(h_full[0], x[-3:].T)       # new history = last 3 raw inputs
+    # one call over 11 tokens == 11 one-token calls == calls of 1, 2 and 8 tokens
+    h = hist.copy(); outs = []
+    for t in range(11):
+        o1, h = oracle.conv1d_silu(x[t:t + 1], [0, 1], w, conv_state=h)
+        outs.append(o1)
+    np.testing.assert_array_equal(np.concatenate(outs), full)
+    np.testing.assert_array_equal(h, h_full)
+    h = hist.copy(); outs = []
+    for a, b in [(0, 1), (1, 3), (3, 11)]:
+        o1, h = oracle.conv1d_silu(x[a:b], [0, b - a], w, conv_state=h)
+        outs.append(o1)
+    np.testing.assert_array_equal(np.concatenate(outs), full)
+    np.testing.assert_array_equal(h, h_full)
+    # a 2-token sequence keeps the newest old-history tap
+    _, h2 = oracle.conv1d_silu(x[:2], [0, 2], w, conv_state=hist)
+    np.testing.assert_array_equal(h2[0], np.stack([hist[0, :, 2], x[0], x[1]], 1))
+    # empty sequence leaves the history unchanged
+    _, h0 = oracle.conv1d_silu(np.zeros((0, CH)), [0, 0], w, conv_state=hist)
+    np.testing.assert_array_equal(h0, hist)
+
+
+def test_conv_varlen_no_leakage_and_padding_slot():
+    rng = np.random.default_rng(42)
+    CH = 4
+    w = rng.standard_normal((CH, 4))
+    hist = rng.standard_normal((3, CH, 3))
+    x = rng.standard_normal((10, CH))
+    cu = [0, 4, 4, 10]
+    out, h = oracle.conv1d_silu(x, cu, w, conv_state=hist, slot_idx=[2, 0, -1])
+    o0, h0 = oracle.conv1d_silu(x[:4], [0, 4], w, conv_state=hist[2:3])
+    o2, _ = oracle.conv1d_silu(x[4:], [0, 6], w)                  # padding lane: zero history
+    np.testing.assert_array_equal(out[:4], o0)
+    np.testing.assert_array_equal(out[4:], o2)
+    np.testing.assert_array_equal(h[2], h0[0])
+    np.testing.assert_array_equal(h[0], hist[0])                  # empty sequence
+    np.testing.assert_array_equal(h[1], hist[1])                  # untouched slot
+
+
+# ----------------------------------------------------- gates, L2, gated norm
+
+def test_gates_match_library_routines():
+    rng = np.random.default_rng(50)
+    T, HV = 33, 3
+    u = rng.standard_normal((T, HV)) * 4; b = rng.standard_normal((T, HV)) * 4
+    A = rng.uniform(-1, 1, HV); dt = rng.standard_normal(HV)
+    g, beta = oracle.gates(u, b, A, dt)
+    sp = torch.nn.functional.softplus(torch.tensor(u + dt)).numpy()
+    np.testing.assert_allclose(g, -np.exp(A) * sp, rtol=1e-14)
+    np.testing.assert_allclose(beta, torch.sigmoid(torch.tensor(b)).numpy(), rtol=1e-14)
+    assert (g < 0).all() and (beta > 0).all() and (beta < 1).all()
+
+
+def test_l2norm_closed_form():
+    xa = np.zeros((1, 2 * 2 + 2))
+    xa[0, :2] = [3.0, 4.0]            # q head (HK=1, dk=2)
+    xa[0, 2:4] = [0.0, 2.0]           # k head
+    xa[0, 4:] = [7.0, 8.0]            # v untouched
+    eps, qs = 1e-6, 0.5
+    out = oracle.l2norm_qk(xa, 1, 2, eps=eps, q_scale=qs)
+    np.testing.assert_allclose(out[0, :2], qs * np.array([3, 4]) / np.sqrt(25 + eps), rtol=1e-15)
+    np.testing.assert_allclose(out[0, 2:4], np.array([0, 2]) / np.sqrt(4 + eps), rtol=1e-15)
+    np.testing.assert_array_equal(out[0, 4:], [7, 8])
+
+
+def test_gated_rmsnorm_cases():
+    rng = np.random.default_rng(60)
+    T, HV, dv, eps = 4, 2, 8, 1e-6
+    o = rng.standard_normal((T, HV * dv)); w = rng.standard_normal(dv)
+    y = oracle.gated_rmsnorm(o, np.zeros_like(o), w, HV, dv, eps)
+    np.testing.assert_array_equal(y, 0.0)                          # z = 0 => y = 0
+    c = 0.37
+    z = rng.standard_normal((T, HV * dv))
+    y = oracle.gated_rmsnorm(np.full_like(o, c), z, np.ones(dv), HV, dv, eps)
+    silu = z / (1 + np.exp(-z))
+    np.testing.assert_allclose(y, c / np.sqrt(c * c + eps) * silu, rtol=1e-14)
+    # library routine: torch rms_norm over each head, then the gate
+    y = oracle.gated_rmsnorm(o, z, w, HV, dv, eps)
+    ref = torch.nn.functional.rms_norm(torch.tensor(o).view(T, HV, dv), (dv,),
+                                       weight=torch.tensor(w), eps=eps).view(T, -1).numpy() * silu
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------- whole mixer
+
+def _mixer_inputs(rng, lens, HK=2, HV=4, d=8, with_state=True):
+    CH = 2 * HK * d + HV * d
+    T = sum(lens); N = len(lens)
+    return dict(
+        x=rng.standard_normal((T, CH)), conv_w=rng.standard_normal((CH, 4)) * 0.25,
+        u=rng.standard_normal((T, HV)), b_logit=rng.standard_normal((T, HV)),
+        A_log=rng.uniform(-1, 1, HV), dt_bias=np.zeros(HV), z=rng.standard_normal((T, HV * d)),
+        norm_w=np.ones(d), cu_seqlens=np.concatenate([[0], np.cumsum(lens)]).astype(np.int32),
+        HK=HK, HV=HV, dk=d, dv=d,
+        state=rng.standard_normal((N, HV, d, d)) * 0.02 if with_state else None,
+        conv_state=rng.standard_normal((N, CH, 3)) if with_state else None)
+
+
+def test_mixer_split_invariance():
+    """prefill(T) == prefill(T1) then prefill(T2) == prefill(T1) then one-token steps."""
+    rng = np.random.default_rng(70)
+    I = _mixer_inputs(rng, [23])
+    full = oracle.mixer(**I, n_threads=2)
+    T1 = 9
+
+    def sub(a, b, state, conv):
+        J = dict(I)
+        for key in ("x", "u", "b_logit", "z"):
+            J[key] = I[key][a:b]
+        J["cu_seqlens"] = np.array([0, b - a], np.int32)
+        J["state"], J["conv_state"] = state, conv
+        return oracle.mixer(**J, n_threads=2)
+
+    p1 = sub(0, T1, I["state"], I["conv_state"])
+    p2 = sub(T1, 23, p1["state"], p1["conv_state"])
+    np.testing.assert_allclose(np.concatenate([p1["y"], p2["y"]]), full["y"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(p2["state"], full["state"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(p2["conv_state"], full["conv_state"])
+    st, cs, ys = p1["state"], p1["conv_state"], [p1["y"]]
+    for t in range(T1, 23):
+        r = sub(t, t + 1, st, cs)
+        st, cs = r["state"], r["conv_state"]
+        ys.append(r["y"])
+    np.testing.assert_allclose(np.concatenate(ys), full["y"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(st, full["state"], rtol=1e-12, atol=1e-14)
+
+
+def test_mixer_varlen_equals_separate_and_padding_lane():
+    rng = np.random.default_rng(71)
+    lens = [5, 0, 12, 3]
+    I = _mixer_inputs(rng, lens)
+    packed = oracle.mixer(**I, n_threads=2)
+    cu = I["cu_seqlens"]
+    for n, L in enumerate(lens):
+        J = dict(I)
+        for key in ("x", "u", "b_logit", "z"):
+            J[key] = I[key][cu[n]:cu[n + 1]]
+        J["cu_seqlens"] = np.array([0, L], np.int32)
+        J["state"], J["conv_state"] = I["state"][n:n + 1], I["conv_state"][n:n + 1]
+        r = oracle.mixer(**J, n_threads=1)
+        np.testing.assert_array_equal(r["y"], packed["y"][cu[n]:cu[n + 1]])
+        np.testing.assert_array_equal(r["state"][0], packed["state"][n])
+        np.testing.assert_array_equal(r["conv_state"][0], packed["conv_state"][n])
+    # slot mapping with a padding lane: zero output, its slot untouched
+    pad = oracle.mixer(**I, slot_idx=np.array([3, 1, -1, 0], np.int32), n_threads=2)
+    np.testing.assert_array_equal(pad["y"][cu[2]:cu[3]], 0.0)
+    np.testing.assert_array_equal(pad["state"][2], I["state"][2])
+    np.testing.assert_array_equal(pad["conv_state"][2], I["conv_state"][2])
