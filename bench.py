@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark of the GatedDeltaNet mixer hot path on one GB300 (or N, weakly scaled).
+
+Default workload: single-sequence chunked prefill, T=8192 tokens, 16 q/k heads,
+32 v heads, dk=dv=128, chunk 64, bf16 inputs, zero initial state.  One step is
+one pass of the prefill path over that batch: gate prep, causal conv1d+SiLU
+(+history update), the chunked gated delta rule with in-kernel q/k L2 norm and
+state out, and the gated RMSNorm.  The decode path (64 sequences x 256
+one-token steps, fused conv/L2/gates/state update/norm) is measured in the same
+run and reported under "decode".
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gateddeltanet_linear_attention_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "GDN prefill tokens/s (% bf16 TC peak); decode state-update GB/s (% HBM peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def chunk_flops(lens, C, dk, dv, HV):
+    """Algorithmic contraction FLOPs of the chunked rule: per chunk of L tokens
+    and v-head, 2L^2dk (KK^T) + 2L^2dk (QK^T) + 2L^2dk (W) + 2L^2dv (U)
+    + 2L^2dv (intra O) + 3*2L*dk*dv (W M, Q M, K~^T U') + 2L^3/3 (solve)."""
+    tot = 0.0
+    for L in lens:
+        full, rem = divmod(int(L), C)
+        for Lc in [C] * full + ([rem] if rem else []):
+            tot += (6 * Lc * Lc * dk + 4 * Lc * Lc * dv + 6 * Lc * dk * dv + 2 * Lc ** 3 / 3)
+    return tot * HV
+
+
+def src_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(name):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    has not changed since the counters were taken (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p)).get(name)
+        if d and d.get("src_sha") == src_sha(d["sources"]):
+            return d["dram_bytes_per_launch"]
+    except Exception:
+        return None
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.path = "/tmp/gdn_clocks_%d.csv" % os.getpid()
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10 or (self.uuid and f[1] != self.uuid):
+                continue
+            try:
+                sm.append(float(f[2]))
+                mx = float(f[3])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[6:10]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_desc(wl, inp):
+    lens = inp["seqlens"]
+    return ("%s: N=%d, T=%d, HK=%d, HV=%d, dk=dv=%d, chunk %d, %s inputs, %s initial state"
+            % (wl.name, len(lens), sum(lens), wl.HK, wl.HV, wl.dk, wl.chunk, wl.act,
+               "nonzero" if wl.init_state else "zero"))
+
+
+# ----------------------------------------------------------- CPU oracle arm
+
+def oracle_sample(wl, inp, kheads):
+    """Run the oracle on k-heads `kheads` of the workload; returns (seconds,
+    token-heads processed, threads used)."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from gpu_util import oracle_mixer
+    oracle.build()
+    G = wl.HV // wl.HK
+    units = len(inp["seqlens"]) * len(kheads) * G
+    threads = max(1, min(os.cpu_count() or 1, units))
+    t0 = time.perf_counter()
+    oracle_mixer(wl, inp, kheads=kheads, n_threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, sum(inp["seqlens"]) * len(kheads) * G, threads
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl)
+    T = sum(inp["seqlens"])
+    kheads = list(range(min(4, wl.HK)))          # bounded sample: 4 q/k heads (8 v-heads)
+    for _ in range(args.warmup):
+        oracle_sample(wl, inp, kheads)
+    times, th = [], 1
+    for _ in range(args.steps):
+        dt, th_units, th = oracle_sample(wl, inp, kheads)
+        times.append(dt)
+    tot = sum(times)
+    frac = len(kheads) * (wl.HV // wl.HK) / wl.HV
+    value = T * frac * len(times) / tot                 # full-workload tokens/s equivalent
+    sample = ("%d of %d v-heads over all %d tokens per step; tokens/s scaled by the head fraction"
+              % (len(kheads) * (wl.HV // wl.HK), wl.HV, T))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / len(times) / frac, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(wl, inp)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": th, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, rank, ws, local):
+    from gateddeltanet_linear_attention_gb300 import gdn
+    assert torch.cuda.is_available(), "the GPU arm needs a CUDA device"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    gdn.load()
+    pk, pk_src = peaks()
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl)
+    lens = inp["seqlens"]
+    T, N = sum(lens), len(lens)
+    cfg = gdn.make_config(wl.HK, wl.HV, wl.dk, wl.dv, wl.chunk, wl.act, n_slots=N)
+    d = {k: v.to(dev) for k, v in inp.items() if hasattr(v, "to")}
+    H = wl.HK * wl.dk
+    stream = torch.cuda.current_stream()
+
+    # buffers (caller-owned; nothing is allocated inside the timed region)
+    g = torch.empty((T, wl.HV), device=dev)
+    beta = torch.empty_like(g)
+    xa = torch.empty((T, wl.CH), device=dev)
+    o = torch.empty((T, wl.HV * wl.dv), device=dev)
+    y = torch.empty((T, wl.HV * wl.dv), dtype=torch.bfloat16, device=dev)
+    state_out = torch.empty((N, wl.HV, wl.dk, wl.dv), device=dev)
+    conv = (d["conv_state"].clone() if wl.init_conv
+            else torch.zeros((N, wl.CH, 3), dtype=wl.torch_act, device=dev))
+    state_in = d["state"] if wl.init_state else None
+    ev_c0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_c1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+    def step(i=None):
+        gdn.gdn_gate_prep(cfg, d["u"], d["b_logit"], d["A_log"], d["dt_bias"], g, beta)
+        gdn.gdn_conv1d_prefill(cfg, d["x"], d["cu_seqlens"], d["conv_w"], conv, None, xa)
+        if i is not None:
+            ev_c0[i].record(stream)
+        gdn.gdn_chunk_prefill(cfg, xa[:, :H], xa[:, H:2 * H], xa[:, 2 * H:], g, beta,
+                              d["cu_seqlens"], state_in, state_out, None, o)
+        if i is not None:
+            ev_c1[i].record(stream)
+        gdn.gdn_gated_rmsnorm(cfg, o, d["z"], d["norm_w"], y)
+
+    launches_per_step = 5    # gate, conv, conv-history update, chunk, norm
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(uuid) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    assert gdn.gdn_device_error() == 0
+    elapsed = e0.elapsed_time(e1) / 1e3
+    elapsed = max_over_ranks(elapsed, ws)
+    chunk_s = sum(a.elapsed_time(b) for a, b in zip(ev_c0, ev_c1)) / 1e3 / args.steps
+    value = ws * T * args.steps / elapsed
+    flops = chunk_flops(lens, wl.chunk, wl.dk, wl.dv, wl.HV)
+    tc_peak = pk["bf16_tflops"]
+    roof = {"kernel": "chunk_simt_kernel", "bound": "tensor", "achieved": flops / chunk_s / 1e12,
+            "peak": tc_peak, "unit": "TFLOP/s", "frac": flops / chunk_s / 1e12 / tc_peak,
+            "traffic": traffic_for("chunk_prefill_8k"), "peak_source": pk_src + " bf16 burst",
+            "kernel_ms": chunk_s * 1e3, "flops_per_launch": flops}
+
+    # ---- decode: 64 sequences x S one-token steps, L2 flushed between steps
+    dec = None
+    if args.decode_steps > 0:
+        dec = bench_decode(args, dev, gdn, pk, pk_src)
+
+    # ---- end to end through the public fused call with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = bench_e2e(args, dev, gdn, cfg, wl, inp, d, N, T)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        dt, th_units, th = oracle_sample(wl, inp, list(range(wl.HK)))
+        cpu = {"value": T / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
+               "sample": "the whole workload (all %d v-heads, %d tokens), once" % (wl.HV, T)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+                "config": {"workload": workload_desc(wl, inp), "parallelism": "dp%d" % ws,
+                           "l2": "inputs larger than L2 (x %d MiB + z %d MiB per step)"
+                                 % (T * wl.CH * 2 >> 20, T * wl.HV * wl.dv * 2 >> 20),
+                           "activations": wl.act, "y_dtype": "bf16"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps,
+                "clocks": clk.summary(), "decode": dec}
+        print(json.dumps(line), flush=True)
+
+
+def bench_decode(args, dev, gdn, pk, pk_src):
+    wl = WORKLOADS["decode_64x256"]
+    S = args.decode_steps
+    from dataclasses import replace
+    wl = replace(wl, decode_steps=S)
+    inp = make_inputs(wl)
+    N = wl.n_decode
+    cfg = gdn.make_config(wl.HK, wl.HV, wl.dk, wl.dv, wl.chunk, wl.act, n_slots=N)
+    state = inp["state"].to(dev)
+    conv = inp["conv_state"].to(dev)
+    cw, A, dt, nw = (inp[k].to(dev) for k in ("conv_w", "A_log", "dt_bias", "norm_w"))
+    xs, zs, us, bs = (inp[k].to(dev) for k in ("dec_x", "dec_z", "dec_u", "dec_b_logit"))
+    y = torch.empty((N, wl.HV * wl.dv), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(S)]
+    stream = torch.cuda.current_stream()
+    for t in range(min(3, S)):   # warm-up on copies of the state (steps replayed below)
+        st2, cv2 = state.clone(), conv.clone()
+        gdn.gdn_mixer_decode(cfg, xs[t], zs[t], us[t], bs[t], cw, A, dt, nw, y, st2, cv2)
+    torch.cuda.synchronize()
+    for t in range(S):
+        flush.zero_()
+        evs[t][0].record(stream)
+        gdn.gdn_mixer_decode(cfg, xs[t], zs[t], us[t], bs[t], cw, A, dt, nw, y, state, conv)
+        evs[t][1].record(stream)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_error() == 0
+    ms = [a.elapsed_time(b) for a, b in evs]
+    per = sum(ms) / S / 1e3
+    state_bytes = 2 * N * wl.HV * wl.dk * wl.dv * 4
+    gbs = state_bytes / per / 1e9
+    return {"workload": "decode_64x256: 64 sequences x %d one-token steps, HK=16, HV=32, "
+                        "dk=dv=128, bf16 inputs, fp32 state (128 MiB), L2 flushed between steps"
+                        % S,
+            "value": gbs, "unit": "GB/s", "us_per_step": per * 1e6,
+            "state_bytes_per_step": state_bytes,
+            "roofline": {"kernel": "decode_kernel (fused)", "bound": "hbm", "achieved": gbs,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                         "traffic": traffic_for("decode_64x256"),
+                         "peak_source": pk_src + " copy"},
+            "gpu_launches": S}
+
+
+def bench_e2e(args, dev, gdn, cfg, wl, inp, d, N, T):
+    hx = inp["x"].pin_memory(); hz = inp["z"].pin_memory()
+    hu = inp["u"].pin_memory(); hb = inp["b_logit"].pin_memory()
+    hy = torch.empty((T, wl.HV * wl.dv), dtype=torch.bfloat16).pin_memory()
+    dx, dz, du, db = (torch.empty_like(t, device=dev) for t in (hx, hz, hu, hb))
+    y = torch.empty((T, wl.HV * wl.dv), dtype=torch.bfloat16, device=dev)
+    st = torch.empty((N, wl.HV, wl.dk, wl.dv), device=dev)
+    conv = torch.zeros((N, wl.CH, 3), dtype=wl.torch_act, device=dev)
+    ws = torch.empty(gdn.gdn_workspace_size(cfg, T, N), dtype=torch.uint8, device=dev)
+    sin = d["state"] if wl.init_state else None
+
+    def step():
+        for h, t in ((hx, dx), (hz, dz), (hu, du), (hb, db)):
+            t.copy_(h, non_blocking=True)
+        gdn.gdn_mixer_prefill(cfg, dx, dz, du, db, d["conv_w"], d["A_log"], d["dt_bias"],
+                              d["norm_w"], d["cu_seqlens"], y, state_in=sin, state_out=st,
+                              conv_state=conv, workspace=ws)
+        hy.copy_(y, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    el = e0.elapsed_time(e1) / 1e3
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hz, hu, hb))
+    return {"value": T * args.steps / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": hy.numel() * hy.element_size()}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill_8k", choices=["prefill_8k", "varlen_16"])
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    rank, ws, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, ws)
+    else:
+        run_ours(args, rank, ws, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

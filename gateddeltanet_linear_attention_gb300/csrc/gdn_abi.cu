@@ -1,0 +1,352 @@
+// gdn_abi.cu -- the extern "C" entry points of include/gdn.h: host-side
+// argument validation (before any launch), workspace carving, dispatch to the
+// kernels, and the device error word.
+#include <cmath>
+#include <mutex>
+
+#include "gdn_common.cuh"
+
+namespace {
+
+// Device-side fault word: kernels OR GDN_DEVERR_* bits into it, never trap.
+__device__ unsigned g_gdn_error_word;
+
+constexpr int kMaxDevices = 64;
+unsigned *g_err_ptr[kMaxDevices];
+std::mutex g_err_mu;
+
+// Address of the error word on the current device (resolved once per device).
+gdn_status error_word(unsigned **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_gdn_error_word) != cudaSuccess) return GDN_ERR_CUDA;
+        g_err_ptr[dev] = (unsigned *)p;
+    }
+    *out = g_err_ptr[dev];
+    return GDN_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Largest sequence count a call accepts (one grid dimension per sequence).
+constexpr int kMaxSeqs = 65535;
+
+bool valid_dtype(gdn_dtype t) { return t == GDN_BF16 || t == GDN_FP32; }
+
+// Validate the configuration and derive the kernel-side dimensions.
+gdn_status check_cfg(const gdn_config *c, gdn::Dims *d) {
+    if (!c) return GDN_ERR_INVALID_ARG;
+    if (c->hk <= 0 || c->hv <= 0 || c->dk <= 0 || c->dv <= 0 || c->chunk <= 0 ||
+        c->n_slots < 0 || !valid_dtype(c->act))
+        return GDN_ERR_INVALID_ARG;
+    if (!(std::isfinite(c->q_scale) && std::isfinite(c->l2_eps) && std::isfinite(c->norm_eps)) ||
+        c->l2_eps < 0.f || c->norm_eps < 0.f)
+        return GDN_ERR_INVALID_ARG;
+    if (c->hv % c->hk != 0) return GDN_ERR_INVALID_ARG;
+    const int grp = c->hv / c->hk;
+    if (grp != 1 && grp != 2 && grp != 4) return GDN_ERR_UNSUPPORTED;
+    if (c->dk != c->dv || (c->dk != 32 && c->dk != 64 && c->dk != 128)) return GDN_ERR_UNSUPPORTED;
+    if (c->chunk != 16 && c->chunk != 64) return GDN_ERR_UNSUPPORTED;
+    long long ch = 2LL * c->hk * c->dk + (long long)c->hv * c->dv;
+    if (ch > (1LL << 22)) return GDN_ERR_UNSUPPORTED;
+    d->hk = c->hk; d->hv = c->hv; d->dk = c->dk; d->dv = c->dv; d->grp = grp;
+    d->ch = (int)ch; d->chunk = c->chunk; d->n_slots = c->n_slots;
+    d->q_scale = c->q_scale; d->l2_eps = c->l2_eps; d->norm_eps = c->norm_eps;
+    return GDN_OK;
+}
+
+// A row-strided [rows][ld] view with `width` used elements per row.
+bool valid_view(const void *p, long long ld, long long width) {
+    return p && aligned16(p) && ld >= width && ld % 8 == 0;
+}
+
+gdn_status launch_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct PrefillWs {
+    float *xa, *g, *beta, *o;
+};
+
+size_t prefill_ws_bytes(const gdn::Dims &d, long long T) {
+    size_t t = (size_t)(T > 0 ? T : 0);
+    return align256(t * d.ch * 4) + 2 * align256(t * d.hv * 4) + align256(t * d.hv * d.dv * 4);
+}
+
+PrefillWs carve_prefill(const gdn::Dims &d, long long T, void *ws) {
+    size_t t = (size_t)T;
+    char *p = (char *)ws;
+    PrefillWs w;
+    w.xa = (float *)p; p += align256(t * d.ch * 4);
+    w.g = (float *)p; p += align256(t * d.hv * 4);
+    w.beta = (float *)p; p += align256(t * d.hv * 4);
+    w.o = (float *)p;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDN_ERR_CUDA: return "CUDA error";
+        case GDN_ERR_DEVICE: return "device-side fault reported";
+    }
+    return "unknown status";
+}
+
+size_t gdn_workspace_size(const gdn_config *cfg, int64_t max_tokens, int32_t max_seqs) {
+    gdn::Dims d;
+    if (check_cfg(cfg, &d) != GDN_OK || max_tokens < 0 || max_seqs < 0) return 0;
+    return prefill_ws_bytes(d, max_tokens) + 256;
+}
+
+gdn_status gdn_gate_prep(const gdn_config *cfg, const void *u, const void *b_logit, int64_t ld_ub,
+                         int64_t T, const float *A_log, const float *dt_bias, float *g,
+                         float *beta, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (T < 0) return GDN_ERR_INVALID_ARG;
+    if (T == 0) return GDN_OK;
+    if (!valid_view(u, ld_ub, d.hv) || !valid_view(b_logit, ld_ub, d.hv) || !A_log || !dt_bias ||
+        !g || !beta)
+        return GDN_ERR_INVALID_ARG;
+    return launch_status(gdn::launch_gate_prep(d, cfg->act == GDN_BF16, u, b_logit, ld_ub, T,
+                                               A_log, dt_bias, g, beta, (cudaStream_t)stream));
+}
+
+gdn_status gdn_conv1d_prefill(const gdn_config *cfg, const void *x, int64_t ld_x,
+                              const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
+                              const void *w, void *conv_state, const int32_t *state_idx,
+                              void *out, gdn_dtype out_dtype, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (T < 0 || n_seqs < 0 || !valid_dtype(out_dtype)) return GDN_ERR_INVALID_ARG;
+    if (n_seqs > kMaxSeqs) return GDN_ERR_UNSUPPORTED;
+    if (n_seqs == 0 || T == 0) {
+        if (T != 0) return GDN_ERR_INVALID_ARG;
+        if (n_seqs == 0) return GDN_OK;
+    }
+    if (!cu_seqlens || !w || !out || (T > 0 && !valid_view(x, ld_x, d.ch))) return GDN_ERR_INVALID_ARG;
+    if (conv_state && !aligned16(conv_state)) return GDN_ERR_INVALID_ARG;
+    if (conv_state && d.n_slots == 0) return GDN_ERR_INVALID_ARG;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool bf = cfg->act == GDN_BF16;
+    cudaError_t e = gdn::launch_conv_prefill(d, bf, x, ld_x, cu_seqlens, n_seqs, T, w, conv_state,
+                                             state_idx, out, out_dtype == GDN_BF16, err, s);
+    if (e == cudaSuccess)
+        e = gdn::launch_conv_state_update(d, bf, x, ld_x, cu_seqlens, n_seqs, T, conv_state,
+                                          state_idx, err, s);
+    return launch_status(e);
+}
+
+gdn_status gdn_conv1d_step(const gdn_config *cfg, const void *x, int64_t ld_x, int32_t n,
+                           const void *w, void *conv_state, const int32_t *state_idx, void *out,
+                           gdn_dtype out_dtype, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (n < 0 || !valid_dtype(out_dtype)) return GDN_ERR_INVALID_ARG;
+    if (n > kMaxSeqs) return GDN_ERR_UNSUPPORTED;
+    if (n == 0) return GDN_OK;
+    if (!valid_view(x, ld_x, d.ch) || !w || !conv_state || !aligned16(conv_state) || !out ||
+        d.n_slots == 0)
+        return GDN_ERR_INVALID_ARG;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    return launch_status(gdn::launch_conv_step(d, cfg->act == GDN_BF16, x, ld_x, n, w, conv_state,
+                                               state_idx, out, out_dtype == GDN_BF16, err,
+                                               (cudaStream_t)stream));
+}
+
+gdn_status gdn_chunk_prefill(const gdn_config *cfg, const void *q, const void *k, int64_t ld_qk,
+                             const void *v, int64_t ld_v, gdn_dtype in_dtype, const float *g,
+                             const float *beta, const int32_t *cu_seqlens, int32_t n_seqs,
+                             int64_t T, const float *state_in, float *state_out,
+                             const int32_t *state_idx, void *o, gdn_dtype o_dtype, uint32_t flags,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (T < 0 || n_seqs < 0 || !valid_dtype(in_dtype) || !valid_dtype(o_dtype) ||
+        (flags & ~GDN_FLAG_L2NORM_QK))
+        return GDN_ERR_INVALID_ARG;
+    if (n_seqs > kMaxSeqs) return GDN_ERR_UNSUPPORTED;
+    if (n_seqs == 0) return T == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (!cu_seqlens || !g || !beta || !o) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (!valid_view(q, ld_qk, (long long)d.hk * d.dk) ||
+                  !valid_view(k, ld_qk, (long long)d.hk * d.dk) ||
+                  !valid_view(v, ld_v, (long long)d.hv * d.dv)))
+        return GDN_ERR_INVALID_ARG;
+    if ((state_in && !aligned16(state_in)) || (state_out && !aligned16(state_out)))
+        return GDN_ERR_INVALID_ARG;
+    if ((state_in || state_out) && d.n_slots == 0) return GDN_ERR_INVALID_ARG;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    gdn::ChunkArgs a;
+    a.q = q; a.k = k; a.v = v; a.ld_qk = ld_qk; a.ld_v = ld_v; a.g = g; a.beta = beta;
+    a.cu_seqlens = cu_seqlens; a.n_seqs = n_seqs; a.T = T; a.state_in = state_in;
+    a.state_out = state_out; a.state_idx = state_idx; a.o = o; a.flags = flags; a.d = d;
+    a.err = err;
+    return launch_status(gdn::launch_chunk_simt(a, in_dtype == GDN_BF16, o_dtype == GDN_BF16,
+                                                (cudaStream_t)stream));
+}
+
+gdn_status gdn_recurrent_decode(const gdn_config *cfg, const void *q, const void *k, int64_t ld_qk,
+                                const void *v, int64_t ld_v, gdn_dtype in_dtype, const float *g,
+                                const float *beta, int32_t n, float *state,
+                                const int32_t *state_idx, void *o, gdn_dtype o_dtype,
+                                uint32_t flags, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (n < 0 || !valid_dtype(in_dtype) || !valid_dtype(o_dtype) || (flags & ~GDN_FLAG_L2NORM_QK))
+        return GDN_ERR_INVALID_ARG;
+    if (n > kMaxSeqs) return GDN_ERR_UNSUPPORTED;
+    if (n == 0) return GDN_OK;
+    if (!valid_view(q, ld_qk, (long long)d.hk * d.dk) ||
+        !valid_view(k, ld_qk, (long long)d.hk * d.dk) ||
+        !valid_view(v, ld_v, (long long)d.hv * d.dv) || !g || !beta || !state ||
+        !aligned16(state) || !o || d.n_slots == 0)
+        return GDN_ERR_INVALID_ARG;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    gdn::DecodeArgs a = {};
+    a.q = q; a.k = k; a.v = v; a.ld_qk = ld_qk; a.ld_v = ld_v; a.g = g; a.beta = beta;
+    a.n = n; a.state = state; a.state_idx = state_idx; a.out = o; a.flags = flags; a.d = d;
+    a.err = err;
+    return launch_status(gdn::launch_decode(a, false, in_dtype == GDN_BF16, o_dtype == GDN_BF16,
+                                            (cudaStream_t)stream));
+}
+
+gdn_status gdn_gated_rmsnorm(const gdn_config *cfg, const void *o, gdn_dtype o_dtype,
+                             const void *z, int64_t ld_z, const float *w, int64_t T, void *y,
+                             gdn_dtype y_dtype, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (T < 0 || !valid_dtype(o_dtype) || !valid_dtype(y_dtype)) return GDN_ERR_INVALID_ARG;
+    if (T == 0) return GDN_OK;
+    if (!o || !aligned16(o) || !valid_view(z, ld_z, (long long)d.hv * d.dv) || !w || !y)
+        return GDN_ERR_INVALID_ARG;
+    return launch_status(gdn::launch_gated_rmsnorm(d, cfg->act == GDN_BF16, o, o_dtype == GDN_BF16,
+                                                   z, ld_z, w, T, y, y_dtype == GDN_BF16,
+                                                   (cudaStream_t)stream));
+}
+
+// Validation shared by the fused entry points.
+static gdn_status check_mixer_io(const gdn::Dims &d, const gdn_mixer_io *io, bool decode) {
+    if (!io || io->n_seqs < 0 || io->T < 0 || !valid_dtype(io->y_dtype)) return GDN_ERR_INVALID_ARG;
+    if (io->n_seqs > kMaxSeqs) return GDN_ERR_UNSUPPORTED;
+    if (decode && io->T != io->n_seqs) return GDN_ERR_INVALID_ARG;
+    if (io->T == 0) return GDN_OK;
+    if (!valid_view(io->x, io->ld_x, d.ch) || !valid_view(io->z, io->ld_z, (long long)d.hv * d.dv) ||
+        !valid_view(io->u, io->ld_ub, d.hv) || !valid_view(io->b_logit, io->ld_ub, d.hv) ||
+        !io->conv_w || !io->A_log || !io->dt_bias || !io->norm_w || !io->y)
+        return GDN_ERR_INVALID_ARG;
+    if (!decode && !io->cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if ((io->state_in && !aligned16(io->state_in)) || (io->state_out && !aligned16(io->state_out)) ||
+        (io->conv_state && !aligned16(io->conv_state)))
+        return GDN_ERR_INVALID_ARG;
+    if ((io->state_in || io->state_out || io->conv_state) && d.n_slots == 0)
+        return GDN_ERR_INVALID_ARG;
+    if (decode && (!io->state_in || io->state_out != io->state_in || !io->conv_state))
+        return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if ((st = check_mixer_io(d, io, false)) != GDN_OK) return st;
+    if (io->n_seqs == 0) return io->T == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    unsigned *err = nullptr;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (io->T == 0) {
+        // only empty sequences: the state passes through (written when out != in)
+        if (!io->state_out || io->state_out == io->state_in) return GDN_OK;
+        if ((st = error_word(&err)) != GDN_OK) return st;
+        gdn::ChunkArgs a = {};
+        a.cu_seqlens = io->cu_seqlens; a.n_seqs = io->n_seqs; a.T = 0;
+        a.state_in = io->state_in; a.state_out = io->state_out; a.state_idx = io->state_idx;
+        a.o = io->y; a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
+        return launch_status(gdn::launch_chunk_simt(a, false, false, s));
+    }
+    if (!workspace || !aligned16(workspace) || workspace_bytes < prefill_ws_bytes(d, io->T))
+        return GDN_ERR_WORKSPACE;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    const bool bf = cfg->act == GDN_BF16;
+    PrefillWs w = carve_prefill(d, io->T, workspace);
+    cudaError_t e = gdn::launch_gate_prep(d, bf, io->u, io->b_logit, io->ld_ub, io->T, io->A_log,
+                                          io->dt_bias, w.g, w.beta, s);
+    if (e == cudaSuccess)
+        e = gdn::launch_conv_prefill(d, bf, io->x, io->ld_x, io->cu_seqlens, io->n_seqs, io->T,
+                                     io->conv_w, io->conv_state, io->state_idx, w.xa, false, err,
+                                     s);
+    if (e == cudaSuccess)
+        e = gdn::launch_conv_state_update(d, bf, io->x, io->ld_x, io->cu_seqlens, io->n_seqs,
+                                          io->T, io->conv_state, io->state_idx, err, s);
+    if (e == cudaSuccess) {
+        gdn::ChunkArgs a;
+        a.q = w.xa;
+        a.k = w.xa + (long long)d.hk * d.dk;
+        a.v = w.xa + 2LL * d.hk * d.dk;
+        a.ld_qk = d.ch; a.ld_v = d.ch; a.g = w.g; a.beta = w.beta;
+        a.cu_seqlens = io->cu_seqlens; a.n_seqs = io->n_seqs; a.T = io->T;
+        a.state_in = io->state_in; a.state_out = io->state_out; a.state_idx = io->state_idx;
+        a.o = w.o; a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
+        e = gdn::launch_chunk_simt(a, false, false, s);
+    }
+    if (e == cudaSuccess)
+        e = gdn::launch_gated_rmsnorm(d, bf, w.o, false, io->z, io->ld_z, io->norm_w, io->T, io->y,
+                                      io->y_dtype == GDN_BF16, s);
+    return launch_status(e);
+}
+
+gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if ((st = check_mixer_io(d, io, true)) != GDN_OK) return st;
+    if (io->n_seqs == 0) return GDN_OK;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    gdn::DecodeArgs a = {};
+    a.x = io->x; a.ld_x = io->ld_x; a.conv_w = io->conv_w; a.conv_state = io->conv_state;
+    a.u = io->u; a.b_logit = io->b_logit; a.ld_ub = io->ld_ub; a.A_log = io->A_log;
+    a.dt_bias = io->dt_bias; a.z = io->z; a.ld_z = io->ld_z; a.norm_w = io->norm_w;
+    a.n = io->n_seqs; a.state = io->state_out; a.state_idx = io->state_idx; a.out = io->y;
+    a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
+    return launch_status(gdn::launch_decode(a, true, cfg->act == GDN_BF16,
+                                            io->y_dtype == GDN_BF16, (cudaStream_t)stream));
+}
+
+gdn_status gdn_device_error(void *stream, uint32_t *code) {
+    if (!code) return GDN_ERR_INVALID_ARG;
+    *code = 0;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gdn_error_word, sizeof(v)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_gdn_error_word, &zero, sizeof(zero)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    *code = v;
+    return v ? GDN_ERR_DEVICE : GDN_OK;
+}
+
+}  // extern "C"

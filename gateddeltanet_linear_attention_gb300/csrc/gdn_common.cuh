@@ -1,0 +1,127 @@
+// gdn_common.cuh -- device helpers shared by the GDN kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Shapes and scalars every kernel needs, passed by value.
+struct Dims {
+    int hk, hv, dk, dv, grp;  // grp = hv / hk (v-heads sharing one q/k head)
+    int ch;                   // 2*hk*dk + hv*dv
+    int chunk;
+    int n_slots;
+    float q_scale, l2_eps, norm_eps;
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Record a device-side fault in the library's error word (never traps).
+__device__ __forceinline__ void set_error(unsigned *err, unsigned code) {
+    if (err) atomicOr(err, code);
+}
+
+// Slot of sequence n: identity without a map; -1 (padding lane) when the map
+// says so or the entry is out of range (the latter is also reported).
+__device__ __forceinline__ int slot_of(const int32_t *state_idx, int n, int n_slots,
+                                       unsigned *err) {
+    int s = state_idx ? state_idx[n] : n;
+    if (s >= n_slots) {
+        set_error(err, GDN_DEVERR_SLOT);
+        return -1;
+    }
+    return s;
+}
+
+// Bounds of sequence n, clamped to [0, T] so that malformed cu_seqlens never
+// lead to an out-of-range access; malformed input is reported.
+__device__ __forceinline__ void seq_bounds(const int32_t *cu, int n, long long T, unsigned *err,
+                                           long long &s, long long &e) {
+    long long a = cu[n], b = cu[n + 1];
+    if (a < 0 || b < a || b > T) {
+        set_error(err, GDN_DEVERR_CU_SEQLENS);
+        a = a < 0 ? 0 : (a > T ? T : a);
+        b = b < a ? a : (b > T ? T : b);
+    }
+    s = a;
+    e = b;
+}
+
+}  // namespace gdn
+
+// Launchers implemented by the kernel translation units and called by the ABI.
+namespace gdn {
+struct ChunkArgs {
+    const void *q, *k, *v;
+    long long ld_qk, ld_v;
+    const float *g, *beta;
+    const int32_t *cu_seqlens;
+    int n_seqs;
+    long long T;
+    const float *state_in;
+    float *state_out;
+    const int32_t *state_idx;
+    void *o;
+    unsigned flags;
+    Dims d;
+    unsigned *err;
+};
+
+struct DecodeArgs {
+    // fused form: raw x / conv; unfused form: q, k, v post-conv
+    const void *x; long long ld_x; const void *conv_w; void *conv_state;
+    const void *q, *k, *v; long long ld_qk, ld_v;
+    const void *u, *b_logit; long long ld_ub; const float *A_log, *dt_bias;  // fused gates
+    const float *g, *beta;                                                   // unfused gates
+    const void *z; long long ld_z; const float *norm_w;                      // fused norm
+    int n;
+    float *state;
+    const int32_t *state_idx;
+    void *out;  // fused: y; unfused: o
+    unsigned flags;
+    Dims d;
+    unsigned *err;
+};
+
+cudaError_t launch_gate_prep(const Dims &d, bool act_bf16, const void *u, const void *b,
+                             long long ld_ub, long long T, const float *A_log,
+                             const float *dt_bias, float *g, float *beta, cudaStream_t s);
+cudaError_t launch_conv_prefill(const Dims &d, bool act_bf16, const void *x, long long ld_x,
+                                const int32_t *cu, int n_seqs, long long T, const void *w,
+                                const void *conv_state, const int32_t *state_idx, void *out,
+                                bool out_bf16, unsigned *err, cudaStream_t s);
+cudaError_t launch_conv_state_update(const Dims &d, bool act_bf16, const void *x,
+                                     long long ld_x, const int32_t *cu, int n_seqs, long long T,
+                                     void *conv_state, const int32_t *state_idx, unsigned *err,
+                                     cudaStream_t s);
+cudaError_t launch_conv_step(const Dims &d, bool act_bf16, const void *x, long long ld_x, int n,
+                             const void *w, void *conv_state, const int32_t *state_idx,
+                             void *out, bool out_bf16, unsigned *err, cudaStream_t s);
+cudaError_t launch_gated_rmsnorm(const Dims &d, bool act_bf16, const void *o, bool o_bf16,
+                                 const void *z, long long ld_z, const float *w, long long T,
+                                 void *y, bool y_bf16, cudaStream_t s);
+cudaError_t launch_chunk_simt(const ChunkArgs &a, bool in_bf16, bool o_bf16, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs &a, bool fused, bool in_bf16, bool out_bf16,
+                          cudaStream_t s);
+}  // namespace gdn

@@ -1,0 +1,142 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+entry point include/gdn.h declares, and rejects bad arguments with a typed
+status BEFORE touching CUDA (fake, never-dereferenced pointers are enough to
+reach each check)."""
+import ctypes
+
+import pytest
+
+from gateddeltanet_linear_attention_gb300 import gdn
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+P = ctypes.c_void_p
+A16 = P(0x100000)          # 16-byte aligned fake device address
+A16b = P(0x200000)
+MIS = P(0x100004)          # misaligned
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return gdn.load()
+
+
+def cfg(**kw):
+    base = dict(HK=16, HV=32, dk=128, dv=128, chunk=64, act="bf16", n_slots=4)
+    base.update(kw)
+    return gdn.make_config(**base)
+
+
+def test_exports_every_declared_entry_point(lib):
+    names = gdn.header_entry_points()
+    assert {"gdn_conv1d_prefill", "gdn_conv1d_step", "gdn_chunk_prefill", "gdn_recurrent_decode",
+            "gdn_gated_rmsnorm", "gdn_mixer_prefill", "gdn_mixer_decode", "gdn_gate_prep",
+            "gdn_workspace_size", "gdn_device_error", "gdn_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert gdn.gdn_status_string(s) != "unknown status"
+    assert gdn.gdn_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(chunk=32), UNSUPPORTED), (dict(dk=128, dv=64), UNSUPPORTED), (dict(dk=96, dv=96), UNSUPPORTED),
+    (dict(HK=16, HV=24), INVALID), (dict(HK=4, HV=32), UNSUPPORTED), (dict(HK=0), INVALID),
+    (dict(n_slots=-1), INVALID), (dict(chunk=0), INVALID),
+])
+def test_config_validation(lib, kw, expect):
+    c = cfg(**kw)
+    st = lib.gdn_gate_prep(ctypes.byref(c), A16, A16b, 32, 10, A16, A16, A16, A16, None)
+    assert st == expect
+    assert lib.gdn_workspace_size(ctypes.byref(c), 100, 1) == 0
+
+
+def test_null_config(lib):
+    assert lib.gdn_gate_prep(None, A16, A16, 32, 1, A16, A16, A16, A16, None) == INVALID
+    assert lib.gdn_workspace_size(None, 1, 1) == 0
+
+
+def test_view_checks(lib):
+    c = cfg()
+    # ld smaller than HV, ld not a multiple of 8, misaligned, null
+    assert lib.gdn_gate_prep(ctypes.byref(c), A16, A16, 16, 1, A16, A16, A16, A16, None) == INVALID
+    assert lib.gdn_gate_prep(ctypes.byref(c), A16, A16, 33, 1, A16, A16, A16, A16, None) == INVALID
+    assert lib.gdn_gate_prep(ctypes.byref(c), MIS, A16, 32, 1, A16, A16, A16, A16, None) == INVALID
+    assert lib.gdn_gate_prep(ctypes.byref(c), None, A16, 32, 1, A16, A16, A16, A16, None) == INVALID
+    # T = 0 is a no-op that never touches the GPU
+    assert lib.gdn_gate_prep(ctypes.byref(c), None, None, 0, 0, None, None, None, None, None) == OK
+    assert lib.gdn_gate_prep(ctypes.byref(c), A16, A16, 32, -1, A16, A16, A16, A16, None) == INVALID
+
+
+def test_chunk_prefill_validation(lib):
+    c = cfg()
+    ch = ctypes.byref(c)
+    # bad flag bit
+    assert lib.gdn_chunk_prefill(ch, A16, A16, 2048, A16, 4096, 0, A16, A16, A16, 1, 64, None, None,
+                                 None, A16, 1, 0x10, None, 0, None) == INVALID
+    # q/k row stride narrower than HK*dk
+    assert lib.gdn_chunk_prefill(ch, A16, A16, 1024, A16, 4096, 0, A16, A16, A16, 1, 64, None, None,
+                                 None, A16, 1, 1, None, 0, None) == INVALID
+    # misaligned state
+    assert lib.gdn_chunk_prefill(ch, A16, A16, 2048, A16, 4096, 0, A16, A16, A16, 1, 64, MIS, None,
+                                 None, A16, 1, 1, None, 0, None) == INVALID
+    # state without slots
+    c0 = cfg(n_slots=0)
+    assert lib.gdn_chunk_prefill(ctypes.byref(c0), A16, A16, 2048, A16, 4096, 0, A16, A16, A16, 1, 64,
+                                 A16, A16, None, A16, 1, 1, None, 0, None) == INVALID
+    # zero sequences with tokens is inconsistent; zero of both is a no-op
+    assert lib.gdn_chunk_prefill(ch, A16, A16, 2048, A16, 4096, 0, A16, A16, A16, 0, 5, None, None,
+                                 None, A16, 1, 1, None, 0, None) == INVALID
+    assert lib.gdn_chunk_prefill(ch, None, None, 0, None, 0, 0, None, None, None, 0, 0, None, None,
+                                 None, None, 1, 1, None, 0, None) == OK
+
+
+def _io(T=64, n=1, **kw):
+    io = gdn.MixerIO(A16, 8192, A16, 4096, A16, A16, 32, A16, A16, A16, A16, A16, n, T, None, None,
+                     None, None, A16, 1)
+    for k, v in kw.items():
+        setattr(io, k, v)
+    return io
+
+
+def test_mixer_validation_and_workspace(lib):
+    c = cfg()
+    ch = ctypes.byref(c)
+    need = lib.gdn_workspace_size(ch, 64, 1)
+    assert need >= 64 * (8192 + 4096 + 64) * 4
+    io = _io()
+    assert lib.gdn_mixer_prefill(ch, ctypes.byref(io), None, 0, None) == WORKSPACE
+    assert lib.gdn_mixer_prefill(ch, ctypes.byref(io), A16, 1024, None) == WORKSPACE
+    assert lib.gdn_mixer_prefill(ch, ctypes.byref(io), MIS, need, None) == WORKSPACE
+    bad = _io(ld_x=8000)                       # narrower than CH
+    assert lib.gdn_mixer_prefill(ch, ctypes.byref(bad), A16, need, None) == INVALID
+    bad = _io(cu_seqlens=None)
+    assert lib.gdn_mixer_prefill(ch, ctypes.byref(bad), A16, need, None) == INVALID
+    bad = _io(y_dtype=7)
+    assert lib.gdn_mixer_prefill(ch, ctypes.byref(bad), A16, need, None) == INVALID
+    assert lib.gdn_mixer_prefill(ch, None, A16, need, None) == INVALID
+    # decode: T must equal n_seqs, state in place and required, conv history required
+    d = _io(T=4, n=4, state_in=A16, state_out=A16, conv_state=A16b)
+    bad = _io(T=5, n=4, state_in=A16, state_out=A16, conv_state=A16b)
+    assert lib.gdn_mixer_decode(ch, ctypes.byref(bad), None) == INVALID
+    bad = _io(T=4, n=4, state_in=A16, state_out=A16b, conv_state=A16b)
+    assert lib.gdn_mixer_decode(ch, ctypes.byref(bad), None) == INVALID
+    bad = _io(T=4, n=4, state_in=A16, state_out=A16, conv_state=None)
+    assert lib.gdn_mixer_decode(ch, ctypes.byref(bad), None) == INVALID
+    c0 = cfg(n_slots=0)
+    assert lib.gdn_mixer_decode(ctypes.byref(c0), ctypes.byref(d), None) == INVALID
+
+
+def test_decode_and_norm_validation(lib):
+    c = cfg()
+    ch = ctypes.byref(c)
+    assert lib.gdn_recurrent_decode(ch, A16, A16, 2048, A16, 4096, 0, A16, A16, 4, None, None, A16, 1,
+                                    1, None) == INVALID          # no state
+    assert lib.gdn_recurrent_decode(ch, A16, A16, 2048, A16, 4096, 0, A16, A16, 4, MIS, None, A16, 1,
+                                    1, None) == INVALID          # misaligned state
+    assert lib.gdn_gated_rmsnorm(ch, A16, 1, A16, 100, A16, 4, A16, 1, None) == INVALID
+    assert lib.gdn_gated_rmsnorm(ch, A16, 3, A16, 4096, A16, 4, A16, 1, None) == INVALID
+    assert lib.gdn_conv1d_step(ch, A16, 8192, 2, A16, None, None, A16, 1, None) == INVALID
+    assert lib.gdn_conv1d_prefill(ch, A16, 8192, None, 1, 10, A16, None, None, A16, 1, None) == INVALID
