@@ -58,9 +58,15 @@ gdn_status check_cfg(const gdn_config *c, gdn::Dims *d) {
     return GDN_OK;
 }
 
-// A row-strided [rows][ld] view with `width` used elements per row.
+// A row-strided [rows][ld] view with `width` used elements per row, rows
+// 16-byte aligned (vector / bulk loads).
 bool valid_view(const void *p, long long ld, long long width) {
     return p && aligned16(p) && ld >= width && ld % 8 == 0;
+}
+
+// A narrow row-strided view read element by element (u, b_logit: HV columns).
+bool valid_narrow_view(const void *p, long long ld, long long width) {
+    return p && ((uintptr_t)p & 3u) == 0 && ld >= width;
 }
 
 gdn_status launch_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
@@ -87,7 +93,37 @@ PrefillWs carve_prefill(const gdn::Dims &d, long long T, void *ws) {
     return w;
 }
 
+// The chunked rule: bf16-activation configurations with dk = dv = 128 and
+// 64-token chunks run on the tensor cores (split-bf16 operands); everything
+// else, and the fp32-activation mode, runs the exact fp32 SIMT kernel.  The
+// state-column slice per CTA is 32 when few (sequence, head) units exist (to
+// spread a long sequence over more SMs), else 64 (less duplicated work).
+cudaError_t launch_chunk(const gdn::ChunkArgs &a, bool act_bf16, bool in_bf16, bool o_bf16,
+                         cudaStream_t s) {
+    if (act_bf16 && gdn::chunk_tc_supported(a.d)) {
+        const long long units = (long long)a.n_seqs * a.d.hv;
+        const int dvs = units * 2 >= gdn::sm_count() ? 64 : 32;
+        return gdn::launch_chunk_tc(a, in_bf16, o_bf16, dvs, s);
+    }
+    return gdn::launch_chunk_simt(a, in_bf16, o_bf16, s);
+}
+
 }  // namespace
+
+namespace gdn {
+int sm_count() {
+    static int cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    if (!cached[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+}  // namespace gdn
 
 extern "C" {
 
@@ -117,7 +153,7 @@ gdn_status gdn_gate_prep(const gdn_config *cfg, const void *u, const void *b_log
     if (st != GDN_OK) return st;
     if (T < 0) return GDN_ERR_INVALID_ARG;
     if (T == 0) return GDN_OK;
-    if (!valid_view(u, ld_ub, d.hv) || !valid_view(b_logit, ld_ub, d.hv) || !A_log || !dt_bias ||
+    if (!valid_narrow_view(u, ld_ub, d.hv) || !valid_narrow_view(b_logit, ld_ub, d.hv) || !A_log || !dt_bias ||
         !g || !beta)
         return GDN_ERR_INVALID_ARG;
     return launch_status(gdn::launch_gate_prep(d, cfg->act == GDN_BF16, u, b_logit, ld_ub, T,
@@ -202,8 +238,8 @@ gdn_status gdn_chunk_prefill(const gdn_config *cfg, const void *q, const void *k
     a.cu_seqlens = cu_seqlens; a.n_seqs = n_seqs; a.T = T; a.state_in = state_in;
     a.state_out = state_out; a.state_idx = state_idx; a.o = o; a.flags = flags; a.d = d;
     a.err = err;
-    return launch_status(gdn::launch_chunk_simt(a, in_dtype == GDN_BF16, o_dtype == GDN_BF16,
-                                                (cudaStream_t)stream));
+    return launch_status(launch_chunk(a, cfg->act == GDN_BF16, in_dtype == GDN_BF16,
+                                      o_dtype == GDN_BF16, (cudaStream_t)stream));
 }
 
 gdn_status gdn_recurrent_decode(const gdn_config *cfg, const void *q, const void *k, int64_t ld_qk,
@@ -255,7 +291,7 @@ static gdn_status check_mixer_io(const gdn::Dims &d, const gdn_mixer_io *io, boo
     if (decode && io->T != io->n_seqs) return GDN_ERR_INVALID_ARG;
     if (io->T == 0) return GDN_OK;
     if (!valid_view(io->x, io->ld_x, d.ch) || !valid_view(io->z, io->ld_z, (long long)d.hv * d.dv) ||
-        !valid_view(io->u, io->ld_ub, d.hv) || !valid_view(io->b_logit, io->ld_ub, d.hv) ||
+        !valid_narrow_view(io->u, io->ld_ub, d.hv) || !valid_narrow_view(io->b_logit, io->ld_ub, d.hv) ||
         !io->conv_w || !io->A_log || !io->dt_bias || !io->norm_w || !io->y)
         return GDN_ERR_INVALID_ARG;
     if (!decode && !io->cu_seqlens) return GDN_ERR_INVALID_ARG;
@@ -286,7 +322,7 @@ gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void
         a.cu_seqlens = io->cu_seqlens; a.n_seqs = io->n_seqs; a.T = 0;
         a.state_in = io->state_in; a.state_out = io->state_out; a.state_idx = io->state_idx;
         a.o = io->y; a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
-        return launch_status(gdn::launch_chunk_simt(a, false, false, s));
+        return launch_status(launch_chunk(a, cfg->act == GDN_BF16, false, false, s));
     }
     if (!workspace || !aligned16(workspace) || workspace_bytes < prefill_ws_bytes(d, io->T))
         return GDN_ERR_WORKSPACE;
@@ -311,7 +347,7 @@ gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void
         a.cu_seqlens = io->cu_seqlens; a.n_seqs = io->n_seqs; a.T = io->T;
         a.state_in = io->state_in; a.state_out = io->state_out; a.state_idx = io->state_idx;
         a.o = w.o; a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
-        e = gdn::launch_chunk_simt(a, false, false, s);
+        e = launch_chunk(a, bf, false, false, s);
     }
     if (e == cudaSuccess)
         e = gdn::launch_gated_rmsnorm(d, bf, w.o, false, io->z, io->ld_z, io->norm_w, io->T, io->y,

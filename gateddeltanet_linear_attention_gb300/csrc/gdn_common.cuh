@@ -122,6 +122,10 @@ cudaError_t launch_gated_rmsnorm(const Dims &d, bool act_bf16, const void *o, bo
                                  const void *z, long long ld_z, const float *w, long long T,
                                  void *y, bool y_bf16, cudaStream_t s);
 cudaError_t launch_chunk_simt(const ChunkArgs &a, bool in_bf16, bool o_bf16, cudaStream_t s);
+bool chunk_tc_supported(const Dims &d);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, cudaStream_t s);
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
 cudaError_t launch_decode(const DecodeArgs &a, bool fused, bool in_bf16, bool out_bf16,
                           cudaStream_t s);
 }  // namespace gdn

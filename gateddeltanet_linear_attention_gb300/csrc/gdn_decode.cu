@@ -22,6 +22,7 @@
 // has exactly one owner, so the in-place shift is race-free), SiLU, the q/k L2
 // norm, the gates and the gated RMSNorm: one launch per decode step.
 #include "gdn_common.cuh"
+#include "tc_sm103.cuh"
 
 namespace gdn {
 
@@ -38,11 +39,14 @@ template <int DK, int DV, typename TA, typename TOut, bool FUSED>
 __global__ void __launch_bounds__(4 * DV) decode_kernel(DecodeArgs a) {
     using Cfg = DecodeCfg<DK, DV>;
     constexpr int NT = Cfg::NT, LPR = Cfg::LPR, RPP = Cfg::RPP, RPT = Cfg::RPT;
-    __shared__ float qs[DK], ks[DK];
-    __shared__ float vs[Cfg::MAXG][DV];
+    __shared__ __align__(16) float qs[DK];
+    __shared__ __align__(16) float ks[DK];
+    __shared__ __align__(16) float vs[Cfg::MAXG][DV];
     __shared__ float gate_a[Cfg::MAXG], gate_b[Cfg::MAXG];
-    __shared__ float red_p[RPP][DV], red_s[RPP][DV];
-    __shared__ float up[DV], os[DV];
+    __shared__ __align__(16) float red_p[RPP][DV];
+    __shared__ __align__(16) float red_s[RPP][DV];
+    __shared__ __align__(16) float up[DV];
+    __shared__ __align__(16) float os[DV];
     __shared__ float scal[8];
 
     const Dims &d = a.d;
@@ -211,11 +215,246 @@ __global__ void __launch_bounds__(4 * DV) decode_kernel(DecodeArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming form of the fused decode (the product path).  A persistent grid of
+// one CTA per SM walks its (sequence, q/k head) units; each unit's G head
+// states (dk*dv*4 bytes each) flow HBM -> shared memory through a ring of NS
+// slots filled by bulk asynchronous copies (cp.async.bulk, completion counted
+// on one mbarrier per slot), so that while one head is being updated the next
+// NS-1 are already in flight.  The arithmetic per head is the same as
+// decode_kernel's; the new state goes straight from registers to HBM.
+template <int DK, int DV>
+struct StreamCfg {
+    static constexpr int NT = 4 * DV;
+    static constexpr int LPR = DV / 4, RPP = NT / LPR, RPT = DK / RPP;
+    static constexpr int SLOT = DK * DV * 4;                        // bytes of one head state
+    static constexpr int NS = SLOT >= 65536 ? 3 : (SLOT >= 16384 ? 8 : 16);
+    static constexpr int MAXG = 4;
+    static constexpr int CHUNK = SLOT < 16384 ? SLOT : 16384;       // bytes per bulk copy
+};
+
+// Every array read or written as float4 is 16-byte aligned explicitly.
+template <int DK, int DV>
+struct StreamTail {
+    alignas(16) uint64_t full[StreamCfg<DK, DV>::NS];
+    alignas(16) float qs[DK];
+    alignas(16) float ks[DK];
+    alignas(16) float vs[StreamCfg<DK, DV>::MAXG][DV];
+    alignas(16) float red_p[StreamCfg<DK, DV>::RPP][DV];
+    alignas(16) float red_s[StreamCfg<DK, DV>::RPP][DV];
+    alignas(16) float up[DV];
+    alignas(16) float os[DV];
+    float gate_a[StreamCfg<DK, DV>::MAXG], gate_b[StreamCfg<DK, DV>::MAXG];
+    float scal[8];
+    int unit_slot;
+};
+
+template <int DK, int DV>
+constexpr size_t stream_smem_bytes() {
+    return (size_t)StreamCfg<DK, DV>::NS * StreamCfg<DK, DV>::SLOT + sizeof(StreamTail<DK, DV>);
+}
+
+template <int DK, int DV, typename TA, typename TOut>
+__global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) {
+    using Cfg = StreamCfg<DK, DV>;
+    constexpr int NT = Cfg::NT, LPR = Cfg::LPR, RPP = Cfg::RPP, RPT = Cfg::RPT, NS = Cfg::NS;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *slots = reinterpret_cast<float *>(smem_raw);
+    StreamTail<DK, DV> &tl = *reinterpret_cast<StreamTail<DK, DV> *>(smem_raw + NS * Cfg::SLOT);
+
+    const Dims &d = a.d;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = d.grp;
+    const int n_units = a.n * d.hk;
+    if ((int)blockIdx.x >= n_units) return;
+    const int my_units = (n_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int n_items = my_units * G;
+    TOut *out = (TOut *)a.out;
+    const int rg = tid / LPR, c4 = (tid % LPR) * 4;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) tc::mbar_init(tc::smem_u32(&tl.full[s]), 1);
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
+
+    // producer (thread 0): bulk-load item `it`'s head state into slot it % NS
+    auto issue = [&](int it) {
+        const int u = (int)blockIdx.x + (it / G) * (int)gridDim.x, gi = it % G;
+        const int n = u / d.hk, kh = u % d.hk;
+        const int slot = a.state_idx ? a.state_idx[n] : n;
+        const uint32_t mb = tc::smem_u32(&tl.full[it % NS]);
+        if (slot < 0 || slot >= d.n_slots) {  // padding lane: complete the phase, no copy
+            tc::mbar_arrive(mb);
+            return;
+        }
+        const char *src = reinterpret_cast<const char *>(
+            a.state + ((long long)slot * d.hv + (long long)kh * G + gi) * DK * DV);
+        const uint32_t dst = tc::smem_u32(slots) + (uint32_t)((it % NS) * Cfg::SLOT);
+        tc::mbar_arrive_expect_tx(mb, Cfg::SLOT);
+        for (int c = 0; c < Cfg::SLOT; c += Cfg::CHUNK) tc::bulk_g2s(dst + c, src + c, Cfg::CHUNK, mb);
+    };
+    if (tid == 0)
+        for (int it = 0; it < NS && it < n_items; ++it) issue(it);
+
+    for (int it = 0; it < n_items; ++it) {
+        const int gi = it % G;
+        const int u = (int)blockIdx.x + (it / G) * (int)gridDim.x;
+        const int n = u / d.hk, kh = u % d.hk;
+        const int h = kh * G + gi;
+        const long long out_row = (long long)n * d.hv * DV;
+        if (gi == 0) {
+            // ---- unit prologue: conv step of this unit's q/k/v channels, SiLU, L2, gates
+            const int slot = slot_of(a.state_idx, n, d.n_slots, a.err);
+            if (tid == 0) tl.unit_slot = slot;
+            if (slot >= 0) {
+                const TA *x = (const TA *)a.x + (long long)n * a.ld_x;
+                const TA *w = (const TA *)a.conv_w;
+                TA *cs = (TA *)a.conv_state + (long long)slot * d.ch * 3;
+                const int nch = 2 * DK + G * DV;
+                for (int ci = tid; ci < nch; ci += NT) {
+                    int c;
+                    if (ci < DK) c = kh * DK + ci;
+                    else if (ci < 2 * DK) c = d.hk * DK + kh * DK + (ci - DK);
+                    else c = 2 * d.hk * DK + kh * G * DV + (ci - 2 * DK);
+                    TA *hc = cs + (long long)c * 3;
+                    TA h0 = hc[0], h1 = hc[1], h2 = hc[2], xc = x[c];
+                    float acc = to_f32(w[c * 4 + 0]) * to_f32(h0) + to_f32(w[c * 4 + 1]) * to_f32(h1) +
+                                to_f32(w[c * 4 + 2]) * to_f32(h2) + to_f32(w[c * 4 + 3]) * to_f32(xc);
+                    hc[0] = h1;
+                    hc[1] = h2;
+                    hc[2] = xc;
+                    float val = silu_f(acc);
+                    if (ci < DK) tl.qs[ci] = val;
+                    else if (ci < 2 * DK) tl.ks[ci - DK] = val;
+                    else tl.vs[(ci - 2 * DK) / DV][(ci - 2 * DK) % DV] = val;
+                }
+                if (tid < G) {
+                    const int hh = kh * G + tid;
+                    const TA *uu = (const TA *)a.u + (long long)n * a.ld_ub;
+                    const TA *bb = (const TA *)a.b_logit + (long long)n * a.ld_ub;
+                    float gg = -expf(a.A_log[hh]) * softplus_f(to_f32(uu[hh]) + a.dt_bias[hh]);
+                    tl.gate_a[tid] = expf(gg);
+                    tl.gate_b[tid] = sigmoid_f(to_f32(bb[hh]));
+                }
+            }
+            __syncthreads();
+            if (slot >= 0) {
+                if (warp < 2) {
+                    float *vec = warp == 0 ? tl.qs : tl.ks;
+                    float ss = 0.f;
+                    for (int i = lane; i < DK; i += 32) ss += vec[i] * vec[i];
+                    ss = warp_sum(ss);
+                    if (lane == 0) tl.scal[warp] = ss;
+                }
+                __syncthreads();
+                const float sq = rsqrtf(tl.scal[0] + d.l2_eps) * d.q_scale;
+                const float sk = rsqrtf(tl.scal[1] + d.l2_eps);
+                for (int i = tid; i < DK; i += NT) {
+                    tl.qs[i] *= sq;
+                    tl.ks[i] *= sk;
+                }
+                __syncthreads();
+                if (warp == 0) {
+                    float kq = 0.f;
+                    for (int i = lane; i < DK; i += 32) kq += tl.ks[i] * tl.qs[i];
+                    kq = warp_sum(kq);
+                    if (lane == 0) tl.scal[2] = kq;
+                }
+            }
+        }
+        const int slot = tl.unit_slot;
+        // ---- this head's state has arrived?
+        const bool ok = tc::mbar_wait(tc::smem_u32(&tl.full[it % NS]), (uint32_t)((it / NS) & 1));
+        if (!ok && tid == 0) set_error(a.err, GDN_DEVERR_TIMEOUT);
+        const float *Ms = slots + (it % NS) * (DK * DV);
+        float4 m[RPT];
+        float kr[RPT], qr[RPT];
+        if (slot >= 0) {
+#pragma unroll
+            for (int x = 0; x < RPT; ++x) {
+                m[x] = *reinterpret_cast<const float4 *>(Ms + (rg + x * RPP) * DV + c4);
+                kr[x] = tl.ks[rg + x * RPP];
+                qr[x] = tl.qs[rg + x * RPP];
+            }
+            float4 pp = make_float4(0.f, 0.f, 0.f, 0.f), ss = pp;
+#pragma unroll
+            for (int x = 0; x < RPT; ++x) {
+                pp.x += m[x].x * kr[x]; pp.y += m[x].y * kr[x]; pp.z += m[x].z * kr[x]; pp.w += m[x].w * kr[x];
+                ss.x += m[x].x * qr[x]; ss.y += m[x].y * qr[x]; ss.z += m[x].z * qr[x]; ss.w += m[x].w * qr[x];
+            }
+            *reinterpret_cast<float4 *>(&tl.red_p[rg][c4]) = pp;
+            *reinterpret_cast<float4 *>(&tl.red_s[rg][c4]) = ss;
+        }
+        __syncthreads();  // (A) every thread holds its part of the slot in registers
+        if (tid == 0 && it + NS < n_items) {
+            tc::fence_async_smem();
+            issue(it + NS);
+        }
+        if (slot < 0) {   // padding lane: zero output row of this head
+            for (int j = tid; j < DV; j += NT) out[out_row + (long long)h * DV + j] = from_f32<TOut>(0.f);
+            __syncthreads();
+            continue;
+        }
+        const float ga = tl.gate_a[gi], gb = tl.gate_b[gi];
+        if (tid < DV) {
+            float p = 0.f, s2 = 0.f;
+#pragma unroll
+            for (int r = 0; r < RPP; ++r) {
+                p += tl.red_p[r][tid];
+                s2 += tl.red_s[r][tid];
+            }
+            float uu = gb * (tl.vs[gi][tid] - ga * p);
+            tl.up[tid] = uu;
+            tl.os[tid] = ga * s2 + uu * tl.scal[2];
+        }
+        __syncthreads();  // (B)
+        {
+            float *Mg = a.state + ((long long)slot * d.hv + h) * DK * DV;
+            const float4 u4 = *reinterpret_cast<const float4 *>(&tl.up[c4]);
+#pragma unroll
+            for (int x = 0; x < RPT; ++x) {
+                float4 mn;
+                mn.x = ga * m[x].x + kr[x] * u4.x;
+                mn.y = ga * m[x].y + kr[x] * u4.y;
+                mn.z = ga * m[x].z + kr[x] * u4.z;
+                mn.w = ga * m[x].w + kr[x] * u4.w;
+                *reinterpret_cast<float4 *>(Mg + (long long)(rg + x * RPP) * DV + c4) = mn;
+            }
+        }
+        float ov = tid < DV ? tl.os[tid] : 0.f;
+        float sq = warp_sum(ov * ov);
+        if (tid < DV && lane == 0) tl.scal[4 + warp] = sq;   // DV/32 <= 4 partials
+        __syncthreads();  // (C)
+        if (tid < DV) {
+            float tot = 0.f;
+            for (int wi = 0; wi < DV / 32; ++wi) tot += tl.scal[4 + wi];
+            float rs = rsqrtf(tot / (float)DV + d.norm_eps);
+            const TA *z = (const TA *)a.z + (long long)n * a.ld_z + (long long)h * DV;
+            out[out_row + (long long)h * DV + tid] =
+                from_f32<TOut>(ov * rs * a.norm_w[tid] * silu_f(to_f32(z[tid])));
+        }
+        __syncthreads();  // (D) smem scratch free for the next item / unit
+    }
+}
+
+template <int DK, int DV, typename TA, typename TOut>
+static cudaError_t launch_stream_t(const DecodeArgs &a, cudaStream_t s) {
+    auto kern = decode_stream_kernel<DK, DV, TA, TOut>;
+    constexpr size_t smem = stream_smem_bytes<DK, DV>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int units = a.n * a.d.hk;
+    const int grid = units < sm_count() ? units : sm_count();
+    kern<<<grid, 4 * DV, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int DK, int DV, typename TA, typename TOut>
 static cudaError_t launch_dec_t(const DecodeArgs &a, bool fused, cudaStream_t s) {
     dim3 grid(a.n * a.d.hk);
     if (fused)
-        decode_kernel<DK, DV, TA, TOut, true><<<grid, 4 * DV, 0, s>>>(a);
+        return launch_stream_t<DK, DV, TA, TOut>(a, s);
     else
         decode_kernel<DK, DV, TA, TOut, false><<<grid, 4 * DV, 0, s>>>(a);
     return cudaGetLastError();

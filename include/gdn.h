@@ -40,9 +40,12 @@
  *    S[j][i] (S is dv x dk; the buffer stores S transposed, so the dk index is
  *    the slow one).  Conv history: act dtype [slots][CH][3], oldest tap first.
  *  - Channels of the raw projection x: [q (HK*dk) | k (HK*dk) | v (HV*dv)],
- *    head-major, CH = 2*HK*dk + HV*dv.  Row strides (ld_*) are in ELEMENTS and
- *    must be multiples of 8 elements (16 bytes for bf16); base pointers must
- *    be 16-byte aligned.
+ *    head-major, CH = 2*HK*dk + HV*dv.  Row strides (ld_*) are in ELEMENTS.
+ *    Wide views (x, z, q, k, v) need 16-byte aligned bases and strides that
+ *    are multiples of 8 elements; the narrow [T][HV] views u and b_logit need
+ *    only element alignment and ld >= HV.
+ *  - The live (non-negative) entries of state_idx must be distinct within a
+ *    call: two sequences writing one slot race.
  *  - Outputs never alias inputs, except state_out == state_in (in place).
  *
  * Errors: every entry point validates its arguments on the host BEFORE any

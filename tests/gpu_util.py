@@ -23,6 +23,11 @@ def rel_max(gpu, ref):
     return float(np.abs(g - r).max() / rms)
 
 
+def report(name, **errs):
+    """Print measured parity errors (visible with pytest -s)."""
+    print("PARITY %-40s %s" % (name, " ".join("%s=%.3e" % kv for kv in errs.items())), flush=True)
+
+
 def dev(t, device="cuda"):
     return None if t is None else t.to(device).contiguous()
 

@@ -60,10 +60,10 @@ def test_null_config(lib):
 
 def test_view_checks(lib):
     c = cfg()
-    # ld smaller than HV, ld not a multiple of 8, misaligned, null
+    # u / b_logit: ld smaller than HV, misaligned, null
     assert lib.gdn_gate_prep(ctypes.byref(c), A16, A16, 16, 1, A16, A16, A16, A16, None) == INVALID
-    assert lib.gdn_gate_prep(ctypes.byref(c), A16, A16, 33, 1, A16, A16, A16, A16, None) == INVALID
-    assert lib.gdn_gate_prep(ctypes.byref(c), MIS, A16, 32, 1, A16, A16, A16, A16, None) == INVALID
+    odd = P(0x100002)      # not even element-aligned for fp32 / 4-byte loads
+    assert lib.gdn_gate_prep(ctypes.byref(c), odd, A16, 32, 1, A16, A16, A16, A16, None) == INVALID
     assert lib.gdn_gate_prep(ctypes.byref(c), None, A16, 32, 1, A16, A16, A16, A16, None) == INVALID
     # T = 0 is a no-op that never touches the GPU
     assert lib.gdn_gate_prep(ctypes.byref(c), None, None, 0, 0, None, None, None, None, None) == OK
@@ -111,6 +111,10 @@ def test_mixer_validation_and_workspace(lib):
     assert lib.gdn_mixer_prefill(ch, ctypes.byref(io), A16, 1024, None) == WORKSPACE
     assert lib.gdn_mixer_prefill(ch, ctypes.byref(io), MIS, need, None) == WORKSPACE
     bad = _io(ld_x=8000)                       # narrower than CH
+    assert lib.gdn_mixer_prefill(ch, ctypes.byref(bad), A16, need, None) == INVALID
+    bad = _io(ld_z=4100)                       # wide view stride not a multiple of 8
+    assert lib.gdn_mixer_prefill(ch, ctypes.byref(bad), A16, need, None) == INVALID
+    bad = _io(x=MIS)                           # wide view base not 16-byte aligned
     assert lib.gdn_mixer_prefill(ch, ctypes.byref(bad), A16, need, None) == INVALID
     bad = _io(cu_seqlens=None)
     assert lib.gdn_mixer_prefill(ch, ctypes.byref(bad), A16, need, None) == INVALID

@@ -10,7 +10,7 @@ import torch
 from gateddeltanet_linear_attention_gb300 import gdn
 from gateddeltanet_linear_attention_gb300.inputs import WORKLOADS, make_inputs
 
-from gpu_util import TOL_BF16, GpuMixer, head_channels, oracle_mixer, rel_max, vcols
+from gpu_util import TOL_BF16, GpuMixer, head_channels, oracle_mixer, rel_max, report, vcols
 
 pytestmark = pytest.mark.gpu
 
@@ -26,9 +26,12 @@ def _cmp(wl, y_gpu, ref, kheads, state_gpu=None, what=""):
     _, vh = head_channels(wl, kheads)
     cols = vcols(wl, vh)
     ey = rel_max(y_gpu[:, torch.as_tensor(cols, device=y_gpu.device)], ref["y"])
-    assert ey <= TOL_BF16, (what, "y", ey)
+    es = None
     if state_gpu is not None:
         es = rel_max(state_gpu[:, torch.as_tensor(vh, device=state_gpu.device)], ref["state"])
+    report(what, y=ey, state=es if es is not None else float("nan"))
+    assert ey <= TOL_BF16, (what, "y", ey)
+    if es is not None:
         assert es <= TOL_BF16, (what, "state", es)
     return ey
 
@@ -91,8 +94,9 @@ def test_decode_64x256():
                            conv_state=cs)
         st, cs = torch.tensor(ref["state"]), torch.tensor(ref["conv_state"])
         worst = max(worst, rel_max(ys[t][:, torch.as_tensor(cols, device="cuda")], ref["y"]))
-    assert worst <= TOL_BF16, ("decode y", worst)
     es = rel_max(m.state[:, torch.as_tensor(vh, device="cuda")], ref["state"])
+    report("decode_64x256", y_worst_step=worst, state=es)
+    assert worst <= TOL_BF16, ("decode y", worst)
     assert es <= TOL_BF16, ("decode state", es)
 
 
@@ -130,6 +134,7 @@ def test_long_64k_then_512_decode_steps():
         st, cs = torch.tensor(r["state"]), torch.tensor(r["conv_state"])
         yd.append(r["y"])
     ey = rel_max(torch.cat(ys)[:, torch.as_tensor(cols, device="cuda")], np.concatenate(yd))
-    assert ey <= TOL_BF16, ("long decode y", ey)
     es = rel_max(m.state[:, torch.as_tensor(vh, device="cuda")], r["state"])
+    report("long_64k decode", y=ey, state=es)
+    assert ey <= TOL_BF16, ("long decode y", ey)
     assert es <= TOL_BF16, ("long final state", es)

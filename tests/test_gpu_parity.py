@@ -15,7 +15,7 @@ from gateddeltanet_linear_attention_gb300 import gdn
 from gateddeltanet_linear_attention_gb300.inputs import WORKLOADS, Workload, make_inputs, shrink
 
 from gpu_util import (TOL_BF16, TOL_FP32, GpuMixer, dev, head_channels, oracle_mixer, rel_max,
-                      vcols)
+                      report, vcols)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,6 +37,7 @@ def _check_prefill(wl, inp, tol, y_dtype=torch.float32, state_idx=None, slot_idx
     assert gdn.gdn_device_error() == 0
     ey = rel_max(y, ref["y"])
     es = rel_max(m.state, ref["state"])
+    report(wl.name + str(inp["seqlens"])[:30], y=ey, state=es)
     assert ey <= tol, ("y", ey)
     assert es <= tol, ("state", es)
     if wl.act == "bf16":
