@@ -351,7 +351,7 @@ def bench_decode(args, dev, gdn, pk, pk_src):
     for t in range(S):
         # evict L2 with a read-only pass (a write flush would leave dirty lines whose
         # write-back the timed kernel would pay for)
-        torch.sum(flush, out=sink)
+        torch.sum(flush, 0, out=sink)
         evs[t][0].record(stream)
         gdn.gdn_mixer_decode(cfg, xs[t], zs[t], us[t], bs[t], cw, A, dt, nw, y, state, conv)
         evs[t][1].record(stream)

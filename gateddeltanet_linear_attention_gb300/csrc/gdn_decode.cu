@@ -221,32 +221,38 @@ __global__ void __launch_bounds__(4 * DV) decode_kernel(DecodeArgs a) {
 // states (dk*dv*4 bytes each) flow HBM -> shared memory through a ring of NS
 // slots filled by bulk asynchronous copies (cp.async.bulk, completion counted
 // on one mbarrier per slot), so that while one head is being updated the next
-// NS-1 are already in flight.  The arithmetic per head is the same as
-// decode_kernel's; the new state goes straight from registers to HBM.
+// NS-1 are already in flight.  The small per-unit inputs (conv step of the
+// unit's q/k/v channels, SiLU, L2, gates, and the z rows of the norm) are
+// computed for a batch of HB heads at once, so their global loads overlap
+// each other and the state copies instead of sitting on every head's critical
+// path; per head only shared memory is touched before the state write.
 template <int DK, int DV>
 struct StreamCfg {
     static constexpr int NT = 4 * DV;
     static constexpr int LPR = DV / 4, RPP = NT / LPR, RPT = DK / RPP;
     static constexpr int SLOT = DK * DV * 4;                        // bytes of one head state
     static constexpr int NS = SLOT >= 65536 ? 3 : (SLOT >= 16384 ? 8 : 16);
-    static constexpr int MAXG = 4;
     static constexpr int CHUNK = SLOT < 16384 ? SLOT : 16384;       // bytes per bulk copy
+    static constexpr int HB = 4;                                    // heads per prologue batch
 };
 
 // Every array read or written as float4 is 16-byte aligned explicitly.
 template <int DK, int DV>
 struct StreamTail {
+    static constexpr int HB = StreamCfg<DK, DV>::HB;
     alignas(16) uint64_t full[StreamCfg<DK, DV>::NS];
-    alignas(16) float qs[DK];
-    alignas(16) float ks[DK];
-    alignas(16) float vs[StreamCfg<DK, DV>::MAXG][DV];
+    alignas(16) float qk[HB][2][DK];      // normalised q (0) and k (1) per unit of the batch
+    alignas(16) float vs[HB][DV];         // conv'd v per head of the batch
+    alignas(16) float zs[HB][DV];         // SiLU(z) per head of the batch
     alignas(16) float red_p[StreamCfg<DK, DV>::RPP][DV];
     alignas(16) float red_s[StreamCfg<DK, DV>::RPP][DV];
     alignas(16) float up[DV];
-    alignas(16) float os[DV];
-    float gate_a[StreamCfg<DK, DV>::MAXG], gate_b[StreamCfg<DK, DV>::MAXG];
-    float scal[8];
-    int unit_slot;
+    alignas(16) float nw[DV];
+    float gate_a[HB], gate_b[HB];
+    float ssq[HB][2];                     // |q|^2, |k|^2 per unit
+    float kq[HB];
+    float npart[4];
+    int uslot[HB];
 };
 
 template <int DK, int DV>
@@ -254,17 +260,22 @@ constexpr size_t stream_smem_bytes() {
     return (size_t)StreamCfg<DK, DV>::NS * StreamCfg<DK, DV>::SLOT + sizeof(StreamTail<DK, DV>);
 }
 
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
 template <int DK, int DV, typename TA, typename TOut>
 __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) {
     using Cfg = StreamCfg<DK, DV>;
     constexpr int NT = Cfg::NT, LPR = Cfg::LPR, RPP = Cfg::RPP, RPT = Cfg::RPT, NS = Cfg::NS;
+    constexpr int HB = Cfg::HB;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float *slots = reinterpret_cast<float *>(smem_raw);
     StreamTail<DK, DV> &tl = *reinterpret_cast<StreamTail<DK, DV> *>(smem_raw + NS * Cfg::SLOT);
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int G = d.grp;
+    const int G = d.grp;                 // 1, 2 or 4: HB % G == 0
     const int n_units = a.n * d.hk;
     if ((int)blockIdx.x >= n_units) return;
     const int my_units = (n_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -276,6 +287,7 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
         for (int s = 0; s < NS; ++s) tc::mbar_init(tc::smem_u32(&tl.full[s]), 1);
         tc::mbar_fence_init();
     }
+    for (int j = tid; j < DV; j += NT) tl.nw[j] = a.norm_w[j];
     __syncthreads();
 
     // producer (thread 0): bulk-load item `it`'s head state into slot it % NS
@@ -297,85 +309,116 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
     if (tid == 0)
         for (int it = 0; it < NS && it < n_items; ++it) issue(it);
 
+    bool timed_out = false;
     for (int it = 0; it < n_items; ++it) {
-        const int gi = it % G;
-        const int u = (int)blockIdx.x + (it / G) * (int)gridDim.x;
-        const int n = u / d.hk, kh = u % d.hk;
-        const int h = kh * G + gi;
-        const long long out_row = (long long)n * d.hv * DV;
-        if (gi == 0) {
-            // ---- unit prologue: conv step of this unit's q/k/v channels, SiLU, L2, gates
-            const int slot = slot_of(a.state_idx, n, d.n_slots, a.err);
-            if (tid == 0) tl.unit_slot = slot;
-            if (slot >= 0) {
+        const int hb = it % HB;
+        if (hb == 0) {
+            // ---- batch prologue for heads it .. it+HB-1 (units it/G .. (it+HB-1)/G)
+            __syncthreads();   // the previous batch's inputs are no longer read
+            const int ub0 = it / G, nub = HB / G;
+            const int nch = 2 * DK + G * DV;
+            for (int idx = tid; idx < nub * nch; idx += NT) {
+                const int ub = idx / nch, ci = idx % nch;
+                const int uu = ub0 + ub;
+                if (uu >= my_units) continue;
+                const int u = (int)blockIdx.x + uu * (int)gridDim.x;
+                const int n = u / d.hk, kh = u % d.hk;
+                const int slot = a.state_idx ? a.state_idx[n] : n;
+                if (slot < 0 || slot >= d.n_slots) continue;
+                int c;
+                if (ci < DK) c = kh * DK + ci;
+                else if (ci < 2 * DK) c = d.hk * DK + kh * DK + (ci - DK);
+                else c = 2 * d.hk * DK + kh * G * DV + (ci - 2 * DK);
                 const TA *x = (const TA *)a.x + (long long)n * a.ld_x;
                 const TA *w = (const TA *)a.conv_w;
-                TA *cs = (TA *)a.conv_state + (long long)slot * d.ch * 3;
-                const int nch = 2 * DK + G * DV;
-                for (int ci = tid; ci < nch; ci += NT) {
-                    int c;
-                    if (ci < DK) c = kh * DK + ci;
-                    else if (ci < 2 * DK) c = d.hk * DK + kh * DK + (ci - DK);
-                    else c = 2 * d.hk * DK + kh * G * DV + (ci - 2 * DK);
-                    TA *hc = cs + (long long)c * 3;
-                    TA h0 = hc[0], h1 = hc[1], h2 = hc[2], xc = x[c];
-                    float acc = to_f32(w[c * 4 + 0]) * to_f32(h0) + to_f32(w[c * 4 + 1]) * to_f32(h1) +
-                                to_f32(w[c * 4 + 2]) * to_f32(h2) + to_f32(w[c * 4 + 3]) * to_f32(xc);
-                    hc[0] = h1;
-                    hc[1] = h2;
-                    hc[2] = xc;
-                    float val = silu_f(acc);
-                    if (ci < DK) tl.qs[ci] = val;
-                    else if (ci < 2 * DK) tl.ks[ci - DK] = val;
-                    else tl.vs[(ci - 2 * DK) / DV][(ci - 2 * DK) % DV] = val;
+                TA *hc = (TA *)a.conv_state + ((long long)slot * d.ch + c) * 3;
+                TA h0 = hc[0], h1 = hc[1], h2 = hc[2], xc = x[c];
+                float acc = to_f32(w[c * 4 + 0]) * to_f32(h0) + to_f32(w[c * 4 + 1]) * to_f32(h1) +
+                            to_f32(w[c * 4 + 2]) * to_f32(h2) + to_f32(w[c * 4 + 3]) * to_f32(xc);
+                hc[0] = h1;
+                hc[1] = h2;
+                hc[2] = xc;
+                const float val = silu_f(acc);
+                if (ci < 2 * DK) tl.qk[ub][ci / DK][ci % DK] = val;
+                else tl.vs[ub * G + (ci - 2 * DK) / DV][(ci - 2 * DK) % DV] = val;
+            }
+            for (int idx = tid; idx < HB * DV; idx += NT) {   // SiLU(z) of the batch's heads
+                const int hbi = idx / DV, j = idx % DV;
+                const int uu = ub0 + hbi / G;
+                if (uu >= my_units) continue;
+                const int u = (int)blockIdx.x + uu * (int)gridDim.x;
+                const int n = u / d.hk, h = (u % d.hk) * G + hbi % G;
+                const TA *z = (const TA *)a.z + (long long)n * a.ld_z + (long long)h * DV;
+                tl.zs[hbi][j] = silu_f(to_f32(z[j]));
+            }
+            if (tid < HB) {
+                const int uu = ub0 + tid / G;
+                float ga = 0.f, gb = 0.f;
+                if (uu < my_units) {
+                    const int u = (int)blockIdx.x + uu * (int)gridDim.x;
+                    const int n = u / d.hk, h = (u % d.hk) * G + tid % G;
+                    const TA *uv = (const TA *)a.u + (long long)n * a.ld_ub;
+                    const TA *bv = (const TA *)a.b_logit + (long long)n * a.ld_ub;
+                    const float gg = -expf(a.A_log[h]) * softplus_f(to_f32(uv[h]) + a.dt_bias[h]);
+                    ga = expf(gg);
+                    gb = sigmoid_f(to_f32(bv[h]));
                 }
-                if (tid < G) {
-                    const int hh = kh * G + tid;
-                    const TA *uu = (const TA *)a.u + (long long)n * a.ld_ub;
-                    const TA *bb = (const TA *)a.b_logit + (long long)n * a.ld_ub;
-                    float gg = -expf(a.A_log[hh]) * softplus_f(to_f32(uu[hh]) + a.dt_bias[hh]);
-                    tl.gate_a[tid] = expf(gg);
-                    tl.gate_b[tid] = sigmoid_f(to_f32(bb[hh]));
+                tl.gate_a[tid] = ga;
+                tl.gate_b[tid] = gb;
+            }
+            if (tid < nub) {
+                const int uu = ub0 + tid;
+                int slot = -1;
+                if (uu < my_units) {
+                    const int u = (int)blockIdx.x + uu * (int)gridDim.x;
+                    slot = slot_of(a.state_idx, u / d.hk, d.n_slots, a.err);
                 }
+                tl.uslot[tid] = slot;
             }
             __syncthreads();
-            if (slot >= 0) {
-                if (warp < 2) {
-                    float *vec = warp == 0 ? tl.qs : tl.ks;
-                    float ss = 0.f;
-                    for (int i = lane; i < DK; i += 32) ss += vec[i] * vec[i];
-                    ss = warp_sum(ss);
-                    if (lane == 0) tl.scal[warp] = ss;
-                }
-                __syncthreads();
-                const float sq = rsqrtf(tl.scal[0] + d.l2_eps) * d.q_scale;
-                const float sk = rsqrtf(tl.scal[1] + d.l2_eps);
-                for (int i = tid; i < DK; i += NT) {
-                    tl.qs[i] *= sq;
-                    tl.ks[i] *= sk;
-                }
-                __syncthreads();
-                if (warp == 0) {
-                    float kq = 0.f;
-                    for (int i = lane; i < DK; i += 32) kq += tl.ks[i] * tl.qs[i];
-                    kq = warp_sum(kq);
-                    if (lane == 0) tl.scal[2] = kq;
-                }
+            if (warp < 2 * nub) {    // |q|^2 and |k|^2 of each unit, one warp per vector
+                const float *vec = tl.qk[warp >> 1][warp & 1];
+                float ss = 0.f;
+                for (int i = lane; i < DK; i += 32) ss += vec[i] * vec[i];
+                ss = warp_sum(ss);
+                if (lane == 0) tl.ssq[warp >> 1][warp & 1] = ss;
             }
+            __syncthreads();
+            for (int idx = tid; idx < nub * 2 * DK; idx += NT) {
+                const int ub = idx / (2 * DK), part = (idx / DK) & 1, i = idx % DK;
+                float f = rsqrtf(tl.ssq[ub][part] + d.l2_eps);
+                if (part == 0) f *= d.q_scale;
+                tl.qk[ub][part][i] *= f;
+            }
+            __syncthreads();
+            if (warp < nub) {
+                float kq = 0.f;
+                for (int i = lane; i < DK; i += 32) kq += tl.qk[warp][0][i] * tl.qk[warp][1][i];
+                kq = warp_sum(kq);
+                if (lane == 0) tl.kq[warp] = kq;
+            }
+            __syncthreads();
         }
-        const int slot = tl.unit_slot;
+        const int ub = hb / G, gi = it % G;
+        const int u = (int)blockIdx.x + (it / G) * (int)gridDim.x;
+        const int n = u / d.hk, kh = u % d.hk, h = kh * G + gi;
+        const long long out_row = (long long)n * d.hv * DV;
+        const int slot = tl.uslot[ub];
         // ---- this head's state has arrived?
-        const bool ok = tc::mbar_wait(tc::smem_u32(&tl.full[it % NS]), (uint32_t)((it / NS) & 1));
-        if (!ok && tid == 0) set_error(a.err, GDN_DEVERR_TIMEOUT);
+        if (!timed_out && !tc::mbar_wait(tc::smem_u32(&tl.full[it % NS]), (uint32_t)((it / NS) & 1))) {
+            timed_out = true;
+            set_error(a.err, GDN_DEVERR_TIMEOUT);
+        }
         const float *Ms = slots + (it % NS) * (DK * DV);
         float4 m[RPT];
-        float kr[RPT], qr[RPT];
+        float kr[RPT];
         if (slot >= 0) {
+            float qr[RPT];
 #pragma unroll
             for (int x = 0; x < RPT; ++x) {
                 m[x] = *reinterpret_cast<const float4 *>(Ms + (rg + x * RPP) * DV + c4);
-                kr[x] = tl.ks[rg + x * RPP];
-                qr[x] = tl.qs[rg + x * RPP];
+                kr[x] = tl.qk[ub][1][rg + x * RPP];
+                qr[x] = tl.qk[ub][0][rg + x * RPP];
             }
             float4 pp = make_float4(0.f, 0.f, 0.f, 0.f), ss = pp;
 #pragma unroll
@@ -393,10 +436,10 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
         }
         if (slot < 0) {   // padding lane: zero output row of this head
             for (int j = tid; j < DV; j += NT) out[out_row + (long long)h * DV + j] = from_f32<TOut>(0.f);
-            __syncthreads();
             continue;
         }
-        const float ga = tl.gate_a[gi], gb = tl.gate_b[gi];
+        const float ga = tl.gate_a[hb], gb = tl.gate_b[hb];
+        float ov = 0.f;
         if (tid < DV) {
             float p = 0.f, s2 = 0.f;
 #pragma unroll
@@ -404,9 +447,9 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
                 p += tl.red_p[r][tid];
                 s2 += tl.red_s[r][tid];
             }
-            float uu = gb * (tl.vs[gi][tid] - ga * p);
+            const float uu = gb * (tl.vs[hb][tid] - ga * p);
             tl.up[tid] = uu;
-            tl.os[tid] = ga * s2 + uu * tl.scal[2];
+            ov = ga * s2 + uu * tl.kq[ub];
         }
         __syncthreads();  // (B)
         {
@@ -422,19 +465,16 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
                 *reinterpret_cast<float4 *>(Mg + (long long)(rg + x * RPP) * DV + c4) = mn;
             }
         }
-        float ov = tid < DV ? tl.os[tid] : 0.f;
-        float sq = warp_sum(ov * ov);
-        if (tid < DV && lane == 0) tl.scal[4 + warp] = sq;   // DV/32 <= 4 partials
-        __syncthreads();  // (C)
-        if (tid < DV) {
+        if (tid < DV) {   // gated RMSNorm of this head's o, among the DV threads that hold it
+            const float sq = warp_sum(ov * ov);
+            if (lane == 0) tl.npart[warp] = sq;
+            named_bar(1, DV);
             float tot = 0.f;
-            for (int wi = 0; wi < DV / 32; ++wi) tot += tl.scal[4 + wi];
-            float rs = rsqrtf(tot / (float)DV + d.norm_eps);
-            const TA *z = (const TA *)a.z + (long long)n * a.ld_z + (long long)h * DV;
-            out[out_row + (long long)h * DV + tid] =
-                from_f32<TOut>(ov * rs * a.norm_w[tid] * silu_f(to_f32(z[tid])));
+#pragma unroll
+            for (int wi = 0; wi < DV / 32; ++wi) tot += tl.npart[wi];
+            const float rs = rsqrtf(tot / (float)DV + d.norm_eps);
+            out[out_row + (long long)h * DV + tid] = from_f32<TOut>(ov * rs * tl.nw[tid] * tl.zs[hb][tid]);
         }
-        __syncthreads();  // (D) smem scratch free for the next item / unit
     }
 }
 
