@@ -223,7 +223,7 @@ gdn_status gdn_chunk_prefill(const gdn_config *cfg, const void *q, const void *k
         return GDN_ERR_INVALID_ARG;
     if (n_seqs > kMaxSeqs) return GDN_ERR_UNSUPPORTED;
     if (n_seqs == 0) return T == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
-    if (!cu_seqlens || !g || !beta || !o) return GDN_ERR_INVALID_ARG;
+    if (!cu_seqlens || !g || !beta || !o || !aligned16(o)) return GDN_ERR_INVALID_ARG;
     if (T > 0 && (!valid_view(q, ld_qk, (long long)d.hk * d.dk) ||
                   !valid_view(k, ld_qk, (long long)d.hk * d.dk) ||
                   !valid_view(v, ld_v, (long long)d.hv * d.dv)))

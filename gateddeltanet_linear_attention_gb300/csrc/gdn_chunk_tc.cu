@@ -23,13 +23,17 @@
 // DVS state columns); the columns of M evolve independently, so slices only
 // duplicate the dv-independent products.  Per chunk, five MMA groups, all
 // M = 128 (64-row problems are stacked or padded):
-//   G1  D1 = [K ; Q] (128 x 128) . K^T            -> K K^T (lanes 0-63), Q K^T (64-127)
-//   G2  D2 = [T ; P] (128 x 64)  . [bgK | bV]^T   -> W (cols 0-127), U (cols 128..) on lanes 0-63
-//   G3  D3 = [W ; gQ] (128x128)  . M              -> W M (lanes 0-63), gamma Q M (64-127)
-//   G4  D3 += [T ; P] (128 x 64) . U'             -> lanes 64-127 become O
-//   G5  D5 = K~^T (128 x 64) . U'                 -> the state increment
-// The triangular inverse T is formed on the SIMT pipes (four 16x16 diagonal
-// blocks by forward substitution in registers, then block rows).
+//   G1  D1 = [K ; Q] . K^T               -> K K^T (TMEM lanes 0-63), Q K^T (64-127)
+//   G2  D2 = [T ; P] . [bgK | bV]        -> W (cols 0-127) | U on lanes 0-63
+//   G3  D3 = [W ; gQ] . M                -> W M (lanes 0-63), gamma Q M (64-127)
+//   G4  D3 += [T ; P] . U'               -> lanes 64-127 become O
+//   G5  D5 = K~^T . U'                   -> the state increment
+// Operands whose contraction index is the token or the dk row (bgK|bV, K~,
+// M, U') are stored MN-major, so that every operand is written from its
+// natural row layout with 16-byte stores.  The triangular inverse T is formed
+// in fp32 on the SIMT pipes (four 16x16 diagonal blocks by forward
+// substitution in registers, then block rows), with T kept transposed in the
+// unused upper triangle of A.
 #include "gdn_common.cuh"
 #include "tc_sm103.cuh"
 
@@ -41,69 +45,151 @@ constexpr int TC_NT = 256;
 constexpr int TC_C = 64;     // chunk
 constexpr int TC_DK = 128;   // dk == dv
 
-// Shared-memory map (bytes).  Every tile has a hi and a lo part.
+// Shared-memory map (bytes).  Every bf16 tile has a hi part and a lo part.
 template <int DVS>
 struct TcSmem {
-    static constexpr int A1 = 128 * 128 * 2;               // [K;Q] -> [W;gQ], K = 128
-    static constexpr int B2 = (128 + DVS) * 64 * 2;        // [bgK | bV]^T -> K~^T (rows 0-127), K = 64
-    static constexpr int A3 = 128 * 64 * 2;                // [T ; P], K = 64
-    static constexpr int B3 = DVS * 128 * 2;               // M^T, K = 128
-    static constexpr int B4 = DVS * 64 * 2;                // U'^T, K = 64
-    static constexpr int OFF_A1 = 0;                        // hi at +0, lo at +A1
-    static constexpr int OFF_B2 = OFF_A1 + 2 * A1;
-    static constexpr int OFF_A3 = OFF_B2 + 2 * B2;
-    static constexpr int OFF_B3 = OFF_A3 + 2 * A3;
-    static constexpr int OFF_B4 = OFF_B3 + 2 * B3;
-    static constexpr int OFF_SA = OFF_B4 + 2 * B4;          // fp32 A [64][65] for the solve
-    static constexpr int OFF_X = OFF_SA + 64 * 65 * 4;      // fp32 scratch 3 x 16 x 17
+    static constexpr int NB = 128 + DVS;                   // N of G2's B operand
+    static constexpr int KQ = 128 * 128 * 2;               // [K;Q] -> [W;gQ], K-major, K = 128
+    static constexpr int BW = NB * 64 * 2;                 // [bgK|bV] MN-major (MN = NB, K = 64) -> K~ (MN = 128)
+    static constexpr int TP = 128 * 64 * 2;                // [T ; P], K-major, K = 64
+    static constexpr int MT = DVS * 128 * 2;               // M, MN-major (MN = DVS, K = 128)
+    static constexpr int UT = DVS * 64 * 2;                // U', MN-major (MN = DVS, K = 64)
+    static constexpr int OFF_KQ = 0;
+    static constexpr int OFF_BW = OFF_KQ + 2 * KQ;
+    static constexpr int OFF_TP = OFF_BW + 2 * BW;
+    static constexpr int OFF_MT = OFF_TP + 2 * TP;
+    static constexpr int OFF_UT = OFF_MT + 2 * MT;
+    static constexpr int OFF_SA = OFF_UT + 2 * UT;          // fp32 [64][65]: A below, T^T above the diagonal
+    static constexpr int OFF_X = OFF_SA + 64 * 65 * 4;      // fp32 [3][16][17]
     static constexpr int OFF_G = OFF_X + 3 * 16 * 17 * 4;   // G[64], beta[64]
     static constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;      // mbarrier, tmem base, timeout flag
     static constexpr int BYTES = OFF_BAR + 16;
 };
 
-__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
-    hi = __float2bfloat16_rn(v);
-    lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-}
-
-// Store 8 consecutive-k values of row r (k0 % 8 == 0) of a K-major tile as
-// one 16-byte hi store and one 16-byte lo store.
-__device__ __forceinline__ void put8(unsigned char *hi_tile, unsigned char *lo_tile, int Kdim, int r,
-                                     int k0, const float *v) {
-    __align__(16) __nv_bfloat16 h[8], l[8];
+// Store 8 values at byte offset `off` (16-byte aligned) of a hi and a lo tile
+// (packed two-at-a-time conversions).
+__device__ __forceinline__ void put8(unsigned char *hi, unsigned char *lo, uint32_t off, const float *v) {
+    __nv_bfloat162 h2[4], l2[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) split_bf16(v[i], h[i], l[i]);
-    const uint32_t off = tc::kmaj_off(r, k0, Kdim);
-    *reinterpret_cast<uint4 *>(hi_tile + off) = *reinterpret_cast<const uint4 *>(h);
-    *reinterpret_cast<uint4 *>(lo_tile + off) = *reinterpret_cast<const uint4 *>(l);
+    for (int i = 0; i < 4; ++i) {
+        h2[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        const float2 hf = __bfloat1622float2(h2[i]);
+        l2[i] = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+    }
+    *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<const uint4 *>(h2);
+    *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<const uint4 *>(l2);
 }
 
-__device__ __forceinline__ void put1(unsigned char *hi_tile, unsigned char *lo_tile, int Kdim, int r,
-                                     int k, float v) {
-    __nv_bfloat16 h, l;
-    split_bf16(v, h, l);
-    const uint32_t off = tc::kmaj_off(r, k, Kdim);
-    *reinterpret_cast<__nv_bfloat16 *>(hi_tile + off) = h;
-    *reinterpret_cast<__nv_bfloat16 *>(lo_tile + off) = l;
+// Read back 8 values (hi + lo) at a 16-byte aligned offset of a hi and a lo tile.
+__device__ __forceinline__ void get8(const unsigned char *hi, const unsigned char *lo, uint32_t off, float *v) {
+    const uint4 hv = *reinterpret_cast<const uint4 *>(hi + off);
+    const uint4 lv = *reinterpret_cast<const uint4 *>(lo + off);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&hv);
+    const __nv_bfloat162 *l = reinterpret_cast<const __nv_bfloat162 *>(&lv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 a = __bfloat1622float2(h[i]), b = __bfloat1622float2(l[i]);
+        v[2 * i] = a.x + b.x;
+        v[2 * i + 1] = a.y + b.y;
+    }
 }
 
-__device__ __forceinline__ float get1(const unsigned char *hi_tile, const unsigned char *lo_tile,
-                                      int Kdim, int r, int k) {
-    const uint32_t off = tc::kmaj_off(r, k, Kdim);
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(hi_tile + off)) +
-           __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(lo_tile + off));
+// Load n (multiple of 8) consecutive elements as fp32 with 16-byte loads.
+template <int n>
+__device__ __forceinline__ void load_row(const float *p, float *out) {
+#pragma unroll
+    for (int i = 0; i < n; i += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(p + i);
+        out[i] = v.x; out[i + 1] = v.y; out[i + 2] = v.z; out[i + 3] = v.w;
+    }
+}
+template <int n>
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float *out) {
+#pragma unroll
+    for (int i = 0; i < n; i += 8) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p + i);
+        const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) out[i + j] = __bfloat162float(b[j]);
+    }
 }
 
-// Issue D (+)= A . B^T over Kdim in 16-wide steps with the three split
-// products.  A: 128 rows, B: N rows, both K-major hi/lo pairs.
-__device__ __forceinline__ void mma3(uint32_t d_tmem, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi,
-                                     uint32_t b_lo, int Kdim, uint32_t idesc, bool accumulate) {
+template <int n>
+__device__ __forceinline__ void store_row(float *p, const float *v) {
+#pragma unroll
+    for (int i = 0; i < n; i += 4) *reinterpret_cast<float4 *>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+template <int n>
+__device__ __forceinline__ void store_row(__nv_bfloat16 *p, const float *v) {
+#pragma unroll
+    for (int i = 0; i < n; i += 8) {
+        __align__(16) __nv_bfloat16 b[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) b[j] = __float2bfloat16_rn(v[i + j]);
+        *reinterpret_cast<uint4 *>(p + i) = *reinterpret_cast<const uint4 *>(b);
+    }
+}
+
+template <int n>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float *v) {
+    if constexpr (n == 32) {
+        float t[32];
+        tc::tmem_ld32(taddr, t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = t[i];
+    } else {
+        static_assert(n == 16, "16 or 32 columns");
+        float t[16];
+        tc::tmem_ld16(taddr, t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = t[i];
+    }
+}
+
+// Issue D (+)= A . B over Kdim in 16-wide steps with the three split
+// products.  A_MN / B_MN select MN-major operands (with their MN extent).
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void mma3(uint32_t d_tmem, uint32_t a_hi, uint32_t a_lo, uint32_t a_mn,
+                                     uint32_t b_hi, uint32_t b_lo, uint32_t b_mn, int Kdim,
+                                     uint32_t idesc, bool accumulate) {
     for (int k0 = 0; k0 < Kdim; k0 += 16) {
-        const uint64_t ah = tc::kmaj_desc(a_hi, Kdim, k0), al = tc::kmaj_desc(a_lo, Kdim, k0);
-        const uint64_t bh = tc::kmaj_desc(b_hi, Kdim, k0), bl = tc::kmaj_desc(b_lo, Kdim, k0);
+        const uint64_t ah = A_MN ? tc::mnmaj_desc(a_hi, a_mn, k0) : tc::kmaj_desc(a_hi, Kdim, k0);
+        const uint64_t al = A_MN ? tc::mnmaj_desc(a_lo, a_mn, k0) : tc::kmaj_desc(a_lo, Kdim, k0);
+        const uint64_t bh = B_MN ? tc::mnmaj_desc(b_hi, b_mn, k0) : tc::kmaj_desc(b_hi, Kdim, k0);
+        const uint64_t bl = B_MN ? tc::mnmaj_desc(b_lo, b_mn, k0) : tc::kmaj_desc(b_lo, Kdim, k0);
         tc::mma_bf16(d_tmem, ah, bh, idesc, (accumulate || k0 > 0) ? 1u : 0u);
         tc::mma_bf16(d_tmem, ah, bl, idesc, 1u);
         tc::mma_bf16(d_tmem, al, bh, idesc, 1u);
+    }
+}
+
+// One block of the triangular inverse, for the block column held by a warp:
+// rows of block bi = bj + DB, column m of T, from the rows already in tcol.
+template <int DB>
+__device__ __forceinline__ void solve_block_col(float *sA, float (&tcol)[48], int bj, int m, int rh) {
+    // Blocks past the last row block are computed on clamped (valid) addresses
+    // and not stored, so that the warp's code has no data-dependent branches.
+    const bool live = bj + DB < 4;
+    const int bi = live ? bj + DB : 3;
+    float xr[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const float *arow = sA + (bi * 16 + r) * 65 + bj * 16;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16 * DB; ++k) acc = fmaf(arow[k], tcol[k], acc);
+        xr[r] = acc;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        float acc = xr[r];
+#pragma unroll
+        for (int mm = 0; mm < r; ++mm) acc = fmaf(sA[(bi * 16 + mm) * 65 + bi * 16 + r], xr[mm], acc);
+        tcol[16 * DB + r] = -acc;
+    }
+    if (live) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) sA[m * 65 + bi * 16 + rh * 8 + r] = tcol[16 * DB + rh * 8 + r];
     }
 }
 
@@ -113,12 +199,14 @@ template <int DVS, typename TIn, typename TOut>
 __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
     using L = TcSmem<DVS>;
     constexpr int HALF = DVS / 2;                 // state columns per thread in lane mapping
+    constexpr int VQ = DVS / 4;                   // v columns per thread in row mapping
+    constexpr int NB = L::NB;
     extern __shared__ __align__(1024) unsigned char sm[];
-    unsigned char *a1h = sm + L::OFF_A1, *a1l = a1h + L::A1;
-    unsigned char *b2h = sm + L::OFF_B2, *b2l = b2h + L::B2;
-    unsigned char *a3h = sm + L::OFF_A3, *a3l = a3h + L::A3;
-    unsigned char *b3h = sm + L::OFF_B3, *b3l = b3h + L::B3;
-    unsigned char *b4h = sm + L::OFF_B4, *b4l = b4h + L::B4;
+    unsigned char *kqh = sm + L::OFF_KQ, *kql = kqh + L::KQ;
+    unsigned char *bwh = sm + L::OFF_BW, *bwl = bwh + L::BW;
+    unsigned char *tph = sm + L::OFF_TP, *tpl = tph + L::TP;
+    unsigned char *mth = sm + L::OFF_MT, *mtl = mth + L::MT;
+    unsigned char *uth = sm + L::OFF_UT, *utl = uth + L::UT;
     float *sA = reinterpret_cast<float *>(sm + L::OFF_SA);     // [64][65]
     float *sX = reinterpret_cast<float *>(sm + L::OFF_X);      // [3][16][17]
     float *sG = reinterpret_cast<float *>(sm + L::OFF_G);      // [64]
@@ -132,7 +220,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int kh = h / d.grp;
     const int col0 = h * TC_DK + slice * DVS;      // this slice's first column in o / v / state
-    // row mapping (staging): row r, column quarter cq
+    // row mapping (staging): row rr, column quarter cq
     const int rr = tid >> 2, cq = tid & 3;
     // lane mapping (TMEM epilogues): TMEM lane quarter qd, column half hf
     const int qd = warp & 3, hf = warp >> 2;
@@ -178,49 +266,57 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
         tc::fence_after_sync();
         return ok;
     };
+    auto sync_for_mma = [&]() {   // generic smem writes -> visible to the tensor core
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    };
 
     constexpr uint32_t ID_G1 = tc::idesc_bf16(128, 64);
-    constexpr uint32_t ID_G2 = tc::idesc_bf16(128, 128 + DVS);
-    constexpr uint32_t ID_S = tc::idesc_bf16(128, DVS);
-    const uint32_t sa1h = tc::smem_u32(a1h), sa1l = tc::smem_u32(a1l);
-    const uint32_t sb2h = tc::smem_u32(b2h), sb2l = tc::smem_u32(b2l);
-    const uint32_t sa3h = tc::smem_u32(a3h), sa3l = tc::smem_u32(a3l);
-    const uint32_t sb3h = tc::smem_u32(b3h), sb3l = tc::smem_u32(b3l);
-    const uint32_t sb4h = tc::smem_u32(b4h), sb4l = tc::smem_u32(b4l);
+    constexpr uint32_t ID_G2 = tc::idesc_bf16(128, NB) | tc::kTransB;
+    constexpr uint32_t ID_G34 = tc::idesc_bf16(128, DVS) | tc::kTransB;
+    constexpr uint32_t ID_G5 = tc::idesc_bf16(128, DVS) | tc::kTransA | tc::kTransB;
+    const uint32_t s_kqh = tc::smem_u32(kqh), s_kql = tc::smem_u32(kql);
+    const uint32_t s_bwh = tc::smem_u32(bwh), s_bwl = tc::smem_u32(bwl);
+    const uint32_t s_tph = tc::smem_u32(tph), s_tpl = tc::smem_u32(tpl);
+    const uint32_t s_mth = tc::smem_u32(mth), s_mtl = tc::smem_u32(mtl);
+    const uint32_t s_uth = tc::smem_u32(uth), s_utl = tc::smem_u32(utl);
 
     // ---- initial state: thread (lane tl = dk row, half hf) holds M[tl][hf*HALF ..]
     float Mr[HALF];
     {
-        const float *sin = (a.state_in && slot >= 0)
-                               ? a.state_in + ((long long)slot * d.hv + h) * TC_DK * TC_DK +
-                                     (long long)tl * TC_DK + slice * DVS + hf * HALF
-                               : nullptr;
+        if (a.state_in && slot >= 0) {
+            const float *sin = a.state_in + ((long long)slot * d.hv + h) * TC_DK * TC_DK +
+                               (long long)tl * TC_DK + slice * DVS + hf * HALF;
+            load_row<HALF>(sin, Mr);
+        } else {
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) Mr[j] = sin ? sin[j] : 0.f;
+            for (int j = 0; j < HALF; ++j) Mr[j] = 0.f;
+        }
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) put1(b3h, b3l, 128, hf * HALF + j, tl, Mr[j]);
+        for (int j8 = 0; j8 < HALF; j8 += 8) put8(mth, mtl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &Mr[j8]);
     }
 
-    const TIn *qg = (const TIn *)a.q + (long long)kh * TC_DK;
-    const TIn *kg = (const TIn *)a.k + (long long)kh * TC_DK;
-    const TIn *vg = (const TIn *)a.v + col0;
+    const TIn *qg = (const TIn *)a.q + (long long)kh * TC_DK + cq * 32;
+    const TIn *kg = (const TIn *)a.k + (long long)kh * TC_DK + cq * 32;
+    const TIn *vg = (const TIn *)a.v + col0 + cq * VQ;
     const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
-    constexpr int VQ = DVS / 4;   // v columns per thread in row mapping
 
     for (long long c0 = s; c0 < e; c0 += TC_C) {
         const int Lc = (int)((e - c0) < TC_C ? (e - c0) : TC_C);
         // ---------------- S0: stage row rr (32 columns of q and k, VQ of v), gates
         float kv[32], qv[32], vv[VQ];
-        const bool live = rr < Lc;
-        {
+        if (rr < Lc) {
             const long long t = c0 + rr;
+            load_row<32>(kg + t * a.ld_qk, kv);
+            load_row<32>(qg + t * a.ld_qk, qv);
+            load_row<VQ>(vg + t * a.ld_v, vv);
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                kv[i] = live ? to_f32(kg[t * a.ld_qk + cq * 32 + i]) : 0.f;
-                qv[i] = live ? to_f32(qg[t * a.ld_qk + cq * 32 + i]) : 0.f;
-            }
+            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
 #pragma unroll
-            for (int i = 0; i < VQ; ++i) vv[i] = live ? to_f32(vg[t * a.ld_v + cq * VQ + i]) : 0.f;
+            for (int i = 0; i < VQ; ++i) vv[i] = 0.f;
         }
         if (tid < TC_C) {
             const bool lv = tid < Lc;
@@ -247,74 +343,76 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
         }
         __syncthreads();
         if (warp == 0) {  // inclusive scan of g over 64 rows (2 per lane); padded rows add 0
-            float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
-            float pair = g0 + g1, inc = pair;
+            const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
+            const float pair = g0 + g1;
+            float inc = pair;
 #pragma unroll
             for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                float t2 = __shfl_up_sync(0xffffffffu, inc, o2);
+                const float t2 = __shfl_up_sync(0xffffffffu, inc, o2);
                 if (lane >= o2) inc += t2;
             }
-            const float excl = inc - pair;
-            sG[2 * lane] = excl + g0;
+            sG[2 * lane] = inc - pair + g0;
             sG[2 * lane + 1] = inc;
         }
         __syncthreads();
         const float Gr = sG[rr], br = sB[rr], Gl = sG[TC_C - 1];
-        const float gam_r = expf(Gr), bg = br * gam_r, kdec = expf(Gl - Gr);
-        // ---------------- S2: operands of G1 and G2
+        const float gam_r = expf(Gr), bg = br * gam_r;
+        // ---------------- S2: operands of G1 (K and Q rows) and G2 ([bgK | bV], MN-major)
 #pragma unroll
         for (int k8 = 0; k8 < 32; k8 += 8) {
-            put8(a1h, a1l, 128, rr, cq * 32 + k8, &kv[k8]);         // K rows 0-63
-            put8(a1h, a1l, 128, 64 + rr, cq * 32 + k8, &qv[k8]);    // Q rows 64-127
+            put8(kqh, kql, tc::kmaj_off(rr, cq * 32 + k8, 128), &kv[k8]);
+            put8(kqh, kql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), &qv[k8]);
+            float t8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = bg * kv[k8 + i];
+            put8(bwh, bwl, tc::mnmaj_off(cq * 32 + k8, rr, NB), t8);
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) put1(b2h, b2l, 64, cq * 32 + i, rr, bg * kv[i]);   // (b g K)^T
+        for (int k8 = 0; k8 < VQ; k8 += 8) {
+            float t8[8];
 #pragma unroll
-        for (int i = 0; i < VQ; ++i) put1(b2h, b2l, 64, 128 + cq * VQ + i, rr, br * vv[i]);  // (b V)^T
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
+            for (int i = 0; i < 8; ++i) t8[i] = br * vv[k8 + i];
+            put8(bwh, bwl, tc::mnmaj_off(128 + cq * VQ + k8, rr, NB), t8);
+        }
+        sync_for_mma();
         // ---------------- G1: [K;Q] K^T
         if (tid == 0) {
-            mma3(T_D1, sa1h, sa1l, sa1h, sa1l, 128, ID_G1, false);
+            mma3<false, false>(T_D1, s_kqh, s_kql, 0, s_kqh, s_kql, 0, 128, ID_G1, false);
             tc::mma_commit(tc::smem_u32(mbar));
         }
         if (!wait_mma()) { timed_out = true; break; }
-        // ---------------- E1: A (fp32, for the solve) and P (operand); gamma Q into A1
+        // ---------------- E1: A (fp32, for the solve), P (operand), gamma Q in place
         {
             float v32[32];
             tc::tmem_ld32(T_D1 + lane_off + hf * 32, v32);
             const int r = tl & 63;
             const float Gq = sG[r], bq = sB[r];
-            if (qd < 2) {  // K K^T rows
+            if (qd < 2) {  // K K^T rows -> A (strictly lower)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int c = hf * 32 + i;
-                    sA[r * 65 + c] = (c < r) ? bq * expf(Gq - sG[c]) * v32[i] : 0.f;
+                    if (c < r) sA[r * 65 + c] = bq * expf(Gq - sG[c]) * v32[i];
                 }
-            } else {       // Q K^T rows -> P
-                float pv[32];
+            } else {       // Q K^T rows -> P (lower incl. diagonal)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int c = hf * 32 + i;
-                    pv[i] = (c <= r) ? expf(Gq - sG[c]) * v32[i] : 0.f;
+                    v32[i] = (c <= r) ? expf(Gq - sG[c]) * v32[i] : 0.f;
                 }
 #pragma unroll
-                for (int k8 = 0; k8 < 32; k8 += 8) put8(a3h, a3l, 64, 64 + r, hf * 32 + k8, &pv[k8]);
+                for (int k8 = 0; k8 < 32; k8 += 8) put8(tph, tpl, tc::kmaj_off(64 + r, hf * 32 + k8, 64), &v32[k8]);
             }
         }
-        tc::fence_before_sync();
-        __syncthreads();   // G1 has finished reading A1; A is complete
-        {
-            float gq[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) gq[i] = gam_r * qv[i];
+        for (int k8 = 0; k8 < 32; k8 += 8) {   // G1 is done with Q: replace it by gamma Q
+            float t8[8];
 #pragma unroll
-            for (int k8 = 0; k8 < 32; k8 += 8) put8(a1h, a1l, 128, 64 + rr, cq * 32 + k8, &gq[k8]);
+            for (int i = 0; i < 8; ++i) t8[i] = gam_r * qv[k8 + i];
+            put8(kqh, kql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), t8);
         }
-        // ---------------- solve T = (I + A)^-1, written as bf16 hi/lo into A3 rows 0-63
-        if (warp < 4 && lane < 16) {   // diagonal 16x16 blocks, column `lane` of block `warp`
+        __syncthreads();
+        // ---------------- solve T = (I + A)^-1: diagonal 16x16 blocks (column `lane` of block `warp`)
+        if (warp < 4 && lane < 16) {
             const int b0 = warp * 16, c = lane;
             float col[16];
 #pragma unroll
@@ -326,108 +424,94 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
                 col[r] = (r == c) ? 1.f : ((r > c) ? -acc : 0.f);
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) put1(a3h, a3l, 64, b0 + r, b0 + c, col[r]);
+            for (int r = 0; r < 16; ++r)
+                if (r > c) sA[(b0 + c) * 65 + b0 + r] = col[r];   // T[b0+r][b0+c], stored transposed
         }
         __syncthreads();
-        for (int bi = 1; bi < 4; ++bi) {
-            // X_j = sum_{k=j}^{bi-1} A_{bi,k} T_{k,j}   for j < bi (one 16x16 block each)
-            for (int idx = tid; idx < bi * 256; idx += TC_NT) {
-                const int bj = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
-                float acc = 0.f;
-                for (int bk = bj; bk < bi; ++bk)
-                    for (int m = 0; m < 16; ++m)
-                        acc += sA[(bi * 16 + r) * 65 + bk * 16 + m] *
-                               get1(a3h, a3l, 64, bk * 16 + m, bj * 16 + c);
-                sX[(bj * 16 + r) * 17 + c] = acc;
+        // Off-diagonal blocks, one warp per block column bj (no barriers inside):
+        // T[bi][bj] = -T[bi][bi] . sum_{k=bj}^{bi-1} A[bi][k] T[k][bj]   for bi > bj.
+        // Lane (c = lane & 15, row half rh = lane >> 4) keeps column c of the block
+        // column in registers and stores rows 8*rh .. 8*rh+7 of each new block.
+        if (warp < 3) {
+            const int bj = warp, c = lane & 15, rh = lane >> 4;
+            const int m = bj * 16 + c;
+            float tcol[48];   // T[16*bj + k][m], k < 48
+#pragma unroll
+            for (int k = 0; k < 48; ++k) {
+                const int row = bj * 16 + k;
+                tcol[k] = (k < 16) ? ((row > m) ? sA[m * 65 + row] : ((row == m) ? 1.f : 0.f)) : 0.f;
             }
-            __syncthreads();
-            // T_{bi,j} = - T_{bi,bi} X_j
-            for (int idx = tid; idx < bi * 256; idx += TC_NT) {
-                const int bj = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
-                float acc = 0.f;
-                for (int m = 0; m <= r; ++m)
-                    acc += get1(a3h, a3l, 64, bi * 16 + r, bi * 16 + m) * sX[(bj * 16 + m) * 17 + c];
-                put1(a3h, a3l, 64, bi * 16 + r, bj * 16 + c, -acc);
-            }
-            __syncthreads();
+            solve_block_col<1>(sA, tcol, bj, m, rh);
+            solve_block_col<2>(sA, tcol, bj, m, rh);
+            solve_block_col<3>(sA, tcol, bj, m, rh);
         }
-        // zero the strictly upper part of T's off-diagonal blocks (rows 0-63, k > row block)
-        for (int idx = tid; idx < 64 * 64; idx += TC_NT) {
-            const int r = idx >> 6, c = idx & 63;
-            if ((c >> 4) > (r >> 4)) put1(a3h, a3l, 64, r, c, 0.f);
-        }
-        tc::fence_async_smem();
-        tc::fence_before_sync();
         __syncthreads();
-        tc::fence_after_sync();
-        // ---------------- G2: [T;P] . [bgK | bV]^T  ->  W | U  (rows 0-63)
+        // T -> bf16 hi/lo, rows 0-63 of TP (K-major): 64 rows x 8 groups of 8 columns
+        for (int task = tid; task < 64 * 8; task += TC_NT) {
+            const int r = task >> 3, c8 = (task & 7) * 8;
+            float t8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = c8 + i;
+                t8[i] = (c < r) ? sA[c * 65 + r] : ((c == r) ? 1.f : 0.f);
+            }
+            put8(tph, tpl, tc::kmaj_off(r, c8, 64), t8);
+        }
+        sync_for_mma();
+        // ---------------- G2: [T;P] . [bgK | bV]  ->  W | U  (rows 0-63)
         if (tid == 0) {
-            mma3(T_D2, sa3h, sa3l, sb2h, sb2l, 64, ID_G2, false);
+            mma3<false, true>(T_D2, s_tph, s_tpl, 0, s_bwh, s_bwl, NB, 64, ID_G2, false);
             tc::mma_commit(tc::smem_u32(mbar));
         }
         if (!wait_mma()) { timed_out = true; break; }
-        // ---------------- E2: W -> A1 rows 0-63, U -> registers; K~^T -> B2 rows 0-127
+        // ---------------- E2a: K~ = exp(G_last - G_r) K_r (MN-major A of G5) into the freed B2
+        // region; K is read back (hi + lo) from KQ rows 0-63 before W replaces it
+        {
+            const float kdec = expf(Gl - Gr);
+#pragma unroll
+            for (int k8 = 0; k8 < 32; k8 += 8) {
+                float t8[8];
+                get8(kqh, kql, tc::kmaj_off(rr, cq * 32 + k8, 128), t8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t8[i] *= kdec;
+                put8(bwh, bwl, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
+            }
+        }
+        __syncthreads();
+        // ---------------- E2b: W -> rows 0-63 of KQ (G1 is done with K), U -> registers
         float Ur[HALF];
         if (qd < 2) {
-            const int r = tl;
             float v32[32];
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
                 tc::tmem_ld32(T_D2 + lane_off + hf * 64 + part * 32, v32);
 #pragma unroll
                 for (int k8 = 0; k8 < 32; k8 += 8)
-                    put8(a1h, a1l, 128, r, hf * 64 + part * 32 + k8, &v32[k8]);
+                    put8(kqh, kql, tc::kmaj_off(tl, hf * 64 + part * 32 + k8, 128), &v32[k8]);
             }
-            if (HALF == 32) {
-                tc::tmem_ld32(T_D2 + lane_off + 128 + hf * HALF, v32);
-#pragma unroll
-                for (int j = 0; j < HALF; ++j) Ur[j] = v32[j];
-            } else {
-                float v16[16];
-                tc::tmem_ld16(T_D2 + lane_off + 128 + hf * HALF, v16);
-#pragma unroll
-                for (int j = 0; j < HALF; ++j) Ur[j] = v16[j];
-            }
+            tmem_ld<HALF>(T_D2 + lane_off + 128 + hf * HALF, Ur);
         }
-        tc::fence_before_sync();
-        __syncthreads();   // G2 done with B2: overwrite rows 0-127 with K~^T
-#pragma unroll
-        for (int i = 0; i < 32; ++i) put1(b2h, b2l, 64, cq * 32 + i, rr, kdec * kv[i]);
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
+        sync_for_mma();
         // ---------------- G3: [W ; gQ] . M
         if (tid == 0) {
-            mma3(T_D3, sa1h, sa1l, sb3h, sb3l, 128, ID_S, false);
+            mma3<false, true>(T_D3, s_kqh, s_kql, 0, s_mth, s_mtl, DVS, 128, ID_G34, false);
             tc::mma_commit(tc::smem_u32(mbar));
         }
         if (!wait_mma()) { timed_out = true; break; }
-        // ---------------- E3: U' = U - W M  -> U'^T (B4)
+        // ---------------- E3: U' = U - W M  -> MN-major B operand
         if (qd < 2) {
             float wm[HALF];
-            if (HALF == 32) {
-                float v32[32];
-                tc::tmem_ld32(T_D3 + lane_off + hf * HALF, v32);
+            tmem_ld<HALF>(T_D3 + lane_off + hf * HALF, wm);
 #pragma unroll
-                for (int j = 0; j < HALF; ++j) wm[j] = v32[j];
-            } else {
-                float v16[16];
-                tc::tmem_ld16(T_D3 + lane_off + hf * HALF, v16);
+            for (int j = 0; j < HALF; ++j) wm[j] = Ur[j] - wm[j];
 #pragma unroll
-                for (int j = 0; j < HALF; ++j) wm[j] = v16[j];
-            }
-#pragma unroll
-            for (int j = 0; j < HALF; ++j) put1(b4h, b4l, 64, hf * HALF + j, tl, Ur[j] - wm[j]);
+            for (int j8 = 0; j8 < HALF; j8 += 8) put8(uth, utl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &wm[j8]);
         }
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
+        sync_for_mma();
         // ---------------- G4 (O += P U') and G5 (dM = K~^T U')
         if (tid == 0) {
-            mma3(T_D3, sa3h, sa3l, sb4h, sb4l, 64, ID_S, true);
-            mma3(T_D5, sb2h, sb2l, sb4h, sb4l, 64, ID_S, false);
+            mma3<false, true>(T_D3, s_tph, s_tpl, 0, s_uth, s_utl, DVS, 64, ID_G34, true);
+            mma3<true, true>(T_D5, s_bwh, s_bwl, 128, s_uth, s_utl, DVS, 64, ID_G5, false);
             tc::mma_commit(tc::smem_u32(mbar));
         }
         if (!wait_mma()) { timed_out = true; break; }
@@ -436,45 +520,17 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
             float v[HALF];
             if (qd >= 2) {
                 const int r = tl - 64;
-                if (HALF == 32) {
-                    float v32[32];
-                    tc::tmem_ld32(T_D3 + lane_off + hf * HALF, v32);
-#pragma unroll
-                    for (int j = 0; j < HALF; ++j) v[j] = v32[j];
-                } else {
-                    float v16[16];
-                    tc::tmem_ld16(T_D3 + lane_off + hf * HALF, v16);
-#pragma unroll
-                    for (int j = 0; j < HALF; ++j) v[j] = v16[j];
-                }
-                if (r < Lc) {
-                    TOut *orow = o + (c0 + r) * ldo + col0 + hf * HALF;
-#pragma unroll
-                    for (int j = 0; j < HALF; ++j) orow[j] = from_f32<TOut>(v[j]);
-                }
+                tmem_ld<HALF>(T_D3 + lane_off + hf * HALF, v);
+                if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, v);
             }
-            if (HALF == 32) {
-                float v32[32];
-                tc::tmem_ld32(T_D5 + lane_off + hf * HALF, v32);
-#pragma unroll
-                for (int j = 0; j < HALF; ++j) v[j] = v32[j];
-            } else {
-                float v16[16];
-                tc::tmem_ld16(T_D5 + lane_off + hf * HALF, v16);
-#pragma unroll
-                for (int j = 0; j < HALF; ++j) v[j] = v16[j];
-            }
+            tmem_ld<HALF>(T_D5 + lane_off + hf * HALF, v);
             const float gl = expf(Gl);
 #pragma unroll
-            for (int j = 0; j < HALF; ++j) {
-                Mr[j] = gl * Mr[j] + v[j];
-                put1(b3h, b3l, 128, hf * HALF + j, tl, Mr[j]);
-            }
+            for (int j = 0; j < HALF; ++j) Mr[j] = gl * Mr[j] + v[j];
+#pragma unroll
+            for (int j8 = 0; j8 < HALF; j8 += 8) put8(mth, mtl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &Mr[j8]);
         }
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
+        sync_for_mma();
     }
     if (timed_out) {
         // give the outstanding MMAs one more bounded chance to retire before TMEM is freed
@@ -487,8 +543,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
     if (a.state_out && slot >= 0) {
         float *so = a.state_out + ((long long)slot * d.hv + h) * TC_DK * TC_DK +
                     (long long)tl * TC_DK + slice * DVS + hf * HALF;
-#pragma unroll
-        for (int j = 0; j < HALF; ++j) so[j] = Mr[j];
+        store_row<HALF>(so, Mr);
     }
     tc::fence_before_sync();
     __syncthreads();

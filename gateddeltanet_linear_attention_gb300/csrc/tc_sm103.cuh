@@ -49,6 +49,21 @@ __device__ __forceinline__ uint64_t kmaj_desc(uint32_t tile_saddr, uint32_t K, u
     return smem_desc(tile_saddr + (k0 >> 3) * 128u, 128u, (K >> 3) * 128u);
 }
 
+// MN-major ("transposed") operand layout, no swizzle: the 8 MN-consecutive
+// elements of one k form a 16-byte core-matrix row, core matrices are
+// arranged MN-fastest: core (mn block mb, k block kb) starts at byte
+// (kb * (MN/8) + mb) * 128.  So the leading byte offset (next core matrix
+// along K) is MN/8 * 128 and the stride byte offset (next along MN) is 128;
+// the MMA's instruction descriptor marks the operand as transposed.
+__host__ __device__ __forceinline__ uint32_t mnmaj_off(uint32_t mn, uint32_t k, uint32_t MN) {
+    return ((k >> 3) * (MN >> 3) + (mn >> 3)) * 128u + (k & 7u) * 16u + (mn & 7u) * 2u;
+}
+__device__ __forceinline__ uint64_t mnmaj_desc(uint32_t tile_saddr, uint32_t MN, uint32_t k0) {
+    return smem_desc(tile_saddr + (k0 >> 3) * (MN >> 3) * 128u, (MN >> 3) * 128u, 128u);
+}
+constexpr uint32_t kTransA = 1u << 15;   // instruction-descriptor bit: A is MN-major
+constexpr uint32_t kTransB = 1u << 16;   // instruction-descriptor bit: B is MN-major
+
 // Instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
     return (1u << 4)            // D format f32
