@@ -87,6 +87,7 @@ def load(path: str | None = None):
             "gdn_gated_rmsnorm": ([CP, P, I32, P, I64, P, I64, P, I32, V], I32),
             "gdn_mixer_prefill": ([CP, ctypes.POINTER(MixerIO), P, SZ, V], I32),
             "gdn_mixer_decode": ([CP, ctypes.POINTER(MixerIO), V], I32),
+            "gdn_mixer_prefill_static": ([CP, ctypes.POINTER(MixerIO), V], I32),
             "gdn_device_error": ([V, ctypes.POINTER(U32)], I32),
             "gdn_status_string": ([I32], ctypes.c_char_p),
         }
@@ -204,6 +205,16 @@ def gdn_mixer_prefill(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, cu_
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().gdn_mixer_prefill(ctypes.byref(cfg), ctypes.byref(io), _ptr(workspace),
                                     ws_bytes, _stream(stream)), "gdn_mixer_prefill")
+
+
+def gdn_mixer_prefill_static(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, cu_seqlens, y,
+                             state_in=None, state_out=None, conv_state=None, state_idx=None,
+                             stream=None):
+    """gdn_mixer_prefill without a workspace: the library's fixed scratch is used."""
+    io = _mixer_io(x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, cu_seqlens, state_in,
+                   state_out, conv_state, state_idx, y, cu_seqlens.shape[0] - 1)
+    _check(load().gdn_mixer_prefill_static(ctypes.byref(cfg), ctypes.byref(io), _stream(stream)),
+           "gdn_mixer_prefill_static")
 
 
 def gdn_mixer_decode(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, state,

@@ -187,6 +187,24 @@ gdn_status gdn_gated_rmsnorm(const gdn_config *cfg, const void *o, gdn_dtype o_d
 gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void *workspace,
                              size_t workspace_bytes, void *stream);
 
+/* Size of the library-owned scratch array used by gdn_mixer_prefill_static. */
+#define GDN_STATIC_SCRATCH_BYTES (64u << 20)
+
+/* Fused prefill for callers that cannot allocate device memory (the pages
+ * have no counterpart: it exists for callers such as allocation-free step
+ * loops or plugins that receive only a stream and their tensors).  Same
+ * arguments and results as gdn_mixer_prefill, without the workspace: the
+ * intermediates live in a GDN_STATIC_SCRATCH_BYTES array compiled into the
+ * library, which every GPU that loads the library keeps until exit.
+ *  - Allocates nothing.  Returns GDN_ERR_WORKSPACE when
+ *    gdn_workspace_size(cfg, io->T, io->n_seqs) exceeds the array.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make it before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents:
+ *    calls whose GPU work overlaps (other streams, other host threads) race
+ *    and must be serialised by the caller. */
+gdn_status gdn_mixer_prefill_static(const gdn_config *cfg, const gdn_mixer_io *io, void *stream);
+
 /* Fused decode, a8: one token per sequence (io->T == io->n_seqs), conv history
  * and state updated in place (io->state_out must equal io->state_in and be
  * non-NULL; io->conv_state must be non-NULL).  Needs no workspace. */
