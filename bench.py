@@ -68,7 +68,7 @@ def src_sha(paths):
 def traffic_for(name):
     """DRAM bytes per launch from a committed ncu summary, if the kernel source
     has not changed since the counters were taken (else None)."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     try:
