@@ -95,7 +95,7 @@ class Clocks:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -285,8 +285,7 @@ def run_ours(args, rank, ws, local):
     flops = chunk_flops(lens, wl.chunk, wl.dk, wl.dv, wl.HV)
     tc_peak = pk["bf16_tflops"]
     tc_path = wl.act == "bf16" and wl.dk == 128 and wl.dv == 128 and wl.chunk == 64
-    dvs = 64 if N * wl.HV * 2 >= torch.cuda.get_device_properties(dev).multi_processor_count else 32
-    kname = "chunk_tc_kernel<%d> (tcgen05, bf16x3 operands)" % dvs if tc_path else "chunk_simt_kernel"
+    kname = "chunk_tc_kernel<32> (tcgen05, bf16x3 operands)" if tc_path else "chunk_simt_kernel"
     roof = {"kernel": kname, "bound": "tensor", "achieved": flops / chunk_s / 1e12,
             "peak": tc_peak, "unit": "TFLOP/s", "frac": flops / chunk_s / 1e12 / tc_peak,
             "traffic": traffic_for("chunk_prefill_8k"), "peak_source": pk_src + " bf16 burst",
@@ -411,7 +410,7 @@ def bench_e2e(args, dev, gdn, cfg, wl, inp, d, N, T):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_8k", choices=["prefill_8k", "varlen_16"])

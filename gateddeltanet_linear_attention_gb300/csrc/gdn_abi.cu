@@ -95,16 +95,11 @@ PrefillWs carve_prefill(const gdn::Dims &d, long long T, void *ws) {
 
 // The chunked rule: bf16-activation configurations with dk = dv = 128 and
 // 64-token chunks run on the tensor cores (split-bf16 operands); everything
-// else, and the fp32-activation mode, runs the exact fp32 SIMT kernel.  The
-// state-column slice per CTA is 32 when few (sequence, head) units exist (to
-// spread a long sequence over more SMs), else 64 (less duplicated work).
+// else, and the fp32-activation mode, runs the exact fp32 SIMT kernel.  Each
+// tensor-core CTA owns a 32-column slice of one head's state.
 cudaError_t launch_chunk(const gdn::ChunkArgs &a, bool act_bf16, bool in_bf16, bool o_bf16,
                          cudaStream_t s) {
-    if (act_bf16 && gdn::chunk_tc_supported(a.d)) {
-        const long long units = (long long)a.n_seqs * a.d.hv;
-        const int dvs = units * 2 >= gdn::sm_count() ? 64 : 32;
-        return gdn::launch_chunk_tc(a, in_bf16, o_bf16, dvs, s);
-    }
+    if (act_bf16 && gdn::chunk_tc_supported(a.d)) return gdn::launch_chunk_tc(a, in_bf16, o_bf16, 32, s);
     return gdn::launch_chunk_simt(a, in_bf16, o_bf16, s);
 }
 

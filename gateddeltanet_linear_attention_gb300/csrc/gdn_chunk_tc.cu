@@ -60,8 +60,9 @@ struct TcSmem {
     static constexpr int OFF_MT = OFF_TP + 2 * TP;
     static constexpr int OFF_UT = OFF_MT + 2 * MT;
     static constexpr int OFF_SA = OFF_UT + 2 * UT;          // fp32 [64][65]: A below, T^T above the diagonal
-    static constexpr int OFF_X = OFF_SA + 64 * 65 * 4;      // fp32 [3][16][17]
-    static constexpr int OFF_G = OFF_X + 3 * 16 * 17 * 4;   // G[64], beta[64]
+    static constexpr int OFF_GAM = OFF_SA + 64 * 65 * 4;    // fp32 [64][65]: exp(G_r - G_c), c <= r
+    static constexpr int OFF_X = OFF_GAM + 64 * 65 * 4;     // (reserved)
+    static constexpr int OFF_G = OFF_X + 16;                // G[64], beta[64]
     static constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;      // mbarrier, tmem base, timeout flag
     static constexpr int BYTES = OFF_BAR + 16;
 };
@@ -165,6 +166,7 @@ __device__ __forceinline__ void mma3(uint32_t d_tmem, uint32_t a_hi, uint32_t a_
 
 // One block of the triangular inverse, for the block column held by a warp:
 // rows of block bi = bj + DB, column m of T, from the rows already in tcol.
+// (Lanes c and c+16 hold the same column; each stores half of the new rows.)
 template <int DB>
 __device__ __forceinline__ void solve_block_col(float *sA, float (&tcol)[48], int bj, int m, int rh) {
     // Blocks past the last row block are computed on clamped (valid) addresses
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
     unsigned char *mth = sm + L::OFF_MT, *mtl = mth + L::MT;
     unsigned char *uth = sm + L::OFF_UT, *utl = uth + L::UT;
     float *sA = reinterpret_cast<float *>(sm + L::OFF_SA);     // [64][65]
-    float *sX = reinterpret_cast<float *>(sm + L::OFF_X);      // [3][16][17]
+    float *sGam = reinterpret_cast<float *>(sm + L::OFF_GAM);  // [64][65]
     float *sG = reinterpret_cast<float *>(sm + L::OFF_G);      // [64]
     float *sB = sG + 64;                                        // [64]
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
@@ -303,12 +305,12 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
     const TIn *vg = (const TIn *)a.v + col0 + cq * VQ;
     const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
 
-    for (long long c0 = s; c0 < e; c0 += TC_C) {
-        const int Lc = (int)((e - c0) < TC_C ? (e - c0) : TC_C);
-        // ---------------- S0: stage row rr (32 columns of q and k, VQ of v), gates
-        float kv[32], qv[32], vv[VQ];
-        if (rr < Lc) {
-            const long long t = c0 + rr;
+    // Raw rows of the chunk at c0 (row rr of the row mapping) and its gates: the
+    // loads of chunk c+1 are issued while chunk c's second MMA group runs.
+    float kv[32], qv[32], vv[VQ];
+    auto load_chunk = [&](long long c0) {
+        const long long t = c0 + rr;
+        if (t < e) {
             load_row<32>(kg + t * a.ld_qk, kv);
             load_row<32>(qg + t * a.ld_qk, qv);
             load_row<VQ>(vg + t * a.ld_v, vv);
@@ -318,11 +320,28 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
 #pragma unroll
             for (int i = 0; i < VQ; ++i) vv[i] = 0.f;
         }
+    };
+    float gn = 0.f, bn = 0.f;     // gates of the next chunk (threads tid < 64)
+    auto load_gates = [&](long long c0) {
         if (tid < TC_C) {
-            const bool lv = tid < Lc;
-            sG[tid] = lv ? a.g[(c0 + tid) * d.hv + h] : 0.f;
-            sB[tid] = lv ? a.beta[(c0 + tid) * d.hv + h] : 0.f;
+            const long long t = c0 + tid;
+            gn = t < e ? a.g[t * d.hv + h] : 0.f;
+            bn = t < e ? a.beta[t * d.hv + h] : 0.f;
         }
+    };
+    if (s < e) {
+        load_chunk(s);
+        load_gates(s);
+        if (tid < TC_C) {
+            sG[tid] = gn;
+            sB[tid] = bn;
+        }
+    }
+
+    for (long long c0 = s; c0 < e; c0 += TC_C) {
+        const int Lc = (int)((e - c0) < TC_C ? (e - c0) : TC_C);
+        const bool has_next = c0 + TC_C < e;
+        // ---------------- S0: L2 norm of the staged rows; gate scan
         if (l2) {
             float sk = 0.f, sq = 0.f;
 #pragma unroll
@@ -341,8 +360,8 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
                 qv[i] *= fq;
             }
         }
-        __syncthreads();
-        if (warp == 0) {  // inclusive scan of g over 64 rows (2 per lane); padded rows add 0
+        __syncthreads();   // raw gates of this chunk are in sG / sB
+        if (warp == 0) {   // inclusive scan of g over 64 rows (2 per lane); padded rows add 0
             const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
             const float pair = g0 + g1;
             float inc = pair;
@@ -356,7 +375,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
         }
         __syncthreads();
         const float Gr = sG[rr], br = sB[rr], Gl = sG[TC_C - 1];
-        const float gam_r = expf(Gr), bg = br * gam_r;
+        const float bg = br * expf(Gr);
         // ---------------- S2: operands of G1 (K and Q rows) and G2 ([bgK | bV], MN-major)
 #pragma unroll
         for (int k8 = 0; k8 < 32; k8 += 8) {
@@ -375,10 +394,18 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
             put8(bwh, bwl, tc::mnmaj_off(128 + cq * VQ + k8, rr, NB), t8);
         }
         sync_for_mma();
-        // ---------------- G1: [K;Q] K^T
+        // ---------------- G1: [K;Q] K^T;  meanwhile the decay table
         if (tid == 0) {
             mma3<false, false>(T_D1, s_kqh, s_kql, 0, s_kqh, s_kql, 0, 128, ID_G1, false);
             tc::mma_commit(tc::smem_u32(mbar));
+        }
+        {
+            const float Gq = sG[rr];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int c = cq * 16 + i;
+                sGam[rr * 65 + c] = (c <= rr) ? expf(Gq - sG[c]) : 0.f;
+            }
         }
         if (!wait_mma()) { timed_out = true; break; }
         // ---------------- E1: A (fp32, for the solve), P (operand), gamma Q in place
@@ -386,29 +413,32 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
             float v32[32];
             tc::tmem_ld32(T_D1 + lane_off + hf * 32, v32);
             const int r = tl & 63;
-            const float Gq = sG[r], bq = sB[r];
+            const float *grow = sGam + r * 65 + hf * 32;
             if (qd < 2) {  // K K^T rows -> A (strictly lower)
+                const float bq = sB[r];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int c = hf * 32 + i;
-                    if (c < r) sA[r * 65 + c] = bq * expf(Gq - sG[c]) * v32[i];
+                    if (c < r) sA[r * 65 + c] = bq * grow[i] * v32[i];
                 }
-            } else {       // Q K^T rows -> P (lower incl. diagonal)
+            } else {       // Q K^T rows -> P (lower incl. diagonal; Gamma is 0 above)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = hf * 32 + i;
-                    v32[i] = (c <= r) ? expf(Gq - sG[c]) * v32[i] : 0.f;
-                }
+                for (int i = 0; i < 32; ++i) v32[i] *= grow[i];
 #pragma unroll
                 for (int k8 = 0; k8 < 32; k8 += 8) put8(tph, tpl, tc::kmaj_off(64 + r, hf * 32 + k8, 64), &v32[k8]);
             }
         }
+        {   // G1 is done with Q: replace it by gamma Q (read back hi + lo)
+            const float gam_r = expf(Gr);
 #pragma unroll
-        for (int k8 = 0; k8 < 32; k8 += 8) {   // G1 is done with Q: replace it by gamma Q
-            float t8[8];
+            for (int k8 = 0; k8 < 32; k8 += 8) {
+                float t8[8];
+                const uint32_t off = tc::kmaj_off(64 + rr, cq * 32 + k8, 128);
+                get8(kqh, kql, off, t8);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) t8[i] = gam_r * qv[k8 + i];
-            put8(kqh, kql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), t8);
+                for (int i = 0; i < 8; ++i) t8[i] *= gam_r;
+                put8(kqh, kql, off, t8);
+            }
         }
         __syncthreads();
         // ---------------- solve T = (I + A)^-1: diagonal 16x16 blocks (column `lane` of block `warp`)
@@ -430,8 +460,6 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
         __syncthreads();
         // Off-diagonal blocks, one warp per block column bj (no barriers inside):
         // T[bi][bj] = -T[bi][bi] . sum_{k=bj}^{bi-1} A[bi][k] T[k][bj]   for bi > bj.
-        // Lane (c = lane & 15, row half rh = lane >> 4) keeps column c of the block
-        // column in registers and stores rows 8*rh .. 8*rh+7 of each new block.
         if (warp < 3) {
             const int bj = warp, c = lane & 15, rh = lane >> 4;
             const int m = bj * 16 + c;
@@ -458,10 +486,16 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
             put8(tph, tpl, tc::kmaj_off(r, c8, 64), t8);
         }
         sync_for_mma();
-        // ---------------- G2: [T;P] . [bgK | bV]  ->  W | U  (rows 0-63)
+        // ---------------- G2: [T;P] . [bgK | bV]  ->  W | U  (rows 0-63); meanwhile the
+        // next chunk's rows and gates are loaded (after the shared-memory-heavy solve, so
+        // that the global loads do not queue in front of it)
         if (tid == 0) {
             mma3<false, true>(T_D2, s_tph, s_tpl, 0, s_bwh, s_bwl, NB, 64, ID_G2, false);
             tc::mma_commit(tc::smem_u32(mbar));
+        }
+        if (has_next) {
+            load_chunk(c0 + TC_C);
+            load_gates(c0 + TC_C);
         }
         if (!wait_mma()) { timed_out = true; break; }
         // ---------------- E2a: K~ = exp(G_last - G_r) K_r (MN-major A of G5) into the freed B2
@@ -508,11 +542,15 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
             for (int j8 = 0; j8 < HALF; j8 += 8) put8(uth, utl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &wm[j8]);
         }
         sync_for_mma();
-        // ---------------- G4 (O += P U') and G5 (dM = K~^T U')
+        // ---------------- G4 (O += P U') and G5 (dM = K~^T U'); meanwhile the next chunk's gates
         if (tid == 0) {
             mma3<false, true>(T_D3, s_tph, s_tpl, 0, s_uth, s_utl, DVS, 64, ID_G34, true);
             mma3<true, true>(T_D5, s_bwh, s_bwl, 128, s_uth, s_utl, DVS, 64, ID_G5, false);
             tc::mma_commit(tc::smem_u32(mbar));
+        }
+        if (has_next && tid < TC_C) {
+            sG[tid] = gn;
+            sB[tid] = bn;
         }
         if (!wait_mma()) { timed_out = true; break; }
         // ---------------- E4: outputs (lanes 64-127) and the state (all lanes)
@@ -530,7 +568,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
 #pragma unroll
             for (int j8 = 0; j8 < HALF; j8 += 8) put8(mth, mtl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &Mr[j8]);
         }
-        sync_for_mma();
+        // (the next chunk's first operand writes are followed by sync_for_mma before G1)
     }
     if (timed_out) {
         // give the outstanding MMAs one more bounded chance to retire before TMEM is freed
@@ -575,7 +613,6 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int d
                       : launch_tc_t<DVS_, float, float>(a, s);                                \
     }
     GDN_TC(32)
-    GDN_TC(64)
 #undef GDN_TC
     return cudaErrorInvalidValue;
 }
