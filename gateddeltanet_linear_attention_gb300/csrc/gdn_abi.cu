@@ -168,7 +168,9 @@ gdn_status gdn_conv1d_prefill(const gdn_config *cfg, const void *x, int64_t ld_x
         if (T != 0) return GDN_ERR_INVALID_ARG;
         if (n_seqs == 0) return GDN_OK;
     }
-    if (!cu_seqlens || !w || !out || (T > 0 && !valid_view(x, ld_x, d.ch))) return GDN_ERR_INVALID_ARG;
+    if (!cu_seqlens || !w || !aligned16(w) || !out || !aligned16(out) ||
+        (T > 0 && !valid_view(x, ld_x, d.ch)))
+        return GDN_ERR_INVALID_ARG;
     if (conv_state && !aligned16(conv_state)) return GDN_ERR_INVALID_ARG;
     if (conv_state && d.n_slots == 0) return GDN_ERR_INVALID_ARG;
     unsigned *err = nullptr;
@@ -272,7 +274,8 @@ gdn_status gdn_gated_rmsnorm(const gdn_config *cfg, const void *o, gdn_dtype o_d
     if (st != GDN_OK) return st;
     if (T < 0 || !valid_dtype(o_dtype) || !valid_dtype(y_dtype)) return GDN_ERR_INVALID_ARG;
     if (T == 0) return GDN_OK;
-    if (!o || !aligned16(o) || !valid_view(z, ld_z, (long long)d.hv * d.dv) || !w || !y)
+    if (!o || !aligned16(o) || !valid_view(z, ld_z, (long long)d.hv * d.dv) || !w ||
+        !aligned16(w) || !y || !aligned16(y))
         return GDN_ERR_INVALID_ARG;
     return launch_status(gdn::launch_gated_rmsnorm(d, cfg->act == GDN_BF16, o, o_dtype == GDN_BF16,
                                                    z, ld_z, w, T, y, y_dtype == GDN_BF16,
@@ -287,7 +290,8 @@ static gdn_status check_mixer_io(const gdn::Dims &d, const gdn_mixer_io *io, boo
     if (io->T == 0) return GDN_OK;
     if (!valid_view(io->x, io->ld_x, d.ch) || !valid_view(io->z, io->ld_z, (long long)d.hv * d.dv) ||
         !valid_narrow_view(io->u, io->ld_ub, d.hv) || !valid_narrow_view(io->b_logit, io->ld_ub, d.hv) ||
-        !io->conv_w || !io->A_log || !io->dt_bias || !io->norm_w || !io->y)
+        !io->conv_w || !aligned16(io->conv_w) || !io->A_log || !io->dt_bias || !io->norm_w ||
+        !aligned16(io->norm_w) || !io->y || !aligned16(io->y))
         return GDN_ERR_INVALID_ARG;
     if (!decode && !io->cu_seqlens) return GDN_ERR_INVALID_ARG;
     if ((io->state_in && !aligned16(io->state_in)) || (io->state_out && !aligned16(io->state_out)) ||

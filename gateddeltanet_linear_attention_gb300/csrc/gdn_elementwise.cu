@@ -44,28 +44,64 @@ cudaError_t launch_gate_prep(const Dims &d, bool act_bf16, const void *u, const 
 }
 
 // ------------------------------------------------------------ conv prefill
-// One thread per channel, CONV_TT consecutive tokens per CTA row.  Token t of
-// sequence n (start s) reads taps x[t-3..t]; taps before s come from the
-// sequence's history slot (zero without one).  Outputs only: the history is
-// replaced afterwards by conv_state_update_kernel, so no CTA can overwrite a
-// history another CTA still has to read.
+// Each thread owns 8 consecutive channels (one 16-byte row segment of bf16
+// input) for CONV_TT consecutive tokens, sliding a 3-token window in
+// registers: one vector load and one or two vector stores per token.  Taps
+// before a sequence start come from its history slot (zero without one).
+// Outputs only: the history is replaced afterwards by
+// conv_state_update_kernel, so no CTA can overwrite a history another CTA
+// still has to read.
 constexpr int CONV_TT = 32;
 constexpr int CONV_NT = 128;
+constexpr int CONV_V = 8;
+
+__device__ __forceinline__ void load8f(const float *p, float *v) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8f(const __nv_bfloat16 *p, float *v) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void store8f(float *p, const float *v) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8f(__nv_bfloat16 *p, const float *v) {
+    __nv_bfloat162 h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    *reinterpret_cast<uint4 *>(p) = *reinterpret_cast<const uint4 *>(h);
+}
 
 template <typename TA, typename TO>
 __global__ void __launch_bounds__(CONV_NT)
     conv_prefill_kernel(Dims d, const TA *x, long long ld_x, const int32_t *cu, int n_seqs,
                         long long T, const TA *w, const TA *conv_state,
                         const int32_t *state_idx, TO *out, unsigned *err) {
-    int c = blockIdx.y * CONV_NT + threadIdx.x;
-    long long t0 = (long long)blockIdx.x * CONV_TT;
-    if (c >= d.ch || t0 >= T) return;
-    float w0 = to_f32(w[c * 4 + 0]), w1 = to_f32(w[c * 4 + 1]), w2 = to_f32(w[c * 4 + 2]),
-          w3 = to_f32(w[c * 4 + 3]);
-    // sequence containing t0: last n with cu[n] <= t0 (first of equal starts skipped below)
+    const int c0 = (blockIdx.y * CONV_NT + threadIdx.x) * CONV_V;
+    const long long t0 = (long long)blockIdx.x * CONV_TT;
+    if (c0 >= d.ch || t0 >= T) return;
+    float wv[CONV_V][4];
+    {
+        float wf[4 * CONV_V];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) load8f(w + (long long)c0 * 4 + 8 * i, wf + 8 * i);
+#pragma unroll
+        for (int i = 0; i < CONV_V; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) wv[i][j] = wf[4 * i + j];
+    }
+    // sequence containing t0: last n with cu[n] <= t0 (empty sequences skipped below)
     int lo = 0, hi = n_seqs - 1;
     while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
+        const int mid = (lo + hi + 1) >> 1;
         if (cu[mid] <= t0) lo = mid; else hi = mid - 1;
     }
     int n = lo;
@@ -73,27 +109,57 @@ __global__ void __launch_bounds__(CONV_NT)
     seq_bounds(cu, n, T, err, s, e);
     while (t0 >= e && n + 1 < n_seqs) { ++n; seq_bounds(cu, n, T, err, s, e); }
     int slot = slot_of(state_idx, n, d.n_slots, err);
-    long long t_end = t0 + CONV_TT < T ? t0 + CONV_TT : T;
-    for (long long t = t0; t < t_end; ++t) {
-        while (t >= e && n + 1 < n_seqs) {
-            ++n;
-            seq_bounds(cu, n, T, err, s, e);
-            slot = slot_of(state_idx, n, d.n_slots, err);
-        }
-        float tap[4];
+    // the three taps before token t of the current sequence (window[0] oldest)
+    float win[3][CONV_V];
+    auto fill_window = [&](long long t) {
+        float hist[3 * CONV_V];
+        const bool has_hist = conv_state && slot >= 0;
+        if (has_hist) {
+            const TA *hp = conv_state + ((long long)slot * d.ch + c0) * 3;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            long long tt = t - 3 + j;
-            float val = 0.0f;
-            if (tt >= s) {
-                val = to_f32(x[tt * ld_x + c]);
-            } else if (conv_state && slot >= 0 && tt >= s - 3) {
-                val = to_f32(conv_state[((long long)slot * d.ch + c) * 3 + (tt - s + 3)]);
-            }
-            tap[j] = val;
+            for (int i = 0; i < 3; ++i) load8f(hp + 8 * i, hist + 8 * i);
         }
-        float acc = w0 * tap[0] + w1 * tap[1] + w2 * tap[2] + w3 * tap[3];
-        out[t * d.ch + c] = from_f32<TO>(silu_f(acc));
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const long long tt = t - 3 + j;
+            if (tt >= s) {
+                load8f(x + tt * ld_x + c0, win[j]);
+            } else {
+                const int hj = (int)(tt - s + 3);     // in [0, 3) since t >= s
+#pragma unroll
+                for (int i = 0; i < CONV_V; ++i) {
+                    float hv = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 3; ++q)
+                        if (q == hj) hv = hist[3 * i + q];
+                    win[j][i] = has_hist ? hv : 0.f;
+                }
+            }
+        }
+    };
+    fill_window(t0);
+    const long long t_end = t0 + CONV_TT < T ? t0 + CONV_TT : T;
+    for (long long t = t0; t < t_end; ++t) {
+        if (t >= e && n + 1 < n_seqs) {
+            while (t >= e && n + 1 < n_seqs) {
+                ++n;
+                seq_bounds(cu, n, T, err, s, e);
+            }
+            slot = slot_of(state_idx, n, d.n_slots, err);
+            fill_window(t);
+        }
+        float cur[CONV_V], o[CONV_V];
+        load8f(x + t * ld_x + c0, cur);
+#pragma unroll
+        for (int i = 0; i < CONV_V; ++i) {
+            const float acc = wv[i][0] * win[0][i] + wv[i][1] * win[1][i] + wv[i][2] * win[2][i] +
+                              wv[i][3] * cur[i];
+            o[i] = silu_f(acc);
+            win[0][i] = win[1][i];
+            win[1][i] = win[2][i];
+            win[2][i] = cur[i];
+        }
+        store8f(out + t * d.ch + c0, o);
     }
 }
 
@@ -130,7 +196,7 @@ cudaError_t launch_conv_prefill(const Dims &d, bool act_bf16, const void *x, lon
                                 const void *conv_state, const int32_t *state_idx, void *out,
                                 bool out_bf16, unsigned *err, cudaStream_t s) {
     if (T == 0 || n_seqs == 0) return cudaSuccess;
-    dim3 grid((unsigned)((T + CONV_TT - 1) / CONV_TT), (d.ch + CONV_NT - 1) / CONV_NT);
+    dim3 grid((unsigned)((T + CONV_TT - 1) / CONV_TT), (d.ch + CONV_NT * CONV_V - 1) / (CONV_NT * CONV_V));
 #define GDN_CONV(TA, TO)                                                                   \
     conv_prefill_kernel<TA, TO><<<grid, CONV_NT, 0, s>>>(                                   \
         d, (const TA *)x, ld_x, cu, n_seqs, T, (const TA *)w, (const TA *)conv_state,       \
@@ -207,34 +273,65 @@ cudaError_t launch_conv_step(const Dims &d, bool act_bf16, const void *x, long l
 }
 
 // ------------------------------------------------------------ gated norm
-// One warp per (token, v-head) row of dv values: y = o*rsqrt(mean(o^2)+eps)*w*SiLU(z).
+// One warp per (token, v-head) row of dv values, lane l holding the dv/32
+// consecutive values l*dv/32 ..: y = o*rsqrt(mean(o^2)+eps)*w*SiLU(z).
+template <int PER, typename T>
+__device__ __forceinline__ void loadv(const T *p, float *v) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) v[i] = to_f32(p[i]);
+}
+template <>
+__device__ __forceinline__ void loadv<4, float>(const float *p, float *v) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+template <>
+__device__ __forceinline__ void loadv<4, __nv_bfloat16>(const __nv_bfloat16 *p, float *v) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+    const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+template <int PER, typename T>
+__device__ __forceinline__ void storev(T *p, const float *v) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) p[i] = from_f32<T>(v[i]);
+}
+template <>
+__device__ __forceinline__ void storev<4, float>(float *p, const float *v) {
+    *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void storev<4, __nv_bfloat16>(__nv_bfloat16 *p, const float *v) {
+    __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
+    *reinterpret_cast<uint2 *>(p) = *reinterpret_cast<const uint2 *>(h);
+}
+
 template <int DV, typename TO_IN, typename TZ, typename TY>
 __global__ void gated_rmsnorm_kernel(Dims d, const TO_IN *o, const TZ *z, long long ld_z,
                                      const float *w, long long T, TY *y) {
     constexpr int PER = DV / 32;
-    long long rows = T * d.hv;
-    int lane = threadIdx.x & 31;
-    long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-    long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long rows = T * d.hv;
+    const int lane = threadIdx.x & 31;
+    const long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    float wv[PER];
+    loadv<PER>(w + lane * PER, wv);
     for (long long r = warp; r < rows; r += nwarps) {
-        long long t = r / d.hv;
-        int h = (int)(r - t * d.hv);
-        const TO_IN *orow = o + r * DV;
-        const TZ *zrow = z + t * ld_z + (long long)h * DV;
-        float ov[PER], ss = 0.f;
+        const long long t = r / d.hv;
+        const int h = (int)(r - t * d.hv);
+        float ov[PER], zv[PER];
+        loadv<PER>(o + r * DV + lane * PER, ov);
+        loadv<PER>(z + t * ld_z + (long long)h * DV + lane * PER, zv);
+        float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            ov[i] = to_f32(orow[lane + 32 * i]);
-            ss += ov[i] * ov[i];
-        }
+        for (int i = 0; i < PER; ++i) ss += ov[i] * ov[i];
         ss = warp_sum(ss);
-        float rs = rsqrtf(ss / (float)DV + d.norm_eps);
-        TY *yrow = y + r * DV;
+        const float rs = rsqrtf(ss / (float)DV + d.norm_eps);
+        float yv[PER];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            int j = lane + 32 * i;
-            yrow[j] = from_f32<TY>(ov[i] * rs * w[j] * silu_f(to_f32(zrow[j])));
-        }
+        for (int i = 0; i < PER; ++i) yv[i] = ov[i] * rs * wv[i] * silu_f(zv[i]);
+        storev<PER>(y + r * DV + lane * PER, yv);
     }
 }
 

@@ -43,7 +43,8 @@
  *    head-major, CH = 2*HK*dk + HV*dv.  Row strides (ld_*) are in ELEMENTS.
  *    Wide views (x, z, q, k, v) need 16-byte aligned bases and strides that
  *    are multiples of 8 elements; the narrow [T][HV] views u and b_logit need
- *    only element alignment and ld >= HV.
+ *    only element alignment and ld >= HV.  Conv weights, the norm weight,
+ *    states, histories, workspaces and outputs need 16-byte aligned bases.
  *  - The live (non-negative) entries of state_idx must be distinct within a
  *    call: two sequences writing one slot race.
  *  - Outputs never alias inputs, except state_out == state_in (in place).
