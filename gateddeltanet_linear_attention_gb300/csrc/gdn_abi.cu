@@ -137,7 +137,8 @@ const char *gdn_status_string(gdn_status s) {
 size_t gdn_workspace_size(const gdn_config *cfg, int64_t max_tokens, int32_t max_seqs) {
     gdn::Dims d;
     if (check_cfg(cfg, &d) != GDN_OK || max_tokens < 0 || max_seqs < 0) return 0;
-    return prefill_ws_bytes(d, max_tokens) + 256;
+    const size_t pre = prefill_ws_bytes(d, max_tokens), dec = gdn::decode_ws_bytes(d, max_seqs);
+    return (pre > dec ? pre : dec) + 256;
 }
 
 gdn_status gdn_gate_prep(const gdn_config *cfg, const void *u, const void *b_logit, int64_t ld_ub,
@@ -354,12 +355,16 @@ gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void
     return launch_status(e);
 }
 
-gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *stream) {
+gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *workspace,
+                            size_t workspace_bytes, void *stream) {
     gdn::Dims d;
     gdn_status st = check_cfg(cfg, &d);
     if (st != GDN_OK) return st;
     if ((st = check_mixer_io(d, io, true)) != GDN_OK) return st;
     if (io->n_seqs == 0) return GDN_OK;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < gdn::decode_ws_bytes(d, io->n_seqs))
+        return GDN_ERR_WORKSPACE;
     unsigned *err = nullptr;
     if ((st = error_word(&err)) != GDN_OK) return st;
     gdn::DecodeArgs a = {};
@@ -367,6 +372,7 @@ gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void 
     a.u = io->u; a.b_logit = io->b_logit; a.ld_ub = io->ld_ub; a.A_log = io->A_log;
     a.dt_bias = io->dt_bias; a.z = io->z; a.ld_z = io->ld_z; a.norm_w = io->norm_w;
     a.n = io->n_seqs; a.state = io->state_out; a.state_idx = io->state_idx; a.out = io->y;
+    a.ws = (float *)workspace;
     a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
     return launch_status(gdn::launch_decode(a, true, cfg->act == GDN_BF16,
                                             io->y_dtype == GDN_BF16, (cudaStream_t)stream));

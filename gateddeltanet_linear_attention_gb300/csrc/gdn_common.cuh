@@ -99,10 +99,24 @@ struct DecodeArgs {
     float *state;
     const int32_t *state_idx;
     void *out;  // fused: y; unfused: o
+    float *ws;  // fused: per-unit records written by the prep kernel (caller workspace)
     unsigned flags;
     Dims d;
     unsigned *err;
 };
+
+// Per-(sequence, q/k head) record the fused decode's prep kernel writes and its
+// streaming kernel reads (floats): normalised q and k, conv'd v and SiLU(z) of
+// the unit's G v-heads, the gates a and beta, k.q, and the state slot.
+struct DecRec {
+    int q, k, v, z, ga, gb, kq, slot, size;
+    __host__ __device__ DecRec(int dk, int dv, int g) {
+        q = 0; k = dk; v = 2 * dk; z = v + g * dv; ga = z + g * dv; gb = ga + g; kq = gb + g;
+        slot = kq + 1;
+        size = (slot + 1 + 3) & ~3;      // 16-byte multiple
+    }
+};
+size_t decode_ws_bytes(const Dims &d, long long n_seqs);
 
 cudaError_t launch_gate_prep(const Dims &d, bool act_bf16, const void *u, const void *b,
                              long long ld_ub, long long T, const float *A_log,

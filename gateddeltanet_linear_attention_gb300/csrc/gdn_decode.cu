@@ -17,10 +17,9 @@
 // store is a fully coalesced 16-byte vector access.  Column sums over rows go
 // through registers, then one shared-memory pass over the 16 row groups.
 //
-// The fused form also runs, for the same CTA, the conv step of the q/k
-// channels of its q/k head and the v channels of its v-heads (each history
-// has exactly one owner, so the in-place shift is race-free), SiLU, the q/k L2
-// norm, the gates and the gated RMSNorm: one launch per decode step.
+// decode_kernel below serves gdn_recurrent_decode (q, k, v, g, beta given);
+// the fused mixer decode (conv step, gates and gated RMSNorm included) is the
+// prep + streaming pair further down.
 #include "gdn_common.cuh"
 #include "tc_sm103.cuh"
 
@@ -35,7 +34,7 @@ struct DecodeCfg {
     static constexpr int MAXG = 4;             // largest GQA group
 };
 
-template <int DK, int DV, typename TA, typename TOut, bool FUSED>
+template <int DK, int DV, typename TA, typename TOut>
 __global__ void __launch_bounds__(4 * DV) decode_kernel(DecodeArgs a) {
     using Cfg = DecodeCfg<DK, DV>;
     constexpr int NT = Cfg::NT, LPR = Cfg::LPR, RPP = Cfg::RPP, RPT = Cfg::RPT;
@@ -74,37 +73,7 @@ __global__ void __launch_bounds__(4 * DV) decode_kernel(DecodeArgs a) {
         m[x] = *reinterpret_cast<const float4 *>(Mbase + (long long)(rg + x * RPP) * DV + c4);
 
     // ---- prologue: q, k (this q/k head) and v (its v-heads), gates
-    if (FUSED) {
-        const TA *x = (const TA *)a.x + (long long)n * a.ld_x;
-        const TA *w = (const TA *)a.conv_w;
-        TA *cs = (TA *)a.conv_state + (long long)slot * d.ch * 3;
-        const int nch = 2 * DK + G * DV;
-        for (int ci = tid; ci < nch; ci += NT) {
-            int c;
-            if (ci < DK) c = kh * DK + ci;
-            else if (ci < 2 * DK) c = d.hk * DK + kh * DK + (ci - DK);
-            else c = 2 * d.hk * DK + kh * G * DV + (ci - 2 * DK);
-            TA *hc = cs + (long long)c * 3;
-            TA h0 = hc[0], h1 = hc[1], h2 = hc[2], xc = x[c];
-            float acc = to_f32(w[c * 4 + 0]) * to_f32(h0) + to_f32(w[c * 4 + 1]) * to_f32(h1) +
-                        to_f32(w[c * 4 + 2]) * to_f32(h2) + to_f32(w[c * 4 + 3]) * to_f32(xc);
-            hc[0] = h1;
-            hc[1] = h2;
-            hc[2] = xc;
-            float val = silu_f(acc);
-            if (ci < DK) qs[ci] = val;
-            else if (ci < 2 * DK) ks[ci - DK] = val;
-            else vs[(ci - 2 * DK) / DV][(ci - 2 * DK) % DV] = val;
-        }
-        if (tid < G) {
-            const int h = kh * G + tid;
-            const TA *u = (const TA *)a.u + (long long)n * a.ld_ub;
-            const TA *b = (const TA *)a.b_logit + (long long)n * a.ld_ub;
-            float gg = -expf(a.A_log[h]) * softplus_f(to_f32(u[h]) + a.dt_bias[h]);
-            gate_a[tid] = expf(gg);
-            gate_b[tid] = sigmoid_f(to_f32(b[h]));
-        }
-    } else {
+    {
         const TA *q = (const TA *)a.q + (long long)n * a.ld_qk + (long long)kh * DK;
         const TA *k = (const TA *)a.k + (long long)n * a.ld_qk + (long long)kh * DK;
         const TA *v = (const TA *)a.v + (long long)n * a.ld_v + (long long)kh * G * DV;
@@ -120,7 +89,7 @@ __global__ void __launch_bounds__(4 * DV) decode_kernel(DecodeArgs a) {
         }
     }
     __syncthreads();
-    const bool l2 = FUSED || (a.flags & GDN_FLAG_L2NORM_QK);
+    const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
     if (warp < 2) {  // warp 0: |q|, warp 1: |k|
         float *vec = warp == 0 ? qs : ks;
         float ss = 0.f;
@@ -195,37 +164,106 @@ __global__ void __launch_bounds__(4 * DV) decode_kernel(DecodeArgs a) {
             }
         }
         // output row of this v-head
-        if (FUSED) {
-            float ov = tid < DV ? os[tid] : 0.f;
-            float sq = warp_sum(ov * ov);
-            if (tid < DV && lane == 0) red_p[0][warp] = sq;  // red_p is free again here
-            __syncthreads();
-            if (tid < DV) {
-                float tot = 0.f;
-                for (int wi = 0; wi < DV / 32; ++wi) tot += red_p[0][wi];
-                float rs = rsqrtf(tot / (float)DV + d.norm_eps);
-                const TA *z = (const TA *)a.z + (long long)n * a.ld_z + (long long)h * DV;
-                out[out_row + (long long)h * DV + tid] =
-                    from_f32<TOut>(ov * rs * a.norm_w[tid] * silu_f(to_f32(z[tid])));
-            }
-        } else {
-            if (tid < DV) out[out_row + (long long)h * DV + tid] = from_f32<TOut>(os[tid]);
-        }
+        if (tid < DV) out[out_row + (long long)h * DV + tid] = from_f32<TOut>(os[tid]);
         __syncthreads();
     }
 }
 
 // ---------------------------------------------------------------------------
-// Streaming form of the fused decode (the product path).  A persistent grid of
-// one CTA per SM walks its (sequence, q/k head) units; each unit's G head
-// states (dk*dv*4 bytes each) flow HBM -> shared memory through a ring of NS
-// slots filled by bulk asynchronous copies (cp.async.bulk, completion counted
-// on one mbarrier per slot), so that while one head is being updated the next
-// NS-1 are already in flight.  The small per-unit inputs (conv step of the
-// unit's q/k/v channels, SiLU, L2, gates, and the z rows of the norm) are
-// computed for a batch of HB heads at once, so their global loads overlap
-// each other and the state copies instead of sitting on every head's critical
-// path; per head only shared memory is touched before the state write.
+// Fused decode, the product path: two launches.
+//
+// decode_prep_kernel (one CTA per (sequence, q/k head) unit, all units in
+// parallel): the conv step of the unit's q/k channels and of its G v-heads'
+// channels (each history has exactly one owner, so the in-place shift is
+// race-free), SiLU, the q/k L2 norm, k.q, the gates and SiLU(z), written as one
+// record per unit to the caller's workspace.  Doing this for every unit at
+// once pays the global-load latency once, instead of on the state stream's
+// critical path.
+//
+// decode_stream_kernel (persistent, one CTA per SM): walks its units; each
+// unit's G head states (dk*dv*4 bytes each) flow HBM -> shared memory through
+// a ring of NS slots filled by bulk asynchronous copies (cp.async.bulk,
+// completion counted on one mbarrier per slot), so that while one head is
+// updated the next NS-1 are in flight.  The records of the next batch of HB
+// heads are bulk-copied into shared memory one batch ahead, so each head
+// touches only shared memory before its state is written back.
+template <int DK, int DV, typename TA>
+__global__ void __launch_bounds__(256) decode_prep_kernel(DecodeArgs a) {
+    __shared__ __align__(16) float qs[DK], ks[DK];
+    __shared__ float scal[8 + 8];
+    const Dims &d = a.d;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // The streaming kernel may be scheduled as soon as every prep CTA has
+    // started: it cannot share an SM with one, and it waits for this grid's
+    // completion (griddepcontrol.wait) before it reads any record.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int u = blockIdx.x, n = u / d.hk, kh = u % d.hk, G = d.grp;
+    const DecRec R(DK, DV, G);
+    float *rec = a.ws + (long long)u * R.size;
+    const int slot = slot_of(a.state_idx, n, d.n_slots, a.err);
+    if (slot < 0) {
+        if (tid == 0) rec[R.slot] = __int_as_float(-1);
+        return;
+    }
+    const TA *x = (const TA *)a.x + (long long)n * a.ld_x;
+    const TA *w = (const TA *)a.conv_w;
+    TA *cs = (TA *)a.conv_state + (long long)slot * d.ch * 3;
+    const int nch = 2 * DK + G * DV;
+    for (int ci = tid; ci < nch; ci += 256) {
+        int c;
+        if (ci < DK) c = kh * DK + ci;
+        else if (ci < 2 * DK) c = d.hk * DK + kh * DK + (ci - DK);
+        else c = 2 * d.hk * DK + kh * G * DV + (ci - 2 * DK);
+        TA *hc = cs + (long long)c * 3;
+        const TA h0 = hc[0], h1 = hc[1], h2 = hc[2], xc = x[c];
+        const float acc = to_f32(w[c * 4 + 0]) * to_f32(h0) + to_f32(w[c * 4 + 1]) * to_f32(h1) +
+                          to_f32(w[c * 4 + 2]) * to_f32(h2) + to_f32(w[c * 4 + 3]) * to_f32(xc);
+        hc[0] = h1;
+        hc[1] = h2;
+        hc[2] = xc;
+        const float val = silu_f(acc);
+        if (ci < DK) qs[ci] = val;
+        else if (ci < 2 * DK) ks[ci - DK] = val;
+        else rec[R.v + (ci - 2 * DK)] = val;
+    }
+    const TA *z = (const TA *)a.z + (long long)n * a.ld_z + (long long)kh * G * DV;
+    for (int idx = tid; idx < G * DV; idx += 256) rec[R.z + idx] = silu_f(to_f32(z[idx]));
+    if (tid < G) {
+        const int h = kh * G + tid;
+        const TA *uv = (const TA *)a.u + (long long)n * a.ld_ub;
+        const TA *bv = (const TA *)a.b_logit + (long long)n * a.ld_ub;
+        const float gg = -expf(a.A_log[h]) * softplus_f(to_f32(uv[h]) + a.dt_bias[h]);
+        rec[R.ga + tid] = expf(gg);
+        rec[R.gb + tid] = sigmoid_f(to_f32(bv[h]));
+    }
+    __syncthreads();
+    if (warp < 2) {   // |q|^2 (warp 0), |k|^2 (warp 1)
+        const float *vec = warp == 0 ? qs : ks;
+        float ss = 0.f;
+        for (int i = lane; i < DK; i += 32) ss += vec[i] * vec[i];
+        ss = warp_sum(ss);
+        if (lane == 0) scal[warp] = ss;
+    }
+    __syncthreads();
+    const float fq = rsqrtf(scal[0] + d.l2_eps) * d.q_scale, fk = rsqrtf(scal[1] + d.l2_eps);
+    float kq = 0.f;
+    for (int i = tid; i < DK; i += 256) {
+        const float qn = qs[i] * fq, kn = ks[i] * fk;
+        rec[R.q + i] = qn;
+        rec[R.k + i] = kn;
+        kq += qn * kn;
+    }
+    kq = warp_sum(kq);
+    if (lane == 0) scal[8 + warp] = kq;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+        for (int wi = 0; wi < 8; ++wi) t += scal[8 + wi];
+        rec[R.kq] = t;
+        rec[R.slot] = __int_as_float(slot);
+    }
+}
+
 template <int DK, int DV>
 struct StreamCfg {
     static constexpr int NT = 4 * DV;
@@ -233,26 +271,25 @@ struct StreamCfg {
     static constexpr int SLOT = DK * DV * 4;                        // bytes of one head state
     static constexpr int NS = SLOT >= 65536 ? 3 : (SLOT >= 16384 ? 8 : 16);
     static constexpr int CHUNK = SLOT < 16384 ? SLOT : 16384;       // bytes per bulk copy
-    static constexpr int HB = 4;                                    // heads per prologue batch
+    static constexpr int HB = 4;                                    // heads per record batch
+    // largest (HB/G) * record size over G in {1, 2, 4}: the records of one batch
+    static constexpr int rec_floats(int g) { return (2 * DK + 2 * g * DV + 2 * g + 2 + 3) & ~3; }
+    static constexpr int max2(int x, int y) { return x > y ? x : y; }
+    static constexpr int RECBUF = max2(max2(HB * rec_floats(1), (HB / 2) * rec_floats(2)), rec_floats(4));
 };
 
 // Every array read or written as float4 is 16-byte aligned explicitly.
 template <int DK, int DV>
 struct StreamTail {
-    static constexpr int HB = StreamCfg<DK, DV>::HB;
     alignas(16) uint64_t full[StreamCfg<DK, DV>::NS];
-    alignas(16) float qk[HB][2][DK];      // normalised q (0) and k (1) per unit of the batch
-    alignas(16) float vs[HB][DV];         // conv'd v per head of the batch
-    alignas(16) float zs[HB][DV];         // SiLU(z) per head of the batch
+    alignas(16) uint64_t rfull[2];
+    alignas(16) float rec[2][StreamCfg<DK, DV>::RECBUF];   // records of the current / next batch
     alignas(16) float red_p[StreamCfg<DK, DV>::RPP][DV];
     alignas(16) float red_s[StreamCfg<DK, DV>::RPP][DV];
     alignas(16) float up[DV];
     alignas(16) float nw[DV];
-    float gate_a[HB], gate_b[HB];
-    float ssq[HB][2];                     // |q|^2, |k|^2 per unit
-    float kq[HB];
     float npart[4];
-    int uslot[HB];
+    int rec_bad;
 };
 
 template <int DK, int DV>
@@ -264,7 +301,7 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
-template <int DK, int DV, typename TA, typename TOut>
+template <int DK, int DV, typename TOut>
 __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) {
     using Cfg = StreamCfg<DK, DV>;
     constexpr int NT = Cfg::NT, LPR = Cfg::LPR, RPP = Cfg::RPP, RPT = Cfg::RPT, NS = Cfg::NS;
@@ -276,16 +313,21 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = d.grp;                 // 1, 2 or 4: HB % G == 0
+    const DecRec R(DK, DV, G);
     const int n_units = a.n * d.hk;
     if ((int)blockIdx.x >= n_units) return;
     const int my_units = (n_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     const int n_items = my_units * G;
+    const int nub = HB / G;              // units per batch
+    const int n_batches = (n_items + HB - 1) / HB;
     TOut *out = (TOut *)a.out;
     const int rg = tid / LPR, c4 = (tid % LPR) * 4;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) tc::mbar_init(tc::smem_u32(&tl.full[s]), 1);
+        for (int s = 0; s < 2; ++s) tc::mbar_init(tc::smem_u32(&tl.rfull[s]), 1);
         tc::mbar_fence_init();
+        tl.rec_bad = 0;
     }
     for (int j = tid; j < DV; j += NT) tl.nw[j] = a.norm_w[j];
     __syncthreads();
@@ -306,104 +348,54 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
         tc::mbar_arrive_expect_tx(mb, Cfg::SLOT);
         for (int c = 0; c < Cfg::SLOT; c += Cfg::CHUNK) tc::bulk_g2s(dst + c, src + c, Cfg::CHUNK, mb);
     };
+    // producer (thread 0): bulk-load the records of batch bb into buffer bb & 1
+    auto issue_rec = [&](int bb) {
+        if (bb >= n_batches) return;
+        const uint32_t mb = tc::smem_u32(&tl.rfull[bb & 1]);
+        int cnt = 0;
+        for (int k = 0; k < nub; ++k) cnt += (bb * nub + k < my_units) ? 1 : 0;
+        tc::mbar_arrive_expect_tx(mb, (uint32_t)(cnt * R.size * 4));
+        for (int k = 0; k < nub; ++k) {
+            const int uu = bb * nub + k;
+            if (uu >= my_units) break;
+            const int u = (int)blockIdx.x + uu * (int)gridDim.x;
+            tc::bulk_g2s(tc::smem_u32(&tl.rec[bb & 1][k * R.size]), a.ws + (long long)u * R.size,
+                         (uint32_t)(R.size * 4), mb);
+        }
+    };
+    // The state ring does not depend on the prep kernel: start it, then wait
+    // for the prep grid (a no-op when launched without programmatic
+    // serialisation) before the first record copy.
     if (tid == 0)
         for (int it = 0; it < NS && it < n_items; ++it) issue(it);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) issue_rec(0);
 
     bool timed_out = false;
     for (int it = 0; it < n_items; ++it) {
-        const int hb = it % HB;
+        const int hb = it % HB, bb = it / HB;
         if (hb == 0) {
-            // ---- batch prologue for heads it .. it+HB-1 (units it/G .. (it+HB-1)/G)
-            __syncthreads();   // the previous batch's inputs are no longer read
-            const int ub0 = it / G, nub = HB / G;
-            const int nch = 2 * DK + G * DV;
-            for (int idx = tid; idx < nub * nch; idx += NT) {
-                const int ub = idx / nch, ci = idx % nch;
-                const int uu = ub0 + ub;
-                if (uu >= my_units) continue;
-                const int u = (int)blockIdx.x + uu * (int)gridDim.x;
-                const int n = u / d.hk, kh = u % d.hk;
-                const int slot = a.state_idx ? a.state_idx[n] : n;
-                if (slot < 0 || slot >= d.n_slots) continue;
-                int c;
-                if (ci < DK) c = kh * DK + ci;
-                else if (ci < 2 * DK) c = d.hk * DK + kh * DK + (ci - DK);
-                else c = 2 * d.hk * DK + kh * G * DV + (ci - 2 * DK);
-                const TA *x = (const TA *)a.x + (long long)n * a.ld_x;
-                const TA *w = (const TA *)a.conv_w;
-                TA *hc = (TA *)a.conv_state + ((long long)slot * d.ch + c) * 3;
-                TA h0 = hc[0], h1 = hc[1], h2 = hc[2], xc = x[c];
-                float acc = to_f32(w[c * 4 + 0]) * to_f32(h0) + to_f32(w[c * 4 + 1]) * to_f32(h1) +
-                            to_f32(w[c * 4 + 2]) * to_f32(h2) + to_f32(w[c * 4 + 3]) * to_f32(xc);
-                hc[0] = h1;
-                hc[1] = h2;
-                hc[2] = xc;
-                const float val = silu_f(acc);
-                if (ci < 2 * DK) tl.qk[ub][ci / DK][ci % DK] = val;
-                else tl.vs[ub * G + (ci - 2 * DK) / DV][(ci - 2 * DK) % DV] = val;
-            }
-            for (int idx = tid; idx < HB * DV; idx += NT) {   // SiLU(z) of the batch's heads
-                const int hbi = idx / DV, j = idx % DV;
-                const int uu = ub0 + hbi / G;
-                if (uu >= my_units) continue;
-                const int u = (int)blockIdx.x + uu * (int)gridDim.x;
-                const int n = u / d.hk, h = (u % d.hk) * G + hbi % G;
-                const TA *z = (const TA *)a.z + (long long)n * a.ld_z + (long long)h * DV;
-                tl.zs[hbi][j] = silu_f(to_f32(z[j]));
-            }
-            if (tid < HB) {
-                const int uu = ub0 + tid / G;
-                float ga = 0.f, gb = 0.f;
-                if (uu < my_units) {
-                    const int u = (int)blockIdx.x + uu * (int)gridDim.x;
-                    const int n = u / d.hk, h = (u % d.hk) * G + tid % G;
-                    const TA *uv = (const TA *)a.u + (long long)n * a.ld_ub;
-                    const TA *bv = (const TA *)a.b_logit + (long long)n * a.ld_ub;
-                    const float gg = -expf(a.A_log[h]) * softplus_f(to_f32(uv[h]) + a.dt_bias[h]);
-                    ga = expf(gg);
-                    gb = sigmoid_f(to_f32(bv[h]));
+            // Thread 0 refills the other record buffer (every thread is done with
+            // batch bb-1's records) and waits for this batch's; a wait that gives
+            // up marks every later record bad, for all threads alike.
+            __syncthreads();
+            if (tid == 0) {
+                tc::fence_async_smem();
+                issue_rec(bb + 1);
+                if (!tl.rec_bad && !tc::mbar_wait(tc::smem_u32(&tl.rfull[bb & 1]), (uint32_t)((bb >> 1) & 1))) {
+                    tl.rec_bad = 1;
+                    set_error(a.err, GDN_DEVERR_TIMEOUT);
                 }
-                tl.gate_a[tid] = ga;
-                tl.gate_b[tid] = gb;
-            }
-            if (tid < nub) {
-                const int uu = ub0 + tid;
-                int slot = -1;
-                if (uu < my_units) {
-                    const int u = (int)blockIdx.x + uu * (int)gridDim.x;
-                    slot = slot_of(a.state_idx, u / d.hk, d.n_slots, a.err);
-                }
-                tl.uslot[tid] = slot;
-            }
-            __syncthreads();
-            if (warp < 2 * nub) {    // |q|^2 and |k|^2 of each unit, one warp per vector
-                const float *vec = tl.qk[warp >> 1][warp & 1];
-                float ss = 0.f;
-                for (int i = lane; i < DK; i += 32) ss += vec[i] * vec[i];
-                ss = warp_sum(ss);
-                if (lane == 0) tl.ssq[warp >> 1][warp & 1] = ss;
-            }
-            __syncthreads();
-            for (int idx = tid; idx < nub * 2 * DK; idx += NT) {
-                const int ub = idx / (2 * DK), part = (idx / DK) & 1, i = idx % DK;
-                float f = rsqrtf(tl.ssq[ub][part] + d.l2_eps);
-                if (part == 0) f *= d.q_scale;
-                tl.qk[ub][part][i] *= f;
-            }
-            __syncthreads();
-            if (warp < nub) {
-                float kq = 0.f;
-                for (int i = lane; i < DK; i += 32) kq += tl.qk[warp][0][i] * tl.qk[warp][1][i];
-                kq = warp_sum(kq);
-                if (lane == 0) tl.kq[warp] = kq;
             }
             __syncthreads();
         }
         const int ub = hb / G, gi = it % G;
+        const float *rc = &tl.rec[bb & 1][ub * R.size];
         const int u = (int)blockIdx.x + (it / G) * (int)gridDim.x;
         const int n = u / d.hk, kh = u % d.hk, h = kh * G + gi;
         const long long out_row = (long long)n * d.hv * DV;
-        const int slot = tl.uslot[ub];
+        const int rslot = __float_as_int(rc[R.slot]);
+        const int slot = (tl.rec_bad || rslot >= d.n_slots) ? -1 : rslot;
         // ---- this head's state has arrived?
         if (!timed_out && !tc::mbar_wait(tc::smem_u32(&tl.full[it % NS]), (uint32_t)((it / NS) & 1))) {
             timed_out = true;
@@ -417,8 +409,8 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
 #pragma unroll
             for (int x = 0; x < RPT; ++x) {
                 m[x] = *reinterpret_cast<const float4 *>(Ms + (rg + x * RPP) * DV + c4);
-                kr[x] = tl.qk[ub][1][rg + x * RPP];
-                qr[x] = tl.qk[ub][0][rg + x * RPP];
+                kr[x] = rc[R.k + rg + x * RPP];
+                qr[x] = rc[R.q + rg + x * RPP];
             }
             float4 pp = make_float4(0.f, 0.f, 0.f, 0.f), ss = pp;
 #pragma unroll
@@ -438,7 +430,7 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
             for (int j = tid; j < DV; j += NT) out[out_row + (long long)h * DV + j] = from_f32<TOut>(0.f);
             continue;
         }
-        const float ga = tl.gate_a[hb], gb = tl.gate_b[hb];
+        const float ga = rc[R.ga + gi], gb = rc[R.gb + gi];
         float ov = 0.f;
         if (tid < DV) {
             float p = 0.f, s2 = 0.f;
@@ -447,9 +439,9 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
                 p += tl.red_p[r][tid];
                 s2 += tl.red_s[r][tid];
             }
-            const float uu = gb * (tl.vs[hb][tid] - ga * p);
+            const float uu = gb * (rc[R.v + gi * DV + tid] - ga * p);
             tl.up[tid] = uu;
-            ov = ga * s2 + uu * tl.kq[ub];
+            ov = ga * s2 + uu * rc[R.kq];
         }
         __syncthreads();  // (B)
         {
@@ -473,21 +465,35 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
 #pragma unroll
             for (int wi = 0; wi < DV / 32; ++wi) tot += tl.npart[wi];
             const float rs = rsqrtf(tot / (float)DV + d.norm_eps);
-            out[out_row + (long long)h * DV + tid] = from_f32<TOut>(ov * rs * tl.nw[tid] * tl.zs[hb][tid]);
+            out[out_row + (long long)h * DV + tid] =
+                from_f32<TOut>(ov * rs * tl.nw[tid] * rc[R.z + gi * DV + tid]);
         }
     }
 }
 
 template <int DK, int DV, typename TA, typename TOut>
 static cudaError_t launch_stream_t(const DecodeArgs &a, cudaStream_t s) {
-    auto kern = decode_stream_kernel<DK, DV, TA, TOut>;
-    constexpr size_t smem = stream_smem_bytes<DK, DV>();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     const int units = a.n * a.d.hk;
-    const int grid = units < sm_count() ? units : sm_count();
-    kern<<<grid, 4 * DV, smem, s>>>(a);
-    return cudaGetLastError();
+    decode_prep_kernel<DK, DV, TA><<<units, 256, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto kern = decode_stream_kernel<DK, DV, TOut>;
+    constexpr size_t smem = stream_smem_bytes<DK, DV>();
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // programmatic dependent launch: overlaps this kernel's launch and its
+    // first state copies with the tail of the prep kernel
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(units < sm_count() ? units : sm_count());
+    lc.blockDim = dim3(4 * DV);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kern, a);
 }
 
 template <int DK, int DV, typename TA, typename TOut>
@@ -496,7 +502,7 @@ static cudaError_t launch_dec_t(const DecodeArgs &a, bool fused, cudaStream_t s)
     if (fused)
         return launch_stream_t<DK, DV, TA, TOut>(a, s);
     else
-        decode_kernel<DK, DV, TA, TOut, false><<<grid, 4 * DV, 0, s>>>(a);
+        decode_kernel<DK, DV, TA, TOut><<<grid, 4 * DV, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -522,4 +528,11 @@ cudaError_t launch_decode(const DecodeArgs &a, bool fused, bool in_bf16, bool ou
     }
 }
 
+}  // namespace gdn
+
+namespace gdn {
+size_t decode_ws_bytes(const Dims &d, long long n_seqs) {
+    const DecRec R(d.dk, d.dv, d.grp);
+    return (size_t)(n_seqs > 0 ? n_seqs : 0) * d.hk * R.size * sizeof(float);
+}
 }  // namespace gdn

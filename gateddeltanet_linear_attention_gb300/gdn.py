@@ -86,7 +86,7 @@ def load(path: str | None = None):
                                      I32),
             "gdn_gated_rmsnorm": ([CP, P, I32, P, I64, P, I64, P, I32, V], I32),
             "gdn_mixer_prefill": ([CP, ctypes.POINTER(MixerIO), P, SZ, V], I32),
-            "gdn_mixer_decode": ([CP, ctypes.POINTER(MixerIO), V], I32),
+            "gdn_mixer_decode": ([CP, ctypes.POINTER(MixerIO), P, SZ, V], I32),
             "gdn_mixer_prefill_static": ([CP, ctypes.POINTER(MixerIO), V], I32),
             "gdn_device_error": ([V, ctypes.POINTER(U32)], I32),
             "gdn_status_string": ([I32], ctypes.c_char_p),
@@ -218,11 +218,13 @@ def gdn_mixer_prefill_static(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm
 
 
 def gdn_mixer_decode(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, state,
-                     conv_state, state_idx=None, stream=None):
+                     conv_state, workspace, state_idx=None, stream=None):
+    """workspace: a device byte tensor of gdn_workspace_size(cfg, n, n) bytes or more."""
     io = _mixer_io(x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, None, state, state,
                    conv_state, state_idx, y, x.shape[0])
-    _check(load().gdn_mixer_decode(ctypes.byref(cfg), ctypes.byref(io), _stream(stream)),
-           "gdn_mixer_decode")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_mixer_decode(ctypes.byref(cfg), ctypes.byref(io), _ptr(workspace), ws_bytes,
+                                   _stream(stream)), "gdn_mixer_decode")
 
 
 def gdn_device_error(stream=None) -> int:

@@ -208,8 +208,14 @@ gdn_status gdn_mixer_prefill_static(const gdn_config *cfg, const gdn_mixer_io *i
 
 /* Fused decode, a8: one token per sequence (io->T == io->n_seqs), conv history
  * and state updated in place (io->state_out must equal io->state_in and be
- * non-NULL; io->conv_state must be non-NULL).  Needs no workspace. */
-gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *stream);
+ * non-NULL; io->conv_state must be non-NULL).  Two launches: a per-(sequence,
+ * q/k head) prep kernel (conv step, SiLU, L2, gates, SiLU(z)) writes a small
+ * record per unit to `workspace` (DEVICE, caller-owned, 16-byte aligned, at
+ * least gdn_workspace_size(cfg, n_seqs, n_seqs) bytes, else GDN_ERR_WORKSPACE);
+ * a persistent kernel then streams every head state through shared memory
+ * once.  The workspace holds nothing between calls. */
+gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *workspace,
+                            size_t workspace_bytes, void *stream);
 
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device into *code (HOST pointer; GDN_DEVERR_* bits).  Returns

@@ -113,7 +113,13 @@ class GpuMixer:
 
     def decode(self, x, z, u, b):
         d = self.d
-        y = torch.empty((x.shape[0], self.wl.HV * self.wl.dv), dtype=self.y_dtype, device="cuda")
+        n = x.shape[0]
+        y = torch.empty((n, self.wl.HV * self.wl.dv), dtype=self.y_dtype, device="cuda")
+        if getattr(self, "_dec_ws", None) is None or self._dec_ws.numel() < gdn.gdn_workspace_size(
+                self.cfg, n, n):
+            self._dec_ws = torch.empty(gdn.gdn_workspace_size(self.cfg, n, n), dtype=torch.uint8,
+                                       device="cuda")
         gdn.gdn_mixer_decode(self.cfg, x, z, u, b, d["conv_w"], d["A_log"], d["dt_bias"],
-                             d["norm_w"], y, self.state, self.conv, state_idx=self.state_idx)
+                             d["norm_w"], y, self.state, self.conv, self._dec_ws,
+                             state_idx=self.state_idx)
         return y

@@ -123,14 +123,20 @@ def test_mixer_validation_and_workspace(lib):
     assert lib.gdn_mixer_prefill(ch, None, A16, need, None) == INVALID
     # decode: T must equal n_seqs, state in place and required, conv history required
     d = _io(T=4, n=4, state_in=A16, state_out=A16, conv_state=A16b)
+    dneed = lib.gdn_workspace_size(ch, 4, 4)
     bad = _io(T=5, n=4, state_in=A16, state_out=A16, conv_state=A16b)
-    assert lib.gdn_mixer_decode(ch, ctypes.byref(bad), None) == INVALID
+    assert lib.gdn_mixer_decode(ch, ctypes.byref(bad), A16, dneed, None) == INVALID
     bad = _io(T=4, n=4, state_in=A16, state_out=A16b, conv_state=A16b)
-    assert lib.gdn_mixer_decode(ch, ctypes.byref(bad), None) == INVALID
+    assert lib.gdn_mixer_decode(ch, ctypes.byref(bad), A16, dneed, None) == INVALID
     bad = _io(T=4, n=4, state_in=A16, state_out=A16, conv_state=None)
-    assert lib.gdn_mixer_decode(ch, ctypes.byref(bad), None) == INVALID
+    assert lib.gdn_mixer_decode(ch, ctypes.byref(bad), A16, dneed, None) == INVALID
     c0 = cfg(n_slots=0)
-    assert lib.gdn_mixer_decode(ctypes.byref(c0), ctypes.byref(d), None) == INVALID
+    assert lib.gdn_mixer_decode(ctypes.byref(c0), ctypes.byref(d), A16, dneed, None) == INVALID
+    # decode workspace: one record per (sequence, q/k head), missing / short / misaligned rejected
+    assert dneed >= 4 * 16 * (2 * 128 + 2 * 2 * 128) * 4
+    assert lib.gdn_mixer_decode(ch, ctypes.byref(d), None, 0, None) == WORKSPACE
+    assert lib.gdn_mixer_decode(ch, ctypes.byref(d), A16, 1024, None) == WORKSPACE
+    assert lib.gdn_mixer_decode(ch, ctypes.byref(d), MIS, dneed, None) == WORKSPACE
 
 
 def test_decode_and_norm_validation(lib):
