@@ -75,31 +75,46 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct PrefillWs {
     float *xa, *g, *beta, *o;
+    void *chunk;   // tensor-core chunk workspace (chunk map + [T ; PT] operands), or NULL
 };
 
-size_t prefill_ws_bytes(const gdn::Dims &d, long long T) {
-    size_t t = (size_t)(T > 0 ? T : 0);
-    return align256(t * d.ch * 4) + 2 * align256(t * d.hv * 4) + align256(t * d.hv * d.dv * 4);
+// The chunked rule: bf16-activation configurations with dk = dv = 128 and
+// 64-token chunks run on the tensor cores (split-bf16 operands); everything
+// else, and the fp32-activation mode, runs the exact fp32 SIMT kernel.
+bool uses_tc(const gdn::Dims &d, bool act_bf16) { return act_bf16 && gdn::chunk_tc_supported(d); }
+
+size_t chunk_ws_bytes(const gdn::Dims &d, bool act_bf16, long long T, long long n_seqs) {
+    return uses_tc(d, act_bf16) ? gdn::chunk_tc_ws_bytes(d, T, n_seqs) : 0;
 }
 
-PrefillWs carve_prefill(const gdn::Dims &d, long long T, void *ws) {
+// The tensor-core path launches one CTA per (chunk, v-head) in a 1-D grid.
+bool tc_grid_fits(const gdn::Dims &d, bool act_bf16, long long T, long long n_seqs) {
+    return !uses_tc(d, act_bf16) || gdn::chunk_tc_max_chunks(T, n_seqs) * d.hv <= 0x7fffffffLL;
+}
+
+size_t prefill_ws_bytes(const gdn::Dims &d, bool act_bf16, long long T, long long n_seqs) {
+    size_t t = (size_t)(T > 0 ? T : 0);
+    return align256(t * d.ch * 4) + 2 * align256(t * d.hv * 4) + align256(t * d.hv * d.dv * 4) +
+           align256(chunk_ws_bytes(d, act_bf16, T, n_seqs));
+}
+
+PrefillWs carve_prefill(const gdn::Dims &d, bool act_bf16, long long T, long long n_seqs, void *ws) {
     size_t t = (size_t)T;
     char *p = (char *)ws;
     PrefillWs w;
     w.xa = (float *)p; p += align256(t * d.ch * 4);
     w.g = (float *)p; p += align256(t * d.hv * 4);
     w.beta = (float *)p; p += align256(t * d.hv * 4);
-    w.o = (float *)p;
+    w.o = (float *)p; p += align256(t * d.hv * d.dv * 4);
+    w.chunk = chunk_ws_bytes(d, act_bf16, T, n_seqs) ? (void *)p : nullptr;
     return w;
 }
 
-// The chunked rule: bf16-activation configurations with dk = dv = 128 and
-// 64-token chunks run on the tensor cores (split-bf16 operands); everything
-// else, and the fp32-activation mode, runs the exact fp32 SIMT kernel.  Each
-// tensor-core CTA owns a 32-column slice of one head's state.
+// Each tensor-core CTA owns a 32-column slice of one head's state; the chunk
+// workspace `ws` must already be carved into `a` (chunk_tc_carve).
 cudaError_t launch_chunk(const gdn::ChunkArgs &a, bool act_bf16, bool in_bf16, bool o_bf16,
                          cudaStream_t s) {
-    if (act_bf16 && gdn::chunk_tc_supported(a.d)) return gdn::launch_chunk_tc(a, in_bf16, o_bf16, 32, s);
+    if (uses_tc(a.d, act_bf16)) return gdn::launch_chunk_tc(a, in_bf16, o_bf16, 32, s);
     return gdn::launch_chunk_simt(a, in_bf16, o_bf16, s);
 }
 
@@ -137,7 +152,8 @@ const char *gdn_status_string(gdn_status s) {
 size_t gdn_workspace_size(const gdn_config *cfg, int64_t max_tokens, int32_t max_seqs) {
     gdn::Dims d;
     if (check_cfg(cfg, &d) != GDN_OK || max_tokens < 0 || max_seqs < 0) return 0;
-    const size_t pre = prefill_ws_bytes(d, max_tokens), dec = gdn::decode_ws_bytes(d, max_seqs);
+    const size_t pre = prefill_ws_bytes(d, cfg->act == GDN_BF16, max_tokens, max_seqs),
+                 dec = gdn::decode_ws_bytes(d, max_seqs);
     return (pre > dec ? pre : dec) + 256;
 }
 
@@ -211,8 +227,6 @@ gdn_status gdn_chunk_prefill(const gdn_config *cfg, const void *q, const void *k
                              int64_t T, const float *state_in, float *state_out,
                              const int32_t *state_idx, void *o, gdn_dtype o_dtype, uint32_t flags,
                              void *workspace, size_t workspace_bytes, void *stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     gdn::Dims d;
     gdn_status st = check_cfg(cfg, &d);
     if (st != GDN_OK) return st;
@@ -229,14 +243,20 @@ gdn_status gdn_chunk_prefill(const gdn_config *cfg, const void *q, const void *k
     if ((state_in && !aligned16(state_in)) || (state_out && !aligned16(state_out)))
         return GDN_ERR_INVALID_ARG;
     if ((state_in || state_out) && d.n_slots == 0) return GDN_ERR_INVALID_ARG;
+    const bool bf = cfg->act == GDN_BF16;
+    if (!tc_grid_fits(d, bf, T, n_seqs)) return GDN_ERR_UNSUPPORTED;
+    const size_t need = chunk_ws_bytes(d, bf, T, n_seqs);
+    if (need && (!workspace || !aligned16(workspace) || workspace_bytes < need))
+        return GDN_ERR_WORKSPACE;
     unsigned *err = nullptr;
     if ((st = error_word(&err)) != GDN_OK) return st;
-    gdn::ChunkArgs a;
+    gdn::ChunkArgs a = {};
     a.q = q; a.k = k; a.v = v; a.ld_qk = ld_qk; a.ld_v = ld_v; a.g = g; a.beta = beta;
     a.cu_seqlens = cu_seqlens; a.n_seqs = n_seqs; a.T = T; a.state_in = state_in;
     a.state_out = state_out; a.state_idx = state_idx; a.o = o; a.flags = flags; a.d = d;
     a.err = err;
-    return launch_status(launch_chunk(a, cfg->act == GDN_BF16, in_dtype == GDN_BF16,
+    if (need) gdn::chunk_tc_carve(a, workspace);
+    return launch_status(launch_chunk(a, bf, in_dtype == GDN_BF16,
                                       o_dtype == GDN_BF16, (cudaStream_t)stream));
 }
 
@@ -324,11 +344,13 @@ gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void
         a.o = io->y; a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
         return launch_status(launch_chunk(a, cfg->act == GDN_BF16, false, false, s));
     }
-    if (!workspace || !aligned16(workspace) || workspace_bytes < prefill_ws_bytes(d, io->T))
+    const bool bf = cfg->act == GDN_BF16;
+    if (!tc_grid_fits(d, bf, io->T, io->n_seqs)) return GDN_ERR_UNSUPPORTED;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < prefill_ws_bytes(d, bf, io->T, io->n_seqs))
         return GDN_ERR_WORKSPACE;
     if ((st = error_word(&err)) != GDN_OK) return st;
-    const bool bf = cfg->act == GDN_BF16;
-    PrefillWs w = carve_prefill(d, io->T, workspace);
+    PrefillWs w = carve_prefill(d, bf, io->T, io->n_seqs, workspace);
     cudaError_t e = gdn::launch_gate_prep(d, bf, io->u, io->b_logit, io->ld_ub, io->T, io->A_log,
                                           io->dt_bias, w.g, w.beta, s);
     if (e == cudaSuccess)
@@ -339,7 +361,7 @@ gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void
         e = gdn::launch_conv_state_update(d, bf, io->x, io->ld_x, io->cu_seqlens, io->n_seqs,
                                           io->T, io->conv_state, io->state_idx, err, s);
     if (e == cudaSuccess) {
-        gdn::ChunkArgs a;
+        gdn::ChunkArgs a = {};
         a.q = w.xa;
         a.k = w.xa + (long long)d.hk * d.dk;
         a.v = w.xa + 2LL * d.hk * d.dk;
@@ -347,6 +369,7 @@ gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void
         a.cu_seqlens = io->cu_seqlens; a.n_seqs = io->n_seqs; a.T = io->T;
         a.state_in = io->state_in; a.state_out = io->state_out; a.state_idx = io->state_idx;
         a.o = w.o; a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
+        if (w.chunk) gdn::chunk_tc_carve(a, w.chunk);
         e = launch_chunk(a, bf, false, false, s);
     }
     if (e == cudaSuccess)

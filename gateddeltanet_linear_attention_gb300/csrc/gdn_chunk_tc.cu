@@ -1,15 +1,29 @@
 // gdn_chunk_tc.cu -- chunked gated delta rule on the 5th-generation tensor
 // cores (tcgen05, accumulators in TMEM), for dk = dv = 128 and 64-token chunks.
 //
-// Chunk algebra (as in the fp32 SIMT kernel; M = S^T is dk x dv, G the
-// in-chunk cumulative log-decay, gamma = exp(G), chunks restart at every
-// sequence start since they are relative to each invocation -- hyperflare
-// core-design, GDN numerics paragraph):
-//   A  = strict_lower(diag(beta) (K K^T o Gamma)),  T = (I + A)^-1
+// Chunk algebra (M = S^T is dk x dv, G the in-chunk cumulative log-decay,
+// gamma = exp(G), chunks restart at every sequence start since they are
+// relative to each invocation -- hyperflare core-design, GDN numerics
+// paragraph; the WY / UT form of the chunked delta rule):
+//   A  = strict_lower(diag(beta) (K K^T o Gamma)),  T = (I + A)^-1,  P = Q K^T o Gamma
 //   W  = T diag(beta gamma) K,  U = T diag(beta) V
 //   U' = U - W M
-//   O  = diag(gamma) Q M + (Q K^T o Gamma) U'
+//   O  = diag(gamma) Q M + P U'  =  (gamma Q - P W) M + P U
 //   M <- gamma_last M + (diag(exp(G_last - G)) K)^T U'
+//
+// Two kernels split the work by what depends on the carried state.
+//  * chunk_tp_kernel, parallel over every (chunk, v-head): the Gram products
+//    [K;Q] K^T on the tensor cores, A and P, the 64x64 inverse T in fp32 on
+//    the SIMT pipes (16x16 diagonal blocks by forward substitution, then
+//    block columns), and PT = P T on the tensor cores.  It writes [T ; PT] as
+//    a ready-made bf16 hi/lo MMA operand (32 KB) to the workspace.
+//  * chunk_chain_kernel, one CTA per (sequence, v-head, slice of DVS state
+//    columns), walks the chunks in order with three MMA groups per chunk:
+//      G2  D2 = [T ; PT] . [bgK | bV]  -> W, PW (cols 0-127) and U, PU (D3)
+//      G3  D3 += [-W ; gQ - PW] . M    -> U' (TMEM lanes 0-63), O (lanes 64-127)
+//      G5  D5 = K~^T . U'              -> the state increment
+//    The [T ; PT] operand of the next chunk is bulk-copied while the current
+//    one runs.
 //
 // Precision.  The gated RMSNorm that follows divides every token-head by the
 // RMS of its own o, so on quiet tokens absolute errors in o are amplified up
@@ -19,21 +33,9 @@
 // 2^-16 relative), with fp32 accumulation in TMEM and the state kept in fp32
 // registers.
 //
-// Work decomposition: one CTA (256 threads) per (sequence, v-head, slice of
-// DVS state columns); the columns of M evolve independently, so slices only
-// duplicate the dv-independent products.  Per chunk, five MMA groups, all
-// M = 128 (64-row problems are stacked or padded):
-//   G1  D1 = [K ; Q] . K^T               -> K K^T (TMEM lanes 0-63), Q K^T (64-127)
-//   G2  D2 = [T ; P] . [bgK | bV]        -> W (cols 0-127) | U on lanes 0-63
-//   G3  D3 = [W ; gQ] . M                -> W M (lanes 0-63), gamma Q M (64-127)
-//   G4  D3 += [T ; P] . U'               -> lanes 64-127 become O
-//   G5  D5 = K~^T . U'                   -> the state increment
 // Operands whose contraction index is the token or the dk row (bgK|bV, K~,
-// M, U') are stored MN-major, so that every operand is written from its
-// natural row layout with 16-byte stores.  The triangular inverse T is formed
-// in fp32 on the SIMT pipes (four 16x16 diagonal blocks by forward
-// substitution in registers, then block rows), with T kept transposed in the
-// unused upper triangle of A.
+// M, U', T^T) are stored MN-major, so that every operand is written from its
+// natural row layout with 16-byte stores.
 #include "gdn_common.cuh"
 #include "tc_sm103.cuh"
 
@@ -44,28 +46,8 @@ namespace {
 constexpr int TC_NT = 256;
 constexpr int TC_C = 64;     // chunk
 constexpr int TC_DK = 128;   // dk == dv
-
-// Shared-memory map (bytes).  Every bf16 tile has a hi part and a lo part.
-template <int DVS>
-struct TcSmem {
-    static constexpr int NB = 128 + DVS;                   // N of G2's B operand
-    static constexpr int KQ = 128 * 128 * 2;               // [K;Q] -> [W;gQ], K-major, K = 128
-    static constexpr int BW = NB * 64 * 2;                 // [bgK|bV] MN-major (MN = NB, K = 64) -> K~ (MN = 128)
-    static constexpr int TP = 128 * 64 * 2;                // [T ; P], K-major, K = 64
-    static constexpr int MT = DVS * 128 * 2;               // M, MN-major (MN = DVS, K = 128)
-    static constexpr int UT = DVS * 64 * 2;                // U', MN-major (MN = DVS, K = 64)
-    static constexpr int OFF_KQ = 0;
-    static constexpr int OFF_BW = OFF_KQ + 2 * KQ;
-    static constexpr int OFF_TP = OFF_BW + 2 * BW;
-    static constexpr int OFF_MT = OFF_TP + 2 * TP;
-    static constexpr int OFF_UT = OFF_MT + 2 * MT;
-    static constexpr int OFF_SA = OFF_UT + 2 * UT;          // fp32 [64][65]: A below, T^T above the diagonal
-    static constexpr int OFF_GAM = OFF_SA + 64 * 65 * 4;    // fp32 [64][65]: exp(G_r - G_c), c <= r
-    static constexpr int OFF_X = OFF_GAM + 64 * 65 * 4;     // (reserved)
-    static constexpr int OFF_G = OFF_X + 16;                // G[64], beta[64]
-    static constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;      // mbarrier, tmem base, timeout flag
-    static constexpr int BYTES = OFF_BAR + 16;
-};
+constexpr int TP_HALF = 128 * 64 * 2;     // one bf16 part of [T ; PT] (K-major, K = 64)
+constexpr int TP_BYTES = 2 * TP_HALF;     // hi + lo, as stored in the workspace
 
 // Store 8 values at byte offset `off` (16-byte aligned) of a hi and a lo tile
 // (packed two-at-a-time conversions).
@@ -147,20 +129,29 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, float *v) {
     }
 }
 
-// Issue D (+)= A . B over Kdim in 16-wide steps with the three split
+// Issue D (+)= A . B over KDIM in 16-wide steps with the three split
 // products.  A_MN / B_MN select MN-major operands (with their MN extent).
-template <bool A_MN, bool B_MN>
+// Each descriptor is built once; a 16-wide K step only advances its start
+// address field (the low 14 bits hold address >> 4, and shared-memory
+// addresses stay below 2^18, so the addition never carries out of the field).
+template <bool A_MN, bool B_MN, int KDIM>
 __device__ __forceinline__ void mma3(uint32_t d_tmem, uint32_t a_hi, uint32_t a_lo, uint32_t a_mn,
-                                     uint32_t b_hi, uint32_t b_lo, uint32_t b_mn, int Kdim,
-                                     uint32_t idesc, bool accumulate) {
-    for (int k0 = 0; k0 < Kdim; k0 += 16) {
-        const uint64_t ah = A_MN ? tc::mnmaj_desc(a_hi, a_mn, k0) : tc::kmaj_desc(a_hi, Kdim, k0);
-        const uint64_t al = A_MN ? tc::mnmaj_desc(a_lo, a_mn, k0) : tc::kmaj_desc(a_lo, Kdim, k0);
-        const uint64_t bh = B_MN ? tc::mnmaj_desc(b_hi, b_mn, k0) : tc::kmaj_desc(b_hi, Kdim, k0);
-        const uint64_t bl = B_MN ? tc::mnmaj_desc(b_lo, b_mn, k0) : tc::kmaj_desc(b_lo, Kdim, k0);
-        tc::mma_bf16(d_tmem, ah, bh, idesc, (accumulate || k0 > 0) ? 1u : 0u);
-        tc::mma_bf16(d_tmem, ah, bl, idesc, 1u);
-        tc::mma_bf16(d_tmem, al, bh, idesc, 1u);
+                                     uint32_t b_hi, uint32_t b_lo, uint32_t b_mn, uint32_t idesc,
+                                     bool accumulate) {
+    const uint64_t ah = A_MN ? tc::mnmaj_desc(a_hi, a_mn, 0) : tc::kmaj_desc(a_hi, KDIM, 0);
+    const uint64_t al = A_MN ? tc::mnmaj_desc(a_lo, a_mn, 0) : tc::kmaj_desc(a_lo, KDIM, 0);
+    const uint64_t bh = B_MN ? tc::mnmaj_desc(b_hi, b_mn, 0) : tc::kmaj_desc(b_hi, KDIM, 0);
+    const uint64_t bl = B_MN ? tc::mnmaj_desc(b_lo, b_mn, 0) : tc::kmaj_desc(b_lo, KDIM, 0);
+    // start-address advance per 16-wide K step, in 16-byte units
+    const uint32_t as = A_MN ? (a_mn >> 3) * 2u * 8u : 16u;
+    const uint32_t bs = B_MN ? (b_mn >> 3) * 2u * 8u : 16u;
+#pragma unroll
+    for (int ks = 0; ks < KDIM / 16; ++ks) {
+        const uint64_t ahk = ah + (uint64_t)(ks * as), alk = al + (uint64_t)(ks * as);
+        const uint64_t bhk = bh + (uint64_t)(ks * bs), blk = bl + (uint64_t)(ks * bs);
+        tc::mma_bf16(d_tmem, ahk, bhk, idesc, (accumulate || ks > 0) ? 1u : 0u);
+        tc::mma_bf16(d_tmem, ahk, blk, idesc, 1u);
+        tc::mma_bf16(d_tmem, alk, bhk, idesc, 1u);
     }
 }
 
@@ -195,38 +186,374 @@ __device__ __forceinline__ void solve_block_col(float *sA, float (&tcol)[48], in
     }
 }
 
+
+// Shared pieces of the per-CTA setup: one thread polls the MMA barrier
+// (bounded) and the block agrees on the outcome, so a timeout leaves any loop
+// uniformly.
+struct MmaSync {
+    uint64_t *mbar;
+    volatile uint32_t *flag;
+    uint32_t phase;
+    __device__ bool wait(int tid, bool issued_ok = true) {
+        if (tid == 0) *flag = (issued_ok && tc::mbar_wait(tc::smem_u32(mbar), phase)) ? 0u : 1u;
+        __syncthreads();
+        const bool ok = *flag == 0u;
+        if (ok) phase ^= 1u;
+        tc::fence_after_sync();
+        return ok;
+    }
+};
+
+// generic shared-memory writes -> visible to the tensor core, block-wide
+__device__ __forceinline__ void sync_for_mma() {
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+}
+
+// L2 normalisation of a row held by 4 consecutive lanes (32 values each).
+__device__ __forceinline__ void l2norm_row4(float (&v)[32], float eps, float scale) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float f = rsqrtf(ss + eps) * scale;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= f;
+}
+
+// In-place inclusive scan of the 64 gate values in sG by warp 0 (2 per lane).
+__device__ __forceinline__ void scan64(float *sG, int lane) {
+    const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
+    const float pair = g0 + g1;
+    float inc = pair;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const float t2 = __shfl_up_sync(0xffffffffu, inc, o2);
+        if (lane >= o2) inc += t2;
+    }
+    sG[2 * lane] = inc - pair + g0;
+    sG[2 * lane + 1] = inc;
+}
+
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Chunk map: chunk_base[n] = number of 64-token chunks of sequences before n
+// (exclusive scan over the clamped lengths), chunk_base[n_seqs] = the total.
+__global__ void __launch_bounds__(1024) chunk_map_kernel(ChunkArgs a) {
+    __shared__ int wsum[32];
+    __shared__ int carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int b0 = 0; b0 < a.n_seqs; b0 += 1024) {
+        const int n = b0 + tid;
+        int nc = 0;
+        if (n < a.n_seqs) {
+            long long s, e;
+            seq_bounds(a.cu_seqlens, n, a.T, a.err, s, e);
+            nc = (int)((e - s + TC_C - 1) / TC_C);
+        }
+        int inc = nc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += t;
+        }
+        if (lane == 31) wsum[warp] = inc;
+        __syncthreads();
+        if (warp == 0) {
+            const int w = wsum[lane];
+            int wi = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += t;
+            }
+            wsum[lane] = wi - w;
+        }
+        __syncthreads();
+        const int excl = carry + wsum[warp] + inc - nc;
+        if (n < a.n_seqs) a.chunk_base[n] = excl;
+        __syncthreads();
+        if (tid == 1023) carry = excl + nc;
+        __syncthreads();
+    }
+    if (tid == 0) a.chunk_base[a.n_seqs] = carry;
+}
+
+// ---------------------------------------------------------------------------
+// [T ; PT] of one (chunk, v-head).  Shared memory: the [K;Q] hi/lo Gram
+// operand (64 KB); once G1 has consumed it, the same bytes hold the fp32 A
+// (T^T above the diagonal) and the bf16 operands of PT = P T (P, and T^T
+// as K-major rows).
+struct TpSmem {
+    static constexpr int KQ = 128 * 128 * 2;
+    static constexpr int OFF_KQ = 0;
+    static constexpr int OFF_SA = 0;                       // fp32 [64][65]
+    static constexpr int OPH = 64 * 64 * 2;                // one bf16 part of a 64x64 operand
+    static constexpr int OFF_P = (64 * 65 * 4 + 1023) & ~1023;  // P, K-major (M = 64, K = 64), hi + lo
+    static constexpr int OFF_B2 = OFF_P + 2 * OPH;         // B2[c][k] = T[k][c], K-major, hi + lo
+    static constexpr int OFF_G = 2 * KQ;                   // G[64], beta[64]
+    static constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;     // mbarrier, tmem slot, flag, search
+    static constexpr int BYTES = OFF_BAR + 32;
+    static_assert(OFF_P % 1024 == 0, "operand alignment");
+    static_assert(OFF_B2 + 2 * OPH <= 2 * KQ, "PT operands exceed the Gram region");
+};
+
+template <typename TIn>
+__global__ void __launch_bounds__(TC_NT) chunk_tp_kernel(ChunkArgs a) {
+    using L = TpSmem;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    unsigned char *kqh = sm + L::OFF_KQ, *kql = kqh + L::KQ;
+    float *sA = reinterpret_cast<float *>(sm + L::OFF_SA);
+    unsigned char *ph = sm + L::OFF_P, *pl = ph + L::OPH;
+    unsigned char *b2h = sm + L::OFF_B2, *b2l = b2h + L::OPH;
+    float *sG = reinterpret_cast<float *>(sm + L::OFF_G);
+    float *sB = sG + 64;
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 8);
+    volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 12);
+    int *sfind = reinterpret_cast<int *>(sm + L::OFF_BAR + 16);
+
+    const Dims &d = a.d;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = (int)(blockIdx.x % (unsigned)d.hv);
+    const long long j = blockIdx.x / (unsigned)d.hv;
+    const int kh = h / d.grp;
+    const int total = a.chunk_base[a.n_seqs];
+    if (j >= total || j >= a.max_chunks) return;
+
+    // ---- the sequence n with chunk_base[n] <= j < chunk_base[n+1] (256-way search)
+    int lo = 0, hi = a.n_seqs;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + TC_NT - 1) / TC_NT;
+        if (tid == 0) *sfind = lo;
+        __syncthreads();
+        const int p = lo + tid * step;
+        if (p < hi && a.chunk_base[p] <= j) atomicMax(sfind, p);
+        __syncthreads();
+        const int nlo = *sfind;
+        __syncthreads();
+        hi = min(nlo + step, hi);
+        lo = nlo;
+    }
+    long long s, e;
+    seq_bounds(a.cu_seqlens, lo, a.T, nullptr, s, e);   // malformed bounds are reported by the map
+    const long long t0 = s + (j - a.chunk_base[lo]) * TC_C;
+
+    if (warp == 0) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), 64);
+        tc::tmem_relinquish();
+    }
+    if (tid == 32) {
+        tc::mbar_init(tc::smem_u32(mbar), 1);
+        tc::mbar_fence_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = *tmem_slot;
+    MmaSync ms{mbar, wait_flag, 0u};
+    const int rr = tid >> 2, cq = tid & 3;
+    const int qd = warp & 3, hf = warp >> 2, tl = qd * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+
+    // ---- rows of K and Q (L2-normalised), gates
+    {
+        float kv[32], qv[32];
+        const long long t = t0 + rr;
+        if (t < e) {
+            load_row<32>((const TIn *)a.k + t * a.ld_qk + (long long)kh * TC_DK + cq * 32, kv);
+            load_row<32>((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK + cq * 32, qv);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
+        }
+        if (a.flags & GDN_FLAG_L2NORM_QK) {
+            l2norm_row4(kv, d.l2_eps, 1.f);
+            l2norm_row4(qv, d.l2_eps, d.q_scale);
+        }
+#pragma unroll
+        for (int k8 = 0; k8 < 32; k8 += 8) {
+            put8(kqh, kql, tc::kmaj_off(rr, cq * 32 + k8, 128), &kv[k8]);
+            put8(kqh, kql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), &qv[k8]);
+        }
+        if (tid < TC_C) {
+            const long long tt = t0 + tid;
+            sG[tid] = tt < e ? a.g[tt * d.hv + h] : 0.f;
+            sB[tid] = tt < e ? a.beta[tt * d.hv + h] : 0.f;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) scan64(sG, lane);
+    sync_for_mma();
+    // ---- G1: [K;Q] K^T -> K K^T (TMEM lanes 0-63), Q K^T (64-127)
+    if (tid == 0) {
+        mma3<false, false, 128>(tbase, tc::smem_u32(kqh), tc::smem_u32(kql), 0, tc::smem_u32(kqh),
+                                tc::smem_u32(kql), 0, tc::idesc_bf16(128, 64), false);
+        tc::mma_commit(tc::smem_u32(mbar));
+    }
+    bool ok = ms.wait(tid);
+    if (ok) {
+        // ---- E1: A (strictly lower, fp32) and P (lower incl. the diagonal, bf16 hi/lo
+        // operand), over the Gram region
+        float v32[32];
+        tc::tmem_ld32(tbase + lane_off + hf * 32, v32);
+        const int r = tl & 63;
+        const float Gr = sG[r];
+        if (qd < 2) {
+            const float br = sB[r];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = hf * 32 + i;
+                if (c < r) sA[r * 65 + c] = br * expf(Gr - sG[c]) * v32[i];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = hf * 32 + i;
+                v32[i] = (c <= r) ? expf(Gr - sG[c]) * v32[i] : 0.f;
+            }
+#pragma unroll
+            for (int k8 = 0; k8 < 32; k8 += 8) put8(ph, pl, tc::kmaj_off(r, hf * 32 + k8, 64), &v32[k8]);
+        }
+        __syncthreads();
+        // ---- T = (I + A)^-1: diagonal 16x16 blocks (column `lane` of block `warp`)
+        if (warp < 4 && lane < 16) {
+            const int b0 = warp * 16, c = lane;
+            float col[16];
+#pragma unroll
+            for (int rw = 0; rw < 16; ++rw) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (i < rw) acc += sA[(b0 + rw) * 65 + b0 + i] * col[i];
+                col[rw] = (rw == c) ? 1.f : ((rw > c) ? -acc : 0.f);
+            }
+#pragma unroll
+            for (int rw = 0; rw < 16; ++rw)
+                if (rw > c) sA[(b0 + c) * 65 + b0 + rw] = col[rw];   // T[b0+rw][b0+c], transposed
+        }
+        __syncthreads();
+        // off-diagonal blocks, one warp per block column bj
+        if (warp < 3) {
+            const int bj = warp, c = lane & 15, rh = lane >> 4;
+            const int m = bj * 16 + c;
+            float tcol[48];
+#pragma unroll
+            for (int k = 0; k < 48; ++k) {
+                const int row = bj * 16 + k;
+                tcol[k] = (k < 16) ? ((row > m) ? sA[m * 65 + row] : ((row == m) ? 1.f : 0.f)) : 0.f;
+            }
+            solve_block_col<1>(sA, tcol, bj, m, rh);
+            solve_block_col<2>(sA, tcol, bj, m, rh);
+            solve_block_col<3>(sA, tcol, bj, m, rh);
+        }
+        __syncthreads();
+        // ---- T's rows -> the workspace (rows 0-63 of [T ; PT]); B2 = T^T rows (B2[c][k] = T[k][c])
+        unsigned char *gout = a.tp + ((long long)j * d.hv + h) * TP_BYTES;
+        for (int task = tid; task < 64 * 8; task += TC_NT) {
+            // consecutive tasks -> consecutive 16-byte rows of one core-matrix block
+            const int r2 = (task >> 6) * 8 + (task & 7), c8 = ((task >> 3) & 7) * 8;
+            float t8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = c8 + i;
+                t8[i] = (c < r2) ? sA[c * 65 + r2] : ((c == r2) ? 1.f : 0.f);
+            }
+            put8(gout, gout + TP_HALF, tc::kmaj_off(r2, c8, 64), t8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = c8 + i;
+                t8[i] = (k > r2) ? sA[r2 * 65 + k] : ((k == r2) ? 1.f : 0.f);
+            }
+            put8(b2h, b2l, tc::kmaj_off(r2, c8, 64), t8);
+        }
+        sync_for_mma();
+        // ---- G: P . T (M = 64): row r of PT lands on TMEM lane 32*(r/16) + r%16
+        if (tid == 0) {
+            mma3<false, false, 64>(tbase, tc::smem_u32(ph), tc::smem_u32(pl), 0, tc::smem_u32(b2h),
+                                   tc::smem_u32(b2l), 0, tc::idesc_bf16(64, 64), false);
+            tc::mma_commit(tc::smem_u32(mbar));
+        }
+        ok = ms.wait(tid);
+        if (ok) {
+            tc::tmem_ld32(tbase + lane_off + hf * 32, v32);
+            if (lane < 16) {
+                const int r2 = qd * 16 + lane;
+#pragma unroll
+                for (int k8 = 0; k8 < 32; k8 += 8)
+                    put8(gout, gout + TP_HALF, tc::kmaj_off(64 + r2, hf * 32 + k8, 64), &v32[k8]);
+            }
+        }
+    }
+    if (!ok) {
+        if (tid == 0) {
+            set_error(a.err, GDN_DEVERR_TIMEOUT);
+            tc::mbar_wait(tc::smem_u32(mbar), ms.phase);
+        }
+        __syncthreads();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tbase, 64);
+}
+
+// ---------------------------------------------------------------------------
+// The state chain.  Shared-memory map (bytes); every bf16 tile has a hi and a
+// lo part.
+template <int DVS>
+struct ChainSmem {
+    static constexpr int NB = 128 + DVS;                   // N of G2's B operand
+    static constexpr int WQ = 128 * 128 * 2;               // [-W ; Q'] K-major, K = 128
+    static constexpr int BW = NB * 64 * 2;                 // [bgK | bV] MN-major (MN = NB, K = 64)
+    static constexpr int KT = 128 * 64 * 2;                // K~ MN-major (MN = 128, K = 64)
+    static constexpr int MT = DVS * 128 * 2;               // M MN-major (MN = DVS, K = 128)
+    static constexpr int UT = DVS * 64 * 2;                // U' MN-major (MN = DVS, K = 64)
+    static constexpr int OFF_WQ = 0;
+    static constexpr int OFF_BW = OFF_WQ + 2 * WQ;
+    static constexpr int OFF_KT = OFF_BW + 2 * BW;
+    static constexpr int OFF_TP = OFF_KT + 2 * KT;         // [T ; PT], bulk-copied (hi then lo)
+    static constexpr int OFF_MT = OFF_TP + TP_BYTES;
+    static constexpr int OFF_UT = OFF_MT + 2 * MT;
+    static constexpr int OFF_G = OFF_UT + 2 * UT;          // G[64], beta[64]
+    static constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;     // MMA barrier, copy barrier, tmem slot, flag
+    static constexpr int BYTES = OFF_BAR + 32;
+    static_assert(OFF_TP % 16 == 0, "bulk-copy destination alignment");
+};
+
 template <int DVS, typename TIn, typename TOut>
-__global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
-    using L = TcSmem<DVS>;
+__global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
+    using L = ChainSmem<DVS>;
     constexpr int HALF = DVS / 2;                 // state columns per thread in lane mapping
     constexpr int VQ = DVS / 4;                   // v columns per thread in row mapping
     constexpr int NB = L::NB;
     extern __shared__ __align__(1024) unsigned char sm[];
-    unsigned char *kqh = sm + L::OFF_KQ, *kql = kqh + L::KQ;
+    unsigned char *wqh = sm + L::OFF_WQ, *wql = wqh + L::WQ;
     unsigned char *bwh = sm + L::OFF_BW, *bwl = bwh + L::BW;
-    unsigned char *tph = sm + L::OFF_TP, *tpl = tph + L::TP;
+    unsigned char *kth = sm + L::OFF_KT, *ktl = kth + L::KT;
+    unsigned char *tph = sm + L::OFF_TP, *tpl = tph + TP_HALF;
     unsigned char *mth = sm + L::OFF_MT, *mtl = mth + L::MT;
     unsigned char *uth = sm + L::OFF_UT, *utl = uth + L::UT;
-    float *sA = reinterpret_cast<float *>(sm + L::OFF_SA);     // [64][65]
-    float *sGam = reinterpret_cast<float *>(sm + L::OFF_GAM);  // [64][65]
-    float *sG = reinterpret_cast<float *>(sm + L::OFF_G);      // [64]
-    float *sB = sG + 64;                                        // [64]
+    float *sG = reinterpret_cast<float *>(sm + L::OFF_G);
+    float *sB = sG + 64;
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 8);
-    volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 12);
+    uint64_t *tpbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR + 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 16);
+    volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 20);
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int kh = h / d.grp;
     const int col0 = h * TC_DK + slice * DVS;      // this slice's first column in o / v / state
-    // row mapping (staging): row rr, column quarter cq
-    const int rr = tid >> 2, cq = tid & 3;
-    // lane mapping (TMEM epilogues): TMEM lane quarter qd, column half hf
-    const int qd = warp & 3, hf = warp >> 2;
-    const int tl = qd * 32 + lane;                 // this thread's TMEM lane / tile row
+    const int rr = tid >> 2, cq = tid & 3;         // row mapping (staging)
+    const int qd = warp & 3, hf = warp >> 2;       // lane mapping (TMEM epilogues)
+    const int tl = qd * 32 + lane;
 
     long long s, e;
     seq_bounds(a.cu_seqlens, n, a.T, a.err, s, e);
@@ -240,50 +567,53 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
             o[t * ldo + col0 + tid % DVS] = from_f32<TOut>(0.f);
         return;
     }
+    // this sequence's chunks in the [T ; PT] workspace (a malformed map is reported, not followed)
+    long long jc = 0;
+    if (s < e) {
+        jc = a.chunk_base[n];
+        if (jc < 0 || jc + (e - s + TC_C - 1) / TC_C > a.max_chunks) {
+            if (tid == 0) set_error(a.err, GDN_DEVERR_CU_SEQLENS);
+            e = s;
+        }
+    }
 
-    // ---- TMEM (512 columns) and the MMA-completion barrier
     if (warp == 0) {
-        tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
         tc::tmem_relinquish();
     }
     if (tid == 32) {
         tc::mbar_init(tc::smem_u32(mbar), 1);
+        tc::mbar_init(tc::smem_u32(tpbar), 1);
         tc::mbar_fence_init();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tmem_slot;
-    const uint32_t T_D1 = tbase + 0, T_D2 = tbase + 64, T_D3 = tbase + 320, T_D5 = tbase + 384;
+    const uint32_t T_D2 = tbase, T_D3 = tbase + 128, T_D5 = tbase + 128 + DVS;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-    uint32_t phase = 0;
+    MmaSync ms{mbar, wait_flag, 0u};
+    uint32_t tp_phase = 0;
     bool timed_out = false;
-    // One thread polls the MMA barrier (bounded); the block then agrees on the
-    // outcome, so a timeout leaves the chunk loop uniformly.
-    auto wait_mma = [&]() -> bool {
-        if (tid == 0) *wait_flag = tc::mbar_wait(tc::smem_u32(mbar), phase) ? 0u : 1u;
-        __syncthreads();
-        const bool ok = *wait_flag == 0u;
-        if (ok) phase ^= 1u;
-        tc::fence_after_sync();
-        return ok;
-    };
-    auto sync_for_mma = [&]() {   // generic smem writes -> visible to the tensor core
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-    };
 
-    constexpr uint32_t ID_G1 = tc::idesc_bf16(128, 64);
     constexpr uint32_t ID_G2 = tc::idesc_bf16(128, NB) | tc::kTransB;
-    constexpr uint32_t ID_G34 = tc::idesc_bf16(128, DVS) | tc::kTransB;
+    constexpr uint32_t ID_G3 = tc::idesc_bf16(128, DVS) | tc::kTransB;
     constexpr uint32_t ID_G5 = tc::idesc_bf16(128, DVS) | tc::kTransA | tc::kTransB;
-    const uint32_t s_kqh = tc::smem_u32(kqh), s_kql = tc::smem_u32(kql);
+    const uint32_t s_wqh = tc::smem_u32(wqh), s_wql = tc::smem_u32(wql);
     const uint32_t s_bwh = tc::smem_u32(bwh), s_bwl = tc::smem_u32(bwl);
+    const uint32_t s_kth = tc::smem_u32(kth), s_ktl = tc::smem_u32(ktl);
     const uint32_t s_tph = tc::smem_u32(tph), s_tpl = tc::smem_u32(tpl);
     const uint32_t s_mth = tc::smem_u32(mth), s_mtl = tc::smem_u32(mtl);
     const uint32_t s_uth = tc::smem_u32(uth), s_utl = tc::smem_u32(utl);
+
+    // [T ; PT] of chunk i of this sequence -> TP (thread 0)
+    auto fetch_tp = [&](long long i) {
+        const unsigned char *src = a.tp + ((jc + i) * d.hv + h) * TP_BYTES;
+        const uint32_t mb = tc::smem_u32(tpbar);
+        tc::mbar_arrive_expect_tx(mb, TP_BYTES);
+        tc::bulk_g2s(s_tph, src, TP_HALF, mb);
+        tc::bulk_g2s(s_tpl, src + TP_HALF, TP_HALF, mb);
+    };
 
     // ---- initial state: thread (lane tl = dk row, half hf) holds M[tl][hf*HALF ..]
     float Mr[HALF];
@@ -294,7 +624,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
             load_row<HALF>(sin, Mr);
         } else {
 #pragma unroll
-            for (int j = 0; j < HALF; ++j) Mr[j] = 0.f;
+            for (int jj = 0; jj < HALF; ++jj) Mr[jj] = 0.f;
         }
 #pragma unroll
         for (int j8 = 0; j8 < HALF; j8 += 8) put8(mth, mtl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &Mr[j8]);
@@ -306,7 +636,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
     const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
 
     // Raw rows of the chunk at c0 (row rr of the row mapping) and its gates: the
-    // loads of chunk c+1 are issued while chunk c's second MMA group runs.
+    // loads of chunk c+1 are issued while chunk c's first MMA group runs.
     float kv[32], qv[32], vv[VQ];
     auto load_chunk = [&](long long c0) {
         const long long t = c0 + rr;
@@ -330,6 +660,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
         }
     };
     if (s < e) {
+        if (tid == 0) fetch_tp(0);
         load_chunk(s);
         load_gates(s);
         if (tid < TC_C) {
@@ -338,53 +669,33 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
         }
     }
 
-    for (long long c0 = s; c0 < e; c0 += TC_C) {
+    long long ci = 0;
+    for (long long c0 = s; c0 < e; c0 += TC_C, ++ci) {
         const int Lc = (int)((e - c0) < TC_C ? (e - c0) : TC_C);
         const bool has_next = c0 + TC_C < e;
         // ---------------- S0: L2 norm of the staged rows; gate scan
         if (l2) {
-            float sk = 0.f, sq = 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                sk += kv[i] * kv[i];
-                sq += qv[i] * qv[i];
-            }
-            sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-            sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-            sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-            sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-            const float fk = rsqrtf(sk + d.l2_eps), fq = rsqrtf(sq + d.l2_eps) * d.q_scale;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                kv[i] *= fk;
-                qv[i] *= fq;
-            }
+            l2norm_row4(kv, d.l2_eps, 1.f);
+            l2norm_row4(qv, d.l2_eps, d.q_scale);
         }
         __syncthreads();   // raw gates of this chunk are in sG / sB
-        if (warp == 0) {   // inclusive scan of g over 64 rows (2 per lane); padded rows add 0
-            const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
-            const float pair = g0 + g1;
-            float inc = pair;
-#pragma unroll
-            for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                const float t2 = __shfl_up_sync(0xffffffffu, inc, o2);
-                if (lane >= o2) inc += t2;
-            }
-            sG[2 * lane] = inc - pair + g0;
-            sG[2 * lane + 1] = inc;
-        }
+        if (warp == 0) scan64(sG, lane);
         __syncthreads();
         const float Gr = sG[rr], br = sB[rr], Gl = sG[TC_C - 1];
-        const float bg = br * expf(Gr);
-        // ---------------- S2: operands of G1 (K and Q rows) and G2 ([bgK | bV], MN-major)
+        const float gq = expf(Gr), bg = br * gq, kdec = expf(Gl - Gr);
+        // ---------------- S2: [bgK | bV] and K~ (MN-major), gamma Q (rows 64-127 of WQ)
 #pragma unroll
         for (int k8 = 0; k8 < 32; k8 += 8) {
-            put8(kqh, kql, tc::kmaj_off(rr, cq * 32 + k8, 128), &kv[k8]);
-            put8(kqh, kql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), &qv[k8]);
             float t8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) t8[i] = bg * kv[k8 + i];
             put8(bwh, bwl, tc::mnmaj_off(cq * 32 + k8, rr, NB), t8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = kdec * kv[k8 + i];
+            put8(kth, ktl, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = gq * qv[k8 + i];
+            put8(wqh, wql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), t8);
         }
 #pragma unroll
         for (int k8 = 0; k8 < VQ; k8 += 8) {
@@ -394,187 +705,94 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
             put8(bwh, bwl, tc::mnmaj_off(128 + cq * VQ + k8, rr, NB), t8);
         }
         sync_for_mma();
-        // ---------------- G1: [K;Q] K^T;  meanwhile the decay table
+        // ---------------- G2: [T ; PT] . [bgK | bV] -> W | U (lanes 0-63), PW | PU (64-127)
+        bool issued = true;
         if (tid == 0) {
-            mma3<false, false>(T_D1, s_kqh, s_kql, 0, s_kqh, s_kql, 0, 128, ID_G1, false);
-            tc::mma_commit(tc::smem_u32(mbar));
-        }
-        {
-            const float Gq = sG[rr];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int c = cq * 16 + i;
-                sGam[rr * 65 + c] = (c <= rr) ? expf(Gq - sG[c]) : 0.f;
+            issued = tc::mbar_wait(tc::smem_u32(tpbar), tp_phase);
+            if (issued) {
+                mma3<false, true, 64>(T_D2, s_tph, s_tpl, 0, s_bwh, s_bwl, NB, ID_G2, false);
+                tc::mma_commit(tc::smem_u32(mbar));
             }
         }
-        if (!wait_mma()) { timed_out = true; break; }
-        // ---------------- E1: A (fp32, for the solve), P (operand), gamma Q in place
-        {
-            float v32[32];
-            tc::tmem_ld32(T_D1 + lane_off + hf * 32, v32);
-            const int r = tl & 63;
-            const float *grow = sGam + r * 65 + hf * 32;
-            if (qd < 2) {  // K K^T rows -> A (strictly lower)
-                const float bq = sB[r];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = hf * 32 + i;
-                    if (c < r) sA[r * 65 + c] = bq * grow[i] * v32[i];
-                }
-            } else {       // Q K^T rows -> P (lower incl. diagonal; Gamma is 0 above)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v32[i] *= grow[i];
-#pragma unroll
-                for (int k8 = 0; k8 < 32; k8 += 8) put8(tph, tpl, tc::kmaj_off(64 + r, hf * 32 + k8, 64), &v32[k8]);
-            }
-        }
-        {   // G1 is done with Q: replace it by gamma Q (read back hi + lo)
-            const float gam_r = expf(Gr);
-#pragma unroll
-            for (int k8 = 0; k8 < 32; k8 += 8) {
-                float t8[8];
-                const uint32_t off = tc::kmaj_off(64 + rr, cq * 32 + k8, 128);
-                get8(kqh, kql, off, t8);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) t8[i] *= gam_r;
-                put8(kqh, kql, off, t8);
-            }
-        }
-        __syncthreads();
-        // ---------------- solve T = (I + A)^-1: diagonal 16x16 blocks (column `lane` of block `warp`)
-        if (warp < 4 && lane < 16) {
-            const int b0 = warp * 16, c = lane;
-            float col[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (i < r) acc += sA[(b0 + r) * 65 + b0 + i] * col[i];
-                col[r] = (r == c) ? 1.f : ((r > c) ? -acc : 0.f);
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r)
-                if (r > c) sA[(b0 + c) * 65 + b0 + r] = col[r];   // T[b0+r][b0+c], stored transposed
-        }
-        __syncthreads();
-        // Off-diagonal blocks, one warp per block column bj (no barriers inside):
-        // T[bi][bj] = -T[bi][bi] . sum_{k=bj}^{bi-1} A[bi][k] T[k][bj]   for bi > bj.
-        if (warp < 3) {
-            const int bj = warp, c = lane & 15, rh = lane >> 4;
-            const int m = bj * 16 + c;
-            float tcol[48];   // T[16*bj + k][m], k < 48
-#pragma unroll
-            for (int k = 0; k < 48; ++k) {
-                const int row = bj * 16 + k;
-                tcol[k] = (k < 16) ? ((row > m) ? sA[m * 65 + row] : ((row == m) ? 1.f : 0.f)) : 0.f;
-            }
-            solve_block_col<1>(sA, tcol, bj, m, rh);
-            solve_block_col<2>(sA, tcol, bj, m, rh);
-            solve_block_col<3>(sA, tcol, bj, m, rh);
-        }
-        __syncthreads();
-        // T -> bf16 hi/lo, rows 0-63 of TP (K-major): 64 rows x 8 groups of 8 columns
-        for (int task = tid; task < 64 * 8; task += TC_NT) {
-            const int r = task >> 3, c8 = (task & 7) * 8;
-            float t8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int c = c8 + i;
-                t8[i] = (c < r) ? sA[c * 65 + r] : ((c == r) ? 1.f : 0.f);
-            }
-            put8(tph, tpl, tc::kmaj_off(r, c8, 64), t8);
-        }
-        sync_for_mma();
-        // ---------------- G2: [T;P] . [bgK | bV]  ->  W | U  (rows 0-63); meanwhile the
-        // next chunk's rows and gates are loaded (after the shared-memory-heavy solve, so
-        // that the global loads do not queue in front of it)
-        if (tid == 0) {
-            mma3<false, true>(T_D2, s_tph, s_tpl, 0, s_bwh, s_bwl, NB, 64, ID_G2, false);
-            tc::mma_commit(tc::smem_u32(mbar));
-        }
-        if (has_next) {
+        tp_phase ^= 1u;
+        if (has_next) {               // next chunk's rows and gates, in flight during G2 / G3
             load_chunk(c0 + TC_C);
             load_gates(c0 + TC_C);
         }
-        if (!wait_mma()) { timed_out = true; break; }
-        // ---------------- E2a: K~ = exp(G_last - G_r) K_r (MN-major A of G5) into the freed B2
-        // region; K is read back (hi + lo) from KQ rows 0-63 before W replaces it
+        if (!ms.wait(tid, issued)) { timed_out = true; break; }
+        if (tid == 0 && has_next) fetch_tp(ci + 1);     // TP is free once G2 has completed
+        // ---------------- E2: -W -> WQ rows 0-63; Q' = gamma Q - PW -> WQ rows 64-127
         {
-            const float kdec = expf(Gl - Gr);
-#pragma unroll
-            for (int k8 = 0; k8 < 32; k8 += 8) {
-                float t8[8];
-                get8(kqh, kql, tc::kmaj_off(rr, cq * 32 + k8, 128), t8);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) t8[i] *= kdec;
-                put8(bwh, bwl, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
-            }
-        }
-        __syncthreads();
-        // ---------------- E2b: W -> rows 0-63 of KQ (G1 is done with K), U -> registers
-        float Ur[HALF];
-        if (qd < 2) {
             float v32[32];
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
-                tc::tmem_ld32(T_D2 + lane_off + hf * 64 + part * 32, v32);
+                const int cb = hf * 64 + part * 32;
+                tc::tmem_ld32(T_D2 + lane_off + cb, v32);
 #pragma unroll
-                for (int k8 = 0; k8 < 32; k8 += 8)
-                    put8(kqh, kql, tc::kmaj_off(tl, hf * 64 + part * 32 + k8, 128), &v32[k8]);
+                for (int k8 = 0; k8 < 32; k8 += 8) {
+                    const uint32_t off = tc::kmaj_off(tl, cb + k8, 128);
+                    float t8[8];
+                    if (qd < 2) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) t8[i] = -v32[k8 + i];
+                    } else {
+                        get8(wqh, wql, off, t8);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) t8[i] -= v32[k8 + i];
+                    }
+                    put8(wqh, wql, off, t8);
+                }
             }
-            tmem_ld<HALF>(T_D2 + lane_off + 128 + hf * HALF, Ur);
         }
         sync_for_mma();
-        // ---------------- G3: [W ; gQ] . M
+        // ---------------- G3: D3 += [-W ; Q'] . M -> U' (lanes 0-63), O (64-127)
         if (tid == 0) {
-            mma3<false, true>(T_D3, s_kqh, s_kql, 0, s_mth, s_mtl, DVS, 128, ID_G34, false);
-            tc::mma_commit(tc::smem_u32(mbar));
-        }
-        if (!wait_mma()) { timed_out = true; break; }
-        // ---------------- E3: U' = U - W M  -> MN-major B operand
-        if (qd < 2) {
-            float wm[HALF];
-            tmem_ld<HALF>(T_D3 + lane_off + hf * HALF, wm);
-#pragma unroll
-            for (int j = 0; j < HALF; ++j) wm[j] = Ur[j] - wm[j];
-#pragma unroll
-            for (int j8 = 0; j8 < HALF; j8 += 8) put8(uth, utl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &wm[j8]);
-        }
-        sync_for_mma();
-        // ---------------- G4 (O += P U') and G5 (dM = K~^T U'); meanwhile the next chunk's gates
-        if (tid == 0) {
-            mma3<false, true>(T_D3, s_tph, s_tpl, 0, s_uth, s_utl, DVS, 64, ID_G34, true);
-            mma3<true, true>(T_D5, s_bwh, s_bwl, 128, s_uth, s_utl, DVS, 64, ID_G5, false);
+            mma3<false, true, 128>(T_D3, s_wqh, s_wql, 0, s_mth, s_mtl, DVS, ID_G3, true);
             tc::mma_commit(tc::smem_u32(mbar));
         }
         if (has_next && tid < TC_C) {
-            sG[tid] = gn;
+            sG[tid] = gn;       // this chunk's gates are in registers by now
             sB[tid] = bn;
         }
-        if (!wait_mma()) { timed_out = true; break; }
-        // ---------------- E4: outputs (lanes 64-127) and the state (all lanes)
+        if (!ms.wait(tid)) { timed_out = true; break; }
+        // ---------------- E3: U' -> MN-major B operand; O rows -> o
         {
             float v[HALF];
-            if (qd >= 2) {
+            tmem_ld<HALF>(T_D3 + lane_off + hf * HALF, v);
+            if (qd < 2) {
+#pragma unroll
+                for (int j8 = 0; j8 < HALF; j8 += 8)
+                    put8(uth, utl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &v[j8]);
+            } else {
                 const int r = tl - 64;
-                tmem_ld<HALF>(T_D3 + lane_off + hf * HALF, v);
                 if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, v);
             }
+        }
+        sync_for_mma();
+        // ---------------- G5: dM = K~^T U'
+        if (tid == 0) {
+            mma3<true, true, 64>(T_D5, s_kth, s_ktl, 128, s_uth, s_utl, DVS, ID_G5, false);
+            tc::mma_commit(tc::smem_u32(mbar));
+        }
+        if (!ms.wait(tid)) { timed_out = true; break; }
+        // ---------------- E5: M <- gamma_last M + dM
+        {
+            float v[HALF];
             tmem_ld<HALF>(T_D5 + lane_off + hf * HALF, v);
             const float gl = expf(Gl);
 #pragma unroll
-            for (int j = 0; j < HALF; ++j) Mr[j] = gl * Mr[j] + v[j];
+            for (int jj = 0; jj < HALF; ++jj) Mr[jj] = gl * Mr[jj] + v[jj];
 #pragma unroll
             for (int j8 = 0; j8 < HALF; j8 += 8) put8(mth, mtl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &Mr[j8]);
         }
-        // (the next chunk's first operand writes are followed by sync_for_mma before G1)
+        // (the next chunk's operand writes are followed by sync_for_mma before G2)
     }
     if (timed_out) {
-        // give the outstanding MMAs one more bounded chance to retire before TMEM is freed
+        // give outstanding MMAs and copies one more bounded chance to retire before TMEM is freed
         if (tid == 0) {
             set_error(a.err, GDN_DEVERR_TIMEOUT);
-            tc::mbar_wait(tc::smem_u32(mbar), phase);
+            tc::mbar_wait(tc::smem_u32(mbar), ms.phase);
+            tc::mbar_wait(tc::smem_u32(tpbar), tp_phase);
         }
         __syncthreads();
     }
@@ -585,14 +803,26 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_tc_kernel(ChunkArgs a) {
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tbase, 512);
+    if (warp == 0) tc::tmem_dealloc(tbase, 256);
 }
 
 template <int DVS, typename TIn, typename TOut>
 static cudaError_t launch_tc_t(const ChunkArgs &a, cudaStream_t s) {
-    auto kern = chunk_tc_kernel<DVS, TIn, TOut>;
-    constexpr int smem = TcSmem<DVS>::BYTES;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t err;
+    if (a.T > 0) {
+        chunk_map_kernel<<<1, 1024, 0, s>>>(a);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if (a.max_chunks > 0) {
+            auto tp = chunk_tp_kernel<TIn>;
+            err = cudaFuncSetAttribute(tp, cudaFuncAttributeMaxDynamicSharedMemorySize, TpSmem::BYTES);
+            if (err != cudaSuccess) return err;
+            tp<<<(unsigned)(a.max_chunks * a.d.hv), TC_NT, TpSmem::BYTES, s>>>(a);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        }
+    }
+    auto kern = chunk_chain_kernel<DVS, TIn, TOut>;
+    constexpr int smem = ChainSmem<DVS>::BYTES;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     dim3 grid(TC_DK / DVS, a.d.hv, a.n_seqs);
     kern<<<grid, TC_NT, smem, s>>>(a);
@@ -601,9 +831,33 @@ static cudaError_t launch_tc_t(const ChunkArgs &a, cudaStream_t s) {
 
 bool chunk_tc_supported(const Dims &d) { return d.dk == 128 && d.dv == 128 && d.chunk == 64; }
 
+long long chunk_tc_max_chunks(long long T, long long n_seqs) {
+    if (T <= 0 || n_seqs <= 0) return 0;
+    return T / TC_C + (n_seqs < T ? n_seqs : T);
+}
+
+size_t chunk_tc_ws_bytes(const Dims &d, long long T, long long n_seqs) {
+    const long long mc = chunk_tc_max_chunks(T, n_seqs);
+    if (mc == 0) return 0;
+    const size_t base = (((size_t)n_seqs + 1) * 4 + 255) & ~(size_t)255;
+    return base + (size_t)mc * d.hv * TP_BYTES;
+}
+
+void chunk_tc_carve(ChunkArgs &a, void *ws) {
+    a.max_chunks = chunk_tc_max_chunks(a.T, a.n_seqs);
+    if (a.max_chunks == 0 || !ws) {
+        a.chunk_base = nullptr;
+        a.tp = nullptr;
+        return;
+    }
+    a.chunk_base = (int *)ws;
+    a.tp = (unsigned char *)ws + ((((size_t)a.n_seqs + 1) * 4 + 255) & ~(size_t)255);
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, cudaStream_t s) {
     if (a.n_seqs == 0) return cudaSuccess;
     if (!chunk_tc_supported(a.d)) return cudaErrorInvalidValue;
+    if (a.T > 0 && (!a.chunk_base || !a.tp)) return cudaErrorInvalidValue;
 #define GDN_TC(DVS_)                                                                         \
     if (dvs == DVS_) {                                                                        \
         if (in_bf16)                                                                          \

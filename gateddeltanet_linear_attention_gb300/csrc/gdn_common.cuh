@@ -86,6 +86,11 @@ struct ChunkArgs {
     unsigned flags;
     Dims d;
     unsigned *err;
+    // tensor-core path: per-sequence chunk offsets and the [T ; PT] operands
+    // (caller workspace, carved by chunk_tc_carve)
+    int *chunk_base;
+    unsigned char *tp;
+    long long max_chunks;
 };
 
 struct DecodeArgs {
@@ -137,6 +142,9 @@ cudaError_t launch_gated_rmsnorm(const Dims &d, bool act_bf16, const void *o, bo
                                  void *y, bool y_bf16, cudaStream_t s);
 cudaError_t launch_chunk_simt(const ChunkArgs &a, bool in_bf16, bool o_bf16, cudaStream_t s);
 bool chunk_tc_supported(const Dims &d);
+long long chunk_tc_max_chunks(long long T, long long n_seqs);
+size_t chunk_tc_ws_bytes(const Dims &d, long long T, long long n_seqs);
+void chunk_tc_carve(ChunkArgs &a, void *ws);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, cudaStream_t s);
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();

@@ -91,6 +91,18 @@ def test_chunk_prefill_validation(lib):
                                  None, A16, 1, 1, None, 0, None) == INVALID
     assert lib.gdn_chunk_prefill(ch, None, None, 0, None, 0, 0, None, None, None, 0, 0, None, None,
                                  None, None, 1, 1, None, 0, None) == OK
+    # the tensor-core path (bf16, d = 128, chunk 64) needs its [T ; PT] workspace
+    need = lib.gdn_workspace_size(ch, 64, 1)
+    assert lib.gdn_chunk_prefill(ch, A16, A16, 2048, A16, 4096, 0, A16, A16, A16, 1, 64, None, None,
+                                 None, A16, 1, 1, None, 0, None) == WORKSPACE
+    assert lib.gdn_chunk_prefill(ch, A16, A16, 2048, A16, 4096, 0, A16, A16, A16, 1, 64, None, None,
+                                 None, A16, 1, 1, MIS, need, None) == WORKSPACE
+    # one (chunk, v-head) operand of 32 KB each, plus the chunk map
+    assert need >= 32 * 32768
+    # the fp32 mode runs the SIMT kernel and needs none
+    c32 = cfg(act="fp32")
+    assert lib.gdn_chunk_prefill(ctypes.byref(c32), A16, A16, 2048, A16, 4096, 1, A16, A16, A16, 0, 5,
+                                 None, None, None, A16, 1, 1, None, 0, None) == INVALID
 
 
 def _io(T=64, n=1, **kw):

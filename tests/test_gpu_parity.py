@@ -180,8 +180,10 @@ def test_standalone_entry_points():
     o = torch.empty((T, wl.HV * wl.dv), device="cuda")
     st_out = torch.empty_like(d["state"])
     H = wl.HK * wl.dk
+    cws = torch.empty(max(gdn.gdn_workspace_size(cfg, T, len(inp["cu_seqlens"]) - 1), 16),
+                      dtype=torch.uint8, device="cuda")
     gdn.gdn_chunk_prefill(cfg, xa[:, :H], xa[:, H:2 * H], xa[:, 2 * H:], g, beta, d["cu_seqlens"],
-                          d["state"], st_out, None, o)
+                          d["state"], st_out, None, o, workspace=cws)
     rxn = oracle.l2norm_qk(rxa, wl.HK, wl.dk)
     ro, rst = oracle.delta_rule(rxn, rg, rb, inp["cu_seqlens"], wl.HK, wl.HV, wl.dk, wl.dv,
                                 state=inp["state"])
