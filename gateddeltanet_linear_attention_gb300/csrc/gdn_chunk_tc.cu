@@ -12,18 +12,19 @@
 //   M <- gamma_last M + (diag(exp(G_last - G)) K)^T U'
 //
 // Two kernels split the work by what depends on the carried state.
-//  * chunk_tp_kernel, parallel over every (chunk, v-head): the Gram products
-//    [K;Q] K^T on the tensor cores, A and P, the 64x64 inverse T in fp32 on
-//    the SIMT pipes (16x16 diagonal blocks by forward substitution, then
-//    block columns), and PT = P T on the tensor cores.  It writes [T ; PT] as
-//    a ready-made bf16 hi/lo MMA operand (32 KB) to the workspace.
+//  * chunk_tp_kernel, parallel over every (chunk, v-head), computes every
+//    state-independent operand: the Gram products [K;Q] K^T, A and P, the
+//    64x64 inverse T in fp32 (16x16 diagonal blocks by forward substitution,
+//    then two levels of blocked products: T21 = -T22 A21 T11), PT = P T, and
+//    [W ; PW] = [T ; PT] diag(beta gamma) K, all products on the tensor cores.
+//    It writes [T ; PT] and [-W ; gamma Q - PW] as ready-made bf16 hi/lo MMA
+//    operands (96 KB per chunk and v-head) to the workspace.
 //  * chunk_chain_kernel, one CTA per (sequence, v-head, slice of DVS state
-//    columns), walks the chunks in order with three MMA groups per chunk:
-//      G2  D2 = [T ; PT] . [bgK | bV]  -> W, PW (cols 0-127) and U, PU (D3)
-//      G3  D3 += [-W ; gQ - PW] . M    -> U' (TMEM lanes 0-63), O (lanes 64-127)
-//      G5  D5 = K~^T . U'              -> the state increment
-//    The [T ; PT] operand of the next chunk is bulk-copied while the current
-//    one runs.
+//    columns), walks the chunks in order with two MMA round trips per chunk:
+//      D3  = [T ; PT] . bV            -> U, PU
+//      D3 += [-W ; Q'] . M            -> U' (TMEM lanes 0-63), O (lanes 64-127)
+//      D5  = K~^T . U'                -> the state increment
+//    The next chunk's operands are bulk-copied while the current one runs.
 //
 // Precision.  The gated RMSNorm that follows divides every token-head by the
 // RMS of its own o, so on quiet tokens absolute errors in o are amplified up
@@ -48,6 +49,8 @@ constexpr int TC_C = 64;     // chunk
 constexpr int TC_DK = 128;   // dk == dv
 constexpr int TP_HALF = 128 * 64 * 2;     // one bf16 part of [T ; PT] (K-major, K = 64)
 constexpr int TP_BYTES = 2 * TP_HALF;     // hi + lo, as stored in the workspace
+constexpr int WQ_BYTES = 2 * 128 * 128 * 2;             // [-W ; Q'] hi + lo (K-major, K = 128)
+constexpr int CH_BYTES = TP_BYTES + WQ_BYTES;           // workspace bytes per (chunk, v-head)
 
 // Store 8 values at byte offset `off` (16-byte aligned) of a hi and a lo tile
 // (packed two-at-a-time conversions).
@@ -61,20 +64,6 @@ __device__ __forceinline__ void put8(unsigned char *hi, unsigned char *lo, uint3
     }
     *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<const uint4 *>(h2);
     *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<const uint4 *>(l2);
-}
-
-// Read back 8 values (hi + lo) at a 16-byte aligned offset of a hi and a lo tile.
-__device__ __forceinline__ void get8(const unsigned char *hi, const unsigned char *lo, uint32_t off, float *v) {
-    const uint4 hv = *reinterpret_cast<const uint4 *>(hi + off);
-    const uint4 lv = *reinterpret_cast<const uint4 *>(lo + off);
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&hv);
-    const __nv_bfloat162 *l = reinterpret_cast<const __nv_bfloat162 *>(&lv);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 a = __bfloat1622float2(h[i]), b = __bfloat1622float2(l[i]);
-        v[2 * i] = a.x + b.x;
-        v[2 * i + 1] = a.y + b.y;
-    }
 }
 
 // Load n (multiple of 8) consecutive elements as fp32 with 16-byte loads.
@@ -155,38 +144,6 @@ __device__ __forceinline__ void mma3(uint32_t d_tmem, uint32_t a_hi, uint32_t a_
     }
 }
 
-// One block of the triangular inverse, for the block column held by a warp:
-// rows of block bi = bj + DB, column m of T, from the rows already in tcol.
-// (Lanes c and c+16 hold the same column; each stores half of the new rows.)
-template <int DB>
-__device__ __forceinline__ void solve_block_col(float *sA, float (&tcol)[48], int bj, int m, int rh) {
-    // Blocks past the last row block are computed on clamped (valid) addresses
-    // and not stored, so that the warp's code has no data-dependent branches.
-    const bool live = bj + DB < 4;
-    const int bi = live ? bj + DB : 3;
-    float xr[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        const float *arow = sA + (bi * 16 + r) * 65 + bj * 16;
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16 * DB; ++k) acc = fmaf(arow[k], tcol[k], acc);
-        xr[r] = acc;
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        float acc = xr[r];
-#pragma unroll
-        for (int mm = 0; mm < r; ++mm) acc = fmaf(sA[(bi * 16 + mm) * 65 + bi * 16 + r], xr[mm], acc);
-        tcol[16 * DB + r] = -acc;
-    }
-    if (live) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) sA[m * 65 + bi * 16 + rh * 8 + r] = tcol[16 * DB + rh * 8 + r];
-    }
-}
-
-
 // Shared pieces of the per-CTA setup: one thread polls the MMA barrier
 // (bounded) and the block agrees on the outcome, so a timeout leaves any loop
 // uniformly.
@@ -212,16 +169,25 @@ __device__ __forceinline__ void sync_for_mma() {
     tc::fence_after_sync();
 }
 
-// L2 normalisation of a row held by 4 consecutive lanes (32 values each).
-__device__ __forceinline__ void l2norm_row4(float (&v)[32], float eps, float scale) {
+// Row mapping of the staging phases: warp w holds rows 8w .. 8w+7, lane l row
+// 8w + l%8 and dk columns 32*(l/8) .. +31.  Each group of 8 lanes (one phase of
+// a 16-byte shared-memory store) then writes 8 consecutive rows of the same
+// columns: one 128-byte core matrix, free of bank conflicts.
+__device__ __forceinline__ int stage_row(int tid) { return 8 * (tid >> 5) + (tid & 7); }
+__device__ __forceinline__ int stage_quarter(int tid) { return (tid & 31) >> 3; }
+
+// L2 normalisation of a row held by lanes l, l+8, l+16, l+24 (32 values each).
+// Returns the factor applied.
+__device__ __forceinline__ float l2norm_row4(float (&v)[32], float eps, float scale) {
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
     const float f = rsqrtf(ss + eps) * scale;
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] *= f;
+    return f;
 }
 
 // In-place inclusive scan of the 64 gate values in sG by warp 0 (2 per lane).
@@ -286,34 +252,44 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(ChunkArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// [T ; PT] of one (chunk, v-head).  Shared memory: the [K;Q] hi/lo Gram
-// operand (64 KB); once G1 has consumed it, the same bytes hold the fp32 A
-// (T^T above the diagonal) and the bf16 operands of PT = P T (P, and T^T
-// as K-major rows).
+// Per-(chunk, v-head) operands of the state chain, written to the workspace:
+//   TP = [T ; PT]          K-major (M = 128, K = 64),  hi then lo   (32 KB)
+//   WQ = [-W ; gQ - PW]    K-major (M = 128, K = 128), hi then lo   (64 KB)
+// Shared memory: the [K;Q] hi/lo Gram operand (64 KB) and bgK (MN-major, the B
+// operand of W, 32 KB).  Once G1 has consumed [K;Q], its bytes hold the fp32 A
+// (T^T above the diagonal), P and T^T as bf16 operands, the solve's scratch,
+// and finally [T ; PT].
 struct TpSmem {
     static constexpr int KQ = 128 * 128 * 2;
+    static constexpr int OPH = 64 * 64 * 2;                // one bf16 part of a 64x64 operand
     static constexpr int OFF_KQ = 0;
     static constexpr int OFF_SA = 0;                       // fp32 [64][65]
-    static constexpr int OPH = 64 * 64 * 2;                // one bf16 part of a 64x64 operand
-    static constexpr int OFF_P = (64 * 65 * 4 + 1023) & ~1023;  // P, K-major (M = 64, K = 64), hi + lo
-    static constexpr int OFF_B2 = OFF_P + 2 * OPH;         // B2[c][k] = T[k][c], K-major, hi + lo
-    static constexpr int OFF_G = 2 * KQ;                   // G[64], beta[64]
-    static constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;     // mbarrier, tmem slot, flag, search
+    static constexpr int OFF_P = (64 * 65 * 4 + 1023) & ~1023;   // P (M = 64, K = 64), hi + lo
+    static constexpr int OFF_B2 = OFF_P + 2 * OPH;         // B2[c][k] = T[k][c], hi + lo; solve scratch before
+    static constexpr int OFF_A3 = OFF_P;                   // [T ; PT] hi + lo, after P and B2 are consumed
+    static constexpr int OFF_B3 = 2 * KQ;                  // beta gamma K (MN-major, MN = 128, K = 64), hi + lo
+    static constexpr int OFF_G = OFF_B3 + 2 * 128 * 64 * 2;        // G[64], beta[64], q factor[64]
+    static constexpr int OFF_BAR = OFF_G + 3 * 64 * 4;     // mbarrier, tmem slot, flag, search
     static constexpr int BYTES = OFF_BAR + 32;
-    static_assert(OFF_P % 1024 == 0, "operand alignment");
     static_assert(OFF_B2 + 2 * OPH <= 2 * KQ, "PT operands exceed the Gram region");
+    static_assert(OFF_A3 + TP_BYTES <= 2 * KQ, "[T ; PT] exceeds the Gram region");
+    static_assert(OFF_B2 + 2 * 32 * 33 * 4 <= OFF_B2 + 2 * OPH, "solve scratch exceeds B2");
 };
 
 template <typename TIn>
-__global__ void __launch_bounds__(TC_NT) chunk_tp_kernel(ChunkArgs a) {
+__global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     using L = TpSmem;
     extern __shared__ __align__(1024) unsigned char sm[];
     unsigned char *kqh = sm + L::OFF_KQ, *kql = kqh + L::KQ;
     float *sA = reinterpret_cast<float *>(sm + L::OFF_SA);
     unsigned char *ph = sm + L::OFF_P, *pl = ph + L::OPH;
     unsigned char *b2h = sm + L::OFF_B2, *b2l = b2h + L::OPH;
+    float *sY = reinterpret_cast<float *>(sm + L::OFF_B2);      // solve scratch (before B2)
+    unsigned char *a3h = sm + L::OFF_A3, *a3l = a3h + TP_HALF;
+    unsigned char *b3h = sm + L::OFF_B3, *b3l = b3h + 128 * 64 * 2;
     float *sG = reinterpret_cast<float *>(sm + L::OFF_G);
     float *sB = sG + 64;
+    float *sFq = sG + 128;
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 8);
     volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 12);
@@ -344,9 +320,11 @@ __global__ void __launch_bounds__(TC_NT) chunk_tp_kernel(ChunkArgs a) {
     long long s, e;
     seq_bounds(a.cu_seqlens, lo, a.T, nullptr, s, e);   // malformed bounds are reported by the map
     const long long t0 = s + (j - a.chunk_base[lo]) * TC_C;
+    unsigned char *gtp = a.tp + ((long long)j * d.hv + h) * CH_BYTES;   // [T ; PT]
+    unsigned char *gwq = gtp + TP_BYTES;                                 // [-W ; Q']
 
     if (warp == 0) {
-        tc::tmem_alloc(tc::smem_u32(tmem_slot), 64);
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), 128);
         tc::tmem_relinquish();
     }
     if (tid == 32) {
@@ -358,11 +336,12 @@ __global__ void __launch_bounds__(TC_NT) chunk_tp_kernel(ChunkArgs a) {
     tc::fence_after_sync();
     const uint32_t tbase = *tmem_slot;
     MmaSync ms{mbar, wait_flag, 0u};
-    const int rr = tid >> 2, cq = tid & 3;
+    const int rr = stage_row(tid), cq = stage_quarter(tid);
     const int qd = warp & 3, hf = warp >> 2, tl = qd * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
 
-    // ---- rows of K and Q (L2-normalised), gates
+    // ---- rows of K and Q (L2-normalised) and gates; operands [K;Q] (K-major) and bgK (MN-major)
     {
         float kv[32], qv[32];
         const long long t = t0 + rr;
@@ -373,25 +352,30 @@ __global__ void __launch_bounds__(TC_NT) chunk_tp_kernel(ChunkArgs a) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
         }
-        if (a.flags & GDN_FLAG_L2NORM_QK) {
-            l2norm_row4(kv, d.l2_eps, 1.f);
-            l2norm_row4(qv, d.l2_eps, d.q_scale);
-        }
-#pragma unroll
-        for (int k8 = 0; k8 < 32; k8 += 8) {
-            put8(kqh, kql, tc::kmaj_off(rr, cq * 32 + k8, 128), &kv[k8]);
-            put8(kqh, kql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), &qv[k8]);
-        }
         if (tid < TC_C) {
             const long long tt = t0 + tid;
             sG[tid] = tt < e ? a.g[tt * d.hv + h] : 0.f;
             sB[tid] = tt < e ? a.beta[tt * d.hv + h] : 0.f;
         }
+        __syncthreads();
+        if (warp == 0) scan64(sG, lane);
+        const float fq = l2 ? l2norm_row4(qv, d.l2_eps, d.q_scale) : 1.f;
+        if (l2) l2norm_row4(kv, d.l2_eps, 1.f);
+        if (cq == 0) sFq[rr] = fq;
+        __syncthreads();
+        const float bg = sB[rr] * expf(sG[rr]);
+#pragma unroll
+        for (int k8 = 0; k8 < 32; k8 += 8) {
+            put8(kqh, kql, tc::kmaj_off(rr, cq * 32 + k8, 128), &kv[k8]);
+            put8(kqh, kql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), &qv[k8]);
+            float t8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = bg * kv[k8 + i];
+            put8(b3h, b3l, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
+        }
     }
-    __syncthreads();
-    if (warp == 0) scan64(sG, lane);
     sync_for_mma();
-    // ---- G1: [K;Q] K^T -> K K^T (TMEM lanes 0-63), Q K^T (64-127)
+    // ---- G1: [K;Q] K^T -> K K^T (TMEM lanes 0-63), Q K^T (64-127), columns 0-63
     if (tid == 0) {
         mma3<false, false, 128>(tbase, tc::smem_u32(kqh), tc::smem_u32(kql), 0, tc::smem_u32(kqh),
                                 tc::smem_u32(kql), 0, tc::idesc_bf16(128, 64), false);
@@ -401,28 +385,31 @@ __global__ void __launch_bounds__(TC_NT) chunk_tp_kernel(ChunkArgs a) {
     if (ok) {
         // ---- E1: A (strictly lower, fp32) and P (lower incl. the diagonal, bf16 hi/lo
         // operand), over the Gram region
-        float v32[32];
-        tc::tmem_ld32(tbase + lane_off + hf * 32, v32);
-        const int r = tl & 63;
-        const float Gr = sG[r];
-        if (qd < 2) {
-            const float br = sB[r];
+        {
+            float v32[32];
+            tc::tmem_ld32(tbase + lane_off + hf * 32, v32);
+            const int r = tl & 63;
+            const float Gr = sG[r];
+            if (qd < 2) {
+                const float br = sB[r];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = hf * 32 + i;
-                if (c < r) sA[r * 65 + c] = br * expf(Gr - sG[c]) * v32[i];
+                for (int i = 0; i < 32; ++i) {
+                    const int c = hf * 32 + i;
+                    if (c < r) sA[r * 65 + c] = br * expf(Gr - sG[c]) * v32[i];
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = hf * 32 + i;
+                    v32[i] = (c <= r) ? expf(Gr - sG[c]) * v32[i] : 0.f;
+                }
+#pragma unroll
+                for (int k8 = 0; k8 < 32; k8 += 8) put8(ph, pl, tc::kmaj_off(r, hf * 32 + k8, 64), &v32[k8]);
             }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = hf * 32 + i;
-                v32[i] = (c <= r) ? expf(Gr - sG[c]) * v32[i] : 0.f;
-            }
-#pragma unroll
-            for (int k8 = 0; k8 < 32; k8 += 8) put8(ph, pl, tc::kmaj_off(r, hf * 32 + k8, 64), &v32[k8]);
         }
         __syncthreads();
-        // ---- T = (I + A)^-1: diagonal 16x16 blocks (column `lane` of block `warp`)
+        // ---- T = (I + A)^-1, kept transposed above the diagonal of sA: T[r][c] = sA[c*65 + r], r > c.
+        // Step 1: the four 16x16 diagonal blocks, by forward substitution (column `lane` of block `warp`).
         if (warp < 4 && lane < 16) {
             const int b0 = warp * 16, c = lane;
             float col[16];
@@ -436,36 +423,81 @@ __global__ void __launch_bounds__(TC_NT) chunk_tp_kernel(ChunkArgs a) {
             }
 #pragma unroll
             for (int rw = 0; rw < 16; ++rw)
-                if (rw > c) sA[(b0 + c) * 65 + b0 + rw] = col[rw];   // T[b0+rw][b0+c], transposed
+                if (rw > c) sA[(b0 + c) * 65 + b0 + rw] = col[rw];
         }
         __syncthreads();
-        // off-diagonal blocks, one warp per block column bj
-        if (warp < 3) {
-            const int bj = warp, c = lane & 15, rh = lane >> 4;
-            const int m = bj * 16 + c;
-            float tcol[48];
+        // Step 2: the 16x16 blocks below them within each 32x32 diagonal block:
+        // T[R][C] = -T[R][R] A[R][C] T[C][C] for (R, C) = (1, 0) and (3, 2).
+        {
+            float y[2];
 #pragma unroll
-            for (int k = 0; k < 48; ++k) {
-                const int row = bj * 16 + k;
-                tcol[k] = (k < 16) ? ((row > m) ? sA[m * 65 + row] : ((row == m) ? 1.f : 0.f)) : 0.f;
+            for (int u = 0; u < 2; ++u) {
+                const int idx = tid + u * TC_NT, b = idx >> 8, i = (idx >> 4) & 15, jj = idx & 15;
+                const int R0 = 32 * b + 16, C0 = 32 * b;
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {     // A[R0+i][C0+k] T[C0+k][C0+jj], k >= jj
+                    const float tkj = (k > jj) ? sA[(C0 + jj) * 65 + C0 + k] : ((k == jj) ? 1.f : 0.f);
+                    acc = fmaf(sA[(R0 + i) * 65 + C0 + k], tkj, acc);
+                }
+                y[u] = acc;
             }
-            solve_block_col<1>(sA, tcol, bj, m, rh);
-            solve_block_col<2>(sA, tcol, bj, m, rh);
-            solve_block_col<3>(sA, tcol, bj, m, rh);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int idx = tid + u * TC_NT;
+                sY[idx] = y[u];                      // [b][i][jj]
+            }
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int idx = tid + u * TC_NT, b = idx >> 8, i = (idx >> 4) & 15, jj = idx & 15;
+                const int R0 = 32 * b + 16, C0 = 32 * b;
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {     // T[R0+i][R0+m] Y[m][jj], m <= i
+                    const float tim = (i > m) ? sA[(R0 + m) * 65 + R0 + i] : ((i == m) ? 1.f : 0.f);
+                    acc = fmaf(tim, sY[(b * 16 + m) * 16 + jj], acc);
+                }
+                sA[(C0 + jj) * 65 + R0 + i] = -acc;
+            }
         }
         __syncthreads();
-        // ---- T's rows -> the workspace (rows 0-63 of [T ; PT]); B2 = T^T rows (B2[c][k] = T[k][c])
-        unsigned char *gout = a.tp + ((long long)j * d.hv + h) * TP_BYTES;
+        // Step 3: the lower-left 32x32 block: T[2][1] = -T[2][2] A[2][1] T[1][1] (32-blocks).
+        // Thread (warp w, lane jj) computes rows i = w + 8u (u < 4) of column jj; each
+        // element of T loaded serves the four rows.
+        {
+            const int jj = lane;
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {        // Y = A[2][1] T[1][1]; T[k][jj] = 0 for k < jj
+                const float tkj = (k > jj) ? sA[jj * 65 + k] : ((k == jj) ? 1.f : 0.f);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) y[u] = fmaf(sA[(32 + warp + 8 * u) * 65 + k], tkj, y[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sY[(warp + 8 * u) * 33 + jj] = y[u];
+            __syncthreads();
+            float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {        // T[2][2] Y; T[32+i][32+m] = 0 for m > i
+                const float ym = sY[m * 33 + jj];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = warp + 8 * u;
+                    const float tim = (i > m) ? sA[(32 + m) * 65 + 32 + i] : ((i == m) ? 1.f : 0.f);
+                    z[u] = fmaf(tim, ym, z[u]);
+                }
+            }
+            __syncthreads();                      // every read of the scratch is done
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sA[jj * 65 + 32 + warp + 8 * u] = -z[u];
+        }
+        __syncthreads();
+        // ---- B2 = T^T rows (B2[c][k] = T[k][c]), the B operand of PT = P T
         for (int task = tid; task < 64 * 8; task += TC_NT) {
             // consecutive tasks -> consecutive 16-byte rows of one core-matrix block
             const int r2 = (task >> 6) * 8 + (task & 7), c8 = ((task >> 3) & 7) * 8;
             float t8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int c = c8 + i;
-                t8[i] = (c < r2) ? sA[c * 65 + r2] : ((c == r2) ? 1.f : 0.f);
-            }
-            put8(gout, gout + TP_HALF, tc::kmaj_off(r2, c8, 64), t8);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int k = c8 + i;
@@ -474,20 +506,84 @@ __global__ void __launch_bounds__(TC_NT) chunk_tp_kernel(ChunkArgs a) {
             put8(b2h, b2l, tc::kmaj_off(r2, c8, 64), t8);
         }
         sync_for_mma();
-        // ---- G: P . T (M = 64): row r of PT lands on TMEM lane 32*(r/16) + r%16
+        // ---- G: P . T (M = 64) into columns 64-127: row r lands on TMEM lane 32*(r/16) + r%16
         if (tid == 0) {
-            mma3<false, false, 64>(tbase, tc::smem_u32(ph), tc::smem_u32(pl), 0, tc::smem_u32(b2h),
+            mma3<false, false, 64>(tbase + 64, tc::smem_u32(ph), tc::smem_u32(pl), 0, tc::smem_u32(b2h),
                                    tc::smem_u32(b2l), 0, tc::idesc_bf16(64, 64), false);
             tc::mma_commit(tc::smem_u32(mbar));
         }
         ok = ms.wait(tid);
-        if (ok) {
-            tc::tmem_ld32(tbase + lane_off + hf * 32, v32);
+    }
+    if (ok) {
+        // ---- [T ; PT] -> A3 (shared, operand of W) and the workspace
+        for (int task = tid; task < 64 * 8; task += TC_NT) {
+            const int r2 = (task >> 6) * 8 + (task & 7), c8 = ((task >> 3) & 7) * 8;
+            float t8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = c8 + i;
+                t8[i] = (c < r2) ? sA[c * 65 + r2] : ((c == r2) ? 1.f : 0.f);
+            }
+            put8(a3h, a3l, tc::kmaj_off(r2, c8, 64), t8);
+        }
+        {
+            float v32[32];
+            tc::tmem_ld32(tbase + 64 + lane_off + hf * 32, v32);
             if (lane < 16) {
                 const int r2 = qd * 16 + lane;
 #pragma unroll
-                for (int k8 = 0; k8 < 32; k8 += 8)
-                    put8(gout, gout + TP_HALF, tc::kmaj_off(64 + r2, hf * 32 + k8, 64), &v32[k8]);
+                for (int k8 = 0; k8 < 32; k8 += 8) {
+                    put8(a3h, a3l, tc::kmaj_off(64 + r2, hf * 32 + k8, 64), &v32[k8]);
+                }
+            }
+        }
+        sync_for_mma();
+        // ---- W: [T ; PT] . bgK -> W (lanes 0-63), PW (64-127), columns 0-127; [T ; PT]
+        // also leaves for the workspace as one bulk store
+        if (tid == 0) {
+            tc::bulk_s2g(gtp, tc::smem_u32(a3h), TP_BYTES);
+            tc::bulk_commit();
+            mma3<false, true, 64>(tbase, tc::smem_u32(a3h), tc::smem_u32(a3l), 0, tc::smem_u32(b3h),
+                                  tc::smem_u32(b3l), 128, tc::idesc_bf16(128, 128) | tc::kTransB, false);
+            tc::mma_commit(tc::smem_u32(mbar));
+        }
+        // meanwhile: the q rows the Q' epilogue needs (lane mapping: row tl-64, half hf)
+        float qrow[64];
+        if (qd >= 2) {
+            const int r = tl - 64;
+            const long long t = t0 + r;
+            if (t < e) {
+                load_row<64>((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK + hf * 64, qrow);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) qrow[i] = 0.f;
+            }
+        }
+        if (tid == 0) tc::bulk_wait_read_all();   // [T ; PT] has left A3 (long before W completes)
+        ok = ms.wait(tid);
+        if (ok) {
+            // ---- [-W ; gamma q - PW] -> shared (over the consumed Gram region), then one
+            // bulk store to the workspace (hi then lo, K-major, K = 128)
+            float v64[64];
+            tc::tmem_ld64(tbase + lane_off + hf * 64, v64);
+            if (qd < 2) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) v64[i] = -v64[i];
+            } else {
+                const int r = tl - 64;
+                const float f = sFq[r] * expf(sG[r]);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) v64[i] = fmaf(f, qrow[i], -v64[i]);
+            }
+#pragma unroll
+            for (int k8 = 0; k8 < 64; k8 += 8)
+                put8(kqh, kql, tc::kmaj_off(tl, hf * 64 + k8, 128), &v64[k8]);
+            tc::fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                tc::bulk_s2g(gwq, tc::smem_u32(kqh), WQ_BYTES);
+                tc::bulk_commit();
+                tc::bulk_wait_read_all();   // shared memory must outlive the reads, not the writes
             }
         }
     }
@@ -500,58 +596,110 @@ __global__ void __launch_bounds__(TC_NT) chunk_tp_kernel(ChunkArgs a) {
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tbase, 64);
+    if (warp == 0) tc::tmem_dealloc(tbase, 128);
 }
 
 // ---------------------------------------------------------------------------
-// The state chain.  Shared-memory map (bytes); every bf16 tile has a hi and a
-// lo part.
+// The state chain.
+//
+// A tcgen05.mma with M = 128 costs about the same for every N up to 128, so
+// the split products of a B operand with DVS columns are issued as two MMAs
+// per 16-wide K slice instead of three: A_hi . [B_hi | B_lo] (N = 2 DVS) into
+// accumulator columns [0, 2 DVS), and A_lo . B_hi (N = DVS) into [2 DVS,
+// 3 DVS).  Such "concatenated" B operands hold the hi part in MN positions
+// [0, DVS) and the lo part in [DVS, 2 DVS) of one MN-major tile, and an
+// epilogue sums the three column blocks.
 template <int DVS>
 struct ChainSmem {
-    static constexpr int NB = 128 + DVS;                   // N of G2's B operand
-    static constexpr int WQ = 128 * 128 * 2;               // [-W ; Q'] K-major, K = 128
-    static constexpr int BW = NB * 64 * 2;                 // [bgK | bV] MN-major (MN = NB, K = 64)
-    static constexpr int KT = 128 * 64 * 2;                // K~ MN-major (MN = 128, K = 64)
-    static constexpr int MT = DVS * 128 * 2;               // M MN-major (MN = DVS, K = 128)
-    static constexpr int UT = DVS * 64 * 2;                // U' MN-major (MN = DVS, K = 64)
+    static constexpr int WQ = 128 * 128 * 2;               // [-W ; Q'] K-major, K = 128 (bulk-copied)
+    static constexpr int BV = 2 * DVS * 64 * 2;            // [bV_hi | bV_lo] MN-major (MN = 2 DVS, K = 64)
+    static constexpr int KT = 128 * 64 * 2;                // K~ MN-major (MN = 128, K = 64), per part
+    static constexpr int MT = 2 * DVS * 128 * 2;           // [M_hi | M_lo] MN-major (MN = 2 DVS, K = 128)
+    static constexpr int UT = 2 * DVS * 64 * 2;            // [U'_hi | U'_lo] MN-major (MN = 2 DVS, K = 64)
     static constexpr int OFF_WQ = 0;
-    static constexpr int OFF_BW = OFF_WQ + 2 * WQ;
-    static constexpr int OFF_KT = OFF_BW + 2 * BW;
-    static constexpr int OFF_TP = OFF_KT + 2 * KT;         // [T ; PT], bulk-copied (hi then lo)
-    static constexpr int OFF_MT = OFF_TP + TP_BYTES;
-    static constexpr int OFF_UT = OFF_MT + 2 * MT;
-    static constexpr int OFF_G = OFF_UT + 2 * UT;          // G[64], beta[64]
-    static constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;     // MMA barrier, copy barrier, tmem slot, flag
-    static constexpr int BYTES = OFF_BAR + 32;
-    static_assert(OFF_TP % 16 == 0, "bulk-copy destination alignment");
+    static constexpr int OFF_TP = OFF_WQ + 2 * WQ;         // [T ; PT] x 2 buffers, bulk-copied (hi then lo)
+    static constexpr int OFF_BV = OFF_TP + 2 * TP_BYTES;
+    static constexpr int OFF_KT = OFF_BV + BV;
+    static constexpr int OFF_MT = OFF_KT + 2 * KT;
+    static constexpr int OFF_UT = OFF_MT + MT;
+    static constexpr int OFF_G = OFF_UT + UT;              // G[64], beta[64]
+    static constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;     // MMA, WQ and 2 TP copy barriers, tmem slot, flag
+    static constexpr int BYTES = OFF_BAR + 48;
+    static_assert(OFF_TP % 16 == 0 && OFF_WQ % 16 == 0, "bulk-copy destination alignment");
 };
+
+// D (+)= A . B with a concatenated B operand (see above): two MMAs per K slice.
+template <bool A_MN, int KDIM, int DVS>
+__device__ __forceinline__ void mma2cat(uint32_t d_tmem, uint32_t a_hi, uint32_t a_lo, uint32_t a_mn,
+                                        uint32_t b_cat, bool accumulate, uint32_t trans_a) {
+    constexpr uint32_t ID2 = tc::idesc_bf16(128, 2 * DVS) | tc::kTransB;
+    constexpr uint32_t ID1 = tc::idesc_bf16(128, DVS) | tc::kTransB;
+    const uint64_t ah = A_MN ? tc::mnmaj_desc(a_hi, a_mn, 0) : tc::kmaj_desc(a_hi, KDIM, 0);
+    const uint64_t al = A_MN ? tc::mnmaj_desc(a_lo, a_mn, 0) : tc::kmaj_desc(a_lo, KDIM, 0);
+    const uint64_t b = tc::mnmaj_desc(b_cat, 2 * DVS, 0);
+    const uint32_t as = A_MN ? (a_mn >> 3) * 2u * 8u : 16u;
+    constexpr uint32_t bs = (2 * DVS >> 3) * 2u * 8u;
+#pragma unroll
+    for (int ks = 0; ks < KDIM / 16; ++ks) {
+        const uint64_t ahk = ah + (uint64_t)(ks * as), alk = al + (uint64_t)(ks * as);
+        const uint64_t bk = b + (uint64_t)(ks * bs);
+        const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+        tc::mma_bf16(d_tmem, ahk, bk, ID2 | trans_a, acc);
+        tc::mma_bf16(d_tmem + 2 * DVS, alk, bk, ID1 | trans_a, acc);
+    }
+}
+
+// Store 8 values of MN positions j8..j8+7 at row k of a concatenated tile.
+template <int DVS>
+__device__ __forceinline__ void put8cat(unsigned char *tile, int j8, int k, const float *v) {
+    __nv_bfloat162 h2[4], l2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h2[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        const float2 hf = __bfloat1622float2(h2[i]);
+        l2[i] = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+    }
+    *reinterpret_cast<uint4 *>(tile + tc::mnmaj_off(j8, k, 2 * DVS)) = *reinterpret_cast<const uint4 *>(h2);
+    *reinterpret_cast<uint4 *>(tile + tc::mnmaj_off(DVS + j8, k, 2 * DVS)) = *reinterpret_cast<const uint4 *>(l2);
+}
+
+// Sum of the three column blocks of a concatenated accumulator, columns c0..c0+15.
+template <int DVS>
+__device__ __forceinline__ void tmem_ld_cat16(uint32_t taddr, float (&v)[16]) {
+    float x[16], y[16];
+    tmem_ld<16>(taddr, v);
+    tmem_ld<16>(taddr + DVS, x);
+    tmem_ld<16>(taddr + 2 * DVS, y);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] += x[i] + y[i];
+}
 
 template <int DVS, typename TIn, typename TOut>
 __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     using L = ChainSmem<DVS>;
     constexpr int HALF = DVS / 2;                 // state columns per thread in lane mapping
     constexpr int VQ = DVS / 4;                   // v columns per thread in row mapping
-    constexpr int NB = L::NB;
+    static_assert(HALF == 16, "epilogues load 16 columns per block");
     extern __shared__ __align__(1024) unsigned char sm[];
-    unsigned char *wqh = sm + L::OFF_WQ, *wql = wqh + L::WQ;
-    unsigned char *bwh = sm + L::OFF_BW, *bwl = bwh + L::BW;
+    unsigned char *wqh = sm + L::OFF_WQ;
+    unsigned char *bvt = sm + L::OFF_BV;
     unsigned char *kth = sm + L::OFF_KT, *ktl = kth + L::KT;
-    unsigned char *tph = sm + L::OFF_TP, *tpl = tph + TP_HALF;
-    unsigned char *mth = sm + L::OFF_MT, *mtl = mth + L::MT;
-    unsigned char *uth = sm + L::OFF_UT, *utl = uth + L::UT;
+    unsigned char *mtt = sm + L::OFF_MT;
+    unsigned char *utt = sm + L::OFF_UT;
     float *sG = reinterpret_cast<float *>(sm + L::OFF_G);
     float *sB = sG + 64;
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
-    uint64_t *tpbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR + 8);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 16);
-    volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 20);
+    uint64_t *wqbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR + 8);
+    uint64_t *tpbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR + 16);   // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 32);
+    volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 36);
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int kh = h / d.grp;
     const int col0 = h * TC_DK + slice * DVS;      // this slice's first column in o / v / state
-    const int rr = tid >> 2, cq = tid & 3;         // row mapping (staging)
+    const int rr = stage_row(tid), cq = stage_quarter(tid);   // row mapping (staging)
     const int qd = warp & 3, hf = warp >> 2;       // lane mapping (TMEM epilogues)
     const int tl = qd * 32 + lane;
 
@@ -567,7 +715,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
             o[t * ldo + col0 + tid % DVS] = from_f32<TOut>(0.f);
         return;
     }
-    // this sequence's chunks in the [T ; PT] workspace (a malformed map is reported, not followed)
+    // this sequence's chunks in the workspace (a malformed map is reported, not followed)
     long long jc = 0;
     if (s < e) {
         jc = a.chunk_base[n];
@@ -576,6 +724,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
             e = s;
         }
     }
+    const long long n_chunks = (e - s + TC_C - 1) / TC_C;
 
     if (warp == 0) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
@@ -583,36 +732,41 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     }
     if (tid == 32) {
         tc::mbar_init(tc::smem_u32(mbar), 1);
-        tc::mbar_init(tc::smem_u32(tpbar), 1);
+        tc::mbar_init(tc::smem_u32(wqbar), 1);
+        tc::mbar_init(tc::smem_u32(&tpbar[0]), 1);
+        tc::mbar_init(tc::smem_u32(&tpbar[1]), 1);
         tc::mbar_fence_init();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tmem_slot;
-    const uint32_t T_D2 = tbase, T_D3 = tbase + 128, T_D5 = tbase + 128 + DVS;
+    const uint32_t T_D3 = tbase, T_D5 = tbase + 3 * DVS;     // concatenated accumulators
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     MmaSync ms{mbar, wait_flag, 0u};
-    uint32_t tp_phase = 0;
     bool timed_out = false;
+    constexpr int FETCHER = 32;                    // issues the operand copies (not the MMA thread)
 
-    constexpr uint32_t ID_G2 = tc::idesc_bf16(128, NB) | tc::kTransB;
-    constexpr uint32_t ID_G3 = tc::idesc_bf16(128, DVS) | tc::kTransB;
-    constexpr uint32_t ID_G5 = tc::idesc_bf16(128, DVS) | tc::kTransA | tc::kTransB;
-    const uint32_t s_wqh = tc::smem_u32(wqh), s_wql = tc::smem_u32(wql);
-    const uint32_t s_bwh = tc::smem_u32(bwh), s_bwl = tc::smem_u32(bwl);
+    const uint32_t s_wqh = tc::smem_u32(wqh), s_wql = s_wqh + L::WQ;
+    const uint32_t s_tp = tc::smem_u32(sm + L::OFF_TP);
+    const uint32_t s_bv = tc::smem_u32(bvt);
     const uint32_t s_kth = tc::smem_u32(kth), s_ktl = tc::smem_u32(ktl);
-    const uint32_t s_tph = tc::smem_u32(tph), s_tpl = tc::smem_u32(tpl);
-    const uint32_t s_mth = tc::smem_u32(mth), s_mtl = tc::smem_u32(mtl);
-    const uint32_t s_uth = tc::smem_u32(uth), s_utl = tc::smem_u32(utl);
+    const uint32_t s_mt = tc::smem_u32(mtt);
+    const uint32_t s_ut = tc::smem_u32(utt);
 
-    // [T ; PT] of chunk i of this sequence -> TP (thread 0)
+    // Operands of chunk i of this sequence (thread FETCHER): [T ; PT] -> TP buffer i&1,
+    // [-W ; Q'] -> WQ
     auto fetch_tp = [&](long long i) {
-        const unsigned char *src = a.tp + ((jc + i) * d.hv + h) * TP_BYTES;
-        const uint32_t mb = tc::smem_u32(tpbar);
+        const unsigned char *src = a.tp + ((jc + i) * d.hv + h) * CH_BYTES;
+        const uint32_t mb = tc::smem_u32(&tpbar[i & 1]);
         tc::mbar_arrive_expect_tx(mb, TP_BYTES);
-        tc::bulk_g2s(s_tph, src, TP_HALF, mb);
-        tc::bulk_g2s(s_tpl, src + TP_HALF, TP_HALF, mb);
+        tc::bulk_g2s(s_tp + (uint32_t)((i & 1) * TP_BYTES), src, TP_BYTES, mb);
+    };
+    auto fetch_wq = [&](long long i) {
+        const unsigned char *src = a.tp + ((jc + i) * d.hv + h) * CH_BYTES + TP_BYTES;
+        const uint32_t mb = tc::smem_u32(wqbar);
+        tc::mbar_arrive_expect_tx(mb, WQ_BYTES);
+        tc::bulk_g2s(s_wqh, src, WQ_BYTES, mb);
     };
 
     // ---- initial state: thread (lane tl = dk row, half hf) holds M[tl][hf*HALF ..]
@@ -627,26 +781,24 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
             for (int jj = 0; jj < HALF; ++jj) Mr[jj] = 0.f;
         }
 #pragma unroll
-        for (int j8 = 0; j8 < HALF; j8 += 8) put8(mth, mtl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &Mr[j8]);
+        for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(mtt, hf * HALF + j8, tl, &Mr[j8]);
     }
 
-    const TIn *qg = (const TIn *)a.q + (long long)kh * TC_DK + cq * 32;
     const TIn *kg = (const TIn *)a.k + (long long)kh * TC_DK + cq * 32;
     const TIn *vg = (const TIn *)a.v + col0 + cq * VQ;
     const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
 
     // Raw rows of the chunk at c0 (row rr of the row mapping) and its gates: the
-    // loads of chunk c+1 are issued while chunk c's first MMA group runs.
-    float kv[32], qv[32], vv[VQ];
+    // loads of chunk c+1 are issued while chunk c's MMAs run.
+    float kv[32], vv[VQ];
     auto load_chunk = [&](long long c0) {
         const long long t = c0 + rr;
         if (t < e) {
             load_row<32>(kg + t * a.ld_qk, kv);
-            load_row<32>(qg + t * a.ld_qk, qv);
             load_row<VQ>(vg + t * a.ld_v, vv);
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
+            for (int i = 0; i < 32; ++i) kv[i] = 0.f;
 #pragma unroll
             for (int i = 0; i < VQ; ++i) vv[i] = 0.f;
         }
@@ -659,110 +811,94 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
             bn = t < e ? a.beta[t * d.hv + h] : 0.f;
         }
     };
+    // L2 prefetch of the rows and gates of the chunk at c0 (two chunks ahead of use)
+    auto prefetch_chunk = [&](long long c0) {
+        const long long t = c0 + rr;
+        if (t < e) {
+            tc::prefetch_l2(kg + t * a.ld_qk);
+            tc::prefetch_l2(vg + t * a.ld_v);
+        }
+        if (tid < TC_C && c0 + tid < e) {
+            tc::prefetch_l2(a.g + (c0 + tid) * d.hv + h);
+            tc::prefetch_l2(a.beta + (c0 + tid) * d.hv + h);
+        }
+    };
+    long long wq_last = 0, tp_last = n_chunks > 1 ? 1 : 0;   // last chunk fetched into each
     if (s < e) {
-        if (tid == 0) fetch_tp(0);
+        if (tid == FETCHER) {
+            fetch_tp(0);
+            if (n_chunks > 1) fetch_tp(1);
+            fetch_wq(0);
+        }
         load_chunk(s);
         load_gates(s);
-        if (tid < TC_C) {
-            sG[tid] = gn;
-            sB[tid] = bn;
-        }
+        if (s + TC_C < e) prefetch_chunk(s + TC_C);
     }
 
     long long ci = 0;
     for (long long c0 = s; c0 < e; c0 += TC_C, ++ci) {
         const int Lc = (int)((e - c0) < TC_C ? (e - c0) : TC_C);
         const bool has_next = c0 + TC_C < e;
-        // ---------------- S0: L2 norm of the staged rows; gate scan
-        if (l2) {
-            l2norm_row4(kv, d.l2_eps, 1.f);
-            l2norm_row4(qv, d.l2_eps, d.q_scale);
+        // ---------------- S0: L2 norm of the staged k rows; gate scan
+        if (tid < TC_C) {  // (nothing reads sG / sB after the previous chunk's S0)
+            sG[tid] = gn;
+            sB[tid] = bn;
         }
+        if (l2) l2norm_row4(kv, d.l2_eps, 1.f);
         __syncthreads();   // raw gates of this chunk are in sG / sB
         if (warp == 0) scan64(sG, lane);
         __syncthreads();
-        const float Gr = sG[rr], br = sB[rr], Gl = sG[TC_C - 1];
-        const float gq = expf(Gr), bg = br * gq, kdec = expf(Gl - Gr);
-        // ---------------- S2: [bgK | bV] and K~ (MN-major), gamma Q (rows 64-127 of WQ)
+        const float br = sB[rr], Gl = sG[TC_C - 1];
+        const float kdec = expf(Gl - sG[rr]);
+        // ---------------- S2: K~ (MN-major) and [bV_hi | bV_lo]
 #pragma unroll
         for (int k8 = 0; k8 < 32; k8 += 8) {
             float t8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) t8[i] = bg * kv[k8 + i];
-            put8(bwh, bwl, tc::mnmaj_off(cq * 32 + k8, rr, NB), t8);
-#pragma unroll
             for (int i = 0; i < 8; ++i) t8[i] = kdec * kv[k8 + i];
             put8(kth, ktl, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) t8[i] = gq * qv[k8 + i];
-            put8(wqh, wql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), t8);
         }
 #pragma unroll
         for (int k8 = 0; k8 < VQ; k8 += 8) {
             float t8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) t8[i] = br * vv[k8 + i];
-            put8(bwh, bwl, tc::mnmaj_off(128 + cq * VQ + k8, rr, NB), t8);
+            put8cat<DVS>(bvt, cq * VQ + k8, rr, t8);
         }
         sync_for_mma();
-        // ---------------- G2: [T ; PT] . [bgK | bV] -> W | U (lanes 0-63), PW | PU (64-127)
+        // ---------------- G2 + G3 (one accumulator, issued back to back):
+        //   D3  = [T ; PT] . bV           -> U, PU
+        //   D3 += [-W ; Q'] . M           -> U' (lanes 0-63), O (64-127)
         bool issued = true;
         if (tid == 0) {
-            issued = tc::mbar_wait(tc::smem_u32(tpbar), tp_phase);
-            if (issued) {
-                mma3<false, true, 64>(T_D2, s_tph, s_tpl, 0, s_bwh, s_bwl, NB, ID_G2, false);
-                tc::mma_commit(tc::smem_u32(mbar));
-            }
+            const uint32_t tb = s_tp + (uint32_t)((ci & 1) * TP_BYTES);
+            const bool tp_ok = tc::mbar_wait(tc::smem_u32(&tpbar[ci & 1]), (uint32_t)((ci >> 1) & 1));
+            if (tp_ok) mma2cat<false, 64, DVS>(T_D3, tb, tb + TP_HALF, 0, s_bv, false, 0u);
+            issued = tp_ok && tc::mbar_wait(tc::smem_u32(wqbar), (uint32_t)(ci & 1));
+            if (issued) mma2cat<false, 128, DVS>(T_D3, s_wqh, s_wql, 0, s_mt, true, 0u);
+            if (tp_ok) tc::mma_commit(tc::smem_u32(mbar));   // (what was issued can be waited for)
         }
-        tp_phase ^= 1u;
-        if (has_next) {               // next chunk's rows and gates, in flight during G2 / G3
+        if (has_next) {               // next chunk's rows and gates, in flight during the MMAs
             load_chunk(c0 + TC_C);
             load_gates(c0 + TC_C);
+            if (c0 + 2 * TC_C < e) prefetch_chunk(c0 + 2 * TC_C);
         }
         if (!ms.wait(tid, issued)) { timed_out = true; break; }
-        if (tid == 0 && has_next) fetch_tp(ci + 1);     // TP is free once G2 has completed
-        // ---------------- E2: -W -> WQ rows 0-63; Q' = gamma Q - PW -> WQ rows 64-127
-        {
-            float v32[32];
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const int cb = hf * 64 + part * 32;
-                tc::tmem_ld32(T_D2 + lane_off + cb, v32);
-#pragma unroll
-                for (int k8 = 0; k8 < 32; k8 += 8) {
-                    const uint32_t off = tc::kmaj_off(tl, cb + k8, 128);
-                    float t8[8];
-                    if (qd < 2) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) t8[i] = -v32[k8 + i];
-                    } else {
-                        get8(wqh, wql, off, t8);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) t8[i] -= v32[k8 + i];
-                    }
-                    put8(wqh, wql, off, t8);
-                }
+        if (has_next) {                     // into the buffers G2 / G3 just consumed
+            if (tid == FETCHER) fetch_wq(ci + 1);
+            wq_last = ci + 1;
+            if (ci + 2 < n_chunks) {
+                if (tid == FETCHER) fetch_tp(ci + 2);
+                tp_last = ci + 2;
             }
         }
-        sync_for_mma();
-        // ---------------- G3: D3 += [-W ; Q'] . M -> U' (lanes 0-63), O (64-127)
-        if (tid == 0) {
-            mma3<false, true, 128>(T_D3, s_wqh, s_wql, 0, s_mth, s_mtl, DVS, ID_G3, true);
-            tc::mma_commit(tc::smem_u32(mbar));
-        }
-        if (has_next && tid < TC_C) {
-            sG[tid] = gn;       // this chunk's gates are in registers by now
-            sB[tid] = bn;
-        }
-        if (!ms.wait(tid)) { timed_out = true; break; }
-        // ---------------- E3: U' -> MN-major B operand; O rows -> o
+        // ---------------- E3: U' -> concatenated B operand; O rows -> o
         {
             float v[HALF];
-            tmem_ld<HALF>(T_D3 + lane_off + hf * HALF, v);
+            tmem_ld_cat16<DVS>(T_D3 + lane_off + hf * HALF, v);
             if (qd < 2) {
 #pragma unroll
-                for (int j8 = 0; j8 < HALF; j8 += 8)
-                    put8(uth, utl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &v[j8]);
+                for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(utt, hf * HALF + j8, tl, &v[j8]);
             } else {
                 const int r = tl - 64;
                 if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, v);
@@ -771,19 +907,19 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
         sync_for_mma();
         // ---------------- G5: dM = K~^T U'
         if (tid == 0) {
-            mma3<true, true, 64>(T_D5, s_kth, s_ktl, 128, s_uth, s_utl, DVS, ID_G5, false);
+            mma2cat<true, 64, DVS>(T_D5, s_kth, s_ktl, 128, s_ut, false, tc::kTransA);
             tc::mma_commit(tc::smem_u32(mbar));
         }
         if (!ms.wait(tid)) { timed_out = true; break; }
         // ---------------- E5: M <- gamma_last M + dM
         {
             float v[HALF];
-            tmem_ld<HALF>(T_D5 + lane_off + hf * HALF, v);
+            tmem_ld_cat16<DVS>(T_D5 + lane_off + hf * HALF, v);
             const float gl = expf(Gl);
 #pragma unroll
             for (int jj = 0; jj < HALF; ++jj) Mr[jj] = gl * Mr[jj] + v[jj];
 #pragma unroll
-            for (int j8 = 0; j8 < HALF; j8 += 8) put8(mth, mtl, tc::mnmaj_off(hf * HALF + j8, tl, DVS), &Mr[j8]);
+            for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(mtt, hf * HALF + j8, tl, &Mr[j8]);
         }
         // (the next chunk's operand writes are followed by sync_for_mma before G2)
     }
@@ -792,7 +928,11 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
         if (tid == 0) {
             set_error(a.err, GDN_DEVERR_TIMEOUT);
             tc::mbar_wait(tc::smem_u32(mbar), ms.phase);
-            tc::mbar_wait(tc::smem_u32(tpbar), tp_phase);
+            // the last copies issued into each buffer may still be in flight
+            tc::mbar_wait(tc::smem_u32(wqbar), (uint32_t)(wq_last & 1));
+            tc::mbar_wait(tc::smem_u32(&tpbar[tp_last & 1]), (uint32_t)((tp_last >> 1) & 1));
+            if (tp_last >= 1)
+                tc::mbar_wait(tc::smem_u32(&tpbar[(tp_last - 1) & 1]), (uint32_t)(((tp_last - 1) >> 1) & 1));
         }
         __syncthreads();
     }
@@ -840,7 +980,7 @@ size_t chunk_tc_ws_bytes(const Dims &d, long long T, long long n_seqs) {
     const long long mc = chunk_tc_max_chunks(T, n_seqs);
     if (mc == 0) return 0;
     const size_t base = (((size_t)n_seqs + 1) * 4 + 255) & ~(size_t)255;
-    return base + (size_t)mc * d.hv * TP_BYTES;
+    return base + (size_t)mc * d.hv * CH_BYTES;
 }
 
 void chunk_tc_carve(ChunkArgs &a, void *ws) {
