@@ -50,7 +50,12 @@ constexpr int TC_DK = 128;   // dk == dv
 constexpr int TP_HALF = 128 * 64 * 2;     // one bf16 part of [T ; PT] (K-major, K = 64)
 constexpr int TP_BYTES = 2 * TP_HALF;     // hi + lo, as stored in the workspace
 constexpr int WQ_BYTES = 2 * 128 * 128 * 2;             // [-W ; Q'] hi + lo (K-major, K = 128)
-constexpr int CH_BYTES = TP_BYTES + WQ_BYTES;           // workspace bytes per (chunk, v-head)
+constexpr int KT_HALF = 128 * 64 * 2;                   // K~ (MN-major, MN = 128, K = 64), one part
+constexpr int KT_BYTES = 2 * KT_HALF;
+constexpr int CH_DVS = 32;                              // state columns per chain CTA
+constexpr int BV_SLICE = 2 * CH_DVS * 64 * 2;           // [bV_hi | bV_lo] of one slice (MN-major, MN = 64, K = 64)
+constexpr int OFF_CH_WQ = TP_BYTES, OFF_CH_KT = OFF_CH_WQ + WQ_BYTES, OFF_CH_BV = OFF_CH_KT + KT_BYTES;
+constexpr int CH_BYTES = OFF_CH_BV + (128 / CH_DVS) * BV_SLICE;   // workspace bytes per (chunk, v-head)
 
 // Store 8 values at byte offset `off` (16-byte aligned) of a hi and a lo tile
 // (packed two-at-a-time conversions).
@@ -142,6 +147,22 @@ __device__ __forceinline__ void mma3(uint32_t d_tmem, uint32_t a_hi, uint32_t a_
         tc::mma_bf16(d_tmem, ahk, blk, idesc, 1u);
         tc::mma_bf16(d_tmem, alk, bhk, idesc, 1u);
     }
+}
+
+// Store 8 values at MN positions j8..j8+7, row k, of a "concatenated" tile: one
+// MN-major bf16 tile (MN = 2 DVS) holding the hi parts at MN [0, DVS) and the
+// lo parts at [DVS, 2 DVS) (shared or global memory).
+template <int DVS>
+__device__ __forceinline__ void put8cat(unsigned char *tile, int j8, int k, const float *v) {
+    __nv_bfloat162 h2[4], l2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h2[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        const float2 hf = __bfloat1622float2(h2[i]);
+        l2[i] = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+    }
+    *reinterpret_cast<uint4 *>(tile + tc::mnmaj_off(j8, k, 2 * DVS)) = *reinterpret_cast<const uint4 *>(h2);
+    *reinterpret_cast<uint4 *>(tile + tc::mnmaj_off(DVS + j8, k, 2 * DVS)) = *reinterpret_cast<const uint4 *>(l2);
 }
 
 // Shared pieces of the per-CTA setup: one thread polls the MMA barrier
@@ -321,7 +342,7 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     seq_bounds(a.cu_seqlens, lo, a.T, nullptr, s, e);   // malformed bounds are reported by the map
     const long long t0 = s + (j - a.chunk_base[lo]) * TC_C;
     unsigned char *gtp = a.tp + ((long long)j * d.hv + h) * CH_BYTES;   // [T ; PT]
-    unsigned char *gwq = gtp + TP_BYTES;                                 // [-W ; Q']
+    unsigned char *gwq = gtp + OFF_CH_WQ;                                // [-W ; Q']
 
     if (warp == 0) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), 128);
@@ -363,7 +384,9 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
         if (l2) l2norm_row4(kv, d.l2_eps, 1.f);
         if (cq == 0) sFq[rr] = fq;
         __syncthreads();
-        const float bg = sB[rr] * expf(sG[rr]);
+        const float Gr = sG[rr], br = sB[rr], Gl = sG[TC_C - 1];
+        const float bg = br * expf(Gr), kdec = expf(Gl - Gr);
+        unsigned char *gkt = gtp + OFF_CH_KT;
 #pragma unroll
         for (int k8 = 0; k8 < 32; k8 += 8) {
             put8(kqh, kql, tc::kmaj_off(rr, cq * 32 + k8, 128), &kv[k8]);
@@ -372,7 +395,30 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) t8[i] = bg * kv[k8 + i];
             put8(b3h, b3l, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
+            // the chain's G5 operand: K~ = exp(G_last - G_r) k_r (MN-major), to the workspace
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = kdec * kv[k8 + i];
+            put8(gkt, gkt + KT_HALF, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
         }
+        // the chain's G2 operand: beta v of the state slice cq (its 32 columns), as a
+        // concatenated [hi | lo] tile (MN-major, MN = 64), to the workspace
+        {
+            float vv[32];
+            if (t < e) load_row<32>((const TIn *)a.v + t * a.ld_v + (long long)h * TC_DK + cq * 32, vv);
+            else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) vv[i] = 0.f;
+            }
+            unsigned char *gbv = gtp + OFF_CH_BV + cq * BV_SLICE;
+#pragma unroll
+            for (int k8 = 0; k8 < 32; k8 += 8) {
+                float t8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t8[i] = br * vv[k8 + i];
+                put8cat<CH_DVS>(gbv, k8, rr, t8);
+            }
+        }
+        if (tid == 0) a.gl[j * d.hv + h] = Gl;
     }
     sync_for_mma();
     // ---- G1: [K;Q] K^T -> K K^T (TMEM lanes 0-63), Q K^T (64-127), columns 0-63
@@ -611,21 +657,20 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
 // epilogue sums the three column blocks.
 template <int DVS>
 struct ChainSmem {
-    static constexpr int WQ = 128 * 128 * 2;               // [-W ; Q'] K-major, K = 128 (bulk-copied)
-    static constexpr int BV = 2 * DVS * 64 * 2;            // [bV_hi | bV_lo] MN-major (MN = 2 DVS, K = 64)
-    static constexpr int KT = 128 * 64 * 2;                // K~ MN-major (MN = 128, K = 64), per part
+    static constexpr int WQ = 128 * 128 * 2;               // [-W ; Q'] K-major, K = 128, per part
     static constexpr int MT = 2 * DVS * 128 * 2;           // [M_hi | M_lo] MN-major (MN = 2 DVS, K = 128)
     static constexpr int UT = 2 * DVS * 64 * 2;            // [U'_hi | U'_lo] MN-major (MN = 2 DVS, K = 64)
+    // bulk-copied from the workspace: WQ (hi then lo), [T ; PT] x 2 buffers, [bV_hi | bV_lo], K~ (hi then lo)
     static constexpr int OFF_WQ = 0;
-    static constexpr int OFF_TP = OFF_WQ + 2 * WQ;         // [T ; PT] x 2 buffers, bulk-copied (hi then lo)
+    static constexpr int OFF_TP = OFF_WQ + 2 * WQ;
     static constexpr int OFF_BV = OFF_TP + 2 * TP_BYTES;
-    static constexpr int OFF_KT = OFF_BV + BV;
-    static constexpr int OFF_MT = OFF_KT + 2 * KT;
+    static constexpr int OFF_KT = OFF_BV + BV_SLICE;
+    static constexpr int OFF_MT = OFF_KT + KT_BYTES;
     static constexpr int OFF_UT = OFF_MT + MT;
-    static constexpr int OFF_G = OFF_UT + UT;              // G[64], beta[64]
-    static constexpr int OFF_BAR = OFF_G + 2 * 64 * 4;     // MMA, WQ and 2 TP copy barriers, tmem slot, flag
-    static constexpr int BYTES = OFF_BAR + 48;
-    static_assert(OFF_TP % 16 == 0 && OFF_WQ % 16 == 0, "bulk-copy destination alignment");
+    static constexpr int OFF_BAR = OFF_UT + UT;            // 9 mbarriers, tmem slot, flags
+    static constexpr int BYTES = OFF_BAR + 96;
+    static_assert(DVS == CH_DVS, "the workspace holds bV in slices of CH_DVS columns");
+    static_assert(OFF_TP % 16 == 0 && OFF_BV % 16 == 0 && OFF_KT % 16 == 0, "bulk-copy alignment");
 };
 
 // D (+)= A . B with a concatenated B operand (see above): two MMAs per K slice.
@@ -649,20 +694,6 @@ __device__ __forceinline__ void mma2cat(uint32_t d_tmem, uint32_t a_hi, uint32_t
     }
 }
 
-// Store 8 values of MN positions j8..j8+7 at row k of a concatenated tile.
-template <int DVS>
-__device__ __forceinline__ void put8cat(unsigned char *tile, int j8, int k, const float *v) {
-    __nv_bfloat162 h2[4], l2[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        h2[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-        const float2 hf = __bfloat1622float2(h2[i]);
-        l2[i] = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
-    }
-    *reinterpret_cast<uint4 *>(tile + tc::mnmaj_off(j8, k, 2 * DVS)) = *reinterpret_cast<const uint4 *>(h2);
-    *reinterpret_cast<uint4 *>(tile + tc::mnmaj_off(DVS + j8, k, 2 * DVS)) = *reinterpret_cast<const uint4 *>(l2);
-}
-
 // Sum of the three column blocks of a concatenated accumulator, columns c0..c0+15.
 template <int DVS>
 __device__ __forceinline__ void tmem_ld_cat16(uint32_t taddr, float (&v)[16]) {
@@ -674,34 +705,64 @@ __device__ __forceinline__ void tmem_ld_cat16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] += x[i] + y[i];
 }
 
+// Warp roles: warp 8 copies every operand of the state chain from the
+// workspace (bulk copies) and issues every MMA; warps 0-7 (256 threads) run
+// the two epilogues, which carry the state.  The sides meet only on
+// mbarriers, each wait bounded in time, so a lost arrival ends in an error
+// flag rather than a hang:
+//   mtbar (256 arrivals)  M entering chunk c is in shared memory
+//   utbar (256 arrivals)  U' of chunk c is in shared memory
+//   g3bar (MMA commit)    D3 of chunk c complete (G2 + G3)
+//   g5bar (MMA commit)    D5 of chunk c complete (G5)
+//   wq/tp/bv/kt bars      operand copies landed
+// Phase c of each completes once per chunk, and no phase can complete twice
+// before its waiter looks, because each depends on the other side's progress.
+// The critical path is M -> G3 -> E3 -> G5 -> E5 -> M; G2 of chunk c+1 is
+// issued right behind G5 of chunk c.
+constexpr int CHAIN_NT = 288;
+
+__device__ __forceinline__ void bar_sync_staging() {   // warps 0-7 only
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// One epilogue thread polls an MMA barrier (bounded); the epilogue warps then
+// agree on the outcome through `flag` (one flag per barrier, so that the
+// next wait never overwrites a value a slow thread has yet to read).
+__device__ __forceinline__ bool staging_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *flag,
+                                             int tid) {
+    if (tid == 0) *flag = tc::mbar_wait(tc::smem_u32(bar), parity) ? 0u : 1u;
+    bar_sync_staging();
+    const bool ok = *flag == 0u;
+    tc::fence_after_sync();
+    return ok;
+}
+
+// every epilogue thread: its shared-memory operand writes -> visible to the tensor core
+__device__ __forceinline__ void arrive_staged(uint64_t *bar) {
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    tc::mbar_arrive(tc::smem_u32(bar));
+}
+
 template <int DVS, typename TIn, typename TOut>
-__global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
+__global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     using L = ChainSmem<DVS>;
     constexpr int HALF = DVS / 2;                 // state columns per thread in lane mapping
-    constexpr int VQ = DVS / 4;                   // v columns per thread in row mapping
     static_assert(HALF == 16, "epilogues load 16 columns per block");
     extern __shared__ __align__(1024) unsigned char sm[];
-    unsigned char *wqh = sm + L::OFF_WQ;
-    unsigned char *bvt = sm + L::OFF_BV;
-    unsigned char *kth = sm + L::OFF_KT, *ktl = kth + L::KT;
     unsigned char *mtt = sm + L::OFF_MT;
     unsigned char *utt = sm + L::OFF_UT;
-    float *sG = reinterpret_cast<float *>(sm + L::OFF_G);
-    float *sB = sG + 64;
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
-    uint64_t *wqbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR + 8);
-    uint64_t *tpbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR + 16);   // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 32);
-    volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 36);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
+    uint64_t *wqbar = bars + 0, *tpbar = bars + 1 /* [2] */, *bvbar = bars + 3, *ktbar = bars + 4,
+             *mtbar = bars + 5, *utbar = bars + 6, *g3bar = bars + 7, *g5bar = bars + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
+    volatile uint32_t *flag3 = reinterpret_cast<uint32_t *>(bars + 9) + 1;
+    volatile uint32_t *flag5 = reinterpret_cast<uint32_t *>(bars + 10);
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
-    const int kh = h / d.grp;
     const int col0 = h * TC_DK + slice * DVS;      // this slice's first column in o / v / state
-    const int rr = stage_row(tid), cq = stage_quarter(tid);   // row mapping (staging)
-    const int qd = warp & 3, hf = warp >> 2;       // lane mapping (TMEM epilogues)
-    const int tl = qd * 32 + lane;
 
     long long s, e;
     seq_bounds(a.cu_seqlens, n, a.T, a.err, s, e);
@@ -711,7 +772,7 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     TOut *o = (TOut *)a.o;
     const long long ldo = (long long)d.hv * TC_DK;
     if (a.state_idx && slot < 0) {
-        for (long long t = s + tid / DVS; t < e; t += TC_NT / DVS)
+        for (long long t = s + tid / DVS; t < e; t += CHAIN_NT / DVS)
             o[t * ldo + col0 + tid % DVS] = from_f32<TOut>(0.f);
         return;
     }
@@ -731,10 +792,15 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
         tc::tmem_relinquish();
     }
     if (tid == 32) {
-        tc::mbar_init(tc::smem_u32(mbar), 1);
         tc::mbar_init(tc::smem_u32(wqbar), 1);
         tc::mbar_init(tc::smem_u32(&tpbar[0]), 1);
         tc::mbar_init(tc::smem_u32(&tpbar[1]), 1);
+        tc::mbar_init(tc::smem_u32(bvbar), 1);
+        tc::mbar_init(tc::smem_u32(ktbar), 1);
+        tc::mbar_init(tc::smem_u32(mtbar), 256);
+        tc::mbar_init(tc::smem_u32(utbar), 256);
+        tc::mbar_init(tc::smem_u32(g3bar), 1);
+        tc::mbar_init(tc::smem_u32(g5bar), 1);
         tc::mbar_fence_init();
     }
     tc::fence_before_sync();
@@ -742,204 +808,152 @@ __global__ void __launch_bounds__(TC_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     tc::fence_after_sync();
     const uint32_t tbase = *tmem_slot;
     const uint32_t T_D3 = tbase, T_D5 = tbase + 3 * DVS;     // concatenated accumulators
-    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-    MmaSync ms{mbar, wait_flag, 0u};
-    bool timed_out = false;
-    constexpr int FETCHER = 32;                    // issues the operand copies (not the MMA thread)
 
-    const uint32_t s_wqh = tc::smem_u32(wqh), s_wql = s_wqh + L::WQ;
-    const uint32_t s_tp = tc::smem_u32(sm + L::OFF_TP);
-    const uint32_t s_bv = tc::smem_u32(bvt);
-    const uint32_t s_kth = tc::smem_u32(kth), s_ktl = tc::smem_u32(ktl);
-    const uint32_t s_mt = tc::smem_u32(mtt);
-    const uint32_t s_ut = tc::smem_u32(utt);
-
-    // Operands of chunk i of this sequence (thread FETCHER): [T ; PT] -> TP buffer i&1,
-    // [-W ; Q'] -> WQ
-    auto fetch_tp = [&](long long i) {
-        const unsigned char *src = a.tp + ((jc + i) * d.hv + h) * CH_BYTES;
-        const uint32_t mb = tc::smem_u32(&tpbar[i & 1]);
-        tc::mbar_arrive_expect_tx(mb, TP_BYTES);
-        tc::bulk_g2s(s_tp + (uint32_t)((i & 1) * TP_BYTES), src, TP_BYTES, mb);
-    };
-    auto fetch_wq = [&](long long i) {
-        const unsigned char *src = a.tp + ((jc + i) * d.hv + h) * CH_BYTES + TP_BYTES;
-        const uint32_t mb = tc::smem_u32(wqbar);
-        tc::mbar_arrive_expect_tx(mb, WQ_BYTES);
-        tc::bulk_g2s(s_wqh, src, WQ_BYTES, mb);
-    };
-
-    // ---- initial state: thread (lane tl = dk row, half hf) holds M[tl][hf*HALF ..]
-    float Mr[HALF];
-    {
-        if (a.state_in && slot >= 0) {
-            const float *sin = a.state_in + ((long long)slot * d.hv + h) * TC_DK * TC_DK +
-                               (long long)tl * TC_DK + slice * DVS + hf * HALF;
-            load_row<HALF>(sin, Mr);
-        } else {
-#pragma unroll
-            for (int jj = 0; jj < HALF; ++jj) Mr[jj] = 0.f;
-        }
-#pragma unroll
-        for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(mtt, hf * HALF + j8, tl, &Mr[j8]);
-    }
-
-    const TIn *kg = (const TIn *)a.k + (long long)kh * TC_DK + cq * 32;
-    const TIn *vg = (const TIn *)a.v + col0 + cq * VQ;
-    const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
-
-    // Raw rows of the chunk at c0 (row rr of the row mapping) and its gates: the
-    // loads of chunk c+1 are issued while chunk c's MMAs run.
-    float kv[32], vv[VQ];
-    auto load_chunk = [&](long long c0) {
-        const long long t = c0 + rr;
-        if (t < e) {
-            load_row<32>(kg + t * a.ld_qk, kv);
-            load_row<VQ>(vg + t * a.ld_v, vv);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) kv[i] = 0.f;
-#pragma unroll
-            for (int i = 0; i < VQ; ++i) vv[i] = 0.f;
-        }
-    };
-    float gn = 0.f, bn = 0.f;     // gates of the next chunk (threads tid < 64)
-    auto load_gates = [&](long long c0) {
-        if (tid < TC_C) {
-            const long long t = c0 + tid;
-            gn = t < e ? a.g[t * d.hv + h] : 0.f;
-            bn = t < e ? a.beta[t * d.hv + h] : 0.f;
-        }
-    };
-    // L2 prefetch of the rows and gates of the chunk at c0 (two chunks ahead of use)
-    auto prefetch_chunk = [&](long long c0) {
-        const long long t = c0 + rr;
-        if (t < e) {
-            tc::prefetch_l2(kg + t * a.ld_qk);
-            tc::prefetch_l2(vg + t * a.ld_v);
-        }
-        if (tid < TC_C && c0 + tid < e) {
-            tc::prefetch_l2(a.g + (c0 + tid) * d.hv + h);
-            tc::prefetch_l2(a.beta + (c0 + tid) * d.hv + h);
-        }
-    };
-    long long wq_last = 0, tp_last = n_chunks > 1 ? 1 : 0;   // last chunk fetched into each
-    if (s < e) {
-        if (tid == FETCHER) {
+    if (warp == 8) {
+        // ============ copy and MMA warp (lane 0 issues everything) ============
+        if (lane == 0 && n_chunks > 0) {
+            const uint32_t s_wqh = tc::smem_u32(sm + L::OFF_WQ), s_wql = s_wqh + L::WQ;
+            const uint32_t s_tp = tc::smem_u32(sm + L::OFF_TP), s_bv = tc::smem_u32(sm + L::OFF_BV);
+            const uint32_t s_kth = tc::smem_u32(sm + L::OFF_KT), s_ktl = s_kth + KT_HALF;
+            const uint32_t s_mt = tc::smem_u32(mtt), s_ut = tc::smem_u32(utt);
+            auto src = [&](long long i) { return a.tp + ((jc + i) * d.hv + h) * CH_BYTES; };
+            auto fetch = [&](uint64_t *bar, uint32_t dst, const unsigned char *from, uint32_t bytes) {
+                const uint32_t mb = tc::smem_u32(bar);
+                tc::mbar_arrive_expect_tx(mb, bytes);
+                tc::bulk_g2s(dst, from, bytes, mb);
+            };
+            auto fetch_tp = [&](long long i) {
+                fetch(&tpbar[i & 1], s_tp + (uint32_t)((i & 1) * TP_BYTES), src(i), TP_BYTES);
+            };
+            auto fetch_wq = [&](long long i) { fetch(wqbar, s_wqh, src(i) + OFF_CH_WQ, WQ_BYTES); };
+            auto fetch_bv = [&](long long i) {
+                fetch(bvbar, s_bv, src(i) + OFF_CH_BV + slice * BV_SLICE, BV_SLICE);
+            };
+            auto fetch_kt = [&](long long i) { fetch(ktbar, s_kth, src(i) + OFF_CH_KT, KT_BYTES); };
+            // G2 of chunk i: D3 = [T ; PT] . bV  (U, PU)
+            auto issue_g2 = [&](long long i) -> bool {
+                if (!tc::mbar_wait(tc::smem_u32(bvbar), (uint32_t)(i & 1)) ||
+                    !tc::mbar_wait(tc::smem_u32(&tpbar[i & 1]), (uint32_t)((i >> 1) & 1)))
+                    return false;
+                const uint32_t tb = s_tp + (uint32_t)((i & 1) * TP_BYTES);
+                mma2cat<false, 64, DVS>(T_D3, tb, tb + TP_HALF, 0, s_bv, false, 0u);
+                return true;
+            };
             fetch_tp(0);
             if (n_chunks > 1) fetch_tp(1);
             fetch_wq(0);
-        }
-        load_chunk(s);
-        load_gates(s);
-        if (s + TC_C < e) prefetch_chunk(s + TC_C);
-    }
-
-    long long ci = 0;
-    for (long long c0 = s; c0 < e; c0 += TC_C, ++ci) {
-        const int Lc = (int)((e - c0) < TC_C ? (e - c0) : TC_C);
-        const bool has_next = c0 + TC_C < e;
-        // ---------------- S0: L2 norm of the staged k rows; gate scan
-        if (tid < TC_C) {  // (nothing reads sG / sB after the previous chunk's S0)
-            sG[tid] = gn;
-            sB[tid] = bn;
-        }
-        if (l2) l2norm_row4(kv, d.l2_eps, 1.f);
-        __syncthreads();   // raw gates of this chunk are in sG / sB
-        if (warp == 0) scan64(sG, lane);
-        __syncthreads();
-        const float br = sB[rr], Gl = sG[TC_C - 1];
-        const float kdec = expf(Gl - sG[rr]);
-        // ---------------- S2: K~ (MN-major) and [bV_hi | bV_lo]
-#pragma unroll
-        for (int k8 = 0; k8 < 32; k8 += 8) {
-            float t8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) t8[i] = kdec * kv[k8 + i];
-            put8(kth, ktl, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
-        }
-#pragma unroll
-        for (int k8 = 0; k8 < VQ; k8 += 8) {
-            float t8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) t8[i] = br * vv[k8 + i];
-            put8cat<DVS>(bvt, cq * VQ + k8, rr, t8);
-        }
-        sync_for_mma();
-        // ---------------- G2 + G3 (one accumulator, issued back to back):
-        //   D3  = [T ; PT] . bV           -> U, PU
-        //   D3 += [-W ; Q'] . M           -> U' (lanes 0-63), O (64-127)
-        bool issued = true;
-        if (tid == 0) {
-            const uint32_t tb = s_tp + (uint32_t)((ci & 1) * TP_BYTES);
-            const bool tp_ok = tc::mbar_wait(tc::smem_u32(&tpbar[ci & 1]), (uint32_t)((ci >> 1) & 1));
-            if (tp_ok) mma2cat<false, 64, DVS>(T_D3, tb, tb + TP_HALF, 0, s_bv, false, 0u);
-            issued = tp_ok && tc::mbar_wait(tc::smem_u32(wqbar), (uint32_t)(ci & 1));
-            if (issued) mma2cat<false, 128, DVS>(T_D3, s_wqh, s_wql, 0, s_mt, true, 0u);
-            if (tp_ok) tc::mma_commit(tc::smem_u32(mbar));   // (what was issued can be waited for)
-        }
-        if (has_next) {               // next chunk's rows and gates, in flight during the MMAs
-            load_chunk(c0 + TC_C);
-            load_gates(c0 + TC_C);
-            if (c0 + 2 * TC_C < e) prefetch_chunk(c0 + 2 * TC_C);
-        }
-        if (!ms.wait(tid, issued)) { timed_out = true; break; }
-        if (has_next) {                     // into the buffers G2 / G3 just consumed
-            if (tid == FETCHER) fetch_wq(ci + 1);
-            wq_last = ci + 1;
-            if (ci + 2 < n_chunks) {
-                if (tid == FETCHER) fetch_tp(ci + 2);
-                tp_last = ci + 2;
+            fetch_bv(0);
+            fetch_kt(0);
+            long long ci = 0;
+            bool ok = issue_g2(0);
+            for (; ok && ci < n_chunks; ++ci) {
+                const uint32_t par = (uint32_t)(ci & 1);
+                // G3: D3 += [-W ; Q'] . M  (U' on lanes 0-63, O on 64-127)
+                ok = tc::mbar_wait(tc::smem_u32(mtbar), par) && tc::mbar_wait(tc::smem_u32(wqbar), par);
+                if (!ok) break;
+                tc::fence_after_sync();
+                mma2cat<false, 128, DVS>(T_D3, s_wqh, s_wql, 0, s_mt, true, 0u);
+                tc::mma_commit(tc::smem_u32(g3bar));
+                // refill what G2 / G3 have read
+                ok = tc::mbar_wait(tc::smem_u32(g3bar), par);
+                if (!ok) break;
+                if (ci + 1 < n_chunks) { fetch_wq(ci + 1); fetch_bv(ci + 1); }
+                if (ci + 2 < n_chunks) fetch_tp(ci + 2);
+                // G5: D5 = K~^T . U'
+                ok = tc::mbar_wait(tc::smem_u32(utbar), par) && tc::mbar_wait(tc::smem_u32(ktbar), par);
+                if (!ok) break;
+                tc::fence_after_sync();
+                mma2cat<true, 64, DVS>(T_D5, s_kth, s_ktl, 128, s_ut, false, tc::kTransA);
+                tc::mma_commit(tc::smem_u32(g5bar));
+                if (ci + 1 < n_chunks) {
+                    // G2 of the next chunk, behind G5 in the tensor pipe (D3 has been read by E3),
+                    // then the next K~ once G5 has read this one
+                    ok = issue_g2(ci + 1) && tc::mbar_wait(tc::smem_u32(g5bar), par);
+                    if (ok) fetch_kt(ci + 1);
+                }
+            }
+            if (!ok) {
+                // the epilogue warps stop on their own bounded waits; let outstanding MMAs and
+                // copies retire (bounded) before the kernel's end frees TMEM and shared memory
+                set_error(a.err, GDN_DEVERR_TIMEOUT);
+                tc::mma_commit(tc::smem_u32(g3bar));
+                tc::mbar_wait(tc::smem_u32(g3bar), (uint32_t)(ci & 1));
+                for (int k = 0; k < 2; ++k) {    // each copy barrier: its current and next phase
+                    tc::mbar_wait(tc::smem_u32(wqbar), (uint32_t)((ci + k) & 1));
+                    tc::mbar_wait(tc::smem_u32(bvbar), (uint32_t)((ci + k) & 1));
+                    tc::mbar_wait(tc::smem_u32(ktbar), (uint32_t)((ci + k) & 1));
+                }
+            } else {
+                tc::mbar_wait(tc::smem_u32(g5bar), (uint32_t)((n_chunks - 1) & 1));   // last G5 retired
             }
         }
-        // ---------------- E3: U' -> concatenated B operand; O rows -> o
+    } else {
+        // ========================= epilogue warps 0-7 ==========================
+        const int qd = warp & 3, hf = warp >> 2;   // lane mapping: TMEM lane tl, column half hf
+        const int tl = qd * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+        const float *glp = a.gl + jc * d.hv + h;   // G_last of chunk i at glp[i * hv]
+
+        // ---- the initial state (thread: dk row tl, columns hf*HALF ..)
+        float Mr[HALF];
         {
-            float v[HALF];
-            tmem_ld_cat16<DVS>(T_D3 + lane_off + hf * HALF, v);
+            if (a.state_in && slot >= 0) {
+                const float *sin = a.state_in + ((long long)slot * d.hv + h) * TC_DK * TC_DK +
+                                   (long long)tl * TC_DK + slice * DVS + hf * HALF;
+                load_row<HALF>(sin, Mr);
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < HALF; ++jj) Mr[jj] = 0.f;
+            }
+#pragma unroll
+            for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(mtt, hf * HALF + j8, tl, &Mr[j8]);
+        }
+        float Gl = 0.f;
+        if (s < e) {
+            arrive_staged(mtbar);
+            Gl = glp[0];
+        }
+
+        long long ci = 0;
+        for (long long c0 = s; c0 < e; c0 += TC_C, ++ci) {
+            const int Lc = (int)((e - c0) < TC_C ? (e - c0) : TC_C);
+            const bool has_next = c0 + TC_C < e;
+            const uint32_t par = (uint32_t)(ci & 1);
+            // ---------------- E3: U' -> concatenated B operand -> utbar
+            if (!staging_wait(g3bar, par, flag3, tid)) break;
+            float ov[HALF];
+            tmem_ld_cat16<DVS>(T_D3 + lane_off + hf * HALF, ov);
             if (qd < 2) {
 #pragma unroll
-                for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(utt, hf * HALF + j8, tl, &v[j8]);
-            } else {
-                const int r = tl - 64;
-                if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, v);
+                for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(utt, hf * HALF + j8, tl, &ov[j8]);
             }
-        }
-        sync_for_mma();
-        // ---------------- G5: dM = K~^T U'
-        if (tid == 0) {
-            mma2cat<true, 64, DVS>(T_D5, s_kth, s_ktl, 128, s_ut, false, tc::kTransA);
-            tc::mma_commit(tc::smem_u32(mbar));
-        }
-        if (!ms.wait(tid)) { timed_out = true; break; }
-        // ---------------- E5: M <- gamma_last M + dM
-        {
+            arrive_staged(utbar);
+            // ---------------- E5: M <- gamma_last M + dM -> mtbar
+            if (!staging_wait(g5bar, par, flag5, tid)) break;
             float v[HALF];
             tmem_ld_cat16<DVS>(T_D5 + lane_off + hf * HALF, v);
             const float gl = expf(Gl);
 #pragma unroll
             for (int jj = 0; jj < HALF; ++jj) Mr[jj] = gl * Mr[jj] + v[jj];
+            if (has_next) {
 #pragma unroll
-            for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(mtt, hf * HALF + j8, tl, &Mr[j8]);
+                for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(mtt, hf * HALF + j8, tl, &Mr[j8]);
+                arrive_staged(mtbar);
+                Gl = glp[(ci + 1) * d.hv];
+            }
+            // ---------------- O rows -> o (after the publish, so that no operand fence waits on them)
+            if (qd >= 2) {
+                const int r = tl - 64;
+                if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, ov);
+            }
         }
-        // (the next chunk's operand writes are followed by sync_for_mma before G2)
-    }
-    if (timed_out) {
-        // give outstanding MMAs and copies one more bounded chance to retire before TMEM is freed
-        if (tid == 0) {
-            set_error(a.err, GDN_DEVERR_TIMEOUT);
-            tc::mbar_wait(tc::smem_u32(mbar), ms.phase);
-            // the last copies issued into each buffer may still be in flight
-            tc::mbar_wait(tc::smem_u32(wqbar), (uint32_t)(wq_last & 1));
-            tc::mbar_wait(tc::smem_u32(&tpbar[tp_last & 1]), (uint32_t)((tp_last >> 1) & 1));
-            if (tp_last >= 1)
-                tc::mbar_wait(tc::smem_u32(&tpbar[(tp_last - 1) & 1]), (uint32_t)(((tp_last - 1) >> 1) & 1));
+        if (ci < n_chunks) {
+            if (tid == 0) set_error(a.err, GDN_DEVERR_TIMEOUT);
+        } else if (a.state_out && slot >= 0) {
+            float *so = a.state_out + ((long long)slot * d.hv + h) * TC_DK * TC_DK +
+                        (long long)tl * TC_DK + slice * DVS + hf * HALF;
+            store_row<HALF>(so, Mr);
         }
-        __syncthreads();
-    }
-    if (a.state_out && slot >= 0) {
-        float *so = a.state_out + ((long long)slot * d.hv + h) * TC_DK * TC_DK +
-                    (long long)tl * TC_DK + slice * DVS + hf * HALF;
-        store_row<HALF>(so, Mr);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -965,7 +979,7 @@ static cudaError_t launch_tc_t(const ChunkArgs &a, cudaStream_t s) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     dim3 grid(TC_DK / DVS, a.d.hv, a.n_seqs);
-    kern<<<grid, TC_NT, smem, s>>>(a);
+    kern<<<grid, CHAIN_NT, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -980,7 +994,7 @@ size_t chunk_tc_ws_bytes(const Dims &d, long long T, long long n_seqs) {
     const long long mc = chunk_tc_max_chunks(T, n_seqs);
     if (mc == 0) return 0;
     const size_t base = (((size_t)n_seqs + 1) * 4 + 255) & ~(size_t)255;
-    return base + (size_t)mc * d.hv * CH_BYTES;
+    return base + (size_t)mc * d.hv * CH_BYTES + (((size_t)mc * d.hv * 4 + 255) & ~(size_t)255);
 }
 
 void chunk_tc_carve(ChunkArgs &a, void *ws) {
@@ -992,6 +1006,7 @@ void chunk_tc_carve(ChunkArgs &a, void *ws) {
     }
     a.chunk_base = (int *)ws;
     a.tp = (unsigned char *)ws + ((((size_t)a.n_seqs + 1) * 4 + 255) & ~(size_t)255);
+    a.gl = (float *)(a.tp + (size_t)a.max_chunks * a.d.hv * CH_BYTES);
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, cudaStream_t s) {

@@ -90,6 +90,7 @@ struct ChunkArgs {
     // (caller workspace, carved by chunk_tc_carve)
     int *chunk_base;
     unsigned char *tp;
+    float *gl;            // G_last of every (chunk, v-head)
     long long max_chunks;
 };
 
