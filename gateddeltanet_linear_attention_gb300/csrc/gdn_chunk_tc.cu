@@ -663,11 +663,11 @@ struct ChainSmem {
     // bulk-copied from the workspace: WQ (hi then lo), [T ; PT] x 2 buffers, [bV_hi | bV_lo], K~ (hi then lo)
     static constexpr int OFF_WQ = 0;
     static constexpr int OFF_TP = OFF_WQ + 2 * WQ;
-    static constexpr int OFF_BV = OFF_TP + 2 * TP_BYTES;
-    static constexpr int OFF_KT = OFF_BV + BV_SLICE;
+    static constexpr int OFF_BV = OFF_TP + 2 * TP_BYTES;   // x 2 buffers
+    static constexpr int OFF_KT = OFF_BV + 2 * BV_SLICE;
     static constexpr int OFF_MT = OFF_KT + KT_BYTES;
     static constexpr int OFF_UT = OFF_MT + MT;
-    static constexpr int OFF_BAR = OFF_UT + UT;            // 9 mbarriers, tmem slot, flags
+    static constexpr int OFF_BAR = OFF_UT + UT;            // 10 mbarriers, tmem slot, flags
     static constexpr int BYTES = OFF_BAR + 96;
     static_assert(DVS == CH_DVS, "the workspace holds bV in slices of CH_DVS columns");
     static_assert(OFF_TP % 16 == 0 && OFF_BV % 16 == 0 && OFF_KT % 16 == 0, "bulk-copy alignment");
@@ -698,9 +698,7 @@ __device__ __forceinline__ void mma2cat(uint32_t d_tmem, uint32_t a_hi, uint32_t
 template <int DVS>
 __device__ __forceinline__ void tmem_ld_cat16(uint32_t taddr, float (&v)[16]) {
     float x[16], y[16];
-    tmem_ld<16>(taddr, v);
-    tmem_ld<16>(taddr + DVS, x);
-    tmem_ld<16>(taddr + 2 * DVS, y);
+    tc::tmem_ld16x3(taddr, taddr + DVS, taddr + 2 * DVS, v, x, y);
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] += x[i] + y[i];
 }
@@ -753,11 +751,11 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     unsigned char *mtt = sm + L::OFF_MT;
     unsigned char *utt = sm + L::OFF_UT;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
-    uint64_t *wqbar = bars + 0, *tpbar = bars + 1 /* [2] */, *bvbar = bars + 3, *ktbar = bars + 4,
-             *mtbar = bars + 5, *utbar = bars + 6, *g3bar = bars + 7, *g5bar = bars + 8;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
-    volatile uint32_t *flag3 = reinterpret_cast<uint32_t *>(bars + 9) + 1;
-    volatile uint32_t *flag5 = reinterpret_cast<uint32_t *>(bars + 10);
+    uint64_t *wqbar = bars + 0, *tpbar = bars + 1 /* [2] */, *bvbar = bars + 3 /* [2] */,
+             *ktbar = bars + 5, *mtbar = bars + 6, *utbar = bars + 7, *g3bar = bars + 8, *g5bar = bars + 9;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
+    volatile uint32_t *flag3 = reinterpret_cast<uint32_t *>(bars + 10) + 1;
+    volatile uint32_t *flag5 = reinterpret_cast<uint32_t *>(bars + 11);
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -795,7 +793,8 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
         tc::mbar_init(tc::smem_u32(wqbar), 1);
         tc::mbar_init(tc::smem_u32(&tpbar[0]), 1);
         tc::mbar_init(tc::smem_u32(&tpbar[1]), 1);
-        tc::mbar_init(tc::smem_u32(bvbar), 1);
+        tc::mbar_init(tc::smem_u32(&bvbar[0]), 1);
+        tc::mbar_init(tc::smem_u32(&bvbar[1]), 1);
         tc::mbar_init(tc::smem_u32(ktbar), 1);
         tc::mbar_init(tc::smem_u32(mtbar), 256);
         tc::mbar_init(tc::smem_u32(utbar), 256);
@@ -826,23 +825,29 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
                 fetch(&tpbar[i & 1], s_tp + (uint32_t)((i & 1) * TP_BYTES), src(i), TP_BYTES);
             };
             auto fetch_wq = [&](long long i) { fetch(wqbar, s_wqh, src(i) + OFF_CH_WQ, WQ_BYTES); };
-            auto fetch_bv = [&](long long i) {
-                fetch(bvbar, s_bv, src(i) + OFF_CH_BV + slice * BV_SLICE, BV_SLICE);
+            auto fetch_bv = [&](long long i) {   // -> BV buffer i&1
+                fetch(&bvbar[i & 1], s_bv + (uint32_t)((i & 1) * BV_SLICE),
+                      src(i) + OFF_CH_BV + slice * BV_SLICE, BV_SLICE);
             };
             auto fetch_kt = [&](long long i) { fetch(ktbar, s_kth, src(i) + OFF_CH_KT, KT_BYTES); };
             // G2 of chunk i: D3 = [T ; PT] . bV  (U, PU)
             auto issue_g2 = [&](long long i) -> bool {
-                if (!tc::mbar_wait(tc::smem_u32(bvbar), (uint32_t)(i & 1)) ||
-                    !tc::mbar_wait(tc::smem_u32(&tpbar[i & 1]), (uint32_t)((i >> 1) & 1)))
+                const uint32_t par2 = (uint32_t)((i >> 1) & 1);
+                if (!tc::mbar_wait(tc::smem_u32(&bvbar[i & 1]), par2) ||
+                    !tc::mbar_wait(tc::smem_u32(&tpbar[i & 1]), par2))
                     return false;
                 const uint32_t tb = s_tp + (uint32_t)((i & 1) * TP_BYTES);
-                mma2cat<false, 64, DVS>(T_D3, tb, tb + TP_HALF, 0, s_bv, false, 0u);
+                mma2cat<false, 64, DVS>(T_D3, tb, tb + TP_HALF, 0, s_bv + (uint32_t)((i & 1) * BV_SLICE),
+                                        false, 0u);
                 return true;
             };
             fetch_tp(0);
-            if (n_chunks > 1) fetch_tp(1);
-            fetch_wq(0);
             fetch_bv(0);
+            if (n_chunks > 1) {
+                fetch_tp(1);
+                fetch_bv(1);
+            }
+            fetch_wq(0);
             fetch_kt(0);
             long long ci = 0;
             bool ok = issue_g2(0);
@@ -857,8 +862,11 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
                 // refill what G2 / G3 have read
                 ok = tc::mbar_wait(tc::smem_u32(g3bar), par);
                 if (!ok) break;
-                if (ci + 1 < n_chunks) { fetch_wq(ci + 1); fetch_bv(ci + 1); }
-                if (ci + 2 < n_chunks) fetch_tp(ci + 2);
+                if (ci + 1 < n_chunks) fetch_wq(ci + 1);
+                if (ci + 2 < n_chunks) {   // into the buffers G2 of this chunk has read
+                    fetch_tp(ci + 2);
+                    fetch_bv(ci + 2);
+                }
                 // G5: D5 = K~^T . U'
                 ok = tc::mbar_wait(tc::smem_u32(utbar), par) && tc::mbar_wait(tc::smem_u32(ktbar), par);
                 if (!ok) break;
@@ -880,8 +888,11 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
                 tc::mbar_wait(tc::smem_u32(g3bar), (uint32_t)(ci & 1));
                 for (int k = 0; k < 2; ++k) {    // each copy barrier: its current and next phase
                     tc::mbar_wait(tc::smem_u32(wqbar), (uint32_t)((ci + k) & 1));
-                    tc::mbar_wait(tc::smem_u32(bvbar), (uint32_t)((ci + k) & 1));
                     tc::mbar_wait(tc::smem_u32(ktbar), (uint32_t)((ci + k) & 1));
+                    for (int b = 0; b < 2; ++b) {
+                        tc::mbar_wait(tc::smem_u32(&bvbar[b]), (uint32_t)(((ci + k) >> 1) & 1));
+                        tc::mbar_wait(tc::smem_u32(&tpbar[b]), (uint32_t)(((ci + k) >> 1) & 1));
+                    }
                 }
             } else {
                 tc::mbar_wait(tc::smem_u32(g5bar), (uint32_t)((n_chunks - 1) & 1));   // last G5 retired
