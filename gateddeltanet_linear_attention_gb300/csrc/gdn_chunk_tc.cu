@@ -165,6 +165,58 @@ __device__ __forceinline__ void put8cat(unsigned char *tile, int j8, int k, cons
     *reinterpret_cast<uint4 *>(tile + tc::mnmaj_off(DVS + j8, k, 2 * DVS)) = *reinterpret_cast<const uint4 *>(l2);
 }
 
+// Store 4 values (8 bytes of bf16 in each of a hi and a lo tile) at byte offset
+// `off`, 8-byte aligned.
+__device__ __forceinline__ void put4(unsigned char *hi, unsigned char *lo, uint32_t off, const float *v) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]), h1 = __floats2bfloat162_rn(v[2], v[3]);
+    const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+    const __nv_bfloat162 l0 = __floats2bfloat162_rn(v[0] - f0.x, v[1] - f0.y);
+    const __nv_bfloat162 l1 = __floats2bfloat162_rn(v[2] - f1.x, v[3] - f1.y);
+    uint2 hv, lv;
+    hv.x = *reinterpret_cast<const uint32_t *>(&h0); hv.y = *reinterpret_cast<const uint32_t *>(&h1);
+    lv.x = *reinterpret_cast<const uint32_t *>(&l0); lv.y = *reinterpret_cast<const uint32_t *>(&l1);
+    *reinterpret_cast<uint2 *>(hi + off) = hv;
+    *reinterpret_cast<uint2 *>(lo + off) = lv;
+}
+
+// Interleaved row mapping of the parallel kernel: warp w holds token rows
+// 8w .. 8w+7, lane l row 8w + l/4, and of each 16-column group of the row the
+// 4 columns 4*(l%4) .. +3.  A warp's 16-byte load then covers 8 rows x 64
+// contiguous bytes, and its 8-byte hi/lo stores of one group fill 256
+// contiguous bytes of a core-matrix tile.  Column of group i, part j: 16 i + 4 q + j.
+__device__ __forceinline__ int il_row(int tid) { return 8 * (tid >> 5) + ((tid & 31) >> 2); }
+__device__ __forceinline__ int il_q(int tid) { return tid & 3; }
+template <typename T>
+__device__ __forceinline__ void load_row_il(const T *row, int q, float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float t[4];
+        if constexpr (sizeof(T) == 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(row + 16 * i + 4 * q);
+            t[0] = f.x; t[1] = f.y; t[2] = f.z; t[3] = f.w;
+        } else {
+            const uint2 u = *reinterpret_cast<const uint2 *>(row + 16 * i + 4 * q);
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+            t[0] = a.x; t[1] = a.y; t[2] = b.x; t[3] = b.y;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[4 * i + j] = t[j];
+    }
+}
+// L2 normalisation of a row held by lanes 4m .. 4m+3 (32 values each).
+__device__ __forceinline__ float l2norm_row_il(float (&v)[32], float eps, float scale) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float f = rsqrtf(ss + eps) * scale;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= f;
+    return f;
+}
+
 // Shared pieces of the per-CTA setup: one thread polls the MMA barrier
 // (bounded) and the block agrees on the outcome, so a timeout leaves any loop
 // uniformly.
@@ -188,27 +240,6 @@ __device__ __forceinline__ void sync_for_mma() {
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-}
-
-// Row mapping of the staging phases: warp w holds rows 8w .. 8w+7, lane l row
-// 8w + l%8 and dk columns 32*(l/8) .. +31.  Each group of 8 lanes (one phase of
-// a 16-byte shared-memory store) then writes 8 consecutive rows of the same
-// columns: one 128-byte core matrix, free of bank conflicts.
-__device__ __forceinline__ int stage_row(int tid) { return 8 * (tid >> 5) + (tid & 7); }
-__device__ __forceinline__ int stage_quarter(int tid) { return (tid & 31) >> 3; }
-
-// L2 normalisation of a row held by lanes l, l+8, l+16, l+24 (32 values each).
-// Returns the factor applied.
-__device__ __forceinline__ float l2norm_row4(float (&v)[32], float eps, float scale) {
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
-    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-    const float f = rsqrtf(ss + eps) * scale;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= f;
-    return f;
 }
 
 // In-place inclusive scan of the 64 gate values in sG by warp 0 (2 per lane).
@@ -357,21 +388,23 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     tc::fence_after_sync();
     const uint32_t tbase = *tmem_slot;
     MmaSync ms{mbar, wait_flag, 0u};
-    const int rr = stage_row(tid), cq = stage_quarter(tid);
     const int qd = warp & 3, hf = warp >> 2, tl = qd * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
 
-    // ---- rows of K and Q (L2-normalised) and gates; operands [K;Q] (K-major) and bgK (MN-major)
+    // ---- rows of K and Q (L2-normalised) and gates; operands [K;Q] (K-major) and bgK
+    // (MN-major); K~ and beta V for the state chain straight to the workspace
     {
-        float kv[32], qv[32];
-        const long long t = t0 + rr;
+        const int ir = il_row(tid), iq = il_q(tid);
+        float kv[32], qv[32], vv[32];
+        const long long t = t0 + ir;
         if (t < e) {
-            load_row<32>((const TIn *)a.k + t * a.ld_qk + (long long)kh * TC_DK + cq * 32, kv);
-            load_row<32>((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK + cq * 32, qv);
+            load_row_il((const TIn *)a.k + t * a.ld_qk + (long long)kh * TC_DK, iq, kv);
+            load_row_il((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK, iq, qv);
+            load_row_il((const TIn *)a.v + t * a.ld_v + (long long)h * TC_DK, iq, vv);
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
+            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = vv[i] = 0.f;
         }
         if (tid < TC_C) {
             const long long tt = t0 + tid;
@@ -380,43 +413,33 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
         }
         __syncthreads();
         if (warp == 0) scan64(sG, lane);
-        const float fq = l2 ? l2norm_row4(qv, d.l2_eps, d.q_scale) : 1.f;
-        if (l2) l2norm_row4(kv, d.l2_eps, 1.f);
-        if (cq == 0) sFq[rr] = fq;
+        const float fq = l2 ? l2norm_row_il(qv, d.l2_eps, d.q_scale) : 1.f;
+        if (l2) l2norm_row_il(kv, d.l2_eps, 1.f);
+        if (iq == 0) sFq[ir] = fq;
         __syncthreads();
-        const float Gr = sG[rr], br = sB[rr], Gl = sG[TC_C - 1];
+        const float Gr = sG[ir], br = sB[ir], Gl = sG[TC_C - 1];
         const float bg = br * expf(Gr), kdec = expf(Gl - Gr);
         unsigned char *gkt = gtp + OFF_CH_KT;
 #pragma unroll
-        for (int k8 = 0; k8 < 32; k8 += 8) {
-            put8(kqh, kql, tc::kmaj_off(rr, cq * 32 + k8, 128), &kv[k8]);
-            put8(kqh, kql, tc::kmaj_off(64 + rr, cq * 32 + k8, 128), &qv[k8]);
-            float t8[8];
+        for (int i = 0; i < 8; ++i) {
+            const int c = 16 * i + 4 * iq;          // first of this group's 4 columns (dk)
+            put4(kqh, kql, tc::kmaj_off(ir, c, 128), &kv[4 * i]);
+            put4(kqh, kql, tc::kmaj_off(64 + ir, c, 128), &qv[4 * i]);
+            float t4[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) t8[i] = bg * kv[k8 + i];
-            put8(b3h, b3l, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
-            // the chain's G5 operand: K~ = exp(G_last - G_r) k_r (MN-major), to the workspace
+            for (int j = 0; j < 4; ++j) t4[j] = bg * kv[4 * i + j];
+            put4(b3h, b3l, tc::mnmaj_off(c, ir, 128), t4);
+            // the chain's G5 operand: K~ = exp(G_last - G_r) k_r (MN-major)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) t8[i] = kdec * kv[k8 + i];
-            put8(gkt, gkt + KT_HALF, tc::mnmaj_off(cq * 32 + k8, rr, 128), t8);
-        }
-        // the chain's G2 operand: beta v of the state slice cq (its 32 columns), as a
-        // concatenated [hi | lo] tile (MN-major, MN = 64), to the workspace
-        {
-            float vv[32];
-            if (t < e) load_row<32>((const TIn *)a.v + t * a.ld_v + (long long)h * TC_DK + cq * 32, vv);
-            else {
+            for (int j = 0; j < 4; ++j) t4[j] = kdec * kv[4 * i + j];
+            put4(gkt, gkt + KT_HALF, tc::mnmaj_off(c, ir, 128), t4);
+            // the chain's G2 operand: beta v, as one concatenated [hi | lo] tile (MN-major,
+            // MN = 2 CH_DVS) per state slice of CH_DVS columns
 #pragma unroll
-                for (int i = 0; i < 32; ++i) vv[i] = 0.f;
-            }
-            unsigned char *gbv = gtp + OFF_CH_BV + cq * BV_SLICE;
-#pragma unroll
-            for (int k8 = 0; k8 < 32; k8 += 8) {
-                float t8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) t8[i] = br * vv[k8 + i];
-                put8cat<CH_DVS>(gbv, k8, rr, t8);
-            }
+            for (int j = 0; j < 4; ++j) t4[j] = br * vv[4 * i + j];
+            unsigned char *gbv = gtp + OFF_CH_BV + (c / CH_DVS) * BV_SLICE;
+            const int m = c % CH_DVS;
+            put4(gbv + tc::mnmaj_off(m, ir, 2 * CH_DVS), gbv + tc::mnmaj_off(CH_DVS + m, ir, 2 * CH_DVS), 0u, t4);
         }
         if (tid == 0) a.gl[j * d.hv + h] = Gl;
     }
