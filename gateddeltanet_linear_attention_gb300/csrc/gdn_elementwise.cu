@@ -52,6 +52,7 @@ cudaError_t launch_gate_prep(const Dims &d, bool act_bf16, const void *u, const 
 // conv_state_update_kernel, so no CTA can overwrite a history another CTA
 // still has to read.
 constexpr int CONV_TT = 32;
+constexpr int CONV_B = 8;      // tokens whose loads are issued together
 constexpr int CONV_NT = 128;
 constexpr int CONV_V = 8;
 
@@ -139,17 +140,9 @@ __global__ void __launch_bounds__(CONV_NT)
     };
     fill_window(t0);
     const long long t_end = t0 + CONV_TT < T ? t0 + CONV_TT : T;
-    for (long long t = t0; t < t_end; ++t) {
-        if (t >= e && n + 1 < n_seqs) {
-            while (t >= e && n + 1 < n_seqs) {
-                ++n;
-                seq_bounds(cu, n, T, err, s, e);
-            }
-            slot = slot_of(state_idx, n, d.n_slots, err);
-            fill_window(t);
-        }
-        float cur[CONV_V], o[CONV_V];
-        load8f(x + t * ld_x + c0, cur);
+    // one output token of the current sequence, sliding the window
+    auto step = [&](const float (&cur)[CONV_V], long long t) {
+        float o[CONV_V];
 #pragma unroll
         for (int i = 0; i < CONV_V; ++i) {
             const float acc = wv[i][0] * win[0][i] + wv[i][1] * win[1][i] + wv[i][2] * win[2][i] +
@@ -160,6 +153,31 @@ __global__ void __launch_bounds__(CONV_NT)
             win[2][i] = cur[i];
         }
         store8f(out + t * d.ch + c0, o);
+    };
+    for (long long tb = t0; tb < t_end; tb += CONV_B) {
+        if (tb + CONV_B <= t_end && tb + CONV_B <= e) {
+            // CONV_B tokens inside the current sequence: all their loads in flight at once
+            float cur[CONV_B][CONV_V];
+#pragma unroll
+            for (int b = 0; b < CONV_B; ++b) load8f(x + (tb + b) * ld_x + c0, cur[b]);
+#pragma unroll
+            for (int b = 0; b < CONV_B; ++b) step(cur[b], tb + b);
+        } else {
+            const long long tend = tb + CONV_B < t_end ? tb + CONV_B : t_end;
+            for (long long t = tb; t < tend; ++t) {
+                if (t >= e && n + 1 < n_seqs) {   // the next sequence starts here
+                    while (t >= e && n + 1 < n_seqs) {
+                        ++n;
+                        seq_bounds(cu, n, T, err, s, e);
+                    }
+                    slot = slot_of(state_idx, n, d.n_slots, err);
+                    fill_window(t);
+                }
+                float cur[CONV_V];
+                load8f(x + t * ld_x + c0, cur);
+                step(cur, t);
+            }
+        }
     }
 }
 
