@@ -52,7 +52,7 @@ cudaError_t launch_gate_prep(const Dims &d, bool act_bf16, const void *u, const 
 // conv_state_update_kernel, so no CTA can overwrite a history another CTA
 // still has to read.
 constexpr int CONV_TT = 32;
-constexpr int CONV_B = 8;      // tokens whose loads are issued together
+constexpr int CONV_B = 4;      // tokens whose loads are issued together
 constexpr int CONV_NT = 128;
 constexpr int CONV_V = 8;
 
@@ -82,7 +82,7 @@ __device__ __forceinline__ void store8f(__nv_bfloat16 *p, const float *v) {
 }
 
 template <typename TA, typename TO>
-__global__ void __launch_bounds__(CONV_NT)
+__global__ void __launch_bounds__(CONV_NT, 4)
     conv_prefill_kernel(Dims d, const TA *x, long long ld_x, const int32_t *cu, int n_seqs,
                         long long T, const TA *w, const TA *conv_state,
                         const int32_t *state_idx, TO *out, unsigned *err) {
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(CONV_NT)
         for (int i = 0; i < CONV_V; ++i) {
             const float acc = wv[i][0] * win[0][i] + wv[i][1] * win[1][i] + wv[i][2] * win[2][i] +
                               wv[i][3] * cur[i];
-            o[i] = silu_f(acc);
+            o[i] = silu_fast(acc);
             win[0][i] = win[1][i];
             win[1][i] = win[2][i];
             win[2][i] = cur[i];
@@ -348,7 +348,7 @@ __global__ void gated_rmsnorm_kernel(Dims d, const TO_IN *o, const TZ *z, long l
         const float rs = rsqrtf(ss / (float)DV + d.norm_eps);
         float yv[PER];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) yv[i] = ov[i] * rs * wv[i] * silu_f(zv[i]);
+        for (int i = 0; i < PER; ++i) yv[i] = ov[i] * rs * wv[i] * silu_fast(zv[i]);
         storev<PER>(y + r * DV + lane * PER, yv);
     }
 }
