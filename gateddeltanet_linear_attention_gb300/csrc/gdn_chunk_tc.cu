@@ -453,7 +453,9 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     bool ok = ms.wait(tid);
     if (ok) {
         // ---- E1: A (strictly lower, fp32) and P (lower incl. the diagonal, bf16 hi/lo
-        // operand), over the Gram region
+        // operand), over the Gram region.  The decay factors exp(G_r - G_c) <= 1 use the
+        // approximate-exp intrinsic (relative error about 1e-6, far below the 2^-16 of the
+        // split operands they feed).
         {
             float v32[32];
             tc::tmem_ld32(tbase + lane_off + hf * 32, v32);
@@ -464,13 +466,13 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int c = hf * 32 + i;
-                    if (c < r) sA[r * 65 + c] = br * expf(Gr - sG[c]) * v32[i];
+                    if (c < r) sA[r * 65 + c] = br * __expf(Gr - sG[c]) * v32[i];
                 }
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int c = hf * 32 + i;
-                    v32[i] = (c <= r) ? expf(Gr - sG[c]) * v32[i] : 0.f;
+                    v32[i] = (c <= r) ? __expf(Gr - sG[c]) * v32[i] : 0.f;
                 }
 #pragma unroll
                 for (int k8 = 0; k8 < 32; k8 += 8) put8(ph, pl, tc::kmaj_off(r, hf * 32 + k8, 64), &v32[k8]);
