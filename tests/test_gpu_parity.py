@@ -68,6 +68,36 @@ def test_bf16_prefill_ragged(lens):
     _check_prefill(wl, make_inputs(wl), TOL_BF16)
 
 
+def test_bf16_tensor_core_many_short_sequences():
+    # 300 sequences (more than the 256-way chunk search of the parallel kernel covers in one
+    # round), lengths 0 .. 70 including empty and one-token ones
+    rng = np.random.default_rng(5)
+    lens = tuple(int(x) for x in rng.integers(0, 71, size=300))
+    lens = (0, 1) + lens[2:]
+    wl = Workload("many", HK=1, HV=2, dk=128, dv=128, chunk=64, act="bf16", seed=16, seqlens=lens,
+                  init_state=True, init_conv=True)
+    _check_prefill(wl, make_inputs(wl), TOL_BF16)
+
+
+def test_bf16_tensor_core_padding_lane():
+    lens = (5, 0, 70, 3, 130)
+    wl = Workload("t", HK=2, HV=4, dk=128, dv=128, chunk=64, act="bf16", seed=17, seqlens=lens,
+                  init_state=True, init_conv=True)
+    inp = make_inputs(wl)
+    smap = torch.tensor([4, 2, -1, 0, 1], dtype=torch.int32)   # lane 2 is padding; slot 3 unused
+    m = GpuMixer(wl, inp, state_idx=smap, n_slots=5)
+    y = m.prefill()
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_error() == 0
+    ref = oracle_mixer(wl, inp, slot_idx=smap.numpy())
+    cu = inp["cu_seqlens"]
+    ey, es = rel_max(y, ref["y"]), rel_max(m.state, ref["state"])
+    report("tc padding lane", y=ey, state=es)
+    assert ey <= TOL_BF16 and es <= TOL_BF16
+    assert torch.count_nonzero(y[cu[2]:cu[3]]) == 0
+    torch.testing.assert_close(m.state[3].cpu(), inp["state"][3], rtol=0, atol=0)  # untouched
+
+
 def test_bf16_y_is_rounded_fp32_y():
     wl = Workload("t", HK=2, HV=4, dk=128, dv=128, chunk=64, act="bf16", seed=13, seqlens=(150,),
                   init_state=True, init_conv=True)
