@@ -379,37 +379,63 @@ def bench_decode(args, dev, gdn, pk, pk_src):
 
 
 def bench_e2e(args, dev, gdn, cfg, wl, inp, d, N, T):
+    """End to end through gdn_mixer_prefill: every step copies its inputs from pinned host
+    memory and reads y back, inside the timed region.  Like a serving loop, the copies of step
+    i+1 (and the read-back of step i-1) run on their own streams while step i computes, with
+    two device buffer sets."""
     hx = inp["x"].pin_memory(); hz = inp["z"].pin_memory()
     hu = inp["u"].pin_memory(); hb = inp["b_logit"].pin_memory()
-    hy = torch.empty((T, wl.HV * wl.dv), dtype=torch.bfloat16).pin_memory()
-    dx, dz, du, db = (torch.empty_like(t, device=dev) for t in (hx, hz, hu, hb))
-    y = torch.empty((T, wl.HV * wl.dv), dtype=torch.bfloat16, device=dev)
+    hy = [torch.empty((T, wl.HV * wl.dv), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dins = [tuple(torch.empty_like(t, device=dev) for t in (hx, hz, hu, hb)) for _ in range(2)]
+    ys = [torch.empty((T, wl.HV * wl.dv), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     st = torch.empty((N, wl.HV, wl.dk, wl.dv), device=dev)
     conv = torch.zeros((N, wl.CH, 3), dtype=wl.torch_act, device=dev)
     ws = torch.empty(gdn.gdn_workspace_size(cfg, T, N), dtype=torch.uint8, device=dev)
     sin = d["state"] if wl.init_state else None
+    main = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    ev_in, ev_comp, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    used = [False, False]
 
-    def step():
-        for h, t in ((hx, dx), (hz, dz), (hu, du), (hb, db)):
-            t.copy_(h, non_blocking=True)
+    def step(i):
+        k = i & 1
+        dx, dz, du, db = dins[k]
+        with torch.cuda.stream(s_in):
+            if used[k]:
+                s_in.wait_event(ev_comp[k])      # step i-2 is done reading this input set
+            for h, t in ((hx, dx), (hz, dz), (hu, du), (hb, db)):
+                t.copy_(h, non_blocking=True)
+            ev_in[k].record(s_in)
+        main.wait_event(ev_in[k])
+        if used[k]:
+            main.wait_event(ev_out[k])           # y of step i-2 has been read back
         gdn.gdn_mixer_prefill(cfg, dx, dz, du, db, d["conv_w"], d["A_log"], d["dt_bias"],
-                              d["norm_w"], d["cu_seqlens"], y, state_in=sin, state_out=st,
-                              conv_state=conv, workspace=ws)
-        hy.copy_(y, non_blocking=True)
+                              d["norm_w"], d["cu_seqlens"], ys[k], state_in=sin, state_out=st,
+                              conv_state=conv, workspace=ws, stream=main)
+        ev_comp[k].record(main)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[k])
+            hy[k].copy_(ys[k], non_blocking=True)
+            ev_out[k].record(s_out)
+        used[k] = True
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        step()
-    e1.record()
+    e0.record(main)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    for k in range(2):
+        main.wait_event(ev_out[k])               # the last read-backs are inside the region
+    e1.record(main)
     torch.cuda.synchronize()
     el = e0.elapsed_time(e1) / 1e3
     h2d = sum(t.numel() * t.element_size() for t in (hx, hz, hu, hb))
     return {"value": T * args.steps / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": hy.numel() * hy.element_size()}
+            "d2h_bytes_per_step": hy[0].numel() * hy[0].element_size(),
+            "overlap": "copies of step i+1 and read-back of step i-1 overlap step i (2 buffer sets)"}
 
 
 def main():
