@@ -157,7 +157,11 @@ gdn_status gdn_conv1d_step(const gdn_config *cfg, const void *x, int64_t ld_x, i
  * call, FP32 state).  q, k: [T][ld_qk] in_dtype, head kh at column kh*dk;
  * v: [T][ld_v] in_dtype, head h at column h*dv; g, beta: [T][HV] fp32.
  * state_in may be NULL (zero state); state_out may be NULL or == state_in.
- * o: [T][HV*dv] o_dtype.  flags: GDN_FLAG_L2NORM_QK. */
+ * o: [T][HV*dv] o_dtype.  flags: GDN_FLAG_L2NORM_QK.
+ * workspace: DEVICE, caller-owned, 16-byte aligned.  The tensor-core path
+ * (bf16 activations, dk = dv = 128, chunk 64) keeps per-(chunk, v-head)
+ * operands there and needs gdn_workspace_size(cfg, T, n_seqs) bytes, else
+ * GDN_ERR_WORKSPACE; the fp32 path needs none (NULL, 0 accepted). */
 gdn_status gdn_chunk_prefill(const gdn_config *cfg, const void *q, const void *k, int64_t ld_qk,
                              const void *v, int64_t ld_v, gdn_dtype in_dtype, const float *g,
                              const float *beta, const int32_t *cu_seqlens, int32_t n_seqs,
