@@ -92,9 +92,15 @@ bool tc_grid_fits(const gdn::Dims &d, bool act_bf16, long long T, long long n_se
     return !uses_tc(d, act_bf16) || gdn::chunk_tc_max_chunks(T, n_seqs) * d.hv <= 0x7fffffffLL;
 }
 
+// The fp32 o between the chunked rule and the gated norm exists only on the
+// SIMT path; the tensor-core chain applies the norm itself.
+size_t prefill_o_bytes(const gdn::Dims &d, bool act_bf16, long long T) {
+    return uses_tc(d, act_bf16) ? 0 : align256((size_t)(T > 0 ? T : 0) * d.hv * d.dv * 4);
+}
+
 size_t prefill_ws_bytes(const gdn::Dims &d, bool act_bf16, long long T, long long n_seqs) {
     size_t t = (size_t)(T > 0 ? T : 0);
-    return align256(t * d.ch * 4) + 2 * align256(t * d.hv * 4) + align256(t * d.hv * d.dv * 4) +
+    return align256(t * d.ch * 4) + 2 * align256(t * d.hv * 4) + prefill_o_bytes(d, act_bf16, T) +
            align256(chunk_ws_bytes(d, act_bf16, T, n_seqs));
 }
 
@@ -105,7 +111,7 @@ PrefillWs carve_prefill(const gdn::Dims &d, bool act_bf16, long long T, long lon
     w.xa = (float *)p; p += align256(t * d.ch * 4);
     w.g = (float *)p; p += align256(t * d.hv * 4);
     w.beta = (float *)p; p += align256(t * d.hv * 4);
-    w.o = (float *)p; p += align256(t * d.hv * d.dv * 4);
+    w.o = (float *)p; p += prefill_o_bytes(d, act_bf16, T);
     w.chunk = chunk_ws_bytes(d, act_bf16, T, n_seqs) ? (void *)p : nullptr;
     return w;
 }
@@ -113,8 +119,8 @@ PrefillWs carve_prefill(const gdn::Dims &d, bool act_bf16, long long T, long lon
 // Each tensor-core CTA owns a 32-column slice of one head's state; the chunk
 // workspace `ws` must already be carved into `a` (chunk_tc_carve).
 cudaError_t launch_chunk(const gdn::ChunkArgs &a, bool act_bf16, bool in_bf16, bool o_bf16,
-                         cudaStream_t s) {
-    if (uses_tc(a.d, act_bf16)) return gdn::launch_chunk_tc(a, in_bf16, o_bf16, 32, s);
+                         cudaStream_t s, bool fuse_norm = false) {
+    if (uses_tc(a.d, act_bf16)) return gdn::launch_chunk_tc(a, in_bf16, o_bf16, 32, fuse_norm, s);
     return gdn::launch_chunk_simt(a, in_bf16, o_bf16, s);
 }
 
@@ -368,13 +374,20 @@ gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void
         a.ld_qk = d.ch; a.ld_v = d.ch; a.g = w.g; a.beta = w.beta;
         a.cu_seqlens = io->cu_seqlens; a.n_seqs = io->n_seqs; a.T = io->T;
         a.state_in = io->state_in; a.state_out = io->state_out; a.state_idx = io->state_idx;
-        a.o = w.o; a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
-        if (w.chunk) gdn::chunk_tc_carve(a, w.chunk);
-        e = launch_chunk(a, bf, false, false, s);
+        a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
+        if (uses_tc(d, bf)) {
+            // the chain applies the gated norm to its output rows and writes y
+            gdn::chunk_tc_carve(a, w.chunk);
+            a.o = io->y; a.z = io->z; a.ld_z = io->ld_z; a.norm_w = io->norm_w;
+            e = launch_chunk(a, bf, false, io->y_dtype == GDN_BF16, s, true);
+        } else {
+            a.o = w.o;
+            e = launch_chunk(a, bf, false, false, s);
+            if (e == cudaSuccess)
+                e = gdn::launch_gated_rmsnorm(d, bf, w.o, false, io->z, io->ld_z, io->norm_w, io->T,
+                                              io->y, io->y_dtype == GDN_BF16, s);
+        }
     }
-    if (e == cudaSuccess)
-        e = gdn::launch_gated_rmsnorm(d, bf, w.o, false, io->z, io->ld_z, io->norm_w, io->T, io->y,
-                                      io->y_dtype == GDN_BF16, s);
     return launch_status(e);
 }
 

@@ -301,6 +301,8 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(ChunkArgs a) {
         __syncthreads();
     }
     if (tid == 0) a.chunk_base[a.n_seqs] = carry;
+    if (a.ncnt)   // the fused norm's per-(chunk, v-head) publish counters start at zero
+        for (long long i = tid; i < a.max_chunks * a.d.hv; i += 1024) a.ncnt[i] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -693,7 +695,8 @@ struct ChainSmem {
     static constexpr int OFF_MT = OFF_KT + KT_BYTES;
     static constexpr int OFF_UT = OFF_MT + MT;
     static constexpr int OFF_BAR = OFF_UT + UT;            // 10 mbarriers, tmem slot, flags
-    static constexpr int BYTES = OFF_BAR + 96;
+    static constexpr int OFF_NP = OFF_BAR + 96;            // fused norm: half-row sums [64], flag
+    static constexpr int BYTES = OFF_NP + 64 * 4 + 16;
     static_assert(DVS == CH_DVS, "the workspace holds bV in slices of CH_DVS columns");
     static_assert(OFF_TP % 16 == 0 && OFF_BV % 16 == 0 && OFF_KT % 16 == 0, "bulk-copy alignment");
 };
@@ -767,7 +770,23 @@ __device__ __forceinline__ void arrive_staged(uint64_t *bar) {
     tc::mbar_arrive(tc::smem_u32(bar));
 }
 
-template <int DVS, typename TIn, typename TOut>
+// The fused gated RMSNorm needs each row's sum of squares over all dv columns,
+// which the four slice CTAs of a head hold a quarter each.  A slice publishes
+// its 64 per-row sums of chunk c to the workspace and counts itself in
+// ncnt[chunk][head] (release); one chunk later, when the peers have long done
+// the same, it waits (bounded, acquire) for the count to reach 4, adds the
+// four sums and writes y.  The four CTAs are launched as one cluster, so they
+// are always resident together.
+__device__ __forceinline__ void named_bar_o() {   // the 128 threads holding O rows (warps 2, 3, 6, 7)
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <int DVS, typename TIn, typename TOut, bool NORM>
 __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     using L = ChainSmem<DVS>;
     constexpr int HALF = DVS / 2;                 // state columns per thread in lane mapping
@@ -781,6 +800,8 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
     volatile uint32_t *flag3 = reinterpret_cast<uint32_t *>(bars + 10) + 1;
     volatile uint32_t *flag5 = reinterpret_cast<uint32_t *>(bars + 11);
+    float *sNp = reinterpret_cast<float *>(sm + L::OFF_NP);
+    volatile uint32_t *flagN = reinterpret_cast<uint32_t *>(sm + L::OFF_NP + 64 * 4);
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -929,6 +950,52 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
         const int tl = qd * 32 + lane;
         const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
         const float *glp = a.gl + jc * d.hv + h;   // G_last of chunk i at glp[i * hv]
+        // fused norm (threads holding O rows: TMEM lanes 64-127, row r = tl - 64)
+        const int orow = tl - 64;
+        auto publish_sums = [&](long long i, const float (&ov)[HALF]) {
+            float ss = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < HALF; ++jj) ss += ov[jj] * ov[jj];
+            if (hf == 1) sNp[orow] = ss;
+            named_bar_o();
+            if (hf == 0) {
+                a.npart[(((jc + i) * d.hv + h) * (TC_DK / DVS) + slice) * 64 + orow] = ss + sNp[orow];
+                __threadfence();
+            }
+            named_bar_o();
+            if (hf == 0 && orow == 0) atomicAdd(a.ncnt + (jc + i) * d.hv + h, 1u);
+        };
+        auto finish_norm = [&](long long i, long long ci0, int Li, const float (&ov)[HALF]) {
+            if (hf == 0 && orow == 0) {
+                const unsigned *cnt = a.ncnt + (jc + i) * d.hv + h;
+                bool ok = ld_acquire_gpu(cnt) >= (unsigned)(TC_DK / DVS);
+                if (!ok) {
+                    const uint64_t t0 = tc::globaltimer_ns();
+                    for (uint32_t it = 0; it < tc::kSpinLimit && !ok; ++it) {
+                        ok = ld_acquire_gpu(cnt) >= (unsigned)(TC_DK / DVS);
+                        if (!ok && (it & 63u) == 63u && tc::globaltimer_ns() - t0 > tc::kWaitNs) break;
+                    }
+                }
+                *flagN = ok ? 0u : 1u;
+                if (!ok) set_error(a.err, GDN_DEVERR_TIMEOUT);
+            }
+            named_bar_o();
+            if (*flagN != 0u || orow >= Li) return;
+            const float *np = a.npart + ((jc + i) * d.hv + h) * (TC_DK / DVS) * 64 + orow;
+            float tot = 0.f;
+#pragma unroll
+            for (int q = 0; q < TC_DK / DVS; ++q) tot += __ldcg(np + q * 64);
+            const float rs = rsqrtf(tot / (float)TC_DK + d.norm_eps);
+            const long long t = ci0 + orow;
+            const int c = slice * DVS + hf * HALF;   // column within the head
+            float zv[HALF], wv[HALF], yv[HALF];
+            load_row<HALF>((const __nv_bfloat16 *)a.z + t * a.ld_z + (long long)h * TC_DK + c, zv);
+            load_row<HALF>(a.norm_w + c, wv);
+#pragma unroll
+            for (int jj = 0; jj < HALF; ++jj) yv[jj] = ov[jj] * rs * wv[jj] * silu_fast(zv[jj]);
+            store_row<HALF>(o + t * ldo + col0 + hf * HALF, yv);
+        };
+        float ovp[HALF];   // O rows of the previous chunk, until their norm completes
 
         // ---- the initial state (thread: dk row tl, columns hf*HALF ..)
         float Mr[HALF];
@@ -977,10 +1044,24 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
                 arrive_staged(mtbar);
                 Gl = glp[(ci + 1) * d.hv];
             }
-            // ---------------- O rows -> o (after the publish, so that no operand fence waits on them)
+            // ---------------- O rows -> o, or through the fused norm to y (after the publish,
+            // so that no operand fence waits on these global accesses)
             if (qd >= 2) {
-                const int r = tl - 64;
-                if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, ov);
+                if constexpr (NORM) {
+                    if (ci > 0) finish_norm(ci - 1, c0 - TC_C, TC_C, ovp);
+                    publish_sums(ci, ov);
+#pragma unroll
+                    for (int jj = 0; jj < HALF; ++jj) ovp[jj] = ov[jj];
+                } else {
+                    const int r = tl - 64;
+                    if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, ov);
+                }
+            }
+        }
+        if constexpr (NORM) {
+            if (qd >= 2 && ci == n_chunks && n_chunks > 0) {
+                const long long cl = s + (n_chunks - 1) * TC_C;
+                finish_norm(n_chunks - 1, cl, (int)(e - cl), ovp);
             }
         }
         if (ci < n_chunks) {
@@ -996,7 +1077,7 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     if (warp == 0) tc::tmem_dealloc(tbase, 256);
 }
 
-template <int DVS, typename TIn, typename TOut>
+template <int DVS, typename TIn, typename TOut, bool NORM>
 static cudaError_t launch_tc_t(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t err;
     if (a.T > 0) {
@@ -1010,13 +1091,23 @@ static cudaError_t launch_tc_t(const ChunkArgs &a, cudaStream_t s) {
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     }
-    auto kern = chunk_chain_kernel<DVS, TIn, TOut>;
+    auto kern = chunk_chain_kernel<DVS, TIn, TOut, NORM>;
     constexpr int smem = ChainSmem<DVS>::BYTES;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    dim3 grid(TC_DK / DVS, a.d.hv, a.n_seqs);
-    kern<<<grid, CHAIN_NT, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(TC_DK / DVS, a.d.hv, a.n_seqs);
+    lc.blockDim = dim3(CHAIN_NT);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;   // the slice CTAs of a head, resident together
+    at[0].val.clusterDim.x = TC_DK / DVS;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = NORM ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, kern, a);
 }
 
 bool chunk_tc_supported(const Dims &d) { return d.dk == 128 && d.dv == 128 && d.chunk == 64; }
@@ -1030,7 +1121,10 @@ size_t chunk_tc_ws_bytes(const Dims &d, long long T, long long n_seqs) {
     const long long mc = chunk_tc_max_chunks(T, n_seqs);
     if (mc == 0) return 0;
     const size_t base = (((size_t)n_seqs + 1) * 4 + 255) & ~(size_t)255;
-    return base + (size_t)mc * d.hv * CH_BYTES + (((size_t)mc * d.hv * 4 + 255) & ~(size_t)255);
+    const size_t gl = ((size_t)mc * d.hv * 4 + 255) & ~(size_t)255;
+    const size_t np = ((size_t)mc * d.hv * (TC_DK / CH_DVS) * 64 * 4 + 255) & ~(size_t)255;
+    const size_t nc = ((size_t)mc * d.hv * 4 + 255) & ~(size_t)255;
+    return base + (size_t)mc * d.hv * CH_BYTES + gl + np + nc;
 }
 
 void chunk_tc_carve(ChunkArgs &a, void *ws) {
@@ -1043,23 +1137,27 @@ void chunk_tc_carve(ChunkArgs &a, void *ws) {
     a.chunk_base = (int *)ws;
     a.tp = (unsigned char *)ws + ((((size_t)a.n_seqs + 1) * 4 + 255) & ~(size_t)255);
     a.gl = (float *)(a.tp + (size_t)a.max_chunks * a.d.hv * CH_BYTES);
+    const size_t mh = (size_t)a.max_chunks * a.d.hv;
+    a.npart = (float *)((unsigned char *)a.gl + ((mh * 4 + 255) & ~(size_t)255));
+    a.ncnt = (unsigned *)((unsigned char *)a.npart + ((mh * (TC_DK / CH_DVS) * 64 * 4 + 255) & ~(size_t)255));
 }
 
-cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, cudaStream_t s) {
+cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, bool fuse_norm,
+                            cudaStream_t s) {
     if (a.n_seqs == 0) return cudaSuccess;
     if (!chunk_tc_supported(a.d)) return cudaErrorInvalidValue;
     if (a.T > 0 && (!a.chunk_base || !a.tp)) return cudaErrorInvalidValue;
-#define GDN_TC(DVS_)                                                                         \
-    if (dvs == DVS_) {                                                                        \
-        if (in_bf16)                                                                          \
-            return o_bf16 ? launch_tc_t<DVS_, __nv_bfloat16, __nv_bfloat16>(a, s)             \
-                          : launch_tc_t<DVS_, __nv_bfloat16, float>(a, s);                    \
-        return o_bf16 ? launch_tc_t<DVS_, float, __nv_bfloat16>(a, s)                         \
-                      : launch_tc_t<DVS_, float, float>(a, s);                                \
+    if (fuse_norm && (!a.z || !a.norm_w || !a.npart || !a.ncnt)) return cudaErrorInvalidValue;
+    if (dvs != CH_DVS) return cudaErrorInvalidValue;
+#define GDN_TC(TI, TO)                                                                       \
+    return fuse_norm ? launch_tc_t<CH_DVS, TI, TO, true>(a, s) : launch_tc_t<CH_DVS, TI, TO, false>(a, s)
+    if (in_bf16) {
+        if (o_bf16) GDN_TC(__nv_bfloat16, __nv_bfloat16);
+        GDN_TC(__nv_bfloat16, float);
     }
-    GDN_TC(32)
+    if (o_bf16) GDN_TC(float, __nv_bfloat16);
+    GDN_TC(float, float);
 #undef GDN_TC
-    return cudaErrorInvalidValue;
 }
 
 }  // namespace gdn

@@ -95,6 +95,13 @@ struct ChunkArgs {
     unsigned char *tp;
     float *gl;            // G_last of every (chunk, v-head)
     long long max_chunks;
+    // gated RMSNorm fused into the chain's output (then `o` receives y):
+    // y = o * rsqrt(mean(o^2) + norm_eps) * w * SiLU(z) per (token, v-head)
+    const void *z;        // [T][ld_z] activation dtype
+    long long ld_z;
+    const float *norm_w;  // [dv]
+    float *npart;         // [max_chunks][HV][128/32 slices][64 rows]: per-slice sums of o^2
+    unsigned *ncnt;       // [max_chunks][HV]: slices that have published their sums
 };
 
 struct DecodeArgs {
@@ -149,7 +156,8 @@ bool chunk_tc_supported(const Dims &d);
 long long chunk_tc_max_chunks(long long T, long long n_seqs);
 size_t chunk_tc_ws_bytes(const Dims &d, long long T, long long n_seqs);
 void chunk_tc_carve(ChunkArgs &a, void *ws);
-cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, cudaStream_t s);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, bool fuse_norm,
+                            cudaStream_t s);
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 cudaError_t launch_decode(const DecodeArgs &a, bool fused, bool in_bf16, bool out_bf16,
