@@ -53,6 +53,7 @@ constexpr int WQ_BYTES = 2 * 128 * 128 * 2;             // [-W ; Q'] hi + lo (K-
 constexpr int KT_HALF = 128 * 64 * 2;                   // K~ (MN-major, MN = 128, K = 64), one part
 constexpr int KT_BYTES = 2 * KT_HALF;
 constexpr int CH_DVS = 32;                              // state columns per chain CTA
+constexpr uint32_t NP_EMPTY = 0xFFFFFFFFu;   // unwritten npart entry: a NaN no sum of squares takes
 constexpr int BV_SLICE = 2 * CH_DVS * 64 * 2;           // [bV_hi | bV_lo] of one slice (MN-major, MN = 64, K = 64)
 constexpr int OFF_CH_WQ = TP_BYTES, OFF_CH_KT = OFF_CH_WQ + WQ_BYTES, OFF_CH_BV = OFF_CH_KT + KT_BYTES;
 constexpr int CH_BYTES = OFF_CH_BV + (128 / CH_DVS) * BV_SLICE;   // workspace bytes per (chunk, v-head)
@@ -301,8 +302,6 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(ChunkArgs a) {
         __syncthreads();
     }
     if (tid == 0) a.chunk_base[a.n_seqs] = carry;
-    if (a.ncnt)   // the fused norm's per-(chunk, v-head) publish counters start at zero
-        for (long long i = tid; i < a.max_chunks * a.d.hv; i += 1024) a.ncnt[i] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -374,6 +373,7 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     long long s, e;
     seq_bounds(a.cu_seqlens, lo, a.T, nullptr, s, e);   // malformed bounds are reported by the map
     const long long t0 = s + (j - a.chunk_base[lo]) * TC_C;
+    if (a.npart) a.npart[(j * d.hv + h) * 256 + tid] = __uint_as_float(NP_EMPTY);   // (fused norm)
     unsigned char *gtp = a.tp + ((long long)j * d.hv + h) * CH_BYTES;   // [T ; PT]
     unsigned char *gwq = gtp + OFF_CH_WQ;                                // [-W ; Q']
 
@@ -694,9 +694,10 @@ struct ChainSmem {
     static constexpr int OFF_KT = OFF_BV + 2 * BV_SLICE;
     static constexpr int OFF_MT = OFF_KT + KT_BYTES;
     static constexpr int OFF_UT = OFF_MT + MT;
-    static constexpr int OFF_BAR = OFF_UT + UT;            // 10 mbarriers, tmem slot, flags
-    static constexpr int OFF_NP = OFF_BAR + 96;            // fused norm: half-row sums [64], flag
-    static constexpr int BYTES = OFF_NP + 64 * 4 + 16;
+    static constexpr int OFF_BAR = OFF_UT + UT;            // 14 mbarriers; tmem slot and 4 flags (3 words)
+    static constexpr int SOS = DVS + 4;                    // row stride of the O tiles (conflict-free float4)
+    static constexpr int OFF_SO = OFF_BAR + 144;           // fused norm: O rows x 2 buffers (fp32 [64][SOS])
+    static constexpr int BYTES = OFF_SO + 2 * 64 * SOS * 4;
     static_assert(DVS == CH_DVS, "the workspace holds bV in slices of CH_DVS columns");
     static_assert(OFF_TP % 16 == 0 && OFF_BV % 16 == 0 && OFF_KT % 16 == 0, "bulk-copy alignment");
 };
@@ -746,6 +747,7 @@ __device__ __forceinline__ void tmem_ld_cat16(uint32_t taddr, float (&v)[16]) {
 // The critical path is M -> G3 -> E3 -> G5 -> E5 -> M; G2 of chunk c+1 is
 // issued right behind G5 of chunk c.
 constexpr int CHAIN_NT = 288;
+constexpr int CHAIN_NT_NORM = 416;   // + 4 warps (9-12) applying the fused gated norm
 
 __device__ __forceinline__ void bar_sync_staging() {   // warps 0-7 only
     asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -770,24 +772,33 @@ __device__ __forceinline__ void arrive_staged(uint64_t *bar) {
     tc::mbar_arrive(tc::smem_u32(bar));
 }
 
-// The fused gated RMSNorm needs each row's sum of squares over all dv columns,
-// which the four slice CTAs of a head hold a quarter each.  A slice publishes
-// its 64 per-row sums of chunk c to the workspace and counts itself in
-// ncnt[chunk][head] (release); one chunk later, when the peers have long done
-// the same, it waits (bounded, acquire) for the count to reach 4, adds the
-// four sums and writes y.  The four CTAs are launched as one cluster, so they
-// are always resident together.
-__device__ __forceinline__ void named_bar_o() {   // the 128 threads holding O rows (warps 2, 3, 6, 7)
-    asm volatile("bar.sync 2, 128;" ::: "memory");
+// The fused gated RMSNorm runs on four extra warps (9-12), off the chain's
+// path: E3 hands each chunk's O rows over through a double-buffered tile in
+// shared memory (mbarriers obar / ofree).  A row's sum of squares spans all dv
+// columns, which the four slice CTAs of a head hold a quarter each: a slice
+// writes its per-row sum of chunk c into its entry of npart[chunk][head][row]
+// (four 32-bit entries, one per slice).  chunk_tp_kernel fills every entry with
+// the marker NP_EMPTY beforehand, and a sum never has that bit pattern, so an
+// entry is its own ready flag: two chunks later the row's threads load the four
+// entries in one 16-byte load (repeated, bounded, until none is the marker), add
+// them and write y.  No fence or counter is needed.  The four CTAs are launched
+// as one cluster, so they are always resident together.
+__device__ __forceinline__ void st_relaxed_gpu(float *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+__device__ __forceinline__ uint4 ld_relaxed_gpu_v4(const float *p) {
+    uint4 u;
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "l"(p) : "memory");
+    return u;
+}
+__device__ __forceinline__ bool np_ready(const uint4 &u) {
+    return u.x != NP_EMPTY && u.y != NP_EMPTY && u.z != NP_EMPTY && u.w != NP_EMPTY;
 }
 
 template <int DVS, typename TIn, typename TOut, bool NORM>
-__global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
+__global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
+    constexpr int NT = NORM ? CHAIN_NT_NORM : CHAIN_NT;
     using L = ChainSmem<DVS>;
     constexpr int HALF = DVS / 2;                 // state columns per thread in lane mapping
     static_assert(HALF == 16, "epilogues load 16 columns per block");
@@ -797,11 +808,11 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint64_t *wqbar = bars + 0, *tpbar = bars + 1 /* [2] */, *bvbar = bars + 3 /* [2] */,
              *ktbar = bars + 5, *mtbar = bars + 6, *utbar = bars + 7, *g3bar = bars + 8, *g5bar = bars + 9;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
-    volatile uint32_t *flag3 = reinterpret_cast<uint32_t *>(bars + 10) + 1;
-    volatile uint32_t *flag5 = reinterpret_cast<uint32_t *>(bars + 11);
-    float *sNp = reinterpret_cast<float *>(sm + L::OFF_NP);
-    volatile uint32_t *flagN = reinterpret_cast<uint32_t *>(sm + L::OFF_NP + 64 * 4);
+    uint64_t *obar = bars + 10 /* [2] */, *ofree = bars + 12 /* [2] */;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
+    volatile uint32_t *flag3 = reinterpret_cast<uint32_t *>(bars + 14) + 1;
+    volatile uint32_t *flag5 = reinterpret_cast<uint32_t *>(bars + 15);
+    float *sO = reinterpret_cast<float *>(sm + L::OFF_SO);     // [2][64][SOS]
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -816,7 +827,7 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
     TOut *o = (TOut *)a.o;
     const long long ldo = (long long)d.hv * TC_DK;
     if (a.state_idx && slot < 0) {
-        for (long long t = s + tid / DVS; t < e; t += CHAIN_NT / DVS)
+        for (long long t = s + tid / DVS; t < e; t += NT / DVS)
             o[t * ldo + col0 + tid % DVS] = from_f32<TOut>(0.f);
         return;
     }
@@ -846,6 +857,10 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
         tc::mbar_init(tc::smem_u32(utbar), 256);
         tc::mbar_init(tc::smem_u32(g3bar), 1);
         tc::mbar_init(tc::smem_u32(g5bar), 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(tc::smem_u32(&obar[b]), 128);
+            tc::mbar_init(tc::smem_u32(&ofree[b]), 128);
+        }
         tc::mbar_fence_init();
     }
     tc::fence_before_sync();
@@ -944,58 +959,105 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
                 tc::mbar_wait(tc::smem_u32(g5bar), (uint32_t)((n_chunks - 1) & 1));   // last G5 retired
             }
         }
+    } else if (warp >= 9) {
+        // ================= fused gated norm (warps 9-12, NORM only) ================
+        if constexpr (NORM) {
+            static_assert(TC_DK / DVS == 4, "one 16-byte npart word per row");
+            const int nid = tid - 288, r = nid >> 1, hh = nid & 1;   // row r, columns hh*HALF ..
+            const int c = slice * DVS + hh * HALF;                     // column within the head
+            auto np_row = [&](long long i) { return a.npart + (((jc + i) * d.hv + h) * 64 + r) * 4; };
+            // z of the rows of chunk i (packed bf16, 16 values), loaded ahead of use
+            auto load_z = [&](long long i, uint4 (&zp)[2]) {
+                const long long t = s + i * TC_C + r;
+                if (t < e) {
+                    const uint4 *zz = reinterpret_cast<const uint4 *>(
+                        (const __nv_bfloat16 *)a.z + t * a.ld_z + (long long)h * TC_DK + c);
+                    zp[0] = zz[0];
+                    zp[1] = zz[1];
+                } else {
+                    zp[0] = zp[1] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            };
+            // y of row r of chunk i from its O values, its z and u, an earlier load of the four
+            // slices' sums (repeated, bounded, until all are written); false on a timeout
+            auto finish = [&](long long i, uint4 u, const float (&ov)[HALF], const uint4 (&zp)[2]) -> bool {
+                const long long t = s + i * TC_C + r;
+                if (t >= e) return true;
+                if (!np_ready(u)) {
+                    const uint64_t t0 = tc::globaltimer_ns();
+                    for (uint32_t it = 0; it < tc::kSpinLimit && !np_ready(u); ++it) {
+                        u = ld_relaxed_gpu_v4(np_row(i));
+                        if ((it & 63u) == 63u && tc::globaltimer_ns() - t0 > tc::kWaitNs) break;
+                    }
+                    if (!np_ready(u)) return false;
+                }
+                const float tot = (__uint_as_float(u.x) + __uint_as_float(u.y)) +
+                                  (__uint_as_float(u.z) + __uint_as_float(u.w));
+                const float rs = rsqrtf(tot / (float)TC_DK + d.norm_eps);
+                float wv[HALF];
+                load_row<HALF>(a.norm_w + c, wv);   // (L1-resident)
+                const __nv_bfloat162 *z2 = reinterpret_cast<const __nv_bfloat162 *>(zp);
+                float yv[HALF];
+#pragma unroll
+                for (int jj = 0; jj < HALF; jj += 2) {
+                    const float2 zf = __bfloat1622float2(z2[jj / 2]);
+                    yv[jj] = ov[jj] * rs * wv[jj] * silu_fast(zf.x);
+                    yv[jj + 1] = ov[jj + 1] * rs * wv[jj + 1] * silu_fast(zf.y);
+                }
+                store_row<HALF>(o + t * ldo + col0 + hh * HALF, yv);
+                return true;
+            };
+            // Pipeline, chunk i: request z and the sums of chunk i-2, wait for O_i, free its tile,
+            // publish its sums, then finish chunk i-2 (its peers published it a chunk ago).
+            float ov1[HALF], ov2[HALF];   // O rows of chunks i-1 and i-2
+            bool ok = true;
+            long long i = 0;
+            for (; i < n_chunks; ++i) {
+                uint4 zp[2], u = make_uint4(NP_EMPTY, NP_EMPTY, NP_EMPTY, NP_EMPTY);
+                if (i >= 2) {
+                    load_z(i - 2, zp);
+                    u = ld_relaxed_gpu_v4(np_row(i - 2));
+                }
+                if (!tc::mbar_wait(tc::smem_u32(&obar[i & 1]), (uint32_t)((i >> 1) & 1))) break;
+                float ov[HALF];
+                const float *src = sO + ((int)(i & 1) * 64 + r) * L::SOS + hh * HALF;
+#pragma unroll
+                for (int j4 = 0; j4 < HALF; j4 += 4) {
+                    const float4 f = *reinterpret_cast<const float4 *>(src + j4);
+                    ov[j4] = f.x; ov[j4 + 1] = f.y; ov[j4 + 2] = f.z; ov[j4 + 3] = f.w;
+                }
+                tc::mbar_arrive(tc::smem_u32(&ofree[i & 1]));   // the tile may be refilled
+                float ss = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < HALF; ++jj) ss += ov[jj] * ov[jj];
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (hh == 0) {
+                    const uint32_t bits = __float_as_uint(ss);
+                    st_relaxed_gpu(np_row(i) + slice, bits == NP_EMPTY ? 0x7FFFFFFFu : bits);
+                }
+                if (i >= 2 && ok) ok = finish(i - 2, u, ov2, zp);
+#pragma unroll
+                for (int jj = 0; jj < HALF; ++jj) { ov2[jj] = ov1[jj]; ov1[jj] = ov[jj]; }
+            }
+            // drain: chunks n-2 and n-1
+            if (i == n_chunks && ok && n_chunks >= 2) {
+                uint4 zp[2];
+                load_z(n_chunks - 2, zp);
+                ok = finish(n_chunks - 2, ld_relaxed_gpu_v4(np_row(n_chunks - 2)), ov2, zp);
+            }
+            if (i == n_chunks && ok && n_chunks >= 1) {
+                uint4 zp[2];
+                load_z(n_chunks - 1, zp);
+                ok = finish(n_chunks - 1, ld_relaxed_gpu_v4(np_row(n_chunks - 1)), ov1, zp);
+            }
+            if (i < n_chunks || !ok) set_error(a.err, GDN_DEVERR_TIMEOUT);
+        }
     } else {
         // ========================= epilogue warps 0-7 ==========================
         const int qd = warp & 3, hf = warp >> 2;   // lane mapping: TMEM lane tl, column half hf
         const int tl = qd * 32 + lane;
         const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
         const float *glp = a.gl + jc * d.hv + h;   // G_last of chunk i at glp[i * hv]
-        // fused norm (threads holding O rows: TMEM lanes 64-127, row r = tl - 64)
-        const int orow = tl - 64;
-        auto publish_sums = [&](long long i, const float (&ov)[HALF]) {
-            float ss = 0.f;
-#pragma unroll
-            for (int jj = 0; jj < HALF; ++jj) ss += ov[jj] * ov[jj];
-            if (hf == 1) sNp[orow] = ss;
-            named_bar_o();
-            if (hf == 0) {
-                a.npart[(((jc + i) * d.hv + h) * (TC_DK / DVS) + slice) * 64 + orow] = ss + sNp[orow];
-                __threadfence();
-            }
-            named_bar_o();
-            if (hf == 0 && orow == 0) atomicAdd(a.ncnt + (jc + i) * d.hv + h, 1u);
-        };
-        auto finish_norm = [&](long long i, long long ci0, int Li, const float (&ov)[HALF]) {
-            if (hf == 0 && orow == 0) {
-                const unsigned *cnt = a.ncnt + (jc + i) * d.hv + h;
-                bool ok = ld_acquire_gpu(cnt) >= (unsigned)(TC_DK / DVS);
-                if (!ok) {
-                    const uint64_t t0 = tc::globaltimer_ns();
-                    for (uint32_t it = 0; it < tc::kSpinLimit && !ok; ++it) {
-                        ok = ld_acquire_gpu(cnt) >= (unsigned)(TC_DK / DVS);
-                        if (!ok && (it & 63u) == 63u && tc::globaltimer_ns() - t0 > tc::kWaitNs) break;
-                    }
-                }
-                *flagN = ok ? 0u : 1u;
-                if (!ok) set_error(a.err, GDN_DEVERR_TIMEOUT);
-            }
-            named_bar_o();
-            if (*flagN != 0u || orow >= Li) return;
-            const float *np = a.npart + ((jc + i) * d.hv + h) * (TC_DK / DVS) * 64 + orow;
-            float tot = 0.f;
-#pragma unroll
-            for (int q = 0; q < TC_DK / DVS; ++q) tot += __ldcg(np + q * 64);
-            const float rs = rsqrtf(tot / (float)TC_DK + d.norm_eps);
-            const long long t = ci0 + orow;
-            const int c = slice * DVS + hf * HALF;   // column within the head
-            float zv[HALF], wv[HALF], yv[HALF];
-            load_row<HALF>((const __nv_bfloat16 *)a.z + t * a.ld_z + (long long)h * TC_DK + c, zv);
-            load_row<HALF>(a.norm_w + c, wv);
-#pragma unroll
-            for (int jj = 0; jj < HALF; ++jj) yv[jj] = ov[jj] * rs * wv[jj] * silu_fast(zv[jj]);
-            store_row<HALF>(o + t * ldo + col0 + hf * HALF, yv);
-        };
-        float ovp[HALF];   // O rows of the previous chunk, until their norm completes
 
         // ---- the initial state (thread: dk row tl, columns hf*HALF ..)
         float Mr[HALF];
@@ -1031,6 +1093,19 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
                 for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(utt, hf * HALF + j8, tl, &ov[j8]);
             }
             arrive_staged(utbar);
+            if constexpr (NORM) {
+                // O rows -> the norm warps (shared memory only, off the chain's path)
+                if (qd >= 2) {
+                    const int k = (int)(ci & 1);
+                    if (ci >= 2 && !tc::mbar_wait(tc::smem_u32(&ofree[k]), (uint32_t)(((ci >> 1) - 1) & 1)))
+                        set_error(a.err, GDN_DEVERR_TIMEOUT);
+                    float *dst = sO + (k * 64 + (tl - 64)) * L::SOS + hf * HALF;
+#pragma unroll
+                    for (int j4 = 0; j4 < HALF; j4 += 4)
+                        *reinterpret_cast<float4 *>(dst + j4) = make_float4(ov[j4], ov[j4 + 1], ov[j4 + 2], ov[j4 + 3]);
+                    tc::mbar_arrive(tc::smem_u32(&obar[k]));
+                }
+            }
             // ---------------- E5: M <- gamma_last M + dM -> mtbar
             if (!staging_wait(g5bar, par, flag5, tid)) break;
             float v[HALF];
@@ -1046,22 +1121,9 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) chunk_chain_kernel(ChunkArgs a) {
             }
             // ---------------- O rows -> o, or through the fused norm to y (after the publish,
             // so that no operand fence waits on these global accesses)
-            if (qd >= 2) {
-                if constexpr (NORM) {
-                    if (ci > 0) finish_norm(ci - 1, c0 - TC_C, TC_C, ovp);
-                    publish_sums(ci, ov);
-#pragma unroll
-                    for (int jj = 0; jj < HALF; ++jj) ovp[jj] = ov[jj];
-                } else {
-                    const int r = tl - 64;
-                    if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, ov);
-                }
-            }
-        }
-        if constexpr (NORM) {
-            if (qd >= 2 && ci == n_chunks && n_chunks > 0) {
-                const long long cl = s + (n_chunks - 1) * TC_C;
-                finish_norm(n_chunks - 1, cl, (int)(e - cl), ovp);
+            if (!NORM && qd >= 2) {
+                const int r = tl - 64;
+                if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, ov);
             }
         }
         if (ci < n_chunks) {
@@ -1097,7 +1159,7 @@ static cudaError_t launch_tc_t(const ChunkArgs &a, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(TC_DK / DVS, a.d.hv, a.n_seqs);
-    lc.blockDim = dim3(CHAIN_NT);
+    lc.blockDim = dim3(NORM ? CHAIN_NT_NORM : CHAIN_NT);
     lc.dynamicSmemBytes = smem;
     lc.stream = s;
     cudaLaunchAttribute at[1];
@@ -1123,8 +1185,7 @@ size_t chunk_tc_ws_bytes(const Dims &d, long long T, long long n_seqs) {
     const size_t base = (((size_t)n_seqs + 1) * 4 + 255) & ~(size_t)255;
     const size_t gl = ((size_t)mc * d.hv * 4 + 255) & ~(size_t)255;
     const size_t np = ((size_t)mc * d.hv * (TC_DK / CH_DVS) * 64 * 4 + 255) & ~(size_t)255;
-    const size_t nc = ((size_t)mc * d.hv * 4 + 255) & ~(size_t)255;
-    return base + (size_t)mc * d.hv * CH_BYTES + gl + np + nc;
+    return base + (size_t)mc * d.hv * CH_BYTES + gl + np;
 }
 
 void chunk_tc_carve(ChunkArgs &a, void *ws) {
@@ -1139,7 +1200,6 @@ void chunk_tc_carve(ChunkArgs &a, void *ws) {
     a.gl = (float *)(a.tp + (size_t)a.max_chunks * a.d.hv * CH_BYTES);
     const size_t mh = (size_t)a.max_chunks * a.d.hv;
     a.npart = (float *)((unsigned char *)a.gl + ((mh * 4 + 255) & ~(size_t)255));
-    a.ncnt = (unsigned *)((unsigned char *)a.npart + ((mh * (TC_DK / CH_DVS) * 64 * 4 + 255) & ~(size_t)255));
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, bool fuse_norm,
@@ -1147,10 +1207,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int d
     if (a.n_seqs == 0) return cudaSuccess;
     if (!chunk_tc_supported(a.d)) return cudaErrorInvalidValue;
     if (a.T > 0 && (!a.chunk_base || !a.tp)) return cudaErrorInvalidValue;
-    if (fuse_norm && (!a.z || !a.norm_w || !a.npart || !a.ncnt)) return cudaErrorInvalidValue;
+    if (fuse_norm && (!a.z || !a.norm_w || !a.npart)) return cudaErrorInvalidValue;
     if (dvs != CH_DVS) return cudaErrorInvalidValue;
+    ChunkArgs b = a;
+    b.npart = nullptr;   // no fused norm: no sums to mark
 #define GDN_TC(TI, TO)                                                                       \
-    return fuse_norm ? launch_tc_t<CH_DVS, TI, TO, true>(a, s) : launch_tc_t<CH_DVS, TI, TO, false>(a, s)
+    return fuse_norm ? launch_tc_t<CH_DVS, TI, TO, true>(a, s) : launch_tc_t<CH_DVS, TI, TO, false>(b, s)
     if (in_bf16) {
         if (o_bf16) GDN_TC(__nv_bfloat16, __nv_bfloat16);
         GDN_TC(__nv_bfloat16, float);

@@ -100,8 +100,8 @@ struct ChunkArgs {
     const void *z;        // [T][ld_z] activation dtype
     long long ld_z;
     const float *norm_w;  // [dv]
-    float *npart;         // [max_chunks][HV][128/32 slices][64 rows]: per-slice sums of o^2
-    unsigned *ncnt;       // [max_chunks][HV]: slices that have published their sums
+    float *npart;         // [max_chunks][HV][64 rows][128/32 slices]: per-slice sums of o^2
+                          // (null: chunk_tp_kernel leaves no markers there)
 };
 
 struct DecodeArgs {
