@@ -58,6 +58,17 @@ def chunk_flops(lens, C, dk, dv, HV):
     return tot * HV
 
 
+def step_hbm_bytes(wl, T, N):
+    """Algorithmic HBM bytes of one mixer prefill step: per token x (CH activations), z and y
+    (HV*dv activations each) and g, beta (HV fp32 each); per sequence the fp32 state read and
+    written (zero initial state: written only) and the conv history read and written."""
+    a = 2 if wl.act == "bf16" else 4
+    per_tok = wl.CH * a + 2 * wl.HV * wl.dv * a + 2 * wl.HV * 4
+    state = wl.HV * wl.dk * wl.dv * 4 * (2 if wl.init_state else 1)
+    conv = wl.CH * 3 * a * (2 if wl.init_conv else 1)
+    return T * per_tok + N * (state + conv)
+
+
 def src_sha(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -304,11 +315,27 @@ def run_ours(args, rank, ws, local):
             "traffic": traffic_for("chunk_prefill_8k"), "peak_source": pk_src + " bf16 burst",
             "kernel_ms": chunk_s * 1e3, "flops_per_launch": flops}
     del g, beta, xa, o, flush
+    # the whole step against both bounds: the step's algorithmic bytes (x, z, y, g and beta per
+    # token, state in and out per sequence) at the copy peak and its contraction FLOPs at the
+    # tensor peak, the larger over the measured step time
+    step_s = elapsed / args.steps
+    step_bytes = step_hbm_bytes(wl, T, N)
+    t_tc, t_hbm = flops / (tc_peak * 1e12), step_bytes / (pk["hbm_gbs"] * 1e9)
+    step_roof = {"scope": "one gdn_mixer_prefill step", "flops": flops, "bytes": step_bytes,
+                 "tensor_floor_us": t_tc * 1e6, "hbm_floor_us": t_hbm * 1e6,
+                 "bound": "hbm" if t_hbm >= t_tc else "tensor", "step_us": step_s * 1e6,
+                 "frac": max(t_tc, t_hbm) / step_s, "tensor_frac": t_tc / step_s,
+                 "peak_source": pk_src}
 
     # ---- decode: 64 sequences x S one-token steps, L2 flushed between steps
     dec = None
     if args.decode_steps > 0:
         dec = bench_decode(args, dev, gdn, pk, pk_src)
+
+    # ---- slot snapshot (state + conv history) through gdn_state_copy
+    snap = None
+    if args.decode_steps > 0:
+        snap = bench_state_copy(args, dev, gdn, pk, pk_src)
 
     # ---- end to end through the public fused call with pinned host buffers
     e2e = None
@@ -331,9 +358,9 @@ def run_ours(args, rank, ws, local):
                            "l2": "inputs larger than L2 (x %d MiB + z %d MiB per step)"
                                  % (T * wl.CH * 2 >> 20, T * wl.HV * wl.dv * 2 >> 20),
                            "activations": wl.act, "y_dtype": "bf16"},
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk.summary(), "decode": dec}
+                "clocks": clk.summary(), "decode": dec, "state_copy": snap}
         print(json.dumps(line), flush=True)
 
 
@@ -386,6 +413,45 @@ def bench_decode(args, dev, gdn, pk, pk_src):
                          "traffic": traffic_for("decode_64x256"),
                          "peak_source": pk_src + " copy"},
             "gpu_launches": 2 * S}
+
+
+def bench_state_copy(args, dev, gdn, pk, pk_src):
+    """Snapshot of the decode workload's 64 live slots (fp32 state + bf16 conv history) into 64
+    snapshot rows of the same pool, through gdn_state_copy; L2 evicted before each launch."""
+    wl = WORKLOADS["decode_64x256"]
+    N = wl.n_decode
+    cfg = gdn.make_config(wl.HK, wl.HV, wl.dk, wl.dv, wl.chunk, wl.act, n_slots=2 * N)
+    state = torch.zeros((2 * N, wl.HV, wl.dk, wl.dv), device=dev)
+    conv = torch.zeros((2 * N, wl.CH, 3), dtype=wl.torch_act, device=dev)
+    state[:N].normal_(0.0, 0.02)
+    conv[:N].normal_()
+    live = torch.arange(N, dtype=torch.int32, device=dev)
+    snap = live + N
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+    flush.fill_(1.0)
+    sink = torch.empty((), device=dev)
+    stream = torch.cuda.current_stream()
+    reps = max(5, min(args.decode_steps, 20))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps + 3)]
+    for i in range(reps + 3):           # 3 untimed warm-ups
+        torch.sum(flush, 0, out=sink)
+        evs[i][0].record(stream)
+        gdn.gdn_state_copy(cfg, state, conv, state, conv, live, snap)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_error() == 0
+    assert torch.equal(state[:N], state[N:]) and torch.equal(conv[:N], conv[N:])
+    per = sum(a.elapsed_time(b) for a, b in evs[3:]) / reps / 1e3
+    moved = 2 * N * (wl.HV * wl.dk * wl.dv * 4 + wl.CH * 3 * 2)
+    gbs = moved / per / 1e9
+    return {"workload": "snapshot of 64 live slots (fp32 state 2 MiB + bf16 conv history 48 KiB "
+                        "each) into 64 rows of the same pool, L2 evicted before each launch",
+            "value": gbs, "unit": "GB/s", "us_per_launch": per * 1e6, "bytes_per_launch": moved,
+            "roofline": {"kernel": "state_copy_kernel", "bound": "hbm", "achieved": gbs,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                         "traffic": None, "peak_source": pk_src + " copy"},
+            "gpu_launches": reps}
 
 
 def bench_e2e(args, dev, gdn, cfg, wl, inp, d, N, T):

@@ -414,6 +414,27 @@ gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void 
                                             io->y_dtype == GDN_BF16, (cudaStream_t)stream));
 }
 
+gdn_status gdn_state_copy(const gdn_config *cfg, const float *src_state, const void *src_conv,
+                          int32_t n_src_slots, float *dst_state, void *dst_conv,
+                          int32_t n_dst_slots, const int32_t *src_idx, const int32_t *dst_idx,
+                          int32_t n, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (n < 0 || n > kMaxSeqs || n_src_slots < 0 || n_dst_slots < 0) return GDN_ERR_INVALID_ARG;
+    if (n == 0 || (!dst_state && !dst_conv)) return GDN_OK;
+    if (!src_idx || !dst_idx) return GDN_ERR_INVALID_ARG;
+    if ((src_state && !aligned16(src_state)) || (dst_state && !aligned16(dst_state)) ||
+        (src_conv && !aligned16(src_conv)) || (dst_conv && !aligned16(dst_conv)))
+        return GDN_ERR_INVALID_ARG;
+    if ((long long)d.ch * 3 * (cfg->act == GDN_BF16 ? 2 : 4) % 16 != 0) return GDN_ERR_UNSUPPORTED;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    return launch_status(gdn::launch_state_copy(d, cfg->act == GDN_BF16, src_state, src_conv,
+                                                n_src_slots, dst_state, dst_conv, n_dst_slots,
+                                                src_idx, dst_idx, n, err, (cudaStream_t)stream));
+}
+
 gdn_status gdn_device_error(void *stream, uint32_t *code) {
     if (!code) return GDN_ERR_INVALID_ARG;
     *code = 0;

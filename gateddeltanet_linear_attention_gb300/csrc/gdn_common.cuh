@@ -141,6 +141,12 @@ cudaError_t launch_conv_prefill(const Dims &d, bool act_bf16, const void *x, lon
                                 const int32_t *cu, int n_seqs, long long T, const void *w,
                                 const void *conv_state, const int32_t *state_idx, void *out,
                                 bool out_bf16, unsigned *err, cudaStream_t s);
+// Snapshot / restore / reset of state slots (gdn_state_copy); the history
+// words per slot assume CH * 3 * element size is a multiple of 16 bytes.
+cudaError_t launch_state_copy(const Dims &d, bool act_bf16, const float *src_state,
+                              const void *src_conv, int n_src, float *dst_state, void *dst_conv,
+                              int n_dst, const int32_t *src_idx, const int32_t *dst_idx, int n,
+                              unsigned *err, cudaStream_t s);
 cudaError_t launch_conv_state_update(const Dims &d, bool act_bf16, const void *x,
                                      long long ld_x, const int32_t *cu, int n_seqs, long long T,
                                      void *conv_state, const int32_t *state_idx, unsigned *err,

@@ -88,6 +88,7 @@ def load(path: str | None = None):
             "gdn_mixer_prefill": ([CP, ctypes.POINTER(MixerIO), P, SZ, V], I32),
             "gdn_mixer_decode": ([CP, ctypes.POINTER(MixerIO), P, SZ, V], I32),
             "gdn_mixer_prefill_static": ([CP, ctypes.POINTER(MixerIO), V], I32),
+            "gdn_state_copy": ([CP, P, P, I32, P, P, I32, P, P, I32, V], I32),
             "gdn_device_error": ([V, ctypes.POINTER(U32)], I32),
             "gdn_status_string": ([I32], ctypes.c_char_p),
         }
@@ -225,6 +226,35 @@ def gdn_mixer_decode(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, s
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().gdn_mixer_decode(ctypes.byref(cfg), ctypes.byref(io), _ptr(workspace), ws_bytes,
                                    _stream(stream)), "gdn_mixer_decode")
+
+
+def gdn_state_copy(cfg, src_state, src_conv, dst_state, dst_conv, src_idx, dst_idx, stream=None):
+    """Snapshot / restore / reset: slot src_idx[i] -> slot dst_idx[i] (src < 0: reset to zeros,
+    dst < 0: nothing).  The slot counts come from the pools' first dimension; src and dst may be
+    the same tensors."""
+    import torch
+    CH = 2 * cfg.hk * cfg.dk + cfg.hv * cfg.dv
+    act = torch.bfloat16 if cfg.act == GDN_BF16 else torch.float32
+    for t in (src_state, dst_state):
+        if t is not None and (tuple(t.shape[1:]) != (cfg.hv, cfg.dk, cfg.dv) or t.dtype != torch.float32
+                              or not t.is_contiguous()):
+            raise ValueError("state pools are contiguous fp32 [slots][HV][dk][dv]")
+    for t in (src_conv, dst_conv):
+        if t is not None and (tuple(t.shape[1:]) != (CH, 3) or t.dtype != act or not t.is_contiguous()):
+            raise ValueError("history pools are contiguous [slots][CH][3] in the activation dtype")
+    for t in (src_idx, dst_idx):
+        if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+            raise ValueError("slot indices are contiguous int32")
+    if src_idx is not None and dst_idx is not None and src_idx.numel() != dst_idx.numel():
+        raise ValueError("src_idx and dst_idx differ in length")
+
+    def slots(*ts):
+        return min([t.shape[0] for t in ts if t is not None] or [0])
+    n = 0 if dst_idx is None else dst_idx.numel()
+    _check(load().gdn_state_copy(ctypes.byref(cfg), _ptr(src_state), _ptr(src_conv),
+                                 slots(src_state, src_conv), _ptr(dst_state), _ptr(dst_conv),
+                                 slots(dst_state, dst_conv), _ptr(src_idx), _ptr(dst_idx), n,
+                                 _stream(stream)), "gdn_state_copy")
 
 
 def gdn_device_error(stream=None) -> int:

@@ -221,6 +221,33 @@ gdn_status gdn_mixer_prefill_static(const gdn_config *cfg, const gdn_mixer_io *i
 gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* State maintenance: snapshot, restore, initialise and reset of state slots
+ * as one indirect copy driven by device-resident slot-index buffers
+ * (hyperflare core-design: the "State operations" row of the native model
+ * contract, the state-maintenance graph entries, and the speculative-state
+ * section: a snapshot selects one recurrent state column and copies its
+ * three-token conv window; snapshot and restore preserve committed state
+ * exactly and allocate nothing).  For each pair i < n, with s = src_idx[i]
+ * and t = dst_idx[i] (int32, DEVICE):
+ *   t < 0          nothing (an inactive lane);
+ *   s >= 0, t >= 0 slot s of (src_state, src_conv) is copied to slot t of
+ *                  (dst_state, dst_conv) bit for bit;
+ *   s < 0,  t >= 0 slot t is reset to zeros (the initial state and history).
+ * src_state / dst_state: fp32 [slots][HV][dk][dv]; src_conv / dst_conv: act
+ * [slots][CH][3].  dst_state == NULL leaves states untouched (and src_state
+ * is not read); likewise dst_conv.  A NULL source with a non-NULL
+ * destination resets.  n_src_slots / n_dst_slots bound the indices: a pair
+ * with t >= n_dst_slots, or s >= n_src_slots while a source pool is given,
+ * is skipped and reported as GDN_DEVERR_SLOT.  Source and destination may be the same pool (a pool
+ * holding live and snapshot rows); then the live destination slots of one
+ * call must be distinct and must not be read as a source by another pair of
+ * the same call (the indices are device data and are not checked on the
+ * host).  n == 0 launches nothing. */
+gdn_status gdn_state_copy(const gdn_config *cfg, const float *src_state, const void *src_conv,
+                          int32_t n_src_slots, float *dst_state, void *dst_conv,
+                          int32_t n_dst_slots, const int32_t *src_idx, const int32_t *dst_idx,
+                          int32_t n, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device into *code (HOST pointer; GDN_DEVERR_* bits).  Returns
  * GDN_ERR_DEVICE when a code was set, GDN_OK otherwise. */

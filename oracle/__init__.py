@@ -170,3 +170,38 @@ def mixer(x, conv_w, u, b_logit, A_log, dt_bias, z, norm_w, cu_seqlens, HK, HV, 
         out["xa"] = xa
         out["o"] = o
     return out
+
+
+def state_copy(src_state, src_conv, dst_state, dst_conv, src_idx, dst_idx):
+    """Slot maintenance (hyperflare core-design, "State operations": snapshot, restore and
+    reset as indirect copies over slot indices).  For each pair (s, t): t < 0 does nothing;
+    s >= 0 copies source slot s to destination slot t exactly; s < 0 resets slot t to zeros.
+    A pair whose t is past the destination pool, or whose s is past a given source pool, is
+    skipped and flagged.  The pairs are applied in order, each reading the sources as they were
+    before the call (the library's contract keeps sources and destinations apart, where order
+    cannot matter).  Works on any array dtype (bit-exact: plain element copies).
+
+    Returns (new dst_state or None, new dst_conv or None, slot_error)."""
+    out_s = None if dst_state is None else np.array(dst_state, copy=True)
+    out_c = None if dst_conv is None else np.array(dst_conv, copy=True)
+    srcs = [a for a in (src_state, src_conv) if a is not None]
+    dsts = [a for a in (out_s, out_c) if a is not None]
+    n_src = min((a.shape[0] for a in srcs), default=0)
+    n_dst = min((a.shape[0] for a in dsts), default=0)
+    src_s0 = None if src_state is None else np.array(src_state, copy=True)
+    src_c0 = None if src_conv is None else np.array(src_conv, copy=True)
+    err = False
+    for s, t in zip(np.asarray(src_idx).tolist(), np.asarray(dst_idx).tolist()):
+        if t < 0:
+            continue
+        if t >= n_dst or (s >= n_src and srcs):
+            err = True
+            continue
+        for src, dst in ((src_s0, out_s), (src_c0, out_c)):
+            if dst is None:
+                continue
+            if s >= 0 and src is not None:
+                dst[t] = src[s]
+            else:
+                dst[t] = 0
+    return out_s, out_c, err

@@ -162,3 +162,23 @@ def test_decode_and_norm_validation(lib):
     assert lib.gdn_gated_rmsnorm(ch, A16, 3, A16, 4096, A16, 4, A16, 1, None) == INVALID
     assert lib.gdn_conv1d_step(ch, A16, 8192, 2, A16, None, None, A16, 1, None) == INVALID
     assert lib.gdn_conv1d_prefill(ch, A16, 8192, None, 1, 10, A16, None, None, A16, 1, None) == INVALID
+
+
+def test_state_copy_validation(lib):
+    c = cfg()
+    ch = ctypes.byref(c)
+    # n < 0, negative pool sizes, missing index buffers, misaligned pools
+    assert lib.gdn_state_copy(ch, A16, A16, 4, A16b, A16b, 4, A16, A16, -1, None) == INVALID
+    assert lib.gdn_state_copy(ch, A16, A16, -1, A16b, A16b, 4, A16, A16, 1, None) == INVALID
+    assert lib.gdn_state_copy(ch, A16, A16, 4, A16b, A16b, -2, A16, A16, 1, None) == INVALID
+    assert lib.gdn_state_copy(ch, A16, A16, 4, A16b, A16b, 4, None, A16, 1, None) == INVALID
+    assert lib.gdn_state_copy(ch, A16, A16, 4, A16b, A16b, 4, A16, None, 1, None) == INVALID
+    assert lib.gdn_state_copy(ch, MIS, None, 4, A16b, None, 4, A16, A16, 1, None) == INVALID
+    assert lib.gdn_state_copy(ch, A16, None, 4, P(0x200008), None, 4, A16, A16, 1, None) == INVALID
+    assert lib.gdn_state_copy(ch, None, MIS, 4, None, A16b, 4, A16, A16, 1, None) == INVALID
+    # nothing to do: no pairs, or no destination pool -- never touches the GPU
+    assert lib.gdn_state_copy(ch, A16, A16, 4, A16b, A16b, 4, A16, A16, 0, None) == OK
+    assert lib.gdn_state_copy(ch, A16, A16, 4, None, None, 4, A16, A16, 3, None) == OK
+    # an invalid configuration is refused first
+    bad = cfg(dk=96, dv=96)
+    assert lib.gdn_state_copy(ctypes.byref(bad), A16, A16, 4, A16b, A16b, 4, A16, A16, 1, None) == UNSUPPORTED

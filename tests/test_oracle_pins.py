@@ -352,3 +352,30 @@ def test_mixer_varlen_equals_separate_and_padding_lane():
     np.testing.assert_array_equal(pad["y"][cu[2]:cu[3]], 0.0)
     np.testing.assert_array_equal(pad["state"][2], I["state"][2])
     np.testing.assert_array_equal(pad["conv_state"][2], I["conv_state"][2])
+
+
+# ----------------------------------------------------------- slot maintenance
+
+def test_state_copy_hand_example():
+    """Snapshot / restore / reset on a hand-written pool: the expected pools are spelled out
+    element by element (hyperflare core-design, "State operations")."""
+    src = np.array([[[10., 11.]], [[20., 21.]], [[30., 31.]]])          # 3 slots of [1, 2]
+    srcc = np.array([[[1, 2, 3]], [[4, 5, 6]], [[7, 8, 9]]], np.int16)  # 3 histories of [1, 3]
+    dst = np.full((3, 1, 2), -1.0)
+    dstc = np.full((3, 1, 3), -1, np.int16)
+    # slot 2 -> 0 (copy), reset 1, inactive lane, out-of-range source (flagged, skipped)
+    s, c, err = oracle.state_copy(src, srcc, dst, dstc, [2, -1, 0, 7], [0, 1, -1, 2])
+    assert s.tolist() == [[[30., 31.]], [[0., 0.]], [[-1., -1.]]]
+    assert c.tolist() == [[[7, 8, 9]], [[0, 0, 0]], [[-1, -1, -1]]]
+    assert err
+    assert dst.tolist() == [[[-1., -1.]]] * 3                         # inputs untouched
+    # in one pool: snapshot then restore gives back the original slot bit for bit
+    pool = np.array([[[1.5, -2.25]], [[0., 0.]]])
+    snap, _, e1 = oracle.state_copy(pool, None, pool, None, [0], [1])
+    assert snap.tolist() == [[[1.5, -2.25]], [[1.5, -2.25]]] and not e1
+    live = snap.copy(); live[0] = 99.0
+    back, _, e2 = oracle.state_copy(live, None, live, None, [1], [0])
+    assert back[0].tolist() == [[1.5, -2.25]] and not e2
+    # without a source pool every active pair resets; a destination index past the pool is flagged
+    z, _, e3 = oracle.state_copy(None, None, pool, None, [5, -3], [0, 4])
+    assert z.tolist() == [[[0., 0.]], [[0., 0.]]] and e3
