@@ -337,6 +337,11 @@ def run_ours(args, rank, ws, local):
     if args.decode_steps > 0:
         snap = bench_state_copy(args, dev, gdn, pk, pk_src)
 
+    # ---- multi-token verification round (8 tokens per sequence) through gdn_mixer_verify
+    ver = None
+    if args.decode_steps > 0:
+        ver = bench_verify(args, dev, gdn, pk, pk_src)
+
     # ---- end to end through the public fused call with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -360,7 +365,7 @@ def run_ours(args, rank, ws, local):
                            "activations": wl.act, "y_dtype": "bf16"},
                 "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk.summary(), "decode": dec, "state_copy": snap}
+                "clocks": clk.summary(), "decode": dec, "state_copy": snap, "verify": ver}
         print(json.dumps(line), flush=True)
 
 
@@ -452,6 +457,59 @@ def bench_state_copy(args, dev, gdn, pk, pk_src):
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
                          "traffic": None, "peak_source": pk_src + " copy"},
             "gpu_launches": reps}
+
+
+def bench_verify(args, dev, gdn, pk, pk_src, k=8):
+    """One verification round of k tokens for the decode workload's 64 sequences through
+    gdn_mixer_verify: each head state read once and written k times (one checkpoint column per
+    token); L2 evicted before each launch."""
+    wl = WORKLOADS["decode_64x256"]
+    N = wl.n_decode
+    slots = N + N * k
+    cfg = gdn.make_config(wl.HK, wl.HV, wl.dk, wl.dv, wl.chunk, wl.act, n_slots=slots)
+    g = torch.Generator(device=dev).manual_seed(7)
+    rn = lambda *s: torch.randn(*s, generator=g, device=dev)
+    state = torch.zeros((slots, wl.HV, wl.dk, wl.dv), device=dev)
+    state[:N] = rn(N, wl.HV, wl.dk, wl.dv) * 0.02
+    conv = torch.zeros((slots, wl.CH, 3), dtype=wl.torch_act, device=dev)
+    conv[:N] = rn(N, wl.CH, 3).to(wl.torch_act)
+    x = rn(N * k, wl.CH).to(wl.torch_act); z = rn(N * k, wl.HV * wl.dv).to(wl.torch_act)
+    u = rn(N * k, wl.HV).to(wl.torch_act); b = rn(N * k, wl.HV).to(wl.torch_act)
+    cw = (rn(wl.CH, 4) * 0.25).to(wl.torch_act)
+    A = torch.rand(wl.HV, generator=g, device=dev) * 2 - 1
+    dt = torch.zeros(wl.HV, device=dev); nw = torch.ones(wl.dv, device=dev)
+    y = torch.empty((N * k, wl.HV * wl.dv), dtype=torch.bfloat16, device=dev)
+    src = torch.arange(N, dtype=torch.int32, device=dev)
+    ckpt = N + k * src
+    ws = torch.empty(gdn.gdn_workspace_size(cfg, N * k, N), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+    flush.fill_(1.0)
+    sink = torch.empty((), device=dev)
+    stream = torch.cuda.current_stream()
+    reps = max(5, min(args.decode_steps, 20))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps + 3)]
+    for i in range(reps + 3):           # 3 untimed warm-ups
+        torch.sum(flush, 0, out=sink)
+        evs[i][0].record(stream)
+        gdn.gdn_mixer_verify(cfg, x, z, u, b, cw, A, dt, nw, y, state, conv, ckpt, k, ws,
+                             state_idx=src)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_error() == 0
+    per = sum(a.elapsed_time(b) for a, b in evs[3:]) / reps / 1e3
+    moved = (1 + k) * N * wl.HV * wl.dk * wl.dv * 4
+    gbs = moved / per / 1e9
+    return {"workload": "verification round: 64 sequences x %d tokens, HK=16, HV=32, dk=dv=128, "
+                        "bf16 inputs; each 64 KiB head state read once and written to %d "
+                        "checkpoint columns; L2 evicted before each launch" % (k, k),
+            "value": gbs, "unit": "GB/s", "us_per_round": per * 1e6,
+            "tokens_per_s": N * k / per, "state_bytes_per_round": moved,
+            "roofline": {"kernel": "verify_prep_kernel + verify_kernel", "bound": "hbm",
+                         "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "peak_source": pk_src + " copy"},
+            "gpu_launches": 2 * reps}
 
 
 def bench_e2e(args, dev, gdn, cfg, wl, inp, d, N, T):

@@ -159,8 +159,10 @@ size_t gdn_workspace_size(const gdn_config *cfg, int64_t max_tokens, int32_t max
     gdn::Dims d;
     if (check_cfg(cfg, &d) != GDN_OK || max_tokens < 0 || max_seqs < 0) return 0;
     const size_t pre = prefill_ws_bytes(d, cfg->act == GDN_BF16, max_tokens, max_seqs),
-                 dec = gdn::decode_ws_bytes(d, max_seqs);
-    return (pre > dec ? pre : dec) + 256;
+                 dec = gdn::decode_ws_bytes(d, max_seqs),
+                 ver = gdn::verify_ws_bytes(d, max_tokens);
+    const size_t m = pre > dec ? pre : dec;
+    return (m > ver ? m : ver) + 256;
 }
 
 gdn_status gdn_gate_prep(const gdn_config *cfg, const void *u, const void *b_logit, int64_t ld_ub,
@@ -433,6 +435,36 @@ gdn_status gdn_state_copy(const gdn_config *cfg, const float *src_state, const v
     return launch_status(gdn::launch_state_copy(d, cfg->act == GDN_BF16, src_state, src_conv,
                                                 n_src_slots, dst_state, dst_conv, n_dst_slots,
                                                 src_idx, dst_idx, n, err, (cudaStream_t)stream));
+}
+
+gdn_status gdn_mixer_verify(const gdn_config *cfg, const gdn_mixer_io *io, int32_t k,
+                            const int32_t *ckpt_idx, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (!io || k < 1 || k > gdn::kMaxVerify || io->n_seqs < 0) return GDN_ERR_INVALID_ARG;
+    if (io->T != (int64_t)io->n_seqs * k) return GDN_ERR_INVALID_ARG;
+    // the token-level checks of the one-token decode, applied to the n*k rows
+    gdn_mixer_io one = *io;
+    one.T = one.n_seqs = (int32_t)((int64_t)io->n_seqs * k > kMaxSeqs ? kMaxSeqs + 1 : io->n_seqs * k);
+    if ((st = check_mixer_io(d, &one, true)) != GDN_OK) return st;
+    if (io->n_seqs == 0) return GDN_OK;
+    if (!ckpt_idx) return GDN_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < gdn::verify_ws_bytes(d, io->T))
+        return GDN_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    gdn::DecodeArgs a = {};
+    a.x = io->x; a.ld_x = io->ld_x; a.conv_w = io->conv_w; a.conv_state = io->conv_state;
+    a.u = io->u; a.b_logit = io->b_logit; a.ld_ub = io->ld_ub; a.A_log = io->A_log;
+    a.dt_bias = io->dt_bias; a.z = io->z; a.ld_z = io->ld_z; a.norm_w = io->norm_w;
+    a.n = io->n_seqs; a.state = io->state_out; a.state_idx = io->state_idx; a.out = io->y;
+    a.ws = (float *)workspace;
+    a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
+    a.k_tokens = k; a.ckpt_idx = ckpt_idx;
+    return launch_status(gdn::launch_verify(a, cfg->act == GDN_BF16, io->y_dtype == GDN_BF16,
+                                            (cudaStream_t)stream));
 }
 
 gdn_status gdn_device_error(void *stream, uint32_t *code) {

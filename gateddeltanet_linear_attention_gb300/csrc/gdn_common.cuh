@@ -119,6 +119,10 @@ struct DecodeArgs {
     unsigned flags;
     Dims d;
     unsigned *err;
+    // multi-token verification (gdn_mixer_verify): k tokens per sequence; the state and conv
+    // history after token j go to slot ckpt_idx[n] + j
+    int k_tokens;
+    const int32_t *ckpt_idx;
 };
 
 // Per-(sequence, q/k head) record the fused decode's prep kernel writes and its
@@ -133,6 +137,10 @@ struct DecRec {
     }
 };
 size_t decode_ws_bytes(const Dims &d, long long n_seqs);
+// gdn_mixer_verify: a record per (sequence, q/k head, token); ws_bytes for n_seqs * k tokens
+constexpr int kMaxVerify = 8;
+size_t verify_ws_bytes(const Dims &d, long long tokens);
+cudaError_t launch_verify(const DecodeArgs &a, bool in_bf16, bool out_bf16, cudaStream_t s);
 
 cudaError_t launch_gate_prep(const Dims &d, bool act_bf16, const void *u, const void *b,
                              long long ld_ub, long long T, const float *A_log,

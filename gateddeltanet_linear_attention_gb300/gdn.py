@@ -89,6 +89,7 @@ def load(path: str | None = None):
             "gdn_mixer_decode": ([CP, ctypes.POINTER(MixerIO), P, SZ, V], I32),
             "gdn_mixer_prefill_static": ([CP, ctypes.POINTER(MixerIO), V], I32),
             "gdn_state_copy": ([CP, P, P, I32, P, P, I32, P, P, I32, V], I32),
+            "gdn_mixer_verify": ([CP, ctypes.POINTER(MixerIO), I32, P, P, SZ, V], I32),
             "gdn_device_error": ([V, ctypes.POINTER(U32)], I32),
             "gdn_status_string": ([I32], ctypes.c_char_p),
         }
@@ -226,6 +227,21 @@ def gdn_mixer_decode(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, s
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().gdn_mixer_decode(ctypes.byref(cfg), ctypes.byref(io), _ptr(workspace), ws_bytes,
                                    _stream(stream)), "gdn_mixer_decode")
+
+
+def gdn_mixer_verify(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, state,
+                     conv_state, ckpt_idx, k, workspace, state_idx=None, stream=None):
+    """k tokens per sequence (rows n*k .. n*k+k-1 of x, z, u, b_logit, y); the state and conv
+    history after token j go to slot ckpt_idx[n] + j of the same pools."""
+    n = x.shape[0] // k
+    if n * k != x.shape[0]:
+        raise ValueError("x holds %d rows, not a multiple of k=%d" % (x.shape[0], k))
+    io = _mixer_io(x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, None, state, state,
+                   conv_state, state_idx, y, x.shape[0])
+    io.n_seqs = n
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_mixer_verify(ctypes.byref(cfg), ctypes.byref(io), k, _ptr(ckpt_idx),
+                                   _ptr(workspace), ws_bytes, _stream(stream)), "gdn_mixer_verify")
 
 
 def gdn_state_copy(cfg, src_state, src_conv, dst_state, dst_conv, src_idx, dst_idx, stream=None):

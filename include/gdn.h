@@ -221,6 +221,32 @@ gdn_status gdn_mixer_prefill_static(const gdn_config *cfg, const gdn_mixer_io *i
 gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* Multi-token verification decode (hyperflare core-design, speculative
+ * target state: each request reserves eight recurrent checkpoint columns, a
+ * verification round writes the columns of its inputs, and the round after
+ * continues from the column of the last accepted input, whose three-token
+ * conv window goes with it).  k (1..8) tokens for each of io->n_seqs
+ * sequences, packed sequence-major: rows n*k .. n*k+k-1 of io->x, io->z,
+ * io->u, io->b_logit and io->y (io->T == n_seqs * k; cu_seqlens unused).
+ * Sequence n starts from the state and conv history of slot
+ * io->state_idx[n] (NULL: slot n), which are read and not modified; the
+ * one-token rule of gdn_mixer_decode is applied to its k tokens in order,
+ * y row n*k+j is token j's output, and the state and conv history after
+ * token j are written to slot ckpt_idx[n] + j (ckpt_idx: int32 [n_seqs],
+ * DEVICE).  io->state_out must equal io->state_in (one pool, non-NULL) and
+ * io->conv_state must be non-NULL.  To commit `a` accepted tokens, continue
+ * from slot ckpt_idx[n] + a - 1 (as the next call's state_idx, or copy it to
+ * a live slot with gdn_state_copy).  The columns of different sequences must
+ * not overlap one another or another sequence's source slot; a sequence's
+ * own source slot may be its column 0 (it is read before it is written).
+ * A negative state_idx[n] is a padding lane (zero outputs, nothing written);
+ * columns reaching past n_slots are reported as GDN_DEVERR_SLOT and that
+ * sequence is skipped.  Workspace: DEVICE, 16-byte aligned, at least
+ * gdn_workspace_size(cfg, n_seqs * k, n_seqs) bytes. */
+gdn_status gdn_mixer_verify(const gdn_config *cfg, const gdn_mixer_io *io, int32_t k,
+                            const int32_t *ckpt_idx, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
 /* State maintenance: snapshot, restore, initialise and reset of state slots
  * as one indirect copy driven by device-resident slot-index buffers
  * (hyperflare core-design: the "State operations" row of the native model

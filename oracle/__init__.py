@@ -205,3 +205,36 @@ def state_copy(src_state, src_conv, dst_state, dst_conv, src_idx, dst_idx):
             else:
                 dst[t] = 0
     return out_s, out_c, err
+
+
+def mixer_verify(x, conv_w, u, b_logit, A_log, dt_bias, z, norm_w, k, HK, HV, dk, dv, state,
+                 conv_state, src_idx=None, q_scale=1.0, l2_eps=1e-6, norm_eps=1e-6, n_threads=None):
+    """Multi-token verification (hyperflare core-design, speculative target state: a round
+    writes one recurrent checkpoint column per verification input).  Sequence n holds rows
+    n*k .. n*k+k-1; it starts from slot src_idx[n] (default n) of state / conv_state, and the
+    checkpoint column j is the state and conv history after its first j+1 tokens.
+
+    Computed as the plain mixer over the k prefixes of each sequence (lengths 1..k, each from
+    its own copy of the source slot).  Returns y [n*k, HV*dv], states [n, k, HV, dk, dv] and
+    convs [n, k, CH, 3]."""
+    x = _f64(x); T, CH = x.shape
+    n = T // k
+    assert n * k == T
+    st0 = _f64(state); cs0 = _f64(conv_state)
+    src = list(range(n)) if src_idx is None else [int(s) for s in np.asarray(src_idx)]
+    y = np.zeros((T, HV * dv))
+    states = np.zeros((n, k, HV, dk, dv))
+    convs = np.zeros((n, k, CH, 3))
+    for i in range(n):
+        rows = np.concatenate([np.arange(i * k, i * k + j + 1) for j in range(k)])
+        cu = np.concatenate([[0], np.cumsum(np.arange(1, k + 1))]).astype(np.int32)
+        out = mixer(x[rows], conv_w, _f64(u)[rows], _f64(b_logit)[rows], A_log, dt_bias,
+                    _f64(z)[rows], norm_w, cu, HK, HV, dk, dv,
+                    state=np.repeat(st0[src[i]][None], k, axis=0),
+                    conv_state=np.repeat(cs0[src[i]][None], k, axis=0),
+                    q_scale=q_scale, l2_eps=l2_eps, norm_eps=norm_eps, n_threads=n_threads)
+        for j in range(k):
+            y[i * k + j] = out["y"][cu[j + 1] - 1]
+        states[i] = out["state"]
+        convs[i] = out["conv_state"]
+    return y, states, convs

@@ -182,3 +182,30 @@ def test_state_copy_validation(lib):
     # an invalid configuration is refused first
     bad = cfg(dk=96, dv=96)
     assert lib.gdn_state_copy(ctypes.byref(bad), A16, A16, 4, A16b, A16b, 4, A16, A16, 1, None) == UNSUPPORTED
+
+
+def test_mixer_verify_validation(lib):
+    c = cfg()
+    ch = ctypes.byref(c)
+    k, n = 4, 3
+    good = dict(state_in=A16b, state_out=A16b, conv_state=A16)
+    need = lib.gdn_workspace_size(ch, n * k, n)
+    io = _io(T=n * k, n=n, **good)
+    assert need >= n * k * 16 * (2 * 128 + 4 * 128 + 4 + 1) * 4       # a record per (unit, token)
+    for kk in (0, 9, -1):                                               # 1 <= k <= 8
+        assert lib.gdn_mixer_verify(ch, ctypes.byref(io), kk, A16, A16, need, None) == INVALID
+    bad = _io(T=n * k + 1, n=n, **good)                                 # T != n * k
+    assert lib.gdn_mixer_verify(ch, ctypes.byref(bad), k, A16, A16, need, None) == INVALID
+    assert lib.gdn_mixer_verify(ch, ctypes.byref(io), k, None, A16, need, None) == INVALID
+    bad = _io(T=n * k, n=n, state_in=A16b, state_out=A16, conv_state=A16)   # two pools
+    assert lib.gdn_mixer_verify(ch, ctypes.byref(bad), k, A16, A16, need, None) == INVALID
+    bad = _io(T=n * k, n=n, state_in=A16b, state_out=A16b, conv_state=None)  # no histories
+    assert lib.gdn_mixer_verify(ch, ctypes.byref(bad), k, A16, A16, need, None) == INVALID
+    bad = _io(T=n * k, n=n, ld_x=8000, **good)                          # narrower than CH
+    assert lib.gdn_mixer_verify(ch, ctypes.byref(bad), k, A16, A16, need, None) == INVALID
+    small = n * k * 16 * 4                                              # far short of the records
+    assert lib.gdn_mixer_verify(ch, ctypes.byref(io), k, A16, A16, small, None) == WORKSPACE
+    assert lib.gdn_mixer_verify(ch, ctypes.byref(io), k, A16, None, need, None) == WORKSPACE
+    assert lib.gdn_mixer_verify(ch, ctypes.byref(io), k, A16, MIS, need, None) == WORKSPACE
+    empty = _io(T=0, n=0, **good)
+    assert lib.gdn_mixer_verify(ch, ctypes.byref(empty), k, None, None, 0, None) == OK

@@ -379,3 +379,32 @@ def test_state_copy_hand_example():
     # without a source pool every active pair resets; a destination index past the pool is flagged
     z, _, e3 = oracle.state_copy(None, None, pool, None, [5, -3], [0, 4])
     assert z.tolist() == [[[0., 0.]], [[0., 0.]]] and e3
+
+
+def test_mixer_verify_columns_are_prefix_states():
+    """Verification columns (hyperflare core-design, speculative target state): column j is the
+    state after j+1 tokens, so the last column and every y row equal one plain pass over the k
+    tokens, and column j of a k-token round equals the last column of a (j+1)-token round."""
+    HK, HV, d, k = 1, 2, 4, 4
+    CH = 2 * HK * d + HV * d
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((2 * k, CH)); z = rng.standard_normal((2 * k, HV * d))
+    u = rng.standard_normal((2 * k, HV)); b = rng.standard_normal((2 * k, HV))
+    cw = rng.normal(0, 0.25, (CH, 4)); A = rng.uniform(-1, 1, HV); dt = np.zeros(HV); nw = np.ones(d)
+    st = rng.normal(0, 0.02, (3, HV, d, d)); cs = rng.standard_normal((3, CH, 3))
+    y, S, C = oracle.mixer_verify(x, cw, u, b, A, dt, z, nw, k, HK, HV, d, d, st, cs, src_idx=[2, 0],
+                                  n_threads=1)
+    for i, s in enumerate([2, 0]):
+        one = oracle.mixer(x[i * k:(i + 1) * k], cw, u[i * k:(i + 1) * k], b[i * k:(i + 1) * k], A, dt,
+                           z[i * k:(i + 1) * k], nw, np.array([0, k], np.int32), HK, HV, d, d,
+                           state=st[s:s + 1].copy(), conv_state=cs[s:s + 1].copy(), n_threads=1)
+        assert np.allclose(y[i * k:(i + 1) * k], one["y"], rtol=0, atol=1e-12)
+        assert np.allclose(S[i, -1], one["state"][0], rtol=0, atol=1e-12)
+        assert np.array_equal(C[i, -1], one["conv_state"][0])
+        # the conv window after token j holds raw inputs j-2 .. j (history taps before token 0)
+        X = np.concatenate([cs[s].T, x[i * k:(i + 1) * k]])          # [3 + k, CH]
+        for j in range(k):
+            assert np.array_equal(C[i, j], X[j + 1:j + 4].T)
+    y2, S2, _ = oracle.mixer_verify(x[:2], cw, u[:2], b[:2], A, dt, z[:2], nw, 2, HK, HV, d, d, st, cs,
+                                    src_idx=[2], n_threads=1)
+    assert np.allclose(S2[0, 1], S[0, 1], rtol=0, atol=1e-12) and np.allclose(y2, y[:2], rtol=0, atol=1e-12)
