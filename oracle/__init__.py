@@ -238,3 +238,66 @@ def mixer_verify(x, conv_w, u, b_logit, A_log, dt_bias, z, norm_w, k, HK, HV, dk
         states[i] = out["state"]
         convs[i] = out["conv_state"]
     return y, states, convs
+
+
+def delta_rule_backward(xa, g, beta, cu_seqlens, HK, HV, dk, dv, d_o, state=None, slot_idx=None,
+                        d_state=None):
+    """Reverse-mode gradient of the gated delta rule (the token-by-token definition of
+    `delta_rule`), per sequence and v-head, in numpy fp64 (hyperflare core-design, training
+    plan: a backward per region, the GDN core one among them, from retained chunk-boundary
+    states).  With S the dv x dk state (the buffers hold M = S^T) and per token
+    p = S k, S' = a S + beta (v - a p) k^T, o = S' q, a = exp(g), the loss is
+    sum(d_o * o) + sum(d_state * M_final).
+
+    Returns (dxa [T, CH] = (dq | dk | dv) in the layout of xa, with dq and dk summed over the
+    v-heads of each q/k head; dg [T, HV]; dbeta [T, HV]; d_state_in [slots, HV, dk, dv] or None).
+    The state before every token is kept, so this is for small cases only."""
+    xa = _f64(xa); g = _f64(g); beta = _f64(beta); d_o = _f64(d_o)
+    cu = [int(c) for c in np.asarray(cu_seqlens)]
+    T = xa.shape[0]
+    G = HV // HK
+    n_seqs = len(cu) - 1
+    dxa = np.zeros_like(xa)
+    dg = np.zeros((T, HV)); db = np.zeros((T, HV))
+    d_state_in = None if state is None else np.zeros_like(_f64(state))
+    for n in range(n_seqs):
+        slot = n if slot_idx is None else int(np.asarray(slot_idx)[n])
+        if slot < 0:          # a padding lane: its outputs are zero, so are its gradients
+            continue
+        for h in range(HV):
+            kh = h // G
+            qc = slice(kh * dk, (kh + 1) * dk)
+            kc = slice(HK * dk + kh * dk, HK * dk + (kh + 1) * dk)
+            vc = slice(2 * HK * dk + h * dv, 2 * HK * dk + (h + 1) * dv)
+            S = np.zeros((dv, dk)) if state is None else _f64(state)[slot, h].T.copy()
+            prev = []
+            for t in range(cu[n], cu[n + 1]):                       # forward, keeping S_{t-1}
+                a = np.exp(g[t, h]); b = beta[t, h]; k = xa[t, kc]; v = xa[t, vc]
+                prev.append(S.copy())
+                p = S @ k
+                S = a * S + b * np.outer(v - a * p, k)
+            GS = np.zeros((dv, dk))
+            if d_state is not None:
+                GS = _f64(d_state)[slot, h].T.copy()
+            for i, t in reversed(list(enumerate(range(cu[n], cu[n + 1])))):
+                a = np.exp(g[t, h]); b = beta[t, h]
+                q = xa[t, qc]; k = xa[t, kc]; v = xa[t, vc]; do = d_o[t, h * dv:(h + 1) * dv]
+                Sp = prev[i]
+                p = Sp @ k
+                r = v - a * p
+                St = a * Sp + b * np.outer(r, k)
+                GS = GS + np.outer(do, q)                           # o = S_t q
+                dxa[t, qc] += St.T @ do
+                dw = GS @ k                                         # w = b r, S_t = a Sp + w k^T
+                dxa[t, kc] += GS.T @ (b * r)
+                da = np.sum(GS * Sp)
+                dxa[t, vc] += b * dw
+                db[t, h] = dw @ r
+                dp = -a * b * dw                                    # r = v - a p
+                da += -b * (dw @ p)
+                dxa[t, kc] += Sp.T @ dp                             # p = Sp k
+                GS = a * GS + np.outer(dp, k)
+                dg[t, h] = da * a
+            if d_state_in is not None:
+                d_state_in[slot, h] = GS.T
+    return dxa, dg, db, d_state_in

@@ -408,3 +408,57 @@ def test_mixer_verify_columns_are_prefix_states():
     y2, S2, _ = oracle.mixer_verify(x[:2], cw, u[:2], b[:2], A, dt, z[:2], nw, 2, HK, HV, d, d, st, cs,
                                     src_idx=[2], n_threads=1)
     assert np.allclose(S2[0, 1], S[0, 1], rtol=0, atol=1e-12) and np.allclose(y2, y[:2], rtol=0, atol=1e-12)
+
+
+def test_delta_rule_backward_matches_central_differences():
+    """The oracle's reverse-mode gradient against central differences of the (pinned) forward:
+    L = sum(d_o * o) + sum(d_state * M_final), over q, k, v, g, beta and the initial state, with
+    GQA (two v-heads per q/k head), two sequences (one empty-ended, one of several tokens) and a
+    padding-free slot map."""
+    rng = np.random.default_rng(21)
+    HK, HV, d = 1, 2, 3
+    CH = 2 * HK * d + HV * d
+    T, cu, slots = 7, np.array([0, 3, 7], np.int32), [1, 0]
+    xa = rng.standard_normal((T, CH)) * 0.7
+    g = -rng.uniform(0.05, 0.6, (T, HV)); beta = rng.uniform(0.2, 0.9, (T, HV))
+    S0 = rng.standard_normal((2, HV, d, d)) * 0.3
+    d_o = rng.standard_normal((T, HV * d)); d_S = rng.standard_normal((2, HV, d, d))
+
+    def loss(xa_, g_, b_, S0_):
+        o, st = oracle.delta_rule(xa_, g_, b_, cu, HK, HV, d, d, state=S0_.copy(), slot_idx=slots,
+                                  n_threads=1)
+        return float(np.sum(d_o * o) + np.sum(d_S * st))
+
+    dxa, dg, db, dS0 = oracle.delta_rule_backward(xa, g, beta, cu, HK, HV, d, d, d_o, state=S0,
+                                                  slot_idx=slots, d_state=d_S)
+    eps = 1e-6
+    for arr, grad in ((xa, dxa), (g, dg), (beta, db), (S0, dS0)):
+        for idx in [tuple(rng.integers(0, s) for s in arr.shape) for _ in range(12)]:
+            args_p = [a.copy() for a in (xa, g, beta, S0)]
+            args_m = [a.copy() for a in (xa, g, beta, S0)]
+            pos = [a is arr for a in (xa, g, beta, S0)].index(True)
+            args_p[pos][idx] += eps
+            args_m[pos][idx] -= eps
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (pos, idx, fd, grad[idx])
+
+
+def test_delta_rule_backward_padding_lane_has_no_gradient():
+    """A padding lane (negative slot) produces zero outputs and touches no state, so every
+    gradient of its tokens is zero and the other lanes' gradients are those of the batch
+    without it."""
+    rng = np.random.default_rng(8)
+    HK, HV, d = 1, 1, 2
+    xa = rng.standard_normal((5, 2 * HK * d + HV * d))
+    g = -rng.uniform(0.1, 0.5, (5, HV)); beta = rng.uniform(0.2, 0.8, (5, HV))
+    d_o = rng.standard_normal((5, HV * d)); S0 = rng.standard_normal((1, HV, d, d))
+    o, _ = oracle.delta_rule(xa, g, beta, np.array([0, 2, 5], np.int32), HK, HV, d, d, state=S0.copy(),
+                             slot_idx=[-1, 0], n_threads=1)
+    assert np.all(o[:2] == 0)                                    # the forward's padding rule
+    full = oracle.delta_rule_backward(xa, g, beta, [0, 2, 5], HK, HV, d, d, d_o, state=S0, slot_idx=[-1, 0])
+    alone = oracle.delta_rule_backward(xa[2:], g[2:], beta[2:], [0, 3], HK, HV, d, d, d_o[2:], state=S0,
+                                       slot_idx=[0])
+    assert np.all(full[0][:2] == 0) and np.all(full[1][:2] == 0) and np.all(full[2][:2] == 0)
+    for a, b in zip(full[:3], alone[:3]):
+        assert np.array_equal(a[2:], b)
+    assert np.array_equal(full[3], alone[3])
