@@ -342,6 +342,11 @@ def run_ours(args, rank, ws, local):
     if args.decode_steps > 0:
         ver = bench_verify(args, dev, gdn, pk, pk_src)
 
+    # ---- backward of the core rule (training) at the prefill shape
+    bwd = None
+    if args.decode_steps > 0:
+        bwd = bench_backward(args, dev, gdn, pk, pk_src)
+
     # ---- end to end through the public fused call with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -365,7 +370,8 @@ def run_ours(args, rank, ws, local):
                            "activations": wl.act, "y_dtype": "bf16"},
                 "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk.summary(), "decode": dec, "state_copy": snap, "verify": ver}
+                "clocks": clk.summary(), "decode": dec, "state_copy": snap, "verify": ver,
+                "backward": bwd}
         print(json.dumps(line), flush=True)
 
 
@@ -510,6 +516,63 @@ def bench_verify(args, dev, gdn, pk, pk_src, k=8):
                          "frac": gbs / pk["hbm_gbs"], "traffic": None,
                          "peak_source": pk_src + " copy"},
             "gpu_launches": 2 * reps}
+
+
+def bench_backward(args, dev, gdn, pk, pk_src):
+    """The gated delta rule core backward on one 8,192-token sequence at the prefill shape
+    (HV=32, dk=dv=128, chunk 64, nonzero initial state): gdn_chunk_states once (what the
+    training forward retains), then gdn_chunk_backward timed per call with CUDA events."""
+    wl = WORKLOADS["prefill_8k"]
+    T, HK, HV, d, C = 8192, wl.HK, wl.HV, wl.dk, wl.chunk
+    cfg = gdn.make_config(HK, HV, d, d, C, "bf16", n_slots=1)
+    g = torch.Generator(device=dev).manual_seed(11)
+    rn = lambda *s: torch.randn(*s, generator=g, device=dev)
+    unit = lambda x: x / x.norm(dim=-1, keepdim=True)
+    q = unit(rn(T, HK, d)).reshape(T, HK * d).to(torch.bfloat16)
+    k = unit(rn(T, HK, d)).reshape(T, HK * d).to(torch.bfloat16)
+    v = rn(T, HV * d).to(torch.bfloat16)
+    gl = -torch.nn.functional.softplus(rn(T, HV)) * 0.5
+    beta = torch.sigmoid(rn(T, HV))
+    S0 = rn(1, HV, d, d) * 0.02
+    d_o = rn(T, HV * d); dS = rn(1, HV, d, d) * 0.1
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    nb = gdn.chunk_count([T], C)
+    bnd = torch.empty((nb, HV, d, d), device=dev)
+    ws = torch.empty(gdn.gdn_backward_workspace_size(cfg, T, 1), dtype=torch.uint8, device=dev)
+    dq = torch.empty((T, HK * d), device=dev); dk = torch.empty_like(dq)
+    dv = torch.empty((T, HV * d), device=dev); dg = torch.empty((T, HV), device=dev)
+    db = torch.empty_like(dg); dS0 = torch.empty_like(S0)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    gdn.gdn_chunk_states(cfg, k, v, gl, beta, cu, bnd, ws, state_in=S0)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    states_s = e0.elapsed_time(e1) / 1e3
+    reps = 3
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps + 1)]
+    for i in range(reps + 1):           # 1 untimed warm-up
+        evs[i][0].record(stream)
+        gdn.gdn_chunk_backward(cfg, q, k, v, gl, beta, cu, bnd, d_o, dq, dk, dv, dg, db, ws,
+                               d_state_out=dS, d_state_in=dS0)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_error() == 0
+    per = sum(a.elapsed_time(b) for a, b in evs[1:]) / reps / 1e3
+    # bytes the token-level algorithm moves: per token and v-head the state before the token
+    # written to and read back from the chunk scratch, plus the boundary state per chunk
+    moved = T * HV * 2 * d * d * 4 + nb * HV * d * d * 4
+    return {"workload": "prefill_8k shape: one 8,192-token sequence, HK=16, HV=32, dk=dv=128, "
+                        "chunk 64, bf16 q/k/v, nonzero initial state, d_o and d_state_out given",
+            "tokens_per_s": T / per, "ms_per_call": per * 1e3, "states_ms": states_s * 1e3,
+            "roofline": {"kernel": "bwd_kernel (+ group sum)", "bound": "latency",
+                         "bytes_per_call": moved, "achieved": moved / per / 1e9, "unit": "GB/s",
+                         "peak": pk["hbm_gbs"], "frac": moved / per / 1e9 / pk["hbm_gbs"],
+                         "peak_source": pk_src + " copy",
+                         "note": "32 CTAs (one per v-head) walk 8,192 tokens in sequence; the "
+                                 "per-token states stay in L2 (4 MiB per CTA)"},
+            "gpu_launches": 3 * reps}
 
 
 def bench_e2e(args, dev, gdn, cfg, wl, inp, d, N, T):

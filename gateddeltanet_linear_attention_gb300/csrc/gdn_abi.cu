@@ -467,6 +467,88 @@ gdn_status gdn_mixer_verify(const gdn_config *cfg, const gdn_mixer_io *io, int32
                                             (cudaStream_t)stream));
 }
 
+size_t gdn_backward_workspace_size(const gdn_config *cfg, int64_t max_tokens, int32_t max_seqs) {
+    gdn::Dims d;
+    if (check_cfg(cfg, &d) != GDN_OK || max_tokens < 0 || max_seqs < 0) return 0;
+    return gdn::bwd_ws_bytes(d, max_tokens, max_seqs, false) + 256;
+}
+
+// Arguments both backward entry points share: k, v, gates and the batch.
+static gdn_status check_bwd_common(const gdn::Dims &d, const void *k, int64_t ld_qk, const void *v,
+                                   int64_t ld_v, gdn_dtype in_dtype, const float *g,
+                                   const float *beta, const int32_t *cu_seqlens, int32_t n_seqs,
+                                   int64_t T) {
+    if (n_seqs < 0 || T < 0 || !valid_dtype(in_dtype)) return GDN_ERR_INVALID_ARG;
+    if (n_seqs > kMaxSeqs) return GDN_ERR_UNSUPPORTED;
+    if (T == 0) return GDN_OK;
+    if (n_seqs == 0 || !cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (!valid_view(k, ld_qk, (long long)d.hk * d.dk) || !valid_view(v, ld_v, (long long)d.hv * d.dv) ||
+        !g || !aligned16(g) || !beta || !aligned16(beta))
+        return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_states(const gdn_config *cfg, const void *k, int64_t ld_qk, const void *v,
+                            int64_t ld_v, gdn_dtype in_dtype, const float *g, const float *beta,
+                            const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
+                            const float *state_in, const int32_t *state_idx, float *boundary_states,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if ((st = check_bwd_common(d, k, ld_qk, v, ld_v, in_dtype, g, beta, cu_seqlens, n_seqs, T)) != GDN_OK)
+        return st;
+    if (T == 0) return GDN_OK;
+    if (!boundary_states || !aligned16(boundary_states) || (state_in && !aligned16(state_in)))
+        return GDN_ERR_INVALID_ARG;
+    if (state_in && d.n_slots == 0) return GDN_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < gdn::bwd_ws_bytes(d, T, n_seqs, true))
+        return GDN_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    gdn::BwdArgs a = {};
+    a.k = k; a.v = v; a.ld_qk = ld_qk; a.ld_v = ld_v; a.g = g; a.beta = beta;
+    a.cu_seqlens = cu_seqlens; a.n_seqs = n_seqs; a.T = T; a.state_in = state_in;
+    a.state_idx = state_idx; a.bnd = boundary_states; a.d = d; a.err = err;
+    gdn::bwd_carve(a, workspace, true);
+    return launch_status(gdn::launch_backward(a, in_dtype == GDN_BF16, true, (cudaStream_t)stream));
+}
+
+gdn_status gdn_chunk_backward(const gdn_config *cfg, const void *q, const void *k, int64_t ld_qk,
+                              const void *v, int64_t ld_v, gdn_dtype in_dtype, const float *g,
+                              const float *beta, const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
+                              const int32_t *state_idx, const float *boundary_states,
+                              const float *d_o, const float *d_state_out, float *dq, float *dk,
+                              int64_t ld_dqk, float *dv, float *dg, float *dbeta, float *d_state_in,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if ((st = check_bwd_common(d, k, ld_qk, v, ld_v, in_dtype, g, beta, cu_seqlens, n_seqs, T)) != GDN_OK)
+        return st;
+    if ((d_state_out && !aligned16(d_state_out)) || (d_state_in && !aligned16(d_state_in)))
+        return GDN_ERR_INVALID_ARG;
+    if ((d_state_out || d_state_in) && d.n_slots == 0) return GDN_ERR_INVALID_ARG;
+    if (T == 0) return GDN_OK;
+    if (!valid_view(q, ld_qk, (long long)d.hk * d.dk) || !boundary_states || !aligned16(boundary_states) ||
+        !d_o || !aligned16(d_o) || !dq || !dk || !aligned16(dq) || !aligned16(dk) ||
+        ld_dqk < (long long)d.hk * d.dk || !dv || !aligned16(dv) || !dg || !aligned16(dg) || !dbeta ||
+        !aligned16(dbeta))
+        return GDN_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < gdn::bwd_ws_bytes(d, T, n_seqs, false))
+        return GDN_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    gdn::BwdArgs a = {};
+    a.q = q; a.k = k; a.v = v; a.ld_qk = ld_qk; a.ld_v = ld_v; a.g = g; a.beta = beta;
+    a.cu_seqlens = cu_seqlens; a.n_seqs = n_seqs; a.T = T; a.state_idx = state_idx;
+    a.bnd = const_cast<float *>(boundary_states); a.d_o = d_o; a.d_state_out = d_state_out;
+    a.dq = dq; a.dk = dk; a.ld_dqk = ld_dqk; a.dv = dv; a.dg = dg; a.dbeta = dbeta;
+    a.d_state_in = d_state_in; a.d = d; a.err = err;
+    gdn::bwd_carve(a, workspace, false);
+    return launch_status(gdn::launch_backward(a, in_dtype == GDN_BF16, false, (cudaStream_t)stream));
+}
+
 gdn_status gdn_device_error(void *stream, uint32_t *code) {
     if (!code) return GDN_ERR_INVALID_ARG;
     *code = 0;

@@ -1,0 +1,388 @@
+// gdn_backward.cu -- backward of the gated delta rule core from retained
+// chunk-boundary states (hyperflare core-design, the training plan: a
+// training step retains activations and GDN chunk-boundary states, and the
+// backward has one entry per region, the GDN core among them).
+//
+// With the state held as M = S^T (dk x dv), per token of one v-head
+// (a = exp(g)):
+//   forward   p = M^T k,  w = beta (v - a p),  M' = a M + k w^T,  o = M'^T q
+//   backward, GM = dL/dM' (carried from the later tokens):
+//     GM += q do^T;            dq = M' do
+//     dw = GM^T k;             dk = GM w + M dp
+//     dv = beta dw;            dbeta = dw . (v - a p)
+//     dp = -a beta dw;         da = <GM, M> - beta dw . p;   dg = a da
+//     GM <- a GM + k dp^T      (= dL/dM of the state before the token)
+// Two launches and a reduction:
+//  - bwd_states_kernel (gdn_chunk_states): one CTA per (sequence, v-head), the
+//    forward over the sequence with M in registers (thread: one float4 column
+//    group over RPT rows, a warp per 512-byte row), writing M at every chunk
+//    start: the states a training forward retains;
+//  - bwd_kernel (gdn_chunk_backward): one CTA per (sequence, v-head), the chunks
+//    in reverse: the forward of the chunk from its boundary state, keeping the
+//    state before every token in the workspace, then the tokens in reverse with
+//    GM in registers.  Column sums go through one shared-memory pass, row sums
+//    through shuffles among the lanes that hold the row.  dq and dk come out per
+//    v-head and bwd_group_sum_kernel adds the v-heads of each q/k head.
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+namespace {
+
+template <int DK, int DV>
+struct BwdCfg {
+    static constexpr int NT = 4 * DV, LPR = DV / 4, RPP = NT / LPR, RPT = DK / RPP;
+};
+
+// chunk_base[n] = sum over m < n of ceil(len_m / C): the index of sequence n's first
+// boundary state.  One thread: the batch sizes here are small.
+__global__ void bwd_map_kernel(const int32_t *cu, int n_seqs, long long T, int C, int *base,
+                               unsigned *err) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int acc = 0;
+    for (int n = 0; n < n_seqs; ++n) {
+        long long s, e;
+        seq_bounds(cu, n, T, err, s, e);
+        base[n] = acc;
+        acc += (int)((e - s + C - 1) / C);
+    }
+    base[n_seqs] = acc;
+}
+
+// Sum over the L lanes that hold one state row (L divides 32; rows are lane-aligned).
+template <int L>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+    for (int o = L / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Per-token inputs of one v-head staged in shared memory.
+// Every array read or written as float4 (dout, w, dp, red) is 16-byte aligned explicitly.
+template <int DK, int DV>
+struct TokSmem {
+    alignas(16) float q[DK];
+    alignas(16) float k[DK];
+    alignas(16) float v[DV];
+    alignas(16) float dout[DV];
+    alignas(16) float p[DV];
+    alignas(16) float r[DV];
+    alignas(16) float w[DV];
+    alignas(16) float dp[DV];
+    alignas(16) float red[BwdCfg<DK, DV>::RPP][DV];
+    float wsum[3][BwdCfg<DK, DV>::NT / 32];
+    float a, b;
+};
+
+// The forward step of one token on M in registers: p = M^T k (column sums), w, M <- a M + k w^T.
+template <int DK, int DV>
+__device__ __forceinline__ void fwd_token(float4 (&m)[BwdCfg<DK, DV>::RPT], TokSmem<DK, DV> &sm,
+                                          int tid, int rg, int c4) {
+    using C = BwdCfg<DK, DV>;
+    float4 pp = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int x = 0; x < C::RPT; ++x) {
+        const float kr = sm.k[rg + x * C::RPP];
+        pp.x += m[x].x * kr; pp.y += m[x].y * kr; pp.z += m[x].z * kr; pp.w += m[x].w * kr;
+    }
+    *reinterpret_cast<float4 *>(&sm.red[rg][c4]) = pp;
+    __syncthreads();
+    if (tid < DV) {
+        float p = 0.f;
+#pragma unroll
+        for (int r = 0; r < C::RPP; ++r) p += sm.red[r][tid];
+        sm.w[tid] = sm.b * (sm.v[tid] - sm.a * p);
+    }
+    __syncthreads();
+    const float4 w4 = *reinterpret_cast<const float4 *>(&sm.w[c4]);
+    const float a = sm.a;
+#pragma unroll
+    for (int x = 0; x < C::RPT; ++x) {
+        const float kr = sm.k[rg + x * C::RPP];
+        m[x].x = a * m[x].x + kr * w4.x; m[x].y = a * m[x].y + kr * w4.y;
+        m[x].z = a * m[x].z + kr * w4.z; m[x].w = a * m[x].w + kr * w4.w;
+    }
+}
+
+// Stage token t's q (optional), k, v, do (optional), a, beta of head h into shared memory.
+template <int DK, int DV, typename TA>
+__device__ __forceinline__ void stage_token(const BwdArgs &a, TokSmem<DK, DV> &sm, long long t,
+                                            int h, int kh, int tid, bool with_q) {
+    if (tid < DK) {
+        sm.k[tid] = to_f32(((const TA *)a.k)[t * a.ld_qk + (long long)kh * DK + tid]);
+        if (with_q) sm.q[tid] = to_f32(((const TA *)a.q)[t * a.ld_qk + (long long)kh * DK + tid]);
+    }
+    if (tid < DV) {
+        sm.v[tid] = to_f32(((const TA *)a.v)[t * a.ld_v + (long long)h * DV + tid]);
+        if (with_q) sm.dout[tid] = a.d_o[t * (long long)a.d.hv * DV + (long long)h * DV + tid];
+    }
+    if (tid == 0) {
+        sm.a = expf(a.g[t * a.d.hv + h]);
+        sm.b = a.beta[t * a.d.hv + h];
+    }
+}
+
+template <int DK, int DV, typename TA>
+__global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
+    using C = BwdCfg<DK, DV>;
+    __shared__ __align__(16) TokSmem<DK, DV> sm;
+    const Dims &d = a.d;
+    const int tid = threadIdx.x, h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
+    const int rg = tid / C::LPR, c4 = (tid % C::LPR) * 4;
+    long long s, e;
+    seq_bounds(a.cu_seqlens, n, a.T, a.err, s, e);
+    const int slot = slot_of(a.state_idx, n, d.n_slots, a.err);
+    if (slot < 0 || s >= e) return;                      // padding lane / empty: no chunks
+    const int Cc = d.chunk;
+    float4 m[C::RPT];
+#pragma unroll
+    for (int x = 0; x < C::RPT; ++x) {
+        m[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.state_in)
+            m[x] = *reinterpret_cast<const float4 *>(a.state_in + ((long long)slot * d.hv + h) * DK * DV +
+                                                     (long long)(rg + x * C::RPP) * DV + c4);
+    }
+    const long long b0 = a.chunk_base[n];
+    for (long long t = s; t < e; ++t) {
+        if ((t - s) % Cc == 0) {
+            float *B = a.bnd + ((b0 + (t - s) / Cc) * d.hv + h) * DK * DV;
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x)
+                *reinterpret_cast<float4 *>(B + (long long)(rg + x * C::RPP) * DV + c4) = m[x];
+        }
+        __syncthreads();                                 // the previous token's smem reads are done
+        stage_token<DK, DV, TA>(a, sm, t, h, kh, tid, false);
+        __syncthreads();
+        fwd_token<DK, DV>(m, sm, tid, rg, c4);
+    }
+}
+
+template <int DK, int DV, typename TA>
+__global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
+    using C = BwdCfg<DK, DV>;
+    constexpr int NW = C::NT / 32;
+    __shared__ __align__(16) TokSmem<DK, DV> sm;
+    const Dims &d = a.d;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
+    const int rg = tid / C::LPR, c4 = (tid % C::LPR) * 4;
+    long long s, e;
+    seq_bounds(a.cu_seqlens, n, a.T, a.err, s, e);
+    const int slot = slot_of(a.state_idx, n, d.n_slots, a.err);
+    const long long HVDV = (long long)d.hv * DV;
+    if (slot < 0) {                                      // padding lane: zero gradients
+        for (long long t = s; t < e; ++t) {
+            for (int i = tid; i < DK; i += C::NT) {
+                a.pq[(t * d.hv + h) * DK + i] = 0.f;
+                a.pk[(t * d.hv + h) * DK + i] = 0.f;
+            }
+            for (int j = tid; j < DV; j += C::NT) a.dv[t * HVDV + (long long)h * DV + j] = 0.f;
+            if (tid == 0) { a.dg[t * d.hv + h] = 0.f; a.dbeta[t * d.hv + h] = 0.f; }
+        }
+        return;
+    }
+    const int Cc = d.chunk;
+    float4 gm[C::RPT];
+#pragma unroll
+    for (int x = 0; x < C::RPT; ++x) {
+        gm[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.d_state_out)
+            gm[x] = *reinterpret_cast<const float4 *>(a.d_state_out + ((long long)slot * d.hv + h) * DK * DV +
+                                                      (long long)(rg + x * C::RPP) * DV + c4);
+    }
+    // this CTA's scratch: the state before each token of one chunk
+    float *scr = a.scratch + ((long long)n * d.hv + h) * (long long)Cc * DK * DV;
+    const long long b0 = a.chunk_base[n];
+    const long long nch = (e - s + Cc - 1) / Cc;
+    for (long long c = nch - 1; c >= 0; --c) {
+        const long long t0 = s + c * Cc, t1 = (t0 + Cc < e) ? t0 + Cc : e;
+        float4 m[C::RPT];
+        {
+            const float *B = a.bnd + ((b0 + c) * d.hv + h) * DK * DV;
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x)
+                m[x] = *reinterpret_cast<const float4 *>(B + (long long)(rg + x * C::RPP) * DV + c4);
+        }
+        // forward through the chunk, keeping the state before every token (each thread
+        // reads back only what it wrote)
+        for (long long t = t0; t < t1; ++t) {
+            float *Sc = scr + (t - t0) * DK * DV;
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x)
+                *reinterpret_cast<float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4) = m[x];
+            if (t + 1 == t1) break;
+            __syncthreads();
+            stage_token<DK, DV, TA>(a, sm, t, h, kh, tid, false);
+            __syncthreads();
+            fwd_token<DK, DV>(m, sm, tid, rg, c4);
+        }
+        // the tokens in reverse
+        for (long long t = t1 - 1; t >= t0; --t) {
+            const float *Sc = scr + (t - t0) * DK * DV;
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x)
+                m[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4);
+            __syncthreads();                             // (E) the previous token's smem reads are done
+            stage_token<DK, DV, TA>(a, sm, t, h, kh, tid, true);
+            __syncthreads();
+            // p = M^T k
+            {
+                float4 pp = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int x = 0; x < C::RPT; ++x) {
+                    const float kr = sm.k[rg + x * C::RPP];
+                    pp.x += m[x].x * kr; pp.y += m[x].y * kr; pp.z += m[x].z * kr; pp.w += m[x].w * kr;
+                }
+                *reinterpret_cast<float4 *>(&sm.red[rg][c4]) = pp;
+            }
+            __syncthreads();                             // (A)
+            const float av = sm.a, bv = sm.b;
+            if (tid < DV) {
+                float p = 0.f;
+#pragma unroll
+                for (int r = 0; r < C::RPP; ++r) p += sm.red[r][tid];
+                const float rr = sm.v[tid] - av * p;
+                sm.p[tid] = p;
+                sm.r[tid] = rr;
+                sm.w[tid] = bv * rr;
+            }
+            __syncthreads();                             // (B)
+            const float4 w4 = *reinterpret_cast<const float4 *>(&sm.w[c4]);
+            const float4 do4 = *reinterpret_cast<const float4 *>(&sm.dout[c4]);
+            float4 dwp = make_float4(0.f, 0.f, 0.f, 0.f);
+            float dap = 0.f;
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x) {
+                const int row = rg + x * C::RPP;
+                const float kr = sm.k[row], qr = sm.q[row];
+                float4 mp;                               // M' = a M + k w^T
+                mp.x = av * m[x].x + kr * w4.x; mp.y = av * m[x].y + kr * w4.y;
+                mp.z = av * m[x].z + kr * w4.z; mp.w = av * m[x].w + kr * w4.w;
+                gm[x].x += qr * do4.x; gm[x].y += qr * do4.y; gm[x].z += qr * do4.z; gm[x].w += qr * do4.w;
+                const float dq = row_sum<C::LPR>(mp.x * do4.x + mp.y * do4.y + mp.z * do4.z + mp.w * do4.w);
+                if (lane % C::LPR == 0) a.pq[(t * d.hv + h) * DK + row] = dq;
+                dwp.x += gm[x].x * kr; dwp.y += gm[x].y * kr; dwp.z += gm[x].z * kr; dwp.w += gm[x].w * kr;
+                dap += gm[x].x * m[x].x + gm[x].y * m[x].y + gm[x].z * m[x].z + gm[x].w * m[x].w;
+            }
+            *reinterpret_cast<float4 *>(&sm.red[rg][c4]) = dwp;
+            dap = warp_sum(dap);
+            if (lane == 0) sm.wsum[0][warp] = dap;
+            __syncthreads();                             // (C)
+            if (tid < DV) {
+                float dw = 0.f;
+#pragma unroll
+                for (int r = 0; r < C::RPP; ++r) dw += sm.red[r][tid];
+                a.dv[t * HVDV + (long long)h * DV + tid] = bv * dw;
+                sm.dp[tid] = -av * bv * dw;
+                const float db = warp_sum(dw * sm.r[tid]);
+                const float da2 = warp_sum(dw * sm.p[tid]);
+                if (lane == 0) { sm.wsum[1][warp] = db; sm.wsum[2][warp] = da2; }
+            }
+            __syncthreads();                             // (D)
+            if (tid == 0) {
+                float da = 0.f, db = 0.f, da2 = 0.f;
+                for (int wi = 0; wi < NW; ++wi) da += sm.wsum[0][wi];
+                for (int wi = 0; wi < DV / 32; ++wi) { db += sm.wsum[1][wi]; da2 += sm.wsum[2][wi]; }
+                da -= bv * da2;
+                a.dg[t * d.hv + h] = av * da;
+                a.dbeta[t * d.hv + h] = db;
+            }
+            const float4 dp4 = *reinterpret_cast<const float4 *>(&sm.dp[c4]);
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x) {
+                const int row = rg + x * C::RPP;
+                const float kr = sm.k[row];
+                const float dk = row_sum<C::LPR>(gm[x].x * w4.x + gm[x].y * w4.y + gm[x].z * w4.z +
+                                                 gm[x].w * w4.w + m[x].x * dp4.x + m[x].y * dp4.y +
+                                                 m[x].z * dp4.z + m[x].w * dp4.w);
+                if (lane % C::LPR == 0) a.pk[(t * d.hv + h) * DK + row] = dk;
+                gm[x].x = av * gm[x].x + kr * dp4.x; gm[x].y = av * gm[x].y + kr * dp4.y;
+                gm[x].z = av * gm[x].z + kr * dp4.z; gm[x].w = av * gm[x].w + kr * dp4.w;
+            }
+        }
+    }
+    if (a.d_state_in) {
+        float *D = a.d_state_in + ((long long)slot * d.hv + h) * DK * DV;
+#pragma unroll
+        for (int x = 0; x < C::RPT; ++x)
+            *reinterpret_cast<float4 *>(D + (long long)(rg + x * C::RPP) * DV + c4) = gm[x];
+    }
+}
+
+// dq, dk of each q/k head: the sum of its v-heads' parts, [T][HV][dk] -> [T][HK*dk]
+__global__ void bwd_group_sum_kernel(BwdArgs a) {
+    const Dims &d = a.d;
+    const long long total = a.T * d.hk * d.dk;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const long long t = e / (d.hk * d.dk);
+        const int rem = (int)(e - t * d.hk * d.dk), kh = rem / d.dk, i = rem % d.dk;
+        float sq = 0.f, sk = 0.f;
+        for (int gi = 0; gi < d.grp; ++gi) {
+            const long long src = (t * d.hv + kh * d.grp + gi) * d.dk + i;
+            sq += a.pq[src];
+            sk += a.pk[src];
+        }
+        a.dq[t * a.ld_dqk + (long long)kh * d.dk + i] = sq;
+        a.dk[t * a.ld_dqk + (long long)kh * d.dk + i] = sk;
+    }
+}
+
+template <int D, typename TA>
+cudaError_t launch_bwd_t(const BwdArgs &a, bool states_only, cudaStream_t s) {
+    const dim3 grid(a.d.hv, a.n_seqs);
+    bwd_map_kernel<<<1, 32, 0, s>>>(a.cu_seqlens, a.n_seqs, a.T, a.d.chunk, a.chunk_base, a.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (states_only) {
+        bwd_states_kernel<D, D, TA><<<grid, 4 * D, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    bwd_kernel<D, D, TA><<<grid, 4 * D, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    long long total = a.T * a.d.hk * a.d.dk;
+    int blocks = (int)((total + 255) / 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks > 0) bwd_group_sum_kernel<<<blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename TA>
+cudaError_t launch_bwd_a(const BwdArgs &a, bool states_only, cudaStream_t s) {
+    switch (a.d.dk) {
+        case 32: return launch_bwd_t<32, TA>(a, states_only, s);
+        case 64: return launch_bwd_t<64, TA>(a, states_only, s);
+        case 128: return launch_bwd_t<128, TA>(a, states_only, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+size_t bwd_ws_bytes(const Dims &d, long long T, long long n_seqs, bool states_only) {
+    auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t t = (size_t)(T > 0 ? T : 0), ns = (size_t)(n_seqs > 0 ? n_seqs : 0);
+    size_t b = al((ns + 1) * 4);
+    if (!states_only)
+        b += al(ns * d.hv * (size_t)d.chunk * d.dk * d.dv * 4) + 2 * al(t * d.hv * d.dk * 4);
+    return b;
+}
+
+void bwd_carve(BwdArgs &a, void *ws, bool states_only) {
+    auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    char *p = (char *)ws;
+    const size_t t = (size_t)a.T, ns = (size_t)a.n_seqs;
+    a.chunk_base = (int *)p; p += al((ns + 1) * 4);
+    if (states_only) return;
+    a.scratch = (float *)p; p += al(ns * a.d.hv * (size_t)a.d.chunk * a.d.dk * a.d.dv * 4);
+    a.pq = (float *)p; p += al(t * a.d.hv * a.d.dk * 4);
+    a.pk = (float *)p;
+}
+
+cudaError_t launch_backward(const BwdArgs &a, bool in_bf16, bool states_only, cudaStream_t s) {
+    if (a.n_seqs == 0) return cudaSuccess;
+    return in_bf16 ? launch_bwd_a<__nv_bfloat16>(a, states_only, s)
+                   : launch_bwd_a<float>(a, states_only, s);
+}
+
+}  // namespace gdn

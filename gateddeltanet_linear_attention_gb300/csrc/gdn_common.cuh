@@ -125,6 +125,35 @@ struct DecodeArgs {
     const int32_t *ckpt_idx;
 };
 
+// Backward of the gated delta rule core (gdn_chunk_states / gdn_chunk_backward).
+struct BwdArgs {
+    const void *q, *k, *v;
+    long long ld_qk, ld_v;
+    const float *g, *beta;
+    const int32_t *cu_seqlens;
+    int n_seqs;
+    long long T;
+    const float *state_in;        // [slots][HV][dk][dv] or null (zero initial state)
+    const int32_t *state_idx;
+    float *bnd;                   // [chunks][HV][dk][dv]: the state at every chunk start
+    const float *d_o;             // [T][HV*dv]
+    const float *d_state_out;     // [slots][HV][dk][dv] or null
+    float *dq, *dk;               // [T][ld_dqk], q/k head kh at column kh*dk
+    long long ld_dqk;
+    float *dv;                    // [T][HV*dv]
+    float *dg, *dbeta;            // [T][HV]
+    float *d_state_in;            // [slots][HV][dk][dv] or null
+    Dims d;
+    unsigned *err;
+    // workspace (bwd_carve)
+    int *chunk_base;              // [n_seqs + 1]
+    float *scratch;               // [n_seqs][HV][chunk][dk][dv]: states before each token of a chunk
+    float *pq, *pk;               // [T][HV][dk]: dq, dk per v-head
+};
+size_t bwd_ws_bytes(const Dims &d, long long T, long long n_seqs, bool states_only);
+void bwd_carve(BwdArgs &a, void *ws, bool states_only);
+cudaError_t launch_backward(const BwdArgs &a, bool in_bf16, bool states_only, cudaStream_t s);
+
 // Per-(sequence, q/k head) record the fused decode's prep kernel writes and its
 // streaming kernel reads (floats): normalised q and k, conv'd v and SiLU(z) of
 // the unit's G v-heads, the gates a and beta, k.q, and the state slot.

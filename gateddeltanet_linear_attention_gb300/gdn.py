@@ -90,6 +90,10 @@ def load(path: str | None = None):
             "gdn_mixer_prefill_static": ([CP, ctypes.POINTER(MixerIO), V], I32),
             "gdn_state_copy": ([CP, P, P, I32, P, P, I32, P, P, I32, V], I32),
             "gdn_mixer_verify": ([CP, ctypes.POINTER(MixerIO), I32, P, P, SZ, V], I32),
+            "gdn_backward_workspace_size": ([CP, I64, I32], SZ),
+            "gdn_chunk_states": ([CP, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, SZ, V], I32),
+            "gdn_chunk_backward": ([CP, P, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, P, P,
+                                    I64, P, P, P, P, P, SZ, V], I32),
             "gdn_device_error": ([V, ctypes.POINTER(U32)], I32),
             "gdn_status_string": ([I32], ctypes.c_char_p),
         }
@@ -227,6 +231,39 @@ def gdn_mixer_decode(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, s
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().gdn_mixer_decode(ctypes.byref(cfg), ctypes.byref(io), _ptr(workspace), ws_bytes,
                                    _stream(stream)), "gdn_mixer_decode")
+
+
+def gdn_backward_workspace_size(cfg, max_tokens, max_seqs) -> int:
+    return load().gdn_backward_workspace_size(ctypes.byref(cfg), max_tokens, max_seqs)
+
+
+def chunk_count(seqlens, chunk):
+    """Boundary states of a batch: sum over sequences of ceil(len / chunk)."""
+    return sum((int(L) + chunk - 1) // chunk for L in seqlens)
+
+
+def gdn_chunk_states(cfg, k, v, g, beta, cu_seqlens, boundary_states, workspace, state_in=None,
+                     state_idx=None, stream=None):
+    T = k.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_chunk_states(ctypes.byref(cfg), _ptr(k), _ld(k), _ptr(v), _ld(v), _dt(k),
+                                   _ptr(g), _ptr(beta), _ptr(cu_seqlens), cu_seqlens.shape[0] - 1, T,
+                                   _ptr(state_in), _ptr(state_idx), _ptr(boundary_states),
+                                   _ptr(workspace), ws_bytes, _stream(stream)), "gdn_chunk_states")
+
+
+def gdn_chunk_backward(cfg, q, k, v, g, beta, cu_seqlens, boundary_states, d_o, dq, dk, dv, dg,
+                       dbeta, workspace, d_state_out=None, d_state_in=None, state_idx=None,
+                       stream=None):
+    T = q.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_chunk_backward(ctypes.byref(cfg), _ptr(q), _ptr(k), _ld(q), _ptr(v), _ld(v),
+                                     _dt(q), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                     cu_seqlens.shape[0] - 1, T, _ptr(state_idx),
+                                     _ptr(boundary_states), _ptr(d_o), _ptr(d_state_out), _ptr(dq),
+                                     _ptr(dk), _ld(dq), _ptr(dv), _ptr(dg), _ptr(dbeta),
+                                     _ptr(d_state_in), _ptr(workspace), ws_bytes, _stream(stream)),
+           "gdn_chunk_backward")
 
 
 def gdn_mixer_verify(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, state,

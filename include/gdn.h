@@ -221,6 +221,48 @@ gdn_status gdn_mixer_prefill_static(const gdn_config *cfg, const gdn_mixer_io *i
 gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* Backward of the gated delta rule core from retained chunk-boundary states
+ * (hyperflare core-design, training plan: a training step retains
+ * activations and GDN chunk-boundary states; the backward has one entry per
+ * region, the GDN core among them).  The core is the rule of
+ * gdn_chunk_prefill on q, k, v as given (no in-kernel L2 norm: q and k are
+ * the normalised vectors; the norm's own backward is outside the core).
+ * Chunks are cfg->chunk tokens from each sequence's first token; sequence n
+ * has ceil(len_n / chunk) of them and its chunk c is boundary index
+ * (sum over m < n of ceil(len_m / chunk)) + c.
+ *
+ * gdn_chunk_states: the state before the first token of every chunk, fp32
+ * [n_chunks][HV][dk][dv] (the layout of the recurrent state), from state_in
+ * (NULL: zero) of slot state_idx[n] (NULL: slot n; a negative entry is a
+ * padding lane and gets no entries written).  k: [T][ld_qk], v: [T][ld_v]
+ * in_dtype; g, beta: [T][HV] fp32.  workspace: at least
+ * gdn_backward_workspace_size(cfg, T, n_seqs) bytes (this call uses 256 plus
+ * 4 * (n_seqs + 1) of them).
+ *
+ * gdn_chunk_backward: for the loss sum(d_o * o) + sum(d_state_out * S_final)
+ * (d_state_out NULL: no final-state term), writes dq, dk ([T][ld_dqk] fp32, the
+ * v-heads of each q/k head summed: head kh at column kh*dk), dv ([T][HV*dv]
+ * fp32), dg and dbeta ([T][HV] fp32; dg is the gradient with respect to the
+ * log-decay g, a = exp(g)) and, when non-NULL, d_state_in ([n_slots][HV][dk]
+ * [dv] fp32, the gradient with respect to the initial state of each
+ * sequence's slot).  boundary_states as written by gdn_chunk_states for the
+ * same batch.  Padding lanes get zero gradients.  workspace: at least
+ * gdn_backward_workspace_size(cfg, T, n_seqs) bytes (one chunk of states
+ * per (sequence, v-head), dq and dk per v-head). */
+size_t gdn_backward_workspace_size(const gdn_config *cfg, int64_t max_tokens, int32_t max_seqs);
+gdn_status gdn_chunk_states(const gdn_config *cfg, const void *k, int64_t ld_qk, const void *v,
+                            int64_t ld_v, gdn_dtype in_dtype, const float *g, const float *beta,
+                            const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
+                            const float *state_in, const int32_t *state_idx, float *boundary_states,
+                            void *workspace, size_t workspace_bytes, void *stream);
+gdn_status gdn_chunk_backward(const gdn_config *cfg, const void *q, const void *k, int64_t ld_qk,
+                              const void *v, int64_t ld_v, gdn_dtype in_dtype, const float *g,
+                              const float *beta, const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
+                              const int32_t *state_idx, const float *boundary_states,
+                              const float *d_o, const float *d_state_out, float *dq, float *dk,
+                              int64_t ld_dqk, float *dv, float *dg, float *dbeta, float *d_state_in,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
 /* Multi-token verification decode (hyperflare core-design, speculative
  * target state: each request reserves eight recurrent checkpoint columns, a
  * verification round writes the columns of its inputs, and the round after
