@@ -332,6 +332,11 @@ def run_ours(args, rank, ws, local):
     if args.decode_steps > 0:
         dec = bench_decode(args, dev, gdn, pk, pk_src)
 
+    # ---- the same decode on a Q8 state
+    dq8 = None
+    if args.decode_steps > 0:
+        dq8 = bench_decode_q8(args, dev, gdn, pk, pk_src)
+
     # ---- slot snapshot (state + conv history) through gdn_state_copy
     snap = None
     if args.decode_steps > 0:
@@ -370,7 +375,7 @@ def run_ours(args, rank, ws, local):
                            "activations": wl.act, "y_dtype": "bf16"},
                 "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk.summary(), "decode": dec, "state_copy": snap, "verify": ver,
+                "clocks": clk.summary(), "decode": dec, "decode_q8": dq8, "state_copy": snap, "verify": ver,
                 "backward": bwd}
         print(json.dumps(line), flush=True)
 
@@ -422,6 +427,55 @@ def bench_decode(args, dev, gdn, pk, pk_src):
                          "achieved": gbs,
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
                          "traffic": traffic_for("decode_64x256"),
+                         "peak_source": pk_src + " copy"},
+            "gpu_launches": 2 * S}
+
+
+def bench_decode_q8(args, dev, gdn, pk, pk_src):
+    """decode_64x256 on a Q8 state pool (int8 codes + fp32 row scales) through
+    gdn_mixer_decode_q8, L2 evicted between steps like the fp32 decode."""
+    wl = WORKLOADS["decode_64x256"]
+    S = args.decode_steps
+    from dataclasses import replace
+    wl = replace(wl, decode_steps=S)
+    inp = make_inputs(wl)
+    N = wl.n_decode
+    cfg = gdn.make_config(wl.HK, wl.HV, wl.dk, wl.dv, wl.chunk, wl.act, n_slots=N)
+    codes = torch.empty((N, wl.HV, wl.dk, wl.dv), dtype=torch.int8, device=dev)
+    scales = torch.empty((N, wl.HV, wl.dk), device=dev)
+    gdn.gdn_state_to_q8(cfg, inp["state"].to(dev), codes, scales, 0)
+    conv = inp["conv_state"].to(dev)
+    cw, A, dt, nw = (inp[k].to(dev) for k in ("conv_w", "A_log", "dt_bias", "norm_w"))
+    xs, zs, us, bs = (inp[k].to(dev) for k in ("dec_x", "dec_z", "dec_u", "dec_b_logit"))
+    y = torch.empty((N, wl.HV * wl.dv), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(gdn.gdn_workspace_size(cfg, N, N), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+    flush.fill_(1.0)
+    sink = torch.empty((), device=dev)
+    stream = torch.cuda.current_stream()
+    for t in range(min(3, S)):   # warm-up on copies of the pool
+        c2, s2, v2 = codes.clone(), scales.clone(), conv.clone()
+        gdn.gdn_mixer_decode_q8(cfg, xs[t], zs[t], us[t], bs[t], cw, A, dt, nw, y, c2, s2, v2, 1 + t, ws)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(S)]
+    for t in range(S):
+        torch.sum(flush, 0, out=sink)
+        evs[t][0].record(stream)
+        gdn.gdn_mixer_decode_q8(cfg, xs[t], zs[t], us[t], bs[t], cw, A, dt, nw, y, codes, scales, conv,
+                                1 + t, ws)
+        evs[t][1].record(stream)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_error() == 0
+    per = sum(a.elapsed_time(b) for a, b in evs) / S / 1e3
+    q8_bytes = 2 * N * wl.HV * (wl.dk * wl.dv + wl.dk * 4)
+    gbs = q8_bytes / per / 1e9
+    return {"workload": "decode_64x256 with a Q8 state (int8 codes + fp32 row scales, 16.5 KiB per "
+                        "head), %d steps, L2 evicted between steps" % S,
+            "value": gbs, "unit": "GB/s", "us_per_step": per * 1e6, "state_bytes_per_step": q8_bytes,
+            "roofline": {"kernel": "decode_prep_kernel + decode_q8_kernel", "bound": "hbm",
+                         "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
                          "peak_source": pk_src + " copy"},
             "gpu_launches": 2 * S}
 

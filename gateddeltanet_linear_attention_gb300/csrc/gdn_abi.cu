@@ -312,7 +312,10 @@ gdn_status gdn_gated_rmsnorm(const gdn_config *cfg, const void *o, gdn_dtype o_d
 }
 
 // Validation shared by the fused entry points.
-static gdn_status check_mixer_io(const gdn::Dims &d, const gdn_mixer_io *io, bool decode) {
+// decode: one token per sequence, the state updated in place (q8: the fp32 state pointers must
+// be NULL, the state lives in the caller's Q8 pool)
+static gdn_status check_mixer_io(const gdn::Dims &d, const gdn_mixer_io *io, bool decode,
+                                 bool q8 = false) {
     if (!io || io->n_seqs < 0 || io->T < 0 || !valid_dtype(io->y_dtype)) return GDN_ERR_INVALID_ARG;
     if (io->n_seqs > kMaxSeqs) return GDN_ERR_UNSUPPORTED;
     if (decode && io->T != io->n_seqs) return GDN_ERR_INVALID_ARG;
@@ -328,7 +331,9 @@ static gdn_status check_mixer_io(const gdn::Dims &d, const gdn_mixer_io *io, boo
         return GDN_ERR_INVALID_ARG;
     if ((io->state_in || io->state_out || io->conv_state) && d.n_slots == 0)
         return GDN_ERR_INVALID_ARG;
-    if (decode && (!io->state_in || io->state_out != io->state_in || !io->conv_state))
+    if (decode && !q8 && (!io->state_in || io->state_out != io->state_in || !io->conv_state))
+        return GDN_ERR_INVALID_ARG;
+    if (q8 && (io->state_in || io->state_out || !io->conv_state || d.n_slots == 0))
         return GDN_ERR_INVALID_ARG;
     return GDN_OK;
 }
@@ -547,6 +552,57 @@ gdn_status gdn_chunk_backward(const gdn_config *cfg, const void *q, const void *
     a.d_state_in = d_state_in; a.d = d; a.err = err;
     gdn::bwd_carve(a, workspace, false);
     return launch_status(gdn::launch_backward(a, in_dtype == GDN_BF16, false, (cudaStream_t)stream));
+}
+
+gdn_status gdn_state_to_q8(const gdn_config *cfg, const float *state, int8_t *codes, float *scales,
+                           uint32_t frame, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (!state || !codes || !scales || !aligned16(state) || !aligned16(codes) || !aligned16(scales))
+        return GDN_ERR_INVALID_ARG;
+    if (d.n_slots == 0) return GDN_OK;
+    return launch_status(gdn::launch_q8_convert(d, state, codes, scales, frame, true,
+                                                (cudaStream_t)stream));
+}
+
+gdn_status gdn_state_from_q8(const gdn_config *cfg, const int8_t *codes, const float *scales,
+                             float *state, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if (!state || !codes || !scales || !aligned16(state) || !aligned16(codes) || !aligned16(scales))
+        return GDN_ERR_INVALID_ARG;
+    if (d.n_slots == 0) return GDN_OK;
+    return launch_status(gdn::launch_q8_convert(d, state, const_cast<int8_t *>(codes),
+                                                const_cast<float *>(scales), 0u, false,
+                                                (cudaStream_t)stream));
+}
+
+gdn_status gdn_mixer_decode_q8(const gdn_config *cfg, const gdn_mixer_io *io, int8_t *codes,
+                               float *scales, uint32_t frame, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    gdn::Dims d;
+    gdn_status st = check_cfg(cfg, &d);
+    if (st != GDN_OK) return st;
+    if ((st = check_mixer_io(d, io, true, true)) != GDN_OK) return st;
+    if (io->n_seqs == 0) return GDN_OK;
+    if (!codes || !scales || !aligned16(codes) || !aligned16(scales)) return GDN_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < gdn::decode_ws_bytes(d, io->n_seqs))
+        return GDN_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    if ((st = error_word(&err)) != GDN_OK) return st;
+    gdn::DecodeArgs a = {};
+    a.x = io->x; a.ld_x = io->ld_x; a.conv_w = io->conv_w; a.conv_state = io->conv_state;
+    a.u = io->u; a.b_logit = io->b_logit; a.ld_ub = io->ld_ub; a.A_log = io->A_log;
+    a.dt_bias = io->dt_bias; a.z = io->z; a.ld_z = io->ld_z; a.norm_w = io->norm_w;
+    a.n = io->n_seqs; a.state_idx = io->state_idx; a.out = io->y;
+    a.ws = (float *)workspace;
+    a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
+    a.q8 = codes; a.q8_scale = scales; a.frame = frame;
+    return launch_status(gdn::launch_decode_q8(a, cfg->act == GDN_BF16, io->y_dtype == GDN_BF16,
+                                               (cudaStream_t)stream));
 }
 
 gdn_status gdn_device_error(void *stream, uint32_t *code) {

@@ -123,7 +123,15 @@ struct DecodeArgs {
     // history after token j go to slot ckpt_idx[n] + j
     int k_tokens;
     const int32_t *ckpt_idx;
+    // Q8 state (gdn_mixer_decode_q8): int8 codes [slots][HV][dk][dv], fp32 row scales
+    // [slots][HV][dk], and the frame that keys the rounding dither
+    int8_t *q8;
+    float *q8_scale;
+    uint32_t frame;
 };
+cudaError_t launch_decode_q8(const DecodeArgs &a, bool in_bf16, bool out_bf16, cudaStream_t s);
+cudaError_t launch_q8_convert(const Dims &d, const float *state, int8_t *codes, float *scales,
+                              uint32_t frame, bool to_q8, cudaStream_t s);
 
 // Backward of the gated delta rule core (gdn_chunk_states / gdn_chunk_backward).
 struct BwdArgs {

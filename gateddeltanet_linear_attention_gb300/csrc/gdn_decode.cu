@@ -536,3 +536,221 @@ size_t decode_ws_bytes(const Dims &d, long long n_seqs) {
     return (size_t)(n_seqs > 0 ? n_seqs : 0) * d.hk * R.size * sizeof(float);
 }
 }  // namespace gdn
+
+// ---------------------------------------------------------------------------
+// Q8 recurrent state (int8 codes + one fp32 scale per state row), the decode
+// variant that cuts the state bytes about 4x.  Row i of a head's M (dv
+// values) is stored as code_ij * s_i with s_i = max_j |M_ij| / 127; a new
+// state is encoded with stochastic rounding, code = floor(M * 127/max + u),
+// u in [0, 1) from a counter-based hash of (frame, slot, head, i, j), so that
+// the rounding error has zero mean and does not accumulate a bias across
+// steps.  The hash is the PCG hash of Jarzynski and Olano ("Hash Functions for
+// GPU Rendering", JCGT 2020): one PCG32 LCG step and its RXS-M-XS output.
+// Every step of the encoding is an explicitly rounded fp32 operation.
+namespace gdn {
+
+namespace {
+
+__device__ __forceinline__ uint32_t pcg_hash(uint32_t v) {
+    const uint32_t state = v * 747796405u + 2891336453u;
+    const uint32_t word = ((state >> ((state >> 28u) + 4u)) ^ state) * 277803737u;
+    return (word >> 22u) ^ word;
+}
+
+template <int L>
+__device__ __forceinline__ float row_max(float v) {
+#pragma unroll
+    for (int o = L / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+template <int DK, int DV>
+struct Q8Io {
+    static constexpr int LPR = DV / 4, RPP = 4 * DV / LPR, RPT = DK / RPP;
+    // encode: m (the thread's float4 of rows rg + x*RPP) -> codes, scales
+    static __device__ __forceinline__ void store(const float4 (&m)[RPT], int8_t *codes, float *scales,
+                                                 uint32_t hf, uint32_t base_idx, int rg, int c4,
+                                                 int lane) {
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+            const int row = rg + x * RPP;
+            const float amax = row_max<LPR>(fmaxf(fmaxf(fabsf(m[x].x), fabsf(m[x].y)),
+                                                  fmaxf(fabsf(m[x].z), fabsf(m[x].w))));
+            const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
+            const float v[4] = {m[x].x, m[x].y, m[x].z, m[x].w};
+            char4 c;
+            signed char cc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t idx = base_idx + (uint32_t)(row * DV + c4 + e);
+                const float u = (float)(pcg_hash(idx ^ hf) >> 8) * (1.0f / 16777216.0f);
+                float q = floorf(__fadd_rn(__fmul_rn(v[e], inv), u));
+                q = fminf(fmaxf(q, -127.f), 127.f);
+                cc[e] = amax > 0.f ? (signed char)(int)q : (signed char)0;
+            }
+            c.x = cc[0]; c.y = cc[1]; c.z = cc[2]; c.w = cc[3];
+            *reinterpret_cast<char4 *>(codes + row * DV + c4) = c;
+            if (lane % LPR == 0) scales[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+        }
+    }
+    // decode: codes, scales -> m
+    static __device__ __forceinline__ void load(float4 (&m)[RPT], const int8_t *codes, const float *scales,
+                                                int rg, int c4) {
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+            const int row = rg + x * RPP;
+            const char4 c = *reinterpret_cast<const char4 *>(codes + row * DV + c4);
+            const float s = scales[row];
+            m[x] = make_float4(__fmul_rn((float)c.x, s), __fmul_rn((float)c.y, s),
+                               __fmul_rn((float)c.z, s), __fmul_rn((float)c.w, s));
+        }
+    }
+};
+
+// fp32 pool <-> Q8 pool, one CTA per (slot, head)
+template <int DK, int DV>
+__global__ void __launch_bounds__(4 * DV) q8_convert_kernel(Dims d, const float *state, int8_t *codes,
+                                                            float *scales, uint32_t frame, bool to_q8) {
+    using Q = Q8Io<DK, DV>;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const long long head = blockIdx.x;                       // slot * HV + h
+    const int rg = tid / Q::LPR, c4 = (tid % Q::LPR) * 4;
+    int8_t *cp = codes + head * DK * DV;
+    float *sp = scales + head * DK;
+    float4 m[Q::RPT];
+    if (to_q8) {
+#pragma unroll
+        for (int x = 0; x < Q::RPT; ++x)
+            m[x] = *reinterpret_cast<const float4 *>(state + head * DK * DV + (rg + x * Q::RPP) * DV + c4);
+        Q::store(m, cp, sp, pcg_hash(frame), (uint32_t)(head * DK * DV), rg, c4, lane);
+    } else {
+        Q::load(m, cp, sp, rg, c4);
+        float *out = const_cast<float *>(state);
+#pragma unroll
+        for (int x = 0; x < Q::RPT; ++x)
+            *reinterpret_cast<float4 *>(out + head * DK * DV + (rg + x * Q::RPP) * DV + c4) = m[x];
+    }
+}
+
+// The one-token update on a Q8 state: one CTA per (sequence, v-head), after decode_prep_kernel
+// has written the unit records (the same ones the fp32 streaming kernel reads).
+template <int DK, int DV, typename TOut>
+__global__ void __launch_bounds__(4 * DV, 2) decode_q8_kernel(DecodeArgs a) {
+    using Q = Q8Io<DK, DV>;
+    constexpr int NT = 4 * DV, LPR = Q::LPR, RPP = Q::RPP, RPT = Q::RPT;
+    __shared__ __align__(16) float red_p[RPP][DV];
+    __shared__ __align__(16) float red_s[RPP][DV];
+    __shared__ __align__(16) float up[DV];
+    __shared__ float npart[DV / 32];
+    const Dims &d = a.d;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = d.grp, n = blockIdx.x / d.hv, h = blockIdx.x % d.hv, kh = h / G, gi = h % G;
+    const DecRec R(DK, DV, G);
+    const float *rc = a.ws + (long long)(n * d.hk + kh) * R.size;
+    TOut *out = (TOut *)a.out;
+    const long long orow = (long long)n * d.hv * DV + (long long)h * DV;
+    const int slot = __float_as_int(rc[R.slot]);
+    if (slot < 0 || slot >= d.n_slots) {      // padding lane
+        for (int j = tid; j < DV; j += NT) out[orow + j] = from_f32<TOut>(0.f);
+        return;
+    }
+    const int rg = tid / LPR, c4 = (tid % LPR) * 4;
+    const long long head = (long long)slot * d.hv + h;
+    int8_t *cp = a.q8 + head * DK * DV;
+    float *sp = a.q8_scale + head * DK;
+    float4 m[RPT];
+    Q::load(m, cp, sp, rg, c4);
+    float kr[RPT], qr[RPT];
+#pragma unroll
+    for (int x = 0; x < RPT; ++x) {
+        kr[x] = rc[R.k + rg + x * RPP];
+        qr[x] = rc[R.q + rg + x * RPP];
+    }
+    float4 pp = make_float4(0.f, 0.f, 0.f, 0.f), ss = pp;
+#pragma unroll
+    for (int x = 0; x < RPT; ++x) {
+        pp.x += m[x].x * kr[x]; pp.y += m[x].y * kr[x]; pp.z += m[x].z * kr[x]; pp.w += m[x].w * kr[x];
+        ss.x += m[x].x * qr[x]; ss.y += m[x].y * qr[x]; ss.z += m[x].z * qr[x]; ss.w += m[x].w * qr[x];
+    }
+    *reinterpret_cast<float4 *>(&red_p[rg][c4]) = pp;
+    *reinterpret_cast<float4 *>(&red_s[rg][c4]) = ss;
+    __syncthreads();
+    const float ga = rc[R.ga + gi], gb = rc[R.gb + gi];
+    float ov = 0.f;
+    if (tid < DV) {
+        float p = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int r = 0; r < RPP; ++r) {
+            p += red_p[r][tid];
+            s2 += red_s[r][tid];
+        }
+        const float uu = gb * (rc[R.v + gi * DV + tid] - ga * p);
+        up[tid] = uu;
+        ov = ga * s2 + uu * rc[R.kq];
+    }
+    __syncthreads();
+    {
+        const float4 u4 = *reinterpret_cast<const float4 *>(&up[c4]);
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+            m[x].x = ga * m[x].x + kr[x] * u4.x; m[x].y = ga * m[x].y + kr[x] * u4.y;
+            m[x].z = ga * m[x].z + kr[x] * u4.z; m[x].w = ga * m[x].w + kr[x] * u4.w;
+        }
+        Q::store(m, cp, sp, pcg_hash(a.frame), (uint32_t)(head * DK * DV), rg, c4, lane);
+    }
+    if (tid < DV) {   // gated RMSNorm of this head's o
+        const float sq = warp_sum(ov * ov);
+        if (lane == 0) npart[warp] = sq;
+        asm volatile("bar.sync 1, %0;" :: "r"(DV) : "memory");
+        float tot = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < DV / 32; ++wi) tot += npart[wi];
+        const float rs = rsqrtf(tot / (float)DV + d.norm_eps);
+        out[orow + tid] = from_f32<TOut>(ov * rs * a.norm_w[tid] * rc[R.z + gi * DV + tid]);
+    }
+}
+
+template <int D, typename TA, typename TOut>
+cudaError_t launch_q8_t(const DecodeArgs &a, cudaStream_t s) {
+    decode_prep_kernel<D, D, TA><<<a.n * a.d.hk, 256, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_q8_kernel<D, D, TOut><<<a.n * a.d.hv, 4 * D, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_q8_d(const DecodeArgs &a, bool in_bf16, bool out_bf16, cudaStream_t s) {
+    if (in_bf16)
+        return out_bf16 ? launch_q8_t<D, __nv_bfloat16, __nv_bfloat16>(a, s)
+                        : launch_q8_t<D, __nv_bfloat16, float>(a, s);
+    return out_bf16 ? launch_q8_t<D, float, __nv_bfloat16>(a, s) : launch_q8_t<D, float, float>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_q8(const DecodeArgs &a, bool in_bf16, bool out_bf16, cudaStream_t s) {
+    if (a.n == 0) return cudaSuccess;
+    if (a.d.grp > 4 || !a.q8 || !a.q8_scale) return cudaErrorInvalidValue;
+    switch (a.d.dk) {
+        case 32: return launch_q8_d<32>(a, in_bf16, out_bf16, s);
+        case 64: return launch_q8_d<64>(a, in_bf16, out_bf16, s);
+        case 128: return launch_q8_d<128>(a, in_bf16, out_bf16, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_q8_convert(const Dims &d, const float *state, int8_t *codes, float *scales,
+                              uint32_t frame, bool to_q8, cudaStream_t s) {
+    const long long heads = (long long)d.n_slots * d.hv;
+    if (heads == 0) return cudaSuccess;
+    switch (d.dk) {
+        case 32: q8_convert_kernel<32, 32><<<(unsigned)heads, 128, 0, s>>>(d, state, codes, scales, frame, to_q8); break;
+        case 64: q8_convert_kernel<64, 64><<<(unsigned)heads, 256, 0, s>>>(d, state, codes, scales, frame, to_q8); break;
+        case 128: q8_convert_kernel<128, 128><<<(unsigned)heads, 512, 0, s>>>(d, state, codes, scales, frame, to_q8); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

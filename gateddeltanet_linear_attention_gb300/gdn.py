@@ -91,6 +91,9 @@ def load(path: str | None = None):
             "gdn_state_copy": ([CP, P, P, I32, P, P, I32, P, P, I32, V], I32),
             "gdn_mixer_verify": ([CP, ctypes.POINTER(MixerIO), I32, P, P, SZ, V], I32),
             "gdn_backward_workspace_size": ([CP, I64, I32], SZ),
+            "gdn_state_to_q8": ([CP, P, P, P, U32, V], I32),
+            "gdn_state_from_q8": ([CP, P, P, P, V], I32),
+            "gdn_mixer_decode_q8": ([CP, ctypes.POINTER(MixerIO), P, P, U32, P, SZ, V], I32),
             "gdn_chunk_states": ([CP, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, SZ, V], I32),
             "gdn_chunk_backward": ([CP, P, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, P, P,
                                     I64, P, P, P, P, P, SZ, V], I32),
@@ -231,6 +234,28 @@ def gdn_mixer_decode(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, s
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().gdn_mixer_decode(ctypes.byref(cfg), ctypes.byref(io), _ptr(workspace), ws_bytes,
                                    _stream(stream)), "gdn_mixer_decode")
+
+
+def gdn_state_to_q8(cfg, state, codes, scales, frame, stream=None):
+    _check(load().gdn_state_to_q8(ctypes.byref(cfg), _ptr(state), _ptr(codes), _ptr(scales), frame,
+                                  _stream(stream)), "gdn_state_to_q8")
+
+
+def gdn_state_from_q8(cfg, codes, scales, state, stream=None):
+    _check(load().gdn_state_from_q8(ctypes.byref(cfg), _ptr(codes), _ptr(scales), _ptr(state),
+                                    _stream(stream)), "gdn_state_from_q8")
+
+
+def gdn_mixer_decode_q8(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, codes, scales,
+                        conv_state, frame, workspace, state_idx=None, stream=None):
+    """gdn_mixer_decode on a Q8 state pool (codes int8 [slots][HV][dk][dv], scales fp32
+    [slots][HV][dk]); `frame` keys the rounding dither and should change every step."""
+    io = _mixer_io(x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, None, None, None,
+                   conv_state, state_idx, y, x.shape[0])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_mixer_decode_q8(ctypes.byref(cfg), ctypes.byref(io), _ptr(codes), _ptr(scales),
+                                      frame, _ptr(workspace), ws_bytes, _stream(stream)),
+           "gdn_mixer_decode_q8")
 
 
 def gdn_backward_workspace_size(cfg, max_tokens, max_seqs) -> int:

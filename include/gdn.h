@@ -221,6 +221,31 @@ gdn_status gdn_mixer_prefill_static(const gdn_config *cfg, const gdn_mixer_io *i
 gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* Q8 recurrent state: int8 codes [n_slots][HV][dk][dv] with one fp32 scale
+ * per state row, [n_slots][HV][dk] (the row of dk index i holds M[i][0..dv)),
+ * so M[i][j] = code[i][j] * scale[i]: about 4x fewer state bytes per decode
+ * step.  The state is encoded with stochastic rounding: scale = max_j |M_ij| /
+ * 127, code = clamp(floor(M_ij * (127 / max) + u), -127, 127), u in [0, 1)
+ * from a counter-based hash of (frame, slot, head, i, j) (the PCG hash of
+ * Jarzynski and Olano, JCGT 2020), every step an fp32 operation rounded to
+ * nearest.  The rounding error then has zero mean, so it does not build up a
+ * bias over many steps: the error feedback the pages ask of a quantised state
+ * (hyperflare release notes: a DeltaNet Q8 state whose dither is keyed by a
+ * frame counter).  The caller passes a new frame every step.
+ *
+ * gdn_state_to_q8 / gdn_state_from_q8: convert the whole pool (cfg->n_slots
+ * slots) between fp32 [n_slots][HV][dk][dv] and Q8.
+ * gdn_mixer_decode_q8: gdn_mixer_decode on a Q8 pool; io->state_in and
+ * io->state_out must be NULL; io->conv_state is required; same workspace as
+ * gdn_mixer_decode. */
+gdn_status gdn_state_to_q8(const gdn_config *cfg, const float *state, int8_t *codes, float *scales,
+                           uint32_t frame, void *stream);
+gdn_status gdn_state_from_q8(const gdn_config *cfg, const int8_t *codes, const float *scales,
+                             float *state, void *stream);
+gdn_status gdn_mixer_decode_q8(const gdn_config *cfg, const gdn_mixer_io *io, int8_t *codes,
+                               float *scales, uint32_t frame, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
 /* Backward of the gated delta rule core from retained chunk-boundary states
  * (hyperflare core-design, training plan: a training step retains
  * activations and GDN chunk-boundary states; the backward has one entry per

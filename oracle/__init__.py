@@ -301,3 +301,91 @@ def delta_rule_backward(xa, g, beta, cu_seqlens, HK, HV, dk, dv, d_o, state=None
             if d_state_in is not None:
                 d_state_in[slot, h] = GS.T
     return dxa, dg, db, d_state_in
+
+
+# ------------------------------------------------------------------ Q8 state
+
+def pcg_hash(v):
+    """The PCG hash of Jarzynski and Olano ("Hash Functions for GPU Rendering", JCGT 2020): one
+    step of the PCG32 LCG followed by its RXS-M-XS output permutation, on uint32 (wrapping)."""
+    v = np.asarray(v, dtype=np.uint32)
+    with np.errstate(over="ignore"):
+        state = v * np.uint32(747796405) + np.uint32(2891336453)
+        word = ((state >> ((state >> np.uint32(28)) + np.uint32(4))) ^ state) * np.uint32(277803737)
+    return (word >> np.uint32(22)) ^ word
+
+
+def q8_dither(frame, slot, HV, h, dk, dv):
+    """The rounding offsets u in [0, 1) of one head's [dk, dv] codes at a given frame: 24 bits of
+    pcg_hash(index ^ pcg_hash(frame)), index = ((slot*HV + h)*dk + i)*dv + j (uint32)."""
+    i = np.arange(dk, dtype=np.uint64)[:, None]
+    j = np.arange(dv, dtype=np.uint64)[None, :]
+    idx = ((((np.uint64(slot) * np.uint64(HV) + np.uint64(h)) * np.uint64(dk) + i) * np.uint64(dv) + j)
+           & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    r = pcg_hash(idx ^ pcg_hash(np.uint32(frame)))
+    return (r >> np.uint32(8)).astype(np.float32) * np.float32(1.0 / 16777216.0)
+
+
+def q8_encode_head(M, frame, slot, HV, h):
+    """One head's fp32 [dk, dv] state (M = S^T) to int8 codes and per-row scales, every step in
+    fp32 with round-to-nearest: absmax a_i of row i, scale s_i = a_i / 127, x = M * (127 / a_i),
+    code = clamp(floor(x + u), -127, 127) with the dither u of q8_dither (stochastic rounding:
+    the expected code is x, so the rounding error carries no bias from step to step).  A zero
+    row gets scale 0 and codes 0.  Returns (codes int8 [dk, dv], scales fp32 [dk])."""
+    M = np.asarray(M, dtype=np.float32)
+    dk, dv = M.shape
+    amax = np.max(np.abs(M), axis=1).astype(np.float32)
+    nz = amax > 0
+    scale = np.zeros(dk, np.float32)
+    scale[nz] = amax[nz] / np.float32(127)
+    inv = np.zeros(dk, np.float32)
+    inv[nz] = np.float32(127) / amax[nz]
+    x = (M * inv[:, None]).astype(np.float32)
+    u = q8_dither(frame, slot, HV, h, dk, dv)
+    c = np.floor((x + u).astype(np.float32))
+    c = np.clip(c, -127, 127)
+    c[~nz] = 0
+    return c.astype(np.int8), scale
+
+
+def q8_encode(state, frame):
+    """A whole fp32 pool [slots, HV, dk, dv] -> (codes int8, scales [slots, HV, dk])."""
+    state = np.asarray(state, dtype=np.float32)
+    S, HV, dk, dv = state.shape
+    codes = np.zeros(state.shape, np.int8)
+    scales = np.zeros((S, HV, dk), np.float32)
+    for s in range(S):
+        for h in range(HV):
+            codes[s, h], scales[s, h] = q8_encode_head(state[s, h], frame, s, HV, h)
+    return codes, scales
+
+
+def q8_decode(codes, scales):
+    """Dequantise: M = code * scale (fp32)."""
+    return (np.asarray(codes, np.float32) * np.asarray(scales, np.float32)[..., None]).astype(np.float32)
+
+
+def mixer_decode_q8(x, conv_w, u, b_logit, A_log, dt_bias, z, norm_w, HK, HV, dk, dv, codes, scales,
+                    conv_state, frame, slot_idx=None, q_scale=1.0, l2_eps=1e-6, norm_eps=1e-6):
+    """One decode step (one token for each of n sequences) on a Q8 state pool: the state of
+    each sequence's slot is dequantised, the plain mixer (fp64) runs one token, and the new
+    state is cast to fp32 and quantised again at `frame`.  Returns (y, codes, scales, conv)."""
+    n = _f64(x).shape[0]
+    slots = list(range(n)) if slot_idx is None else [int(s) for s in np.asarray(slot_idx)]
+    codes = np.array(codes, copy=True); scales = np.array(scales, copy=True)
+    conv = _f64(conv_state).copy()
+    y = np.zeros((n, HV * dv))
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        st = q8_decode(codes[s:s + 1], scales[s:s + 1]).astype(np.float64)
+        out = mixer(_f64(x)[i:i + 1], conv_w, _f64(u)[i:i + 1], _f64(b_logit)[i:i + 1], A_log, dt_bias,
+                    _f64(z)[i:i + 1], norm_w, np.array([0, 1], np.int32), HK, HV, dk, dv,
+                    state=st, conv_state=conv[s:s + 1], q_scale=q_scale, l2_eps=l2_eps,
+                    norm_eps=norm_eps, n_threads=1)
+        y[i] = out["y"][0]
+        conv[s] = out["conv_state"][0]
+        for h in range(HV):
+            codes[s, h], scales[s, h] = q8_encode_head(out["state"][0, h].astype(np.float32), frame, s,
+                                                       HV, h)
+    return y, codes, scales, conv

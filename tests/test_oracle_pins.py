@@ -462,3 +462,73 @@ def test_delta_rule_backward_padding_lane_has_no_gradient():
     for a, b in zip(full[:3], alone[:3]):
         assert np.array_equal(a[2:], b)
     assert np.array_equal(full[3], alone[3])
+
+
+# ----------------------------------------------------------- Q8 state
+
+def test_q8_encoding_rules():
+    """Every code lies in [-127, 127], the row's largest magnitude maps to +-127, the decoded
+    value is within one step (the row scale max/127) of the original, and a zero row stays zero."""
+    rng = np.random.default_rng(31)
+    M = (rng.standard_normal((6, 16)) * rng.uniform(0.01, 3, (6, 1))).astype(np.float32)
+    M[4] = 0
+    c, s = oracle.q8_encode_head(M, frame=5, slot=2, HV=3, h=1)
+    assert c.dtype == np.int8 and np.all(np.abs(c.astype(int)) <= 127)
+    for i in range(6):
+        if i == 4:
+            assert s[i] == 0 and np.all(c[i] == 0)
+            continue
+        j = int(np.argmax(np.abs(M[i])))
+        assert abs(int(c[i, j])) == 127 and np.sign(c[i, j]) == np.sign(M[i, j])
+        assert s[i] == np.float32(np.abs(M[i]).max()) / np.float32(127)
+    err = np.abs(oracle.q8_decode(c, s) - M)
+    assert np.all(err < s[:, None] * 1.0001 + 1e-30)
+
+
+def test_q8_dither_uniform_and_rounding_unbiased():
+    """The dither is uniform on [0, 1) (16-bin counts within 5 sigma over 65,536 draws); the
+    stochastic rounding is unbiased: the decoded value averaged over 400 frames sits within a
+    few standard errors of the input."""
+    u = np.concatenate([oracle.q8_dither(f, 0, 4, 1, 64, 64).ravel() for f in range(16)])
+    assert u.min() >= 0 and u.max() < 1
+    counts = np.histogram(u, bins=16, range=(0, 1))[0]
+    expect = u.size / 16
+    assert np.all(np.abs(counts - expect) <= 5 * np.sqrt(expect))
+    assert abs(u.mean() - 0.5) < 5 * np.sqrt(1 / 12 / u.size)
+    rng = np.random.default_rng(32)
+    M = rng.standard_normal((4, 32)).astype(np.float32)
+    acc = np.zeros_like(M, dtype=np.float64)
+    F = 400
+    for f in range(F):
+        c, s = oracle.q8_encode_head(M, frame=f, slot=0, HV=1, h=0)
+        acc += oracle.q8_decode(c, s)
+    step = (np.abs(M).max(axis=1) / 127)[:, None]
+    assert np.all(np.abs(acc / F - M) <= 5 * step / (2 * np.sqrt(F)) + 1e-7)
+    # round-to-nearest (no dither) would be biased for values between codes
+    biased = np.round(M / step) * step
+    assert np.abs(biased - M).max() > 10 * np.abs(acc / F - M).max() / 5
+
+
+def test_mixer_decode_q8_is_decode_of_dequantised_state_then_encode():
+    rng = np.random.default_rng(33)
+    HK, HV, d = 1, 2, 8
+    CH = 2 * HK * d + HV * d
+    st = (rng.standard_normal((2, HV, d, d)) * 0.1).astype(np.float32)
+    codes, scales = oracle.q8_encode(st, frame=1)
+    conv = rng.standard_normal((2, CH, 3))
+    x = rng.standard_normal((2, CH)); z = rng.standard_normal((2, HV * d))
+    u = rng.standard_normal((2, HV)); b = rng.standard_normal((2, HV))
+    cw = rng.normal(0, 0.25, (CH, 4)); A = rng.uniform(-1, 1, HV); dt = np.zeros(HV); nw = np.ones(d)
+    y, c2, s2, conv2 = oracle.mixer_decode_q8(x, cw, u, b, A, dt, z, nw, HK, HV, d, d, codes, scales, conv,
+                                              frame=2, slot_idx=[1, -1])
+    ref = oracle.mixer(x[:1], cw, u[:1], b[:1], A, dt, z[:1], nw, np.array([0, 1], np.int32), HK, HV, d, d,
+                       state=oracle.q8_decode(codes[1:2], scales[1:2]).astype(np.float64),
+                       conv_state=conv[1:2].copy(), n_threads=1)
+    assert np.array_equal(y[0], ref["y"][0]) and np.all(y[1] == 0)
+    ce, se = oracle.q8_encode(ref["state"].astype(np.float32), frame=2)
+    # (the pool's slot index keys the dither: re-encode slot 1's heads at slot 1)
+    for h in range(HV):
+        c_h, s_h = oracle.q8_encode_head(ref["state"][0, h].astype(np.float32), 2, 1, HV, h)
+        assert np.array_equal(c2[1, h], c_h) and np.array_equal(s2[1, h], s_h)
+    assert np.array_equal(c2[0], codes[0]) and np.array_equal(conv2[0], conv[0])   # other slot untouched
+    assert np.array_equal(conv2[1], ref["conv_state"][0])
