@@ -264,11 +264,73 @@ __global__ void __launch_bounds__(256) decode_prep_kernel(DecodeArgs a) {
     }
 }
 
+// ---- Q8 state codec (used by the streaming kernel in its Q8 form and by
+// q8_convert_kernel; the format is described with gdn_state_to_q8 below)
+__device__ __forceinline__ uint32_t pcg_hash(uint32_t v) {
+    const uint32_t state = v * 747796405u + 2891336453u;
+    const uint32_t word = ((state >> ((state >> 28u) + 4u)) ^ state) * 277803737u;
+    return (word >> 22u) ^ word;
+}
+
+template <int L>
+__device__ __forceinline__ float row_max(float v) {
+#pragma unroll
+    for (int o = L / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
 template <int DK, int DV>
+struct Q8Io {
+    static constexpr int LPR = DV / 4, RPP = 4 * DV / LPR, RPT = DK / RPP;
+    // encode: m (the thread's float4 of rows rg + x*RPP) -> codes, scales
+    static __device__ __forceinline__ void store(const float4 (&m)[RPT], int8_t *codes, float *scales,
+                                                 uint32_t hf, uint32_t base_idx, int rg, int c4,
+                                                 int lane) {
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+            const int row = rg + x * RPP;
+            const float amax = row_max<LPR>(fmaxf(fmaxf(fabsf(m[x].x), fabsf(m[x].y)),
+                                                  fmaxf(fabsf(m[x].z), fabsf(m[x].w))));
+            float inv = 0.f;   // 127 / max, divided once per row and broadcast from its first lane
+            if (lane % LPR == 0 && amax > 0.f) inv = __fdiv_rn(127.f, amax);
+            inv = __shfl_sync(0xffffffffu, inv, lane & ~(LPR - 1));
+            const float v[4] = {m[x].x, m[x].y, m[x].z, m[x].w};
+            // one hash per 4 codes: byte e of it is the dither of code e, u = (2 byte + 1) / 512
+            const uint32_t r = pcg_hash(((base_idx + (uint32_t)(row * DV + c4)) >> 2) ^ hf);
+            char4 c;
+            signed char cc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float u = (float)(2u * ((r >> (8 * e)) & 0xFFu) + 1u) * (1.0f / 512.0f);
+                float q = floorf(__fadd_rn(__fmul_rn(v[e], inv), u));
+                q = fminf(fmaxf(q, -127.f), 127.f);
+                cc[e] = amax > 0.f ? (signed char)(int)q : (signed char)0;
+            }
+            c.x = cc[0]; c.y = cc[1]; c.z = cc[2]; c.w = cc[3];
+            *reinterpret_cast<char4 *>(codes + row * DV + c4) = c;
+            if (lane % LPR == 0) scales[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+        }
+    }
+    // decode: codes, scales -> m
+    static __device__ __forceinline__ void load(float4 (&m)[RPT], const int8_t *codes, const float *scales,
+                                                int rg, int c4) {
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+            const int row = rg + x * RPP;
+            const char4 c = *reinterpret_cast<const char4 *>(codes + row * DV + c4);
+            const float s = scales[row];
+            m[x] = make_float4(__fmul_rn((float)c.x, s), __fmul_rn((float)c.y, s),
+                               __fmul_rn((float)c.z, s), __fmul_rn((float)c.w, s));
+        }
+    }
+};
+
+template <int DK, int DV, bool Q8 = false>
 struct StreamCfg {
     static constexpr int NT = 4 * DV;
     static constexpr int LPR = DV / 4, RPP = NT / LPR, RPT = DK / RPP;
-    static constexpr int SLOT = DK * DV * 4;                        // bytes of one head state
+    // bytes of one head state: fp32 M, or int8 codes followed by the fp32 row scales
+    static constexpr int SLOT = Q8 ? DK * DV + DK * 4 : DK * DV * 4;
     static constexpr int NS = SLOT >= 65536 ? 3 : (SLOT >= 16384 ? 8 : 16);
     static constexpr int CHUNK = SLOT < 16384 ? SLOT : 16384;       // bytes per bulk copy
     static constexpr int HB = 4;                                    // heads per record batch
@@ -279,36 +341,36 @@ struct StreamCfg {
 };
 
 // Every array read or written as float4 is 16-byte aligned explicitly.
-template <int DK, int DV>
+template <int DK, int DV, bool Q8 = false>
 struct StreamTail {
-    alignas(16) uint64_t full[StreamCfg<DK, DV>::NS];
+    alignas(16) uint64_t full[StreamCfg<DK, DV, Q8>::NS];
     alignas(16) uint64_t rfull[2];
-    alignas(16) float rec[2][StreamCfg<DK, DV>::RECBUF];   // records of the current / next batch
-    alignas(16) float red_p[StreamCfg<DK, DV>::RPP][DV];
-    alignas(16) float red_s[StreamCfg<DK, DV>::RPP][DV];
+    alignas(16) float rec[2][StreamCfg<DK, DV, Q8>::RECBUF];   // records of the current / next batch
+    alignas(16) float red_p[StreamCfg<DK, DV, Q8>::RPP][DV];
+    alignas(16) float red_s[StreamCfg<DK, DV, Q8>::RPP][DV];
     alignas(16) float up[DV];
     alignas(16) float nw[DV];
     float npart[4];
     int rec_bad;
 };
 
-template <int DK, int DV>
+template <int DK, int DV, bool Q8 = false>
 constexpr size_t stream_smem_bytes() {
-    return (size_t)StreamCfg<DK, DV>::NS * StreamCfg<DK, DV>::SLOT + sizeof(StreamTail<DK, DV>);
+    return (size_t)StreamCfg<DK, DV, Q8>::NS * StreamCfg<DK, DV, Q8>::SLOT + sizeof(StreamTail<DK, DV, Q8>);
 }
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
-template <int DK, int DV, typename TOut>
+template <int DK, int DV, typename TOut, bool Q8 = false>
 __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) {
-    using Cfg = StreamCfg<DK, DV>;
+    using Cfg = StreamCfg<DK, DV, Q8>;
     constexpr int NT = Cfg::NT, LPR = Cfg::LPR, RPP = Cfg::RPP, RPT = Cfg::RPT, NS = Cfg::NS;
     constexpr int HB = Cfg::HB;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float *slots = reinterpret_cast<float *>(smem_raw);
-    StreamTail<DK, DV> &tl = *reinterpret_cast<StreamTail<DK, DV> *>(smem_raw + NS * Cfg::SLOT);
+    StreamTail<DK, DV, Q8> &tl = *reinterpret_cast<StreamTail<DK, DV, Q8> *>(smem_raw + NS * Cfg::SLOT);
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -322,6 +384,7 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
     const int n_batches = (n_items + HB - 1) / HB;
     TOut *out = (TOut *)a.out;
     const int rg = tid / LPR, c4 = (tid % LPR) * 4;
+    const uint32_t hframe = Q8 ? pcg_hash(a.frame) : 0u;   // keys the Q8 rounding dither
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) tc::mbar_init(tc::smem_u32(&tl.full[s]), 1);
@@ -342,11 +405,16 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
             tc::mbar_arrive(mb);
             return;
         }
-        const char *src = reinterpret_cast<const char *>(
-            a.state + ((long long)slot * d.hv + (long long)kh * G + gi) * DK * DV);
+        const long long head = (long long)slot * d.hv + (long long)kh * G + gi;
         const uint32_t dst = tc::smem_u32(slots) + (uint32_t)((it % NS) * Cfg::SLOT);
         tc::mbar_arrive_expect_tx(mb, Cfg::SLOT);
-        for (int c = 0; c < Cfg::SLOT; c += Cfg::CHUNK) tc::bulk_g2s(dst + c, src + c, Cfg::CHUNK, mb);
+        if constexpr (Q8) {   // the codes, then the row scales
+            tc::bulk_g2s(dst, a.q8 + head * DK * DV, DK * DV, mb);
+            tc::bulk_g2s(dst + DK * DV, a.q8_scale + head * DK, DK * 4, mb);
+        } else {
+            const char *src = reinterpret_cast<const char *>(a.state + head * DK * DV);
+            for (int c = 0; c < Cfg::SLOT; c += Cfg::CHUNK) tc::bulk_g2s(dst + c, src + c, Cfg::CHUNK, mb);
+        }
     };
     // producer (thread 0): bulk-load the records of batch bb into buffer bb & 1
     auto issue_rec = [&](int bb) {
@@ -401,14 +469,22 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
             timed_out = true;
             set_error(a.err, GDN_DEVERR_TIMEOUT);
         }
-        const float *Ms = slots + (it % NS) * (DK * DV);
+        const unsigned char *Sb = reinterpret_cast<const unsigned char *>(slots) + (it % NS) * Cfg::SLOT;
         float4 m[RPT];
         float kr[RPT];
         if (slot >= 0) {
             float qr[RPT];
+            if constexpr (Q8) {
+                Q8Io<DK, DV>::load(m, reinterpret_cast<const int8_t *>(Sb),
+                                   reinterpret_cast<const float *>(Sb + DK * DV), rg, c4);
+            } else {
+#pragma unroll
+                for (int x = 0; x < RPT; ++x)
+                    m[x] = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(Sb) +
+                                                             (rg + x * RPP) * DV + c4);
+            }
 #pragma unroll
             for (int x = 0; x < RPT; ++x) {
-                m[x] = *reinterpret_cast<const float4 *>(Ms + (rg + x * RPP) * DV + c4);
                 kr[x] = rc[R.k + rg + x * RPP];
                 qr[x] = rc[R.q + rg + x * RPP];
             }
@@ -445,16 +521,23 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
         }
         __syncthreads();  // (B)
         {
-            float *Mg = a.state + ((long long)slot * d.hv + h) * DK * DV;
+            const long long head = (long long)slot * d.hv + h;
             const float4 u4 = *reinterpret_cast<const float4 *>(&tl.up[c4]);
 #pragma unroll
             for (int x = 0; x < RPT; ++x) {
-                float4 mn;
-                mn.x = ga * m[x].x + kr[x] * u4.x;
-                mn.y = ga * m[x].y + kr[x] * u4.y;
-                mn.z = ga * m[x].z + kr[x] * u4.z;
-                mn.w = ga * m[x].w + kr[x] * u4.w;
-                *reinterpret_cast<float4 *>(Mg + (long long)(rg + x * RPP) * DV + c4) = mn;
+                m[x].x = ga * m[x].x + kr[x] * u4.x;
+                m[x].y = ga * m[x].y + kr[x] * u4.y;
+                m[x].z = ga * m[x].z + kr[x] * u4.z;
+                m[x].w = ga * m[x].w + kr[x] * u4.w;
+            }
+            if constexpr (Q8) {
+                Q8Io<DK, DV>::store(m, a.q8 + head * DK * DV, a.q8_scale + head * DK, hframe,
+                                    (uint32_t)(head * DK * DV), rg, c4, lane);
+            } else {
+                float *Mg = a.state + head * DK * DV;
+#pragma unroll
+                for (int x = 0; x < RPT; ++x)
+                    *reinterpret_cast<float4 *>(Mg + (long long)(rg + x * RPP) * DV + c4) = m[x];
             }
         }
         if (tid < DV) {   // gated RMSNorm of this head's o, among the DV threads that hold it
@@ -471,14 +554,14 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
     }
 }
 
-template <int DK, int DV, typename TA, typename TOut>
+template <int DK, int DV, typename TA, typename TOut, bool Q8 = false>
 static cudaError_t launch_stream_t(const DecodeArgs &a, cudaStream_t s) {
     const int units = a.n * a.d.hk;
     decode_prep_kernel<DK, DV, TA><<<units, 256, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto kern = decode_stream_kernel<DK, DV, TOut>;
-    constexpr size_t smem = stream_smem_bytes<DK, DV>();
+    auto kern = decode_stream_kernel<DK, DV, TOut, Q8>;
+    constexpr size_t smem = stream_smem_bytes<DK, DV, Q8>();
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // programmatic dependent launch: overlaps this kernel's launch and its
@@ -551,62 +634,6 @@ namespace gdn {
 
 namespace {
 
-__device__ __forceinline__ uint32_t pcg_hash(uint32_t v) {
-    const uint32_t state = v * 747796405u + 2891336453u;
-    const uint32_t word = ((state >> ((state >> 28u) + 4u)) ^ state) * 277803737u;
-    return (word >> 22u) ^ word;
-}
-
-template <int L>
-__device__ __forceinline__ float row_max(float v) {
-#pragma unroll
-    for (int o = L / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-template <int DK, int DV>
-struct Q8Io {
-    static constexpr int LPR = DV / 4, RPP = 4 * DV / LPR, RPT = DK / RPP;
-    // encode: m (the thread's float4 of rows rg + x*RPP) -> codes, scales
-    static __device__ __forceinline__ void store(const float4 (&m)[RPT], int8_t *codes, float *scales,
-                                                 uint32_t hf, uint32_t base_idx, int rg, int c4,
-                                                 int lane) {
-#pragma unroll
-        for (int x = 0; x < RPT; ++x) {
-            const int row = rg + x * RPP;
-            const float amax = row_max<LPR>(fmaxf(fmaxf(fabsf(m[x].x), fabsf(m[x].y)),
-                                                  fmaxf(fabsf(m[x].z), fabsf(m[x].w))));
-            const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
-            const float v[4] = {m[x].x, m[x].y, m[x].z, m[x].w};
-            char4 c;
-            signed char cc[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t idx = base_idx + (uint32_t)(row * DV + c4 + e);
-                const float u = (float)(pcg_hash(idx ^ hf) >> 8) * (1.0f / 16777216.0f);
-                float q = floorf(__fadd_rn(__fmul_rn(v[e], inv), u));
-                q = fminf(fmaxf(q, -127.f), 127.f);
-                cc[e] = amax > 0.f ? (signed char)(int)q : (signed char)0;
-            }
-            c.x = cc[0]; c.y = cc[1]; c.z = cc[2]; c.w = cc[3];
-            *reinterpret_cast<char4 *>(codes + row * DV + c4) = c;
-            if (lane % LPR == 0) scales[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
-        }
-    }
-    // decode: codes, scales -> m
-    static __device__ __forceinline__ void load(float4 (&m)[RPT], const int8_t *codes, const float *scales,
-                                                int rg, int c4) {
-#pragma unroll
-        for (int x = 0; x < RPT; ++x) {
-            const int row = rg + x * RPP;
-            const char4 c = *reinterpret_cast<const char4 *>(codes + row * DV + c4);
-            const float s = scales[row];
-            m[x] = make_float4(__fmul_rn((float)c.x, s), __fmul_rn((float)c.y, s),
-                               __fmul_rn((float)c.z, s), __fmul_rn((float)c.w, s));
-        }
-    }
-};
-
 // fp32 pool <-> Q8 pool, one CTA per (slot, head)
 template <int DK, int DV>
 __global__ void __launch_bounds__(4 * DV) q8_convert_kernel(Dims d, const float *state, int8_t *codes,
@@ -632,91 +659,9 @@ __global__ void __launch_bounds__(4 * DV) q8_convert_kernel(Dims d, const float 
     }
 }
 
-// The one-token update on a Q8 state: one CTA per (sequence, v-head), after decode_prep_kernel
-// has written the unit records (the same ones the fp32 streaming kernel reads).
-template <int DK, int DV, typename TOut>
-__global__ void __launch_bounds__(4 * DV, 2) decode_q8_kernel(DecodeArgs a) {
-    using Q = Q8Io<DK, DV>;
-    constexpr int NT = 4 * DV, LPR = Q::LPR, RPP = Q::RPP, RPT = Q::RPT;
-    __shared__ __align__(16) float red_p[RPP][DV];
-    __shared__ __align__(16) float red_s[RPP][DV];
-    __shared__ __align__(16) float up[DV];
-    __shared__ float npart[DV / 32];
-    const Dims &d = a.d;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int G = d.grp, n = blockIdx.x / d.hv, h = blockIdx.x % d.hv, kh = h / G, gi = h % G;
-    const DecRec R(DK, DV, G);
-    const float *rc = a.ws + (long long)(n * d.hk + kh) * R.size;
-    TOut *out = (TOut *)a.out;
-    const long long orow = (long long)n * d.hv * DV + (long long)h * DV;
-    const int slot = __float_as_int(rc[R.slot]);
-    if (slot < 0 || slot >= d.n_slots) {      // padding lane
-        for (int j = tid; j < DV; j += NT) out[orow + j] = from_f32<TOut>(0.f);
-        return;
-    }
-    const int rg = tid / LPR, c4 = (tid % LPR) * 4;
-    const long long head = (long long)slot * d.hv + h;
-    int8_t *cp = a.q8 + head * DK * DV;
-    float *sp = a.q8_scale + head * DK;
-    float4 m[RPT];
-    Q::load(m, cp, sp, rg, c4);
-    float kr[RPT], qr[RPT];
-#pragma unroll
-    for (int x = 0; x < RPT; ++x) {
-        kr[x] = rc[R.k + rg + x * RPP];
-        qr[x] = rc[R.q + rg + x * RPP];
-    }
-    float4 pp = make_float4(0.f, 0.f, 0.f, 0.f), ss = pp;
-#pragma unroll
-    for (int x = 0; x < RPT; ++x) {
-        pp.x += m[x].x * kr[x]; pp.y += m[x].y * kr[x]; pp.z += m[x].z * kr[x]; pp.w += m[x].w * kr[x];
-        ss.x += m[x].x * qr[x]; ss.y += m[x].y * qr[x]; ss.z += m[x].z * qr[x]; ss.w += m[x].w * qr[x];
-    }
-    *reinterpret_cast<float4 *>(&red_p[rg][c4]) = pp;
-    *reinterpret_cast<float4 *>(&red_s[rg][c4]) = ss;
-    __syncthreads();
-    const float ga = rc[R.ga + gi], gb = rc[R.gb + gi];
-    float ov = 0.f;
-    if (tid < DV) {
-        float p = 0.f, s2 = 0.f;
-#pragma unroll
-        for (int r = 0; r < RPP; ++r) {
-            p += red_p[r][tid];
-            s2 += red_s[r][tid];
-        }
-        const float uu = gb * (rc[R.v + gi * DV + tid] - ga * p);
-        up[tid] = uu;
-        ov = ga * s2 + uu * rc[R.kq];
-    }
-    __syncthreads();
-    {
-        const float4 u4 = *reinterpret_cast<const float4 *>(&up[c4]);
-#pragma unroll
-        for (int x = 0; x < RPT; ++x) {
-            m[x].x = ga * m[x].x + kr[x] * u4.x; m[x].y = ga * m[x].y + kr[x] * u4.y;
-            m[x].z = ga * m[x].z + kr[x] * u4.z; m[x].w = ga * m[x].w + kr[x] * u4.w;
-        }
-        Q::store(m, cp, sp, pcg_hash(a.frame), (uint32_t)(head * DK * DV), rg, c4, lane);
-    }
-    if (tid < DV) {   // gated RMSNorm of this head's o
-        const float sq = warp_sum(ov * ov);
-        if (lane == 0) npart[warp] = sq;
-        asm volatile("bar.sync 1, %0;" :: "r"(DV) : "memory");
-        float tot = 0.f;
-#pragma unroll
-        for (int wi = 0; wi < DV / 32; ++wi) tot += npart[wi];
-        const float rs = rsqrtf(tot / (float)DV + d.norm_eps);
-        out[orow + tid] = from_f32<TOut>(ov * rs * a.norm_w[tid] * rc[R.z + gi * DV + tid]);
-    }
-}
-
 template <int D, typename TA, typename TOut>
 cudaError_t launch_q8_t(const DecodeArgs &a, cudaStream_t s) {
-    decode_prep_kernel<D, D, TA><<<a.n * a.d.hk, 256, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    decode_q8_kernel<D, D, TOut><<<a.n * a.d.hv, 4 * D, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_stream_t<D, D, TA, TOut, true>(a, s);   // prep + the streaming kernel on Q8 slots
 }
 
 template <int D>

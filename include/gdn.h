@@ -225,10 +225,12 @@ gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void 
  * per state row, [n_slots][HV][dk] (the row of dk index i holds M[i][0..dv)),
  * so M[i][j] = code[i][j] * scale[i]: about 4x fewer state bytes per decode
  * step.  The state is encoded with stochastic rounding: scale = max_j |M_ij| /
- * 127, code = clamp(floor(M_ij * (127 / max) + u), -127, 127), u in [0, 1)
- * from a counter-based hash of (frame, slot, head, i, j) (the PCG hash of
- * Jarzynski and Olano, JCGT 2020), every step an fp32 operation rounded to
- * nearest.  The rounding error then has zero mean, so it does not build up a
+ * 127, code = clamp(floor(M_ij * (127 / max) + u), -127, 127), every step an
+ * fp32 operation rounded to nearest.  The dither u = (2 b + 1) / 512 takes
+ * its byte b from a counter-based hash: with e = ((slot * HV + head) * dk +
+ * i) * dv + j (uint32), code e uses byte e & 3 of
+ * pcg_hash((e >> 2) ^ pcg_hash(frame)), pcg_hash being the PCG hash of
+ * Jarzynski and Olano (JCGT 2020).  The rounding error then has zero mean, so it does not build up a
  * bias over many steps: the error feedback the pages ask of a quantised state
  * (hyperflare release notes: a DeltaNet Q8 state whose dither is keyed by a
  * frame counter).  The caller passes a new frame every step.

@@ -316,14 +316,17 @@ def pcg_hash(v):
 
 
 def q8_dither(frame, slot, HV, h, dk, dv):
-    """The rounding offsets u in [0, 1) of one head's [dk, dv] codes at a given frame: 24 bits of
-    pcg_hash(index ^ pcg_hash(frame)), index = ((slot*HV + h)*dk + i)*dv + j (uint32)."""
+    """The rounding offsets u in (0, 1) of one head's [dk, dv] codes at a given frame.  With
+    index = ((slot*HV + h)*dk + i)*dv + j (uint32), the codes come in groups of four
+    consecutive indices; group g = index >> 2 draws r = pcg_hash(g ^ pcg_hash(frame)), and code
+    index & 3 = e takes byte e of r: u = (2 * byte + 1) / 512 (the midpoints of 256 cells)."""
     i = np.arange(dk, dtype=np.uint64)[:, None]
     j = np.arange(dv, dtype=np.uint64)[None, :]
     idx = ((((np.uint64(slot) * np.uint64(HV) + np.uint64(h)) * np.uint64(dk) + i) * np.uint64(dv) + j)
            & np.uint64(0xFFFFFFFF)).astype(np.uint32)
-    r = pcg_hash(idx ^ pcg_hash(np.uint32(frame)))
-    return (r >> np.uint32(8)).astype(np.float32) * np.float32(1.0 / 16777216.0)
+    r = pcg_hash((idx >> np.uint32(2)) ^ pcg_hash(np.uint32(frame)))
+    byte = (r >> (np.uint32(8) * (idx & np.uint32(3)))) & np.uint32(0xFF)
+    return (np.uint32(2) * byte + np.uint32(1)).astype(np.float32) * np.float32(1.0 / 512.0)
 
 
 def q8_encode_head(M, frame, slot, HV, h):

@@ -486,11 +486,12 @@ def test_q8_encoding_rules():
 
 
 def test_q8_dither_uniform_and_rounding_unbiased():
-    """The dither is uniform on [0, 1) (16-bin counts within 5 sigma over 65,536 draws); the
+    """The dither takes the 256 cell midpoints of (0, 1), uniformly (16-bin counts within 5 sigma
+    over 65,536 draws); the
     stochastic rounding is unbiased: the decoded value averaged over 400 frames sits within a
     few standard errors of the input."""
     u = np.concatenate([oracle.q8_dither(f, 0, 4, 1, 64, 64).ravel() for f in range(16)])
-    assert u.min() >= 0 and u.max() < 1
+    assert u.min() > 0 and u.max() < 1 and len(np.unique(u)) == 256
     counts = np.histogram(u, bins=16, range=(0, 1))[0]
     expect = u.size / 16
     assert np.all(np.abs(counts - expect) <= 5 * np.sqrt(expect))
