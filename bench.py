@@ -473,9 +473,9 @@ def bench_decode_q8(args, dev, gdn, pk, pk_src):
     return {"workload": "decode_64x256 with a Q8 state (int8 codes + fp32 row scales, 16.5 KiB per "
                         "head), %d steps, L2 evicted between steps" % S,
             "value": gbs, "unit": "GB/s", "us_per_step": per * 1e6, "state_bytes_per_step": q8_bytes,
-            "roofline": {"kernel": "decode_prep_kernel + decode_q8_kernel", "bound": "hbm",
+            "roofline": {"kernel": "decode_prep_kernel + decode_stream_kernel (Q8 slots)", "bound": "hbm",
                          "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "frac": gbs / pk["hbm_gbs"], "traffic": traffic_for("decode_64x256_q8"),
                          "peak_source": pk_src + " copy"},
             "gpu_launches": 2 * S}
 
