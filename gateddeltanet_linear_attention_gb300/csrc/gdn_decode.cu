@@ -283,17 +283,76 @@ template <int DK, int DV>
 struct Q8Io {
     static constexpr int LPR = DV / 4, RPP = 4 * DV / LPR, RPT = DK / RPP;
     // encode: m (the thread's float4 of rows rg + x*RPP) -> codes, scales
+    // Row maxima and 127 / max of the thread's RPT rows.  With a warp per row (LPR = 32) the
+    // 8 rows reduce in one butterfly that halves the rows a lane carries at every stage (9
+    // shuffles instead of 40), lane groups of 4 then hold one row each and divide once per
+    // row, and the results come back by shuffle; the values are the same as row by row.
+    // my_x / my_scale: with LPR = 32, the row (index x) whose scale this lane stores (lanes with
+    // lane % 4 == 0), else -1
+    static __device__ __forceinline__ void row_stats(const float4 (&m)[RPT], int lane,
+                                                     float (&amax)[RPT], float (&inv)[RPT],
+                                                     int &my_x, float &my_scale) {
+        my_x = -1;
+        my_scale = 0.f;
+        float v[RPT];
+#pragma unroll
+        for (int x = 0; x < RPT; ++x)
+            v[x] = fmaxf(fmaxf(fabsf(m[x].x), fabsf(m[x].y)), fmaxf(fabsf(m[x].z), fabsf(m[x].w)));
+        if constexpr (LPR == 32 && RPT == 8) {
+            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+            float w4[4], w2[2];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float send = b4 ? v[k] : v[k + 4], keep = b4 ? v[k + 4] : v[k];
+                w4[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float send = b3 ? w4[k] : w4[k + 2], keep = b3 ? w4[k + 2] : w4[k];
+                w2[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+            }
+            float w1;
+            {
+                const float send = b2 ? w2[0] : w2[1], keep = b2 ? w2[1] : w2[0];
+                w1 = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+            }
+            w1 = fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 2));
+            w1 = fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 1));
+            // this lane now holds the max of row x = 4 b4 + 2 b3 + b2
+            const float iv = w1 > 0.f ? __fdiv_rn(127.f, w1) : 0.f;
+            if ((lane & 3) == 0) {
+                my_x = (b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0);
+                my_scale = w1 > 0.f ? __fdiv_rn(w1, 127.f) : 0.f;
+            }
+#pragma unroll
+            for (int x = 0; x < RPT; ++x) {
+                const int src = ((x >> 2) & 1) * 16 + ((x >> 1) & 1) * 8 + (x & 1) * 4;
+                amax[x] = __shfl_sync(0xffffffffu, w1, src);
+                inv[x] = __shfl_sync(0xffffffffu, iv, src);
+            }
+        } else {
+#pragma unroll
+            for (int x = 0; x < RPT; ++x) {
+                amax[x] = row_max<LPR>(v[x]);
+                float iv = 0.f;   // divided once per row and broadcast from its first lane
+                if (lane % LPR == 0 && amax[x] > 0.f) iv = __fdiv_rn(127.f, amax[x]);
+                inv[x] = __shfl_sync(0xffffffffu, iv, lane & ~(LPR - 1));
+            }
+        }
+    }
     static __device__ __forceinline__ void store(const float4 (&m)[RPT], int8_t *codes, float *scales,
                                                  uint32_t hf, uint32_t base_idx, int rg, int c4,
                                                  int lane) {
+        float amaxs[RPT], invs[RPT], my_scale;
+        int my_x;
+        row_stats(m, lane, amaxs, invs, my_x, my_scale);
+        if constexpr (LPR == 32 && RPT == 8) {
+            if (my_x >= 0) scales[rg + my_x * RPP] = my_scale;
+        }
 #pragma unroll
         for (int x = 0; x < RPT; ++x) {
             const int row = rg + x * RPP;
-            const float amax = row_max<LPR>(fmaxf(fmaxf(fabsf(m[x].x), fabsf(m[x].y)),
-                                                  fmaxf(fabsf(m[x].z), fabsf(m[x].w))));
-            float inv = 0.f;   // 127 / max, divided once per row and broadcast from its first lane
-            if (lane % LPR == 0 && amax > 0.f) inv = __fdiv_rn(127.f, amax);
-            inv = __shfl_sync(0xffffffffu, inv, lane & ~(LPR - 1));
+            const float amax = amaxs[x], inv = invs[x];
             const float v[4] = {m[x].x, m[x].y, m[x].z, m[x].w};
             // one hash per 4 codes: byte e of it is the dither of code e, u = (2 byte + 1) / 512
             const uint32_t r = pcg_hash(((base_idx + (uint32_t)(row * DV + c4)) >> 2) ^ hf);
@@ -301,14 +360,18 @@ struct Q8Io {
             signed char cc[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float u = (float)(2u * ((r >> (8 * e)) & 0xFFu) + 1u) * (1.0f / 512.0f);
-                float q = floorf(__fadd_rn(__fmul_rn(v[e], inv), u));
-                q = fminf(fmaxf(q, -127.f), 127.f);
-                cc[e] = amax > 0.f ? (signed char)(int)q : (signed char)0;
+                // u = (2 byte + 1) / 512, formed exactly as (1 + u) - 1 from its bit pattern (no
+                // int -> float conversion); floor and the conversion in one rounding-down convert
+                const uint32_t b2 = 2u * ((r >> (8 * e)) & 0xFFu) + 1u;
+                const float u = __int_as_float(0x3F800000u | (b2 << 14)) - 1.0f;
+                int q = __float2int_rd(__fadd_rn(__fmul_rn(v[e], inv), u));
+                q = min(max(q, -127), 127);
+                cc[e] = amax > 0.f ? (signed char)q : (signed char)0;
             }
             c.x = cc[0]; c.y = cc[1]; c.z = cc[2]; c.w = cc[3];
             *reinterpret_cast<char4 *>(codes + row * DV + c4) = c;
-            if (lane % LPR == 0) scales[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+            if constexpr (!(LPR == 32 && RPT == 8))
+                if (lane % LPR == 0) scales[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
         }
     }
     // decode: codes, scales -> m
@@ -319,8 +382,12 @@ struct Q8Io {
             const int row = rg + x * RPP;
             const char4 c = *reinterpret_cast<const char4 *>(codes + row * DV + c4);
             const float s = scales[row];
-            m[x] = make_float4(__fmul_rn((float)c.x, s), __fmul_rn((float)c.y, s),
-                               __fmul_rn((float)c.z, s), __fmul_rn((float)c.w, s));
+            // code c (|c| <= 127) as a float without a conversion: 2^23 + (c + 128), minus 2^23 + 128
+            auto cf = [](signed char v) {
+                return __int_as_float(0x4B000000u | (uint32_t)((int)v + 128)) - 8388736.0f;
+            };
+            m[x] = make_float4(__fmul_rn(cf(c.x), s), __fmul_rn(cf(c.y), s), __fmul_rn(cf(c.z), s),
+                               __fmul_rn(cf(c.w), s));
         }
     }
 };
