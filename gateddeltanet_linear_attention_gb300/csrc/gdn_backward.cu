@@ -58,68 +58,92 @@ __device__ __forceinline__ float row_sum(float v) {
 }
 
 // Per-token inputs of one v-head staged in shared memory.
-// Every array read or written as float4 (dout, w, dp, red) is 16-byte aligned explicitly.
+// One token's inputs in shared memory (double-buffered: the next token's are stored while this
+// one's are read).  Every array read or written as float4 is 16-byte aligned explicitly.
 template <int DK, int DV>
-struct TokSmem {
+struct TokIn {
     alignas(16) float q[DK];
     alignas(16) float k[DK];
     alignas(16) float v[DV];
     alignas(16) float dout[DV];
+    float a, b;
+};
+template <int DK, int DV>
+struct TokSmem {
+    TokIn<DK, DV> in[2];
     alignas(16) float p[DV];
     alignas(16) float r[DV];
     alignas(16) float w[DV];
     alignas(16) float dp[DV];
     alignas(16) float red[BwdCfg<DK, DV>::RPP][DV];
     float wsum[3][BwdCfg<DK, DV>::NT / 32];
-    float a, b;
+};
+
+// A thread's share of one token's inputs, loaded into registers ahead of use: k and q for
+// tid < DK, v and do for tid < DV, a and beta for thread 0.
+struct TokReg {
+    float k, q, v, dout, a, b;
 };
 
 // The forward step of one token on M in registers: p = M^T k (column sums), w, M <- a M + k w^T.
-template <int DK, int DV>
+// `after_first_barrier` runs once every thread is past the first barrier (the other input
+// buffer is free then).
+template <int DK, int DV, typename F>
 __device__ __forceinline__ void fwd_token(float4 (&m)[BwdCfg<DK, DV>::RPT], TokSmem<DK, DV> &sm,
-                                          int tid, int rg, int c4) {
+                                          const TokIn<DK, DV> &in, int tid, int rg, int c4,
+                                          F after_first_barrier) {
     using C = BwdCfg<DK, DV>;
     float4 pp = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int x = 0; x < C::RPT; ++x) {
-        const float kr = sm.k[rg + x * C::RPP];
+        const float kr = in.k[rg + x * C::RPP];
         pp.x += m[x].x * kr; pp.y += m[x].y * kr; pp.z += m[x].z * kr; pp.w += m[x].w * kr;
     }
     *reinterpret_cast<float4 *>(&sm.red[rg][c4]) = pp;
     __syncthreads();
+    after_first_barrier();
     if (tid < DV) {
         float p = 0.f;
 #pragma unroll
         for (int r = 0; r < C::RPP; ++r) p += sm.red[r][tid];
-        sm.w[tid] = sm.b * (sm.v[tid] - sm.a * p);
+        sm.w[tid] = in.b * (in.v[tid] - in.a * p);
     }
     __syncthreads();
     const float4 w4 = *reinterpret_cast<const float4 *>(&sm.w[c4]);
-    const float a = sm.a;
+    const float a = in.a;
 #pragma unroll
     for (int x = 0; x < C::RPT; ++x) {
-        const float kr = sm.k[rg + x * C::RPP];
+        const float kr = in.k[rg + x * C::RPP];
         m[x].x = a * m[x].x + kr * w4.x; m[x].y = a * m[x].y + kr * w4.y;
         m[x].z = a * m[x].z + kr * w4.z; m[x].w = a * m[x].w + kr * w4.w;
     }
 }
 
-// Stage token t's q (optional), k, v, do (optional), a, beta of head h into shared memory.
+// Token t's q (optional), k, v, do (optional), a, beta of head h: the thread's share into
+// registers, and from there into an input buffer.
 template <int DK, int DV, typename TA>
-__device__ __forceinline__ void stage_token(const BwdArgs &a, TokSmem<DK, DV> &sm, long long t,
-                                            int h, int kh, int tid, bool with_q) {
+__device__ __forceinline__ TokReg load_token(const BwdArgs &a, long long t, int h, int kh, int tid,
+                                             bool with_q) {
+    TokReg r = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (tid < DK) {
-        sm.k[tid] = to_f32(((const TA *)a.k)[t * a.ld_qk + (long long)kh * DK + tid]);
-        if (with_q) sm.q[tid] = to_f32(((const TA *)a.q)[t * a.ld_qk + (long long)kh * DK + tid]);
+        r.k = to_f32(((const TA *)a.k)[t * a.ld_qk + (long long)kh * DK + tid]);
+        if (with_q) r.q = to_f32(((const TA *)a.q)[t * a.ld_qk + (long long)kh * DK + tid]);
     }
     if (tid < DV) {
-        sm.v[tid] = to_f32(((const TA *)a.v)[t * a.ld_v + (long long)h * DV + tid]);
-        if (with_q) sm.dout[tid] = a.d_o[t * (long long)a.d.hv * DV + (long long)h * DV + tid];
+        r.v = to_f32(((const TA *)a.v)[t * a.ld_v + (long long)h * DV + tid]);
+        if (with_q) r.dout = a.d_o[t * (long long)a.d.hv * DV + (long long)h * DV + tid];
     }
     if (tid == 0) {
-        sm.a = expf(a.g[t * a.d.hv + h]);
-        sm.b = a.beta[t * a.d.hv + h];
+        r.a = a.g[t * a.d.hv + h];
+        r.b = a.beta[t * a.d.hv + h];
     }
+    return r;
+}
+template <int DK, int DV>
+__device__ __forceinline__ void store_token(TokIn<DK, DV> &in, const TokReg &r, int tid) {
+    if (tid < DK) { in.k[tid] = r.k; in.q[tid] = r.q; }
+    if (tid < DV) { in.v[tid] = r.v; in.dout[tid] = r.dout; }
+    if (tid == 0) { in.a = expf(r.a); in.b = r.b; }
 }
 
 template <int DK, int DV, typename TA>
@@ -143,6 +167,8 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
                                                      (long long)(rg + x * C::RPP) * DV + c4);
     }
     const long long b0 = a.chunk_base[n];
+    store_token<DK, DV>(sm.in[0], load_token<DK, DV, TA>(a, s, h, kh, tid, false), tid);
+    __syncthreads();
     for (long long t = s; t < e; ++t) {
         if ((t - s) % Cc == 0) {
             float *B = a.bnd + ((b0 + (t - s) / Cc) * d.hv + h) * DK * DV;
@@ -150,10 +176,14 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
             for (int x = 0; x < C::RPT; ++x)
                 *reinterpret_cast<float4 *>(B + (long long)(rg + x * C::RPP) * DV + c4) = m[x];
         }
-        __syncthreads();                                 // the previous token's smem reads are done
-        stage_token<DK, DV, TA>(a, sm, t, h, kh, tid, false);
-        __syncthreads();
-        fwd_token<DK, DV>(m, sm, tid, rg, c4);
+        // token t+1's inputs load while token t runs; they go to the other buffer once it is free
+        const bool more = t + 1 < e;
+        TokReg nx = {};
+        if (more) nx = load_token<DK, DV, TA>(a, t + 1, h, kh, tid, false);
+        const int bi = (int)((t - s) & 1);
+        fwd_token<DK, DV>(m, sm, sm.in[bi], tid, rg, c4, [&] {
+            if (more) store_token<DK, DV>(sm.in[bi ^ 1], nx, tid);
+        });
     }
 }
 
@@ -204,57 +234,70 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
                 m[x] = *reinterpret_cast<const float4 *>(B + (long long)(rg + x * C::RPP) * DV + c4);
         }
         // forward through the chunk, keeping the state before every token (each thread
-        // reads back only what it wrote)
+        // reads back only what it wrote); token inputs double-buffered (buffer (t - t0) & 1)
+        __syncthreads();                                 // the previous chunk's buffer reads are done
+        if (t0 + 1 < t1) store_token<DK, DV>(sm.in[0], load_token<DK, DV, TA>(a, t0, h, kh, tid, false), tid);
+        __syncthreads();
         for (long long t = t0; t < t1; ++t) {
             float *Sc = scr + (t - t0) * DK * DV;
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x)
                 *reinterpret_cast<float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4) = m[x];
             if (t + 1 == t1) break;
-            __syncthreads();
-            stage_token<DK, DV, TA>(a, sm, t, h, kh, tid, false);
-            __syncthreads();
-            fwd_token<DK, DV>(m, sm, tid, rg, c4);
+            const bool more = t + 2 < t1;               // token t+1 updates the state too
+            TokReg nx = {};
+            if (more) nx = load_token<DK, DV, TA>(a, t + 1, h, kh, tid, false);
+            const int bi = (int)((t - t0) & 1);
+            fwd_token<DK, DV>(m, sm, sm.in[bi], tid, rg, c4, [&] {
+                if (more) store_token<DK, DV>(sm.in[bi ^ 1], nx, tid);
+            });
         }
-        // the tokens in reverse
+        // the tokens in reverse, inputs double-buffered (buffer (t - t0) & 1): token t-1's load
+        // while token t runs and are stored to the other buffer after barrier (A)
+        __syncthreads();                                 // the forward pass's buffer reads are done
+        store_token<DK, DV>(sm.in[(t1 - 1 - t0) & 1], load_token<DK, DV, TA>(a, t1 - 1, h, kh, tid, true), tid);
+        __syncthreads();
         for (long long t = t1 - 1; t >= t0; --t) {
             const float *Sc = scr + (t - t0) * DK * DV;
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x)
                 m[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4);
-            __syncthreads();                             // (E) the previous token's smem reads are done
-            stage_token<DK, DV, TA>(a, sm, t, h, kh, tid, true);
-            __syncthreads();
+            const int bi = (int)((t - t0) & 1);
+            const TokIn<DK, DV> &in = sm.in[bi];
+            const bool more = t - 1 >= t0;
+            TokReg nx = {};
+            if (more) nx = load_token<DK, DV, TA>(a, t - 1, h, kh, tid, true);
             // p = M^T k
             {
                 float4 pp = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int x = 0; x < C::RPT; ++x) {
-                    const float kr = sm.k[rg + x * C::RPP];
+                    const float kr = in.k[rg + x * C::RPP];
                     pp.x += m[x].x * kr; pp.y += m[x].y * kr; pp.z += m[x].z * kr; pp.w += m[x].w * kr;
                 }
                 *reinterpret_cast<float4 *>(&sm.red[rg][c4]) = pp;
             }
-            __syncthreads();                             // (A)
-            const float av = sm.a, bv = sm.b;
+            __syncthreads();                             // (A) the other buffer is free from here
+            if (more) store_token<DK, DV>(sm.in[bi ^ 1], nx, tid);
+            const float av = in.a, bv = in.b;
             if (tid < DV) {
                 float p = 0.f;
 #pragma unroll
                 for (int r = 0; r < C::RPP; ++r) p += sm.red[r][tid];
-                const float rr = sm.v[tid] - av * p;
+                const float rr = in.v[tid] - av * p;
                 sm.p[tid] = p;
                 sm.r[tid] = rr;
                 sm.w[tid] = bv * rr;
             }
             __syncthreads();                             // (B)
             const float4 w4 = *reinterpret_cast<const float4 *>(&sm.w[c4]);
-            const float4 do4 = *reinterpret_cast<const float4 *>(&sm.dout[c4]);
+            const float4 do4 = *reinterpret_cast<const float4 *>(&in.dout[c4]);
             float4 dwp = make_float4(0.f, 0.f, 0.f, 0.f);
             float dap = 0.f;
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x) {
                 const int row = rg + x * C::RPP;
-                const float kr = sm.k[row], qr = sm.q[row];
+                const float kr = in.k[row], qr = in.q[row];
                 float4 mp;                               // M' = a M + k w^T
                 mp.x = av * m[x].x + kr * w4.x; mp.y = av * m[x].y + kr * w4.y;
                 mp.z = av * m[x].z + kr * w4.z; mp.w = av * m[x].w + kr * w4.w;
@@ -291,7 +334,7 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x) {
                 const int row = rg + x * C::RPP;
-                const float kr = sm.k[row];
+                const float kr = in.k[row];
                 const float dk = row_sum<C::LPR>(gm[x].x * w4.x + gm[x].y * w4.y + gm[x].z * w4.z +
                                                  gm[x].w * w4.w + m[x].x * dp4.x + m[x].y * dp4.y +
                                                  m[x].z * dp4.z + m[x].w * dp4.w);
