@@ -51,7 +51,7 @@ cudaError_t launch_gate_prep(const Dims &d, bool act_bf16, const void *u, const 
 // Outputs only: the history is replaced afterwards by
 // conv_state_update_kernel, so no CTA can overwrite a history another CTA
 // still has to read.
-constexpr int CONV_TT = 32;
+constexpr int CONV_TT = 64;
 constexpr int CONV_B = 4;      // tokens whose loads are issued together
 constexpr int CONV_NT = 128;
 constexpr int CONV_V = 8;
