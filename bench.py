@@ -260,8 +260,9 @@ def run_ours(args, rank, ws, local):
                               state_out=state_out, conv_state=conv, workspace=wsp)
 
     tc_path = wl.act == "bf16" and wl.dk == 128 and wl.dv == 128 and wl.chunk == 64
-    # gate, conv, conv-history update, chunk map, [T;PT] kernel, chain (norm fused); SIMT: chunk + norm
-    launches_per_step = 6 if tc_path else 5
+    # conv (gates fused), conv-history update, chunk map, [T;PT] kernel, chain (norm fused);
+    # SIMT: conv, history update, chunk, norm
+    launches_per_step = 5 if tc_path else 4
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()

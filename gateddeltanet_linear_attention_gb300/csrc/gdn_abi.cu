@@ -364,12 +364,11 @@ gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void
         return GDN_ERR_WORKSPACE;
     if ((st = error_word(&err)) != GDN_OK) return st;
     PrefillWs w = carve_prefill(d, bf, io->T, io->n_seqs, workspace);
-    cudaError_t e = gdn::launch_gate_prep(d, bf, io->u, io->b_logit, io->ld_ub, io->T, io->A_log,
-                                          io->dt_bias, w.g, w.beta, s);
-    if (e == cudaSuccess)
-        e = gdn::launch_conv_prefill(d, bf, io->x, io->ld_x, io->cu_seqlens, io->n_seqs, io->T,
-                                     io->conv_w, io->conv_state, io->state_idx, w.xa, false, err,
-                                     s);
+    // the gates come out of the conv kernel (one launch fewer)
+    const gdn::GateArgs ga = {io->u, io->b_logit, io->ld_ub, io->A_log, io->dt_bias, w.g, w.beta};
+    cudaError_t e = gdn::launch_conv_prefill(d, bf, io->x, io->ld_x, io->cu_seqlens, io->n_seqs,
+                                             io->T, io->conv_w, io->conv_state, io->state_idx,
+                                             w.xa, false, err, s, &ga);
     if (e == cudaSuccess)
         e = gdn::launch_conv_state_update(d, bf, io->x, io->ld_x, io->cu_seqlens, io->n_seqs,
                                           io->T, io->conv_state, io->state_idx, err, s);

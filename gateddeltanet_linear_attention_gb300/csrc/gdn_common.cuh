@@ -182,10 +182,19 @@ cudaError_t launch_verify(const DecodeArgs &a, bool in_bf16, bool out_bf16, cuda
 cudaError_t launch_gate_prep(const Dims &d, bool act_bf16, const void *u, const void *b,
                              long long ld_ub, long long T, const float *A_log,
                              const float *dt_bias, float *g, float *beta, cudaStream_t s);
+// Gates computed by the conv kernel (the mixer prefill): u, b_logit [T][ld_ub] in the activation
+// dtype; g, beta [T][HV] fp32.  g == nullptr: none.
+struct GateArgs {
+    const void *u, *b;
+    long long ld_ub;
+    const float *A_log, *dt_bias;
+    float *g, *beta;
+};
 cudaError_t launch_conv_prefill(const Dims &d, bool act_bf16, const void *x, long long ld_x,
                                 const int32_t *cu, int n_seqs, long long T, const void *w,
                                 const void *conv_state, const int32_t *state_idx, void *out,
-                                bool out_bf16, unsigned *err, cudaStream_t s);
+                                bool out_bf16, unsigned *err, cudaStream_t s,
+                                const GateArgs *gates = nullptr);
 // Snapshot / restore / reset of state slots (gdn_state_copy); the history
 // words per slot assume CH * 3 * element size is a multiple of 16 bytes.
 cudaError_t launch_state_copy(const Dims &d, bool act_bf16, const float *src_state,

@@ -85,9 +85,21 @@ template <typename TA, typename TO>
 __global__ void __launch_bounds__(CONV_NT, 4)
     conv_prefill_kernel(Dims d, const TA *x, long long ld_x, const int32_t *cu, int n_seqs,
                         long long T, const TA *w, const TA *conv_state,
-                        const int32_t *state_idx, TO *out, unsigned *err) {
+                        const int32_t *state_idx, TO *out, unsigned *err, GateArgs ga) {
     const int c0 = (blockIdx.y * CONV_NT + threadIdx.x) * CONV_V;
     const long long t0 = (long long)blockIdx.x * CONV_TT;
+    if (ga.g && blockIdx.y == 0 && t0 < T) {
+        // the gates of this CTA's tokens (the mixer prefill folds gate_prep_kernel in here):
+        // the same expressions, element for element
+        const long long tend = t0 + CONV_TT < T ? t0 + CONV_TT : T;
+        for (long long e = t0 * d.hv + threadIdx.x; e < tend * d.hv; e += CONV_NT) {
+            const long long t = e / d.hv;
+            const int h = (int)(e - t * d.hv);
+            const float uu = to_f32(((const TA *)ga.u)[t * ga.ld_ub + h]) + ga.dt_bias[h];
+            ga.g[e] = -expf(ga.A_log[h]) * softplus_f(uu);
+            ga.beta[e] = sigmoid_f(to_f32(((const TA *)ga.b)[t * ga.ld_ub + h]));
+        }
+    }
     if (c0 >= d.ch || t0 >= T) return;
     float wv[CONV_V][4];
     {
@@ -212,13 +224,14 @@ __global__ void conv_state_update_kernel(Dims d, const TA *x, long long ld_x, co
 cudaError_t launch_conv_prefill(const Dims &d, bool act_bf16, const void *x, long long ld_x,
                                 const int32_t *cu, int n_seqs, long long T, const void *w,
                                 const void *conv_state, const int32_t *state_idx, void *out,
-                                bool out_bf16, unsigned *err, cudaStream_t s) {
+                                bool out_bf16, unsigned *err, cudaStream_t s, const GateArgs *gates) {
+    const GateArgs ga = gates ? *gates : GateArgs{};
     if (T == 0 || n_seqs == 0) return cudaSuccess;
     dim3 grid((unsigned)((T + CONV_TT - 1) / CONV_TT), (d.ch + CONV_NT * CONV_V - 1) / (CONV_NT * CONV_V));
 #define GDN_CONV(TA, TO)                                                                   \
     conv_prefill_kernel<TA, TO><<<grid, CONV_NT, 0, s>>>(                                   \
         d, (const TA *)x, ld_x, cu, n_seqs, T, (const TA *)w, (const TA *)conv_state,       \
-        state_idx, (TO *)out, err)
+        state_idx, (TO *)out, err, ga)
     if (act_bf16) {
         if (out_bf16) GDN_CONV(__nv_bfloat16, __nv_bfloat16); else GDN_CONV(__nv_bfloat16, float);
     } else {
