@@ -316,26 +316,37 @@ def pcg_hash(v):
 
 
 def q8_dither(frame, slot, HV, h, dk, dv):
-    """The rounding offsets u in (0, 1) of one head's [dk, dv] codes at a given frame.  With
-    index = ((slot*HV + h)*dk + i)*dv + j (uint32), the codes come in groups of four
-    consecutive indices; group g = index >> 2 draws r = pcg_hash(g ^ pcg_hash(frame)), and code
-    index & 3 = e takes byte e of r: u = (2 * byte + 1) / 512 (the midpoints of 256 cells)."""
+    """The rounding offsets u in [0, 1) of one head's [dk, dv] codes at a given frame.  Every code
+    draws its own: with index = ((slot*HV + h)*dk + i)*dv + j (uint32) and
+    r = pcg_hash(index ^ pcg_hash(frame)), u = (r >> 8) * 2^-24 (24 bits, exact in fp32)."""
     i = np.arange(dk, dtype=np.uint64)[:, None]
     j = np.arange(dv, dtype=np.uint64)[None, :]
     idx = ((((np.uint64(slot) * np.uint64(HV) + np.uint64(h)) * np.uint64(dk) + i) * np.uint64(dv) + j)
            & np.uint64(0xFFFFFFFF)).astype(np.uint32)
-    r = pcg_hash((idx >> np.uint32(2)) ^ pcg_hash(np.uint32(frame)))
-    byte = (r >> (np.uint32(8) * (idx & np.uint32(3)))) & np.uint32(0xFF)
-    return (np.uint32(2) * byte + np.uint32(1)).astype(np.float32) * np.float32(1.0 / 512.0)
+    r = pcg_hash(idx ^ pcg_hash(np.uint32(frame)))
+    return (r >> np.uint32(8)).astype(np.float32) * np.float32(1.0 / 16777216.0)
 
 
-def q8_encode_head(M, frame, slot, HV, h):
+def bf16_round(x):
+    """fp32 -> the nearest bf16 value (ties to even), returned as fp32: the top 16 bits of the
+    fp32 pattern after adding 0x7FFF plus the lowest kept bit (finite inputs)."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)) << np.uint64(16)
+    return (r & np.uint64(0xFFFFFFFF)).astype(np.uint32).view(np.float32)
+
+
+def q8_encode_head(M, frame, slot, HV, h, residual=None):
     """One head's fp32 [dk, dv] state (M = S^T) to int8 codes and per-row scales, every step in
-    fp32 with round-to-nearest: absmax a_i of row i, scale s_i = a_i / 127, x = M * (127 / a_i),
-    code = clamp(floor(x + u), -127, 127) with the dither u of q8_dither (stochastic rounding:
-    the expected code is x, so the rounding error carries no bias from step to step).  A zero
-    row gets scale 0 and codes 0.  Returns (codes int8 [dk, dv], scales fp32 [dk])."""
+    fp32 with round-to-nearest.  The value encoded is x = M, or x = M + residual with error
+    feedback (residual: the bf16 [dk, dv] left by the previous encode).  Absmax a_i of row i of
+    x, scale s_i = a_i / 127, code = clamp(floor(x * (127 / a_i) + u), -127, 127) with the dither
+    u of q8_dither (stochastic rounding: the expected code is x * 127 / a_i).  A zero row gets
+    scale 0 and codes 0.  Returns (codes int8 [dk, dv], scales fp32 [dk]); with a residual also
+    the new residual bf16(x - code * s_i) (as fp32 values), the rounding error this encode
+    leaves for the next one."""
     M = np.asarray(M, dtype=np.float32)
+    if residual is not None:
+        M = (M + np.asarray(residual, dtype=np.float32)).astype(np.float32)
     dk, dv = M.shape
     amax = np.max(np.abs(M), axis=1).astype(np.float32)
     nz = amax > 0
@@ -348,19 +359,29 @@ def q8_encode_head(M, frame, slot, HV, h):
     c = np.floor((x + u).astype(np.float32))
     c = np.clip(c, -127, 127)
     c[~nz] = 0
-    return c.astype(np.int8), scale
+    codes = c.astype(np.int8)
+    if residual is None:
+        return codes, scale
+    back = (codes.astype(np.float32) * scale[:, None]).astype(np.float32)
+    return codes, scale, bf16_round((M - back).astype(np.float32))
 
 
-def q8_encode(state, frame):
-    """A whole fp32 pool [slots, HV, dk, dv] -> (codes int8, scales [slots, HV, dk])."""
+def q8_encode(state, frame, residual=None):
+    """A whole fp32 pool [slots, HV, dk, dv] -> (codes int8, scales [slots, HV, dk]), plus the
+    new residual pool when a residual pool (error feedback) is given."""
     state = np.asarray(state, dtype=np.float32)
     S, HV, dk, dv = state.shape
     codes = np.zeros(state.shape, np.int8)
     scales = np.zeros((S, HV, dk), np.float32)
+    res = None if residual is None else np.zeros(state.shape, np.float32)
     for s in range(S):
         for h in range(HV):
-            codes[s, h], scales[s, h] = q8_encode_head(state[s, h], frame, s, HV, h)
-    return codes, scales
+            if residual is None:
+                codes[s, h], scales[s, h] = q8_encode_head(state[s, h], frame, s, HV, h)
+            else:
+                codes[s, h], scales[s, h], res[s, h] = q8_encode_head(state[s, h], frame, s, HV, h,
+                                                                      residual[s, h])
+    return (codes, scales) if residual is None else (codes, scales, res)
 
 
 def q8_decode(codes, scales):
@@ -369,13 +390,18 @@ def q8_decode(codes, scales):
 
 
 def mixer_decode_q8(x, conv_w, u, b_logit, A_log, dt_bias, z, norm_w, HK, HV, dk, dv, codes, scales,
-                    conv_state, frame, slot_idx=None, q_scale=1.0, l2_eps=1e-6, norm_eps=1e-6):
+                    conv_state, frame, slot_idx=None, q_scale=1.0, l2_eps=1e-6, norm_eps=1e-6,
+                    residual=None):
     """One decode step (one token for each of n sequences) on a Q8 state pool: the state of
     each sequence's slot is dequantised, the plain mixer (fp64) runs one token, and the new
-    state is cast to fp32 and quantised again at `frame`.  Returns (y, codes, scales, conv)."""
+    state is cast to fp32 and quantised again at `frame`.  With a residual pool (error
+    feedback), the slot's residual is added to the new state before it is quantised and is
+    replaced by the rounding error of that encode; the recurrence itself reads only the
+    dequantised codes.  Returns (y, codes, scales, conv), plus the residual pool when given."""
     n = _f64(x).shape[0]
     slots = list(range(n)) if slot_idx is None else [int(s) for s in np.asarray(slot_idx)]
     codes = np.array(codes, copy=True); scales = np.array(scales, copy=True)
+    res = None if residual is None else np.array(residual, dtype=np.float32, copy=True)
     conv = _f64(conv_state).copy()
     y = np.zeros((n, HV * dv))
     for i, s in enumerate(slots):
@@ -389,6 +415,9 @@ def mixer_decode_q8(x, conv_w, u, b_logit, A_log, dt_bias, z, norm_w, HK, HV, dk
         y[i] = out["y"][0]
         conv[s] = out["conv_state"][0]
         for h in range(HV):
-            codes[s, h], scales[s, h] = q8_encode_head(out["state"][0, h].astype(np.float32), frame, s,
-                                                       HV, h)
-    return y, codes, scales, conv
+            Mh = out["state"][0, h].astype(np.float32)
+            if res is None:
+                codes[s, h], scales[s, h] = q8_encode_head(Mh, frame, s, HV, h)
+            else:
+                codes[s, h], scales[s, h], res[s, h] = q8_encode_head(Mh, frame, s, HV, h, res[s, h])
+    return (y, codes, scales, conv) if res is None else (y, codes, scales, conv, res)
