@@ -181,20 +181,27 @@ def workload_desc(wl, inp):
 
 # ----------------------------------------------------------- CPU oracle arm
 
-def oracle_sample(wl, inp, kheads):
-    """Run the oracle on k-heads `kheads` of the workload; returns (seconds,
-    token-heads processed, threads used)."""
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
+def oracle_sample(wl, inp, kheads, max_tokens=None):
+    """Run the oracle on q/k heads `kheads` (and their v-heads) of the workload, each sequence
+    cut to its first `max_tokens // N` tokens when max_tokens is given; returns (seconds,
+    tokens of the sample, v-heads of the sample, threads used)."""
     import oracle
-    from gpu_util import oracle_mixer
     oracle.build()
     G = wl.HV // wl.HK
-    units = len(inp["seqlens"]) * len(kheads) * G
+    lens = list(inp["seqlens"])
+    cu = inp["cu_seqlens"].tolist()
+    keep = lens if max_tokens is None else [min(L, max(64, max_tokens // len(lens))) for L in lens]
+    rows = np.concatenate([np.arange(cu[n], cu[n] + keep[n]) for n in range(len(lens))])
+    cu_s = np.concatenate([[0], np.cumsum(keep)]).astype(np.int32)
+    units = len(lens) * len(kheads) * G
     threads = max(1, min(os.cpu_count() or 1, units))
+    pick = lambda t: None if t is None else t[rows]
     t0 = time.perf_counter()
-    oracle_mixer(wl, inp, kheads=kheads, n_threads=threads)
+    oracle.mixer_heads(pick(inp["x"]), inp["conv_w"], pick(inp["u"]), pick(inp["b_logit"]), inp["A_log"],
+                       inp["dt_bias"], pick(inp["z"]), inp["norm_w"], cu_s, wl.HK, wl.HV, wl.dk, wl.dv,
+                       kheads, state=inp["state"], conv_state=inp["conv_state"], n_threads=threads)
     dt = time.perf_counter() - t0
-    return dt, sum(inp["seqlens"]) * len(kheads) * G, threads
+    return dt, int(sum(keep)), len(kheads) * G, threads
 
 
 def run_reference(args, rank, ws):
@@ -203,23 +210,26 @@ def run_reference(args, rank, ws):
     wl = WORKLOADS[args.workload]
     inp = make_inputs(wl)
     T = sum(inp["seqlens"])
-    kheads = list(range(min(4, wl.HK)))          # bounded sample: 4 q/k heads (8 v-heads)
+    # bounded sample per step: half of the q/k heads (all cores busy) over the first 2048
+    # tokens of the batch; the step time printed is the measured time of that sample
+    kheads = list(range(max(1, wl.HK // 2)))
+    cap = 2048
     for _ in range(args.warmup):
-        oracle_sample(wl, inp, kheads)
-    times, th = [], 1
+        oracle_sample(wl, inp, kheads, cap)
+    times, th, toks, vh = [], 1, 0, 0
     for _ in range(args.steps):
-        dt, th_units, th = oracle_sample(wl, inp, kheads)
+        dt, toks, vh, th = oracle_sample(wl, inp, kheads, cap)
         times.append(dt)
     tot = sum(times)
-    frac = len(kheads) * (wl.HV // wl.HK) / wl.HV
-    value = T * frac * len(times) / tot                 # full-workload tokens/s equivalent
-    sample = ("%d of %d v-heads over all %d tokens per step; tokens/s scaled by the head fraction"
-              % (len(kheads) * (wl.HV // wl.HK), wl.HV, T))
+    step_s = tot / len(times)
+    value = toks * (vh / wl.HV) / step_s                # whole-token equivalents per second
+    sample = ("per step: the first %d of %d tokens, %d of %d v-heads (q/k heads %d-%d); value = "
+              "sample tokens x v-head fraction / measured step time" % (toks, T, vh, wl.HV, kheads[0], kheads[-1]))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * tot / len(times) / frac, "higher_is_better": True,
+            "ms_per_step": 1e3 * step_s, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(wl, inp)},
+            "config": {"workload": workload_desc(wl, inp), "sample": sample},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": th, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -287,35 +297,14 @@ def run_ours(args, rank, ws, local):
     value = ws * T * args.steps / elapsed
 
     # ---- the chunked rule alone (gdn_chunk_prefill on the conv output), for its roofline
-    g = torch.empty((T, wl.HV), device=dev)
-    beta = torch.empty_like(g)
-    xa = torch.empty((T, wl.CH), device=dev)
-    o = torch.empty((T, wl.HV * wl.dv), device=dev)
-    gdn.gdn_gate_prep(cfg, d["u"], d["b_logit"], d["A_log"], d["dt_bias"], g, beta)
-    gdn.gdn_conv1d_prefill(cfg, d["x"], d["cu_seqlens"], d["conv_w"], conv.clone(), None, xa)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
-    flush.fill_(1.0)
-    sink = torch.empty((), device=dev)
-    nchunk = max(3, min(args.steps, 20))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(nchunk + 2)]
-    for i in range(nchunk + 2):     # 2 untimed warm-ups; L2 evicted before each launch
-        torch.sum(flush, 0, out=sink)
-        ev[i][0].record(stream)
-        gdn.gdn_chunk_prefill(cfg, xa[:, :H], xa[:, H:2 * H], xa[:, 2 * H:], g, beta,
-                              d["cu_seqlens"], state_in, state_out, None, o, workspace=wsp)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    chunk_s = sum(a.elapsed_time(b) for a, b in ev[2:]) / 1e3 / nchunk
+    chunk_s = time_chunked_rule(gdn, cfg, wl, d, conv, wsp, state_in, state_out, max(3, min(args.steps, 20)))
     flops = chunk_flops(lens, wl.chunk, wl.dk, wl.dv, wl.HV)
     tc_peak = pk["bf16_tflops"]
-    kname = ("chunked rule: chunk_map + chunk_tp_kernel + chunk_chain_kernel<32> (tcgen05, bf16x3 "
-             "operands), timed together through gdn_chunk_prefill" if tc_path else "chunk_simt_kernel")
-    roof = {"kernel": kname, "bound": "tensor", "achieved": flops / chunk_s / 1e12,
+    roof = {"kernel": CHUNK_KERNELS if tc_path else "chunk_simt_kernel", "bound": "tensor",
+            "achieved": flops / chunk_s / 1e12,
             "peak": tc_peak, "unit": "TFLOP/s", "frac": flops / chunk_s / 1e12 / tc_peak,
             "traffic": traffic_for("chunk_prefill_8k"), "peak_source": pk_src + " bf16 burst",
             "kernel_ms": chunk_s * 1e3, "flops_per_launch": flops}
-    del g, beta, xa, o, flush
     # the whole step against both bounds: the step's algorithmic bytes (x, z, y, g and beta per
     # token, state in and out per sequence) at the copy peak and its contraction FLOPs at the
     # tensor peak, the larger over the measured step time
@@ -328,15 +317,25 @@ def run_ours(args, rank, ws, local):
                  "frac": max(t_tc, t_hbm) / step_s, "tensor_frac": t_tc / step_s,
                  "peak_source": pk_src}
 
+    # ---- the other prefill workloads: varlen packing and a 64K-token sequence
+    legs = {}
+    if not args.no_legs:
+        del wsp
+        torch.cuda.empty_cache()
+        for name in ("varlen_16", "long_64k"):
+            legs[name] = bench_prefill_leg(args, dev, gdn, pk, pk_src, name)
+            torch.cuda.empty_cache()
+
     # ---- decode: 64 sequences x S one-token steps, L2 flushed between steps
     dec = None
     if args.decode_steps > 0:
         dec = bench_decode(args, dev, gdn, pk, pk_src)
 
-    # ---- the same decode on a Q8 state
-    dq8 = None
+    # ---- the same decode on a Q8 state, without and with the error-feedback residual
+    dq8 = dq8e = None
     if args.decode_steps > 0:
         dq8 = bench_decode_q8(args, dev, gdn, pk, pk_src)
+        dq8e = bench_decode_q8(args, dev, gdn, pk, pk_src, ef=True)
 
     # ---- slot snapshot (state + conv history) through gdn_state_copy
     snap = None
@@ -360,7 +359,7 @@ def run_ours(args, rank, ws, local):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        dt, th_units, th = oracle_sample(wl, inp, list(range(wl.HK)))
+        dt, _, _, th = oracle_sample(wl, inp, list(range(wl.HK)))
         cpu = {"value": T / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
                "sample": "the whole workload (all %d v-heads, %d tokens), once" % (wl.HV, T)}
 
@@ -376,9 +375,91 @@ def run_ours(args, rank, ws, local):
                            "activations": wl.act, "y_dtype": "bf16"},
                 "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk.summary(), "decode": dec, "decode_q8": dq8, "state_copy": snap, "verify": ver,
-                "backward": bwd}
+                "clocks": clk.summary(), "varlen_16": legs.get("varlen_16"), "long_64k": legs.get("long_64k"),
+                "decode": dec, "decode_q8": dq8, "decode_q8_ef": dq8e, "state_copy": snap,
+                "verify": ver, "backward": bwd}
         print(json.dumps(line), flush=True)
+
+
+CHUNK_KERNELS = ("chunked rule: chunk_map + chunk_tp_kernel + chunk_chain_kernel (tcgen05, bf16x3 "
+                 "operands), timed together through gdn_chunk_prefill")
+
+
+def time_chunked_rule(gdn, cfg, wl, d, conv, wsp, state_in, state_out, reps):
+    """Seconds per gdn_chunk_prefill launch on the workload's conv output (CUDA events around
+    each launch, L2 evicted by a read before each, 2 untimed warm-ups)."""
+    dev = d["x"].device
+    T = d["x"].shape[0]
+    H = wl.HK * wl.dk
+    stream = torch.cuda.current_stream()
+    g = torch.empty((T, wl.HV), device=dev)
+    beta = torch.empty_like(g)
+    xa = torch.empty((T, wl.CH), device=dev)
+    o = torch.empty((T, wl.HV * wl.dv), device=dev)
+    gdn.gdn_gate_prep(cfg, d["u"], d["b_logit"], d["A_log"], d["dt_bias"], g, beta)
+    gdn.gdn_conv1d_prefill(cfg, d["x"], d["cu_seqlens"], d["conv_w"], conv.clone(), None, xa)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+    flush.fill_(1.0)
+    sink = torch.empty((), device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps + 2)]
+    for i in range(reps + 2):
+        torch.sum(flush, 0, out=sink)
+        ev[i][0].record(stream)
+        gdn.gdn_chunk_prefill(cfg, xa[:, :H], xa[:, H:2 * H], xa[:, 2 * H:], g, beta,
+                              d["cu_seqlens"], state_in, state_out, None, o, workspace=wsp)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_error() == 0
+    return sum(a.elapsed_time(b) for a, b in ev[2:]) / 1e3 / reps
+
+
+def bench_prefill_leg(args, dev, gdn, pk, pk_src, name):
+    """One more prefill workload through gdn_mixer_prefill (tokens/s over a few steps, CUDA
+    events, inputs larger than L2), with its chunked rule timed alone for the roofline; the
+    FLOPs count every chunk at its actual length."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    lens = inp["seqlens"]
+    T, N = sum(lens), len(lens)
+    cfg = gdn.make_config(wl.HK, wl.HV, wl.dk, wl.dv, wl.chunk, wl.act, n_slots=N)
+    d = {k: v.to(dev) for k, v in inp.items() if hasattr(v, "to") and not k.startswith("dec_")}
+    y = torch.empty((T, wl.HV * wl.dv), dtype=torch.bfloat16, device=dev)
+    state_in = d["state"] if wl.init_state else None
+    state_out = torch.empty((N, wl.HV, wl.dk, wl.dv), device=dev)
+    conv0 = (d["conv_state"].clone() if wl.init_conv
+             else torch.zeros((N, wl.CH, 3), dtype=wl.torch_act, device=dev))
+    conv = conv0.clone()
+    wsp = torch.empty(gdn.gdn_workspace_size(cfg, T, N), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gdn.gdn_mixer_prefill(cfg, d["x"], d["z"], d["u"], d["b_logit"], d["conv_w"], d["A_log"],
+                              d["dt_bias"], d["norm_w"], d["cu_seqlens"], y, state_in=state_in,
+                              state_out=state_out, conv_state=conv, workspace=wsp)
+
+    steps = 5 if T < 50000 else 3
+    for _ in range(3):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_error() == 0
+    step_s = e0.elapsed_time(e1) / 1e3 / steps
+    chunk_s = time_chunked_rule(gdn, cfg, wl, d, conv0, wsp, state_in, state_out, 3)
+    flops = chunk_flops(lens, wl.chunk, wl.dk, wl.dv, wl.HV)
+    tc_peak = pk["bf16_tflops"]
+    return {"workload": workload_desc(wl, inp), "value": T / step_s, "unit": "tokens/s",
+            "ms_per_step": step_s * 1e3, "steps": steps, "warmup": 3,
+            "roofline": {"kernel": CHUNK_KERNELS, "bound": "tensor", "achieved": flops / chunk_s / 1e12,
+                         "peak": tc_peak, "unit": "TFLOP/s", "frac": flops / chunk_s / 1e12 / tc_peak,
+                         "traffic": None, "peak_source": pk_src + " bf16 burst",
+                         "kernel_ms": chunk_s * 1e3, "flops_per_launch": flops},
+            "gpu_launches": 5 * steps}
 
 
 def bench_decode(args, dev, gdn, pk, pk_src):
@@ -432,9 +513,10 @@ def bench_decode(args, dev, gdn, pk, pk_src):
             "gpu_launches": 2 * S}
 
 
-def bench_decode_q8(args, dev, gdn, pk, pk_src):
-    """decode_64x256 on a Q8 state pool (int8 codes + fp32 row scales) through
-    gdn_mixer_decode_q8, L2 evicted between steps like the fp32 decode."""
+def bench_decode_q8(args, dev, gdn, pk, pk_src, ef=False):
+    """decode_64x256 on a Q8 state pool (int8 codes + fp32 row scales, and with ef the bf16
+    error-feedback residual) through gdn_mixer_decode_q8, L2 evicted between steps like the
+    fp32 decode."""
     wl = WORKLOADS["decode_64x256"]
     S = args.decode_steps
     from dataclasses import replace
@@ -444,7 +526,8 @@ def bench_decode_q8(args, dev, gdn, pk, pk_src):
     cfg = gdn.make_config(wl.HK, wl.HV, wl.dk, wl.dv, wl.chunk, wl.act, n_slots=N)
     codes = torch.empty((N, wl.HV, wl.dk, wl.dv), dtype=torch.int8, device=dev)
     scales = torch.empty((N, wl.HV, wl.dk), device=dev)
-    gdn.gdn_state_to_q8(cfg, inp["state"].to(dev), codes, scales, 0)
+    res = (torch.empty((N, wl.HV, wl.dk, wl.dv), dtype=torch.bfloat16, device=dev) if ef else None)
+    gdn.gdn_state_to_q8(cfg, inp["state"].to(dev), codes, scales, 0, residual=res)
     conv = inp["conv_state"].to(dev)
     cw, A, dt, nw = (inp[k].to(dev) for k in ("conv_w", "A_log", "dt_bias", "norm_w"))
     xs, zs, us, bs = (inp[k].to(dev) for k in ("dec_x", "dec_z", "dec_u", "dec_b_logit"))
@@ -456,7 +539,9 @@ def bench_decode_q8(args, dev, gdn, pk, pk_src):
     stream = torch.cuda.current_stream()
     for t in range(min(3, S)):   # warm-up on copies of the pool
         c2, s2, v2 = codes.clone(), scales.clone(), conv.clone()
-        gdn.gdn_mixer_decode_q8(cfg, xs[t], zs[t], us[t], bs[t], cw, A, dt, nw, y, c2, s2, v2, 1 + t, ws)
+        r2 = None if res is None else res.clone()
+        gdn.gdn_mixer_decode_q8(cfg, xs[t], zs[t], us[t], bs[t], cw, A, dt, nw, y, c2, s2, v2, 1 + t, ws,
+                                residual=r2)
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(S)]
@@ -464,19 +549,21 @@ def bench_decode_q8(args, dev, gdn, pk, pk_src):
         torch.sum(flush, 0, out=sink)
         evs[t][0].record(stream)
         gdn.gdn_mixer_decode_q8(cfg, xs[t], zs[t], us[t], bs[t], cw, A, dt, nw, y, codes, scales, conv,
-                                1 + t, ws)
+                                1 + t, ws, residual=res)
         evs[t][1].record(stream)
     torch.cuda.synchronize()
     assert gdn.gdn_device_error() == 0
     per = sum(a.elapsed_time(b) for a, b in evs) / S / 1e3
-    q8_bytes = 2 * N * wl.HV * (wl.dk * wl.dv + wl.dk * 4)
+    q8_bytes = 2 * N * wl.HV * (wl.dk * wl.dv * (3 if ef else 1) + wl.dk * 4)
     gbs = q8_bytes / per / 1e9
-    return {"workload": "decode_64x256 with a Q8 state (int8 codes + fp32 row scales, 16.5 KiB per "
-                        "head), %d steps, L2 evicted between steps" % S,
+    what = ("int8 codes + fp32 row scales + bf16 error-feedback residual, 48.5 KiB per head" if ef
+            else "int8 codes + fp32 row scales, 16.5 KiB per head")
+    return {"workload": "decode_64x256 with a Q8 state (%s), %d steps, L2 evicted between steps" % (what, S),
             "value": gbs, "unit": "GB/s", "us_per_step": per * 1e6, "state_bytes_per_step": q8_bytes,
             "roofline": {"kernel": "decode_prep_kernel + decode_stream_kernel (Q8 slots)", "bound": "hbm",
                          "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": traffic_for("decode_64x256_q8"),
+                         "frac": gbs / pk["hbm_gbs"],
+                         "traffic": None if ef else traffic_for("decode_64x256_q8"),
                          "peak_source": pk_src + " copy"},
             "gpu_launches": 2 * S}
 
@@ -700,6 +787,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-legs", action="store_true", help="skip the varlen_16 / long_64k prefill legs")
     args = ap.parse_args()
     rank, ws, local = dist_init()
     if args.impl == "reference":

@@ -2,6 +2,7 @@
 // argument validation (before any launch), workspace carving, dispatch to the
 // kernels, and the device error word.
 #include <cmath>
+#include <atomic>
 #include <mutex>
 
 #include "gdn_common.cuh"
@@ -31,6 +32,11 @@ gdn_status error_word(unsigned **out) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Limit of every bounded wait on the device, and the test hook that makes a
+// launch lose one operand copy (gdn_debug_set_wait); read at each call.
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+std::atomic<unsigned> g_lose{0u};
+
 // Largest sequence count a call accepts (one grid dimension per sequence).
 constexpr int kMaxSeqs = 65535;
 
@@ -55,6 +61,8 @@ gdn_status check_cfg(const gdn_config *c, gdn::Dims *d) {
     d->hk = c->hk; d->hv = c->hv; d->dk = c->dk; d->dv = c->dv; d->grp = grp;
     d->ch = (int)ch; d->chunk = c->chunk; d->n_slots = c->n_slots;
     d->q_scale = c->q_scale; d->l2_eps = c->l2_eps; d->norm_eps = c->norm_eps;
+    d->wait_ns = g_wait_ns.load();
+    d->lose = g_lose.load();
     return GDN_OK;
 }
 
@@ -127,6 +135,13 @@ cudaError_t launch_chunk(const gdn::ChunkArgs &a, bool act_bf16, bool in_bf16, b
 }  // namespace
 
 namespace gdn {
+// Bytes of the fused prefill's intermediates alone (0 for an invalid configuration).
+size_t mixer_prefill_ws_bytes(const gdn_config *cfg, long long T, long long n_seqs) {
+    Dims d;
+    if (check_cfg(cfg, &d) != GDN_OK || T < 0 || n_seqs < 0) return 0;
+    return prefill_ws_bytes(d, cfg->act == GDN_BF16, T, n_seqs);
+}
+
 int sm_count() {
     static int cached[kMaxDevices];
     int dev = 0;
@@ -554,15 +569,16 @@ gdn_status gdn_chunk_backward(const gdn_config *cfg, const void *q, const void *
 }
 
 gdn_status gdn_state_to_q8(const gdn_config *cfg, const float *state, int8_t *codes, float *scales,
-                           uint32_t frame, void *stream) {
+                           void *residual, uint32_t frame, void *stream) {
     gdn::Dims d;
     gdn_status st = check_cfg(cfg, &d);
     if (st != GDN_OK) return st;
-    if (!state || !codes || !scales || !aligned16(state) || !aligned16(codes) || !aligned16(scales))
+    if (!state || !codes || !scales || !aligned16(state) || !aligned16(codes) || !aligned16(scales) ||
+        (residual && !aligned16(residual)))
         return GDN_ERR_INVALID_ARG;
     if (d.n_slots == 0) return GDN_OK;
-    return launch_status(gdn::launch_q8_convert(d, state, codes, scales, frame, true,
-                                                (cudaStream_t)stream));
+    return launch_status(gdn::launch_q8_convert(d, state, codes, scales, (__nv_bfloat16 *)residual, frame,
+                                                true, (cudaStream_t)stream));
 }
 
 gdn_status gdn_state_from_q8(const gdn_config *cfg, const int8_t *codes, const float *scales,
@@ -574,19 +590,20 @@ gdn_status gdn_state_from_q8(const gdn_config *cfg, const int8_t *codes, const f
         return GDN_ERR_INVALID_ARG;
     if (d.n_slots == 0) return GDN_OK;
     return launch_status(gdn::launch_q8_convert(d, state, const_cast<int8_t *>(codes),
-                                                const_cast<float *>(scales), 0u, false,
+                                                const_cast<float *>(scales), nullptr, 0u, false,
                                                 (cudaStream_t)stream));
 }
 
 gdn_status gdn_mixer_decode_q8(const gdn_config *cfg, const gdn_mixer_io *io, int8_t *codes,
-                               float *scales, uint32_t frame, void *workspace,
+                               float *scales, void *residual, uint32_t frame, void *workspace,
                                size_t workspace_bytes, void *stream) {
     gdn::Dims d;
     gdn_status st = check_cfg(cfg, &d);
     if (st != GDN_OK) return st;
     if ((st = check_mixer_io(d, io, true, true)) != GDN_OK) return st;
     if (io->n_seqs == 0) return GDN_OK;
-    if (!codes || !scales || !aligned16(codes) || !aligned16(scales)) return GDN_ERR_INVALID_ARG;
+    if (!codes || !scales || !aligned16(codes) || !aligned16(scales) || (residual && !aligned16(residual)))
+        return GDN_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) ||
         workspace_bytes < gdn::decode_ws_bytes(d, io->n_seqs))
         return GDN_ERR_WORKSPACE;
@@ -599,9 +616,16 @@ gdn_status gdn_mixer_decode_q8(const gdn_config *cfg, const gdn_mixer_io *io, in
     a.n = io->n_seqs; a.state_idx = io->state_idx; a.out = io->y;
     a.ws = (float *)workspace;
     a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
-    a.q8 = codes; a.q8_scale = scales; a.frame = frame;
+    a.q8 = codes; a.q8_scale = scales; a.frame = frame; a.q8_res = (__nv_bfloat16 *)residual;
     return launch_status(gdn::launch_decode_q8(a, cfg->act == GDN_BF16, io->y_dtype == GDN_BF16,
                                                (cudaStream_t)stream));
+}
+
+gdn_status gdn_debug_set_wait(uint64_t wait_ns, uint32_t lose) {
+    if (wait_ns == 0 || wait_ns > 60000000000ull || (lose & ~3u)) return GDN_ERR_INVALID_ARG;
+    g_wait_ns.store(wait_ns);
+    g_lose.store(lose);
+    return GDN_OK;
 }
 
 gdn_status gdn_device_error(void *stream, uint32_t *code) {

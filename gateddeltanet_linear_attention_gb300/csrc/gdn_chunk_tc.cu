@@ -225,8 +225,9 @@ struct MmaSync {
     uint64_t *mbar;
     volatile uint32_t *flag;
     uint32_t phase;
+    uint64_t limit_ns;
     __device__ bool wait(int tid, bool issued_ok = true) {
-        if (tid == 0) *flag = (issued_ok && tc::mbar_wait(tc::smem_u32(mbar), phase)) ? 0u : 1u;
+        if (tid == 0) *flag = (issued_ok && tc::mbar_wait(tc::smem_u32(mbar), phase, limit_ns)) ? 0u : 1u;
         __syncthreads();
         const bool ok = *flag == 0u;
         if (ok) phase ^= 1u;
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tmem_slot;
-    MmaSync ms{mbar, wait_flag, 0u};
+    MmaSync ms{mbar, wait_flag, 0u, a.d.wait_ns};
     const int qd = warp & 3, hf = warp >> 2, tl = qd * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
@@ -663,7 +664,7 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     if (!ok) {
         if (tid == 0) {
             set_error(a.err, GDN_DEVERR_TIMEOUT);
-            tc::mbar_wait(tc::smem_u32(mbar), ms.phase);
+            tc::mbar_wait(tc::smem_u32(mbar), ms.phase, a.d.wait_ns);
         }
         __syncthreads();
     }
@@ -757,8 +758,8 @@ __device__ __forceinline__ void bar_sync_staging() {   // warps 0-7 only
 // agree on the outcome through `flag` (one flag per barrier, so that the
 // next wait never overwrites a value a slow thread has yet to read).
 __device__ __forceinline__ bool staging_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *flag,
-                                             int tid) {
-    if (tid == 0) *flag = tc::mbar_wait(tc::smem_u32(bar), parity) ? 0u : 1u;
+                                             int tid, uint64_t limit_ns) {
+    if (tid == 0) *flag = tc::mbar_wait(tc::smem_u32(bar), parity, limit_ns) ? 0u : 1u;
     bar_sync_staging();
     const bool ok = *flag == 0u;
     tc::fence_after_sync();
@@ -815,6 +816,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
     float *sO = reinterpret_cast<float *>(sm + L::OFF_SO);     // [2][64][SOS]
 
     const Dims &d = a.d;
+    const uint64_t WL = d.wait_ns;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int col0 = h * TC_DK + slice * DVS;      // this slice's first column in o / v / state
@@ -894,8 +896,8 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
             // G2 of chunk i: D3 = [T ; PT] . bV  (U, PU)
             auto issue_g2 = [&](long long i) -> bool {
                 const uint32_t par2 = (uint32_t)((i >> 1) & 1);
-                if (!tc::mbar_wait(tc::smem_u32(&bvbar[i & 1]), par2) ||
-                    !tc::mbar_wait(tc::smem_u32(&tpbar[i & 1]), par2))
+                if (!tc::mbar_wait(tc::smem_u32(&bvbar[i & 1]), par2, WL) ||
+                    !tc::mbar_wait(tc::smem_u32(&tpbar[i & 1]), par2, WL))
                     return false;
                 const uint32_t tb = s_tp + (uint32_t)((i & 1) * TP_BYTES);
                 mma2cat<false, 64, DVS>(T_D3, tb, tb + TP_HALF, 0, s_bv + (uint32_t)((i & 1) * BV_SLICE),
@@ -908,20 +910,20 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 fetch_tp(1);
                 fetch_bv(1);
             }
-            fetch_wq(0);
+            if (!(d.lose & LOSE_CHAIN_OPERAND_COPY)) fetch_wq(0);   // (tests: a lost copy)
             fetch_kt(0);
             long long ci = 0;
             bool ok = issue_g2(0);
             for (; ok && ci < n_chunks; ++ci) {
                 const uint32_t par = (uint32_t)(ci & 1);
                 // G3: D3 += [-W ; Q'] . M  (U' on lanes 0-63, O on 64-127)
-                ok = tc::mbar_wait(tc::smem_u32(mtbar), par) && tc::mbar_wait(tc::smem_u32(wqbar), par);
+                ok = tc::mbar_wait(tc::smem_u32(mtbar), par, WL) && tc::mbar_wait(tc::smem_u32(wqbar), par, WL);
                 if (!ok) break;
                 tc::fence_after_sync();
                 mma2cat<false, 128, DVS>(T_D3, s_wqh, s_wql, 0, s_mt, true, 0u);
                 tc::mma_commit(tc::smem_u32(g3bar));
                 // refill what G2 / G3 have read
-                ok = tc::mbar_wait(tc::smem_u32(g3bar), par);
+                ok = tc::mbar_wait(tc::smem_u32(g3bar), par, WL);
                 if (!ok) break;
                 if (ci + 1 < n_chunks) fetch_wq(ci + 1);
                 if (ci + 2 < n_chunks) {   // into the buffers G2 of this chunk has read
@@ -929,7 +931,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                     fetch_bv(ci + 2);
                 }
                 // G5: D5 = K~^T . U'
-                ok = tc::mbar_wait(tc::smem_u32(utbar), par) && tc::mbar_wait(tc::smem_u32(ktbar), par);
+                ok = tc::mbar_wait(tc::smem_u32(utbar), par, WL) && tc::mbar_wait(tc::smem_u32(ktbar), par, WL);
                 if (!ok) break;
                 tc::fence_after_sync();
                 mma2cat<true, 64, DVS>(T_D5, s_kth, s_ktl, 128, s_ut, false, tc::kTransA);
@@ -937,7 +939,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 if (ci + 1 < n_chunks) {
                     // G2 of the next chunk, behind G5 in the tensor pipe (D3 has been read by E3),
                     // then the next K~ once G5 has read this one
-                    ok = issue_g2(ci + 1) && tc::mbar_wait(tc::smem_u32(g5bar), par);
+                    ok = issue_g2(ci + 1) && tc::mbar_wait(tc::smem_u32(g5bar), par, WL);
                     if (ok) fetch_kt(ci + 1);
                 }
             }
@@ -946,17 +948,17 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 // copies retire (bounded) before the kernel's end frees TMEM and shared memory
                 set_error(a.err, GDN_DEVERR_TIMEOUT);
                 tc::mma_commit(tc::smem_u32(g3bar));
-                tc::mbar_wait(tc::smem_u32(g3bar), (uint32_t)(ci & 1));
+                tc::mbar_wait(tc::smem_u32(g3bar), (uint32_t)(ci & 1), WL);
                 for (int k = 0; k < 2; ++k) {    // each copy barrier: its current and next phase
-                    tc::mbar_wait(tc::smem_u32(wqbar), (uint32_t)((ci + k) & 1));
-                    tc::mbar_wait(tc::smem_u32(ktbar), (uint32_t)((ci + k) & 1));
+                    tc::mbar_wait(tc::smem_u32(wqbar), (uint32_t)((ci + k) & 1), WL);
+                    tc::mbar_wait(tc::smem_u32(ktbar), (uint32_t)((ci + k) & 1), WL);
                     for (int b = 0; b < 2; ++b) {
-                        tc::mbar_wait(tc::smem_u32(&bvbar[b]), (uint32_t)(((ci + k) >> 1) & 1));
-                        tc::mbar_wait(tc::smem_u32(&tpbar[b]), (uint32_t)(((ci + k) >> 1) & 1));
+                        tc::mbar_wait(tc::smem_u32(&bvbar[b]), (uint32_t)(((ci + k) >> 1) & 1), WL);
+                        tc::mbar_wait(tc::smem_u32(&tpbar[b]), (uint32_t)(((ci + k) >> 1) & 1), WL);
                     }
                 }
             } else {
-                tc::mbar_wait(tc::smem_u32(g5bar), (uint32_t)((n_chunks - 1) & 1));   // last G5 retired
+                tc::mbar_wait(tc::smem_u32(g5bar), (uint32_t)((n_chunks - 1) & 1), WL);   // last G5 retired
             }
         }
     } else if (warp >= 9) {
@@ -987,7 +989,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                     const uint64_t t0 = tc::globaltimer_ns();
                     for (uint32_t it = 0; it < tc::kSpinLimit && !np_ready(u); ++it) {
                         u = ld_relaxed_gpu_v4(np_row(i));
-                        if ((it & 63u) == 63u && tc::globaltimer_ns() - t0 > tc::kWaitNs) break;
+                        if ((it & 63u) == 63u && tc::globaltimer_ns() - t0 > WL) break;
                     }
                     if (!np_ready(u)) return false;
                 }
@@ -1018,7 +1020,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                     load_z(i - 2, zp);
                     u = ld_relaxed_gpu_v4(np_row(i - 2));
                 }
-                if (!tc::mbar_wait(tc::smem_u32(&obar[i & 1]), (uint32_t)((i >> 1) & 1))) break;
+                if (!tc::mbar_wait(tc::smem_u32(&obar[i & 1]), (uint32_t)((i >> 1) & 1), WL)) break;
                 float ov[HALF];
                 const float *src = sO + ((int)(i & 1) * 64 + r) * L::SOS + hh * HALF;
 #pragma unroll
@@ -1085,7 +1087,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
             const bool has_next = c0 + TC_C < e;
             const uint32_t par = (uint32_t)(ci & 1);
             // ---------------- E3: U' -> concatenated B operand -> utbar
-            if (!staging_wait(g3bar, par, flag3, tid)) break;
+            if (!staging_wait(g3bar, par, flag3, tid, WL)) break;
             float ov[HALF];
             tmem_ld_cat16<DVS>(T_D3 + lane_off + hf * HALF, ov);
             if (qd < 2) {
@@ -1097,7 +1099,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 // O rows -> the norm warps (shared memory only, off the chain's path)
                 if (qd >= 2) {
                     const int k = (int)(ci & 1);
-                    if (ci >= 2 && !tc::mbar_wait(tc::smem_u32(&ofree[k]), (uint32_t)(((ci >> 1) - 1) & 1)))
+                    if (ci >= 2 && !tc::mbar_wait(tc::smem_u32(&ofree[k]), (uint32_t)(((ci >> 1) - 1) & 1), WL))
                         set_error(a.err, GDN_DEVERR_TIMEOUT);
                     float *dst = sO + (k * 64 + (tl - 64)) * L::SOS + hf * HALF;
 #pragma unroll
@@ -1107,7 +1109,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 }
             }
             // ---------------- E5: M <- gamma_last M + dM -> mtbar
-            if (!staging_wait(g5bar, par, flag5, tid)) break;
+            if (!staging_wait(g5bar, par, flag5, tid, WL)) break;
             float v[HALF];
             tmem_ld_cat16<DVS>(T_D5 + lane_off + hf * HALF, v);
             const float gl = expf(Gl);

@@ -16,7 +16,13 @@ struct Dims {
     int chunk;
     int n_slots;
     float q_scale, l2_eps, norm_eps;
+    // every bounded wait on the device gives up after wait_ns nanoseconds (gdn_debug_set_wait);
+    // `lose` makes chosen launches skip one operand copy so that a wait runs out (tests only)
+    unsigned long long wait_ns;
+    unsigned lose;
 };
+constexpr unsigned LOSE_DECODE_STATE_COPY = 1u;   // decode streaming kernel: the first head's state
+constexpr unsigned LOSE_CHAIN_OPERAND_COPY = 2u;  // state chain: the first chunk's [-W ; Q'] operand
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -75,6 +81,7 @@ __device__ __forceinline__ void seq_bounds(const int32_t *cu, int n, long long T
 
 // Launchers implemented by the kernel translation units and called by the ABI.
 namespace gdn {
+size_t mixer_prefill_ws_bytes(const gdn_config *cfg, long long T, long long n_seqs);
 struct ChunkArgs {
     const void *q, *k, *v;
     long long ld_qk, ld_v;
@@ -128,10 +135,11 @@ struct DecodeArgs {
     int8_t *q8;
     float *q8_scale;
     uint32_t frame;
+    __nv_bfloat16 *q8_res;   // error-feedback residual [slots][HV][dk][dv] (null: no feedback)
 };
 cudaError_t launch_decode_q8(const DecodeArgs &a, bool in_bf16, bool out_bf16, cudaStream_t s);
 cudaError_t launch_q8_convert(const Dims &d, const float *state, int8_t *codes, float *scales,
-                              uint32_t frame, bool to_q8, cudaStream_t s);
+                              __nv_bfloat16 *res, uint32_t frame, bool to_q8, cudaStream_t s);
 
 // Backward of the gated delta rule core (gdn_chunk_states / gdn_chunk_backward).
 struct BwdArgs {

@@ -340,9 +340,25 @@ struct Q8Io {
             }
         }
     }
-    static __device__ __forceinline__ void store(const float4 (&m)[RPT], int8_t *codes, float *scales,
+    // Encode x = m (+ the residual e_in, error feedback) into codes and row scales.  Every code
+    // draws its own dither u = (pcg_hash(index ^ hf) >> 8) * 2^-24, index = base_idx + row*DV + col.
+    // With EF the new residual bf16(x - code*scale) goes to e_out (global, same layout as codes);
+    // e_in is the previous residual (bf16, shared memory, same layout).
+    template <bool EF = false>
+    static __device__ __forceinline__ void store(float4 (&m)[RPT], int8_t *codes, float *scales,
                                                  uint32_t hf, uint32_t base_idx, int rg, int c4,
-                                                 int lane) {
+                                                 int lane, const __nv_bfloat16 *e_in = nullptr,
+                                                 __nv_bfloat16 *e_out = nullptr) {
+        if (EF && e_in) {   // (a null e_in: the first encode, residual zero)
+#pragma unroll
+            for (int x = 0; x < RPT; ++x) {
+                const uint2 eb = *reinterpret_cast<const uint2 *>(e_in + (rg + x * RPP) * DV + c4);
+                const float2 e01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&eb.x));
+                const float2 e23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&eb.y));
+                m[x].x = __fadd_rn(m[x].x, e01.x); m[x].y = __fadd_rn(m[x].y, e01.y);
+                m[x].z = __fadd_rn(m[x].z, e23.x); m[x].w = __fadd_rn(m[x].w, e23.y);
+            }
+        }
         float amaxs[RPT], invs[RPT], my_scale;
         int my_x;
         row_stats(m, lane, amaxs, invs, my_x, my_scale);
@@ -354,24 +370,34 @@ struct Q8Io {
             const int row = rg + x * RPP;
             const float amax = amaxs[x], inv = invs[x];
             const float v[4] = {m[x].x, m[x].y, m[x].z, m[x].w};
-            // one hash per 4 codes: byte e of it is the dither of code e, u = (2 byte + 1) / 512
-            const uint32_t r = pcg_hash(((base_idx + (uint32_t)(row * DV + c4)) >> 2) ^ hf);
-            char4 c;
+            const uint32_t idx0 = base_idx + (uint32_t)(row * DV + c4);
             signed char cc[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                // u = (2 byte + 1) / 512, formed exactly as (1 + u) - 1 from its bit pattern (no
-                // int -> float conversion); floor and the conversion in one rounding-down convert
-                const uint32_t b2 = 2u * ((r >> (8 * e)) & 0xFFu) + 1u;
-                const float u = __int_as_float(0x3F800000u | (b2 << 14)) - 1.0f;
+                // u = (r >> 8) * 2^-24: a 24-bit integer, exact in fp32, times a power of two
+                const uint32_t r = pcg_hash((idx0 + (uint32_t)e) ^ hf);
+                const float u = __fmul_rn(__uint2float_rn(r >> 8), 0x1p-24f);
                 int q = __float2int_rd(__fadd_rn(__fmul_rn(v[e], inv), u));
                 q = min(max(q, -127), 127);
                 cc[e] = amax > 0.f ? (signed char)q : (signed char)0;
             }
+            char4 c;
             c.x = cc[0]; c.y = cc[1]; c.z = cc[2]; c.w = cc[3];
             *reinterpret_cast<char4 *>(codes + row * DV + c4) = c;
             if constexpr (!(LPR == 32 && RPT == 8))
                 if (lane % LPR == 0) scales[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+            if constexpr (EF) {
+                // the residual left for the next encode: bf16(x - code * scale), scale = amax / 127
+                const float sc = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+                float ev[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ev[e] = __fsub_rn(v[e], __fmul_rn((float)cc[e], sc));
+                __nv_bfloat162 lo2 = __floats2bfloat162_rn(ev[0], ev[1]), hi2 = __floats2bfloat162_rn(ev[2], ev[3]);
+                uint2 ob;
+                ob.x = *reinterpret_cast<const uint32_t *>(&lo2);
+                ob.y = *reinterpret_cast<const uint32_t *>(&hi2);
+                *reinterpret_cast<uint2 *>(e_out + row * DV + c4) = ob;
+            }
         }
     }
     // decode: codes, scales -> m
@@ -392,13 +418,14 @@ struct Q8Io {
     }
 };
 
-template <int DK, int DV, bool Q8 = false>
+template <int DK, int DV, bool Q8 = false, bool EF = false>
 struct StreamCfg {
     static constexpr int NT = 4 * DV;
     static constexpr int LPR = DV / 4, RPP = NT / LPR, RPT = DK / RPP;
-    // bytes of one head state: fp32 M, or int8 codes followed by the fp32 row scales
-    static constexpr int SLOT = Q8 ? DK * DV + DK * 4 : DK * DV * 4;
-    static constexpr int NS = SLOT >= 65536 ? 3 : (SLOT >= 16384 ? 8 : 16);
+    // bytes of one head state: fp32 M, or int8 codes followed by the fp32 row scales (and, with
+    // error feedback, the bf16 residual)
+    static constexpr int SLOT = Q8 ? DK * DV + DK * 4 + (EF ? DK * DV * 2 : 0) : DK * DV * 4;
+    static constexpr int NS = SLOT >= 40960 ? 3 : (SLOT >= 16384 ? 8 : 16);
     static constexpr int CHUNK = SLOT < 16384 ? SLOT : 16384;       // bytes per bulk copy
     static constexpr int HB = 4;                                    // heads per record batch
     // largest (HB/G) * record size over G in {1, 2, 4}: the records of one batch
@@ -408,36 +435,38 @@ struct StreamCfg {
 };
 
 // Every array read or written as float4 is 16-byte aligned explicitly.
-template <int DK, int DV, bool Q8 = false>
+template <int DK, int DV, bool Q8 = false, bool EF = false>
 struct StreamTail {
-    alignas(16) uint64_t full[StreamCfg<DK, DV, Q8>::NS];
+    alignas(16) uint64_t full[StreamCfg<DK, DV, Q8, EF>::NS];
     alignas(16) uint64_t rfull[2];
-    alignas(16) float rec[2][StreamCfg<DK, DV, Q8>::RECBUF];   // records of the current / next batch
-    alignas(16) float red_p[StreamCfg<DK, DV, Q8>::RPP][DV];
-    alignas(16) float red_s[StreamCfg<DK, DV, Q8>::RPP][DV];
+    alignas(16) float rec[2][StreamCfg<DK, DV, Q8, EF>::RECBUF];   // records of the current / next batch
+    alignas(16) float red_p[StreamCfg<DK, DV, Q8, EF>::RPP][DV];
+    alignas(16) float red_s[StreamCfg<DK, DV, Q8, EF>::RPP][DV];
     alignas(16) float up[DV];
     alignas(16) float nw[DV];
     float npart[4];
     int rec_bad;
+    int dead;      // a state wait gave up: every later item is handled like a padding lane
 };
 
-template <int DK, int DV, bool Q8 = false>
+template <int DK, int DV, bool Q8 = false, bool EF = false>
 constexpr size_t stream_smem_bytes() {
-    return (size_t)StreamCfg<DK, DV, Q8>::NS * StreamCfg<DK, DV, Q8>::SLOT + sizeof(StreamTail<DK, DV, Q8>);
+    return (size_t)StreamCfg<DK, DV, Q8, EF>::NS * StreamCfg<DK, DV, Q8, EF>::SLOT +
+           sizeof(StreamTail<DK, DV, Q8, EF>);
 }
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
-template <int DK, int DV, typename TOut, bool Q8 = false>
+template <int DK, int DV, typename TOut, bool Q8 = false, bool EF = false>
 __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) {
-    using Cfg = StreamCfg<DK, DV, Q8>;
+    using Cfg = StreamCfg<DK, DV, Q8, EF>;
     constexpr int NT = Cfg::NT, LPR = Cfg::LPR, RPP = Cfg::RPP, RPT = Cfg::RPT, NS = Cfg::NS;
     constexpr int HB = Cfg::HB;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float *slots = reinterpret_cast<float *>(smem_raw);
-    StreamTail<DK, DV, Q8> &tl = *reinterpret_cast<StreamTail<DK, DV, Q8> *>(smem_raw + NS * Cfg::SLOT);
+    StreamTail<DK, DV, Q8, EF> &tl = *reinterpret_cast<StreamTail<DK, DV, Q8, EF> *>(smem_raw + NS * Cfg::SLOT);
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -458,6 +487,7 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
         for (int s = 0; s < 2; ++s) tc::mbar_init(tc::smem_u32(&tl.rfull[s]), 1);
         tc::mbar_fence_init();
         tl.rec_bad = 0;
+        tl.dead = 0;
     }
     for (int j = tid; j < DV; j += NT) tl.nw[j] = a.norm_w[j];
     __syncthreads();
@@ -472,12 +502,15 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
             tc::mbar_arrive(mb);
             return;
         }
+        if (it == 0 && blockIdx.x == 0 && (d.lose & LOSE_DECODE_STATE_COPY)) return;   // (tests)
         const long long head = (long long)slot * d.hv + (long long)kh * G + gi;
         const uint32_t dst = tc::smem_u32(slots) + (uint32_t)((it % NS) * Cfg::SLOT);
         tc::mbar_arrive_expect_tx(mb, Cfg::SLOT);
-        if constexpr (Q8) {   // the codes, then the row scales
+        if constexpr (Q8) {   // the codes, then the row scales (then the residual)
             tc::bulk_g2s(dst, a.q8 + head * DK * DV, DK * DV, mb);
             tc::bulk_g2s(dst + DK * DV, a.q8_scale + head * DK, DK * 4, mb);
+            if constexpr (EF)
+                tc::bulk_g2s(dst + DK * DV + DK * 4, a.q8_res + head * DK * DV, DK * DV * 2, mb);
         } else {
             const char *src = reinterpret_cast<const char *>(a.state + head * DK * DV);
             for (int c = 0; c < Cfg::SLOT; c += Cfg::CHUNK) tc::bulk_g2s(dst + c, src + c, Cfg::CHUNK, mb);
@@ -501,12 +534,13 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
     // The state ring does not depend on the prep kernel: start it, then wait
     // for the prep grid (a no-op when launched without programmatic
     // serialisation) before the first record copy.
+    int n_issued = 0;   // (thread 0) items whose state copy has been issued
     if (tid == 0)
-        for (int it = 0; it < NS && it < n_items; ++it) issue(it);
+        for (; n_issued < NS && n_issued < n_items; ++n_issued) issue(n_issued);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid == 0) issue_rec(0);
+    const uint64_t WL = d.wait_ns;
 
-    bool timed_out = false;
     for (int it = 0; it < n_items; ++it) {
         const int hb = it % HB, bb = it / HB;
         if (hb == 0) {
@@ -517,7 +551,7 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
             if (tid == 0) {
                 tc::fence_async_smem();
                 issue_rec(bb + 1);
-                if (!tl.rec_bad && !tc::mbar_wait(tc::smem_u32(&tl.rfull[bb & 1]), (uint32_t)((bb >> 1) & 1))) {
+                if (!tl.rec_bad && !tc::mbar_wait(tc::smem_u32(&tl.rfull[bb & 1]), (uint32_t)((bb >> 1) & 1), WL)) {
                     tl.rec_bad = 1;
                     set_error(a.err, GDN_DEVERR_TIMEOUT);
                 }
@@ -530,16 +564,20 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
         const int n = u / d.hk, kh = u % d.hk, h = kh * G + gi;
         const long long out_row = (long long)n * d.hv * DV;
         const int rslot = __float_as_int(rc[R.slot]);
-        const int slot = (tl.rec_bad || rslot >= d.n_slots) ? -1 : rslot;
-        // ---- this head's state has arrived?
-        if (!timed_out && !tc::mbar_wait(tc::smem_u32(&tl.full[it % NS]), (uint32_t)((it / NS) & 1))) {
-            timed_out = true;
+        int slot = (tl.rec_bad || rslot >= d.n_slots) ? -1 : rslot;
+        // ---- this head's state has arrived?  A wait that gives up marks the CTA dead; from
+        // the barrier below on, every thread treats this and every later item as a padding
+        // lane (no state store), and no further copy is issued.
+        bool here = slot >= 0 && !tl.dead;
+        if (here && !tc::mbar_wait(tc::smem_u32(&tl.full[it % NS]), (uint32_t)((it / NS) & 1), WL)) {
+            here = false;
+            tl.dead = 1;
             set_error(a.err, GDN_DEVERR_TIMEOUT);
         }
         const unsigned char *Sb = reinterpret_cast<const unsigned char *>(slots) + (it % NS) * Cfg::SLOT;
         float4 m[RPT];
         float kr[RPT];
-        if (slot >= 0) {
+        if (here) {
             float qr[RPT];
             if constexpr (Q8) {
                 Q8Io<DK, DV>::load(m, reinterpret_cast<const int8_t *>(Sb),
@@ -565,9 +603,11 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
             *reinterpret_cast<float4 *>(&tl.red_s[rg][c4]) = ss;
         }
         __syncthreads();  // (A) every thread holds its part of the slot in registers
-        if (tid == 0 && it + NS < n_items) {
+        if (tl.dead) slot = -1;
+        if (tid == 0 && !tl.dead && it + NS < n_items) {
             tc::fence_async_smem();
             issue(it + NS);
+            n_issued = it + NS + 1;
         }
         if (slot < 0) {   // padding lane: zero output row of this head
             for (int j = tid; j < DV; j += NT) out[out_row + (long long)h * DV + j] = from_f32<TOut>(0.f);
@@ -598,8 +638,10 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
                 m[x].w = ga * m[x].w + kr[x] * u4.w;
             }
             if constexpr (Q8) {
-                Q8Io<DK, DV>::store(m, a.q8 + head * DK * DV, a.q8_scale + head * DK, hframe,
-                                    (uint32_t)(head * DK * DV), rg, c4, lane);
+                Q8Io<DK, DV>::template store<EF>(
+                    m, a.q8 + head * DK * DV, a.q8_scale + head * DK, hframe, (uint32_t)(head * DK * DV), rg,
+                    c4, lane, reinterpret_cast<const __nv_bfloat16 *>(Sb + DK * DV + DK * 4),
+                    EF ? a.q8_res + head * DK * DV : nullptr);
             } else {
                 float *Mg = a.state + head * DK * DV;
 #pragma unroll
@@ -619,16 +661,27 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
                 from_f32<TOut>(ov * rs * tl.nw[tid] * rc[R.z + gi * DV + tid]);
         }
     }
+    // After a timeout, shared memory must outlive every copy still in flight: thread 0 waits
+    // (bounded) for the state copies it issued and never consumed, and for the next batch of
+    // records.  Without a timeout every issued copy has been waited for already.
+    __syncthreads();
+    if (tid == 0 && (tl.dead || tl.rec_bad)) {
+        for (int j = n_issued - NS < 0 ? 0 : n_issued - NS; j < n_issued; ++j)
+            tc::mbar_wait(tc::smem_u32(&tl.full[j % NS]), (uint32_t)((j / NS) & 1), WL);
+        for (int b = 0; b < 2; ++b)
+            tc::mbar_wait(tc::smem_u32(&tl.rfull[b]), 0u, WL), tc::mbar_wait(tc::smem_u32(&tl.rfull[b]), 1u, WL);
+    }
 }
 
-template <int DK, int DV, typename TA, typename TOut, bool Q8 = false>
+template <int DK, int DV, typename TA, typename TOut, bool Q8 = false, bool EF = false>
 static cudaError_t launch_stream_t(const DecodeArgs &a, cudaStream_t s) {
     const int units = a.n * a.d.hk;
     decode_prep_kernel<DK, DV, TA><<<units, 256, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto kern = decode_stream_kernel<DK, DV, TOut, Q8>;
-    constexpr size_t smem = stream_smem_bytes<DK, DV, Q8>();
+    auto kern = decode_stream_kernel<DK, DV, TOut, Q8, EF>;
+    constexpr size_t smem = stream_smem_bytes<DK, DV, Q8, EF>();
+    static_assert(smem <= 227 * 1024, "the state ring and its tail exceed one CTA's shared memory");
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // programmatic dependent launch: overlaps this kernel's launch and its
@@ -702,9 +755,11 @@ namespace gdn {
 namespace {
 
 // fp32 pool <-> Q8 pool, one CTA per (slot, head)
+// (to Q8 with a residual pool: the first encode of an error-feedback pool, residual in = 0)
 template <int DK, int DV>
 __global__ void __launch_bounds__(4 * DV) q8_convert_kernel(Dims d, const float *state, int8_t *codes,
-                                                            float *scales, uint32_t frame, bool to_q8) {
+                                                            float *scales, __nv_bfloat16 *res,
+                                                            uint32_t frame, bool to_q8) {
     using Q = Q8Io<DK, DV>;
     const int tid = threadIdx.x, lane = tid & 31;
     const long long head = blockIdx.x;                       // slot * HV + h
@@ -716,7 +771,12 @@ __global__ void __launch_bounds__(4 * DV) q8_convert_kernel(Dims d, const float 
 #pragma unroll
         for (int x = 0; x < Q::RPT; ++x)
             m[x] = *reinterpret_cast<const float4 *>(state + head * DK * DV + (rg + x * Q::RPP) * DV + c4);
-        Q::store(m, cp, sp, pcg_hash(frame), (uint32_t)(head * DK * DV), rg, c4, lane);
+        if (res) {
+            Q::template store<true>(m, cp, sp, pcg_hash(frame), (uint32_t)(head * DK * DV), rg, c4, lane,
+                                    nullptr, res + head * DK * DV);
+        } else {
+            Q::store(m, cp, sp, pcg_hash(frame), (uint32_t)(head * DK * DV), rg, c4, lane);
+        }
     } else {
         Q::load(m, cp, sp, rg, c4);
         float *out = const_cast<float *>(state);
@@ -728,7 +788,9 @@ __global__ void __launch_bounds__(4 * DV) q8_convert_kernel(Dims d, const float 
 
 template <int D, typename TA, typename TOut>
 cudaError_t launch_q8_t(const DecodeArgs &a, cudaStream_t s) {
-    return launch_stream_t<D, D, TA, TOut, true>(a, s);   // prep + the streaming kernel on Q8 slots
+    // prep + the streaming kernel on Q8 slots (with the residual when error feedback is on)
+    return a.q8_res ? launch_stream_t<D, D, TA, TOut, true, true>(a, s)
+                    : launch_stream_t<D, D, TA, TOut, true, false>(a, s);
 }
 
 template <int D>
@@ -753,13 +815,13 @@ cudaError_t launch_decode_q8(const DecodeArgs &a, bool in_bf16, bool out_bf16, c
 }
 
 cudaError_t launch_q8_convert(const Dims &d, const float *state, int8_t *codes, float *scales,
-                              uint32_t frame, bool to_q8, cudaStream_t s) {
+                              __nv_bfloat16 *res, uint32_t frame, bool to_q8, cudaStream_t s) {
     const long long heads = (long long)d.n_slots * d.hv;
     if (heads == 0) return cudaSuccess;
     switch (d.dk) {
-        case 32: q8_convert_kernel<32, 32><<<(unsigned)heads, 128, 0, s>>>(d, state, codes, scales, frame, to_q8); break;
-        case 64: q8_convert_kernel<64, 64><<<(unsigned)heads, 256, 0, s>>>(d, state, codes, scales, frame, to_q8); break;
-        case 128: q8_convert_kernel<128, 128><<<(unsigned)heads, 512, 0, s>>>(d, state, codes, scales, frame, to_q8); break;
+        case 32: q8_convert_kernel<32, 32><<<(unsigned)heads, 128, 0, s>>>(d, state, codes, scales, res, frame, to_q8); break;
+        case 64: q8_convert_kernel<64, 64><<<(unsigned)heads, 256, 0, s>>>(d, state, codes, scales, res, frame, to_q8); break;
+        case 128: q8_convert_kernel<128, 128><<<(unsigned)heads, 512, 0, s>>>(d, state, codes, scales, res, frame, to_q8); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

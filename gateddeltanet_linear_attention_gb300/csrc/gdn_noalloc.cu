@@ -16,7 +16,10 @@
 // cannot use the array's name as a device address, so the address is looked
 // up once per device with cudaGetSymbolAddress (on the first call made while
 // that device is current) and cached; make that first call before any stream
-// capture.  All calls share the one array and it keeps the last call's
+// capture.  The cache lives as long as the device's context: after
+// cudaDeviceReset (or any teardown of the primary context) the cached address
+// is stale, so a process that resets a device must not call this entry point
+// on it again.  All calls share the one array and it keeps the last call's
 // contents: two calls whose work overlaps on the GPU (different streams, or
 // different host threads) race on it and must be serialised by the caller.
 // Nothing in it needs to start at zero: every intermediate a call reads is
@@ -55,9 +58,11 @@ gdn_status scratch_address(void **out) {
 extern "C" gdn_status gdn_mixer_prefill_static(const gdn_config *cfg, const gdn_mixer_io *io,
                                                void *stream) {
     if (!cfg || !io || io->T < 0 || io->n_seqs < 0) return GDN_ERR_INVALID_ARG;
-    const size_t need = gdn_workspace_size(cfg, io->T, io->n_seqs);
-    if (need == 0) return gdn_mixer_prefill(cfg, io, nullptr, 0, stream);  // its config status
-    if (need > kScratchBytes) return GDN_ERR_WORKSPACE; // too many tokens for the fixed scratch
+    if (gdn_workspace_size(cfg, io->T, io->n_seqs) == 0)
+        return gdn_mixer_prefill(cfg, io, nullptr, 0, stream);  // the configuration's own status
+    // only the prefill's own intermediates have to fit
+    if (gdn::mixer_prefill_ws_bytes(cfg, io->T, io->n_seqs) > kScratchBytes)
+        return GDN_ERR_WORKSPACE;   // too many tokens for the fixed scratch
     void *ws = nullptr;
     const gdn_status st = scratch_address(&ws);
     if (st != GDN_OK) return st;

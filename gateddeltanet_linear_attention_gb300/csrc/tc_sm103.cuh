@@ -234,15 +234,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Bounded wait for the phase with the given parity: false once kWaitNs of
-// wall-clock time have passed without the phase completing.
+// Bounded wait for the phase with the given parity: false once limit_ns of
+// wall-clock time (default kWaitNs; the library's callers pass the configured
+// limit) or kSpinLimit polls have passed without the phase completing.
 constexpr uint64_t kWaitNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint32_t saddr, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t saddr, uint32_t parity, uint64_t limit_ns = kWaitNs) {
     if (mbar_try_wait(saddr, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(saddr, parity)) return true;
-        if ((i & 63u) == 63u && globaltimer_ns() - t0 > kWaitNs) return false;
+        if ((i & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) return false;
     }
     return false;
 }

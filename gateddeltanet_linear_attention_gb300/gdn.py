@@ -91,13 +91,14 @@ def load(path: str | None = None):
             "gdn_state_copy": ([CP, P, P, I32, P, P, I32, P, P, I32, V], I32),
             "gdn_mixer_verify": ([CP, ctypes.POINTER(MixerIO), I32, P, P, SZ, V], I32),
             "gdn_backward_workspace_size": ([CP, I64, I32], SZ),
-            "gdn_state_to_q8": ([CP, P, P, P, U32, V], I32),
+            "gdn_state_to_q8": ([CP, P, P, P, P, U32, V], I32),
             "gdn_state_from_q8": ([CP, P, P, P, V], I32),
-            "gdn_mixer_decode_q8": ([CP, ctypes.POINTER(MixerIO), P, P, U32, P, SZ, V], I32),
+            "gdn_mixer_decode_q8": ([CP, ctypes.POINTER(MixerIO), P, P, P, U32, P, SZ, V], I32),
             "gdn_chunk_states": ([CP, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, SZ, V], I32),
             "gdn_chunk_backward": ([CP, P, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, P, P,
                                     I64, P, P, P, P, P, SZ, V], I32),
             "gdn_device_error": ([V, ctypes.POINTER(U32)], I32),
+            "gdn_debug_set_wait": ([ctypes.c_uint64, U32], I32),
             "gdn_status_string": ([I32], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -236,9 +237,10 @@ def gdn_mixer_decode(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, s
                                    _stream(stream)), "gdn_mixer_decode")
 
 
-def gdn_state_to_q8(cfg, state, codes, scales, frame, stream=None):
-    _check(load().gdn_state_to_q8(ctypes.byref(cfg), _ptr(state), _ptr(codes), _ptr(scales), frame,
-                                  _stream(stream)), "gdn_state_to_q8")
+def gdn_state_to_q8(cfg, state, codes, scales, frame, stream=None, residual=None):
+    """residual (bf16 [slots][HV][dk][dv], optional): written for an error-feedback pool."""
+    _check(load().gdn_state_to_q8(ctypes.byref(cfg), _ptr(state), _ptr(codes), _ptr(scales),
+                                  _ptr(residual), frame, _stream(stream)), "gdn_state_to_q8")
 
 
 def gdn_state_from_q8(cfg, codes, scales, state, stream=None):
@@ -247,14 +249,15 @@ def gdn_state_from_q8(cfg, codes, scales, state, stream=None):
 
 
 def gdn_mixer_decode_q8(cfg, x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, y, codes, scales,
-                        conv_state, frame, workspace, state_idx=None, stream=None):
+                        conv_state, frame, workspace, state_idx=None, stream=None, residual=None):
     """gdn_mixer_decode on a Q8 state pool (codes int8 [slots][HV][dk][dv], scales fp32
-    [slots][HV][dk]); `frame` keys the rounding dither and should change every step."""
+    [slots][HV][dk]); `frame` keys the rounding dither and should change every step.  A bf16
+    `residual` pool of the codes' shape turns error feedback on."""
     io = _mixer_io(x, z, u, b_logit, conv_w, A_log, dt_bias, norm_w, None, None, None,
                    conv_state, state_idx, y, x.shape[0])
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().gdn_mixer_decode_q8(ctypes.byref(cfg), ctypes.byref(io), _ptr(codes), _ptr(scales),
-                                      frame, _ptr(workspace), ws_bytes, _stream(stream)),
+                                      _ptr(residual), frame, _ptr(workspace), ws_bytes, _stream(stream)),
            "gdn_mixer_decode_q8")
 
 
@@ -341,6 +344,12 @@ def gdn_device_error(stream=None) -> int:
     if st not in (0, 5):
         raise GDNError(st, "gdn_device_error")
     return code.value
+
+
+def gdn_debug_set_wait(wait_ns=2_000_000_000, lose=0):
+    """Limit of every bounded device wait (ns) and the test hook that drops one operand copy
+    (bit 0: decode, bit 1: state chain); gdn_debug_set_wait() restores the defaults."""
+    _check(load().gdn_debug_set_wait(wait_ns, lose), "gdn_debug_set_wait")
 
 
 def gdn_status_string(status: int) -> str:

@@ -224,28 +224,39 @@ gdn_status gdn_mixer_decode(const gdn_config *cfg, const gdn_mixer_io *io, void 
 /* Q8 recurrent state: int8 codes [n_slots][HV][dk][dv] with one fp32 scale
  * per state row, [n_slots][HV][dk] (the row of dk index i holds M[i][0..dv)),
  * so M[i][j] = code[i][j] * scale[i]: about 4x fewer state bytes per decode
- * step.  The state is encoded with stochastic rounding: scale = max_j |M_ij| /
- * 127, code = clamp(floor(M_ij * (127 / max) + u), -127, 127), every step an
- * fp32 operation rounded to nearest.  The dither u = (2 b + 1) / 512 takes
- * its byte b from a counter-based hash: with e = ((slot * HV + head) * dk +
- * i) * dv + j (uint32), code e uses byte e & 3 of
- * pcg_hash((e >> 2) ^ pcg_hash(frame)), pcg_hash being the PCG hash of
- * Jarzynski and Olano (JCGT 2020).  The rounding error then has zero mean, so it does not build up a
- * bias over many steps: the error feedback the pages ask of a quantised state
- * (hyperflare release notes: a DeltaNet Q8 state whose dither is keyed by a
- * frame counter).  The caller passes a new frame every step.
+ * step (warpfront/hipfire PR #527 thread, STEP-004 note: a DeltaNet Q8 state
+ * requantised stochastically, with an error-feedback residual; issue #588: the
+ * dither is keyed by a frame counter).  The value x of a row is encoded with
+ * stochastic rounding: scale = max_j |x_ij| / 127, code = clamp(floor(x_ij *
+ * (127 / max) + u), -127, 127), every step an fp32 operation rounded to
+ * nearest, a zero row giving scale 0 and codes 0.  Every code draws its own
+ * dither u = (r >> 8) * 2^-24, r = pcg_hash(e ^ pcg_hash(frame)), e = ((slot *
+ * HV + head) * dk + i) * dv + j (uint32), pcg_hash being the PCG hash of
+ * Jarzynski and Olano (JCGT 2020).  The expected code is then exact, so the
+ * rounding adds no bias.  The caller passes a new frame every step.
+ *
+ * Error feedback (optional): `residual` (bf16 [n_slots][HV][dk][dv], 16-byte
+ * aligned, NULL = off) holds the rounding error the last encode left.  With
+ * it, the value encoded is x = M_new + residual and the residual becomes
+ * bf16(x - code * scale).  The running sum of the decoded states then tracks
+ * the running sum of the exact ones to within one residual, instead of
+ * drifting like a random walk.  The recurrence itself reads only the codes.
+ * It costs 2 more bytes per element in each direction.
  *
  * gdn_state_to_q8 / gdn_state_from_q8: convert the whole pool (cfg->n_slots
- * slots) between fp32 [n_slots][HV][dk][dv] and Q8.
+ * slots) between fp32 [n_slots][HV][dk][dv] and Q8; with a residual, to_q8
+ * is the first encode of an error-feedback pool (residual in = 0) and
+ * writes the residual.
  * gdn_mixer_decode_q8: gdn_mixer_decode on a Q8 pool; io->state_in and
  * io->state_out must be NULL; io->conv_state is required; same workspace as
- * gdn_mixer_decode. */
+ * gdn_mixer_decode.  A non-NULL residual turns error feedback on: it is read
+ * and rewritten for the active slots. */
 gdn_status gdn_state_to_q8(const gdn_config *cfg, const float *state, int8_t *codes, float *scales,
-                           uint32_t frame, void *stream);
+                           void *residual, uint32_t frame, void *stream);
 gdn_status gdn_state_from_q8(const gdn_config *cfg, const int8_t *codes, const float *scales,
                              float *state, void *stream);
 gdn_status gdn_mixer_decode_q8(const gdn_config *cfg, const gdn_mixer_io *io, int8_t *codes,
-                               float *scales, uint32_t frame, void *workspace,
+                               float *scales, void *residual, uint32_t frame, void *workspace,
                                size_t workspace_bytes, void *stream);
 
 /* Backward of the gated delta rule core from retained chunk-boundary states
@@ -342,6 +353,20 @@ gdn_status gdn_state_copy(const gdn_config *cfg, const float *src_state, const v
                           int32_t n_src_slots, float *dst_state, void *dst_conv,
                           int32_t n_dst_slots, const int32_t *src_idx, const int32_t *dst_idx,
                           int32_t n, void *stream);
+
+/* Bounded waits (no page counterpart: it makes the device-side timeout
+ * testable without a GPU fault).  Every wait of a kernel on another part of
+ * the kernel (an mbarrier, a copy, a peer CTA's flag) gives up after wait_ns
+ * nanoseconds (default 2 s), records GDN_DEVERR_TIMEOUT, skips the rest of
+ * its work and returns; the caller reads the bit with gdn_device_error().
+ * `lose` (tests only; 0 in normal use) makes the calls that follow drop one
+ * operand copy so that such a wait really runs out: bit 0 the first head
+ * state of a gdn_mixer_decode / gdn_mixer_decode_q8 launch, bit 1 the first
+ * chunk operand of the tensor-core state chain (gdn_chunk_prefill,
+ * gdn_mixer_prefill).  A call that timed out writes no state.  Process-wide,
+ * read at each call; GDN_ERR_INVALID_ARG for wait_ns = 0, above 60 s, or an
+ * unknown bit. */
+gdn_status gdn_debug_set_wait(uint64_t wait_ns, uint32_t lose);
 
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device into *code (HOST pointer; GDN_DEVERR_* bits).  Returns

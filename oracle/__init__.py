@@ -172,6 +172,33 @@ def mixer(x, conv_w, u, b_logit, A_log, dt_bias, z, norm_w, cu_seqlens, HK, HV, 
     return out
 
 
+def head_channels(HK, HV, dk, dv, kheads):
+    """For a subset of q/k heads (with their HV/HK v-heads each): the channel indices into the raw
+    projection [q (HK*dk) | k (HK*dk) | v (HV*dv)], the v-head indices, and the columns of
+    [T, HV*dv] outputs they own.  Heads never interact, so running the mixer on such a subset
+    gives exactly the subset's share of the full result."""
+    G = HV // HK
+    vheads = [kh * G + j for kh in kheads for j in range(G)]
+    q = [kh * dk + i for kh in kheads for i in range(dk)]
+    k = [HK * dk + kh * dk + i for kh in kheads for i in range(dk)]
+    v = [2 * HK * dk + h * dv + j for h in vheads for j in range(dv)]
+    cols = [h * dv + j for h in vheads for j in range(dv)]
+    return np.array(q + k + v), np.array(vheads), np.array(cols)
+
+
+def mixer_heads(x, conv_w, u, b_logit, A_log, dt_bias, z, norm_w, cu_seqlens, HK, HV, dk, dv,
+                kheads, state=None, conv_state=None, **kw):
+    """mixer() on the q/k heads `kheads` only: the inputs are the full-width tensors, sliced
+    here; state [slots, HV, dk, dv] and conv_state [slots, CH, 3] likewise (absent: zeros)."""
+    chs, vh, cols = head_channels(HK, HV, dk, dv, list(kheads))
+    n_seqs = len(np.asarray(cu_seqlens)) - 1
+    st = np.zeros((n_seqs, len(vh), dk, dv)) if state is None else _f64(state)[:, vh]
+    cs = np.zeros((n_seqs, len(chs), 3)) if conv_state is None else _f64(conv_state)[:, chs]
+    return mixer(_f64(x)[:, chs], _f64(conv_w)[chs], _f64(u)[:, vh], _f64(b_logit)[:, vh],
+                 _f64(A_log)[vh], _f64(dt_bias)[vh], _f64(z)[:, cols], norm_w, cu_seqlens,
+                 len(list(kheads)), len(vh), dk, dv, state=st, conv_state=cs, **kw)
+
+
 def state_copy(src_state, src_conv, dst_state, dst_conv, src_idx, dst_idx):
     """Slot maintenance (hyperflare core-design, "State operations": snapshot, restore and
     reset as indirect copies over slot indices).  For each pair (s, t): t < 0 does nothing;

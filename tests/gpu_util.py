@@ -38,12 +38,8 @@ def cfg_for(wl, n_slots):
 
 def head_channels(wl, kheads):
     """Channel indices (into CH) and v-head indices for a subset of q/k heads."""
-    G = wl.HV // wl.HK
-    vheads = [kh * G + j for kh in kheads for j in range(G)]
-    q = [kh * wl.dk + i for kh in kheads for i in range(wl.dk)]
-    k = [wl.HK * wl.dk + kh * wl.dk + i for kh in kheads for i in range(wl.dk)]
-    v = [2 * wl.HK * wl.dk + h * wl.dv + j for h in vheads for j in range(wl.dv)]
-    return np.array(q + k + v), np.array(vheads)
+    chs, vh, _ = oracle.head_channels(wl.HK, wl.HV, wl.dk, wl.dv, kheads)
+    return chs, vh
 
 
 def vcols(wl, vheads):
@@ -52,10 +48,9 @@ def vcols(wl, vheads):
 
 def oracle_mixer(wl, inp, kheads=None, prefix="", x=None, u=None, b=None, z=None, cu=None,
                  state=None, conv_state=None, slot_idx=None, dumps=False, n_threads=None):
-    """Run the oracle on (a head subset of) a workload's inputs."""
+    """Run the oracle on (a head subset of) a workload's inputs (full-width tensors, sliced to
+    the subset by oracle.mixer_heads)."""
     kheads = list(range(wl.HK)) if kheads is None else list(kheads)
-    chs, vh = head_channels(wl, kheads)
-    cols = vcols(wl, vh)
     x = inp[prefix + "x"] if x is None else x
     u = inp[prefix + "u"] if u is None else u
     b = inp[prefix + "b_logit"] if b is None else b
@@ -63,14 +58,9 @@ def oracle_mixer(wl, inp, kheads=None, prefix="", x=None, u=None, b=None, z=None
     st = inp["state"] if state is None else state
     cs = inp["conv_state"] if conv_state is None else conv_state
     cu = inp["cu_seqlens"] if cu is None else cu
-    n_seqs = len(cu) - 1
-    # absent state / history = zeros, passed explicitly so the final values come back
-    st = np.zeros((n_seqs, len(vh), wl.dk, wl.dv)) if st is None else oracle._f64(st)[:, vh]
-    cs = np.zeros((n_seqs, len(chs), 3)) if cs is None else oracle._f64(cs)[:, chs]
-    return oracle.mixer(
-        x[:, chs], inp["conv_w"][chs], u[:, vh], b[:, vh], inp["A_log"][vh], inp["dt_bias"][vh],
-        z[:, cols], inp["norm_w"], cu, len(kheads), len(vh), wl.dk, wl.dv,
-        state=st, conv_state=cs, slot_idx=slot_idx, dumps=dumps, n_threads=n_threads)
+    return oracle.mixer_heads(x, inp["conv_w"], u, b, inp["A_log"], inp["dt_bias"], z, inp["norm_w"], cu,
+                              wl.HK, wl.HV, wl.dk, wl.dv, kheads, state=st, conv_state=cs,
+                              slot_idx=slot_idx, dumps=dumps, n_threads=n_threads)
 
 
 class GpuMixer:

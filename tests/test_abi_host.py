@@ -214,21 +214,23 @@ def test_mixer_verify_validation(lib):
 def test_q8_validation(lib):
     c = cfg()
     ch = ctypes.byref(c)
-    assert lib.gdn_state_to_q8(ch, None, A16, A16b, 0, None) == INVALID
-    assert lib.gdn_state_to_q8(ch, A16, MIS, A16b, 0, None) == INVALID
+    assert lib.gdn_state_to_q8(ch, None, A16, A16b, None, 0, None) == INVALID
+    assert lib.gdn_state_to_q8(ch, A16, MIS, A16b, None, 0, None) == INVALID
     assert lib.gdn_state_from_q8(ch, A16, None, A16b, None) == INVALID
     assert lib.gdn_state_from_q8(ch, A16, A16b, MIS, None) == INVALID
     c0 = cfg(n_slots=0)                                                 # an empty pool: nothing to do
-    assert lib.gdn_state_to_q8(ctypes.byref(c0), A16, A16, A16b, 0, None) == OK
+    assert lib.gdn_state_to_q8(ctypes.byref(c0), A16, A16, A16b, None, 0, None) == OK
     need = lib.gdn_workspace_size(ch, 4, 4)
     q8io = _io(T=4, n=4, conv_state=A16b)                               # no fp32 state pointers
     bad = _io(T=4, n=4, state_in=A16, state_out=A16, conv_state=A16b)   # fp32 state given
-    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(bad), A16, A16b, 0, A16, need, None) == INVALID
+    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(bad), A16, A16b, None, 0, A16, need, None) == INVALID
     bad = _io(T=4, n=4)                                                 # no conv history
-    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(bad), A16, A16b, 0, A16, need, None) == INVALID
+    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(bad), A16, A16b, None, 0, A16, need, None) == INVALID
     bad = _io(T=5, n=4, conv_state=A16b)                                # T != n_seqs
-    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(bad), A16, A16b, 0, A16, need, None) == INVALID
-    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(q8io), None, A16b, 0, A16, need, None) == INVALID
-    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(q8io), A16, MIS, 0, A16, need, None) == INVALID
-    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(q8io), A16, A16b, 0, A16, 64, None) == WORKSPACE
-    assert lib.gdn_mixer_decode_q8(ctypes.byref(c0), ctypes.byref(q8io), A16, A16b, 0, A16, need, None) == INVALID
+    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(bad), A16, A16b, None, 0, A16, need, None) == INVALID
+    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(q8io), None, A16b, None, 0, A16, need, None) == INVALID
+    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(q8io), A16, MIS, None, 0, A16, need, None) == INVALID
+    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(q8io), A16, A16b, MIS, 0, A16, need, None) == INVALID
+    assert lib.gdn_state_to_q8(ch, A16, A16, A16b, MIS, 0, None) == INVALID   # misaligned residual
+    assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(q8io), A16, A16b, None, 0, A16, 64, None) == WORKSPACE
+    assert lib.gdn_mixer_decode_q8(ctypes.byref(c0), ctypes.byref(q8io), A16, A16b, None, 0, A16, need, None) == INVALID

@@ -152,3 +152,10 @@ def test_backward_shapes_and_no_final_state_term(HK, HV, d, chunk):
 def test_backward_bf16_inputs():
     b = Batch((100, 60), HK=2, HV=4, d=128, chunk=64, dtype=torch.bfloat16, seed=77)
     _check_backward(b, "bwd bf16 inputs")
+
+
+def test_backward_at_the_benchmarked_length():
+    """8,192 tokens (the length bench.py times), two q/k heads and their four v-heads: every
+    chunk's workspace slab of the full-length walk is compared through the gradients."""
+    b = Batch((8192,), HK=2, HV=4, d=128, chunk=64, seed=8192)
+    _check_backward(b, "bwd 8192 tokens")

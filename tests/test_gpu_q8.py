@@ -1,14 +1,16 @@
-"""Q8 recurrent state on the GPU against the oracle (a quantised state with
-error feedback, the DeltaNet Q8 state of the hyperflare release notes: int8
-codes with per-row scales, stochastic rounding keyed by a frame counter).
+"""Q8 recurrent state on the GPU against the oracle (the DeltaNet Q8 state of
+the warpfront/hipfire PR #527 thread: int8 codes with per-row scales,
+stochastic requantisation with a dither keyed by a frame counter, and an
+optional error-feedback residual).
 
 The encoder and decoder are bit-exact against oracle.q8_encode / q8_decode
 (every step an fp32 operation rounded to nearest, the same counter-based
-dither on both sides).  The Q8 decode step is compared with
-oracle.mixer_decode_q8: y within the bf16 tolerance and the decoded state
-within a few rounding steps (the two sides round states that differ in the
-last fp32 bits, so a code may land one step apart).  A 64-step run against the
-fp32 decode reports the drift the quantised state adds."""
+dither on both sides), with and without the residual.  The Q8 decode step is
+compared with oracle.mixer_decode_q8: y within the bf16 tolerance and the
+decoded state (plus residual) within a few rounding steps (the two sides
+round states that differ in the last fp32 bits, so a code may land one step
+apart).  A 256-step run against the fp32 decode reports the drift the
+quantised state adds, with and without error feedback."""
 import numpy as np
 import pytest
 import torch
@@ -42,32 +44,39 @@ def _inputs(n, HK, HV, d, steps, seed):
         b=[rn(n, HV).to(torch.bfloat16) for _ in range(steps)])
 
 
+@pytest.mark.parametrize("ef", [False, True])
 @pytest.mark.parametrize("d,frame", [(128, 0), (64, 7), (32, 123456789)])
-def test_q8_encode_decode_bitwise(d, frame):
+def test_q8_encode_decode_bitwise(d, frame, ef):
     cfg = gdn.make_config(2, 4, d, d, 64 if d == 128 else 16, "bf16", 3)
     g = torch.Generator().manual_seed(d)
     st = torch.randn((3, 4, d, d), generator=g) * torch.rand((3, 4, d, 1), generator=g) * 2
     st[1, 2, 5] = 0                                                  # a zero row
     codes = torch.empty((3, 4, d, d), dtype=torch.int8, device="cuda")
     scales = torch.empty((3, 4, d), device="cuda")
-    gdn.gdn_state_to_q8(cfg, st.cuda(), codes, scales, frame)
+    res = torch.full((3, 4, d, d), float("nan"), dtype=torch.bfloat16, device="cuda") if ef else None
+    gdn.gdn_state_to_q8(cfg, st.cuda(), codes, scales, frame, residual=res)
     back = torch.empty((3, 4, d, d), device="cuda")
     gdn.gdn_state_from_q8(cfg, codes, scales, back)
     torch.cuda.synchronize()
-    ec, es = oracle.q8_encode(st.numpy(), frame)
+    if ef:
+        ec, es, er = oracle.q8_encode(st.numpy(), frame, residual=np.zeros(st.shape, np.float32))
+        assert np.array_equal(res.float().cpu().numpy().view(np.int32), er.view(np.int32))
+    else:
+        ec, es = oracle.q8_encode(st.numpy(), frame)
     assert np.array_equal(codes.cpu().numpy(), ec)
     assert np.array_equal(scales.cpu().numpy().view(np.int32), es.view(np.int32))
     assert np.array_equal(back.cpu().numpy().view(np.int32), oracle.q8_decode(ec, es).view(np.int32))
 
 
-def _gpu_q8_run(inp, n, HK, HV, d, steps, frame0, state_idx=None, n_slots=None):
+def _gpu_q8_run(inp, n, HK, HV, d, steps, frame0, state_idx=None, n_slots=None, ef=False):
     cfg = gdn.make_config(HK, HV, d, d, 64 if d == 128 else 16, "bf16", n_slots or n)
     slots = n_slots or n
     st = torch.zeros((slots, HV, d, d)); st[:n] = inp["state"]
     cv = torch.zeros((slots, inp["CH"], 3), dtype=torch.bfloat16); cv[:n] = inp["conv"]
     codes = torch.empty((slots, HV, d, d), dtype=torch.int8, device="cuda")
     scales = torch.empty((slots, HV, d), device="cuda")
-    gdn.gdn_state_to_q8(cfg, st.cuda(), codes, scales, frame0)
+    res = torch.empty((slots, HV, d, d), dtype=torch.bfloat16, device="cuda") if ef else None
+    gdn.gdn_state_to_q8(cfg, st.cuda(), codes, scales, frame0, residual=res)
     conv = cv.cuda()
     ws = torch.empty(gdn.gdn_workspace_size(cfg, n, n), dtype=torch.uint8, device="cuda")
     si = None if state_idx is None else torch.tensor(state_idx, dtype=torch.int32, device="cuda")
@@ -76,31 +85,51 @@ def _gpu_q8_run(inp, n, HK, HV, d, steps, frame0, state_idx=None, n_slots=None):
         y = torch.empty((n, HV * d), device="cuda")
         gdn.gdn_mixer_decode_q8(cfg, inp["x"][t].cuda(), inp["z"][t].cuda(), inp["u"][t].cuda(),
                                 inp["b"][t].cuda(), inp["cw"].cuda(), inp["A"].cuda(), inp["dt"].cuda(),
-                                inp["nw"].cuda(), y, codes, scales, conv, frame0 + 1 + t, ws, state_idx=si)
+                                inp["nw"].cuda(), y, codes, scales, conv, frame0 + 1 + t, ws, state_idx=si,
+                                residual=res)
         ys.append(y)
     torch.cuda.synchronize()
-    return torch.stack(ys), codes, scales, conv
+    out = (torch.stack(ys), codes, scales, conv)
+    return out + (res,) if ef else out
 
 
-def test_q8_decode_matches_oracle():
+@pytest.mark.parametrize("ef", [False, True])
+def test_q8_decode_matches_oracle(ef):
     n, HK, HV, d, steps = 3, 2, 4, 128, 6
     inp = _inputs(n, HK, HV, d, steps, seed=41)
-    y, codes, scales, conv = _gpu_q8_run(inp, n, HK, HV, d, steps, frame0=10)
+    got = _gpu_q8_run(inp, n, HK, HV, d, steps, frame0=10, ef=ef)
+    y, codes, scales, conv = got[:4]
     assert gdn.gdn_device_error() == 0
-    oc, os_ = oracle.q8_encode(inp["state"].numpy(), 10)
+    if ef:
+        oc, os_, ores = oracle.q8_encode(inp["state"].numpy(), 10, residual=np.zeros((n, HV, d, d), np.float32))
+    else:
+        oc, os_ = oracle.q8_encode(inp["state"].numpy(), 10)
+        ores = None
     ocv = oracle._f64(inp["conv"])
-    worst_y, worst_steps = 0.0, 0.0
+    worst_y = 0.0
     for t in range(steps):
-        oy, oc, os_, ocv = oracle.mixer_decode_q8(inp["x"][t], inp["cw"], inp["u"][t], inp["b"][t], inp["A"],
-                                                  inp["dt"], inp["z"][t], inp["nw"], HK, HV, d, d, oc, os_,
-                                                  ocv, frame=11 + t)
+        out = oracle.mixer_decode_q8(inp["x"][t], inp["cw"], inp["u"][t], inp["b"][t], inp["A"], inp["dt"],
+                                     inp["z"][t], inp["nw"], HK, HV, d, d, oc, os_, ocv, frame=11 + t,
+                                     residual=ores)
+        oy, oc, os_, ocv = out[:4]
+        if ef:
+            ores = out[4]
         worst_y = max(worst_y, rel_max(y[t], oy))
     deq_g = oracle.q8_decode(codes.cpu().numpy(), scales.cpu().numpy())
     deq_o = oracle.q8_decode(oc, os_)
     step = np.maximum(os_, scales.cpu().numpy())[..., None]
-    worst_steps = float(np.max(np.abs(deq_g - deq_o) / np.where(step > 0, step, 1)))
+    steps_off = np.abs(deq_g - deq_o) / np.where(step > 0, step, 1)
+    worst_steps = float(np.max(steps_off))
     diff_codes = float(np.mean(codes.cpu().numpy() != oc))
-    report("q8 decode 6 steps", y=worst_y, state_steps=worst_steps, codes_differ=diff_codes)
+    extra = {}
+    if ef:
+        # what the pool represents, codes plus residual, agrees far below one step
+        res_g = got[4].float().cpu().numpy()
+        carried = np.abs((deq_g + res_g) - (deq_o + ores)) / np.where(step > 0, step, 1)
+        extra = dict(carried_steps_max=float(np.max(carried)), carried_steps_mean=float(np.mean(carried)))
+        assert float(np.mean(carried)) <= 1e-2
+    report("q8%s decode 6 steps" % (" EF" if ef else ""), y=worst_y, state_steps=worst_steps,
+           codes_differ=diff_codes, **extra)
     assert worst_y <= TOL_BF16
     assert worst_steps <= 4.0 and diff_codes <= 1e-2
     assert np.array_equal(conv.float().cpu().numpy(), ocv)             # the history: raw inputs
@@ -125,12 +154,14 @@ def _rms_rel(a, b):
 
 
 def test_q8_drift_against_fp32_decode():
-    """64 steps from the same state: the Q8 path's y against the fp32 path's.  The rounding
-    noise is unbiased, so it is damped by the decay instead of accumulating: the RMS error of y
-    over the last 16 steps is no larger (up to sampling noise) than over the first 16."""
-    n, HK, HV, d, steps = 4, 2, 4, 128, 64
+    """256 steps from the same state: the Q8 path's y and state against the fp32 path's, with and
+    without error feedback.  The rounding noise is unbiased, so without feedback it is damped by
+    the decay instead of accumulating: the RMS error of y over the last 64 steps is no larger (up
+    to sampling noise) than over the first 64.  With feedback the error is smaller still."""
+    n, HK, HV, d, steps = 4, 2, 4, 128, 256
     inp = _inputs(n, HK, HV, d, steps, seed=43)
     yq, codes, scales, _ = _gpu_q8_run(inp, n, HK, HV, d, steps, frame0=100)
+    ye, codes_e, scales_e, _, res_e = _gpu_q8_run(inp, n, HK, HV, d, steps, frame0=100, ef=True)
     cfg = gdn.make_config(HK, HV, d, d, 64, "bf16", n)
     st = inp["state"].clone().cuda(); cv = inp["conv"].clone().cuda()
     ws = torch.empty(gdn.gdn_workspace_size(cfg, n, n), dtype=torch.uint8, device="cuda")
@@ -141,11 +172,17 @@ def test_q8_drift_against_fp32_decode():
                              inp["cw"].cuda(), inp["A"].cuda(), inp["dt"].cuda(), inp["nw"].cuda(), y, st, cv, ws)
         yf.append(y)
     torch.cuda.synchronize()
+    assert gdn.gdn_device_error() == 0
     yf = torch.stack(yf)
-    first, last = _rms_rel(yq[:16], yf[:16]), _rms_rel(yq[-16:], yf[-16:])
-    deq = oracle.q8_decode(codes.cpu().numpy(), scales.cpu().numpy())
-    es = _rms_rel(torch.tensor(deq), st)
-    report("q8 drift vs fp32 (64 steps, RMS)", y_first16=first, y_last16=last, state=es,
-           y_max_abs=max(rel_max(yq[t], yf[t].cpu().numpy()) for t in range(steps)))
-    assert first <= 0.05 and last <= 0.05 and es <= 0.05
-    assert last <= 2.0 * first + 0.005
+    out = {}
+    for tag, yy, cc, ss in (("plain", yq, codes, scales), ("ef", ye, codes_e, scales_e)):
+        deq = oracle.q8_decode(cc.cpu().numpy(), ss.cpu().numpy())
+        out[tag] = dict(first64=_rms_rel(yy[:64], yf[:64]), last64=_rms_rel(yy[-64:], yf[-64:]),
+                        state=_rms_rel(torch.tensor(deq), st),
+                        y_max=max(rel_max(yy[t], yf[t].cpu().numpy()) for t in range(steps)))
+    report("q8 drift vs fp32 decode (256 steps, RMS-relative)",
+           **{f"{k}_{m}": v for k, d_ in out.items() for m, v in d_.items()})
+    p, e = out["plain"], out["ef"]
+    assert p["first64"] <= 0.05 and p["last64"] <= 0.05 and p["state"] <= 0.05
+    assert p["last64"] <= 2.0 * p["first64"] + 0.005
+    assert e["last64"] <= p["last64"] and e["state"] <= p["state"]
