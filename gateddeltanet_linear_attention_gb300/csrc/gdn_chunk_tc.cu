@@ -50,13 +50,13 @@ constexpr int TC_DK = 128;   // dk == dv
 constexpr int TP_HALF = 128 * 64 * 2;     // one bf16 part of [T ; PT] (K-major, K = 64)
 constexpr int TP_BYTES = 2 * TP_HALF;     // hi + lo, as stored in the workspace
 constexpr int WQ_BYTES = 2 * 128 * 128 * 2;             // [-W ; Q'] hi + lo (K-major, K = 128)
-constexpr int KT_HALF = 128 * 64 * 2;                   // K~ (MN-major, MN = 128, K = 64), one part
-constexpr int KT_BYTES = 2 * KT_HALF;
+constexpr int KT_HALF = 128 * 64 * 2;                   // K (MN-major, MN = 128, K = 64), one part
+constexpr int KT_BYTES = 2 * KT_HALF;                   // workspace bytes per (chunk, q/k head)
 constexpr int CH_DVS = 32;                              // state columns per chain CTA
 constexpr uint32_t NP_EMPTY = 0xFFFFFFFFu;   // unwritten npart entry: a NaN no sum of squares takes
 constexpr int BV_SLICE = 2 * CH_DVS * 64 * 2;           // [bV_hi | bV_lo] of one slice (MN-major, MN = 64, K = 64)
-constexpr int OFF_CH_WQ = TP_BYTES, OFF_CH_KT = OFF_CH_WQ + WQ_BYTES, OFF_CH_BV = OFF_CH_KT + KT_BYTES;
-constexpr int CH_BYTES = OFF_CH_BV + (128 / CH_DVS) * BV_SLICE;   // workspace bytes per (chunk, v-head)
+constexpr int OFF_CH_WQ = TP_BYTES;
+constexpr int CH_BYTES = TP_BYTES + WQ_BYTES;           // workspace bytes per (chunk, v-head)
 
 // Store 8 values at byte offset `off` (16-byte aligned) of a hi and a lo tile
 // (packed two-at-a-time conversions).
@@ -306,13 +306,24 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(ChunkArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-(chunk, v-head) operands of the state chain, written to the workspace:
+// Per-(chunk, q/k head) operands of the state chain, written to the workspace.
+// One CTA per (chunk, q/k head): the q/k rows are loaded and normalised once,
+// the Gram products [K;Q] K^T are formed once, and the CTA then walks the G
+// v-heads that share that q/k head (each has its own gates).  Per v-head:
 //   TP = [T ; PT]          K-major (M = 128, K = 64),  hi then lo   (32 KB)
 //   WQ = [-W ; gQ - PW]    K-major (M = 128, K = 128), hi then lo   (64 KB)
-// Shared memory: the [K;Q] hi/lo Gram operand (64 KB) and bgK (MN-major, the B
-// operand of W, 32 KB).  Once G1 has consumed [K;Q], its bytes hold the fp32 A
-// (T^T above the diagonal), P and T^T as bf16 operands, the solve's scratch,
-// and finally [T ; PT].
+//   G_last and the row decays exp(G_last - G_r)
+// and once per q/k head the normalised K, MN-major (MN = dk, K = 64 tokens),
+// hi then lo (32 KB): the operand of the chain's state increment K^T U~, the
+// decays being applied to the rows of U' there.
+// W = T diag(beta gamma) K is issued as (T diag(beta gamma)) K: the columns of
+// the staged [T ; PT] are scaled by beta_c gamma_c before the hi/lo split, so
+// the B operand is the plain K every v-head shares.  The workspace copy of
+// [T ; PT] is the unscaled one.
+// Shared memory: the [K;Q] hi/lo Gram operand (64 KB), then per v-head over
+// the same bytes: the fp32 A (T^T above the diagonal), P and T^T as bf16
+// operands, the solve's scratch, the scaled [T ; PT], finally [-W ; Q'];
+// and K (MN-major, hi/lo, 32 KB) for the whole CTA.
 struct TpSmem {
     static constexpr int KQ = 128 * 128 * 2;
     static constexpr int OPH = 64 * 64 * 2;                // one bf16 part of a 64x64 operand
@@ -320,15 +331,25 @@ struct TpSmem {
     static constexpr int OFF_SA = 0;                       // fp32 [64][65]
     static constexpr int OFF_P = (64 * 65 * 4 + 1023) & ~1023;   // P (M = 64, K = 64), hi + lo
     static constexpr int OFF_B2 = OFF_P + 2 * OPH;         // B2[c][k] = T[k][c], hi + lo; solve scratch before
-    static constexpr int OFF_A3 = OFF_P;                   // [T ; PT] hi + lo, after P and B2 are consumed
-    static constexpr int OFF_B3 = 2 * KQ;                  // beta gamma K (MN-major, MN = 128, K = 64), hi + lo
-    static constexpr int OFF_G = OFF_B3 + 2 * 128 * 64 * 2;        // G[64], beta[64], q factor[64]
-    static constexpr int OFF_BAR = OFF_G + 3 * 64 * 4;     // mbarrier, tmem slot, flag, search
+    static constexpr int OFF_A3 = OFF_P;                   // scaled [T ; PT] hi + lo, after P and B2 are consumed
+    static constexpr int OFF_B3 = 2 * KQ;                  // K (MN-major, MN = 128, K = 64), hi + lo
+    static constexpr int OFF_G = OFF_B3 + KT_BYTES;        // G[64], beta[64], q factor[64], beta gamma[64]
+    static constexpr int OFF_BAR = OFF_G + 4 * 64 * 4;     // mbarrier, tmem slot, flag, search
     static constexpr int BYTES = OFF_BAR + 32;
     static_assert(OFF_B2 + 2 * OPH <= 2 * KQ, "PT operands exceed the Gram region");
     static_assert(OFF_A3 + TP_BYTES <= 2 * KQ, "[T ; PT] exceeds the Gram region");
     static_assert(OFF_B2 + 2 * 32 * 33 * 4 <= OFF_B2 + 2 * OPH, "solve scratch exceeds B2");
+    static_assert(OFF_SA + 64 * 65 * 4 <= OFF_A3, "T (in A) overlaps the [T ; PT] stage");
 };
+
+// The TMEM columns of chunk_tp_kernel: G1 (kept for every v-head), PT, W.
+constexpr uint32_t TP_COL_G1 = 0, TP_COL_PT = 64, TP_COL_W = 128, TP_TMEM_COLS = 256;
+
+// Store 8 values at byte offset `off` of a hi and a lo tile in global memory
+// (16-byte stores).
+__device__ __forceinline__ void put8g(unsigned char *hi, unsigned char *lo, uint32_t off, const float *v) {
+    put8(hi, lo, off, v);
+}
 
 template <typename TIn>
 __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
@@ -340,10 +361,11 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     unsigned char *b2h = sm + L::OFF_B2, *b2l = b2h + L::OPH;
     float *sY = reinterpret_cast<float *>(sm + L::OFF_B2);      // solve scratch (before B2)
     unsigned char *a3h = sm + L::OFF_A3, *a3l = a3h + TP_HALF;
-    unsigned char *b3h = sm + L::OFF_B3, *b3l = b3h + 128 * 64 * 2;
+    unsigned char *b3h = sm + L::OFF_B3, *b3l = b3h + KT_HALF;
     float *sG = reinterpret_cast<float *>(sm + L::OFF_G);
     float *sB = sG + 64;
     float *sFq = sG + 128;
+    float *sBG = sG + 192;
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 8);
     volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 12);
@@ -351,9 +373,8 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = (int)(blockIdx.x % (unsigned)d.hv);
-    const long long j = blockIdx.x / (unsigned)d.hv;
-    const int kh = h / d.grp;
+    const int kh = (int)(blockIdx.x % (unsigned)d.hk);
+    const long long j = blockIdx.x / (unsigned)d.hk;
     const int total = a.chunk_base[a.n_seqs];
     if (j >= total || j >= a.max_chunks) return;
 
@@ -374,12 +395,9 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     long long s, e;
     seq_bounds(a.cu_seqlens, lo, a.T, nullptr, s, e);   // malformed bounds are reported by the map
     const long long t0 = s + (j - a.chunk_base[lo]) * TC_C;
-    if (a.npart) a.npart[(j * d.hv + h) * 256 + tid] = __uint_as_float(NP_EMPTY);   // (fused norm)
-    unsigned char *gtp = a.tp + ((long long)j * d.hv + h) * CH_BYTES;   // [T ; PT]
-    unsigned char *gwq = gtp + OFF_CH_WQ;                                // [-W ; Q']
 
     if (warp == 0) {
-        tc::tmem_alloc(tc::smem_u32(tmem_slot), 128);
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), TP_TMEM_COLS);
         tc::tmem_relinquish();
     }
     if (tid == 32) {
@@ -395,20 +413,47 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
 
-    // ---- rows of K and Q (L2-normalised) and gates; operands [K;Q] (K-major) and bgK
-    // (MN-major); K~ and beta V for the state chain straight to the workspace
+    // ---- rows of K and Q (L2-normalised): the Gram operand [K;Q] (K-major) and K (MN-major),
+    // which also leaves for the workspace as the chain's operand (one bulk store)
     {
         const int ir = il_row(tid), iq = il_q(tid);
-        float kv[32], qv[32], vv[32];
+        float kv[32], qv[32];
         const long long t = t0 + ir;
         if (t < e) {
             load_row_il((const TIn *)a.k + t * a.ld_qk + (long long)kh * TC_DK, iq, kv);
             load_row_il((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK, iq, qv);
-            load_row_il((const TIn *)a.v + t * a.ld_v + (long long)h * TC_DK, iq, vv);
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = vv[i] = 0.f;
+            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
         }
+        const float fq = l2 ? l2norm_row_il(qv, d.l2_eps, d.q_scale) : 1.f;
+        if (l2) l2norm_row_il(kv, d.l2_eps, 1.f);
+        if (iq == 0) sFq[ir] = fq;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = 16 * i + 4 * iq;          // first of this group's 4 columns (dk)
+            put4(kqh, kql, tc::kmaj_off(ir, c, 128), &kv[4 * i]);
+            put4(kqh, kql, tc::kmaj_off(64 + ir, c, 128), &qv[4 * i]);
+            put4(b3h, b3l, tc::mnmaj_off(c, ir, 128), &kv[4 * i]);
+        }
+    }
+    sync_for_mma();
+    // ---- G1: [K;Q] K^T -> K K^T (TMEM lanes 0-63), Q K^T (64-127), columns 0-63; K -> workspace
+    if (tid == 0) {
+        tc::bulk_s2g(a.kt + ((long long)j * d.hk + kh) * KT_BYTES, tc::smem_u32(b3h), KT_BYTES);
+        tc::bulk_commit();
+        mma3<false, false, 128>(tbase + TP_COL_G1, tc::smem_u32(kqh), tc::smem_u32(kql), 0,
+                                tc::smem_u32(kqh), tc::smem_u32(kql), 0, tc::idesc_bf16(128, 64), false);
+        tc::mma_commit(tc::smem_u32(mbar));
+    }
+    bool ok = ms.wait(tid);
+
+    for (int gi = 0; gi < d.grp && ok; ++gi) {
+        const int h = kh * d.grp + gi;
+        if (a.npart) a.npart[(j * d.hv + h) * 256 + tid] = __uint_as_float(NP_EMPTY);   // (fused norm)
+        unsigned char *gtp = a.tp + ((long long)j * d.hv + h) * CH_BYTES;   // [T ; PT]
+        unsigned char *gwq = gtp + OFF_CH_WQ;                                // [-W ; Q']
+        // ---- gates of this v-head: G (cumulative), beta, beta gamma, the row decays
         if (tid < TC_C) {
             const long long tt = t0 + tid;
             sG[tid] = tt < e ? a.g[tt * d.hv + h] : 0.f;
@@ -416,52 +461,20 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
         }
         __syncthreads();
         if (warp == 0) scan64(sG, lane);
-        const float fq = l2 ? l2norm_row_il(qv, d.l2_eps, d.q_scale) : 1.f;
-        if (l2) l2norm_row_il(kv, d.l2_eps, 1.f);
-        if (iq == 0) sFq[ir] = fq;
         __syncthreads();
-        const float Gr = sG[ir], br = sB[ir], Gl = sG[TC_C - 1];
-        const float bg = br * expf(Gr), kdec = expf(Gl - Gr);
-        unsigned char *gkt = gtp + OFF_CH_KT;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int c = 16 * i + 4 * iq;          // first of this group's 4 columns (dk)
-            put4(kqh, kql, tc::kmaj_off(ir, c, 128), &kv[4 * i]);
-            put4(kqh, kql, tc::kmaj_off(64 + ir, c, 128), &qv[4 * i]);
-            float t4[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) t4[j] = bg * kv[4 * i + j];
-            put4(b3h, b3l, tc::mnmaj_off(c, ir, 128), t4);
-            // the chain's G5 operand: K~ = exp(G_last - G_r) k_r (MN-major)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) t4[j] = kdec * kv[4 * i + j];
-            put4(gkt, gkt + KT_HALF, tc::mnmaj_off(c, ir, 128), t4);
-            // the chain's G2 operand: beta v, as one concatenated [hi | lo] tile (MN-major,
-            // MN = 2 CH_DVS) per state slice of CH_DVS columns
-#pragma unroll
-            for (int j = 0; j < 4; ++j) t4[j] = br * vv[4 * i + j];
-            unsigned char *gbv = gtp + OFF_CH_BV + (c / CH_DVS) * BV_SLICE;
-            const int m = c % CH_DVS;
-            put4(gbv + tc::mnmaj_off(m, ir, 2 * CH_DVS), gbv + tc::mnmaj_off(CH_DVS + m, ir, 2 * CH_DVS), 0u, t4);
+        if (tid < TC_C) {
+            const float Gr = sG[tid], Gl = sG[TC_C - 1];
+            sBG[tid] = sB[tid] * expf(Gr);
+            a.kdec[((long long)j * d.hv + h) * TC_C + tid] = expf(Gl - Gr);
+            if (tid == 0) a.gl[j * d.hv + h] = Gl;
         }
-        if (tid == 0) a.gl[j * d.hv + h] = Gl;
-    }
-    sync_for_mma();
-    // ---- G1: [K;Q] K^T -> K K^T (TMEM lanes 0-63), Q K^T (64-127), columns 0-63
-    if (tid == 0) {
-        mma3<false, false, 128>(tbase, tc::smem_u32(kqh), tc::smem_u32(kql), 0, tc::smem_u32(kqh),
-                                tc::smem_u32(kql), 0, tc::idesc_bf16(128, 64), false);
-        tc::mma_commit(tc::smem_u32(mbar));
-    }
-    bool ok = ms.wait(tid);
-    if (ok) {
         // ---- E1: A (strictly lower, fp32) and P (lower incl. the diagonal, bf16 hi/lo
         // operand), over the Gram region.  The decay factors exp(G_r - G_c) <= 1 use the
         // approximate-exp intrinsic (relative error about 1e-6, far below the 2^-16 of the
         // split operands they feed).
         {
             float v32[32];
-            tc::tmem_ld32(tbase + lane_off + hf * 32, v32);
+            tc::tmem_ld32(tbase + TP_COL_G1 + lane_off + hf * 32, v32);
             const int r = tl & 63;
             const float Gr = sG[r];
             if (qd < 2) {
@@ -580,86 +593,92 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
             put8(b2h, b2l, tc::kmaj_off(r2, c8, 64), t8);
         }
         sync_for_mma();
+        sync_for_mma();
         // ---- G: P . T (M = 64) into columns 64-127: row r lands on TMEM lane 32*(r/16) + r%16
         if (tid == 0) {
-            mma3<false, false, 64>(tbase + 64, tc::smem_u32(ph), tc::smem_u32(pl), 0, tc::smem_u32(b2h),
+            mma3<false, false, 64>(tbase + TP_COL_PT, tc::smem_u32(ph), tc::smem_u32(pl), 0, tc::smem_u32(b2h),
                                    tc::smem_u32(b2l), 0, tc::idesc_bf16(64, 64), false);
             tc::mma_commit(tc::smem_u32(mbar));
         }
         ok = ms.wait(tid);
-    }
-    if (ok) {
-        // ---- [T ; PT] -> A3 (shared, operand of W) and the workspace
+        if (!ok) break;
+        // ---- [T ; PT]: unscaled to the workspace (16-byte stores), columns scaled by beta gamma
+        // into A3 (shared, the A operand of W)
         for (int task = tid; task < 64 * 8; task += TC_NT) {
             const int r2 = (task >> 6) * 8 + (task & 7), c8 = ((task >> 3) & 7) * 8;
-            float t8[8];
+            float t8[8], s8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int c = c8 + i;
                 t8[i] = (c < r2) ? sA[c * 65 + r2] : ((c == r2) ? 1.f : 0.f);
+                s8[i] = t8[i] * sBG[c];
             }
-            put8(a3h, a3l, tc::kmaj_off(r2, c8, 64), t8);
+            const uint32_t off = tc::kmaj_off(r2, c8, 64);
+            put8g(gtp, gtp + TP_HALF, off, t8);
+            put8(a3h, a3l, off, s8);
         }
         {
             float v32[32];
-            tc::tmem_ld32(tbase + 64 + lane_off + hf * 32, v32);
+            tc::tmem_ld32(tbase + TP_COL_PT + lane_off + hf * 32, v32);
             if (lane < 16) {
                 const int r2 = qd * 16 + lane;
 #pragma unroll
                 for (int k8 = 0; k8 < 32; k8 += 8) {
-                    put8(a3h, a3l, tc::kmaj_off(64 + r2, hf * 32 + k8, 64), &v32[k8]);
+                    float s8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) s8[i] = v32[k8 + i] * sBG[hf * 32 + k8 + i];
+                    const uint32_t off = tc::kmaj_off(64 + r2, hf * 32 + k8, 64);
+                    put8g(gtp, gtp + TP_HALF, off, &v32[k8]);
+                    put8(a3h, a3l, off, s8);
                 }
             }
         }
         sync_for_mma();
-        // ---- W: [T ; PT] . bgK -> W (lanes 0-63), PW (64-127), columns 0-127; [T ; PT]
-        // also leaves for the workspace as one bulk store
+        // ---- W: (([T ; PT] diag(beta gamma)) K -> W (lanes 0-63), PW (64-127), columns 128-255
         if (tid == 0) {
-            tc::bulk_s2g(gtp, tc::smem_u32(a3h), TP_BYTES);
-            tc::bulk_commit();
-            mma3<false, true, 64>(tbase, tc::smem_u32(a3h), tc::smem_u32(a3l), 0, tc::smem_u32(b3h),
+            mma3<false, true, 64>(tbase + TP_COL_W, tc::smem_u32(a3h), tc::smem_u32(a3l), 0, tc::smem_u32(b3h),
                                   tc::smem_u32(b3l), 128, tc::idesc_bf16(128, 128) | tc::kTransB, false);
             tc::mma_commit(tc::smem_u32(mbar));
         }
-        // meanwhile: the q rows the Q' epilogue needs (lane mapping: row tl-64, half hf)
-        float qrow[64];
-        if (qd >= 2) {
-            const int r = tl - 64;
-            const long long t = t0 + r;
-            if (t < e) {
-                load_row<64>((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK + hf * 64, qrow);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) qrow[i] = 0.f;
-            }
-        }
-        if (tid == 0) tc::bulk_wait_read_all();   // [T ; PT] has left A3 (long before W completes)
         ok = ms.wait(tid);
-        if (ok) {
-            // ---- [-W ; gamma q - PW] -> shared (over the consumed Gram region), then one
-            // bulk store to the workspace (hi then lo, K-major, K = 128)
-            float v64[64];
-            tc::tmem_ld64(tbase + lane_off + hf * 64, v64);
-            if (qd < 2) {
+        if (!ok) break;
+        // ---- [-W ; gamma q - PW] -> shared (over the consumed Gram region), two passes of 32
+        // columns, then one bulk store to the workspace (hi then lo, K-major, K = 128)
+        {
+            const int r = tl - 64;                  // (Q' rows)
+            const long long t = t0 + r;
+            const float f = qd >= 2 ? sFq[r] * expf(sG[r]) : 0.f;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) v64[i] = -v64[i];
-            } else {
-                const int r = tl - 64;
-                const float f = sFq[r] * expf(sG[r]);
+            for (int pass = 0; pass < 2; ++pass) {
+                const int c0 = hf * 64 + pass * 32;
+                float v32[32];
+                tc::tmem_ld32(tbase + TP_COL_W + lane_off + c0, v32);
+                if (qd < 2) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) v64[i] = fmaf(f, qrow[i], -v64[i]);
-            }
+                    for (int i = 0; i < 32; ++i) v32[i] = -v32[i];
+                } else {
+                    float qrow[32];
+                    if (t < e) {
+                        load_row<32>((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK + c0, qrow);
+                    } else {
 #pragma unroll
-            for (int k8 = 0; k8 < 64; k8 += 8)
-                put8(kqh, kql, tc::kmaj_off(tl, hf * 64 + k8, 128), &v64[k8]);
-            tc::fence_async_smem();
-            __syncthreads();
-            if (tid == 0) {
-                tc::bulk_s2g(gwq, tc::smem_u32(kqh), WQ_BYTES);
-                tc::bulk_commit();
-                tc::bulk_wait_read_all();   // shared memory must outlive the reads, not the writes
+                        for (int i = 0; i < 32; ++i) qrow[i] = 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v32[i] = fmaf(f, qrow[i], -v32[i]);
+                }
+#pragma unroll
+                for (int k8 = 0; k8 < 32; k8 += 8) put8(kqh, kql, tc::kmaj_off(tl, c0 + k8, 128), &v32[k8]);
             }
         }
+        tc::fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc::bulk_s2g(gwq, tc::smem_u32(kqh), WQ_BYTES);
+            tc::bulk_commit();
+            tc::bulk_wait_read_all();   // the next v-head reuses these bytes
+        }
+        __syncthreads();
     }
     if (!ok) {
         if (tid == 0) {
@@ -668,9 +687,10 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
         }
         __syncthreads();
     }
+    if (tid == 0) tc::bulk_wait_read_all();   // K has left shared memory
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tbase, 128);
+    if (warp == 0) tc::tmem_dealloc(tbase, TP_TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -688,18 +708,19 @@ struct ChainSmem {
     static constexpr int WQ = 128 * 128 * 2;               // [-W ; Q'] K-major, K = 128, per part
     static constexpr int MT = 2 * DVS * 128 * 2;           // [M_hi | M_lo] MN-major (MN = 2 DVS, K = 128)
     static constexpr int UT = 2 * DVS * 64 * 2;            // [U'_hi | U'_lo] MN-major (MN = 2 DVS, K = 64)
-    // bulk-copied from the workspace: WQ (hi then lo), [T ; PT] x 2 buffers, [bV_hi | bV_lo], K~ (hi then lo)
+    // bulk-copied from the workspace: WQ (hi then lo), [T ; PT] x 2 buffers, K (hi then lo); the
+    // [bV_hi | bV_lo] tiles (x 2 buffers) are built in the kernel from V and beta
     static constexpr int OFF_WQ = 0;
     static constexpr int OFF_TP = OFF_WQ + 2 * WQ;
     static constexpr int OFF_BV = OFF_TP + 2 * TP_BYTES;   // x 2 buffers
     static constexpr int OFF_KT = OFF_BV + 2 * BV_SLICE;
     static constexpr int OFF_MT = OFF_KT + KT_BYTES;
     static constexpr int OFF_UT = OFF_MT + MT;
-    static constexpr int OFF_BAR = OFF_UT + UT;            // 14 mbarriers; tmem slot and 4 flags (3 words)
+    static constexpr int OFF_BAR = OFF_UT + UT;            // 16 mbarriers; tmem slot and 2 flags (3 words)
     static constexpr int SOS = DVS + 4;                    // row stride of the O tiles (conflict-free float4)
-    static constexpr int OFF_SO = OFF_BAR + 144;           // fused norm: O rows x 2 buffers (fp32 [64][SOS])
+    static constexpr int OFF_SO = OFF_BAR + 160;           // fused norm: O rows x 2 buffers (fp32 [64][SOS])
     static constexpr int BYTES = OFF_SO + 2 * 64 * SOS * 4;
-    static_assert(DVS == CH_DVS, "the workspace holds bV in slices of CH_DVS columns");
+    static_assert(DVS == CH_DVS, "one bV tile per CH_DVS-column slice");
     static_assert(OFF_TP % 16 == 0 && OFF_BV % 16 == 0 && OFF_KT % 16 == 0, "bulk-copy alignment");
 };
 
@@ -735,20 +756,27 @@ __device__ __forceinline__ void tmem_ld_cat16(uint32_t taddr, float (&v)[16]) {
 
 // Warp roles: warp 8 copies every operand of the state chain from the
 // workspace (bulk copies) and issues every MMA; warps 0-7 (256 threads) run
-// the two epilogues, which carry the state.  The sides meet only on
-// mbarriers, each wait bounded in time, so a lost arrival ends in an error
-// flag rather than a hang:
+// the two epilogues, which carry the state; warps 9-10 (64 threads, one token
+// row each) build the [bV_hi | bV_lo] tile of each chunk from V and beta two
+// chunks ahead.  The sides meet only on mbarriers, each wait bounded in time,
+// so a lost arrival ends in an error flag rather than a hang:
 //   mtbar (256 arrivals)  M entering chunk c is in shared memory
-//   utbar (256 arrivals)  U' of chunk c is in shared memory
+//   utbar (256 arrivals)  U~ of chunk c is in shared memory
 //   g3bar (MMA commit)    D3 of chunk c complete (G2 + G3)
 //   g5bar (MMA commit)    D5 of chunk c complete (G5)
-//   wq/tp/bv/kt bars      operand copies landed
+//   bvbar (64 arrivals)   bV of chunk c is in its buffer
+//   bvfree (MMA warp)     G2 of chunk c has read buffer c & 1 (it may take chunk c + 2)
+//   wq/tp/kt bars         operand copies landed
+// U~ is U' with row r scaled by exp(G_last - G_r), so that G5 = K^T U~ needs
+// only the K every v-head of a q/k head shares.
 // Phase c of each completes once per chunk, and no phase can complete twice
 // before its waiter looks, because each depends on the other side's progress.
 // The critical path is M -> G3 -> E3 -> G5 -> E5 -> M; G2 of chunk c+1 is
 // issued right behind G5 of chunk c.
-constexpr int CHAIN_NT = 288;
-constexpr int CHAIN_NT_NORM = 416;   // + 4 warps (9-12) applying the fused gated norm
+constexpr int CHAIN_NT = 352;
+constexpr int CHAIN_NT_NORM = 480;   // + 4 warps (11-14) applying the fused gated norm
+constexpr int CHAIN_BV_T0 = 288;     // first thread of the bV warps (9-10)
+constexpr int CHAIN_NORM_T0 = 352;   // first thread of the norm warps
 
 __device__ __forceinline__ void bar_sync_staging() {   // warps 0-7 only
     asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -773,7 +801,7 @@ __device__ __forceinline__ void arrive_staged(uint64_t *bar) {
     tc::mbar_arrive(tc::smem_u32(bar));
 }
 
-// The fused gated RMSNorm runs on four extra warps (9-12), off the chain's
+// The fused gated RMSNorm runs on four extra warps (11-14), off the chain's
 // path: E3 hands each chunk's O rows over through a double-buffered tile in
 // shared memory (mbarriers obar / ofree).  A row's sum of squares spans all dv
 // columns, which the four slice CTAs of a head hold a quarter each: a slice
@@ -809,10 +837,10 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint64_t *wqbar = bars + 0, *tpbar = bars + 1 /* [2] */, *bvbar = bars + 3 /* [2] */,
              *ktbar = bars + 5, *mtbar = bars + 6, *utbar = bars + 7, *g3bar = bars + 8, *g5bar = bars + 9;
-    uint64_t *obar = bars + 10 /* [2] */, *ofree = bars + 12 /* [2] */;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
-    volatile uint32_t *flag3 = reinterpret_cast<uint32_t *>(bars + 14) + 1;
-    volatile uint32_t *flag5 = reinterpret_cast<uint32_t *>(bars + 15);
+    uint64_t *obar = bars + 10 /* [2] */, *ofree = bars + 12 /* [2] */, *bvfree = bars + 14 /* [2] */;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    volatile uint32_t *flag3 = reinterpret_cast<uint32_t *>(bars + 16) + 1;
+    volatile uint32_t *flag5 = reinterpret_cast<uint32_t *>(bars + 17);
     float *sO = reinterpret_cast<float *>(sm + L::OFF_SO);     // [2][64][SOS]
 
     const Dims &d = a.d;
@@ -852,8 +880,10 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
         tc::mbar_init(tc::smem_u32(wqbar), 1);
         tc::mbar_init(tc::smem_u32(&tpbar[0]), 1);
         tc::mbar_init(tc::smem_u32(&tpbar[1]), 1);
-        tc::mbar_init(tc::smem_u32(&bvbar[0]), 1);
-        tc::mbar_init(tc::smem_u32(&bvbar[1]), 1);
+        tc::mbar_init(tc::smem_u32(&bvbar[0]), 64);
+        tc::mbar_init(tc::smem_u32(&bvbar[1]), 64);
+        tc::mbar_init(tc::smem_u32(&bvfree[0]), 1);
+        tc::mbar_init(tc::smem_u32(&bvfree[1]), 1);
         tc::mbar_init(tc::smem_u32(ktbar), 1);
         tc::mbar_init(tc::smem_u32(mtbar), 256);
         tc::mbar_init(tc::smem_u32(utbar), 256);
@@ -888,11 +918,9 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 fetch(&tpbar[i & 1], s_tp + (uint32_t)((i & 1) * TP_BYTES), src(i), TP_BYTES);
             };
             auto fetch_wq = [&](long long i) { fetch(wqbar, s_wqh, src(i) + OFF_CH_WQ, WQ_BYTES); };
-            auto fetch_bv = [&](long long i) {   // -> BV buffer i&1
-                fetch(&bvbar[i & 1], s_bv + (uint32_t)((i & 1) * BV_SLICE),
-                      src(i) + OFF_CH_BV + slice * BV_SLICE, BV_SLICE);
+            auto fetch_kt = [&](long long i) {   // K of the chunk's q/k head
+                fetch(ktbar, s_kth, a.kt + ((jc + i) * d.hk + h / d.grp) * KT_BYTES, KT_BYTES);
             };
-            auto fetch_kt = [&](long long i) { fetch(ktbar, s_kth, src(i) + OFF_CH_KT, KT_BYTES); };
             // G2 of chunk i: D3 = [T ; PT] . bV  (U, PU)
             auto issue_g2 = [&](long long i) -> bool {
                 const uint32_t par2 = (uint32_t)((i >> 1) & 1);
@@ -905,11 +933,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 return true;
             };
             fetch_tp(0);
-            fetch_bv(0);
-            if (n_chunks > 1) {
-                fetch_tp(1);
-                fetch_bv(1);
-            }
+            if (n_chunks > 1) fetch_tp(1);
             if (!(d.lose & LOSE_CHAIN_OPERAND_COPY)) fetch_wq(0);   // (tests: a lost copy)
             fetch_kt(0);
             long long ci = 0;
@@ -928,7 +952,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 if (ci + 1 < n_chunks) fetch_wq(ci + 1);
                 if (ci + 2 < n_chunks) {   // into the buffers G2 of this chunk has read
                     fetch_tp(ci + 2);
-                    fetch_bv(ci + 2);
+                    tc::mbar_arrive(tc::smem_u32(&bvfree[ci & 1]));
                 }
                 // G5: D5 = K~^T . U'
                 ok = tc::mbar_wait(tc::smem_u32(utbar), par, WL) && tc::mbar_wait(tc::smem_u32(ktbar), par, WL);
@@ -952,20 +976,45 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 for (int k = 0; k < 2; ++k) {    // each copy barrier: its current and next phase
                     tc::mbar_wait(tc::smem_u32(wqbar), (uint32_t)((ci + k) & 1), WL);
                     tc::mbar_wait(tc::smem_u32(ktbar), (uint32_t)((ci + k) & 1), WL);
-                    for (int b = 0; b < 2; ++b) {
-                        tc::mbar_wait(tc::smem_u32(&bvbar[b]), (uint32_t)(((ci + k) >> 1) & 1), WL);
+                    for (int b = 0; b < 2; ++b)
                         tc::mbar_wait(tc::smem_u32(&tpbar[b]), (uint32_t)(((ci + k) >> 1) & 1), WL);
-                    }
                 }
             } else {
                 tc::mbar_wait(tc::smem_u32(g5bar), (uint32_t)((n_chunks - 1) & 1), WL);   // last G5 retired
             }
         }
-    } else if (warp >= 9) {
-        // ================= fused gated norm (warps 9-12, NORM only) ================
+    } else if (warp == 9 || warp == 10) {
+        // ============ bV staging (warps 9-10): row r of chunk i's [bV_hi | bV_lo] tile ============
+        const int r = tid - CHAIN_BV_T0;
+        for (long long i = 0; i < n_chunks; ++i) {
+            const int b = (int)(i & 1);
+            // the buffer's previous chunk (i - 2) has been read by its G2
+            if (i >= 2 && !tc::mbar_wait(tc::smem_u32(&bvfree[b]), (uint32_t)(((i >> 1) - 1) & 1), WL)) {
+                set_error(a.err, GDN_DEVERR_TIMEOUT);
+                break;
+            }
+            const long long t = s + i * TC_C + r;
+            float v[DVS];
+            if (t < e) {
+                load_row<DVS>((const TIn *)a.v + t * a.ld_v + col0, v);
+                const float br = a.beta[t * d.hv + h];
+#pragma unroll
+                for (int jj = 0; jj < DVS; ++jj) v[jj] *= br;
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < DVS; ++jj) v[jj] = 0.f;
+            }
+            unsigned char *tile = sm + L::OFF_BV + b * BV_SLICE;
+#pragma unroll
+            for (int j8 = 0; j8 < DVS; j8 += 8) put8cat<DVS>(tile, j8, r, &v[j8]);
+            tc::fence_async_smem();
+            tc::mbar_arrive(tc::smem_u32(&bvbar[b]));
+        }
+    } else if (warp >= 11) {
+        // ================= fused gated norm (warps 11-14, NORM only) ================
         if constexpr (NORM) {
             static_assert(TC_DK / DVS == 4, "one 16-byte npart word per row");
-            const int nid = tid - 288, r = nid >> 1, hh = nid & 1;   // row r, columns hh*HALF ..
+            const int nid = tid - CHAIN_NORM_T0, r = nid >> 1, hh = nid & 1;   // row r, columns hh*HALF ..
             const int c = slice * DVS + hh * HALF;                     // column within the head
             auto np_row = [&](long long i) { return a.npart + (((jc + i) * d.hv + h) * 64 + r) * 4; };
             // z of the rows of chunk i (packed bf16, 16 values), loaded ahead of use
@@ -1086,13 +1135,18 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
             const int Lc = (int)((e - c0) < TC_C ? (e - c0) : TC_C);
             const bool has_next = c0 + TC_C < e;
             const uint32_t par = (uint32_t)(ci & 1);
-            // ---------------- E3: U' -> concatenated B operand -> utbar
+            // ---------------- E3: U~ (U' rows scaled by exp(G_last - G_r)) -> concatenated B
+            // operand -> utbar
+            const float kd = qd < 2 ? a.kdec[((jc + ci) * d.hv + h) * TC_C + tl] : 0.f;
             if (!staging_wait(g3bar, par, flag3, tid, WL)) break;
             float ov[HALF];
             tmem_ld_cat16<DVS>(T_D3 + lane_off + hf * HALF, ov);
             if (qd < 2) {
+                float us[HALF];
 #pragma unroll
-                for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(utt, hf * HALF + j8, tl, &ov[j8]);
+                for (int jj = 0; jj < HALF; ++jj) us[jj] = kd * ov[jj];
+#pragma unroll
+                for (int j8 = 0; j8 < HALF; j8 += 8) put8cat<DVS>(utt, hf * HALF + j8, tl, &us[j8]);
             }
             arrive_staged(utbar);
             if constexpr (NORM) {
@@ -1151,7 +1205,7 @@ static cudaError_t launch_tc_t(const ChunkArgs &a, cudaStream_t s) {
             auto tp = chunk_tp_kernel<TIn>;
             err = cudaFuncSetAttribute(tp, cudaFuncAttributeMaxDynamicSharedMemorySize, TpSmem::BYTES);
             if (err != cudaSuccess) return err;
-            tp<<<(unsigned)(a.max_chunks * a.d.hv), TC_NT, TpSmem::BYTES, s>>>(a);
+            tp<<<(unsigned)(a.max_chunks * a.d.hk), TC_NT, TpSmem::BYTES, s>>>(a);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     }
@@ -1181,13 +1235,29 @@ long long chunk_tc_max_chunks(long long T, long long n_seqs) {
     return T / TC_C + (n_seqs < T ? n_seqs : T);
 }
 
+// Workspace of the tensor-core chunked rule, each region 256-byte aligned: the chunk map, the
+// per-(chunk, v-head) operand blocks, the per-(chunk, q/k head) K blocks, G_last, the row
+// decays and the fused norm's partial sums.
+namespace {
+struct TcWs {
+    size_t base, tp, kt, gl, kdec, np, total;
+    TcWs(const Dims &d, long long mc, long long n_seqs) {
+        auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+        base = al(((size_t)n_seqs + 1) * 4);
+        tp = (size_t)mc * d.hv * CH_BYTES;
+        kt = (size_t)mc * d.hk * KT_BYTES;
+        gl = al((size_t)mc * d.hv * 4);
+        kdec = al((size_t)mc * d.hv * TC_C * 4);
+        np = al((size_t)mc * d.hv * (TC_DK / CH_DVS) * 64 * 4);
+        total = base + tp + kt + gl + kdec + np;
+    }
+};
+}  // namespace
+
 size_t chunk_tc_ws_bytes(const Dims &d, long long T, long long n_seqs) {
     const long long mc = chunk_tc_max_chunks(T, n_seqs);
     if (mc == 0) return 0;
-    const size_t base = (((size_t)n_seqs + 1) * 4 + 255) & ~(size_t)255;
-    const size_t gl = ((size_t)mc * d.hv * 4 + 255) & ~(size_t)255;
-    const size_t np = ((size_t)mc * d.hv * (TC_DK / CH_DVS) * 64 * 4 + 255) & ~(size_t)255;
-    return base + (size_t)mc * d.hv * CH_BYTES + gl + np;
+    return TcWs(d, mc, n_seqs).total;
 }
 
 void chunk_tc_carve(ChunkArgs &a, void *ws) {
@@ -1197,11 +1267,19 @@ void chunk_tc_carve(ChunkArgs &a, void *ws) {
         a.tp = nullptr;
         return;
     }
-    a.chunk_base = (int *)ws;
-    a.tp = (unsigned char *)ws + ((((size_t)a.n_seqs + 1) * 4 + 255) & ~(size_t)255);
-    a.gl = (float *)(a.tp + (size_t)a.max_chunks * a.d.hv * CH_BYTES);
-    const size_t mh = (size_t)a.max_chunks * a.d.hv;
-    a.npart = (float *)((unsigned char *)a.gl + ((mh * 4 + 255) & ~(size_t)255));
+    const TcWs w(a.d, a.max_chunks, a.n_seqs);
+    unsigned char *p = (unsigned char *)ws;
+    a.chunk_base = (int *)p;
+    p += w.base;
+    a.tp = p;
+    p += w.tp;
+    a.kt = p;
+    p += w.kt;
+    a.gl = (float *)p;
+    p += w.gl;
+    a.kdec = (float *)p;
+    p += w.kdec;
+    a.npart = (float *)p;
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, bool in_bf16, bool o_bf16, int dvs, bool fuse_norm,

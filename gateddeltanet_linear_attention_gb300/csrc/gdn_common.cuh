@@ -99,8 +99,10 @@ struct ChunkArgs {
     // tensor-core path: per-sequence chunk offsets and the [T ; PT] operands
     // (caller workspace, carved by chunk_tc_carve)
     int *chunk_base;
-    unsigned char *tp;
+    unsigned char *tp;    // [max_chunks][HV] blocks: [T ; PT] and [-W ; Q'] operands
+    unsigned char *kt;    // [max_chunks][HK] blocks: the normalised K (MN-major bf16 hi/lo)
     float *gl;            // G_last of every (chunk, v-head)
+    float *kdec;          // [max_chunks][HV][64]: exp(G_last - G_r) of every row
     long long max_chunks;
     // gated RMSNorm fused into the chain's output (then `o` receives y):
     // y = o * rsqrt(mean(o^2) + norm_eps) * w * SiLU(z) per (token, v-head)
