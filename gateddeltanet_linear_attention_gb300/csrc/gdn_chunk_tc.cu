@@ -340,10 +340,16 @@ struct TpSmem {
     static_assert(OFF_A3 + TP_BYTES <= 2 * KQ, "[T ; PT] exceeds the Gram region");
     static_assert(OFF_B2 + 2 * 32 * 33 * 4 <= OFF_B2 + 2 * OPH, "solve scratch exceeds B2");
     static_assert(OFF_SA + 64 * 65 * 4 <= OFF_A3, "T (in A) overlaps the [T ; PT] stage");
+    // the lower-left inverse block's MMA operands, over B2 and the bytes after it (A: 64 x 32,
+    // B: 32 x 32, bf16, per part)
+    static constexpr int XA = 64 * 32 * 2, XB = 32 * 32 * 2;
+    static constexpr int OFF_X = OFF_B2;
+    static_assert(OFF_X + 4 * XA + 4 * XB <= 2 * KQ, "inverse operands exceed the Gram region");
 };
 
 // The TMEM columns of chunk_tp_kernel: G1 (kept for every v-head), PT, W.
-constexpr uint32_t TP_COL_G1 = 0, TP_COL_PT = 64, TP_COL_W = 128, TP_TMEM_COLS = 256;
+// (TP_COL_INV: the two 32-column products of the inverse's lower-left block, before PT)
+constexpr uint32_t TP_COL_G1 = 0, TP_COL_PT = 64, TP_COL_INV = 64, TP_COL_W = 128, TP_TMEM_COLS = 256;
 
 // Store 8 values at byte offset `off` of a hi and a lo tile in global memory
 // (16-byte stores).
@@ -549,35 +555,65 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
             }
         }
         __syncthreads();
-        // Step 3: the lower-left 32x32 block: T[2][1] = -T[2][2] A[2][1] T[1][1] (32-blocks).
-        // Thread (warp w, lane jj) computes rows i = w + 8u (u < 4) of column jj; each
-        // element of T loaded serves the four rows.
+        // Step 3: the lower-left 32x32 block T[2][1] = -T[2][2] (A[2][1] T[1][1]) (32-blocks), as
+        // two products on the tensor cores (M = 64, the lower 32 rows of each A operand unused,
+        // split operands like every other product): Y = A21 T11, then Z = T22 Y.
         {
-            const int jj = lane;
-            float y[4] = {0.f, 0.f, 0.f, 0.f};
+            unsigned char *x1h = sm + L::OFF_X, *x1l = x1h + L::XA;            // A21 (K-major, K = 32)
+            unsigned char *y1h = x1l + L::XA, *y1l = y1h + L::XB;              // T11^T (K-major: row j, K k)
+            unsigned char *x2h = y1l + L::XB, *x2l = x2h + L::XA;              // T22 (K-major, K = 32)
+            unsigned char *y2h = x2l + L::XA, *y2l = y2h + L::XB;              // Y (MN-major, MN = 32)
+            for (int task = tid; task < 3 * 128; task += TC_NT) {
+                const int which = task >> 7, rr = (task & 127) >> 2, c8 = (task & 3) * 8;
+                float t8[8];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {        // Y = A[2][1] T[1][1]; T[k][jj] = 0 for k < jj
-                const float tkj = (k > jj) ? sA[jj * 65 + k] : ((k == jj) ? 1.f : 0.f);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) y[u] = fmaf(sA[(32 + warp + 8 * u) * 65 + k], tkj, y[u]);
+                for (int i = 0; i < 8; ++i) {
+                    const int c = c8 + i;
+                    if (which == 0) t8[i] = sA[(32 + rr) * 65 + c];                          // A21[rr][c]
+                    else if (which == 1) t8[i] = (c > rr) ? sA[rr * 65 + c] : (c == rr ? 1.f : 0.f);   // T11[c][rr]
+                    else t8[i] = (rr > c) ? sA[(32 + c) * 65 + 32 + rr] : (rr == c ? 1.f : 0.f);      // T22[rr][c]
+                }
+                if (which == 0) put8(x1h, x1l, tc::kmaj_off(rr, c8, 32), t8);
+                else if (which == 1) put8(y1h, y1l, tc::kmaj_off(rr, c8, 32), t8);
+                else put8(x2h, x2l, tc::kmaj_off(rr, c8, 32), t8);
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) sY[(warp + 8 * u) * 33 + jj] = y[u];
-            __syncthreads();
-            float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int m = 0; m < 32; ++m) {        // T[2][2] Y; T[32+i][32+m] = 0 for m > i
-                const float ym = sY[m * 33 + jj];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = warp + 8 * u;
-                    const float tim = (i > m) ? sA[(32 + m) * 65 + 32 + i] : ((i == m) ? 1.f : 0.f);
-                    z[u] = fmaf(tim, ym, z[u]);
+            sync_for_mma();
+            if (tid == 0) {
+                mma3<false, false, 32>(tbase + TP_COL_INV, tc::smem_u32(x1h), tc::smem_u32(x1l), 0,
+                                       tc::smem_u32(y1h), tc::smem_u32(y1l), 0, tc::idesc_bf16(64, 32), false);
+                tc::mma_commit(tc::smem_u32(mbar));
+            }
+            ok = ms.wait(tid);
+            if (!ok) break;
+            // Y rows m (0-31) sit on TMEM lanes 32*(m/16) + m%16: warps 0-1 (lanes < 16), with
+            // warps 4-5 taking the second 16 columns
+            if (qd == 0 || qd == 1) {   // (warp-uniform: the TMEM load is warp-wide)
+                float y16[16];
+                tc::tmem_ld16(tbase + TP_COL_INV + lane_off + hf * 16, y16);
+                if (lane < 16) {
+                    const int m = qd * 16 + lane;
+                    put8(y2h, y2l, tc::mnmaj_off(hf * 16, m, 32), &y16[0]);
+                    put8(y2h, y2l, tc::mnmaj_off(hf * 16 + 8, m, 32), &y16[8]);
                 }
             }
-            __syncthreads();                      // every read of the scratch is done
+            sync_for_mma();
+            if (tid == 0) {
+                mma3<false, true, 32>(tbase + TP_COL_INV + 32, tc::smem_u32(x2h), tc::smem_u32(x2l), 0,
+                                      tc::smem_u32(y2h), tc::smem_u32(y2l), 32,
+                                      tc::idesc_bf16(64, 32) | tc::kTransB, false);
+                tc::mma_commit(tc::smem_u32(mbar));
+            }
+            ok = ms.wait(tid);
+            if (!ok) break;
+            if (qd == 0 || qd == 1) {
+                float z16[16];
+                tc::tmem_ld16(tbase + TP_COL_INV + 32 + lane_off + hf * 16, z16);
+                if (lane < 16) {
+                    const int i = qd * 16 + lane;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) sA[jj * 65 + 32 + warp + 8 * u] = -z[u];
+                    for (int jj = 0; jj < 16; ++jj) sA[(hf * 16 + jj) * 65 + 32 + i] = -z16[jj];
+                }
+            }
         }
         __syncthreads();
         // ---- B2 = T^T rows (B2[c][k] = T[k][c]), the B operand of PT = P T
@@ -778,18 +814,12 @@ constexpr int CHAIN_NT_NORM = 480;   // + 4 warps (11-14) applying the fused gat
 constexpr int CHAIN_BV_T0 = 288;     // first thread of the bV warps (9-10)
 constexpr int CHAIN_NORM_T0 = 352;   // first thread of the norm warps
 
-__device__ __forceinline__ void bar_sync_staging() {   // warps 0-7 only
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-}
-
-// One epilogue thread polls an MMA barrier (bounded); the epilogue warps then
-// agree on the outcome through `flag` (one flag per barrier, so that the
-// next wait never overwrites a value a slow thread has yet to read).
-__device__ __forceinline__ bool staging_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *flag,
-                                             int tid, uint64_t limit_ns) {
-    if (tid == 0) *flag = tc::mbar_wait(tc::smem_u32(bar), parity, limit_ns) ? 0u : 1u;
-    bar_sync_staging();
-    const bool ok = *flag == 0u;
+// Every epilogue thread polls the MMA barrier itself (bounded).  A thread
+// that gives up leaves the chunk loop on its own; the others then give up on
+// their next wait, since nothing is issued any more, and all of them meet at
+// the kernel's final barrier.
+__device__ __forceinline__ bool staging_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    const bool ok = tc::mbar_wait(tc::smem_u32(bar), parity, limit_ns);
     tc::fence_after_sync();
     return ok;
 }
@@ -839,8 +869,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
              *ktbar = bars + 5, *mtbar = bars + 6, *utbar = bars + 7, *g3bar = bars + 8, *g5bar = bars + 9;
     uint64_t *obar = bars + 10 /* [2] */, *ofree = bars + 12 /* [2] */, *bvfree = bars + 14 /* [2] */;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-    volatile uint32_t *flag3 = reinterpret_cast<uint32_t *>(bars + 16) + 1;
-    volatile uint32_t *flag5 = reinterpret_cast<uint32_t *>(bars + 17);
+    volatile uint32_t *abort_flag = reinterpret_cast<uint32_t *>(bars + 16) + 1;
     float *sO = reinterpret_cast<float *>(sm + L::OFF_SO);     // [2][64][SOS]
 
     const Dims &d = a.d;
@@ -884,6 +913,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
         tc::mbar_init(tc::smem_u32(&bvbar[1]), 64);
         tc::mbar_init(tc::smem_u32(&bvfree[0]), 1);
         tc::mbar_init(tc::smem_u32(&bvfree[1]), 1);
+        *abort_flag = 0u;
         tc::mbar_init(tc::smem_u32(ktbar), 1);
         tc::mbar_init(tc::smem_u32(mtbar), 256);
         tc::mbar_init(tc::smem_u32(utbar), 256);
@@ -985,24 +1015,31 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
         }
     } else if (warp == 9 || warp == 10) {
         // ============ bV staging (warps 9-10): row r of chunk i's [bV_hi | bV_lo] tile ============
+        // The V row and beta of chunk i + 1 are loaded while chunk i waits for its buffer.
         const int r = tid - CHAIN_BV_T0;
+        float vn[DVS], bn = 0.f;
+        auto load_v = [&](long long i) {
+            const long long t = s + i * TC_C + r;
+            if (t < e) {
+                load_row<DVS>((const TIn *)a.v + t * a.ld_v + col0, vn);
+                bn = a.beta[t * d.hv + h];
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < DVS; ++jj) vn[jj] = 0.f;
+                bn = 0.f;
+            }
+        };
+        if (n_chunks > 0) load_v(0);
         for (long long i = 0; i < n_chunks; ++i) {
             const int b = (int)(i & 1);
+            float v[DVS];
+#pragma unroll
+            for (int jj = 0; jj < DVS; ++jj) v[jj] = vn[jj] * bn;
+            if (i + 1 < n_chunks) load_v(i + 1);
             // the buffer's previous chunk (i - 2) has been read by its G2
             if (i >= 2 && !tc::mbar_wait(tc::smem_u32(&bvfree[b]), (uint32_t)(((i >> 1) - 1) & 1), WL)) {
                 set_error(a.err, GDN_DEVERR_TIMEOUT);
                 break;
-            }
-            const long long t = s + i * TC_C + r;
-            float v[DVS];
-            if (t < e) {
-                load_row<DVS>((const TIn *)a.v + t * a.ld_v + col0, v);
-                const float br = a.beta[t * d.hv + h];
-#pragma unroll
-                for (int jj = 0; jj < DVS; ++jj) v[jj] *= br;
-            } else {
-#pragma unroll
-                for (int jj = 0; jj < DVS; ++jj) v[jj] = 0.f;
             }
             unsigned char *tile = sm + L::OFF_BV + b * BV_SLICE;
 #pragma unroll
@@ -1138,7 +1175,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
             // ---------------- E3: U~ (U' rows scaled by exp(G_last - G_r)) -> concatenated B
             // operand -> utbar
             const float kd = qd < 2 ? a.kdec[((jc + ci) * d.hv + h) * TC_C + tl] : 0.f;
-            if (!staging_wait(g3bar, par, flag3, tid, WL)) break;
+            if (!staging_wait(g3bar, par, WL)) break;
             float ov[HALF];
             tmem_ld_cat16<DVS>(T_D3 + lane_off + hf * HALF, ov);
             if (qd < 2) {
@@ -1163,10 +1200,10 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 }
             }
             // ---------------- E5: M <- gamma_last M + dM -> mtbar
-            if (!staging_wait(g5bar, par, flag5, tid, WL)) break;
+            const float gl = expf(Gl);
+            if (!staging_wait(g5bar, par, WL)) break;
             float v[HALF];
             tmem_ld_cat16<DVS>(T_D5 + lane_off + hf * HALF, v);
-            const float gl = expf(Gl);
 #pragma unroll
             for (int jj = 0; jj < HALF; ++jj) Mr[jj] = gl * Mr[jj] + v[jj];
             if (has_next) {
@@ -1182,7 +1219,10 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 if (r < Lc) store_row<HALF>(o + (c0 + r) * ldo + col0 + hf * HALF, ov);
             }
         }
-        if (ci < n_chunks) {
+        // a wait that gave up in any epilogue thread: no thread stores its part of the state
+        if (ci < n_chunks) *abort_flag = 1u;
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (*abort_flag) {
             if (tid == 0) set_error(a.err, GDN_DEVERR_TIMEOUT);
         } else if (a.state_out && slot >= 0) {
             float *so = a.state_out + ((long long)slot * d.hv + h) * TC_DK * TC_DK +
