@@ -333,8 +333,9 @@ struct TpSmem {
     static constexpr int OFF_B2 = OFF_P + 2 * OPH;         // B2[c][k] = T[k][c], hi + lo; solve scratch before
     static constexpr int OFF_A3 = OFF_P;                   // scaled [T ; PT] hi + lo, after P and B2 are consumed
     static constexpr int OFF_B3 = 2 * KQ;                  // K (MN-major, MN = 128, K = 64), hi + lo
-    static constexpr int OFF_G = OFF_B3 + KT_BYTES;        // G[64], beta[64], q factor[64], beta gamma[64]
-    static constexpr int OFF_BAR = OFF_G + 4 * 64 * 4;     // mbarrier, tmem slot, flag, search
+    static constexpr int MAXG = 4;                         // v-heads per q/k head
+    static constexpr int OFF_G = OFF_B3 + KT_BYTES;        // G[MAXG][64], beta[MAXG][64], beta gamma[MAXG][64], q factor[64]
+    static constexpr int OFF_BAR = OFF_G + (3 * MAXG + 1) * 64 * 4;   // mbarrier, tmem slot, flag, search
     static constexpr int BYTES = OFF_BAR + 32;
     static_assert(OFF_B2 + 2 * OPH <= 2 * KQ, "PT operands exceed the Gram region");
     static_assert(OFF_A3 + TP_BYTES <= 2 * KQ, "[T ; PT] exceeds the Gram region");
@@ -368,10 +369,10 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     float *sY = reinterpret_cast<float *>(sm + L::OFF_B2);      // solve scratch (before B2)
     unsigned char *a3h = sm + L::OFF_A3, *a3l = a3h + TP_HALF;
     unsigned char *b3h = sm + L::OFF_B3, *b3l = b3h + KT_HALF;
-    float *sG = reinterpret_cast<float *>(sm + L::OFF_G);
-    float *sB = sG + 64;
-    float *sFq = sG + 128;
-    float *sBG = sG + 192;
+    float *sGall = reinterpret_cast<float *>(sm + L::OFF_G);   // [MAXG][64] per v-head
+    float *sBall = sGall + L::MAXG * 64;
+    float *sBGall = sBall + L::MAXG * 64;
+    float *sFq = sBGall + L::MAXG * 64;
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 8);
     volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 12);
@@ -402,6 +403,28 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     seq_bounds(a.cu_seqlens, lo, a.T, nullptr, s, e);   // malformed bounds are reported by the map
     const long long t0 = s + (j - a.chunk_base[lo]) * TC_C;
 
+    // ---- loads first: the q/k rows of this chunk and the gates of every v-head of the q/k head
+    const int ir = il_row(tid), iq = il_q(tid);
+    float kv[32], qv[32];
+    {
+        const long long t = t0 + ir;
+        if (t < e) {
+            load_row_il((const TIn *)a.k + t * a.ld_qk + (long long)kh * TC_DK, iq, kv);
+            load_row_il((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK, iq, qv);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
+        }
+    }
+    float gload = 0.f, bload = 0.f;
+    const int gi_l = tid >> 6, r_l = tid & 63;     // (v-head, row) this thread loads
+    if (gi_l < d.grp) {
+        const long long tt = t0 + r_l;
+        if (tt < e) {
+            gload = a.g[tt * d.hv + kh * d.grp + gi_l];
+            bload = a.beta[tt * d.hv + kh * d.grp + gi_l];
+        }
+    }
     if (warp == 0) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), TP_TMEM_COLS);
         tc::tmem_relinquish();
@@ -409,6 +432,10 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     if (tid == 32) {
         tc::mbar_init(tc::smem_u32(mbar), 1);
         tc::mbar_fence_init();
+    }
+    if (gi_l < d.grp) {
+        sGall[gi_l * 64 + r_l] = gload;
+        sBall[gi_l * 64 + r_l] = bload;
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -419,19 +446,11 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
 
+    // ---- every v-head's gates: warp gi scans its v-head's log-decays (cumulative G)
+    if (warp < d.grp) scan64(sGall + warp * 64, lane);
     // ---- rows of K and Q (L2-normalised): the Gram operand [K;Q] (K-major) and K (MN-major),
     // which also leaves for the workspace as the chain's operand (one bulk store)
     {
-        const int ir = il_row(tid), iq = il_q(tid);
-        float kv[32], qv[32];
-        const long long t = t0 + ir;
-        if (t < e) {
-            load_row_il((const TIn *)a.k + t * a.ld_qk + (long long)kh * TC_DK, iq, kv);
-            load_row_il((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK, iq, qv);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
-        }
         const float fq = l2 ? l2norm_row_il(qv, d.l2_eps, d.q_scale) : 1.f;
         if (l2) l2norm_row_il(kv, d.l2_eps, 1.f);
         if (iq == 0) sFq[ir] = fq;
@@ -452,28 +471,23 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
                                 tc::smem_u32(kqh), tc::smem_u32(kql), 0, tc::idesc_bf16(128, 64), false);
         tc::mma_commit(tc::smem_u32(mbar));
     }
-    bool ok = ms.wait(tid);
+    // ---- per v-head: beta gamma, the row decays exp(G_last - G_r) and G_last (the scans are
+    // done: sync_for_mma's barrier)
+    if (gi_l < d.grp) {
+        const int h = kh * d.grp + gi_l;
+        const float Gr = sGall[gi_l * 64 + r_l], Gl = sGall[gi_l * 64 + TC_C - 1];
+        sBGall[gi_l * 64 + r_l] = sBall[gi_l * 64 + r_l] * expf(Gr);
+        a.kdec[((long long)j * d.hv + h) * TC_C + r_l] = expf(Gl - Gr);
+        if (r_l == 0) a.gl[j * d.hv + h] = Gl;
+    }
+    bool ok = ms.wait(tid);     // (G1; its barrier also publishes the gate arrays)
 
     for (int gi = 0; gi < d.grp && ok; ++gi) {
         const int h = kh * d.grp + gi;
+        const float *sG = sGall + gi * 64, *sB = sBall + gi * 64, *sBG = sBGall + gi * 64;
         if (a.npart) a.npart[(j * d.hv + h) * 256 + tid] = __uint_as_float(NP_EMPTY);   // (fused norm)
         unsigned char *gtp = a.tp + ((long long)j * d.hv + h) * CH_BYTES;   // [T ; PT]
         unsigned char *gwq = gtp + OFF_CH_WQ;                                // [-W ; Q']
-        // ---- gates of this v-head: G (cumulative), beta, beta gamma, the row decays
-        if (tid < TC_C) {
-            const long long tt = t0 + tid;
-            sG[tid] = tt < e ? a.g[tt * d.hv + h] : 0.f;
-            sB[tid] = tt < e ? a.beta[tt * d.hv + h] : 0.f;
-        }
-        __syncthreads();
-        if (warp == 0) scan64(sG, lane);
-        __syncthreads();
-        if (tid < TC_C) {
-            const float Gr = sG[tid], Gl = sG[TC_C - 1];
-            sBG[tid] = sB[tid] * expf(Gr);
-            a.kdec[((long long)j * d.hv + h) * TC_C + tid] = expf(Gl - Gr);
-            if (tid == 0) a.gl[j * d.hv + h] = Gl;
-        }
         // ---- E1: A (strictly lower, fp32) and P (lower incl. the diagonal, bf16 hi/lo
         // operand), over the Gram region.  The decay factors exp(G_r - G_c) <= 1 use the
         // approximate-exp intrinsic (relative error about 1e-6, far below the 2^-16 of the
@@ -482,20 +496,24 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
             float v32[32];
             tc::tmem_ld32(tbase + TP_COL_G1 + lane_off + hf * 32, v32);
             const int r = tl & 63;
-            const float Gr = sG[r];
+            const float Gr = sG[r], scale_r = qd < 2 ? sB[r] : 1.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = hf * 32 + i;
+                v32[i] = (qd < 2 ? c < r : c <= r) ? scale_r * __expf(Gr - sG[c]) * v32[i] : 0.f;
+            }
+            // the previous v-head's [-W ; Q'] store has read the region these writes go to
+            if (gi > 0) {
+                if (tid == 0) tc::bulk_wait_read_all();
+                __syncthreads();
+            }
             if (qd < 2) {
-                const float br = sB[r];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int c = hf * 32 + i;
-                    if (c < r) sA[r * 65 + c] = br * __expf(Gr - sG[c]) * v32[i];
+                    if (c < r) sA[r * 65 + c] = v32[i];
                 }
             } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = hf * 32 + i;
-                    v32[i] = (c <= r) ? __expf(Gr - sG[c]) * v32[i] : 0.f;
-                }
 #pragma unroll
                 for (int k8 = 0; k8 < 32; k8 += 8) put8(ph, pl, tc::kmaj_off(r, hf * 32 + k8, 64), &v32[k8]);
             }
@@ -676,45 +694,43 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
                                   tc::smem_u32(b3l), 128, tc::idesc_bf16(128, 128) | tc::kTransB, false);
             tc::mma_commit(tc::smem_u32(mbar));
         }
+        // meanwhile: the q rows of the Q' epilogue (row tl - 64, columns hf*64 ..), scaled by
+        // gamma_r times the row's normalisation factor
+        float qrow[64];
+        {
+            const int r = tl - 64;
+            const long long t = t0 + r;
+            if (qd >= 2 && t < e) {
+                load_row<64>((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK + hf * 64, qrow);
+                const float f = sFq[r] * expf(sG[r]);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) qrow[i] *= f;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) qrow[i] = 0.f;
+            }
+        }
         ok = ms.wait(tid);
         if (!ok) break;
         // ---- [-W ; gamma q - PW] -> shared (over the consumed Gram region), two passes of 32
-        // columns, then one bulk store to the workspace (hi then lo, K-major, K = 128)
-        {
-            const int r = tl - 64;                  // (Q' rows)
-            const long long t = t0 + r;
-            const float f = qd >= 2 ? sFq[r] * expf(sG[r]) : 0.f;
+        // columns, then one bulk store to the workspace (hi then lo, K-major, K = 128); the
+        // next v-head waits for the store to have read these bytes before it reuses them
 #pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
-                const int c0 = hf * 64 + pass * 32;
-                float v32[32];
-                tc::tmem_ld32(tbase + TP_COL_W + lane_off + c0, v32);
-                if (qd < 2) {
+        for (int pass = 0; pass < 2; ++pass) {
+            const int c0 = hf * 64 + pass * 32;
+            float v32[32];
+            tc::tmem_ld32(tbase + TP_COL_W + lane_off + c0, v32);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v32[i] = -v32[i];
-                } else {
-                    float qrow[32];
-                    if (t < e) {
-                        load_row<32>((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK + c0, qrow);
-                    } else {
+            for (int i = 0; i < 32; ++i) v32[i] = qrow[pass * 32 + i] - v32[i];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) qrow[i] = 0.f;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v32[i] = fmaf(f, qrow[i], -v32[i]);
-                }
-#pragma unroll
-                for (int k8 = 0; k8 < 32; k8 += 8) put8(kqh, kql, tc::kmaj_off(tl, c0 + k8, 128), &v32[k8]);
-            }
+            for (int k8 = 0; k8 < 32; k8 += 8) put8(kqh, kql, tc::kmaj_off(tl, c0 + k8, 128), &v32[k8]);
         }
         tc::fence_async_smem();
         __syncthreads();
         if (tid == 0) {
             tc::bulk_s2g(gwq, tc::smem_u32(kqh), WQ_BYTES);
             tc::bulk_commit();
-            tc::bulk_wait_read_all();   // the next v-head reuses these bytes
         }
-        __syncthreads();
     }
     if (!ok) {
         if (tid == 0) {
