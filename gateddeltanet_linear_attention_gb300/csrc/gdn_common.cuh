@@ -165,8 +165,9 @@ struct BwdArgs {
     unsigned *err;
     // workspace (bwd_carve)
     int *chunk_base;              // [n_seqs + 1]
-    float *scratch;               // [n_seqs][HV][chunk][dk][dv]: states before each token of a chunk
-    float *pq, *pk;               // [T][HV][dk]: dq, dk per v-head
+    float *scratch;               // [n_seqs][HV][slices][chunk][dk][32]: states before each token of a chunk
+    float *pq, *pk;               // [T][HV][slices][dk]: the parts of dq, dk from each 32-column slice
+    float *pda, *pda2, *pdb;      // [T][HV][slices]: the parts of <GM, M>, dw . p and dw . r
 };
 size_t bwd_ws_bytes(const Dims &d, long long T, long long n_seqs, bool states_only);
 void bwd_carve(BwdArgs &a, void *ws, bool states_only);
