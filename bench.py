@@ -712,8 +712,9 @@ def bench_backward(args, dev, gdn, pk, pk_src):
                          "bytes_per_call": moved, "achieved": moved / per / 1e9, "unit": "GB/s",
                          "peak": pk["hbm_gbs"], "frac": moved / per / 1e9 / pk["hbm_gbs"],
                          "peak_source": pk_src + " copy",
-                         "note": "32 CTAs (one per v-head) walk 8,192 tokens in sequence; the "
-                                 "per-token states stay in L2 (4 MiB per CTA)"},
+                         "note": "128 CTAs (one per v-head and 32-column state slice) walk "
+                                 "8,192 tokens in sequence; the per-token states of a chunk stay "
+                                 "in L2 (1 MiB per CTA)"},
             "gpu_launches": 3 * reps}
 
 

@@ -95,7 +95,8 @@ size_t chunk_ws_bytes(const gdn::Dims &d, bool act_bf16, long long T, long long 
     return uses_tc(d, act_bf16) ? gdn::chunk_tc_ws_bytes(d, T, n_seqs) : 0;
 }
 
-// The tensor-core path launches one CTA per (chunk, v-head) in a 1-D grid.
+// The tensor-core path launches one CTA per (chunk, q/k head) in a 1-D grid (checked with
+// HV >= HK, which also bounds the per-(chunk, v-head) workspace indices).
 bool tc_grid_fits(const gdn::Dims &d, bool act_bf16, long long T, long long n_seqs) {
     return !uses_tc(d, act_bf16) || gdn::chunk_tc_max_chunks(T, n_seqs) * d.hv <= 0x7fffffffLL;
 }

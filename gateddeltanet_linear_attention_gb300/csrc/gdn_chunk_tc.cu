@@ -12,18 +12,20 @@
 //   M <- gamma_last M + (diag(exp(G_last - G)) K)^T U'
 //
 // Two kernels split the work by what depends on the carried state.
-//  * chunk_tp_kernel, parallel over every (chunk, v-head), computes every
-//    state-independent operand: the Gram products [K;Q] K^T, A and P, the
-//    64x64 inverse T in fp32 (16x16 diagonal blocks by forward substitution,
-//    then two levels of blocked products: T21 = -T22 A21 T11), PT = P T, and
-//    [W ; PW] = [T ; PT] diag(beta gamma) K, all products on the tensor cores.
-//    It writes [T ; PT] and [-W ; gamma Q - PW] as ready-made bf16 hi/lo MMA
-//    operands (96 KB per chunk and v-head) to the workspace.
+//  * chunk_tp_kernel, parallel over every (chunk, q/k head), computes every
+//    state-independent operand: the Gram products [K;Q] K^T once, then per
+//    v-head of the group A and P, the 64x64 inverse T in fp32 (16x16 diagonal
+//    blocks by forward substitution, then two levels of blocked products:
+//    T21 = -T22 A21 T11, the last level on the tensor cores), PT = P T, and
+//    [W ; PW] = [T ; PT] diag(beta gamma) K.  It writes [T ; PT] and
+//    [-W ; gamma Q - PW] as ready-made bf16 hi/lo MMA operands (96 KB per
+//    chunk and v-head), the row decays exp(G_last - G_r), and the normalised K
+//    once per chunk and q/k head (32 KB) to the workspace.
 //  * chunk_chain_kernel, one CTA per (sequence, v-head, slice of DVS state
 //    columns), walks the chunks in order with two MMA round trips per chunk:
 //      D3  = [T ; PT] . bV            -> U, PU
 //      D3 += [-W ; Q'] . M            -> U' (TMEM lanes 0-63), O (lanes 64-127)
-//      D5  = K~^T . U'                -> the state increment
+//      D5  = K^T . (diag(exp(G_last - G)) U')   -> the state increment
 //    The next chunk's operands are bulk-copied while the current one runs.
 //
 // Precision.  The gated RMSNorm that follows divides every token-head by the
@@ -34,7 +36,7 @@
 // 2^-16 relative), with fp32 accumulation in TMEM and the state kept in fp32
 // registers.
 //
-// Operands whose contraction index is the token or the dk row (bgK|bV, K~,
+// Operands whose contraction index is the token or the dk row (bV, K,
 // M, U', T^T) are stored MN-major, so that every operand is written from its
 // natural row layout with 16-byte stores.
 #include "gdn_common.cuh"
@@ -1000,7 +1002,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                     fetch_tp(ci + 2);
                     tc::mbar_arrive(tc::smem_u32(&bvfree[ci & 1]));
                 }
-                // G5: D5 = K~^T . U'
+                // G5: D5 = K^T . U~  (U~: U' with its rows scaled by the decays)
                 ok = tc::mbar_wait(tc::smem_u32(utbar), par, WL) && tc::mbar_wait(tc::smem_u32(ktbar), par, WL);
                 if (!ok) break;
                 tc::fence_after_sync();
@@ -1008,7 +1010,7 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
                 tc::mma_commit(tc::smem_u32(g5bar));
                 if (ci + 1 < n_chunks) {
                     // G2 of the next chunk, behind G5 in the tensor pipe (D3 has been read by E3),
-                    // then the next K~ once G5 has read this one
+                    // then the next K once G5 has read this one
                     ok = issue_g2(ci + 1) && tc::mbar_wait(tc::smem_u32(g5bar), par, WL);
                     if (ok) fetch_kt(ci + 1);
                 }

@@ -201,8 +201,15 @@ gdn_status gdn_mixer_prefill(const gdn_config *cfg, const gdn_mixer_io *io, void
  * arguments and results as gdn_mixer_prefill, without the workspace: the
  * intermediates live in a GDN_STATIC_SCRATCH_BYTES array compiled into the
  * library, which every GPU that loads the library keeps until exit.
- *  - Allocates nothing.  Returns GDN_ERR_WORKSPACE when
- *    gdn_workspace_size(cfg, io->T, io->n_seqs) exceeds the array.
+ *  - Allocates nothing.  Returns GDN_ERR_WORKSPACE when the prefill's own
+ *    intermediates for (io->T, io->n_seqs) exceed the array (this is at most
+ *    gdn_workspace_size, which covers every mode).  At HK=16, HV=32,
+ *    dk=dv=128 that is more than about 700 packed tokens for one sequence,
+ *    575 for four and 121 for sixteen on the tensor-core (bf16, chunk 64)
+ *    path, whose per-chunk operands dominate, and more than 1,358 tokens
+ *    whatever the sequence count in fp32 mode.
+ *  - The cached array address belongs to the device's context: after
+ *    cudaDeviceReset it is stale, so do not call this again on that device.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make it before any stream capture.
  *  - All calls share the one array and it keeps the last call's contents:

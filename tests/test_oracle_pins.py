@@ -354,6 +354,25 @@ def test_mixer_varlen_equals_separate_and_padding_lane():
     np.testing.assert_array_equal(pad["conv_state"][2], I["conv_state"][2])
 
 
+def test_head_subset_channels_and_outputs():
+    """The head map the full-size GPU checks sample with: HK=2, HV=4, d=2, q/k head 1 owns q
+    channels 2-3, k channels 6-7, v-heads 2 and 3 (v channels 12-15, output columns 4-7); and the
+    mixer over heads {1} or {0, 1} equals the full mixer's share exactly (heads never interact)."""
+    chs, vh, cols = oracle.head_channels(2, 4, 2, 2, [1])
+    assert chs.tolist() == [2, 3, 6, 7, 12, 13, 14, 15]
+    assert vh.tolist() == [2, 3] and cols.tolist() == [4, 5, 6, 7]
+    rng = np.random.default_rng(72)
+    I = _mixer_inputs(rng, [7, 0, 19], HK=4, HV=8, d=4)
+    full = oracle.mixer(**I, n_threads=2)
+    J = {k: v for k, v in I.items() if k not in ("HK", "HV", "dk", "dv")}
+    for heads in ([1], [0, 3], [2, 1]):
+        r = oracle.mixer_heads(**J, HK=4, HV=8, dk=4, dv=4, kheads=heads, n_threads=1)
+        chs, vh, cols = oracle.head_channels(4, 8, 4, 4, heads)
+        np.testing.assert_array_equal(r["y"], full["y"][:, cols])
+        np.testing.assert_array_equal(r["state"], full["state"][:, vh])
+        np.testing.assert_array_equal(r["conv_state"], full["conv_state"][:, chs])
+
+
 # ----------------------------------------------------------- slot maintenance
 
 def test_state_copy_hand_example():
