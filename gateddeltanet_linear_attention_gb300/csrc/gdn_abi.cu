@@ -175,10 +175,8 @@ size_t gdn_workspace_size(const gdn_config *cfg, int64_t max_tokens, int32_t max
     gdn::Dims d;
     if (check_cfg(cfg, &d) != GDN_OK || max_tokens < 0 || max_seqs < 0) return 0;
     const size_t pre = prefill_ws_bytes(d, cfg->act == GDN_BF16, max_tokens, max_seqs),
-                 dec = gdn::decode_ws_bytes(d, max_seqs),
-                 ver = gdn::verify_ws_bytes(d, max_tokens);
-    const size_t m = pre > dec ? pre : dec;
-    return (m > ver ? m : ver) + 256;
+                 dec = gdn::decode_ws_bytes(d, max_seqs);
+    return (pre > dec ? pre : dec) + 256;
 }
 
 gdn_status gdn_gate_prep(const gdn_config *cfg, const void *u, const void *b_logit, int64_t ld_ub,
@@ -471,8 +469,8 @@ gdn_status gdn_mixer_verify(const gdn_config *cfg, const gdn_mixer_io *io, int32
     if ((st = check_mixer_io(d, &one, true)) != GDN_OK) return st;
     if (io->n_seqs == 0) return GDN_OK;
     if (!ckpt_idx) return GDN_ERR_INVALID_ARG;
-    if (!workspace || !aligned16(workspace) || workspace_bytes < gdn::verify_ws_bytes(d, io->T))
-        return GDN_ERR_WORKSPACE;
+    (void)workspace;          // unused: the records live in shared memory
+    (void)workspace_bytes;
     unsigned *err = nullptr;
     if ((st = error_word(&err)) != GDN_OK) return st;
     gdn::DecodeArgs a = {};
@@ -480,7 +478,6 @@ gdn_status gdn_mixer_verify(const gdn_config *cfg, const gdn_mixer_io *io, int32
     a.u = io->u; a.b_logit = io->b_logit; a.ld_ub = io->ld_ub; a.A_log = io->A_log;
     a.dt_bias = io->dt_bias; a.z = io->z; a.ld_z = io->ld_z; a.norm_w = io->norm_w;
     a.n = io->n_seqs; a.state = io->state_out; a.state_idx = io->state_idx; a.out = io->y;
-    a.ws = (float *)workspace;
     a.flags = GDN_FLAG_L2NORM_QK; a.d = d; a.err = err;
     a.k_tokens = k; a.ckpt_idx = ckpt_idx;
     return launch_status(gdn::launch_verify(a, cfg->act == GDN_BF16, io->y_dtype == GDN_BF16,

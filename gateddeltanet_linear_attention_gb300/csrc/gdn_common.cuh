@@ -33,6 +33,22 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(x);
 }
 
+// The four conv taps of one channel (row c of the [CH][4] taps, 16-byte aligned base) in one
+// vector load, kept raw until every load of a thread has been issued.
+template <typename TA> struct TapVec { using type = float4; };
+template <> struct TapVec<__nv_bfloat16> { using type = uint2; };
+template <typename TA>
+__device__ __forceinline__ typename TapVec<TA>::type load_taps(const TA *w, int c) {
+    return *reinterpret_cast<const typename TapVec<TA>::type *>(w + (long long)c * 4);
+}
+__device__ __forceinline__ void taps_f32(const float4 &v, float (&t)[4]) {
+    t[0] = v.x; t[1] = v.y; t[2] = v.z; t[3] = v.w;
+}
+__device__ __forceinline__ void taps_f32(const uint2 &v, float (&t)[4]) {   // bf16 pairs, tap 0 low
+    t[0] = __uint_as_float(v.x << 16); t[1] = __uint_as_float(v.x & 0xffff0000u);
+    t[2] = __uint_as_float(v.y << 16); t[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 // SiLU on the approximate-exp and fast-divide intrinsics (relative error about
 // 1e-6), for the streaming kernels that apply it to every element.
@@ -187,7 +203,6 @@ struct DecRec {
 size_t decode_ws_bytes(const Dims &d, long long n_seqs);
 // gdn_mixer_verify: a record per (sequence, q/k head, token); ws_bytes for n_seqs * k tokens
 constexpr int kMaxVerify = 8;
-size_t verify_ws_bytes(const Dims &d, long long tokens);
 cudaError_t launch_verify(const DecodeArgs &a, bool in_bf16, bool out_bf16, cudaStream_t s);
 
 cudaError_t launch_gate_prep(const Dims &d, bool act_bf16, const void *u, const void *b,

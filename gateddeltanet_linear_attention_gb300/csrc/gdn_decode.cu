@@ -187,8 +187,9 @@ __global__ void __launch_bounds__(4 * DV) decode_kernel(DecodeArgs a) {
 // updated the next NS-1 are in flight.  The records of the next batch of HB
 // heads are bulk-copied into shared memory one batch ahead, so each head
 // touches only shared memory before its state is written back.
-template <int DK, int DV, typename TA>
-__global__ void __launch_bounds__(256) decode_prep_kernel(DecodeArgs a) {
+// GM: the v-heads per q/k head the register arrays are sized for (1, 2 or 4; d.grp <= GM).
+template <int DK, int DV, typename TA, int GM>
+__global__ void __launch_bounds__(256, 8) decode_prep_kernel(DecodeArgs a) {
     __shared__ __align__(16) float qs[DK], ks[DK];
     __shared__ float scal[8 + 8];
     const Dims &d = a.d;
@@ -209,32 +210,66 @@ __global__ void __launch_bounds__(256) decode_prep_kernel(DecodeArgs a) {
     const TA *w = (const TA *)a.conv_w;
     TA *cs = (TA *)a.conv_state + (long long)slot * d.ch * 3;
     const int nch = 2 * DK + G * DV;
-    for (int ci = tid; ci < nch; ci += 256) {
-        int c;
+    // Every global load of the unit is issued before any store (the stores to the history and
+    // the record could alias later loads for the compiler, which would serialise the round trips).
+    constexpr int CPT = (2 * DK + GM * DV + 255) / 256;  // channels per thread
+    constexpr int ZPT = (GM * DV + 255) / 256;           // SiLU(z) values per thread
+    TA hx[CPT][4], zr[ZPT];
+    typename TapVec<TA>::type wv[CPT];
+    int chan[CPT];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int ci = tid + 256 * i;
+        int c = 0;
         if (ci < DK) c = kh * DK + ci;
         else if (ci < 2 * DK) c = d.hk * DK + kh * DK + (ci - DK);
         else c = 2 * d.hk * DK + kh * G * DV + (ci - 2 * DK);
-        TA *hc = cs + (long long)c * 3;
-        const TA h0 = hc[0], h1 = hc[1], h2 = hc[2], xc = x[c];
-        const float acc = to_f32(w[c * 4 + 0]) * to_f32(h0) + to_f32(w[c * 4 + 1]) * to_f32(h1) +
-                          to_f32(w[c * 4 + 2]) * to_f32(h2) + to_f32(w[c * 4 + 3]) * to_f32(xc);
-        hc[0] = h1;
-        hc[1] = h2;
-        hc[2] = xc;
+        chan[i] = c;
+        if (ci < nch) {
+            const TA *hc = cs + (long long)c * 3;
+            hx[i][0] = hc[0];
+            hx[i][1] = hc[1];
+            hx[i][2] = hc[2];
+            hx[i][3] = x[c];
+            wv[i] = load_taps(w, c);
+        }
+    }
+    const TA *z = (const TA *)a.z + (long long)n * a.ld_z + (long long)kh * G * DV;
+#pragma unroll
+    for (int i = 0; i < ZPT; ++i)
+        if (tid + 256 * i < G * DV) zr[i] = z[tid + 256 * i];
+    TA ul = from_f32<TA>(0.f), bl = from_f32<TA>(0.f);
+    float alog = 0.f, dtb = 0.f;
+    if (tid < G) {
+        ul = ((const TA *)a.u + (long long)n * a.ld_ub)[kh * G + tid];
+        bl = ((const TA *)a.b_logit + (long long)n * a.ld_ub)[kh * G + tid];
+        alog = a.A_log[kh * G + tid];
+        dtb = a.dt_bias[kh * G + tid];
+    }
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int ci = tid + 256 * i;
+        if (ci >= nch) break;
+        TA *hc = cs + (long long)chan[i] * 3;
+        float t[4];
+        taps_f32(wv[i], t);
+        const float acc = t[0] * to_f32(hx[i][0]) + t[1] * to_f32(hx[i][1]) + t[2] * to_f32(hx[i][2]) +
+                          t[3] * to_f32(hx[i][3]);
+        hc[0] = hx[i][1];
+        hc[1] = hx[i][2];
+        hc[2] = hx[i][3];
         const float val = silu_f(acc);
         if (ci < DK) qs[ci] = val;
         else if (ci < 2 * DK) ks[ci - DK] = val;
         else rec[R.v + (ci - 2 * DK)] = val;
     }
-    const TA *z = (const TA *)a.z + (long long)n * a.ld_z + (long long)kh * G * DV;
-    for (int idx = tid; idx < G * DV; idx += 256) rec[R.z + idx] = silu_f(to_f32(z[idx]));
+#pragma unroll
+    for (int i = 0; i < ZPT; ++i)
+        if (tid + 256 * i < G * DV) rec[R.z + tid + 256 * i] = silu_f(to_f32(zr[i]));
     if (tid < G) {
-        const int h = kh * G + tid;
-        const TA *uv = (const TA *)a.u + (long long)n * a.ld_ub;
-        const TA *bv = (const TA *)a.b_logit + (long long)n * a.ld_ub;
-        const float gg = -expf(a.A_log[h]) * softplus_f(to_f32(uv[h]) + a.dt_bias[h]);
+        const float gg = -expf(alog) * softplus_f(to_f32(ul) + dtb);
         rec[R.ga + tid] = expf(gg);
-        rec[R.gb + tid] = sigmoid_f(to_f32(bv[h]));
+        rec[R.gb + tid] = sigmoid_f(to_f32(bl));
     }
     __syncthreads();
     if (warp < 2) {   // |q|^2 (warp 0), |k|^2 (warp 1)
@@ -676,7 +711,9 @@ __global__ void __launch_bounds__(4 * DV, 1) decode_stream_kernel(DecodeArgs a) 
 template <int DK, int DV, typename TA, typename TOut, bool Q8 = false, bool EF = false>
 static cudaError_t launch_stream_t(const DecodeArgs &a, cudaStream_t s) {
     const int units = a.n * a.d.hk;
-    decode_prep_kernel<DK, DV, TA><<<units, 256, 0, s>>>(a);
+    if (a.d.grp == 1) decode_prep_kernel<DK, DV, TA, 1><<<units, 256, 0, s>>>(a);
+    else if (a.d.grp == 2) decode_prep_kernel<DK, DV, TA, 2><<<units, 256, 0, s>>>(a);
+    else decode_prep_kernel<DK, DV, TA, 4><<<units, 256, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kern = decode_stream_kernel<DK, DV, TOut, Q8, EF>;

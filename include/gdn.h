@@ -328,8 +328,10 @@ gdn_status gdn_chunk_backward(const gdn_config *cfg, const void *q, const void *
  * own source slot may be its column 0 (it is read before it is written).
  * A negative state_idx[n] is a padding lane (zero outputs, nothing written);
  * columns reaching past n_slots are reported as GDN_DEVERR_SLOT and that
- * sequence is skipped.  Workspace: DEVICE, 16-byte aligned, at least
- * gdn_workspace_size(cfg, n_seqs * k, n_seqs) bytes. */
+ * sequence is skipped.  One launch; the per-token intermediates stay in
+ * shared memory, so `workspace` / `workspace_bytes` are not used (NULL and 0
+ * are accepted; the arguments keep the signature of the other fused entry
+ * points). */
 gdn_status gdn_mixer_verify(const gdn_config *cfg, const gdn_mixer_io *io, int32_t k,
                             const int32_t *ckpt_idx, void *workspace, size_t workspace_bytes,
                             void *stream);

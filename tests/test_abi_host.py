@@ -191,7 +191,6 @@ def test_mixer_verify_validation(lib):
     good = dict(state_in=A16b, state_out=A16b, conv_state=A16)
     need = lib.gdn_workspace_size(ch, n * k, n)
     io = _io(T=n * k, n=n, **good)
-    assert need >= n * k * 16 * (2 * 128 + 4 * 128 + 4 + 1) * 4       # a record per (unit, token)
     for kk in (0, 9, -1):                                               # 1 <= k <= 8
         assert lib.gdn_mixer_verify(ch, ctypes.byref(io), kk, A16, A16, need, None) == INVALID
     bad = _io(T=n * k + 1, n=n, **good)                                 # T != n * k
@@ -203,10 +202,11 @@ def test_mixer_verify_validation(lib):
     assert lib.gdn_mixer_verify(ch, ctypes.byref(bad), k, A16, A16, need, None) == INVALID
     bad = _io(T=n * k, n=n, ld_x=8000, **good)                          # narrower than CH
     assert lib.gdn_mixer_verify(ch, ctypes.byref(bad), k, A16, A16, need, None) == INVALID
-    small = n * k * 16 * 4                                              # far short of the records
-    assert lib.gdn_mixer_verify(ch, ctypes.byref(io), k, A16, A16, small, None) == WORKSPACE
-    assert lib.gdn_mixer_verify(ch, ctypes.byref(io), k, A16, None, need, None) == WORKSPACE
-    assert lib.gdn_mixer_verify(ch, ctypes.byref(io), k, A16, MIS, need, None) == WORKSPACE
+    # the workspace is not used: none, a small one or a misaligned one is no workspace error
+    # (without a GPU the call then stops at the CUDA runtime)
+    for ws, nb in ((None, 0), (A16, 16), (MIS, need)):
+        assert lib.gdn_mixer_verify(ch, ctypes.byref(io), k, A16, ws, nb, None) not in (OK, WORKSPACE,
+                                                                                      INVALID)
     empty = _io(T=0, n=0, **good)
     assert lib.gdn_mixer_verify(ch, ctypes.byref(empty), k, None, None, 0, None) == OK
 
