@@ -653,11 +653,11 @@ def bench_verify(args, dev, gdn, pk, pk_src, k=8):
                         "checkpoint columns; L2 evicted before each launch" % (k, k),
             "value": gbs, "unit": "GB/s", "us_per_round": per * 1e6,
             "tokens_per_s": N * k / per, "state_bytes_per_round": moved,
-            "roofline": {"kernel": "verify_prep_kernel + verify_kernel", "bound": "hbm",
+            "roofline": {"kernel": "verify_kernel (one launch per round)", "bound": "hbm",
                          "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "frac": gbs / pk["hbm_gbs"], "traffic": traffic_for("verify_64x8"),
                          "peak_source": pk_src + " copy"},
-            "gpu_launches": 2 * reps}
+            "gpu_launches": reps}
 
 
 def bench_backward(args, dev, gdn, pk, pk_src):
