@@ -36,7 +36,8 @@ namespace gdn {
 
 namespace {
 
-// DV here is the slice width (32 columns); a thread holds 4 columns of RPT rows.
+// DV here is the slice width (32 columns, one warp for the per-column steps); a thread holds
+// 4 columns of RPT rows.
 constexpr int BWD_DVS = 32;
 template <int DK, int DV>
 struct BwdCfg {
@@ -66,105 +67,180 @@ __device__ __forceinline__ float row_sum(float v) {
     return v;
 }
 
-// Per-token inputs of one v-head staged in shared memory.
-// One token's inputs in shared memory (double-buffered: the next token's are stored while this
-// one's are read).  Every array read or written as float4 is 16-byte aligned explicitly.
-template <int DK, int DV>
-struct TokIn {
-    alignas(16) float q[DK];
-    alignas(16) float k[DK];
-    alignas(16) float v[DV];
-    alignas(16) float dout[DV];
-    float a, b;
+// Row sums of RPT rows held by the LPR lanes of a row group, written to out[row].  With 8 rows
+// over 8 lanes the sums are formed by a transposing butterfly (7 shuffles for all 8 rows): after
+// it, lane q of the group holds the sum of its row x = q, so each lane stores one value.
+// Otherwise every row is reduced on its own (every lane ends with the sum; the first stores it).
+template <int RPT, int LPR, int RPP>
+__device__ __forceinline__ void store_row_sums(float (&v)[RPT], float *out, int rg, int lane) {
+    if constexpr (RPT == 8 && LPR == 8) {
+        const int q = lane & 7;
+        float h4[4], h2[2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool up = q & 4;
+            const float send = up ? v[i] : v[i + 4];
+            h4[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const bool up = q & 2;
+            const float send = up ? h4[i] : h4[i + 2];
+            h2[i] = (up ? h4[i + 2] : h4[i]) + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        const bool up = q & 1;
+        const float send = up ? h2[0] : h2[1];
+        const float tot = (up ? h2[1] : h2[0]) + __shfl_xor_sync(0xffffffffu, send, 1);
+        out[rg + q * RPP] = tot;
+    } else {
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+            const float tot = row_sum<LPR>(v[x]);
+            if (lane % LPR == 0) out[rg + x * RPP] = tot;
+        }
+    }
+}
+
+// Sum of the RPP partial column sums red[0..RPP)[col], as a tree.
+template <int RPP, int DV>
+__device__ __forceinline__ float col_sum(const float (&red)[RPP][DV], int col) {
+    float t[RPP];
+#pragma unroll
+    for (int r = 0; r < RPP; ++r) t[r] = red[r][col];
+#pragma unroll
+    for (int w = RPP / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int r = 0; r < w; ++r) t[r] += t[r + w];
+    return t[0];
+}
+
+// ---- token inputs, staged one chunk at a time
+// A chunk's inputs of one (v-head, slice) go to shared memory by asynchronous copies
+// (cp.async, 16 bytes per copy for the rows, 4 for the gates) issued one chunk ahead, so a
+// token step reads only shared memory and the global-load latency is paid once per chunk.
+// q, k and v stay in the input dtype (converted on read); d_o, g and beta are fp32.
+constexpr int kBwdMaxChunk = 64;
+
+template <int DK, int DV, typename TA>
+struct ChunkIn {
+    alignas(16) TA q[kBwdMaxChunk][DK];
+    alignas(16) TA k[kBwdMaxChunk][DK];
+    alignas(16) TA v[kBwdMaxChunk][DV];
+    alignas(16) float dout[kBwdMaxChunk][DV];
+    alignas(16) float g[kBwdMaxChunk];
+    alignas(16) float b[kBwdMaxChunk];
 };
+
+// Reductions of one token step, and the forward quantities of every token of the chunk that
+// the reverse pass reuses: p = M^T k, r = v - a p and w = beta r (per column of the slice).
 template <int DK, int DV>
-struct TokSmem {
-    TokIn<DK, DV> in[2];
-    alignas(16) float p[DV];
-    alignas(16) float r[DV];
-    alignas(16) float w[DV];
+struct BwdRed {
+    alignas(16) float p[kBwdMaxChunk][DV];
+    alignas(16) float r[kBwdMaxChunk][DV];
+    alignas(16) float w[kBwdMaxChunk][DV];
     alignas(16) float dp[DV];
     alignas(16) float red[BwdCfg<DK, DV>::RPP][DV];
-    float wsum[3][BwdCfg<DK, DV>::NT / 32];
+    float wsum[BwdCfg<DK, DV>::NT / 32];
 };
 
-// A thread's share of one token's inputs, loaded into registers ahead of use: k and q for
-// tid < DK, v and do for tid < DV, a and beta for thread 0.
-struct TokReg {
-    float k, q, v, dout, a, b;
+template <int DK, int DV, typename TA>
+struct BwdSmem {
+    ChunkIn<DK, DV, TA> in[2];
+    BwdRed<DK, DV> rd;
 };
 
-// The forward step of one token on M in registers: p = M^T k (column sums), w, M <- a M + k w^T.
-// `after_first_barrier` runs once every thread is past the first barrier (the other input
-// buffer is free then).
-template <int DK, int DV, typename F>
-__device__ __forceinline__ void fwd_token(float4 (&m)[BwdCfg<DK, DV>::RPT], TokSmem<DK, DV> &sm,
-                                          const TokIn<DK, DV> &in, int tid, int rg, int c4,
-                                          F after_first_barrier) {
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Issue the copies of tokens t0 .. t1-1 (t1 - t0 <= kBwdMaxChunk) into `ci`: k and v always,
+// q and d_o when `with_q`; one commit group per call (possibly empty).  Row starts are 16-byte
+// aligned: the entry points require 16-byte aligned bases and row strides that are multiples of
+// 8 elements, and the slice's first column col0 is a multiple of 32.
+template <int DK, int DV, typename TA>
+__device__ __forceinline__ void stage_chunk(ChunkIn<DK, DV, TA> &ci, const BwdArgs &a, long long t0,
+                                            long long t1, int h, int kh, int col0, bool with_q, int tid) {
+    constexpr int NT = BwdCfg<DK, DV>::NT;
+    constexpr int EK = 16 / (int)sizeof(TA);            // elements per 16-byte copy
+    constexpr int PK = DK / EK, PV = DV / EK, PD = DV / 4;
+    const int L = (int)(t1 - t0);
+    const TA *kq = (const TA *)a.k, *qq = (const TA *)a.q, *vv = (const TA *)a.v;
+    for (int i = tid; i < L * PK; i += NT) {
+        const int r = i / PK, c = (i % PK) * EK;
+        const long long row = (t0 + r) * a.ld_qk + (long long)kh * DK + c;
+        cp_async16(&ci.k[r][c], kq + row);
+        if (with_q) cp_async16(&ci.q[r][c], qq + row);
+    }
+    for (int i = tid; i < L * PV; i += NT) {
+        const int r = i / PV, c = (i % PV) * EK;
+        cp_async16(&ci.v[r][c], vv + (t0 + r) * a.ld_v + (long long)h * a.d.dv + col0 + c);
+    }
+    if (with_q)
+        for (int i = tid; i < L * PD; i += NT) {
+            const int r = i / PD, c = (i % PD) * 4;
+            cp_async16(&ci.dout[r][c], a.d_o + (t0 + r) * (long long)a.d.hv * a.d.dv + (long long)h * a.d.dv + col0 + c);
+        }
+    for (int i = tid; i < 2 * L; i += NT) {
+        const int r = i >> 1;
+        if (i & 1) cp_async4(&ci.b[r], a.beta + (t0 + r) * a.d.hv + h);
+        else cp_async4(&ci.g[r], a.g + (t0 + r) * a.d.hv + h);
+    }
+    cp_async_commit();
+}
+
+// The forward step of token tt of a staged chunk on M in registers: p = M^T k (column sums),
+// r = v - a p, w = beta r (kept in rd at row tt), and, when `update`, M <- a M + k w^T.
+// Two block barriers.
+template <int DK, int DV, typename TA>
+__device__ __forceinline__ void fwd_token(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdRed<DK, DV> &rd,
+                                          const ChunkIn<DK, DV, TA> &in, int tt, int tid, int rg, int c4,
+                                          bool update) {
     using C = BwdCfg<DK, DV>;
+    float kr[C::RPT];
+#pragma unroll
+    for (int x = 0; x < C::RPT; ++x) kr[x] = to_f32(in.k[tt][rg + x * C::RPP]);
     float4 pp = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int x = 0; x < C::RPT; ++x) {
-        const float kr = in.k[rg + x * C::RPP];
-        pp.x += m[x].x * kr; pp.y += m[x].y * kr; pp.z += m[x].z * kr; pp.w += m[x].w * kr;
+        pp.x += m[x].x * kr[x]; pp.y += m[x].y * kr[x]; pp.z += m[x].z * kr[x]; pp.w += m[x].w * kr[x];
     }
-    *reinterpret_cast<float4 *>(&sm.red[rg][c4]) = pp;
+    *reinterpret_cast<float4 *>(&rd.red[rg][c4]) = pp;
     __syncthreads();
-    after_first_barrier();
+    const float av = expf(in.g[tt]);
     if (tid < DV) {
-        float p = 0.f;
-#pragma unroll
-        for (int r = 0; r < C::RPP; ++r) p += sm.red[r][tid];
-        sm.w[tid] = in.b * (in.v[tid] - in.a * p);
+        const float p = col_sum<C::RPP, DV>(rd.red, tid);
+        const float rr = to_f32(in.v[tt][tid]) - av * p;
+        rd.p[tt][tid] = p;
+        rd.r[tt][tid] = rr;
+        rd.w[tt][tid] = in.b[tt] * rr;
     }
     __syncthreads();
-    const float4 w4 = *reinterpret_cast<const float4 *>(&sm.w[c4]);
-    const float a = in.a;
+    if (!update) return;
+    const float4 w4 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4]);
 #pragma unroll
     for (int x = 0; x < C::RPT; ++x) {
-        const float kr = in.k[rg + x * C::RPP];
-        m[x].x = a * m[x].x + kr * w4.x; m[x].y = a * m[x].y + kr * w4.y;
-        m[x].z = a * m[x].z + kr * w4.z; m[x].w = a * m[x].w + kr * w4.w;
+        m[x].x = av * m[x].x + kr[x] * w4.x; m[x].y = av * m[x].y + kr[x] * w4.y;
+        m[x].z = av * m[x].z + kr[x] * w4.z; m[x].w = av * m[x].w + kr[x] * w4.w;
     }
-}
-
-// Token t's q (optional), k, v, do (optional), a, beta of head h: the thread's share into
-// registers, and from there into an input buffer.
-template <int DK, int DV, typename TA>
-__device__ __forceinline__ TokReg load_token(const BwdArgs &a, long long t, int h, int kh, int tid,
-                                             bool with_q, int col0) {
-    TokReg r = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (tid < DK) {
-        r.k = to_f32(((const TA *)a.k)[t * a.ld_qk + (long long)kh * DK + tid]);
-        if (with_q) r.q = to_f32(((const TA *)a.q)[t * a.ld_qk + (long long)kh * DK + tid]);
-    }
-    if (tid < DV) {   // the slice's columns col0 .. col0 + DV of the head
-        r.v = to_f32(((const TA *)a.v)[t * a.ld_v + (long long)h * a.d.dv + col0 + tid]);
-        if (with_q) r.dout = a.d_o[t * (long long)a.d.hv * a.d.dv + (long long)h * a.d.dv + col0 + tid];
-    }
-    if (tid == 0) {
-        r.a = a.g[t * a.d.hv + h];
-        r.b = a.beta[t * a.d.hv + h];
-    }
-    return r;
-}
-template <int DK, int DV>
-__device__ __forceinline__ void store_token(TokIn<DK, DV> &in, const TokReg &r, int tid) {
-    static_assert(DK <= BwdCfg<DK, DV>::NT, "one k / q element per thread");
-    if (tid < DK) { in.k[tid] = r.k; in.q[tid] = r.q; }
-    if (tid < DV) { in.v[tid] = r.v; in.dout[tid] = r.dout; }
-    if (tid == 0) { in.a = expf(r.a); in.b = r.b; }
 }
 
 template <int DK, int DV, typename TA>
 __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
     using C = BwdCfg<DK, DV>;
-    __shared__ __align__(16) TokSmem<DK, DV> sm;
+    extern __shared__ __align__(16) unsigned char smraw[];
+    BwdSmem<DK, DV, TA> &sm = *reinterpret_cast<BwdSmem<DK, DV, TA> *>(smraw);
     const Dims &d = a.d;
     const int tid = threadIdx.x, h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
     const int col0 = blockIdx.z * DV;                   // this CTA's slice of the state columns
-    const int rg = tid / C::LPR, c4 = (tid % C::LPR) * 4 + col0;   // (c4: column in the head)
-    const int c4s = c4 - col0;                          //         (column in the slice)
+    const int rg = tid / C::LPR, c4s = (tid % C::LPR) * 4, c4 = c4s + col0;   // (c4: column in the head)
     long long s, e;
     seq_bounds(a.cu_seqlens, n, a.T, a.err, s, e);
     const int slot = slot_of(a.state_idx, n, d.n_slots, a.err);
@@ -180,23 +256,32 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
                                                      (long long)(rg + x * C::RPP) * DVH + c4);
     }
     const long long b0 = a.chunk_base[n];
-    store_token<DK, DV>(sm.in[0], load_token<DK, DV, TA>(a, s, h, kh, tid, false, col0), tid);
-    __syncthreads();
-    for (long long t = s; t < e; ++t) {
-        if ((t - s) % Cc == 0) {
-            float *B = a.bnd + ((b0 + (t - s) / Cc) * d.hv + h) * DK * DVH;
-#pragma unroll
-            for (int x = 0; x < C::RPT; ++x)
-                *reinterpret_cast<float4 *>(B + (long long)(rg + x * C::RPP) * DVH + c4) = m[x];
+    const long long nch = (e - s + Cc - 1) / Cc;
+    auto bounds = [&](long long c, long long &t0, long long &t1) {
+        t0 = s + c * Cc;
+        t1 = t0 + Cc < e ? t0 + Cc : e;
+    };
+    long long t0, t1;
+    bounds(0, t0, t1);
+    stage_chunk<DK, DV, TA>(sm.in[0], a, t0, t1, h, kh, col0, false, tid);
+    for (long long c = 0; c < nch; ++c) {
+        __syncthreads();                                 // every read of buffer (c + 1) & 1 is done
+        if (c + 1 < nch) {
+            long long u0, u1;
+            bounds(c + 1, u0, u1);
+            stage_chunk<DK, DV, TA>(sm.in[(c + 1) & 1], a, u0, u1, h, kh, col0, false, tid);
+            cp_async_wait<1>();                          // this thread's copies of chunk c landed
+        } else {
+            cp_async_wait<0>();
         }
-        // token t+1's inputs load while token t runs; they go to the other buffer once it is free
-        const bool more = t + 1 < e;
-        TokReg nx = {};
-        if (more) nx = load_token<DK, DV, TA>(a, t + 1, h, kh, tid, false, col0);
-        const int bi = (int)((t - s) & 1);
-        fwd_token<DK, DV>(m, sm, sm.in[bi], tid, rg, c4s, [&] {
-            if (more) store_token<DK, DV>(sm.in[bi ^ 1], nx, tid);
-        });
+        __syncthreads();                                 // ... and everyone's
+        bounds(c, t0, t1);
+        float *B = a.bnd + ((b0 + c) * d.hv + h) * DK * DVH;
+#pragma unroll
+        for (int x = 0; x < C::RPT; ++x)
+            *reinterpret_cast<float4 *>(B + (long long)(rg + x * C::RPP) * DVH + c4) = m[x];
+        const ChunkIn<DK, DV, TA> &in = sm.in[c & 1];
+        for (int tt = 0; tt < (int)(t1 - t0); ++tt) fwd_token<DK, DV, TA>(m, sm.rd, in, tt, tid, rg, c4s, true);
     }
 }
 
@@ -204,7 +289,10 @@ template <int DK, int DV, typename TA>
 __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
     using C = BwdCfg<DK, DV>;
     constexpr int NW = C::NT / 32;
-    __shared__ __align__(16) TokSmem<DK, DV> sm;
+    static_assert(DV == 32, "the per-column steps run on warp 0, one column per lane");
+    extern __shared__ __align__(16) unsigned char smraw[];
+    BwdSmem<DK, DV, TA> &sm = *reinterpret_cast<BwdSmem<DK, DV, TA> *>(smraw);
+    BwdRed<DK, DV> &rd = sm.rd;
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
@@ -240,8 +328,18 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
     float *scr = a.scratch + (((long long)n * d.hv + h) * NS + sl) * (long long)Cc * DK * DV;
     const long long b0 = a.chunk_base[n];
     const long long nch = (e - s + Cc - 1) / Cc;
+    auto bounds = [&](long long c, long long &t0, long long &t1) {
+        t0 = s + c * Cc;
+        t1 = t0 + Cc < e ? t0 + Cc : e;
+    };
+    if (nch > 0) {
+        long long u0, u1;
+        bounds(nch - 1, u0, u1);
+        stage_chunk<DK, DV, TA>(sm.in[(nch - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
+    }
     for (long long c = nch - 1; c >= 0; --c) {
-        const long long t0 = s + c * Cc, t1 = (t0 + Cc < e) ? t0 + Cc : e;
+        long long t0, t1;
+        bounds(c, t0, t1);
         float4 m[C::RPT];
         {
             const float *B = a.bnd + ((b0 + c) * d.hv + h) * DK * DVH;
@@ -249,115 +347,94 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
             for (int x = 0; x < C::RPT; ++x)
                 m[x] = *reinterpret_cast<const float4 *>(B + (long long)(rg + x * C::RPP) * DVH + c4);
         }
-        // forward through the chunk, keeping the state before every token (each thread
-        // reads back only what it wrote); token inputs double-buffered (buffer (t - t0) & 1)
-        __syncthreads();                                 // the previous chunk's buffer reads are done
-        if (t0 + 1 < t1) store_token<DK, DV>(sm.in[0], load_token<DK, DV, TA>(a, t0, h, kh, tid, false, col0), tid);
-        __syncthreads();
+        __syncthreads();                                 // every read of buffer (c - 1) & 1 is done
+        if (c > 0) {
+            long long u0, u1;
+            bounds(c - 1, u0, u1);
+            stage_chunk<DK, DV, TA>(sm.in[(c - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
+            cp_async_wait<1>();                          // this thread's copies of chunk c landed
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();                                 // ... and everyone's
+        const ChunkIn<DK, DV, TA> &in = sm.in[c & 1];
+        // forward through the chunk, keeping the state before every token (each thread reads
+        // back only what it wrote) and every token's p, r and w
         for (long long t = t0; t < t1; ++t) {
             float *Sc = scr + (t - t0) * DK * DV;
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x)
                 *reinterpret_cast<float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s) = m[x];
-            if (t + 1 == t1) break;
-            const bool more = t + 2 < t1;               // token t+1 updates the state too
-            TokReg nx = {};
-            if (more) nx = load_token<DK, DV, TA>(a, t + 1, h, kh, tid, false, col0);
-            const int bi = (int)((t - t0) & 1);
-            fwd_token<DK, DV>(m, sm, sm.in[bi], tid, rg, c4s, [&] {
-                if (more) store_token<DK, DV>(sm.in[bi ^ 1], nx, tid);
-            });
+            fwd_token<DK, DV, TA>(m, rd, in, (int)(t - t0), tid, rg, c4s, t + 1 < t1);
         }
-        // the tokens in reverse, inputs double-buffered (buffer (t - t0) & 1): token t-1's load
-        // while token t runs and are stored to the other buffer after barrier (A)
-        __syncthreads();                                 // the forward pass's buffer reads are done
-        store_token<DK, DV>(sm.in[(t1 - 1 - t0) & 1], load_token<DK, DV, TA>(a, t1 - 1, h, kh, tid, true, col0), tid);
-        __syncthreads();
-        for (long long t = t1 - 1; t >= t0; --t) {
-            const float *Sc = scr + (t - t0) * DK * DV;
+        // the tokens in reverse; the state before token t-1 is loaded while token t runs
+        float4 mn[C::RPT];
+        {
+            const float *Sc = scr + (t1 - 1 - t0) * DK * DV;
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x)
-                m[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s);
-            const int bi = (int)((t - t0) & 1);
-            const TokIn<DK, DV> &in = sm.in[bi];
-            const bool more = t - 1 >= t0;
-            TokReg nx = {};
-            if (more) nx = load_token<DK, DV, TA>(a, t - 1, h, kh, tid, true, col0);
-            // p = M^T k
-            {
-                float4 pp = make_float4(0.f, 0.f, 0.f, 0.f);
+                mn[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s);
+        }
+        for (long long t = t1 - 1; t >= t0; --t) {
+            const int tt = (int)(t - t0);
 #pragma unroll
-                for (int x = 0; x < C::RPT; ++x) {
-                    const float kr = in.k[rg + x * C::RPP];
-                    pp.x += m[x].x * kr; pp.y += m[x].y * kr; pp.z += m[x].z * kr; pp.w += m[x].w * kr;
-                }
-                *reinterpret_cast<float4 *>(&sm.red[rg][c4s]) = pp;
-            }
-            __syncthreads();                             // (A) the other buffer is free from here
-            if (more) store_token<DK, DV>(sm.in[bi ^ 1], nx, tid);
-            const float av = in.a, bv = in.b;
-            if (tid < DV) {
-                float p = 0.f;
+            for (int x = 0; x < C::RPT; ++x) m[x] = mn[x];
+            if (t > t0) {
+                const float *Sc = scr + (tt - 1) * DK * DV;
 #pragma unroll
-                for (int r = 0; r < C::RPP; ++r) p += sm.red[r][tid];
-                const float rr = in.v[tid] - av * p;
-                sm.p[tid] = p;
-                sm.r[tid] = rr;
-                sm.w[tid] = bv * rr;
+                for (int x = 0; x < C::RPT; ++x)
+                    mn[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s);
             }
-            __syncthreads();                             // (B)
-            const float4 w4 = *reinterpret_cast<const float4 *>(&sm.w[c4s]);
-            const float4 do4 = *reinterpret_cast<const float4 *>(&in.dout[c4s]);
+            const float av = expf(in.g[tt]), bv = in.b[tt];
+            const float4 w4 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4s]);
+            const float4 do4 = *reinterpret_cast<const float4 *>(&in.dout[tt][c4s]);
             float4 dwp = make_float4(0.f, 0.f, 0.f, 0.f);
             float dap = 0.f;
+            float kr[C::RPT], dqp[C::RPT];
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x) {
                 const int row = rg + x * C::RPP;
-                const float kr = in.k[row], qr = in.q[row];
+                kr[x] = to_f32(in.k[tt][row]);
+                const float qr = to_f32(in.q[tt][row]);
                 float4 mp;                               // M' = a M + k w^T
-                mp.x = av * m[x].x + kr * w4.x; mp.y = av * m[x].y + kr * w4.y;
-                mp.z = av * m[x].z + kr * w4.z; mp.w = av * m[x].w + kr * w4.w;
+                mp.x = av * m[x].x + kr[x] * w4.x; mp.y = av * m[x].y + kr[x] * w4.y;
+                mp.z = av * m[x].z + kr[x] * w4.z; mp.w = av * m[x].w + kr[x] * w4.w;
                 gm[x].x += qr * do4.x; gm[x].y += qr * do4.y; gm[x].z += qr * do4.z; gm[x].w += qr * do4.w;
-                const float dq = row_sum<C::LPR>(mp.x * do4.x + mp.y * do4.y + mp.z * do4.z + mp.w * do4.w);
-                if (lane % C::LPR == 0) a.pq[part(t) * DK + row] = dq;
-                dwp.x += gm[x].x * kr; dwp.y += gm[x].y * kr; dwp.z += gm[x].z * kr; dwp.w += gm[x].w * kr;
+                dqp[x] = mp.x * do4.x + mp.y * do4.y + mp.z * do4.z + mp.w * do4.w;   // dq = M' do
+                dwp.x += gm[x].x * kr[x]; dwp.y += gm[x].y * kr[x]; dwp.z += gm[x].z * kr[x]; dwp.w += gm[x].w * kr[x];
                 dap += gm[x].x * m[x].x + gm[x].y * m[x].y + gm[x].z * m[x].z + gm[x].w * m[x].w;
             }
-            *reinterpret_cast<float4 *>(&sm.red[rg][c4s]) = dwp;
+            *reinterpret_cast<float4 *>(&rd.red[rg][c4s]) = dwp;
+            store_row_sums<C::RPT, C::LPR, C::RPP>(dqp, a.pq + part(t) * DK, rg, lane);
             dap = warp_sum(dap);
-            if (lane == 0) sm.wsum[0][warp] = dap;
+            if (lane == 0) rd.wsum[warp] = dap;
             __syncthreads();                             // (C)
-            if (tid < DV) {
-                float dw = 0.f;
+            if (warp == 0) {   // dw = GM^T k (column sums), dv, dp; this slice's parts of dg, dbeta
+                const float dw = col_sum<C::RPP, DV>(rd.red, lane);
+                a.dv[t * HVDV + (long long)h * DVH + col0 + lane] = bv * dw;
+                rd.dp[lane] = -av * bv * dw;
+                const float db = warp_sum(dw * rd.r[tt][lane]);
+                const float da2 = warp_sum(dw * rd.p[tt][lane]);
+                if (lane == 0) {
+                    float da = 0.f;
 #pragma unroll
-                for (int r = 0; r < C::RPP; ++r) dw += sm.red[r][tid];
-                a.dv[t * HVDV + (long long)h * DVH + col0 + tid] = bv * dw;
-                sm.dp[tid] = -av * bv * dw;
-                const float db = warp_sum(dw * sm.r[tid]);
-                const float da2 = warp_sum(dw * sm.p[tid]);
-                if (lane == 0) { sm.wsum[1][warp] = db; sm.wsum[2][warp] = da2; }
+                    for (int wi = 0; wi < NW; ++wi) da += rd.wsum[wi];
+                    a.pda[part(t)] = da;
+                    a.pda2[part(t)] = da2;
+                    a.pdb[part(t)] = db;
+                }
             }
             __syncthreads();                             // (D)
-            if (tid == 0) {   // this slice's parts of <GM, M>, dw . p and dw . r
-                float da = 0.f, db = 0.f, da2 = 0.f;
-                for (int wi = 0; wi < NW; ++wi) da += sm.wsum[0][wi];
-                for (int wi = 0; wi < DV / 32; ++wi) { db += sm.wsum[1][wi]; da2 += sm.wsum[2][wi]; }
-                a.pda[part(t)] = da;
-                a.pda2[part(t)] = da2;
-                a.pdb[part(t)] = db;
-            }
-            const float4 dp4 = *reinterpret_cast<const float4 *>(&sm.dp[c4s]);
+            const float4 dp4 = *reinterpret_cast<const float4 *>(&rd.dp[c4s]);
+            float dkp[C::RPT];
 #pragma unroll
-            for (int x = 0; x < C::RPT; ++x) {
-                const int row = rg + x * C::RPP;
-                const float kr = in.k[row];
-                const float dk = row_sum<C::LPR>(gm[x].x * w4.x + gm[x].y * w4.y + gm[x].z * w4.z +
-                                                 gm[x].w * w4.w + m[x].x * dp4.x + m[x].y * dp4.y +
-                                                 m[x].z * dp4.z + m[x].w * dp4.w);
-                if (lane % C::LPR == 0) a.pk[part(t) * DK + row] = dk;
-                gm[x].x = av * gm[x].x + kr * dp4.x; gm[x].y = av * gm[x].y + kr * dp4.y;
-                gm[x].z = av * gm[x].z + kr * dp4.z; gm[x].w = av * gm[x].w + kr * dp4.w;
+            for (int x = 0; x < C::RPT; ++x) {   // dk = GM w + M dp, then GM <- a GM + k dp^T
+                dkp[x] = gm[x].x * w4.x + gm[x].y * w4.y + gm[x].z * w4.z + gm[x].w * w4.w +
+                         m[x].x * dp4.x + m[x].y * dp4.y + m[x].z * dp4.z + m[x].w * dp4.w;
+                gm[x].x = av * gm[x].x + kr[x] * dp4.x; gm[x].y = av * gm[x].y + kr[x] * dp4.y;
+                gm[x].z = av * gm[x].z + kr[x] * dp4.z; gm[x].w = av * gm[x].w + kr[x] * dp4.w;
             }
+            store_row_sums<C::RPT, C::LPR, C::RPP>(dkp, a.pk + part(t) * DK, rg, lane);
         }
     }
     if (a.d_state_in) {
@@ -409,11 +486,18 @@ cudaError_t launch_bwd_t(const BwdArgs &a, bool states_only, cudaStream_t s) {
     bwd_map_kernel<<<1, 32, 0, s>>>(a.cu_seqlens, a.n_seqs, a.T, a.d.chunk, a.chunk_base, a.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    constexpr int smem = (int)sizeof(BwdSmem<D, BWD_DVS, TA>);
     if (states_only) {
-        bwd_states_kernel<D, BWD_DVS, TA><<<grid, 4 * BWD_DVS, 0, s>>>(a);
+        auto kern = bwd_states_kernel<D, BWD_DVS, TA>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return e;
+        kern<<<grid, 4 * BWD_DVS, smem, s>>>(a);
         return cudaGetLastError();
     }
-    bwd_kernel<D, BWD_DVS, TA><<<grid, 4 * BWD_DVS, 0, s>>>(a);
+    auto kern = bwd_kernel<D, BWD_DVS, TA>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+        return e;
+    kern<<<grid, 4 * BWD_DVS, smem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     long long total = a.T * a.d.hk * a.d.dk;
     int blocks = (int)((total + 255) / 256);
