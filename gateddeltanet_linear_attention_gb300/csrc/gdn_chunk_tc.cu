@@ -39,6 +39,8 @@
 // Operands whose contraction index is the token or the dk row (bV, K,
 // M, U', T^T) are stored MN-major, so that every operand is written from its
 // natural row layout with 16-byte stores.
+#include <cuda.h>   // CUtensorMap (the encoder itself is reached through the runtime)
+
 #include "gdn_common.cuh"
 #include "tc_sm103.cuh"
 
@@ -189,6 +191,35 @@ __device__ __forceinline__ void put4(unsigned char *hi, unsigned char *lo, uint3
 // contiguous bytes of a core-matrix tile.  Column of group i, part j: 16 i + 4 q + j.
 __device__ __forceinline__ int il_row(int tid) { return 8 * (tid >> 5) + ((tid & 31) >> 2); }
 __device__ __forceinline__ int il_q(int tid) { return tid & 3; }
+// The q/k rows of a chunk arrive by TMA as one tile per matrix: 128 / sizeof(T)-element wide
+// boxes of 64 rows x 128 bytes (8 KB each, side by side), stored with the 128-byte swizzle
+// (16-byte chunk c of row r at chunk c ^ (r & 7)).  Row `row`, columns 16 i + 4 q + 0..3 for
+// i < 8, into v: the same values load_row_il reads from global memory.
+constexpr int TP_BOX_BYTES = 64 * 128;
+template <typename T>
+__device__ __forceinline__ void read_row_sw(const unsigned char *tile, int row, int q, float (&v)[32]) {
+    const unsigned char *rb = tile + row * 128;
+    const int sw = row & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float t[4];
+        if constexpr (sizeof(T) == 4) {
+            const int c = (i & 1) * 4 + q;
+            const float4 f = *reinterpret_cast<const float4 *>(rb + (i >> 1) * TP_BOX_BYTES + ((c ^ sw) << 4));
+            t[0] = f.x; t[1] = f.y; t[2] = f.z; t[3] = f.w;
+        } else {
+            const int c = (i & 3) * 2 + (q >> 1);
+            const uint2 u = *reinterpret_cast<const uint2 *>(rb + (i >> 2) * TP_BOX_BYTES + ((c ^ sw) << 4) +
+                                                            (q & 1) * 8);
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+            t[0] = a.x; t[1] = a.y; t[2] = b.x; t[3] = b.y;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[4 * i + j] = t[j];
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ void load_row_il(const T *row, int q, float (&v)[32]) {
 #pragma unroll
@@ -361,7 +392,8 @@ __device__ __forceinline__ void put8g(unsigned char *hi, unsigned char *lo, uint
 }
 
 template <typename TIn>
-__global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
+__global__ void __launch_bounds__(TC_NT, 2)
+    chunk_tp_kernel(ChunkArgs a, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q) {
     using L = TpSmem;
     extern __shared__ __align__(1024) unsigned char sm[];
     unsigned char *kqh = sm + L::OFF_KQ, *kql = kqh + L::KQ;
@@ -379,6 +411,7 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 8);
     volatile uint32_t *wait_flag = reinterpret_cast<uint32_t *>(sm + L::OFF_BAR + 12);
     int *sfind = reinterpret_cast<int *>(sm + L::OFF_BAR + 16);
+    uint64_t *tma_bar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR + 24);
 
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -405,19 +438,25 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     seq_bounds(a.cu_seqlens, lo, a.T, nullptr, s, e);   // malformed bounds are reported by the map
     const long long t0 = s + (j - a.chunk_base[lo]) * TC_C;
 
-    // ---- loads first: the q/k rows of this chunk and the gates of every v-head of the q/k head
-    const int ir = il_row(tid), iq = il_q(tid);
-    float kv[32], qv[32];
-    {
-        const long long t = t0 + ir;
-        if (t < e) {
-            load_row_il((const TIn *)a.k + t * a.ld_qk + (long long)kh * TC_DK, iq, kv);
-            load_row_il((const TIn *)a.q + t * a.ld_qk + (long long)kh * TC_DK, iq, qv);
-        } else {
+    // ---- loads first: the chunk's k and q tiles (64 rows x dk) by TMA into the Gram region,
+    // where the [K;Q] operand goes once they are read; the gates of every v-head of the q/k head
+    // by plain loads meanwhile
+    constexpr int TILE = 64 * TC_DK * (int)sizeof(TIn), NBOX = TILE / TP_BOX_BYTES;
+    constexpr int BOXW = 128 / (int)sizeof(TIn);          // elements per box row
+    if (tid == 0) {
+        const uint32_t tb = tc::smem_u32(tma_bar);
+        tc::mbar_init(tb, 1);
+        tc::mbar_fence_init();
+        tc::mbar_arrive_expect_tx(tb, 2 * TILE);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
+        for (int b = 0; b < NBOX; ++b) {
+            tc::tma_load_2d(tc::smem_u32(sm + L::OFF_KQ + b * TP_BOX_BYTES), &tm_k, kh * TC_DK + b * BOXW, (int)t0, tb);
+            tc::tma_load_2d(tc::smem_u32(sm + L::OFF_KQ + TILE + b * TP_BOX_BYTES), &tm_q, kh * TC_DK + b * BOXW,
+                            (int)t0, tb);
         }
     }
+    const int ir = il_row(tid), iq = il_q(tid);
+    float kv[32], qv[32];
     float gload = 0.f, bload = 0.f;
     const int gi_l = tid >> 6, r_l = tid & 63;     // (v-head, row) this thread loads
     if (gi_l < d.grp) {
@@ -444,6 +483,22 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     tc::fence_after_sync();
     const uint32_t tbase = *tmem_slot;
     MmaSync ms{mbar, wait_flag, 0u, a.d.wait_ns};
+    // the tiles (one bounded wait, the outcome shared through the flag), then this thread's row;
+    // rows past the sequence end are zero
+    bool tma_ok;
+    {
+        MmaSync tw{tma_bar, wait_flag, 0u, a.d.wait_ns};
+        tma_ok = tw.wait(tid);
+        const long long t = t0 + ir;
+        if (tma_ok && t < e) {
+            read_row_sw<TIn>(sm + L::OFF_KQ, ir, iq, kv);
+            read_row_sw<TIn>(sm + L::OFF_KQ + TILE, ir, iq, qv);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) kv[i] = qv[i] = 0.f;
+        }
+        __syncthreads();   // every tile read is done before the operands overwrite the region
+    }
     const int qd = warp & 3, hf = warp >> 2, tl = qd * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const bool l2 = (a.flags & GDN_FLAG_L2NORM_QK) != 0;
@@ -466,7 +521,7 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     }
     sync_for_mma();
     // ---- G1: [K;Q] K^T -> K K^T (TMEM lanes 0-63), Q K^T (64-127), columns 0-63; K -> workspace
-    if (tid == 0) {
+    if (tid == 0 && tma_ok) {
         tc::bulk_s2g(a.kt + ((long long)j * d.hk + kh) * KT_BYTES, tc::smem_u32(b3h), KT_BYTES);
         tc::bulk_commit();
         mma3<false, false, 128>(tbase + TP_COL_G1, tc::smem_u32(kqh), tc::smem_u32(kql), 0,
@@ -482,7 +537,7 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
         a.kdec[((long long)j * d.hv + h) * TC_C + r_l] = expf(Gl - Gr);
         if (r_l == 0) a.gl[j * d.hv + h] = Gl;
     }
-    bool ok = ms.wait(tid);     // (G1; its barrier also publishes the gate arrays)
+    bool ok = tma_ok && ms.wait(tid);     // (G1; its barrier also publishes the gate arrays)
 
     for (int gi = 0; gi < d.grp && ok; ++gi) {
         const int h = kh * d.grp + gi;
@@ -737,7 +792,8 @@ __global__ void __launch_bounds__(TC_NT, 2) chunk_tp_kernel(ChunkArgs a) {
     if (!ok) {
         if (tid == 0) {
             set_error(a.err, GDN_DEVERR_TIMEOUT);
-            tc::mbar_wait(tc::smem_u32(mbar), ms.phase, a.d.wait_ns);
+            if (tma_ok) tc::mbar_wait(tc::smem_u32(mbar), ms.phase, a.d.wait_ns);
+            else tc::mbar_wait(tc::smem_u32(tma_bar), 0u, a.d.wait_ns);   // the tiles still in flight
         }
         __syncthreads();
     }
@@ -1253,6 +1309,38 @@ __global__ void __launch_bounds__(NORM ? CHAIN_NT_NORM : CHAIN_NT, 1) chunk_chai
     if (warp == 0) tc::tmem_dealloc(tbase, 256);
 }
 
+// The tensor map of a q or k view, [T][width] elements with a row stride of ld elements, read as
+// 64-row boxes 128 bytes wide with the 128-byte swizzle (read_row_sw undoes it).  The encoder is
+// a driver entry point, looked up once through the runtime.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+template <typename TIn>
+static cudaError_t encode_qk_map(CUtensorMap *m, const void *base, long long ld, int width, long long T) {
+    const EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(TIn)};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / sizeof(TIn)), 64u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(m, sizeof(TIn) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int DVS, typename TIn, typename TOut, bool NORM>
 static cudaError_t launch_tc_t(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t err;
@@ -1260,10 +1348,14 @@ static cudaError_t launch_tc_t(const ChunkArgs &a, cudaStream_t s) {
         chunk_map_kernel<<<1, 1024, 0, s>>>(a);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         if (a.max_chunks > 0) {
+            CUtensorMap tmk, tmq;
+            if ((err = encode_qk_map<TIn>(&tmk, a.k, a.ld_qk, a.d.hk * TC_DK, a.T)) != cudaSuccess ||
+                (err = encode_qk_map<TIn>(&tmq, a.q, a.ld_qk, a.d.hk * TC_DK, a.T)) != cudaSuccess)
+                return err;
             auto tp = chunk_tp_kernel<TIn>;
             err = cudaFuncSetAttribute(tp, cudaFuncAttributeMaxDynamicSharedMemorySize, TpSmem::BYTES);
             if (err != cudaSuccess) return err;
-            tp<<<(unsigned)(a.max_chunks * a.d.hk), TC_NT, TpSmem::BYTES, s>>>(a);
+            tp<<<(unsigned)(a.max_chunks * a.d.hk), TC_NT, TpSmem::BYTES, s>>>(a, tmk, tmq);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     }

@@ -267,6 +267,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_saddr, const void *src, ui
         :: "r"(dst_saddr), "l"(src), "r"(bytes), "r"(mbar_saddr) : "memory");
 }
 
+// 2-D tiled tensor load (TMA): the box at element coordinates (x, y) of the tensor map `tmap`
+// (a kernel parameter, __grid_constant__) into shared memory at dst_saddr, completion counted
+// on the mbarrier.  x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst_saddr, const void *tmap, int x, int y,
+                                            uint32_t mbar_saddr) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst_saddr), "l"(tmap), "r"(x), "r"(y), "r"(mbar_saddr) : "memory");
+}
+
 // Bring the line holding p into L2 (no register result).
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
