@@ -132,11 +132,10 @@ struct ChunkIn {
 };
 
 // Reductions of one token step, and the forward quantities of every token of the chunk that
-// the reverse pass reuses: p = M^T k, r = v - a p and w = beta r (per column of the slice).
+// the reverse pass reuses: p = M^T k and w = beta (v - a p) (per column of the slice).
 template <int DK, int DV>
 struct BwdRed {
     alignas(16) float p[kBwdMaxChunk][DV];
-    alignas(16) float r[kBwdMaxChunk][DV];
     alignas(16) float w[kBwdMaxChunk][DV];
     alignas(16) float dp[DV];
     alignas(16) float red[BwdCfg<DK, DV>::RPP][DV];
@@ -217,10 +216,8 @@ __device__ __forceinline__ void fwd_token(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdR
     const float av = expf(in.g[tt]);
     if (tid < DV) {
         const float p = col_sum<C::RPP, DV>(rd.red, tid);
-        const float rr = to_f32(in.v[tt][tid]) - av * p;
         rd.p[tt][tid] = p;
-        rd.r[tt][tid] = rr;
-        rd.w[tt][tid] = in.b[tt] * rr;
+        rd.w[tt][tid] = in.b[tt] * (to_f32(in.v[tt][tid]) - av * p);
     }
     __syncthreads();
     if (!update) return;
@@ -285,6 +282,90 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
     }
 }
 
+// dL/dS entering the second half of each sequence, for the first half's walk in bwd_kernel: the
+// gradient alone carried back over chunks [cs, nch) from d_state_out.  Per token (reverse),
+// with G = dL/dM after the token: G <- a (G + q do^T) - a beta k (k^T (G + q do^T)), which needs
+// no forward state.  One CTA per (sequence, v-head, slice), two barriers per token.
+template <int DK, int DV, typename TA>
+__global__ void __launch_bounds__(4 * DV) bwd_gm_kernel(BwdArgs a) {
+    using C = BwdCfg<DK, DV>;
+    static_assert(DV == 32, "the per-column steps run on warp 0, one column per lane");
+    extern __shared__ __align__(16) unsigned char smraw[];
+    BwdSmem<DK, DV, TA> &sm = *reinterpret_cast<BwdSmem<DK, DV, TA> *>(smraw);
+    BwdRed<DK, DV> &rd = sm.rd;
+    const Dims &d = a.d;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
+    const int col0 = blockIdx.z * DV;
+    const int rg = tid / C::LPR, c4s = (tid % C::LPR) * 4, c4 = c4s + col0;
+    long long s, e;
+    seq_bounds(a.cu_seqlens, n, a.T, nullptr, s, e);
+    const int slot = slot_of(a.state_idx, n, d.n_slots, nullptr);
+    const int Cc = d.chunk, DVH = d.dv;
+    const long long nch = (e - s + Cc - 1) / Cc, cs = nch / 2;
+    if (slot < 0 || cs == 0) return;                     // no first segment to feed
+    float4 gm[C::RPT];
+#pragma unroll
+    for (int x = 0; x < C::RPT; ++x) {
+        gm[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.d_state_out)
+            gm[x] = *reinterpret_cast<const float4 *>(a.d_state_out + ((long long)slot * d.hv + h) * DK * DVH +
+                                                      (long long)(rg + x * C::RPP) * DVH + c4);
+    }
+    auto bounds = [&](long long c, long long &t0, long long &t1) {
+        t0 = s + c * Cc;
+        t1 = t0 + Cc < e ? t0 + Cc : e;
+    };
+    {
+        long long u0, u1;
+        bounds(nch - 1, u0, u1);
+        stage_chunk<DK, DV, TA>(sm.in[(nch - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
+    }
+    for (long long c = nch - 1; c >= cs; --c) {
+        long long t0, t1;
+        bounds(c, t0, t1);
+        __syncthreads();                                 // every read of buffer (c - 1) & 1 is done
+        if (c > cs) {
+            long long u0, u1;
+            bounds(c - 1, u0, u1);
+            stage_chunk<DK, DV, TA>(sm.in[(c - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const ChunkIn<DK, DV, TA> &in = sm.in[c & 1];
+        for (int tt = (int)(t1 - t0) - 1; tt >= 0; --tt) {
+            const float av = expf(in.g[tt]), bv = in.b[tt];
+            const float4 do4 = *reinterpret_cast<const float4 *>(&in.dout[tt][c4s]);
+            float kr[C::RPT];
+            float4 dwp = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x) {
+                const int row = rg + x * C::RPP;
+                kr[x] = to_f32(in.k[tt][row]);
+                const float qr = to_f32(in.q[tt][row]);
+                gm[x].x += qr * do4.x; gm[x].y += qr * do4.y; gm[x].z += qr * do4.z; gm[x].w += qr * do4.w;
+                dwp.x += gm[x].x * kr[x]; dwp.y += gm[x].y * kr[x]; dwp.z += gm[x].z * kr[x]; dwp.w += gm[x].w * kr[x];
+            }
+            *reinterpret_cast<float4 *>(&rd.red[rg][c4s]) = dwp;
+            __syncthreads();
+            if (warp == 0) rd.dp[lane] = -av * bv * col_sum<C::RPP, DV>(rd.red, lane);
+            __syncthreads();
+            const float4 dp4 = *reinterpret_cast<const float4 *>(&rd.dp[c4s]);
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x) {
+                gm[x].x = av * gm[x].x + kr[x] * dp4.x; gm[x].y = av * gm[x].y + kr[x] * dp4.y;
+                gm[x].z = av * gm[x].z + kr[x] * dp4.z; gm[x].w = av * gm[x].w + kr[x] * dp4.w;
+            }
+        }
+    }
+    float *D = a.gsplit + ((long long)n * d.hv + h) * DK * DVH;
+#pragma unroll
+    for (int x = 0; x < C::RPT; ++x)
+        *reinterpret_cast<float4 *>(D + (long long)(rg + x * C::RPP) * DVH + c4) = gm[x];
+}
+
 template <int DK, int DV, typename TA>
 __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
     using C = BwdCfg<DK, DV>;
@@ -296,7 +377,8 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
-    const int sl = blockIdx.z, NS = gridDim.z, col0 = sl * DV;   // this CTA's slice of the columns
+    const int NS = gridDim.z / 2, sl = blockIdx.z % NS, seg = blockIdx.z / NS;
+    const int col0 = sl * DV;                            // this CTA's slice of the columns
     const int rg = tid / C::LPR, c4s = (tid % C::LPR) * 4, c4 = c4s + col0;
     long long s, e;
     seq_bounds(a.cu_seqlens, n, a.T, a.err, s, e);
@@ -304,7 +386,8 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
     const int DVH = d.dv;
     const long long HVDV = (long long)d.hv * DVH;
     auto part = [&](long long t) { return (t * d.hv + h) * NS + sl; };   // index of this slice's parts
-    if (slot < 0) {                                      // padding lane: zero gradients
+    if (slot < 0) {                                      // padding lane: zero gradients (segment 1)
+        if (seg == 0) return;
         for (long long t = s; t < e; ++t) {
             for (int i = tid; i < DK; i += C::NT) {
                 a.pq[part(t) * DK + i] = 0.f;
@@ -316,28 +399,35 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
         return;
     }
     const int Cc = d.chunk;
+    const long long nch = (e - s + Cc - 1) / Cc;
+    // The sequence's chunks are split in two segments walked at the same time: segment 1 is
+    // chunks [cs, nch), starting from d_state_out; segment 0 is chunks [0, cs), starting from
+    // dL/dS entering chunk cs, which bwd_gm_kernel has carried back over segment 1.
+    const long long cs = nch / 2;
+    const long long c_lo = seg ? cs : 0, c_hi = seg ? nch : cs;
+    if (c_lo >= c_hi && !(seg == 1 && nch == 0)) return;   // (an empty sequence: segment 1 only)
+    const float *g_init = seg ? a.d_state_out : a.gsplit;
+    const long long g_off = seg ? ((long long)slot * d.hv + h) * DK * DVH : ((long long)n * d.hv + h) * DK * DVH;
     float4 gm[C::RPT];
 #pragma unroll
     for (int x = 0; x < C::RPT; ++x) {
         gm[x] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.d_state_out)
-            gm[x] = *reinterpret_cast<const float4 *>(a.d_state_out + ((long long)slot * d.hv + h) * DK * DVH +
-                                                      (long long)(rg + x * C::RPP) * DVH + c4);
+        if (g_init)
+            gm[x] = *reinterpret_cast<const float4 *>(g_init + g_off + (long long)(rg + x * C::RPP) * DVH + c4);
     }
     // this CTA's scratch: the slice of the state before each token of one chunk
-    float *scr = a.scratch + (((long long)n * d.hv + h) * NS + sl) * (long long)Cc * DK * DV;
+    float *scr = a.scratch + ((((long long)n * d.hv + h) * NS + sl) * 2 + seg) * (long long)Cc * DK * DV;
     const long long b0 = a.chunk_base[n];
-    const long long nch = (e - s + Cc - 1) / Cc;
     auto bounds = [&](long long c, long long &t0, long long &t1) {
         t0 = s + c * Cc;
         t1 = t0 + Cc < e ? t0 + Cc : e;
     };
-    if (nch > 0) {
+    if (c_hi > c_lo) {
         long long u0, u1;
-        bounds(nch - 1, u0, u1);
-        stage_chunk<DK, DV, TA>(sm.in[(nch - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
+        bounds(c_hi - 1, u0, u1);
+        stage_chunk<DK, DV, TA>(sm.in[(c_hi - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
     }
-    for (long long c = nch - 1; c >= 0; --c) {
+    for (long long c = c_hi - 1; c >= c_lo; --c) {
         long long t0, t1;
         bounds(c, t0, t1);
         float4 m[C::RPT];
@@ -348,7 +438,7 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
                 m[x] = *reinterpret_cast<const float4 *>(B + (long long)(rg + x * C::RPP) * DVH + c4);
         }
         __syncthreads();                                 // every read of buffer (c - 1) & 1 is done
-        if (c > 0) {
+        if (c > c_lo) {
             long long u0, u1;
             bounds(c - 1, u0, u1);
             stage_chunk<DK, DV, TA>(sm.in[(c - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
@@ -413,8 +503,9 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
                 const float dw = col_sum<C::RPP, DV>(rd.red, lane);
                 a.dv[t * HVDV + (long long)h * DVH + col0 + lane] = bv * dw;
                 rd.dp[lane] = -av * bv * dw;
-                const float db = warp_sum(dw * rd.r[tt][lane]);
-                const float da2 = warp_sum(dw * rd.p[tt][lane]);
+                const float pl = rd.p[tt][lane];
+                const float db = warp_sum(dw * (to_f32(in.v[tt][lane]) - av * pl));   // dw . (v - a p)
+                const float da2 = warp_sum(dw * pl);
                 if (lane == 0) {
                     float da = 0.f;
 #pragma unroll
@@ -437,7 +528,7 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
             store_row_sums<C::RPT, C::LPR, C::RPP>(dkp, a.pk + part(t) * DK, rg, lane);
         }
     }
-    if (a.d_state_in) {
+    if (a.d_state_in && c_lo == 0) {                    // the segment that ends at the first chunk
         float *D = a.d_state_in + ((long long)slot * d.hv + h) * DK * DVH;
 #pragma unroll
         for (int x = 0; x < C::RPT; ++x)
@@ -494,10 +585,15 @@ cudaError_t launch_bwd_t(const BwdArgs &a, bool states_only, cudaStream_t s) {
         kern<<<grid, 4 * BWD_DVS, smem, s>>>(a);
         return cudaGetLastError();
     }
+    auto gk = bwd_gm_kernel<D, BWD_DVS, TA>;
+    if ((e = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+        return e;
+    gk<<<grid, 4 * BWD_DVS, smem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     auto kern = bwd_kernel<D, BWD_DVS, TA>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
         return e;
-    kern<<<grid, 4 * BWD_DVS, smem, s>>>(a);
+    kern<<<dim3(a.d.hv, a.n_seqs, 2 * NS), 4 * BWD_DVS, smem, s>>>(a);   // two segments per sequence
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     long long total = a.T * a.d.hk * a.d.dk;
     int blocks = (int)((total + 255) / 256);
@@ -524,8 +620,8 @@ size_t bwd_ws_bytes(const Dims &d, long long T, long long n_seqs, bool states_on
     const size_t nsl = (size_t)(d.dv / BWD_DVS > 0 ? d.dv / BWD_DVS : 1);
     size_t b = al((ns + 1) * 4);
     if (!states_only)
-        b += al(ns * d.hv * (size_t)d.chunk * d.dk * d.dv * 4) + 2 * al(t * d.hv * nsl * d.dk * 4) +
-             3 * al(t * d.hv * nsl * 4);
+        b += al(2 * ns * d.hv * (size_t)d.chunk * d.dk * d.dv * 4) + al(ns * d.hv * (size_t)d.dk * d.dv * 4) +
+             2 * al(t * d.hv * nsl * d.dk * 4) + 3 * al(t * d.hv * nsl * 4);
     return b;
 }
 
@@ -536,7 +632,8 @@ void bwd_carve(BwdArgs &a, void *ws, bool states_only) {
     const size_t nsl = (size_t)(a.d.dv / BWD_DVS > 0 ? a.d.dv / BWD_DVS : 1);
     a.chunk_base = (int *)p; p += al((ns + 1) * 4);
     if (states_only) return;
-    a.scratch = (float *)p; p += al(ns * a.d.hv * (size_t)a.d.chunk * a.d.dk * a.d.dv * 4);
+    a.scratch = (float *)p; p += al(2 * ns * a.d.hv * (size_t)a.d.chunk * a.d.dk * a.d.dv * 4);
+    a.gsplit = (float *)p; p += al(ns * a.d.hv * (size_t)a.d.dk * a.d.dv * 4);
     a.pq = (float *)p; p += al(t * a.d.hv * nsl * a.d.dk * 4);
     a.pk = (float *)p; p += al(t * a.d.hv * nsl * a.d.dk * 4);
     a.pda = (float *)p; p += al(t * a.d.hv * nsl * 4);
