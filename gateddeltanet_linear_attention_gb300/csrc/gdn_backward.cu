@@ -195,6 +195,13 @@ __device__ __forceinline__ void stage_chunk(ChunkIn<DK, DV, TA> &ci, const BwdAr
     cp_async_commit();
 }
 
+// One row's float4 of the state through one token: M <- a M + k w^T (the replay and the reverse
+// pass's reconstruction use this same expression).
+__device__ __forceinline__ void state_update(float4 &m, float a, float k, const float4 &w) {
+    m.x = a * m.x + k * w.x; m.y = a * m.y + k * w.y;
+    m.z = a * m.z + k * w.z; m.w = a * m.w + k * w.w;
+}
+
 // The forward step of token tt of a staged chunk on M in registers: p = M^T k (column sums),
 // r = v - a p, w = beta r (kept in rd at row tt), and, when `update`, M <- a M + k w^T.
 // Two block barriers.
@@ -223,10 +230,7 @@ __device__ __forceinline__ void fwd_token(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdR
     if (!update) return;
     const float4 w4 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4]);
 #pragma unroll
-    for (int x = 0; x < C::RPT; ++x) {
-        m[x].x = av * m[x].x + kr[x] * w4.x; m[x].y = av * m[x].y + kr[x] * w4.y;
-        m[x].z = av * m[x].z + kr[x] * w4.z; m[x].w = av * m[x].w + kr[x] * w4.w;
-    }
+    for (int x = 0; x < C::RPT; ++x) state_update(m[x], av, kr[x], w4);
 }
 
 template <int DK, int DV, typename TA>
@@ -415,8 +419,8 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
         if (g_init)
             gm[x] = *reinterpret_cast<const float4 *>(g_init + g_off + (long long)(rg + x * C::RPP) * DVH + c4);
     }
-    // this CTA's scratch: the slice of the state before each token of one chunk
-    float *scr = a.scratch + ((((long long)n * d.hv + h) * NS + sl) * 2 + seg) * (long long)Cc * DK * DV;
+    // this CTA's scratch: the slice of the state before each even token of one chunk
+    float *scr = a.scratch + ((((long long)n * d.hv + h) * NS + sl) * 2 + seg) * (long long)((Cc + 1) / 2) * DK * DV;
     const long long b0 = a.chunk_base[n];
     auto bounds = [&](long long c, long long &t0, long long &t1) {
         t0 = s + c * Cc;
@@ -448,32 +452,47 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
         }
         __syncthreads();                                 // ... and everyone's
         const ChunkIn<DK, DV, TA> &in = sm.in[c & 1];
-        // forward through the chunk, keeping the state before every token (each thread reads
-        // back only what it wrote) and every token's p, r and w
+        // forward through the chunk, keeping the state before every even token (each thread
+        // reads back only what it wrote) and every token's p and w
         for (long long t = t0; t < t1; ++t) {
-            float *Sc = scr + (t - t0) * DK * DV;
+            const int tt = (int)(t - t0);
+            if ((tt & 1) == 0) {
+                float *Sc = scr + (tt >> 1) * DK * DV;
 #pragma unroll
-            for (int x = 0; x < C::RPT; ++x)
-                *reinterpret_cast<float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s) = m[x];
-            fwd_token<DK, DV, TA>(m, rd, in, (int)(t - t0), tid, rg, c4s, t + 1 < t1);
+                for (int x = 0; x < C::RPT; ++x)
+                    *reinterpret_cast<float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s) = m[x];
+            }
+            fwd_token<DK, DV, TA>(m, rd, in, tt, tid, rg, c4s, t + 1 < t1);
         }
-        // the tokens in reverse; the state before token t-1 is loaded while token t runs
+        // the tokens in reverse.  mn holds the stored state before the even token of the current
+        // pair; the state before an odd token is that one carried over the even token (its kept
+        // w, as in the replay), and the next pair's state is loaded at the even token.
         float4 mn[C::RPT];
         {
-            const float *Sc = scr + (t1 - 1 - t0) * DK * DV;
+            const float *Sc = scr + ((int)(t1 - 1 - t0) >> 1) * DK * DV;
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x)
                 mn[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s);
         }
         for (long long t = t1 - 1; t >= t0; --t) {
             const int tt = (int)(t - t0);
+            if (tt & 1) {
+                const float a0 = expf(in.g[tt - 1]);
+                const float4 w0 = *reinterpret_cast<const float4 *>(&rd.w[tt - 1][c4s]);
 #pragma unroll
-            for (int x = 0; x < C::RPT; ++x) m[x] = mn[x];
-            if (t > t0) {
-                const float *Sc = scr + (tt - 1) * DK * DV;
+                for (int x = 0; x < C::RPT; ++x) {
+                    m[x] = mn[x];
+                    state_update(m[x], a0, to_f32(in.k[tt - 1][rg + x * C::RPP]), w0);
+                }
+            } else {
 #pragma unroll
-                for (int x = 0; x < C::RPT; ++x)
-                    mn[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s);
+                for (int x = 0; x < C::RPT; ++x) m[x] = mn[x];
+                if (tt >= 2) {
+                    const float *Sc = scr + ((tt >> 1) - 1) * DK * DV;
+#pragma unroll
+                    for (int x = 0; x < C::RPT; ++x)
+                        mn[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s);
+                }
             }
             const float av = expf(in.g[tt]), bv = in.b[tt];
             const float4 w4 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4s]);
@@ -620,7 +639,7 @@ size_t bwd_ws_bytes(const Dims &d, long long T, long long n_seqs, bool states_on
     const size_t nsl = (size_t)(d.dv / BWD_DVS > 0 ? d.dv / BWD_DVS : 1);
     size_t b = al((ns + 1) * 4);
     if (!states_only)
-        b += al(2 * ns * d.hv * (size_t)d.chunk * d.dk * d.dv * 4) + al(ns * d.hv * (size_t)d.dk * d.dv * 4) +
+        b += al(2 * ns * d.hv * (size_t)((d.chunk + 1) / 2) * d.dk * d.dv * 4) + al(ns * d.hv * (size_t)d.dk * d.dv * 4) +
              2 * al(t * d.hv * nsl * d.dk * 4) + 3 * al(t * d.hv * nsl * 4);
     return b;
 }
@@ -632,7 +651,7 @@ void bwd_carve(BwdArgs &a, void *ws, bool states_only) {
     const size_t nsl = (size_t)(a.d.dv / BWD_DVS > 0 ? a.d.dv / BWD_DVS : 1);
     a.chunk_base = (int *)p; p += al((ns + 1) * 4);
     if (states_only) return;
-    a.scratch = (float *)p; p += al(2 * ns * a.d.hv * (size_t)a.d.chunk * a.d.dk * a.d.dv * 4);
+    a.scratch = (float *)p; p += al(2 * ns * a.d.hv * (size_t)((a.d.chunk + 1) / 2) * a.d.dk * a.d.dv * 4);
     a.gsplit = (float *)p; p += al(ns * a.d.hv * (size_t)a.d.dk * a.d.dv * 4);
     a.pq = (float *)p; p += al(t * a.d.hv * nsl * a.d.dk * 4);
     a.pk = (float *)p; p += al(t * a.d.hv * nsl * a.d.dk * 4);
