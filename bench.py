@@ -702,20 +702,20 @@ def bench_backward(args, dev, gdn, pk, pk_src):
     torch.cuda.synchronize()
     assert gdn.gdn_device_error() == 0
     per = sum(a.elapsed_time(b) for a, b in evs[1:]) / reps / 1e3
-    # bytes the token-level algorithm moves: per token and v-head the state before the token
-    # written to and read back from the chunk scratch, plus the boundary state per chunk
-    moved = T * HV * 2 * d * d * 4 + nb * HV * d * d * 4
+    # bytes the token-level algorithm moves: per pair of tokens and v-head the state before the
+    # even token written to and read back from the chunk scratch, plus the boundary state per chunk
+    moved = T * HV * d * d * 4 + nb * HV * d * d * 4
     return {"workload": "prefill_8k shape: one 8,192-token sequence, HK=16, HV=32, dk=dv=128, "
                         "chunk 64, bf16 q/k/v, nonzero initial state, d_o and d_state_out given",
             "tokens_per_s": T / per, "ms_per_call": per * 1e3, "states_ms": states_s * 1e3,
-            "roofline": {"kernel": "bwd_kernel (+ group sum)", "bound": "latency",
+            "roofline": {"kernel": "bwd_gm_kernel + bwd_kernel + bwd_group_sum_kernel", "bound": "latency",
                          "bytes_per_call": moved, "achieved": moved / per / 1e9, "unit": "GB/s",
                          "peak": pk["hbm_gbs"], "frac": moved / per / 1e9 / pk["hbm_gbs"],
-                         "peak_source": pk_src + " copy",
-                         "note": "128 CTAs (one per v-head and 32-column state slice) walk "
-                                 "8,192 tokens in sequence; the per-token states of a chunk stay "
-                                 "in L2 (1 MiB per CTA)"},
-            "gpu_launches": 3 * reps}
+                         "peak_source": pk_src + " copy", "traffic": traffic_for("backward_8k"),
+                         "note": "256 CTAs (v-head x 32-column state slice x two segments of the "
+                                 "sequence) walk 4,096 tokens each; the gradient entering the "
+                                 "second half comes from a pass over it that needs no forward state"},
+            "gpu_launches": 4 * reps}
 
 
 def bench_e2e(args, dev, gdn, cfg, wl, inp, d, N, T):
