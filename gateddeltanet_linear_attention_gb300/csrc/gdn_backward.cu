@@ -142,11 +142,18 @@ struct BwdRed {
     float wsum[BwdCfg<DK, DV>::NT / 32];
 };
 
-template <int DK, int DV, typename TA>
+// NB chunk buffers: two (the next chunk's copies overlap this chunk) where one CTA runs per SM,
+// one where three must fit.
+template <int DK, int DV, typename TA, int NB = 2>
 struct BwdSmem {
-    ChunkIn<DK, DV, TA> in[2];
+    ChunkIn<DK, DV, TA> in[NB];
     BwdRed<DK, DV> rd;
 };
+
+// Segments per sequence walked at once by bwd_kernel: segment k is chunks
+// [k nch / BWD_SEG, (k + 1) nch / BWD_SEG).
+constexpr int BWD_SEG = 3;
+__host__ __device__ __forceinline__ long long seg_split(int k, long long nch) { return k * nch / BWD_SEG; }
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
@@ -286,8 +293,9 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
     }
 }
 
-// dL/dS entering the second half of each sequence, for the first half's walk in bwd_kernel: the
-// gradient alone carried back over chunks [cs, nch) from d_state_out.  Per token (reverse),
+// dL/dS entering each segment's last chunk boundary, for the segments of bwd_kernel that do not
+// end at the sequence end: the gradient alone carried back from d_state_out over chunks
+// [nch / BWD_SEG, nch), and kept at every segment boundary it passes.  Per token (reverse),
 // with G = dL/dM after the token: G <- a (G + q do^T) - a beta k (k^T (G + q do^T)), which needs
 // no forward state.  One CTA per (sequence, v-head, slice), two barriers per token.
 template <int DK, int DV, typename TA>
@@ -306,8 +314,10 @@ __global__ void __launch_bounds__(4 * DV) bwd_gm_kernel(BwdArgs a) {
     seq_bounds(a.cu_seqlens, n, a.T, nullptr, s, e);
     const int slot = slot_of(a.state_idx, n, d.n_slots, nullptr);
     const int Cc = d.chunk, DVH = d.dv;
-    const long long nch = (e - s + Cc - 1) / Cc, cs = nch / 2;
-    if (slot < 0 || cs == 0) return;                     // no first segment to feed
+    const long long nch = (e - s + Cc - 1) / Cc;
+    long long cs = 0;                                    // the first split that has a segment before it
+    for (int k = 1; k < BWD_SEG && cs == 0; ++k) cs = seg_split(k, nch);
+    if (slot < 0 || cs == 0) return;                     // no earlier segment to feed
     float4 gm[C::RPT];
 #pragma unroll
     for (int x = 0; x < C::RPT; ++x) {
@@ -363,25 +373,29 @@ __global__ void __launch_bounds__(4 * DV) bwd_gm_kernel(BwdArgs a) {
                 gm[x].z = av * gm[x].z + kr[x] * dp4.z; gm[x].w = av * gm[x].w + kr[x] * dp4.w;
             }
         }
-    }
-    float *D = a.gsplit + ((long long)n * d.hv + h) * DK * DVH;
+        // the gradient entering chunk c starts every segment that ends there
+        for (int k = 1; k < BWD_SEG; ++k) {
+            if (seg_split(k, nch) != c) continue;
+            float *D = a.gsplit + (((long long)n * d.hv + h) * (BWD_SEG - 1) + (k - 1)) * DK * DVH;
 #pragma unroll
-    for (int x = 0; x < C::RPT; ++x)
-        *reinterpret_cast<float4 *>(D + (long long)(rg + x * C::RPP) * DVH + c4) = gm[x];
+            for (int x = 0; x < C::RPT; ++x)
+                *reinterpret_cast<float4 *>(D + (long long)(rg + x * C::RPP) * DVH + c4) = gm[x];
+        }
+    }
 }
 
 template <int DK, int DV, typename TA>
-__global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
     using C = BwdCfg<DK, DV>;
     constexpr int NW = C::NT / 32;
     static_assert(DV == 32, "the per-column steps run on warp 0, one column per lane");
     extern __shared__ __align__(16) unsigned char smraw[];
-    BwdSmem<DK, DV, TA> &sm = *reinterpret_cast<BwdSmem<DK, DV, TA> *>(smraw);
+    BwdSmem<DK, DV, TA, 1> &sm = *reinterpret_cast<BwdSmem<DK, DV, TA, 1> *>(smraw);
     BwdRed<DK, DV> &rd = sm.rd;
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
-    const int NS = gridDim.z / 2, sl = blockIdx.z % NS, seg = blockIdx.z / NS;
+    const int NS = gridDim.z / BWD_SEG, sl = blockIdx.z % NS, seg = blockIdx.z / NS;
     const int col0 = sl * DV;                            // this CTA's slice of the columns
     const int rg = tid / C::LPR, c4s = (tid % C::LPR) * 4, c4 = c4s + col0;
     long long s, e;
@@ -390,8 +404,8 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
     const int DVH = d.dv;
     const long long HVDV = (long long)d.hv * DVH;
     auto part = [&](long long t) { return (t * d.hv + h) * NS + sl; };   // index of this slice's parts
-    if (slot < 0) {                                      // padding lane: zero gradients (segment 1)
-        if (seg == 0) return;
+    if (slot < 0) {                                      // padding lane: zero gradients (last segment)
+        if (seg != BWD_SEG - 1) return;
         for (long long t = s; t < e; ++t) {
             for (int i = tid; i < DK; i += C::NT) {
                 a.pq[part(t) * DK + i] = 0.f;
@@ -404,14 +418,15 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
     }
     const int Cc = d.chunk;
     const long long nch = (e - s + Cc - 1) / Cc;
-    // The sequence's chunks are split in two segments walked at the same time: segment 1 is
-    // chunks [cs, nch), starting from d_state_out; segment 0 is chunks [0, cs), starting from
-    // dL/dS entering chunk cs, which bwd_gm_kernel has carried back over segment 1.
-    const long long cs = nch / 2;
-    const long long c_lo = seg ? cs : 0, c_hi = seg ? nch : cs;
-    if (c_lo >= c_hi && !(seg == 1 && nch == 0)) return;   // (an empty sequence: segment 1 only)
-    const float *g_init = seg ? a.d_state_out : a.gsplit;
-    const long long g_off = seg ? ((long long)slot * d.hv + h) * DK * DVH : ((long long)n * d.hv + h) * DK * DVH;
+    // The sequence's chunks are split in BWD_SEG segments walked at the same time.  The last
+    // starts from d_state_out; every other one from dL/dS entering the next segment's first
+    // chunk, which bwd_gm_kernel has carried back beforehand.
+    const bool last = seg == BWD_SEG - 1;
+    const long long c_lo = seg_split(seg, nch), c_hi = seg_split(seg + 1, nch);
+    if (c_lo >= c_hi && !(last && nch == 0)) return;     // (an empty sequence: the last segment only)
+    const float *g_init = last ? a.d_state_out : a.gsplit;
+    const long long g_off = last ? ((long long)slot * d.hv + h) * DK * DVH
+                                 : (((long long)n * d.hv + h) * (BWD_SEG - 1) + seg) * DK * DVH;
     float4 gm[C::RPT];
 #pragma unroll
     for (int x = 0; x < C::RPT; ++x) {
@@ -420,17 +435,12 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
             gm[x] = *reinterpret_cast<const float4 *>(g_init + g_off + (long long)(rg + x * C::RPP) * DVH + c4);
     }
     // this CTA's scratch: the slice of the state before each even token of one chunk
-    float *scr = a.scratch + ((((long long)n * d.hv + h) * NS + sl) * 2 + seg) * (long long)((Cc + 1) / 2) * DK * DV;
+    float *scr = a.scratch + ((((long long)n * d.hv + h) * NS + sl) * BWD_SEG + seg) * (long long)((Cc + 1) / 2) * DK * DV;
     const long long b0 = a.chunk_base[n];
     auto bounds = [&](long long c, long long &t0, long long &t1) {
         t0 = s + c * Cc;
         t1 = t0 + Cc < e ? t0 + Cc : e;
     };
-    if (c_hi > c_lo) {
-        long long u0, u1;
-        bounds(c_hi - 1, u0, u1);
-        stage_chunk<DK, DV, TA>(sm.in[(c_hi - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
-    }
     for (long long c = c_hi - 1; c >= c_lo; --c) {
         long long t0, t1;
         bounds(c, t0, t1);
@@ -441,17 +451,13 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
             for (int x = 0; x < C::RPT; ++x)
                 m[x] = *reinterpret_cast<const float4 *>(B + (long long)(rg + x * C::RPP) * DVH + c4);
         }
-        __syncthreads();                                 // every read of buffer (c - 1) & 1 is done
-        if (c > c_lo) {
-            long long u0, u1;
-            bounds(c - 1, u0, u1);
-            stage_chunk<DK, DV, TA>(sm.in[(c - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
-            cp_async_wait<1>();                          // this thread's copies of chunk c landed
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();                                 // ... and everyone's
-        const ChunkIn<DK, DV, TA> &in = sm.in[c & 1];
+        // one chunk buffer (three CTAs per SM): the previous chunk's reads are done, then this
+        // chunk's copies
+        __syncthreads();
+        stage_chunk<DK, DV, TA>(sm.in[0], a, t0, t1, h, kh, col0, true, tid);
+        cp_async_wait<0>();
+        __syncthreads();
+        const ChunkIn<DK, DV, TA> &in = sm.in[0];
         // forward through the chunk, keeping the state before every even token (each thread
         // reads back only what it wrote) and every token's p and w
         for (long long t = t0; t < t1; ++t) {
@@ -548,6 +554,7 @@ __global__ void __launch_bounds__(4 * DV) bwd_kernel(BwdArgs a) {
         }
     }
     if (a.d_state_in && c_lo == 0) {                    // the segment that ends at the first chunk
+        // (the first non-empty one; for an empty sequence, the last)
         float *D = a.d_state_in + ((long long)slot * d.hv + h) * DK * DVH;
 #pragma unroll
         for (int x = 0; x < C::RPT; ++x)
@@ -597,6 +604,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, bool states_only, cudaStream_t s) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     constexpr int smem = (int)sizeof(BwdSmem<D, BWD_DVS, TA>);
+    constexpr int smem1 = (int)sizeof(BwdSmem<D, BWD_DVS, TA, 1>);
     if (states_only) {
         auto kern = bwd_states_kernel<D, BWD_DVS, TA>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
@@ -610,9 +618,9 @@ cudaError_t launch_bwd_t(const BwdArgs &a, bool states_only, cudaStream_t s) {
     gk<<<grid, 4 * BWD_DVS, smem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     auto kern = bwd_kernel<D, BWD_DVS, TA>;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem1)) != cudaSuccess)
         return e;
-    kern<<<dim3(a.d.hv, a.n_seqs, 2 * NS), 4 * BWD_DVS, smem, s>>>(a);   // two segments per sequence
+    kern<<<dim3(a.d.hv, a.n_seqs, BWD_SEG * NS), 4 * BWD_DVS, smem1, s>>>(a);   // BWD_SEG segments per sequence
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     long long total = a.T * a.d.hk * a.d.dk;
     int blocks = (int)((total + 255) / 256);
@@ -639,7 +647,8 @@ size_t bwd_ws_bytes(const Dims &d, long long T, long long n_seqs, bool states_on
     const size_t nsl = (size_t)(d.dv / BWD_DVS > 0 ? d.dv / BWD_DVS : 1);
     size_t b = al((ns + 1) * 4);
     if (!states_only)
-        b += al(2 * ns * d.hv * (size_t)((d.chunk + 1) / 2) * d.dk * d.dv * 4) + al(ns * d.hv * (size_t)d.dk * d.dv * 4) +
+        b += al((size_t)BWD_SEG * ns * d.hv * (size_t)((d.chunk + 1) / 2) * d.dk * d.dv * 4) +
+             al((size_t)(BWD_SEG - 1) * ns * d.hv * (size_t)d.dk * d.dv * 4) +
              2 * al(t * d.hv * nsl * d.dk * 4) + 3 * al(t * d.hv * nsl * 4);
     return b;
 }
@@ -651,8 +660,8 @@ void bwd_carve(BwdArgs &a, void *ws, bool states_only) {
     const size_t nsl = (size_t)(a.d.dv / BWD_DVS > 0 ? a.d.dv / BWD_DVS : 1);
     a.chunk_base = (int *)p; p += al((ns + 1) * 4);
     if (states_only) return;
-    a.scratch = (float *)p; p += al(2 * ns * a.d.hv * (size_t)((a.d.chunk + 1) / 2) * a.d.dk * a.d.dv * 4);
-    a.gsplit = (float *)p; p += al(ns * a.d.hv * (size_t)a.d.dk * a.d.dv * 4);
+    a.scratch = (float *)p; p += al((size_t)BWD_SEG * ns * a.d.hv * (size_t)((a.d.chunk + 1) / 2) * a.d.dk * a.d.dv * 4);
+    a.gsplit = (float *)p; p += al((size_t)(BWD_SEG - 1) * ns * a.d.hv * (size_t)a.d.dk * a.d.dv * 4);
     a.pq = (float *)p; p += al(t * a.d.hv * nsl * a.d.dk * 4);
     a.pk = (float *)p; p += al(t * a.d.hv * nsl * a.d.dk * 4);
     a.pda = (float *)p; p += al(t * a.d.hv * nsl * 4);

@@ -181,8 +181,8 @@ struct BwdArgs {
     unsigned *err;
     // workspace (bwd_carve)
     int *chunk_base;              // [n_seqs + 1]
-    float *scratch;               // [n_seqs][HV][slices][2][chunk/2][dk][32]: states before the even tokens of a chunk
-    float *gsplit;                // [n_seqs][HV][dk][dv]: dL/dS entering the second half of each sequence
+    float *scratch;               // [n_seqs][HV][slices][segments][chunk/2][dk][32]: states before the even tokens
+    float *gsplit;                // [n_seqs][HV][segments-1][dk][dv]: dL/dS entering each later segment
     float *pq, *pk;               // [T][HV][slices][dk]: the parts of dq, dk from each 32-column slice
     float *pda, *pda2, *pdb;      // [T][HV][slices]: the parts of <GM, M>, dw . p and dw . r
 };
