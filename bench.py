@@ -712,9 +712,10 @@ def bench_backward(args, dev, gdn, pk, pk_src):
                          "bytes_per_call": moved, "achieved": moved / per / 1e9, "unit": "GB/s",
                          "peak": pk["hbm_gbs"], "frac": moved / per / 1e9 / pk["hbm_gbs"],
                          "peak_source": pk_src + " copy", "traffic": traffic_for("backward_8k"),
-                         "note": "256 CTAs (v-head x 32-column state slice x two segments of the "
-                                 "sequence) walk 4,096 tokens each; the gradient entering the "
-                                 "second half comes from a pass over it that needs no forward state"},
+                         "note": "384 CTAs (v-head x 32-column state slice x three segments of the "
+                                 "sequence, 3 per SM) walk about 2,731 tokens each; the gradients "
+                                 "entering the later segments come from a pass over them that "
+                                 "needs no forward state"},
             "gpu_launches": 4 * reps}
 
 
