@@ -292,8 +292,10 @@ gdn_status gdn_mixer_decode_q8(const gdn_config *cfg, const gdn_mixer_io *io, in
  * [dv] fp32, the gradient with respect to the initial state of each
  * sequence's slot).  boundary_states as written by gdn_chunk_states for the
  * same batch.  Padding lanes get zero gradients.  workspace: at least
- * gdn_backward_workspace_size(cfg, T, n_seqs) bytes (one chunk of states
- * per (sequence, v-head), dq and dk per v-head). */
+ * gdn_backward_workspace_size(cfg, T, n_seqs) bytes (the replayed states of
+ * one chunk and the gradients entering the segments each sequence is walked
+ * in, per (sequence, v-head), and the per-slice parts of dq, dk, dg and dbeta
+ * per token). */
 size_t gdn_backward_workspace_size(const gdn_config *cfg, int64_t max_tokens, int32_t max_seqs);
 gdn_status gdn_chunk_states(const gdn_config *cfg, const void *k, int64_t ld_qk, const void *v,
                             int64_t ld_v, gdn_dtype in_dtype, const float *g, const float *beta,
