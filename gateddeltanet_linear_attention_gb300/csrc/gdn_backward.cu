@@ -468,11 +468,14 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
                 for (int x = 0; x < C::RPT; ++x)
                     *reinterpret_cast<float4 *>(Sc + (long long)(rg + x * C::RPP) * DV + c4s) = m[x];
             }
-            fwd_token<DK, DV, TA>(m, rd, in, tt, tid, rg, c4s, t + 1 < t1);
+            fwd_token<DK, DV, TA>(m, rd, in, tt, tid, rg, c4s, true);
         }
-        // the tokens in reverse.  mn holds the stored state before the even token of the current
-        // pair; the state before an odd token is that one carried over the even token (its kept
-        // w, as in the replay), and the next pair's state is loaded at the even token.
+        // the tokens in reverse.  m enters each step as the state after the token (the replay
+        // ends with the state after the chunk's last token), which is the M' of dq = M' do; it
+        // then becomes the state before the token.  mn holds the stored state before the even
+        // token of the current pair; the state before an odd token is that one carried over the
+        // even token (its kept w, as in the replay), and the next pair's state is loaded at the
+        // even token.
         float4 mn[C::RPT];
         {
             const float *Sc = scr + ((int)(t1 - 1 - t0) >> 1) * DK * DV;
@@ -482,6 +485,11 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
         }
         for (long long t = t1 - 1; t >= t0; --t) {
             const int tt = (int)(t - t0);
+            const float4 do4 = *reinterpret_cast<const float4 *>(&in.dout[tt][c4s]);
+            float dqp[C::RPT];
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x)                 // dq = M' do, M' the state after the token
+                dqp[x] = m[x].x * do4.x + m[x].y * do4.y + m[x].z * do4.z + m[x].w * do4.w;
             if (tt & 1) {
                 const float a0 = expf(in.g[tt - 1]);
                 const float4 w0 = *reinterpret_cast<const float4 *>(&rd.w[tt - 1][c4s]);
@@ -502,20 +510,15 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
             }
             const float av = expf(in.g[tt]), bv = in.b[tt];
             const float4 w4 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4s]);
-            const float4 do4 = *reinterpret_cast<const float4 *>(&in.dout[tt][c4s]);
             float4 dwp = make_float4(0.f, 0.f, 0.f, 0.f);
             float dap = 0.f;
-            float kr[C::RPT], dqp[C::RPT];
+            float kr[C::RPT];
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x) {
                 const int row = rg + x * C::RPP;
                 kr[x] = to_f32(in.k[tt][row]);
                 const float qr = to_f32(in.q[tt][row]);
-                float4 mp;                               // M' = a M + k w^T
-                mp.x = av * m[x].x + kr[x] * w4.x; mp.y = av * m[x].y + kr[x] * w4.y;
-                mp.z = av * m[x].z + kr[x] * w4.z; mp.w = av * m[x].w + kr[x] * w4.w;
                 gm[x].x += qr * do4.x; gm[x].y += qr * do4.y; gm[x].z += qr * do4.z; gm[x].w += qr * do4.w;
-                dqp[x] = mp.x * do4.x + mp.y * do4.y + mp.z * do4.z + mp.w * do4.w;   // dq = M' do
                 dwp.x += gm[x].x * kr[x]; dwp.y += gm[x].y * kr[x]; dwp.z += gm[x].z * kr[x]; dwp.w += gm[x].w * kr[x];
                 dap += gm[x].x * m[x].x + gm[x].y * m[x].y + gm[x].z * m[x].z + gm[x].w * m[x].w;
             }
