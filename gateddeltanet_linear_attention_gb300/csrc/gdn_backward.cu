@@ -21,7 +21,10 @@
 //    slice), the forward over the sequence with the slice of M in registers
 //    (thread: one float4 column group over RPT rows, 8 lanes per 128-byte row
 //    segment), writing it at every chunk start: the states a training forward
-//    retains;
+//    retains.  It takes the tokens in pairs: one pass over M gives M^T k of
+//    both, and the pair's k . k fixes the second token's p;
+//  - bwd_gm_kernel: dL/dS at the segment boundaries of the walk below,
+//    carried back without the forward states, also in token pairs;
 //  - bwd_kernel (gdn_chunk_backward): one CTA per (sequence, v-head, slice),
 //    the chunks in reverse: the forward of the chunk from its boundary state,
 //    keeping the state before every token in the workspace, then the tokens in
@@ -114,6 +117,19 @@ __device__ __forceinline__ float col_sum(const float (&red)[RPP][DV], int col) {
     return t[0];
 }
 
+// Sum of the RPP partial column sums red[0..RPP)[v][col] of a pair step, as a tree.
+template <int RPP, int DV>
+__device__ __forceinline__ float col_sum2(const float (&red)[RPP][2][DV], int v, int col) {
+    float t[RPP];
+#pragma unroll
+    for (int r = 0; r < RPP; ++r) t[r] = red[r][v][col];
+#pragma unroll
+    for (int w = RPP / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int r = 0; r < w; ++r) t[r] += t[r + w];
+    return t[0];
+}
+
 // ---- token inputs, staged one chunk at a time
 // A chunk's inputs of one (v-head, slice) go to shared memory by asynchronous copies
 // (cp.async, 16 bytes per copy for the rows, 4 for the gates) issued one chunk ahead, so a
@@ -142,13 +158,28 @@ struct BwdRed {
     float wsum[BwdCfg<DK, DV>::NT / 32];
 };
 
+// The same for the steps over pairs of tokens (forward states, gradient pass): two column-sum
+// partials per row group, the pair's two dp, and the pair dot products k_2j . k_2j+1 and
+// q_2j . k_2j.  (The backward walk keeps the smaller single-token form: its shared memory
+// decides how much of the SM's L1 is left, which measurably changes its speed.)
+template <int DK, int DV>
+struct BwdRedPair {
+    alignas(16) float p[kBwdMaxChunk][DV];
+    alignas(16) float w[kBwdMaxChunk][DV];
+    alignas(16) float red2[BwdCfg<DK, DV>::RPP][2][DV];
+    alignas(16) float dp2[2][DV];
+    float kk[kBwdMaxChunk / 2], qk[kBwdMaxChunk / 2];
+};
+
 // NB chunk buffers: two (the next chunk's copies overlap this chunk) where one CTA runs per SM,
 // one where three must fit.
-template <int DK, int DV, typename TA, int NB = 2>
+template <int DK, int DV, typename TA, int NB = 2, typename RED = BwdRed<DK, DV>>
 struct BwdSmem {
     ChunkIn<DK, DV, TA> in[NB];
-    BwdRed<DK, DV> rd;
+    RED rd;
 };
+template <int DK, int DV, typename TA>
+using BwdSmemPair = BwdSmem<DK, DV, TA, 2, BwdRedPair<DK, DV>>;
 
 // Segments per sequence walked at once by bwd_kernel: segment k is chunks
 // [k nch / BWD_SEG, (k + 1) nch / BWD_SEG).
@@ -171,7 +202,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // q and d_o when `with_q`; one commit group per call (possibly empty).  Row starts are 16-byte
 // aligned: the entry points require 16-byte aligned bases and row strides that are multiples of
 // 8 elements, and the slice's first column col0 is a multiple of 32.
-template <int DK, int DV, typename TA>
+template <int DK, int DV, typename TA, bool PAIRS = false>
 __device__ __forceinline__ void stage_chunk(ChunkIn<DK, DV, TA> &ci, const BwdArgs &a, long long t0,
                                             long long t1, int h, int kh, int col0, bool with_q, int tid) {
     constexpr int NT = BwdCfg<DK, DV>::NT;
@@ -200,13 +231,96 @@ __device__ __forceinline__ void stage_chunk(ChunkIn<DK, DV, TA> &ci, const BwdAr
         else cp_async4(&ci.g[r], a.g + (t0 + r) * a.d.hv + h);
     }
     cp_async_commit();
+    // An odd chunk is walked in pairs with one neutral token after its last: k = q = v = d_o = 0,
+    // g = 0 (a = 1) and beta = 0 leave the state, the gradient and every other token unchanged.
+    // Row L is no copy's target; the barrier after the copies' wait publishes these stores.
+    if (PAIRS && (L & 1)) {
+        for (int i = tid; i < DK; i += NT) {
+            ci.k[L][i] = from_f32<TA>(0.f);
+            if (with_q) ci.q[L][i] = from_f32<TA>(0.f);
+        }
+        for (int i = tid; i < DV; i += NT) {
+            ci.v[L][i] = from_f32<TA>(0.f);
+            if (with_q) ci.dout[L][i] = 0.f;
+        }
+        if (tid == 0) { ci.g[L] = 0.f; ci.b[L] = 0.f; }
+    }
 }
+
+// The dot products the pair steps need, for the pairs (2j, 2j+1) of a staged chunk of L tokens:
+// kk[j] = k_2j . k_2j+1 and, with q staged, qk[j] = q_2j . k_2j.  Four threads per product (a
+// quarter of the dk terms each, then two shuffles); the caller's next barrier publishes them.
+template <int DK, int DV, typename TA>
+__device__ __forceinline__ void pair_dots(const ChunkIn<DK, DV, TA> &ci, BwdRedPair<DK, DV> &rd, int L, bool with_q,
+                                          int tid) {
+    constexpr int NT = BwdCfg<DK, DV>::NT, Q = DK / 4;
+    static_assert(NT % 4 == 0 && (2 * kBwdMaxChunk / 2) * 4 % NT == 0, "whole groups of four lanes");
+    const int np = (L + 1) >> 1;
+#pragma unroll
+    for (int u = 0; u < (2 * kBwdMaxChunk / 2) * 4 / NT; ++u) {
+        const int task = tid + u * NT, prod = task >> 2, part = task & 3;
+        const bool isq = prod >= kBwdMaxChunk / 2;
+        const int j = isq ? prod - kBwdMaxChunk / 2 : prod;
+        float acc = 0.f;
+        if (j < np && (!isq || with_q)) {
+            const TA *x = isq ? ci.q[2 * j] : ci.k[2 * j];
+            const TA *y = isq ? ci.k[2 * j] : ci.k[2 * j + 1];
+#pragma unroll 8
+            for (int i = part * Q; i < part * Q + Q; ++i) acc = fmaf(to_f32(x[i]), to_f32(y[i]), acc);
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        if (part == 0 && j < np) (isq ? rd.qk : rd.kk)[j] = acc;
+    }
+}
+
 
 // One row's float4 of the state through one token: M <- a M + k w^T (the replay and the reverse
 // pass's reconstruction use this same expression).
 __device__ __forceinline__ void state_update(float4 &m, float a, float k, const float4 &w) {
     m.x = a * m.x + k * w.x; m.y = a * m.y + k * w.y;
     m.z = a * m.z + k * w.z; m.w = a * m.w + k * w.w;
+}
+
+// The forward step of the token pair (tt, tt + 1) of a staged chunk (tt even) on M in registers:
+// p = M^T k and w = beta (v - a p) of both tokens (kept in rd at rows tt and tt + 1), and
+// M <- a M + k w^T twice.  The second token's p follows from the same pass over M:
+// p_1 = (a_0 M + k_0 w_0^T)^T k_1 = a_0 M^T k_1 + (k_0 . k_1) w_0.  Two block barriers per pair.
+template <int DK, int DV, typename TA>
+__device__ __forceinline__ void fwd_pair(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdRedPair<DK, DV> &rd,
+                                         const ChunkIn<DK, DV, TA> &in, int tt, int warp, int lane, int rg,
+                                         int c4) {
+    using C = BwdCfg<DK, DV>;
+    float kr0[C::RPT], kr1[C::RPT];
+    float4 pp0 = make_float4(0.f, 0.f, 0.f, 0.f), pp1 = pp0;
+#pragma unroll
+    for (int x = 0; x < C::RPT; ++x) {
+        kr0[x] = to_f32(in.k[tt][rg + x * C::RPP]);
+        kr1[x] = to_f32(in.k[tt + 1][rg + x * C::RPP]);
+        pp0.x += m[x].x * kr0[x]; pp0.y += m[x].y * kr0[x]; pp0.z += m[x].z * kr0[x]; pp0.w += m[x].w * kr0[x];
+        pp1.x += m[x].x * kr1[x]; pp1.y += m[x].y * kr1[x]; pp1.z += m[x].z * kr1[x]; pp1.w += m[x].w * kr1[x];
+    }
+    *reinterpret_cast<float4 *>(&rd.red2[rg][0][c4]) = pp0;
+    *reinterpret_cast<float4 *>(&rd.red2[rg][1][c4]) = pp1;
+    __syncthreads();
+    const float a0 = expf(in.g[tt]), a1 = expf(in.g[tt + 1]);
+    if (warp == 0) {
+        const float p0 = col_sum2<C::RPP, DV>(rd.red2, 0, lane);
+        const float w0 = in.b[tt] * (to_f32(in.v[tt][lane]) - a0 * p0);
+        const float p1 = a0 * col_sum2<C::RPP, DV>(rd.red2, 1, lane) + rd.kk[tt >> 1] * w0;
+        rd.p[tt][lane] = p0;
+        rd.w[tt][lane] = w0;
+        rd.p[tt + 1][lane] = p1;
+        rd.w[tt + 1][lane] = in.b[tt + 1] * (to_f32(in.v[tt + 1][lane]) - a1 * p1);
+    }
+    __syncthreads();
+    const float4 w0 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4]);
+    const float4 w1 = *reinterpret_cast<const float4 *>(&rd.w[tt + 1][c4]);
+#pragma unroll
+    for (int x = 0; x < C::RPT; ++x) {
+        state_update(m[x], a0, kr0[x], w0);
+        state_update(m[x], a1, kr1[x], w1);
+    }
 }
 
 // The forward step of token tt of a staged chunk on M in registers: p = M^T k (column sums),
@@ -244,9 +358,9 @@ template <int DK, int DV, typename TA>
 __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
     using C = BwdCfg<DK, DV>;
     extern __shared__ __align__(16) unsigned char smraw[];
-    BwdSmem<DK, DV, TA> &sm = *reinterpret_cast<BwdSmem<DK, DV, TA> *>(smraw);
+    BwdSmemPair<DK, DV, TA> &sm = *reinterpret_cast<BwdSmemPair<DK, DV, TA> *>(smraw);
     const Dims &d = a.d;
-    const int tid = threadIdx.x, h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
     const int col0 = blockIdx.z * DV;                   // this CTA's slice of the state columns
     const int rg = tid / C::LPR, c4s = (tid % C::LPR) * 4, c4 = c4s + col0;   // (c4: column in the head)
     long long s, e;
@@ -271,13 +385,13 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
     };
     long long t0, t1;
     bounds(0, t0, t1);
-    stage_chunk<DK, DV, TA>(sm.in[0], a, t0, t1, h, kh, col0, false, tid);
+    stage_chunk<DK, DV, TA, true>(sm.in[0], a, t0, t1, h, kh, col0, false, tid);
     for (long long c = 0; c < nch; ++c) {
         __syncthreads();                                 // every read of buffer (c + 1) & 1 is done
         if (c + 1 < nch) {
             long long u0, u1;
             bounds(c + 1, u0, u1);
-            stage_chunk<DK, DV, TA>(sm.in[(c + 1) & 1], a, u0, u1, h, kh, col0, false, tid);
+            stage_chunk<DK, DV, TA, true>(sm.in[(c + 1) & 1], a, u0, u1, h, kh, col0, false, tid);
             cp_async_wait<1>();                          // this thread's copies of chunk c landed
         } else {
             cp_async_wait<0>();
@@ -289,7 +403,9 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
         for (int x = 0; x < C::RPT; ++x)
             *reinterpret_cast<float4 *>(B + (long long)(rg + x * C::RPP) * DVH + c4) = m[x];
         const ChunkIn<DK, DV, TA> &in = sm.in[c & 1];
-        for (int tt = 0; tt < (int)(t1 - t0); ++tt) fwd_token<DK, DV, TA>(m, sm.rd, in, tt, tid, rg, c4s, true);
+        const int L = (int)(t1 - t0);
+        pair_dots<DK, DV, TA>(in, sm.rd, L, false, tid);   // (published by the pair step's first barrier)
+        for (int tt = 0; tt < L; tt += 2) fwd_pair<DK, DV, TA>(m, sm.rd, in, tt, warp, lane, rg, c4s);
     }
 }
 
@@ -297,14 +413,16 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
 // end at the sequence end: the gradient alone carried back from d_state_out over chunks
 // [nch / BWD_SEG, nch), and kept at every segment boundary it passes.  Per token (reverse),
 // with G = dL/dM after the token: G <- a (G + q do^T) - a beta k (k^T (G + q do^T)), which needs
-// no forward state.  One CTA per (sequence, v-head, slice), two barriers per token.
+// no forward state.  One CTA per (sequence, v-head, slice); the tokens go in pairs (t, t-1), one
+// pass over X = G + q_t do_t^T giving both X^T k_t and X^T k_(t-1), which with the pair's dot
+// products fixes the second token's column sums too: two barriers per pair.
 template <int DK, int DV, typename TA>
 __global__ void __launch_bounds__(4 * DV) bwd_gm_kernel(BwdArgs a) {
     using C = BwdCfg<DK, DV>;
     static_assert(DV == 32, "the per-column steps run on warp 0, one column per lane");
     extern __shared__ __align__(16) unsigned char smraw[];
-    BwdSmem<DK, DV, TA> &sm = *reinterpret_cast<BwdSmem<DK, DV, TA> *>(smraw);
-    BwdRed<DK, DV> &rd = sm.rd;
+    BwdSmemPair<DK, DV, TA> &sm = *reinterpret_cast<BwdSmemPair<DK, DV, TA> *>(smraw);
+    BwdRedPair<DK, DV> &rd = sm.rd;
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
@@ -333,7 +451,7 @@ __global__ void __launch_bounds__(4 * DV) bwd_gm_kernel(BwdArgs a) {
     {
         long long u0, u1;
         bounds(nch - 1, u0, u1);
-        stage_chunk<DK, DV, TA>(sm.in[(nch - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
+        stage_chunk<DK, DV, TA, true>(sm.in[(nch - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
     }
     for (long long c = nch - 1; c >= cs; --c) {
         long long t0, t1;
@@ -342,35 +460,53 @@ __global__ void __launch_bounds__(4 * DV) bwd_gm_kernel(BwdArgs a) {
         if (c > cs) {
             long long u0, u1;
             bounds(c - 1, u0, u1);
-            stage_chunk<DK, DV, TA>(sm.in[(c - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
+            stage_chunk<DK, DV, TA, true>(sm.in[(c - 1) & 1], a, u0, u1, h, kh, col0, true, tid);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
         }
         __syncthreads();
         const ChunkIn<DK, DV, TA> &in = sm.in[c & 1];
-        for (int tt = (int)(t1 - t0) - 1; tt >= 0; --tt) {
-            const float av = expf(in.g[tt]), bv = in.b[tt];
-            const float4 do4 = *reinterpret_cast<const float4 *>(&in.dout[tt][c4s]);
-            float kr[C::RPT];
-            float4 dwp = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int L = (int)(t1 - t0);
+        pair_dots<DK, DV, TA>(in, rd, L, true, tid);     // (published by the pair step's first barrier)
+        for (int tt = ((L + 1) & ~1) - 1; tt > 0; tt -= 2) {   // the pairs (tt, tt - 1), tt odd
+            const float a1 = expf(in.g[tt]), b1 = in.b[tt], a0 = expf(in.g[tt - 1]), b0 = in.b[tt - 1];
+            const float4 do1 = *reinterpret_cast<const float4 *>(&in.dout[tt][c4s]);
+            const float4 do0 = *reinterpret_cast<const float4 *>(&in.dout[tt - 1][c4s]);
+            float kr1[C::RPT], kr0[C::RPT];
+            float4 yp = make_float4(0.f, 0.f, 0.f, 0.f), zp = yp;
 #pragma unroll
-            for (int x = 0; x < C::RPT; ++x) {
+            for (int x = 0; x < C::RPT; ++x) {   // X = G + q do^T of token tt; X^T k_tt, X^T k_(tt-1)
                 const int row = rg + x * C::RPP;
-                kr[x] = to_f32(in.k[tt][row]);
+                kr1[x] = to_f32(in.k[tt][row]);
+                kr0[x] = to_f32(in.k[tt - 1][row]);
                 const float qr = to_f32(in.q[tt][row]);
-                gm[x].x += qr * do4.x; gm[x].y += qr * do4.y; gm[x].z += qr * do4.z; gm[x].w += qr * do4.w;
-                dwp.x += gm[x].x * kr[x]; dwp.y += gm[x].y * kr[x]; dwp.z += gm[x].z * kr[x]; dwp.w += gm[x].w * kr[x];
+                gm[x].x += qr * do1.x; gm[x].y += qr * do1.y; gm[x].z += qr * do1.z; gm[x].w += qr * do1.w;
+                yp.x += gm[x].x * kr1[x]; yp.y += gm[x].y * kr1[x]; yp.z += gm[x].z * kr1[x]; yp.w += gm[x].w * kr1[x];
+                zp.x += gm[x].x * kr0[x]; zp.y += gm[x].y * kr0[x]; zp.z += gm[x].z * kr0[x]; zp.w += gm[x].w * kr0[x];
             }
-            *reinterpret_cast<float4 *>(&rd.red[rg][c4s]) = dwp;
+            *reinterpret_cast<float4 *>(&rd.red2[rg][0][c4s]) = yp;
+            *reinterpret_cast<float4 *>(&rd.red2[rg][1][c4s]) = zp;
             __syncthreads();
-            if (warp == 0) rd.dp[lane] = -av * bv * col_sum<C::RPP, DV>(rd.red, lane);
+            if (warp == 0) {   // dp of both tokens: dw_(tt-1) = a X^T k_(tt-1) + (k_tt . k_(tt-1)) dp_tt + (q . k)_(tt-1) do
+                const float dp1 = -a1 * b1 * col_sum2<C::RPP, DV>(rd.red2, 0, lane);
+                const float dw0 = a1 * col_sum2<C::RPP, DV>(rd.red2, 1, lane) + rd.kk[tt >> 1] * dp1 +
+                                  rd.qk[tt >> 1] * in.dout[tt - 1][lane];
+                rd.dp2[0][lane] = dp1;
+                rd.dp2[1][lane] = -a0 * b0 * dw0;
+            }
             __syncthreads();
-            const float4 dp4 = *reinterpret_cast<const float4 *>(&rd.dp[c4s]);
+            const float4 dp1 = *reinterpret_cast<const float4 *>(&rd.dp2[0][c4s]);
+            const float4 dp0 = *reinterpret_cast<const float4 *>(&rd.dp2[1][c4s]);
 #pragma unroll
-            for (int x = 0; x < C::RPT; ++x) {
-                gm[x].x = av * gm[x].x + kr[x] * dp4.x; gm[x].y = av * gm[x].y + kr[x] * dp4.y;
-                gm[x].z = av * gm[x].z + kr[x] * dp4.z; gm[x].w = av * gm[x].w + kr[x] * dp4.w;
+            for (int x = 0; x < C::RPT; ++x) {   // G <- a X + k dp^T, twice, with token tt-1's q do^T between
+                const float qr = to_f32(in.q[tt - 1][rg + x * C::RPP]);
+                gm[x].x = a1 * gm[x].x + kr1[x] * dp1.x + qr * do0.x;
+                gm[x].y = a1 * gm[x].y + kr1[x] * dp1.y + qr * do0.y;
+                gm[x].z = a1 * gm[x].z + kr1[x] * dp1.z + qr * do0.z;
+                gm[x].w = a1 * gm[x].w + kr1[x] * dp1.w + qr * do0.w;
+                gm[x].x = a0 * gm[x].x + kr0[x] * dp0.x; gm[x].y = a0 * gm[x].y + kr0[x] * dp0.y;
+                gm[x].z = a0 * gm[x].z + kr0[x] * dp0.z; gm[x].w = a0 * gm[x].w + kr0[x] * dp0.w;
             }
         }
         // the gradient entering chunk c starts every segment that ends there
@@ -606,7 +742,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, bool states_only, cudaStream_t s) {
     bwd_map_kernel<<<1, 32, 0, s>>>(a.cu_seqlens, a.n_seqs, a.T, a.d.chunk, a.chunk_base, a.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    constexpr int smem = (int)sizeof(BwdSmem<D, BWD_DVS, TA>);
+    constexpr int smem = (int)sizeof(BwdSmemPair<D, BWD_DVS, TA>);
     constexpr int smem1 = (int)sizeof(BwdSmem<D, BWD_DVS, TA, 1>);
     if (states_only) {
         auto kern = bwd_states_kernel<D, BWD_DVS, TA>;
