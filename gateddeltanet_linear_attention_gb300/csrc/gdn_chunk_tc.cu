@@ -704,7 +704,6 @@ __global__ void __launch_bounds__(TC_NT, 2)
             put8(b2h, b2l, tc::kmaj_off(r2, c8, 64), t8);
         }
         sync_for_mma();
-        sync_for_mma();
         // ---- G: P . T (M = 64) into columns 64-127: row r lands on TMEM lane 32*(r/16) + r%16
         if (tid == 0) {
             mma3<false, false, 64>(tbase + TP_COL_PT, tc::smem_u32(ph), tc::smem_u32(pl), 0, tc::smem_u32(b2h),
