@@ -405,16 +405,17 @@ struct Q8Io {
             const int row = rg + x * RPP;
             const float amax = amaxs[x], inv = invs[x];
             const float v[4] = {m[x].x, m[x].y, m[x].z, m[x].w};
-            const uint32_t idx0 = base_idx + (uint32_t)(row * DV + c4);
+            // idx0 is a multiple of 4 (so is c4), so (idx0 + e) ^ hf == (idx0 ^ hf) ^ e
+            const uint32_t x0 = (base_idx + (uint32_t)(row * DV + c4)) ^ hf;
             signed char cc[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 // u = (r >> 8) * 2^-24: a 24-bit integer, exact in fp32, times a power of two
-                const uint32_t r = pcg_hash((idx0 + (uint32_t)e) ^ hf);
+                const uint32_t r = pcg_hash(x0 ^ (uint32_t)e);
                 const float u = __fmul_rn(__uint2float_rn(r >> 8), 0x1p-24f);
+                // a zero row has inv == 0, so its codes come out as floor(u) == 0 here too
                 int q = __float2int_rd(__fadd_rn(__fmul_rn(v[e], inv), u));
-                q = min(max(q, -127), 127);
-                cc[e] = amax > 0.f ? (signed char)q : (signed char)0;
+                cc[e] = (signed char)min(max(q, -127), 127);
             }
             char4 c;
             c.x = cc[0]; c.y = cc[1]; c.z = cc[2]; c.w = cc[3];
