@@ -407,19 +407,21 @@ struct Q8Io {
             const float v[4] = {m[x].x, m[x].y, m[x].z, m[x].w};
             // idx0 is a multiple of 4 (so is c4), so (idx0 + e) ^ hf == (idx0 ^ hf) ^ e
             const uint32_t x0 = (base_idx + (uint32_t)(row * DV + c4)) ^ hf;
-            signed char cc[4];
+            int qq[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 // u = (r >> 8) * 2^-24: a 24-bit integer, exact in fp32, times a power of two
                 const uint32_t r = pcg_hash(x0 ^ (uint32_t)e);
                 const float u = __fmul_rn(__uint2float_rn(r >> 8), 0x1p-24f);
                 // a zero row has inv == 0, so its codes come out as floor(u) == 0 here too
-                int q = __float2int_rd(__fadd_rn(__fmul_rn(v[e], inv), u));
-                cc[e] = (signed char)min(max(q, -127), 127);
+                qq[e] = max(__float2int_rd(__fadd_rn(__fmul_rn(v[e], inv), u)), -127);
             }
-            char4 c;
-            c.x = cc[0]; c.y = cc[1]; c.z = cc[2]; c.w = cc[3];
-            *reinterpret_cast<char4 *>(codes + row * DV + c4) = c;
+            // the four codes into one word, the upper clamp at 127 done by the saturating pack:
+            // bytes (q0, q1, q2, q3) from the low end
+            uint32_t w32, hi16;
+            asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi16) : "r"(qq[3]), "r"(qq[2]));
+            asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(w32) : "r"(qq[1]), "r"(qq[0]), "r"(hi16));
+            *reinterpret_cast<uint32_t *>(codes + row * DV + c4) = w32;
             if constexpr (!(LPR == 32 && RPT == 8))
                 if (lane % LPR == 0) scales[row] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
             if constexpr (EF) {
@@ -427,7 +429,7 @@ struct Q8Io {
                 const float sc = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
                 float ev[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ev[e] = __fsub_rn(v[e], __fmul_rn((float)cc[e], sc));
+                for (int e = 0; e < 4; ++e) ev[e] = __fsub_rn(v[e], __fmul_rn((float)min(qq[e], 127), sc));
                 __nv_bfloat162 lo2 = __floats2bfloat162_rn(ev[0], ev[1]), hi2 = __floats2bfloat162_rn(ev[2], ev[3]);
                 uint2 ob;
                 ob.x = *reinterpret_cast<const uint32_t *>(&lo2);
