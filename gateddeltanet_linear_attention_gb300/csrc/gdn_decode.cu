@@ -410,9 +410,11 @@ struct Q8Io {
             int qq[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                // u = (r >> 8) * 2^-24: a 24-bit integer, exact in fp32, times a power of two
+                // u = (r >> 8) * 2^-24, formed as (r with its low 8 bits cleared) * 2^-32: the same
+                // value (at most 24 significant bits, exact in fp32), and the mask fuses with the
+                // hash's last xor
                 const uint32_t r = pcg_hash(x0 ^ (uint32_t)e);
-                const float u = __fmul_rn(__uint2float_rn(r >> 8), 0x1p-24f);
+                const float u = __fmul_rn(__uint2float_rn(r & 0xFFFFFF00u), 0x1p-32f);
                 // a zero row has inv == 0, so its codes come out as floor(u) == 0 here too
                 qq[e] = max(__float2int_rd(__fadd_rn(__fmul_rn(v[e], inv), u)), -127);
             }
