@@ -301,11 +301,12 @@ __global__ void __launch_bounds__(256, 8) decode_prep_kernel(DecodeArgs a) {
 
 // ---- Q8 state codec (used by the streaming kernel in its Q8 form and by
 // q8_convert_kernel; the format is described with gdn_state_to_q8 below)
-__device__ __forceinline__ uint32_t pcg_hash(uint32_t v) {
-    const uint32_t state = v * 747796405u + 2891336453u;
+// The hash's output step from its state (state = v * 747796405 + 2891336453).
+__device__ __forceinline__ uint32_t pcg_output(uint32_t state) {
     const uint32_t word = ((state >> ((state >> 28u) + 4u)) ^ state) * 277803737u;
     return (word >> 22u) ^ word;
 }
+__device__ __forceinline__ uint32_t pcg_hash(uint32_t v) { return pcg_output(v * 747796405u + 2891336453u); }
 
 template <int L>
 __device__ __forceinline__ float row_max(float v) {
@@ -400,20 +401,26 @@ struct Q8Io {
         if constexpr (LPR == 32 && RPT == 8) {
             if (my_x >= 0) scales[rg + my_x * RPP] = my_scale;
         }
+        // The hashed values of a thread's four codes are (idx0 + e) ^ hf with idx0 a multiple of 4
+        // (so is c4): (idx0 ^ (hf & ~3)) + ((hf & 3) ^ e), the two terms sharing no bit.  The
+        // hash's state, that value times 747796405 plus 2891336453 (mod 2^32), is then a per-row
+        // product plus one of four per-call constants.
+        uint32_t kst[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kst[e] = ((hf & 3u) ^ (uint32_t)e) * 747796405u + 2891336453u;
 #pragma unroll
         for (int x = 0; x < RPT; ++x) {
             const int row = rg + x * RPP;
             const float amax = amaxs[x], inv = invs[x];
             const float v[4] = {m[x].x, m[x].y, m[x].z, m[x].w};
-            // idx0 is a multiple of 4 (so is c4), so (idx0 + e) ^ hf == (idx0 ^ hf) ^ e
-            const uint32_t x0 = (base_idx + (uint32_t)(row * DV + c4)) ^ hf;
+            const uint32_t sb = ((base_idx + (uint32_t)(row * DV + c4)) ^ (hf & ~3u)) * 747796405u;
             int qq[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 // u = (r >> 8) * 2^-24, formed as (r with its low 8 bits cleared) * 2^-32: the same
                 // value (at most 24 significant bits, exact in fp32), and the mask fuses with the
                 // hash's last xor
-                const uint32_t r = pcg_hash(x0 ^ (uint32_t)e);
+                const uint32_t r = pcg_output(sb + kst[e]);   // == pcg_hash((idx0 + e) ^ hf)
                 const float u = __fmul_rn(__uint2float_rn(r & 0xFFFFFF00u), 0x1p-32f);
                 // a zero row has inv == 0, so its codes come out as floor(u) == 0 here too
                 qq[e] = max(__float2int_rd(__fadd_rn(__fmul_rn(v[e], inv), u)), -127);
