@@ -455,10 +455,8 @@ struct Q8Io {
             const int row = rg + x * RPP;
             const char4 c = *reinterpret_cast<const char4 *>(codes + row * DV + c4);
             const float s = scales[row];
-            // code c (|c| <= 127) as a float without a conversion: 2^23 + (c + 128), minus 2^23 + 128
-            auto cf = [](signed char v) {
-                return __int_as_float(0x4B000000u | (uint32_t)((int)v + 128)) - 8388736.0f;
-            };
+            // code c as a float by the conversion unit (the integer logic pipe is the busy one)
+            auto cf = [](signed char v) { return __int2float_rn((int)v); };
             m[x] = make_float4(__fmul_rn(cf(c.x), s), __fmul_rn(cf(c.y), s), __fmul_rn(cf(c.z), s),
                                __fmul_rn(cf(c.w), s));
         }
