@@ -705,20 +705,32 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
 // each v-head from its slices' parts (dg = a (<GM, M> - beta dw . p)).
 __global__ void bwd_group_sum_kernel(BwdArgs a, int NS) {
     const Dims &d = a.d;
-    const long long total = a.T * d.hk * d.dk;
-    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const long long t = e / (d.hk * d.dk);
-        const int rem = (int)(e - t * d.hk * d.dk), kh = rem / d.dk, i = rem % d.dk;
-        float sq = 0.f, sk = 0.f;
-        for (int gi = 0; gi < d.grp; ++gi)
-            for (int sl = 0; sl < NS; ++sl) {
-                const long long src = ((t * d.hv + kh * d.grp + gi) * NS + sl) * d.dk + i;
-                sq += a.pq[src];
-                sk += a.pk[src];
+    // dq, dk: a CTA per token row at a time, a thread per four consecutive columns (float4 loads
+    // of the parts; float4 stores when the row stride allows them)
+    const int row4 = d.hk * d.dk / 4;
+    const bool vec = (a.ld_dqk & 3) == 0;
+    for (long long t = blockIdx.x; t < a.T; t += gridDim.x) {
+        for (int j4 = threadIdx.x; j4 < row4; j4 += blockDim.x) {
+            const int kh = (4 * j4) / d.dk, i = (4 * j4) % d.dk;
+            float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
+            for (int gi = 0; gi < d.grp; ++gi)
+                for (int sl = 0; sl < NS; ++sl) {
+                    const long long src = ((t * d.hv + kh * d.grp + gi) * NS + sl) * d.dk + i;
+                    const float4 q4 = *reinterpret_cast<const float4 *>(a.pq + src);
+                    const float4 k4 = *reinterpret_cast<const float4 *>(a.pk + src);
+                    sq.x += q4.x; sq.y += q4.y; sq.z += q4.z; sq.w += q4.w;
+                    sk.x += k4.x; sk.y += k4.y; sk.z += k4.z; sk.w += k4.w;
+                }
+            float *dq = a.dq + t * a.ld_dqk + (long long)kh * d.dk + i;
+            float *dk = a.dk + t * a.ld_dqk + (long long)kh * d.dk + i;
+            if (vec) {
+                *reinterpret_cast<float4 *>(dq) = sq;
+                *reinterpret_cast<float4 *>(dk) = sk;
+            } else {
+                dq[0] = sq.x; dq[1] = sq.y; dq[2] = sq.z; dq[3] = sq.w;
+                dk[0] = sk.x; dk[1] = sk.y; dk[2] = sk.z; dk[3] = sk.w;
             }
-        a.dq[t * a.ld_dqk + (long long)kh * d.dk + i] = sq;
-        a.dk[t * a.ld_dqk + (long long)kh * d.dk + i] = sk;
+        }
     }
     const long long th = a.T * d.hv;
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < th;
@@ -761,9 +773,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, bool states_only, cudaStream_t s) {
         return e;
     kern<<<dim3(a.d.hv, a.n_seqs, BWD_SEG * NS), 4 * BWD_DVS, smem1, s>>>(a);   // BWD_SEG segments per sequence
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    long long total = a.T * a.d.hk * a.d.dk;
-    int blocks = (int)((total + 255) / 256);
-    if (blocks > sm_count() * 16) blocks = sm_count() * 16;
+    int blocks = (int)(a.T < (long long)sm_count() * 8 ? a.T : (long long)sm_count() * 8);
     if (blocks > 0) bwd_group_sum_kernel<<<blocks, 256, 0, s>>>(a, NS);
     return cudaGetLastError();
 }
