@@ -369,7 +369,8 @@ __device__ __forceinline__ void fwd_pair(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdRe
 }
 
 // The forward step of token tt of a staged chunk on M in registers: p = M^T k (column sums),
-// r = v - a p, w = beta r (kept in rd at row tt), and, when `update`, M <- a M + k w^T.
+// r = v - a p, w = beta r (kept in rd at row tt), and, when `update`, M <- a M + k w^T.  The
+// chunk's g row holds a = exp(g) here (the walk converts it once per chunk).
 // Two block barriers.
 template <int DK, int DV, typename TA>
 __device__ __forceinline__ void fwd_token(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdRed<DK, DV> &rd,
@@ -385,7 +386,7 @@ __device__ __forceinline__ void fwd_token(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdR
     }
     *reinterpret_cast<float4 *>(&rd.red[rg][c4]) = pp;
     __syncthreads();
-    const float av = expf(in.g[tt]);
+    const float av = in.g[tt];                           // a = exp(g), staged by the caller
     if (tid < DV) {
         const float p = col_sum<C::RPP, DV>(rd.red, tid);
         rd.p[tt][tid] = p;
@@ -640,7 +641,10 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
         stage_chunk<DK, DV, TA>(sm.in[0], a, t0, t1, h, kh, col0, true, tid);
         cp_async_wait<0>();
         __syncthreads();
-        const ChunkIn<DK, DV, TA> &in = sm.in[0];
+        // the decays a = exp(g) of the chunk's tokens, once, in place of g
+        for (int r = tid; r < (int)(t1 - t0); r += C::NT) sm.in[0].g[r] = expf(sm.in[0].g[r]);
+        __syncthreads();
+        const ChunkIn<DK, DV, TA> &in = sm.in[0];   // (in.g holds a = exp(g) from here)
         // forward through the chunk, keeping the state before every even token (each thread
         // reads back only what it wrote) and every token's p and w
         for (long long t = t0; t < t1; ++t) {
@@ -674,7 +678,7 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
             for (int x = 0; x < C::RPT; ++x)                 // dq = M' do, M' the state after the token
                 dqp[x] = m[x].x * do4.x + m[x].y * do4.y + m[x].z * do4.z + m[x].w * do4.w;
             if (tt & 1) {
-                const float a0 = expf(in.g[tt - 1]);
+                const float a0 = in.g[tt - 1];
                 const float4 w0 = *reinterpret_cast<const float4 *>(&rd.w[tt - 1][c4s]);
                 float k0[C::RPT];
                 load_rows<C::RPT>(in.k[tt - 1] + rg * C::RPT, k0);
@@ -693,7 +697,7 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
                         mn[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg * C::RPT + x) * DV + c4s);
                 }
             }
-            const float av = expf(in.g[tt]), bv = in.b[tt];
+            const float av = in.g[tt], bv = in.b[tt];
             const float4 w4 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4s]);
             float4 dwp = make_float4(0.f, 0.f, 0.f, 0.f);
             float dap = 0.f;
