@@ -348,7 +348,7 @@ __device__ __forceinline__ void fwd_pair(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdRe
     *reinterpret_cast<float4 *>(&rd.red2[rg][0][c4]) = pp0;
     *reinterpret_cast<float4 *>(&rd.red2[rg][1][c4]) = pp1;
     __syncthreads();
-    const float a0 = expf(in.g[tt]), a1 = expf(in.g[tt + 1]);
+    const float a0 = in.g[tt], a1 = in.g[tt + 1];       // a = exp(g), converted by the caller
     if (warp == 0) {
         const float p0 = col_sum2<C::RPP, DV>(rd.red2, 0, lane);
         const float w0 = in.b[tt] * (to_f32(in.v[tt][lane]) - a0 * p0);
@@ -451,7 +451,10 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
             *reinterpret_cast<float4 *>(B + (long long)(rg + x * C::RPP) * DVH + c4) = m[x];
         const ChunkIn<DK, DV, TA> &in = sm.in[c & 1];
         const int L = (int)(t1 - t0);
-        pair_dots<DK, DV, TA>(in, sm.rd, L, false, tid);   // (published by the pair step's first barrier)
+        pair_dots<DK, DV, TA>(in, sm.rd, L, false, tid);
+        // the decays a = exp(g) once, in place of g (the neutral token's g = 0 gives a = 1)
+        for (int r = tid; r < ((L + 1) & ~1); r += C::NT) sm.in[c & 1].g[r] = expf(sm.in[c & 1].g[r]);
+        __syncthreads();
         for (int tt = 0; tt < L; tt += 2) fwd_pair<DK, DV, TA, false>(m, sm.rd, in, tt, warp, lane, rg, c4s);
     }
 }
@@ -515,9 +518,12 @@ __global__ void __launch_bounds__(4 * DV) bwd_gm_kernel(BwdArgs a) {
         __syncthreads();
         const ChunkIn<DK, DV, TA> &in = sm.in[c & 1];
         const int L = (int)(t1 - t0);
-        pair_dots<DK, DV, TA>(in, rd, L, true, tid);     // (published by the pair step's first barrier)
+        pair_dots<DK, DV, TA>(in, rd, L, true, tid);
+        // the decays a = exp(g) once, in place of g (the neutral token's g = 0 gives a = 1)
+        for (int r = tid; r < ((L + 1) & ~1); r += C::NT) sm.in[c & 1].g[r] = expf(sm.in[c & 1].g[r]);
+        __syncthreads();
         for (int tt = ((L + 1) & ~1) - 1; tt > 0; tt -= 2) {   // the pairs (tt, tt - 1), tt odd
-            const float a1 = expf(in.g[tt]), b1 = in.b[tt], a0 = expf(in.g[tt - 1]), b0 = in.b[tt - 1];
+            const float a1 = in.g[tt], b1 = in.b[tt], a0 = in.g[tt - 1], b0 = in.b[tt - 1];   // (a = exp(g))
             const float4 do1 = *reinterpret_cast<const float4 *>(&in.dout[tt][c4s]);
             const float4 do0 = *reinterpret_cast<const float4 *>(&in.dout[tt - 1][c4s]);
             float kr1[C::RPT], kr0[C::RPT], qv[C::RPT];
