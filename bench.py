@@ -663,7 +663,9 @@ def bench_verify(args, dev, gdn, pk, pk_src, k=8):
 def bench_backward(args, dev, gdn, pk, pk_src):
     """The gated delta rule core backward on one 8,192-token sequence at the prefill shape
     (HV=32, dk=dv=128, chunk 64, nonzero initial state): gdn_chunk_states once (what the
-    training forward retains), then gdn_chunk_backward timed per call with CUDA events."""
+    training forward retains: the boundary states and every token's p and w), then
+    gdn_chunk_backward timed per call with CUDA events, reading the retained p and w; the form
+    that recomputes them is timed beside it."""
     wl = WORKLOADS["prefill_8k"]
     T, HK, HV, d, C = 8192, wl.HK, wl.HV, wl.dk, wl.chunk
     cfg = gdn.make_config(HK, HV, d, d, C, "bf16", n_slots=1)
@@ -680,6 +682,7 @@ def bench_backward(args, dev, gdn, pk, pk_src):
     cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
     nb = gdn.chunk_count([T], C)
     bnd = torch.empty((nb, HV, d, d), device=dev)
+    pw = torch.empty((T, HV, 2, d), device=dev)
     ws = torch.empty(gdn.gdn_backward_workspace_size(cfg, T, 1), dtype=torch.uint8, device=dev)
     dq = torch.empty((T, HK * d), device=dev); dk = torch.empty_like(dq)
     dv = torch.empty((T, HV * d), device=dev); dg = torch.empty((T, HV), device=dev)
@@ -687,27 +690,34 @@ def bench_backward(args, dev, gdn, pk, pk_src):
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    gdn.gdn_chunk_states(cfg, k, v, gl, beta, cu, bnd, ws, state_in=S0)
+    gdn.gdn_chunk_states(cfg, k, v, gl, beta, cu, bnd, ws, state_in=S0, token_pw=pw)
     e1.record(stream)
     torch.cuda.synchronize()
     states_s = e0.elapsed_time(e1) / 1e3
     reps = 3
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(reps + 1)]
-    for i in range(reps + 1):           # 1 untimed warm-up
-        evs[i][0].record(stream)
-        gdn.gdn_chunk_backward(cfg, q, k, v, gl, beta, cu, bnd, d_o, dq, dk, dv, dg, db, ws,
-                               d_state_out=dS, d_state_in=dS0)
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    assert gdn.gdn_device_error() == 0
-    per = sum(a.elapsed_time(b) for a, b in evs[1:]) / reps / 1e3
+
+    def timed(token_pw):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps + 1)]
+        for i in range(reps + 1):           # 1 untimed warm-up
+            evs[i][0].record(stream)
+            gdn.gdn_chunk_backward(cfg, q, k, v, gl, beta, cu, bnd, d_o, dq, dk, dv, dg, db, ws,
+                                   d_state_out=dS, d_state_in=dS0, token_pw=token_pw)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert gdn.gdn_device_error() == 0
+        return sum(a.elapsed_time(b) for a, b in evs[1:]) / reps / 1e3
+
+    per_recompute = timed(None)
+    per = timed(pw)
     # bytes the token-level algorithm moves: per pair of tokens and v-head the state before the
-    # even token written to and read back from the chunk scratch, plus the boundary state per chunk
-    moved = T * HV * d * d * 4 + nb * HV * d * d * 4
+    # even token written to and read back from the chunk scratch, plus the boundary state per
+    # chunk and the retained p and w per token
+    moved = T * HV * d * d * 4 + nb * HV * d * d * 4 + T * HV * 2 * d * 4
     return {"workload": "prefill_8k shape: one 8,192-token sequence, HK=16, HV=32, dk=dv=128, "
                         "chunk 64, bf16 q/k/v, nonzero initial state, d_o and d_state_out given",
             "tokens_per_s": T / per, "ms_per_call": per * 1e3, "states_ms": states_s * 1e3,
+            "ms_per_call_recomputing_p_w": per_recompute * 1e3,
             "roofline": {"kernel": "bwd_gm_kernel + bwd_kernel + bwd_group_sum_kernel", "bound": "latency",
                          "bytes_per_call": moved, "achieved": moved / per / 1e9, "unit": "GB/s",
                          "peak": pk["hbm_gbs"], "frac": moved / per / 1e9 / pk["hbm_gbs"],
@@ -716,7 +726,7 @@ def bench_backward(args, dev, gdn, pk, pk_src):
                                  "sequence, 3 per SM) walk about 2,731 tokens each; the gradients "
                                  "entering the later segments come from a pass over them that "
                                  "needs no forward state"},
-            "gpu_launches": 4 * reps}
+            "gpu_launches": 8 * reps}
 
 
 def bench_e2e(args, dev, gdn, cfg, wl, inp, d, N, T):

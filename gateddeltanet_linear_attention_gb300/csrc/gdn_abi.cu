@@ -509,14 +509,15 @@ gdn_status gdn_chunk_states(const gdn_config *cfg, const void *k, int64_t ld_qk,
                             int64_t ld_v, gdn_dtype in_dtype, const float *g, const float *beta,
                             const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
                             const float *state_in, const int32_t *state_idx, float *boundary_states,
-                            void *workspace, size_t workspace_bytes, void *stream) {
+                            float *token_pw, void *workspace, size_t workspace_bytes, void *stream) {
     gdn::Dims d;
     gdn_status st = check_cfg(cfg, &d);
     if (st != GDN_OK) return st;
     if ((st = check_bwd_common(d, k, ld_qk, v, ld_v, in_dtype, g, beta, cu_seqlens, n_seqs, T)) != GDN_OK)
         return st;
     if (T == 0) return GDN_OK;
-    if (!boundary_states || !aligned16(boundary_states) || (state_in && !aligned16(state_in)))
+    if (!boundary_states || !aligned16(boundary_states) || (state_in && !aligned16(state_in)) ||
+        (token_pw && !aligned16(token_pw)))
         return GDN_ERR_INVALID_ARG;
     if (state_in && d.n_slots == 0) return GDN_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) || workspace_bytes < gdn::bwd_ws_bytes(d, T, n_seqs, true))
@@ -526,7 +527,7 @@ gdn_status gdn_chunk_states(const gdn_config *cfg, const void *k, int64_t ld_qk,
     gdn::BwdArgs a = {};
     a.k = k; a.v = v; a.ld_qk = ld_qk; a.ld_v = ld_v; a.g = g; a.beta = beta;
     a.cu_seqlens = cu_seqlens; a.n_seqs = n_seqs; a.T = T; a.state_in = state_in;
-    a.state_idx = state_idx; a.bnd = boundary_states; a.d = d; a.err = err;
+    a.state_idx = state_idx; a.bnd = boundary_states; a.pw = token_pw; a.d = d; a.err = err;
     gdn::bwd_carve(a, workspace, true);
     return launch_status(gdn::launch_backward(a, in_dtype == GDN_BF16, true, (cudaStream_t)stream));
 }
@@ -535,7 +536,8 @@ gdn_status gdn_chunk_backward(const gdn_config *cfg, const void *q, const void *
                               const void *v, int64_t ld_v, gdn_dtype in_dtype, const float *g,
                               const float *beta, const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
                               const int32_t *state_idx, const float *boundary_states,
-                              const float *d_o, const float *d_state_out, float *dq, float *dk,
+                              const float *token_pw, const float *d_o, const float *d_state_out,
+                              float *dq, float *dk,
                               int64_t ld_dqk, float *dv, float *dg, float *dbeta, float *d_state_in,
                               void *workspace, size_t workspace_bytes, void *stream) {
     gdn::Dims d;
@@ -543,7 +545,8 @@ gdn_status gdn_chunk_backward(const gdn_config *cfg, const void *q, const void *
     if (st != GDN_OK) return st;
     if ((st = check_bwd_common(d, k, ld_qk, v, ld_v, in_dtype, g, beta, cu_seqlens, n_seqs, T)) != GDN_OK)
         return st;
-    if ((d_state_out && !aligned16(d_state_out)) || (d_state_in && !aligned16(d_state_in)))
+    if ((d_state_out && !aligned16(d_state_out)) || (d_state_in && !aligned16(d_state_in)) ||
+        (token_pw && !aligned16(token_pw)))
         return GDN_ERR_INVALID_ARG;
     if ((d_state_out || d_state_in) && d.n_slots == 0) return GDN_ERR_INVALID_ARG;
     if (T == 0) return GDN_OK;
@@ -559,7 +562,8 @@ gdn_status gdn_chunk_backward(const gdn_config *cfg, const void *q, const void *
     gdn::BwdArgs a = {};
     a.q = q; a.k = k; a.v = v; a.ld_qk = ld_qk; a.ld_v = ld_v; a.g = g; a.beta = beta;
     a.cu_seqlens = cu_seqlens; a.n_seqs = n_seqs; a.T = T; a.state_idx = state_idx;
-    a.bnd = const_cast<float *>(boundary_states); a.d_o = d_o; a.d_state_out = d_state_out;
+    a.bnd = const_cast<float *>(boundary_states); a.pw = const_cast<float *>(token_pw);
+    a.d_o = d_o; a.d_state_out = d_state_out;
     a.dq = dq; a.dk = dk; a.ld_dqk = ld_dqk; a.dv = dv; a.dg = dg; a.dbeta = dbeta;
     a.d_state_in = d_state_in; a.d = d; a.err = err;
     gdn::bwd_carve(a, workspace, false);

@@ -323,10 +323,14 @@ __device__ __forceinline__ void state_update(float4 &m, float a, float k, const 
 // p = M^T k and w = beta (v - a p) of both tokens (kept in rd at rows tt and tt + 1), and
 // M <- a M + k w^T twice.  The second token's p follows from the same pass over M:
 // p_1 = (a_0 M + k_0 w_0^T)^T k_1 = a_0 M^T k_1 + (k_0 . k_1) w_0.  Two block barriers per pair.
+// With `pwo` (token tt's p row of this slice in the per-token p/w rows; its w row is dvh floats
+// on, the next token's rows `ts` floats on) warp 0 also writes both tokens' p and w there, the
+// second only when `has1` (not the neutral token of an odd chunk).
 template <int DK, int DV, typename TA, bool CONSEC = true>
 __device__ __forceinline__ void fwd_pair(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdRedPair<DK, DV> &rd,
                                          const ChunkIn<DK, DV, TA> &in, int tt, int warp, int lane, int rg,
-                                         int c4) {
+                                         int c4, float *pwo = nullptr, long long ts = 0, int dvh = 0,
+                                         bool has1 = false) {
     using C = BwdCfg<DK, DV>;
     float kr0[C::RPT], kr1[C::RPT];
     if constexpr (CONSEC) {   // rows rg*RPT + x
@@ -355,8 +359,17 @@ __device__ __forceinline__ void fwd_pair(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdRe
         const float p1 = a0 * col_sum2<C::RPP, DV>(rd.red2, 1, lane) + rd.kk[tt >> 1] * w0;
         rd.p[tt][lane] = p0;
         rd.w[tt][lane] = w0;
+        const float w1 = in.b[tt + 1] * (to_f32(in.v[tt + 1][lane]) - a1 * p1);
         rd.p[tt + 1][lane] = p1;
-        rd.w[tt + 1][lane] = in.b[tt + 1] * (to_f32(in.v[tt + 1][lane]) - a1 * p1);
+        rd.w[tt + 1][lane] = w1;
+        if (pwo) {
+            pwo[lane] = p0;
+            pwo[dvh + lane] = w0;
+            if (has1) {
+                pwo[ts + lane] = p1;
+                pwo[ts + dvh + lane] = w1;
+            }
+        }
     }
     __syncthreads();
     const float4 w0 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4]);
@@ -455,7 +468,11 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
         // the decays a = exp(g) once, in place of g (the neutral token's g = 0 gives a = 1)
         for (int r = tid; r < ((L + 1) & ~1); r += C::NT) sm.in[c & 1].g[r] = expf(sm.in[c & 1].g[r]);
         __syncthreads();
-        for (int tt = 0; tt < L; tt += 2) fwd_pair<DK, DV, TA, false>(m, sm.rd, in, tt, warp, lane, rg, c4s);
+        const long long ts = 2LL * d.hv * DVH;           // per-token p/w rows: one token's stride
+        float *pw0 = a.pw ? a.pw + (t0 * d.hv + h) * 2LL * DVH + col0 : nullptr;
+        for (int tt = 0; tt < L; tt += 2)
+            fwd_pair<DK, DV, TA, false>(m, sm.rd, in, tt, warp, lane, rg, c4s, pw0 ? pw0 + tt * ts : nullptr, ts,
+                                        DVH, tt + 1 < L);
     }
 }
 
@@ -645,6 +662,15 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
         // chunk's copies
         __syncthreads();
         stage_chunk<DK, DV, TA>(sm.in[0], a, t0, t1, h, kh, col0, true, tid);
+        if (a.pw) {   // the retained p and w of the chunk's tokens, this slice's columns
+            constexpr int PR = DV / 4;                   // 16-byte copies per row
+            for (int i = tid; i < (int)(t1 - t0) * 2 * PR; i += C::NT) {
+                const int r = i / (2 * PR), half = (i / PR) & 1, c = (i % PR) * 4;
+                cp_async16((half ? rd.w[r] : rd.p[r]) + c,
+                           a.pw + ((t0 + r) * d.hv + h) * 2LL * DVH + (long long)half * DVH + col0 + c);
+            }
+            cp_async_commit();
+        }
         cp_async_wait<0>();
         __syncthreads();
         // the decays a = exp(g) of the chunk's tokens, once, in place of g
@@ -652,16 +678,35 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
         __syncthreads();
         const ChunkIn<DK, DV, TA> &in = sm.in[0];   // (in.g holds a = exp(g) from here)
         // forward through the chunk, keeping the state before every even token (each thread
-        // reads back only what it wrote) and every token's p and w
-        for (long long t = t0; t < t1; ++t) {
-            const int tt = (int)(t - t0);
-            if ((tt & 1) == 0) {
-                float *Sc = scr + (tt >> 1) * DK * DV;
+        // reads back only what it wrote) and every token's p and w.  With the p and w retained
+        // by gdn_chunk_states each thread carries its rows alone: no sums, no barriers (the
+        // update there, with the same w).
+        if (a.pw) {
+            for (int tt = 0; tt < (int)(t1 - t0); ++tt) {
+                if ((tt & 1) == 0) {
+                    float *Sc = scr + (tt >> 1) * DK * DV;
 #pragma unroll
-                for (int x = 0; x < C::RPT; ++x)
-                    *reinterpret_cast<float4 *>(Sc + (long long)(rg * C::RPT + x) * DV + c4s) = m[x];
+                    for (int x = 0; x < C::RPT; ++x)
+                        *reinterpret_cast<float4 *>(Sc + (long long)(rg * C::RPT + x) * DV + c4s) = m[x];
+                }
+                float kr[C::RPT];
+                load_rows<C::RPT>(in.k[tt] + rg * C::RPT, kr);
+                const float av = in.g[tt];
+                const float4 w4 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4s]);
+#pragma unroll
+                for (int x = 0; x < C::RPT; ++x) state_update(m[x], av, kr[x], w4);
             }
-            fwd_token<DK, DV, TA>(m, rd, in, tt, tid, rg, c4s, true);
+        } else {
+            for (long long t = t0; t < t1; ++t) {
+                const int tt = (int)(t - t0);
+                if ((tt & 1) == 0) {
+                    float *Sc = scr + (tt >> 1) * DK * DV;
+#pragma unroll
+                    for (int x = 0; x < C::RPT; ++x)
+                        *reinterpret_cast<float4 *>(Sc + (long long)(rg * C::RPT + x) * DV + c4s) = m[x];
+                }
+                fwd_token<DK, DV, TA>(m, rd, in, tt, tid, rg, c4s, true);
+            }
         }
         // the tokens in reverse.  m enters each step as the state after the token (the replay
         // ends with the state after the chunk's last token), which is the M' of dq = M' do; it

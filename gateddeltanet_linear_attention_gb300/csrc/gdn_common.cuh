@@ -170,6 +170,7 @@ struct BwdArgs {
     const float *state_in;        // [slots][HV][dk][dv] or null (zero initial state)
     const int32_t *state_idx;
     float *bnd;                   // [chunks][HV][dk][dv]: the state at every chunk start
+    float *pw;                    // [T][HV][2][dv] or null: every token's p = M^T k and w = beta (v - a p)
     const float *d_o;             // [T][HV*dv]
     const float *d_state_out;     // [slots][HV][dk][dv] or null
     float *dq, *dk;               // [T][ld_dqk], q/k head kh at column kh*dk

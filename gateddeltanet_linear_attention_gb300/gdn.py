@@ -94,8 +94,8 @@ def load(path: str | None = None):
             "gdn_state_to_q8": ([CP, P, P, P, P, U32, V], I32),
             "gdn_state_from_q8": ([CP, P, P, P, V], I32),
             "gdn_mixer_decode_q8": ([CP, ctypes.POINTER(MixerIO), P, P, P, U32, P, SZ, V], I32),
-            "gdn_chunk_states": ([CP, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, SZ, V], I32),
-            "gdn_chunk_backward": ([CP, P, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, P, P,
+            "gdn_chunk_states": ([CP, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, P, SZ, V], I32),
+            "gdn_chunk_backward": ([CP, P, P, I64, P, I64, I32, P, P, P, I32, I64, P, P, P, P, P, P, P,
                                     I64, P, P, P, P, P, SZ, V], I32),
             "gdn_device_error": ([V, ctypes.POINTER(U32)], I32),
             "gdn_debug_set_wait": ([ctypes.c_uint64, U32], I32),
@@ -271,24 +271,29 @@ def chunk_count(seqlens, chunk):
 
 
 def gdn_chunk_states(cfg, k, v, g, beta, cu_seqlens, boundary_states, workspace, state_in=None,
-                     state_idx=None, stream=None):
+                     state_idx=None, token_pw=None, stream=None):
+    """token_pw: optional fp32 [T, HV, 2, dv] that receives every token's p and w, for
+    gdn_chunk_backward's token_pw."""
     T = k.shape[0]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().gdn_chunk_states(ctypes.byref(cfg), _ptr(k), _ld(k), _ptr(v), _ld(v), _dt(k),
                                    _ptr(g), _ptr(beta), _ptr(cu_seqlens), cu_seqlens.shape[0] - 1, T,
                                    _ptr(state_in), _ptr(state_idx), _ptr(boundary_states),
-                                   _ptr(workspace), ws_bytes, _stream(stream)), "gdn_chunk_states")
+                                   _ptr(token_pw), _ptr(workspace), ws_bytes, _stream(stream)),
+           "gdn_chunk_states")
 
 
 def gdn_chunk_backward(cfg, q, k, v, g, beta, cu_seqlens, boundary_states, d_o, dq, dk, dv, dg,
                        dbeta, workspace, d_state_out=None, d_state_in=None, state_idx=None,
-                       stream=None):
+                       token_pw=None, stream=None):
+    """token_pw: None, or the buffer gdn_chunk_states filled for the same batch."""
     T = q.shape[0]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().gdn_chunk_backward(ctypes.byref(cfg), _ptr(q), _ptr(k), _ld(q), _ptr(v), _ld(v),
                                      _dt(q), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
                                      cu_seqlens.shape[0] - 1, T, _ptr(state_idx),
-                                     _ptr(boundary_states), _ptr(d_o), _ptr(d_state_out), _ptr(dq),
+                                     _ptr(boundary_states), _ptr(token_pw), _ptr(d_o),
+                                     _ptr(d_state_out), _ptr(dq),
                                      _ptr(dk), _ld(dq), _ptr(dv), _ptr(dg), _ptr(dbeta),
                                      _ptr(d_state_in), _ptr(workspace), ws_bytes, _stream(stream)),
            "gdn_chunk_backward")

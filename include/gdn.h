@@ -280,7 +280,11 @@ gdn_status gdn_mixer_decode_q8(const gdn_config *cfg, const gdn_mixer_io *io, in
  * [n_chunks][HV][dk][dv] (the layout of the recurrent state), from state_in
  * (NULL: zero) of slot state_idx[n] (NULL: slot n; a negative entry is a
  * padding lane and gets no entries written).  k: [T][ld_qk], v: [T][ld_v]
- * in_dtype; g, beta: [T][HV] fp32.  workspace: at least
+ * in_dtype; g, beta: [T][HV] fp32.  token_pw (NULL: not written): fp32
+ * [T][HV][2][dv], 16-byte aligned, caller-owned; for every token of every
+ * sequence that is not a padding lane, row 0 gets p = M^T k (the state before
+ * the token read at k) and row 1 gets w = beta (v - a p), the row the token
+ * adds to the state (M <- a M + k w^T).  workspace: at least
  * gdn_backward_workspace_size(cfg, T, n_seqs) bytes (this call uses 256 plus
  * 4 * (n_seqs + 1) of them).
  *
@@ -291,7 +295,9 @@ gdn_status gdn_mixer_decode_q8(const gdn_config *cfg, const gdn_mixer_io *io, in
  * log-decay g, a = exp(g)) and, when non-NULL, d_state_in ([n_slots][HV][dk]
  * [dv] fp32, the gradient with respect to the initial state of each
  * sequence's slot).  boundary_states as written by gdn_chunk_states for the
- * same batch.  Padding lanes get zero gradients.  workspace: at least
+ * same batch; token_pw either NULL (the walk recomputes p and w from the
+ * boundary states) or as written by that same call (the walk reads them and
+ * skips the recomputation: the same result up to rounding, faster).  Padding lanes get zero gradients.  workspace: at least
  * gdn_backward_workspace_size(cfg, T, n_seqs) bytes (the replayed states of
  * one chunk and the gradients entering the segments each sequence is walked
  * in, per (sequence, v-head), and the per-slice parts of dq, dk, dg and dbeta
@@ -301,12 +307,13 @@ gdn_status gdn_chunk_states(const gdn_config *cfg, const void *k, int64_t ld_qk,
                             int64_t ld_v, gdn_dtype in_dtype, const float *g, const float *beta,
                             const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
                             const float *state_in, const int32_t *state_idx, float *boundary_states,
-                            void *workspace, size_t workspace_bytes, void *stream);
+                            float *token_pw, void *workspace, size_t workspace_bytes, void *stream);
 gdn_status gdn_chunk_backward(const gdn_config *cfg, const void *q, const void *k, int64_t ld_qk,
                               const void *v, int64_t ld_v, gdn_dtype in_dtype, const float *g,
                               const float *beta, const int32_t *cu_seqlens, int32_t n_seqs, int64_t T,
                               const int32_t *state_idx, const float *boundary_states,
-                              const float *d_o, const float *d_state_out, float *dq, float *dk,
+                              const float *token_pw, const float *d_o, const float *d_state_out,
+                              float *dq, float *dk,
                               int64_t ld_dqk, float *dv, float *dg, float *dbeta, float *d_state_in,
                               void *workspace, size_t workspace_bytes, void *stream);
 
