@@ -118,17 +118,25 @@ __device__ __forceinline__ float col_sum(const float (&red)[RPP][DV], int col) {
     return t[0];
 }
 
-// Sum of the RPP partial column sums red[0..RPP)[v][col] of a pair step, as a tree.
-template <int RPP, int DV>
-__device__ __forceinline__ float col_sum2(const float (&red)[RPP][2][DV], int v, int col) {
-    float t[RPP];
+// Two column-sum partials (y, z: columns c..c+3 of one row group, c = 4 (lane % 8)) summed over
+// the four row groups of a warp by a transposing butterfly (6 shuffles): after it, each lane
+// holds two of the warp's 64 sums, vector (lane & 16 ? z : y), columns c + (lane & 8 ? 2 : 0)
+// and the next one, and stores them to out[vector][column].
+__device__ __forceinline__ void warp_cols2(const float4 &y, const float4 &z, float (&out)[2][32], int lane) {
+    const float v[8] = {y.x, y.y, y.z, y.w, z.x, z.y, z.z, z.w};
+    float h4[4], h2[2];
+    const bool up16 = lane & 16, up8 = lane & 8;
 #pragma unroll
-    for (int r = 0; r < RPP; ++r) t[r] = red[r][v][col];
+    for (int i = 0; i < 4; ++i) {
+        const float send = up16 ? v[i] : v[i + 4];
+        h4[i] = (up16 ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
 #pragma unroll
-    for (int w = RPP / 2; w > 0; w >>= 1)
-#pragma unroll
-        for (int r = 0; r < w; ++r) t[r] += t[r + w];
-    return t[0];
+    for (int i = 0; i < 2; ++i) {
+        const float send = up8 ? h4[i] : h4[i + 2];
+        h2[i] = (up8 ? h4[i + 2] : h4[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    *reinterpret_cast<float2 *>(&out[up16 ? 1 : 0][(lane & 7) * 4 + (up8 ? 2 : 0)]) = make_float2(h2[0], h2[1]);
 }
 
 // N consecutive values of a staged row from p (aligned to N elements) as fp32, in one or two
@@ -195,15 +203,22 @@ struct BwdRed {
     float wsum[BwdCfg<DK, DV>::NT / 32];
 };
 
-// The same for the steps over pairs of tokens (forward states, gradient pass): two column-sum
-// partials per row group, the pair's two dp, and the pair dot products k_2j . k_2j+1 and
-// q_2j . k_2j.  (The backward walk keeps the smaller single-token form: its shared memory
-// decides how much of the SM's L1 is left, which measurably changes its speed.)
+// The chunk-states kernel's pair steps: the p and w of the chunk's tokens, the two column sums
+// of a pair per warp (pre-summed over the warp's row groups), and the pair dot products
+// k_2j . k_2j+1 (qk is there for pair_dots, which can form q_2j . k_2j too).
 template <int DK, int DV>
 struct BwdRedPair {
     alignas(16) float p[kBwdMaxChunk][DV];
     alignas(16) float w[kBwdMaxChunk][DV];
-    alignas(16) float red2[BwdCfg<DK, DV>::RPP][2][DV];
+    alignas(16) float cs[BwdCfg<DK, DV>::NT / 32][2][DV];
+    float kk[kBwdMaxChunk / 2], qk[kBwdMaxChunk / 2];
+};
+
+// The gradient pass's: the pair's two column sums per warp (pre-summed over the warp's row
+// groups), its two dp and dot products.
+template <int DK, int DV>
+struct BwdRedGm {
+    alignas(16) float cs[BwdCfg<DK, DV>::NT / 32][2][DV];
     alignas(16) float dp2[2][DV];
     float kk[kBwdMaxChunk / 2], qk[kBwdMaxChunk / 2];
 };
@@ -217,6 +232,8 @@ struct BwdSmem {
 };
 template <int DK, int DV, typename TA>
 using BwdSmemPair = BwdSmem<DK, DV, TA, 2, BwdRedPair<DK, DV>>;
+template <int DK, int DV, typename TA>
+using BwdSmemGm = BwdSmem<DK, DV, TA, 2, BwdRedGm<DK, DV>>;
 
 // Segments per sequence walked at once by bwd_kernel: segment k is chunks
 // [k nch / BWD_SEG, (k + 1) nch / BWD_SEG).
@@ -287,9 +304,8 @@ __device__ __forceinline__ void stage_chunk(ChunkIn<DK, DV, TA> &ci, const BwdAr
 // The dot products the pair steps need, for the pairs (2j, 2j+1) of a staged chunk of L tokens:
 // kk[j] = k_2j . k_2j+1 and, with q staged, qk[j] = q_2j . k_2j.  Four threads per product (a
 // quarter of the dk terms each, then two shuffles); the caller's next barrier publishes them.
-template <int DK, int DV, typename TA>
-__device__ __forceinline__ void pair_dots(const ChunkIn<DK, DV, TA> &ci, BwdRedPair<DK, DV> &rd, int L, bool with_q,
-                                          int tid) {
+template <int DK, int DV, typename TA, typename RED>
+__device__ __forceinline__ void pair_dots(const ChunkIn<DK, DV, TA> &ci, RED &rd, int L, bool with_q, int tid) {
     constexpr int NT = BwdCfg<DK, DV>::NT, Q = DK / 4;
     static_assert(NT % 4 == 0 && (2 * kBwdMaxChunk / 2) * 4 % NT == 0, "whole groups of four lanes");
     const int np = (L + 1) >> 1;
@@ -349,14 +365,16 @@ __device__ __forceinline__ void fwd_pair(float4 (&m)[BwdCfg<DK, DV>::RPT], BwdRe
         pp0.x += m[x].x * kr0[x]; pp0.y += m[x].y * kr0[x]; pp0.z += m[x].z * kr0[x]; pp0.w += m[x].w * kr0[x];
         pp1.x += m[x].x * kr1[x]; pp1.y += m[x].y * kr1[x]; pp1.z += m[x].z * kr1[x]; pp1.w += m[x].w * kr1[x];
     }
-    *reinterpret_cast<float4 *>(&rd.red2[rg][0][c4]) = pp0;
-    *reinterpret_cast<float4 *>(&rd.red2[rg][1][c4]) = pp1;
+    warp_cols2(pp0, pp1, rd.cs[warp], lane);
     __syncthreads();
     const float a0 = in.g[tt], a1 = in.g[tt + 1];       // a = exp(g), converted by the caller
     if (warp == 0) {
-        const float p0 = col_sum2<C::RPP, DV>(rd.red2, 0, lane);
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < C::NT / 32; ++wi) { x0 += rd.cs[wi][0][lane]; x1 += rd.cs[wi][1][lane]; }
+        const float p0 = x0;
         const float w0 = in.b[tt] * (to_f32(in.v[tt][lane]) - a0 * p0);
-        const float p1 = a0 * col_sum2<C::RPP, DV>(rd.red2, 1, lane) + rd.kk[tt >> 1] * w0;
+        const float p1 = a0 * x1 + rd.kk[tt >> 1] * w0;
         rd.p[tt][lane] = p0;
         rd.w[tt][lane] = w0;
         const float w1 = in.b[tt + 1] * (to_f32(in.v[tt + 1][lane]) - a1 * p1);
@@ -486,10 +504,11 @@ __global__ void __launch_bounds__(4 * DV) bwd_states_kernel(BwdArgs a) {
 template <int DK, int DV, typename TA>
 __global__ void __launch_bounds__(4 * DV) bwd_gm_kernel(BwdArgs a) {
     using C = BwdCfg<DK, DV>;
+    constexpr int NW = C::NT / 32;
     static_assert(DV == 32, "the per-column steps run on warp 0, one column per lane");
     extern __shared__ __align__(16) unsigned char smraw[];
-    BwdSmemPair<DK, DV, TA> &sm = *reinterpret_cast<BwdSmemPair<DK, DV, TA> *>(smraw);
-    BwdRedPair<DK, DV> &rd = sm.rd;
+    BwdSmemGm<DK, DV, TA> &sm = *reinterpret_cast<BwdSmemGm<DK, DV, TA> *>(smraw);
+    BwdRedGm<DK, DV> &rd = sm.rd;
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, n = blockIdx.y, kh = h / d.grp;
@@ -555,13 +574,14 @@ __global__ void __launch_bounds__(4 * DV) bwd_gm_kernel(BwdArgs a) {
                 yp.x += gm[x].x * kr1[x]; yp.y += gm[x].y * kr1[x]; yp.z += gm[x].z * kr1[x]; yp.w += gm[x].w * kr1[x];
                 zp.x += gm[x].x * kr0[x]; zp.y += gm[x].y * kr0[x]; zp.z += gm[x].z * kr0[x]; zp.w += gm[x].w * kr0[x];
             }
-            *reinterpret_cast<float4 *>(&rd.red2[rg][0][c4s]) = yp;
-            *reinterpret_cast<float4 *>(&rd.red2[rg][1][c4s]) = zp;
+            warp_cols2(yp, zp, rd.cs[warp], lane);
             __syncthreads();
             if (warp == 0) {   // dp of both tokens: dw_(tt-1) = a X^T k_(tt-1) + (k_tt . k_(tt-1)) dp_tt + (q . k)_(tt-1) do
-                const float dp1 = -a1 * b1 * col_sum2<C::RPP, DV>(rd.red2, 0, lane);
-                const float dw0 = a1 * col_sum2<C::RPP, DV>(rd.red2, 1, lane) + rd.kk[tt >> 1] * dp1 +
-                                  rd.qk[tt >> 1] * in.dout[tt - 1][lane];
+                float x1 = 0.f, x0 = 0.f;
+#pragma unroll
+                for (int wi = 0; wi < NW; ++wi) { x1 += rd.cs[wi][0][lane]; x0 += rd.cs[wi][1][lane]; }
+                const float dp1 = -a1 * b1 * x1;
+                const float dw0 = a1 * x0 + rd.kk[tt >> 1] * dp1 + rd.qk[tt >> 1] * in.dout[tt - 1][lane];
                 rd.dp2[0][lane] = dp1;
                 rd.dp2[1][lane] = -a0 * b0 * dw0;
             }
@@ -868,9 +888,10 @@ cudaError_t launch_bwd_t(const BwdArgs &a, bool states_only, cudaStream_t s) {
         return cudaGetLastError();
     }
     auto gk = bwd_gm_kernel<D, BWD_DVS, TA>;
-    if ((e = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    constexpr int smem_gm = (int)sizeof(BwdSmemGm<D, BWD_DVS, TA>);
+    if ((e = cudaFuncSetAttribute(gk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_gm)) != cudaSuccess)
         return e;
-    gk<<<grid, 4 * BWD_DVS, smem, s>>>(a);
+    gk<<<grid, 4 * BWD_DVS, smem_gm, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     auto kern = bwd_kernel<D, BWD_DVS, TA>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem1)) != cudaSuccess)
