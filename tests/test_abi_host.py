@@ -234,3 +234,41 @@ def test_q8_validation(lib):
     assert lib.gdn_state_to_q8(ch, A16, A16, A16b, MIS, 0, None) == INVALID   # misaligned residual
     assert lib.gdn_mixer_decode_q8(ch, ctypes.byref(q8io), A16, A16b, None, 0, A16, 64, None) == WORKSPACE
     assert lib.gdn_mixer_decode_q8(ctypes.byref(c0), ctypes.byref(q8io), A16, A16b, None, 0, A16, need, None) == INVALID
+
+
+def test_backward_validation(lib):
+    """gdn_chunk_states / gdn_chunk_backward: every pointer check, the retained p and w
+    (token_pw) included, and the workspace size, before any CUDA call."""
+    c = cfg()
+    ch = ctypes.byref(c)
+    T, n = 64, 1
+    need = lib.gdn_backward_workspace_size(ch, T, n)
+    assert need > 0
+    assert lib.gdn_backward_workspace_size(ch, -1, n) == 0
+
+    def states(bnd=A16, pw=None, ws_bytes=need, T=T, k=A16, state_in=None):
+        return lib.gdn_chunk_states(ch, k, 2048, A16b, 4096, 0, A16, A16b, A16, n, T, state_in, None,
+                                    bnd, pw, A16, ws_bytes, None)
+
+    assert states(pw=MIS) == INVALID                   # misaligned p/w rows
+    assert states(bnd=None) == INVALID
+    assert states(bnd=MIS) == INVALID
+    assert states(k=MIS) == INVALID
+    assert states(state_in=MIS) == INVALID
+    assert states(ws_bytes=64) == WORKSPACE
+    assert states(pw=A16b, ws_bytes=64) == WORKSPACE   # an aligned buffer passes to the next check
+    assert states(T=0, bnd=None) == OK                 # nothing to do
+
+    def backward(pw=None, d_o=A16, dq=A16, ld_dqk=2048, ws_bytes=need, T=T, d_state_in=None):
+        return lib.gdn_chunk_backward(ch, A16, A16, 2048, A16b, 4096, 0, A16, A16b, A16, n, T, None,
+                                      A16b, pw, d_o, None, dq, A16, ld_dqk, A16b, A16, A16b, d_state_in,
+                                      A16, ws_bytes, None)
+
+    assert backward(pw=MIS) == INVALID
+    assert backward(d_o=MIS) == INVALID
+    assert backward(dq=None) == INVALID
+    assert backward(ld_dqk=1024) == INVALID            # narrower than HK * dk
+    assert backward(d_state_in=MIS) == INVALID
+    assert backward(ws_bytes=need - 257) == WORKSPACE   # (the size includes 256 bytes of slack)
+    assert backward(pw=A16b, ws_bytes=64) == WORKSPACE
+    assert backward(T=0) == OK
