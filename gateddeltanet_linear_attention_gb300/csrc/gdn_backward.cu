@@ -16,20 +16,23 @@
 // column, so each CTA owns one 32-column slice of a head's state; only the
 // outputs that sum over columns (dq and dk: row sums; da: <GM, M> and dw . p;
 // dbeta: dw . r) come out as per-slice parts that a last kernel adds up.
-// Two launches and a reduction:
+// The kernels:
 //  - bwd_states_kernel (gdn_chunk_states): one CTA per (sequence, v-head,
 //    slice), the forward over the sequence with the slice of M in registers
 //    (thread: one float4 column group over RPT rows, 8 lanes per 128-byte row
-//    segment), writing it at every chunk start: the states a training forward
-//    retains.  It takes the tokens in pairs: one pass over M gives M^T k of
-//    both, and the pair's k . k fixes the second token's p;
-//  - bwd_gm_kernel: dL/dS at the segment boundaries of the walk below,
-//    carried back without the forward states, also in token pairs;
-//  - bwd_kernel (gdn_chunk_backward): one CTA per (sequence, v-head, slice),
-//    the chunks in reverse: the forward of the chunk from its boundary state,
-//    keeping the state before every token in the workspace, then the tokens in
-//    reverse with GM in registers.  Column sums go through one shared-memory
-//    pass, row sums through shuffles among the lanes that hold the row;
+//    segment), writing it at every chunk start, and optionally every token's p
+//    and w: what a training forward retains.  It takes the tokens in pairs: one
+//    pass over M gives M^T k of both, and the pair's k . k fixes the second
+//    token's p;
+//  - bwd_gm_kernel (gdn_chunk_backward, first): dL/dS at the segment
+//    boundaries of the walk below, carried back without the forward states,
+//    also in token pairs;
+//  - bwd_kernel: one CTA per (sequence, v-head, slice, segment), the chunks in
+//    reverse: the forward of the chunk from its boundary state (from the
+//    retained p and w when given: no sums), keeping the state before every even
+//    token in the workspace, then the tokens in reverse with GM in registers.
+//    Column sums go through one shared-memory pass, row sums through shuffles
+//    among the lanes that hold the row;
 //  - bwd_group_sum_kernel adds the slices and the v-heads of each q/k head
 //    (dq, dk) and the slices of each v-head (dg = a (<GM, M> - beta dw . p),
 //    dbeta).
