@@ -135,10 +135,10 @@ def test_q8_decode_matches_oracle(ef):
     assert np.array_equal(conv.float().cpu().numpy(), ocv)             # the history: raw inputs
 
 
-def test_q8_decode_padding_lane_untouched():
-    n, HK, HV, d = 3, 2, 4, 64
+@pytest.mark.parametrize("d", [64, 128])   # (at 128 the encode runs on its own warps)
+def test_q8_decode_padding_lane_untouched(d):
+    n, HK, HV = 3, 2, 4
     inp = _inputs(n, HK, HV, d, 1, seed=42)
-    cfg = gdn.make_config(HK, HV, d, d, 16, "bf16", 4)
     y, codes, scales, conv = _gpu_q8_run(inp, n, HK, HV, d, 1, frame0=3, state_idx=[2, -1, 0], n_slots=4)
     assert gdn.gdn_device_error() == 0
     assert torch.all(y[0, 1] == 0)
