@@ -36,6 +36,8 @@
 //  - bwd_group_sum_kernel adds the slices and the v-heads of each q/k head
 //    (dq, dk) and the slices of each v-head (dg = a (<GM, M> - beta dw . p),
 //    dbeta).
+#include <type_traits>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -731,46 +733,49 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
                 fwd_token<DK, DV, TA>(m, rd, in, tt, tid, rg, c4s, true);
             }
         }
-        // the tokens in reverse.  m enters each step as the state after the token (the replay
-        // ends with the state after the chunk's last token), which is the M' of dq = M' do; it
-        // then becomes the state before the token.  mn holds the stored state before the even
-        // token of the current pair; the state before an odd token is that one carried over the
-        // even token (its kept w, as in the replay), and the next pair's state is loaded at the
-        // even token.
+        // The tokens in reverse.  A step takes the state after its token in `mc` (the replay
+        // ends with the state after the chunk's last token), which is the M' of dq = M' do, and
+        // the stored state before the even token of its pair in `ms`.  An odd token turns mc into
+        // the state before it (the stored one carried over the even token, with its kept w); an
+        // even token's state before it is ms itself, and mc, no longer needed after dq, takes the
+        // next pair's stored state.  So after each pair the two arrays have swapped roles: the
+        // loop takes two pairs per turn with the arrays named in turn, and no state is copied.
         float4 mn[C::RPT];
+        const int L = (int)(t1 - t0);
         {
-            const float *Sc = scr + ((int)(t1 - 1 - t0) >> 1) * DK * DV;
+            const float *Sc = scr + ((L - 1) >> 1) * DK * DV;
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x)
                 mn[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg * C::RPT + x) * DV + c4s);
         }
-        for (long long t = t1 - 1; t >= t0; --t) {
-            const int tt = (int)(t - t0);
+        auto rstep = [&](auto odd, float4 (&mc)[C::RPT], float4 (&ms)[C::RPT], int tt) {
+            constexpr bool ODD = decltype(odd)::value;
+            const long long t = t0 + tt;
             const float4 do4 = *reinterpret_cast<const float4 *>(&in.dout[tt][c4s]);
             float dqp[C::RPT];
 #pragma unroll
             for (int x = 0; x < C::RPT; ++x)                 // dq = M' do, M' the state after the token
-                dqp[x] = m[x].x * do4.x + m[x].y * do4.y + m[x].z * do4.z + m[x].w * do4.w;
-            if (tt & 1) {
+                dqp[x] = mc[x].x * do4.x + mc[x].y * do4.y + mc[x].z * do4.z + mc[x].w * do4.w;
+            if constexpr (ODD) {                             // mc <- the state before the token
                 const float a0 = in.g[tt - 1];
                 const float4 w0 = *reinterpret_cast<const float4 *>(&rd.w[tt - 1][c4s]);
                 float k0[C::RPT];
                 load_rows<C::RPT>(in.k[tt - 1] + rg * C::RPT, k0);
 #pragma unroll
                 for (int x = 0; x < C::RPT; ++x) {
-                    m[x] = mn[x];
-                    state_update(m[x], a0, k0[x], w0);
+                    mc[x] = ms[x];
+                    state_update(mc[x], a0, k0[x], w0);
                 }
-            } else {
+            } else if (tt >= 2) {                            // mc <- the next pair's stored state
+                const float *Sc = scr + ((tt >> 1) - 1) * DK * DV;
 #pragma unroll
-                for (int x = 0; x < C::RPT; ++x) m[x] = mn[x];
-                if (tt >= 2) {
-                    const float *Sc = scr + ((tt >> 1) - 1) * DK * DV;
-#pragma unroll
-                    for (int x = 0; x < C::RPT; ++x)
-                        mn[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg * C::RPT + x) * DV + c4s);
-                }
+                for (int x = 0; x < C::RPT; ++x)
+                    mc[x] = *reinterpret_cast<const float4 *>(Sc + (long long)(rg * C::RPT + x) * DV + c4s);
             }
+            float4 (&m)[C::RPT] = *[&]() -> float4 (*)[C::RPT] {   // the state before the token
+                if constexpr (ODD) return &mc;
+                else return &ms;
+            }();
             const float av = in.g[tt], bv = in.b[tt];
             const float4 w4 = *reinterpret_cast<const float4 *>(&rd.w[tt][c4s]);
             float4 dwp = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -817,6 +822,28 @@ __global__ void __launch_bounds__(4 * DV, 3) bwd_kernel(BwdArgs a) {
                 gm[x].z = av * gm[x].z + kr[x] * dp4.z; gm[x].w = av * gm[x].w + kr[x] * dp4.w;
             }
             store_row_sums<C::RPT, C::LPR, C::RPP>(dkp, a.pk + part(t) * DK, rg, lane);
+        };
+        using Odd = std::true_type;
+        using Even = std::false_type;
+        int tt = L - 1;
+        if ((tt & 1) == 0) {   // an odd-length chunk: its last token is even and has no partner
+            rstep(Even{}, m, mn, tt--);
+#pragma unroll
+            for (int x = 0; x < C::RPT; ++x) {   // (once per such chunk: the roles back in place)
+                const float4 tmp = m[x];
+                m[x] = mn[x];
+                mn[x] = tmp;
+            }
+        }
+        for (; tt >= 3; tt -= 4) {
+            rstep(Odd{}, m, mn, tt);
+            rstep(Even{}, m, mn, tt - 1);
+            rstep(Odd{}, mn, m, tt - 2);
+            rstep(Even{}, mn, m, tt - 3);
+        }
+        if (tt == 1) {
+            rstep(Odd{}, m, mn, 1);
+            rstep(Even{}, m, mn, 0);
         }
     }
     if (a.d_state_in && c_lo == 0) {                    // the segment that ends at the first chunk
