@@ -723,9 +723,10 @@ def bench_backward(args, dev, gdn, pk, pk_src):
                          "peak": pk["hbm_gbs"], "frac": moved / per / 1e9 / pk["hbm_gbs"],
                          "peak_source": pk_src + " copy", "traffic": traffic_for("backward_8k"),
                          "note": "384 CTAs (v-head x 32-column state slice x three segments of the "
-                                 "sequence, 3 per SM) walk about 2,731 tokens each; the gradients "
-                                 "entering the later segments come from a pass over them that "
-                                 "needs no forward state"},
+                                 "sequence, 3 per SM) walk about 2,731 tokens each, replaying each "
+                                 "chunk from the p and w that gdn_chunk_states retained; the "
+                                 "gradients entering the later segments come from a pass over them "
+                                 "that needs no forward state"},
             "gpu_launches": 8 * reps}
 
 
